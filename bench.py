@@ -1,0 +1,381 @@
+"""Benchmark: effective HBM GB/s and busBW of the chunk-schedule executor.
+
+One *step* executes every collective of the suite once, each on its own
+synthetic inputs resident in HBM:
+
+  hier_ar   hierarchical AllReduce, R=16 (2 groups x 8), fp32, 64 MiB/rank, 16 micro-batches
+  a2a       two-phase AllToAll, R=32 (4 x 8), fp16, 1 MiB block per (src, dst)
+  ring_bf16 ring AllReduce, R=8, bf16, 256 MiB/rank, 24 channels
+  ring_f32  ring AllReduce, R=8, fp32, 256 MiB/rank, 24 channels
+  a2n       AllToNext, R=24 (3 x 8), fp32, 128 MiB/rank, relayed cross-group pairs
+  ag_3m     ring AllGather, R=8, bf16, 3 MiB/rank output, 4 channels
+  rs_3m     ring ReduceScatter, R=8, bf16, 3 MiB/rank input, 4 channels
+  ar_1m     ring AllReduce, R=8, fp32, 1 MiB/rank, 1 channel
+
+value = schedule bytes of the step (bytes every fused instruction reads and
+writes, FIFO staging included) / device time of the step.  The step's working
+set (~19 GiB) is far larger than L2, so consecutive collectives evict each
+other; no separate flush.
+
+``--impl reference`` times the CPU oracle (single thread) on a bounded
+sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+MiB = 1 << 20
+
+# name, kind, R, G, dtype, bytes per chunk, dist, seed, plan options
+SUITE = [
+    ("hier_ar", 3, 16, 8, 0, 4 * MiB, "normal", 2, dict(channels=8, microbatches=16)),
+    ("a2a", 4, 32, 8, 2, 1 * MiB, "uniform", 3, dict(channels=2)),
+    ("ring_bf16", 0, 8, 0, 1, 32 * MiB, "normal", 4, dict(channels=24)),
+    ("ring_f32", 0, 8, 0, 0, 32 * MiB, "normal", 4, dict(channels=24)),
+    ("a2n", 5, 24, 8, 0, 16 * MiB, "normal", 4, dict(channels=2)),
+    ("ag_3m", 1, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4)),
+    ("rs_3m", 2, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4)),
+    ("ar_1m", 0, 8, 0, 0, 1 * MiB // 8, "uniform", 0, dict(channels=1)),
+]
+ESIZE = {0: 4, 1: 2, 2: 2, 3: 4}
+NAMES = {0: "f32", 1: "bf16", 2: "f16", 3: "i32"}
+METRIC = "effective HBM GB/s & busBW per collective vs GB300 HBM roofline, 1 GPU"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def build_suite(ccl, torch, datagen, with_host=False):
+    import numpy as np
+    items = []
+    for name, kind, R, G, dt, chunk_bytes, dist, seed, opts in SUITE:
+        ce = chunk_bytes // ESIZE[dt]
+        sched = ccl.Schedule.builtin(kind, R, G)
+        plan = ccl.Plan(sched, ce, dt, **opts)
+        st = plan.stats()
+        nin, nout = plan.in_elems, plan.out_elems
+        tdt = {0: torch.float32, 1: torch.int16, 2: torch.int16, 3: torch.int32}[dt]
+        # draw on the host per rank (datagen recipe), copy once to HBM
+        rng = np.random.default_rng(seed)
+        d_in, d_out, h_in, h_out = [], [], [], []
+        for r in range(R):
+            a = datagen.draw(rng, dist, nin, dt)
+            t = torch.from_numpy(a.view(np.int16) if dt in (1, 2) else a)
+            d_in.append(t.cuda())
+            d_out.append(torch.empty(nout, dtype=tdt, device="cuda"))
+            if with_host:
+                h_in.append(t.pin_memory())
+                h_out.append(torch.empty(nout, dtype=tdt).pin_memory())
+        items.append(dict(name=name, kind=kind, R=R, G=G, dt=dt, ce=ce, plan=plan, stats=st, d_in=d_in,
+                          d_out=d_out, h_in=h_in, h_out=h_out, dist=dist, seed=seed))
+    return items
+
+
+def run_gpu(args):
+    import torch
+    import collective_communication_schedule_gb300 as ccl
+    import datagen
+
+    peak, peak_kind = peaks()
+    items = build_suite(ccl, torch, datagen, with_host=True)
+    stream = torch.cuda.current_stream()
+    # warm-up
+    for _ in range(args.warmup):
+        for it in items:
+            it["plan"].execute(it["d_in"], it["d_out"], stream)
+    torch.cuda.synchronize()
+    for it in items:
+        it["plan"].status()
+
+    # timed device region: events around every launch on the launching stream
+    K = args.steps
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in items]
+          for _ in range(K)]
+    t_all0, t_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    t_all0.record(stream)
+    for k in range(K):
+        for j, it in enumerate(items):
+            ev[k][j][0].record(stream)
+            it["plan"].execute(it["d_in"], it["d_out"], stream)
+            ev[k][j][1].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    for it in items:
+        it["plan"].status()
+    total_ms = t_all0.elapsed_time(t_all1)
+    per = []
+    sched_bytes = sum(it["stats"].schedule_bytes for it in items)
+    kern_ms_total = 0.0
+    for j, it in enumerate(items):
+        ts = [ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(K)]
+        mean_ms = sum(ts) / len(ts)
+        kern_ms_total += sum(ts)
+        st = it["stats"]
+        gbs = st.schedule_bytes / (mean_ms * 1e6)
+        algbw = st.data_bytes_per_rank / (mean_ms * 1e6)
+        per.append({
+            "name": it["name"], "ranks": it["R"], "dtype": NAMES[it["dt"]],
+            "bytes_per_rank": st.data_bytes_per_rank, "mean_us": round(mean_ms * 1e3, 2),
+            "median_us": round(statistics.median(ts) * 1e3, 2),
+            "schedule_gbs": round(gbs, 1), "min_bytes_gbs": round(st.min_bytes / (mean_ms * 1e6), 1),
+            "frac_of_peak": round(gbs / peak, 3), "min_bytes_frac": round(st.min_bytes / (mean_ms * 1e6) / peak, 3),
+            "algbw_gbs": round(algbw, 1), "busbw_gbs": round(algbw * st.busbw_factor, 1),
+            "threadblocks": st.nthreadblocks, "channels": st.channels, "microbatches": st.microbatches,
+            "slot_bytes": st.slot_bytes, "nthreads": st.nthreads,
+        })
+    step_ms = total_ms / K
+    value = sched_bytes / (step_ms * 1e6)
+    avg_launch_ms = kern_ms_total / (K * len(items))
+    achieved = (sched_bytes / len(items)) / (avg_launch_ms * 1e6)
+
+    # end to end through the C ABI with host buffers (H2D + execute + D2H)
+    Ke = max(1, min(K, args.e2e_steps))
+    h2d = sum(it["plan"].in_elems * ESIZE[it["dt"]] * it["R"] for it in items)
+    d2h = sum(it["plan"].out_elems * ESIZE[it["dt"]] * it["R"] for it in items)
+    for it in items:   # one warm pass
+        it["plan"].execute_host(it["h_in"], it["h_out"], it["d_in"], it["d_out"], stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        for it in items:
+            it["plan"].execute_host(it["h_in"], it["h_out"], it["d_in"], it["d_out"], stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    for it in items:
+        it["plan"].status()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": 1,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True,
+        "scaling": "replicas only",
+        "vs_baseline": None,
+        "dtype": "f32/bf16/f16 (per collective)",
+        "data": "synthetic (numpy PCG64 seeds 0-4)",
+        "config": {"workload": "collective suite: hier AR 16x64MiB f32 + two-phase A2A 32x32MiB f16 + ring AR "
+                               "8x256MiB bf16 & f32 (24 ch) + AllToNext 24x128MiB f32 + AG/RS 8x3MiB bf16 + "
+                               "ring AR 8x1MiB f32",
+                   "parallelism": "R virtual ranks on one GPU", "l2": "step working set ~19 GiB > L2 (no flush)",
+                   "schedule_bytes_per_step": sched_bytes},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 3), "traffic": None,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s"},
+        "e2e": {"value": round(sched_bytes / (e2e_ms * 1e6), 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3), "steps": Ke},
+        "gpu_launches": K * len(items),
+        "clocks": clk,
+        "per_collective": per,
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(items, args.cpu_seconds)
+    return out
+
+
+def _oracle_inputs(it):
+    """Host copies of the inputs: the GPU arm's pinned buffers, or a fresh
+    draw with the same recipe (reference arm)."""
+    import numpy as np
+    import datagen
+    if it.get("h_in"):
+        return [t.numpy().view(np.uint16) if it["dt"] in (1, 2) else t.numpy() for t in it["h_in"]]
+    rng = np.random.default_rng(it["seed"])
+    nin = it["nin"]
+    return [datagen.draw(rng, it["dist"], nin, it["dt"]) for _ in range(it["R"])]
+
+
+def cpu_baseline(items, budget_s, divisor=None):
+    """The oracle (C, one thread) on a bounded sample: every collective of the
+    suite on the same inputs restricted to 1/divisor of the in-chunk offsets
+    (the oracle maps chunk to chunk offset by offset, so a column sample is
+    an exact part of the full result).  divisor=None calibrates it so that the
+    three timed repetitions take about ``budget_s`` seconds."""
+    import numpy as np
+    import oracle
+    from oracle import schedules as OS
+    names = {0: ("ring_allreduce", lambda R, G: (R,)), 1: ("ring_allgather", lambda R, G: (R,)),
+             2: ("ring_reducescatter", lambda R, G: (R,)), 3: ("hier_allreduce", lambda R, G: (G, R // G)),
+             4: ("alltoall_two_phase", lambda R, G: (G, R // G)), 5: ("alltonext", lambda R, G: (G, R // G))}
+    oracle.build()
+    prepared = []
+    for it in items:
+        nm, a = names[it["kind"]]
+        ops, nch = OS.BUILTINS[nm](*a(it["R"], it["G"]))
+        prepared.append((it, ops, nch, _oracle_inputs(it)))
+
+    def one_pass(div, reps):
+        t_total, bytes_total, sampled = 0.0, 0.0, []
+        for it, ops, nch, ins in prepared:
+            ce = it["ce"]
+            cols = max(1, ce // div)
+            offs = (np.arange(cols, dtype=np.int64) * (ce // cols)).astype(np.int64)
+            cols_in = [np.ascontiguousarray(x.reshape(nch[0], ce)[:, offs]).reshape(-1) for x in ins]
+            ts = []
+            for _ in range(reps):
+                t0 = time.perf_counter()
+                oracle.run(ops, it["R"], nch, cols, it["dt"], cols_in)
+                ts.append(time.perf_counter() - t0)
+            t_total += statistics.median(ts)
+            bytes_total += it["stats"].schedule_bytes * cols / ce
+            sampled.append(f"{it['name']}:{cols}/{ce}")
+        return t_total, bytes_total, sampled
+
+    if divisor is None:
+        t, _, _ = one_pass(4096, 1)
+        want = 4096.0 * 3.0 * t / budget_s      # divisor whose 3 repetitions take ~budget_s
+        divisor = 1
+        while divisor < want and divisor < 4096:
+            divisor *= 2
+    t_total, bytes_total, sampled = one_pass(divisor, 3)
+    return {"value": round(bytes_total / t_total / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "host_cpus": os.cpu_count(),
+            "sample": f"every collective of the step on 1/{divisor} of the in-chunk offsets, median of 3 ("
+                      + ", ".join(sampled) + ")",
+            "seconds": round(t_total, 3)}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: same metric on bounded samples."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import collective_communication_schedule_gb300 as ccl  # only for byte counts via host planning
+    items = []
+    for name, kind, R, G, dt, chunk_bytes, dist, seed, opts in SUITE:
+        ce = chunk_bytes // ESIZE[dt]
+        sch = ccl.Schedule.builtin(kind, R, G)
+        st = sch.check(ce, dt, **opts)
+        nin = sch.info().nchunks[0] * ce
+        items.append(dict(name=name, kind=kind, R=R, G=G, dt=dt, ce=ce, stats=st, dist=dist, seed=seed, nin=nin))
+    cb = None
+    for _ in range(args.warmup + args.steps):
+        cb = cpu_baseline(items, args.cpu_seconds, divisor=1024)
+    return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "replicas only",
+            "vs_baseline": None, "dtype": "f32/bf16/f16 (per collective)", "data": "synthetic (numpy PCG64 seeds 0-4)",
+            "config": {"workload": "collective suite (same as the GPU arm), each step a 1/1024 sample of in-chunk offsets"},
+            "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args)
+        if out is not None:
+            print(json.dumps(out))
+        return
+    if world > 1:
+        # replicas only: every rank runs the same single-GPU suite on its own GPU
+        import torch
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        res = run_gpu(args)
+        t = torch.tensor([res["ms_per_step"]], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        if rank == 0:
+            res["ms_per_step"] = float(t.item())
+            res["value"] = round(res["config"]["schedule_bytes_per_step"] * world / (t.item() * 1e6), 1)
+            res["n_gpus"] = world
+            print(json.dumps(res))
+        dist.destroy_process_group()
+        return
+    import torch
+    torch.cuda.set_device(0)
+    print(json.dumps(run_gpu(args)))
+
+
+if __name__ == "__main__":
+    main()

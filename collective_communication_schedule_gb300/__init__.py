@@ -1,0 +1,299 @@
+"""GB300 executor for chunk-oriented collective schedules (Python binding).
+
+Thin ctypes binding over ``libccl.so`` (C ABI in ``include/ccl.h``): argument
+marshalling only.  Every step of the collective runs in the library's CUDA
+kernel; PyTorch supplies device memory and streams.  Importing this package
+fails loudly when the library has not been built -- there is no CPU path.
+
+    import collective_communication_schedule_gb300 as ccl
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, nranks=8)
+    p = ccl.Plan(s, chunk_elems=32768, dtype=ccl.F32, channels=4)
+    p.execute(inputs, outputs)          # lists of torch CUDA tensors
+    p.status()                          # raises on a device timeout
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libccl.so")
+
+F32, BF16, F16, I32 = 0, 1, 2, 3
+IN, OUT, SCRATCH = 0, 1, 2
+COPY, REDUCE = 0, 1
+RING_ALLREDUCE, RING_ALLGATHER, RING_REDUCESCATTER, HIER_ALLREDUCE, ALLTOALL_2PHASE, ALLTONEXT = range(6)
+FLAG_WRAP, FLAG_NOFUSE = 1, 2
+SCHED_RR, SCHED_HPDS = 0, 1
+TB_CONNECTION, TB_PACKED = 0, 1
+MB_AUTO, MB_ALGO, MB_TASK, MB_SEGMENT = 0, 1, 2, 3
+KIND_NAMES = ["copy", "reduce", "send", "recv", "rrc", "rcs", "fwd", "rrs", "rrcs", "copy_send"]
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", F16: "f16", I32: "i32"}
+ESIZE = {F32: 4, BF16: 2, F16: 2, I32: 4}
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "dependency cycle", 3: "deadlock", 4: "data race",
+          5: "unsupported", 6: "out of device memory", 7: "CUDA error", 8: "device wait timed out",
+          9: "internal error"}
+
+
+class CclError(RuntimeError):
+    def __init__(self, code, detail):
+        super().__init__(f"{STATUS.get(code, code)}: {detail}")
+        self.code = code
+        self.detail = detail
+
+
+class Op(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("op", "src_rank", "src_buf", "src_off", "dst_rank", "dst_buf", "dst_off", "count")]
+
+
+class ScheduleInfo(ctypes.Structure):
+    _fields_ = [("nranks", ctypes.c_int32), ("nchunks", ctypes.c_int32 * 3), ("nops", ctypes.c_int32),
+                ("ninstr", ctypes.c_int32), ("ntransfers", ctypes.c_int32),
+                ("kind_count", ctypes.c_int32 * 10), ("bytes_per_chunk_elem_x_esize", ctypes.c_int64),
+                ("builtin", ctypes.c_int32), ("group_size", ctypes.c_int32)]
+
+
+class InstrInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("kind", "rank", "src_rank", "src_buf", "src_off", "loc_rank", "loc_buf", "loc_off",
+                 "dst_rank", "dst_buf", "dst_off", "count", "peer_in", "peer_out", "xfer_in", "xfer_out",
+                 "position")]
+
+
+class PlanOpts(ctypes.Structure):
+    _fields_ = [("channels", ctypes.c_int32), ("nthreads", ctypes.c_int32), ("slot_bytes", ctypes.c_int64),
+                ("fifo_slots", ctypes.c_int32), ("microbatches", ctypes.c_int32), ("scheduler", ctypes.c_int32),
+                ("tb_alloc", ctypes.c_int32), ("mb_order", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
+                ("instrument", ctypes.c_int32)]
+
+
+class PlanStats(ctypes.Structure):
+    _fields_ = [("schedule_bytes", ctypes.c_int64), ("min_bytes", ctypes.c_int64),
+                ("data_bytes_per_rank", ctypes.c_int64), ("busbw_factor", ctypes.c_double),
+                ("nthreadblocks", ctypes.c_int32), ("nthreadblocks_connection", ctypes.c_int32),
+                ("nsteps", ctypes.c_int32), ("ninstr", ctypes.c_int32), ("nlinks", ctypes.c_int32),
+                ("nsubpipelines", ctypes.c_int32), ("microbatches", ctypes.c_int32), ("mb_order", ctypes.c_int32),
+                ("channels", ctypes.c_int32), ("nthreads", ctypes.c_int32), ("fifo_slots", ctypes.c_int32),
+                ("slot_bytes", ctypes.c_int64), ("fifo_bytes", ctypes.c_int64), ("device_bytes", ctypes.c_int64),
+                ("compile_ms", ctypes.c_double)]
+
+
+class TuneOpts(ctypes.Structure):
+    _fields_ = [("max_rounds", ctypes.c_int32), ("reps", ctypes.c_int32), ("min_gain", ctypes.c_double)]
+
+
+class TuneReport(ctypes.Structure):
+    _fields_ = [("probes", ctypes.c_int32), ("best_us", ctypes.c_double), ("best_gbs", ctypes.c_double),
+                ("default_us", ctypes.c_double)]
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is missing: build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'` (nvcc, sm_103a)")
+    L = ctypes.CDLL(_LIB_PATH)
+    P, I32_, I64_, U32_ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32
+    sig = {
+        "ccl_schedule_compile": [ctypes.POINTER(Op), I32_, I32_, ctypes.POINTER(ctypes.c_int32), I32_,
+                                 ctypes.POINTER(P)],
+        "ccl_schedule_builtin": [I32_, I32_, I32_, U32_, ctypes.POINTER(P)],
+        "ccl_schedule_info": [P, ctypes.POINTER(ScheduleInfo)],
+        "ccl_schedule_get_ops": [P, ctypes.POINTER(Op), I32_, ctypes.POINTER(ctypes.c_int32)],
+        "ccl_schedule_get_instrs": [P, ctypes.POINTER(InstrInfo), I32_, ctypes.POINTER(ctypes.c_int32)],
+        "ccl_plan_create": [P, I64_, I32_, I32_, ctypes.POINTER(PlanOpts), ctypes.POINTER(P)],
+        "ccl_execute": [P, ctypes.POINTER(P), ctypes.POINTER(P), P],
+        "ccl_execute_host": [P, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P), P],
+        "ccl_plan_status": [P],
+        "ccl_plan_stats": [P, ctypes.POINTER(PlanStats)],
+        "ccl_plan_timeline": [P, ctypes.POINTER(ctypes.c_double), I32_, ctypes.POINTER(ctypes.c_double),
+                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
+        "ccl_plan_debug_drop_signal": [P, I32_, I32_],
+        "ccl_plan_check": [P, I64_, I32_, ctypes.POINTER(PlanOpts), ctypes.POINTER(PlanStats)],
+        "ccl_schedule_timeline": [P, I32_, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
+        "ccl_tune": [P, I64_, I32_, ctypes.POINTER(P), ctypes.POINTER(P), P, ctypes.POINTER(TuneOpts),
+                     ctypes.POINTER(PlanOpts), ctypes.POINTER(PlanOpts), ctypes.POINTER(TuneReport)],
+    }
+    for name, args in sig.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    L.ccl_schedule_destroy.argtypes = [P]
+    L.ccl_schedule_destroy.restype = None
+    L.ccl_plan_destroy.argtypes = [P]
+    L.ccl_plan_destroy.restype = None
+    L.ccl_plan_opts_default.argtypes = [ctypes.POINTER(PlanOpts)]
+    L.ccl_plan_opts_default.restype = None
+    for name in ("ccl_last_error_detail", "ccl_version"):
+        getattr(L, name).restype = ctypes.c_char_p
+        getattr(L, name).argtypes = []
+    L.ccl_error_string.restype = ctypes.c_char_p
+    L.ccl_error_string.argtypes = [ctypes.c_int]
+    return L
+
+
+lib = _load()
+LIB_PATH = _LIB_PATH
+
+
+def _check(code):
+    if code != 0:
+        raise CclError(code, lib.ccl_last_error_detail().decode())
+
+
+def _ptrs(bufs):
+    """Device (or host) addresses of a list of torch tensors / ints."""
+    arr = (ctypes.c_void_p * len(bufs))()
+    for i, b in enumerate(bufs):
+        arr[i] = b if isinstance(b, int) else b.data_ptr()
+    return arr
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def default_opts() -> PlanOpts:
+    o = PlanOpts()
+    lib.ccl_plan_opts_default(ctypes.byref(o))
+    return o
+
+
+class Schedule:
+    """A compiled chunk program (``ccl_schedule_t``)."""
+
+    def __init__(self, handle):
+        self._h = ctypes.c_void_p(handle)
+
+    @classmethod
+    def builtin(cls, kind, nranks, group_size=0, flags=0):
+        h = ctypes.c_void_p()
+        _check(lib.ccl_schedule_builtin(kind, nranks, group_size, flags, ctypes.byref(h)))
+        return cls(h.value)
+
+    @classmethod
+    def compile(cls, ops, nranks, nchunks, fuse=True):
+        """``ops``: iterable of 8-int rows (op, src_rank, src_buf, src_off,
+        dst_rank, dst_buf, dst_off, count)."""
+        rows = [tuple(int(v) for v in r) for r in ops]
+        arr = (Op * max(1, len(rows)))(*[Op(*r) for r in rows])
+        nch = (ctypes.c_int32 * 3)(*[int(c) for c in nchunks])
+        h = ctypes.c_void_p()
+        _check(lib.ccl_schedule_compile(arr, len(rows), nranks, nch, 1 if fuse else 0, ctypes.byref(h)))
+        return cls(h.value)
+
+    def info(self) -> ScheduleInfo:
+        i = ScheduleInfo()
+        _check(lib.ccl_schedule_info(self._h, ctypes.byref(i)))
+        return i
+
+    def ops(self):
+        n = ctypes.c_int32()
+        lib.ccl_schedule_get_ops(self._h, None, 0, ctypes.byref(n))
+        arr = (Op * max(1, n.value))()
+        _check(lib.ccl_schedule_get_ops(self._h, arr, n.value, ctypes.byref(n)))
+        return [tuple(getattr(arr[i], f) for f, _ in Op._fields_) for i in range(n.value)]
+
+    def instrs(self):
+        n = ctypes.c_int32()
+        lib.ccl_schedule_get_instrs(self._h, None, 0, ctypes.byref(n))
+        arr = (InstrInfo * max(1, n.value))()
+        _check(lib.ccl_schedule_get_instrs(self._h, arr, n.value, ctypes.byref(n)))
+        return [{f: getattr(arr[i], f) for f, _ in InstrInfo._fields_} for i in range(n.value)]
+
+    def timeline(self, scheduler=SCHED_HPDS):
+        """Sub-pipeline index of every transfer, and the sub-pipeline count."""
+        n = self.info().ntransfers
+        arr = (ctypes.c_int32 * max(1, n))()
+        nsub = ctypes.c_int32()
+        _check(lib.ccl_schedule_timeline(self._h, scheduler, arr, ctypes.byref(nsub)))
+        return list(arr[:n]), nsub.value
+
+    def check(self, chunk_elems, dtype, opts: PlanOpts | None = None, **kw) -> PlanStats:
+        """Plan on the host only (deadlock simulation included, no GPU)."""
+        o = opts if opts is not None else default_opts()
+        for k, v in kw.items():
+            setattr(o, k, v)
+        st = PlanStats()
+        _check(lib.ccl_plan_check(self._h, chunk_elems, dtype, ctypes.byref(o), ctypes.byref(st)))
+        return st
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            lib.ccl_schedule_destroy(h)
+            self._h = ctypes.c_void_p()
+
+
+class Plan:
+    """An executable plan (``ccl_plan_t``) on the current CUDA device."""
+
+    def __init__(self, schedule: Schedule, chunk_elems: int, dtype: int, opts: PlanOpts | None = None, **kw):
+        o = opts if opts is not None else default_opts()
+        for k, v in kw.items():
+            setattr(o, k, v)
+        self.schedule = schedule
+        self.opts = o
+        self.dtype = dtype
+        self.chunk_elems = chunk_elems
+        h = ctypes.c_void_p()
+        _check(lib.ccl_plan_create(schedule._h, chunk_elems, dtype, 0, ctypes.byref(o), ctypes.byref(h)))
+        self._h = h
+        info = schedule.info()
+        self.nranks = info.nranks
+        self.nchunks = tuple(info.nchunks)
+        self.in_elems = info.nchunks[0] * chunk_elems
+        self.out_elems = info.nchunks[1] * chunk_elems
+
+    def execute(self, inputs, outputs, stream=None):
+        _check(lib.ccl_execute(self._h, _ptrs(inputs), _ptrs(outputs), _stream(stream)))
+
+    def execute_host(self, host_in, host_out, dev_in, dev_out, stream=None):
+        _check(lib.ccl_execute_host(self._h, _ptrs(host_in), _ptrs(host_out), _ptrs(dev_in), _ptrs(dev_out),
+                                    _stream(stream)))
+
+    def status(self):
+        _check(lib.ccl_plan_status(self._h))
+
+    def stats(self) -> PlanStats:
+        st = PlanStats()
+        _check(lib.ccl_plan_stats(self._h, ctypes.byref(st)))
+        return st
+
+    def timeline(self):
+        st = self.stats()
+        idle = (ctypes.c_double * st.nthreadblocks)()
+        mean, mx, span = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+        _check(lib.ccl_plan_timeline(self._h, idle, st.nthreadblocks, ctypes.byref(mean), ctypes.byref(mx),
+                                     ctypes.byref(span)))
+        return {"idle": list(idle), "mean_idle": mean.value, "max_idle": mx.value, "span_us": span.value}
+
+    def debug_drop_signal(self, tb, step):
+        _check(lib.ccl_plan_debug_drop_signal(self._h, tb, step))
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            lib.ccl_plan_destroy(h)
+            self._h = ctypes.c_void_p()
+
+
+def tune(schedule: Schedule, chunk_elems, dtype, inputs, outputs, stream=None, start: PlanOpts | None = None,
+         max_rounds=3, reps=5, min_gain=0.01):
+    best = PlanOpts()
+    rep = TuneReport()
+    to = TuneOpts(max_rounds, reps, min_gain)
+    _check(lib.ccl_tune(schedule._h, chunk_elems, dtype, _ptrs(inputs), _ptrs(outputs), _stream(stream),
+                        ctypes.byref(to), ctypes.byref(start) if start is not None else None, ctypes.byref(best),
+                        ctypes.byref(rep)))
+    return best, rep
+
+
+def version() -> str:
+    return lib.ccl_version().decode()

@@ -1,0 +1,43 @@
+// Persistent executor kernel: one CTA per threadblock program.
+//
+// Each CTA walks its list of (instruction, micro-batch) steps.  For every
+// FIFO slot of a step, thread 0 waits (bounded) until the incoming slot is
+// full and the outgoing slot is free, the CTA moves the slot's data with
+// 16-byte vector loads and stores (several in flight per thread), and thread
+// 0 posts the consumed / full flags with gpu-scope release semantics.  The
+// flag protocol stands in for the inter-GPU links of the pages' runtimes
+// (MSCCLang report, §III.1 runtime; ReSCCL report, §II.2 kernel generation):
+// every rank's buffers and every link FIFO live in this GPU's HBM.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "ccl_plan.h"
+
+namespace ccl {
+
+struct KParams {
+    const DInstr* instrs;
+    const DStep* steps;
+    const int32_t* tb_begin;
+    const DLink* links;
+    const DDep* deps;
+    unsigned long long* flags;
+    unsigned long long* counters;
+    char* fifo;
+    int* status;                   // [0] code, [1] threadblock, [2] step, [3] reason
+    unsigned long long* timeline;  // 3 stamps per step, or null
+    long long exec;
+    long long m;
+    long long slot_bytes;
+    unsigned long long timeout_ns;
+    int S;
+    int pad;
+    char* bufs[3][CCL_MAX_RANKS];
+};
+
+enum WaitReason : int { WAIT_DEP = 1, WAIT_FULL = 2, WAIT_FREE = 3 };
+
+}  // namespace ccl

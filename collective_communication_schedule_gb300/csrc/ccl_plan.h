@@ -1,0 +1,108 @@
+// Host-side plan image: everything the executor kernel reads, built by the
+// planner from a compiled schedule and the execution parameters.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include "ccl_internal.h"
+
+namespace ccl {
+
+// operand buffer classes (select cache hints in the kernel)
+enum : int32_t { OPB_NONE = -1 };
+
+// One channel instruction.  Offsets are element offsets of the channel
+// range inside the rank's buffer; a missing operand has buf = -1.
+struct DInstr {
+    int32_t kind;
+    int32_t dtype;
+    int32_t link_in, link_out;
+    int32_t src_rank, src_buf;
+    int32_t loc_rank, loc_buf;
+    int32_t dst_rank, dst_buf;
+    int32_t pad0, pad1;
+    int64_t src_off, loc_off, dst_off;
+    int64_t nelem;
+};
+static_assert(sizeof(DInstr) == 80, "DInstr layout");
+
+// One (channel instruction, micro-batch) step of a threadblock program.
+struct DStep {
+    int32_t instr;
+    int32_t mb;
+    int64_t elem_off;   // piece offset inside the channel range (elements)
+    int64_t nelem;      // piece length (elements)
+    int64_t seq_in;     // first slot sequence number on link_in (per execution)
+    int64_t seq_out;    // first slot sequence number on link_out
+    int32_t nslots;     // FIFO slots this piece occupies (>= 1 when a link is used)
+    int32_t dep_begin;  // waits: deps[dep_begin .. dep_begin + dep_count)
+    int32_t dep_count;
+    int32_t signal;     // counter to post after the step, or -1
+    int32_t flags;      // bit 0: do not post link flags (debug hook)
+    int32_t pad;
+};
+static_assert(sizeof(DStep) == 64, "DStep layout");
+
+struct DLink {
+    int64_t slot_base;  // byte offset of slot 0 in the FIFO pool
+    int64_t total;      // slot sequences per execution
+    int32_t flag_base;  // full flags at [flag_base, +S), consumed at [flag_base+S, +S)
+    int32_t src_rank, dst_rank, channel;
+};
+static_assert(sizeof(DLink) == 32, "DLink layout");
+
+struct DDep {
+    int32_t counter;
+    int32_t pad;
+    int64_t value;      // wait until counter >= exec * m + value
+};
+
+struct PlanImage {
+    std::vector<DInstr> instrs;
+    std::vector<DStep> steps;
+    std::vector<int32_t> tb_begin;   // ntb + 1
+    std::vector<DLink> links;
+    std::vector<DDep> deps;
+    std::vector<int32_t> tb_rank;    // rank each threadblock serves (reporting)
+    int32_t ntb = 0;
+    int32_t ncounters = 0;
+    int32_t nthreads = 512;
+    int32_t S = 4;
+    int64_t slot_bytes = 0;
+    int64_t fifo_bytes = 0;
+    int32_t m = 1;
+    int32_t channels = 1;
+    int32_t mb_order = CCL_MB_ALGO;
+    int32_t nsubpipelines = 0;
+    int32_t ntb_connection = 0;
+    int32_t dtype = CCL_F32;
+    int32_t esize = 4;
+    int64_t chunk_elems = 0;
+    int64_t schedule_bytes = 0;
+    int64_t min_bytes = 0;
+    int64_t data_bytes_per_rank = 0;
+    double busbw_factor = 0;
+    bool scratch_used[CCL_MAX_RANKS] = {};
+    int64_t scratch_elems = 0;       // per rank
+    int64_t in_elems = 0, out_elems = 0;
+    int32_t timeout_ms = 2000;
+    int32_t instrument = 0;
+};
+
+struct Timeline {
+    std::vector<int> sp_lo, sp_hi;   // per instruction
+    std::vector<int> xfer_sp;        // per transfer
+    int nsp = 0;
+};
+
+ccl_status_t build_timeline(const ccl_schedule& s, int scheduler, Timeline* tl);
+
+ccl_status_t build_plan(const ccl_schedule& s, int64_t chunk_elems, int32_t dtype,
+                        const ccl_plan_opts_t& opts, PlanImage* img);
+
+// Abstract execution of the threadblock programs with bounded FIFOs.
+// Returns true when every threadblock finishes; otherwise fills `why`.
+bool simulate_plan(const PlanImage& img, std::string* why);
+
+}  // namespace ccl

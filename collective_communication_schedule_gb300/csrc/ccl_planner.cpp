@@ -1,0 +1,680 @@
+// Planner: compiled schedule + execution parameters -> threadblock programs.
+//
+// Steps (ReSCCL report, §II.1-II.2; MSCCLang report, §III.1):
+//  1. Task timeline.  A task is one cross-rank transfer (it occupies the link
+//     between its two ranks) or one rank-local instruction.  A task waits for
+//     the tasks of every instruction its sender or receiver depends on, and
+//     a transfer that is forwarded waits for the transfer it forwards.  Tasks
+//     are list-scheduled into sub-pipelines; one sub-pipeline never holds two
+//     tasks on the same link and never a task with a predecessor in the same
+//     sub-pipeline.  RR takes ready tasks in program order; HPDS
+//     (hierarchical-priority dynamic scheduling) takes first the tasks of the
+//     chunk that has been scheduled least often.
+//  2. Threadblock allocation.  CONNECTION: first fit, one threadblock holds at
+//     most one incoming and one outgoing link (one threadblock per
+//     connection).  PACKED (state-based): connection threadblocks of a rank
+//     whose sets of active sub-pipelines are disjoint are merged.
+//  3. Program order inside a threadblock: by sub-pipeline, then program
+//     position.  Micro-batch order: ALGO (micro-batch outermost), TASK (an
+//     instruction runs all its micro-batches before the next: task-level
+//     execution) or SEGMENT (task-level across idle gaps of the threadblock,
+//     micro-batch-major between them).  A dependency on a partly overlapping
+//     range inside the current segment always starts a new segment.
+//  4. Geometry.  Every instruction range is split into `channels` pieces and
+//     every channel piece into `m` micro-batch pieces, both in 16-byte units
+//     (the element tail goes to the last piece); a piece moves through the
+//     link FIFO in slots of `slot_bytes`.
+//  5. Link sequence numbers are assigned in the sending threadblock's order;
+//     a receiver waits for the sequence number of the piece it needs, so the
+//     flags are per slot and no piece is read out of turn.
+//  6. Dependencies between instructions in different threadblocks become
+//     counter waits (per micro-batch when the ranges are identical, on the
+//     whole instruction otherwise).
+//  7. The programs are executed abstractly with bounded FIFOs; a plan that
+//     cannot finish is rejected.
+#include <algorithm>
+#include <chrono>
+#include <map>
+#include <set>
+#include <string>
+
+#include "ccl_plan.h"
+
+namespace ccl {
+namespace {
+
+struct Piece {
+    int64_t off, len;
+};
+
+Piece split(int64_t n, int64_t ve, int64_t parts, int64_t k)
+{
+    int64_t V = n / ve;
+    int64_t a = (V * k / parts) * ve;
+    int64_t b = (k == parts - 1) ? n : (V * (k + 1) / parts) * ve;
+    return {a, b - a};
+}
+
+int esize_of(int dt) { return (dt == CCL_BF16 || dt == CCL_F16) ? 2 : 4; }
+
+}  // namespace
+
+ccl_status_t build_timeline(const ccl_schedule& s, int scheduler, Timeline* tl)
+{
+    const int ni = (int)s.instrs.size();
+    const int nx = (int)s.xfers.size();
+    // tasks: transfers first, then local instructions
+    std::vector<std::vector<int>> itasks(ni);
+    struct T {
+        int key, a, b, chunk;
+        std::vector<int> preds;
+        int sp = -1;
+    };
+    std::vector<T> tasks;
+    for (int x = 0; x < nx; ++x) {
+        const Xfer& X = s.xfers[x];
+        tasks.push_back(T{X.op_index, X.src_rank, X.dst_rank, X.chunk_id, {}});
+        itasks[X.send_instr].push_back(x);
+        itasks[X.recv_instr].push_back(x);
+    }
+    for (int i = 0; i < ni; ++i) {
+        if (!itasks[i].empty()) continue;
+        itasks[i].push_back((int)tasks.size());
+        tasks.push_back(T{s.instrs[i].position, -1, -1, (int)s.instrs[i].src.off, {}});
+    }
+    std::vector<std::vector<int>> ideps(ni);
+    for (const Dep& d : s.deps) ideps[d.to].push_back(d.from);
+    auto add_preds_of = [&](int t, int instr) {
+        for (int j : ideps[instr])
+            for (int u : itasks[j])
+                if (u != t) tasks[t].preds.push_back(u);
+    };
+    for (int x = 0; x < nx; ++x) {
+        const Xfer& X = s.xfers[x];
+        add_preds_of(x, X.send_instr);
+        add_preds_of(x, X.recv_instr);
+        int y = s.instrs[X.send_instr].xfer_in;
+        if (y >= 0) tasks[x].preds.push_back(y);
+    }
+    for (int i = 0; i < ni; ++i)
+        if (s.instrs[i].xfer_in < 0 && s.instrs[i].xfer_out < 0) add_preds_of(itasks[i][0], i);
+    for (auto& t : tasks) {
+        std::sort(t.preds.begin(), t.preds.end());
+        t.preds.erase(std::unique(t.preds.begin(), t.preds.end()), t.preds.end());
+    }
+    const int nt = (int)tasks.size();
+    std::vector<int> order(nt);
+    for (int i = 0; i < nt; ++i) order[i] = i;
+    std::sort(order.begin(), order.end(),
+              [&](int a, int b) { return tasks[a].key != tasks[b].key ? tasks[a].key < tasks[b].key : a < b; });
+    std::map<int, int> times;  // chunk -> tasks already scheduled
+    int done = 0, sp = 0;
+    while (done < nt) {
+        std::vector<int> ready;
+        for (int t : order) {
+            if (tasks[t].sp >= 0) continue;
+            bool ok = true;
+            for (int u : tasks[t].preds)
+                if (tasks[u].sp < 0 || tasks[u].sp >= sp) { ok = false; break; }
+            if (ok) ready.push_back(t);
+        }
+        if (ready.empty()) return fail(CCL_ERR_CYCLE, "dependency cycle among compiled instructions");
+        if (scheduler == CCL_SCHED_HPDS) {
+            std::stable_sort(ready.begin(), ready.end(), [&](int a, int b) {
+                int ca = times[tasks[a].chunk], cb = times[tasks[b].chunk];
+                if (ca != cb) return ca < cb;
+                if (tasks[a].chunk != tasks[b].chunk) return tasks[a].chunk < tasks[b].chunk;
+                return false;
+            });
+        }
+        std::set<std::pair<int, int>> used;
+        std::vector<int> chosen;
+        for (int t : ready) {
+            if (tasks[t].a >= 0) {
+                auto key = std::make_pair(tasks[t].a, tasks[t].b);
+                if (used.count(key)) continue;
+                used.insert(key);
+            }
+            chosen.push_back(t);
+        }
+        for (int t : chosen) {
+            tasks[t].sp = sp;
+            times[tasks[t].chunk]++;
+        }
+        done += (int)chosen.size();
+        ++sp;
+    }
+    tl->nsp = sp;
+    tl->xfer_sp.assign(nx, -1);
+    for (int x = 0; x < nx; ++x) tl->xfer_sp[x] = tasks[x].sp;
+    tl->sp_lo.assign(ni, 1 << 30);
+    tl->sp_hi.assign(ni, -1);
+    for (int i = 0; i < ni; ++i)
+        for (int t : itasks[i]) {
+            tl->sp_lo[i] = std::min(tl->sp_lo[i], tasks[t].sp);
+            tl->sp_hi[i] = std::max(tl->sp_hi[i], tasks[t].sp);
+        }
+    return CCL_OK;
+}
+
+namespace {
+
+// rank-level threadblocks: list of instruction ids in program order
+using TBList = std::vector<std::vector<int>>;
+
+void allocate_connection(const ccl_schedule& s, const Timeline& tl, TBList* tbs, std::vector<int>* tb_rank)
+{
+    const int ni = (int)s.instrs.size();
+    std::vector<std::vector<int>> byrank(s.nranks);
+    for (int i = 0; i < ni; ++i) byrank[s.instrs[i].rank].push_back(i);
+    for (int r = 0; r < s.nranks; ++r) {
+        auto& v = byrank[r];
+        std::sort(v.begin(), v.end(), [&](int a, int b) {
+            if (tl.sp_hi[a] != tl.sp_hi[b]) return tl.sp_hi[a] < tl.sp_hi[b];
+            return s.instrs[a].position < s.instrs[b].position;
+        });
+        struct C { int in, out, id; };
+        std::vector<C> cs;
+        for (int i : v) {
+            const Instr& I = s.instrs[i];
+            int in = I.xfer_in >= 0 ? s.xfers[I.xfer_in].src_rank : -1;
+            int out = I.xfer_out >= 0 ? s.xfers[I.xfer_out].dst_rank : -1;
+            auto compat = [&](const C& c) {
+                return (in < 0 || c.in < 0 || c.in == in) && (out < 0 || c.out < 0 || c.out == out);
+            };
+            int pick = -1;
+            for (int k = 0; k < (int)cs.size() && pick < 0; ++k)
+                if (compat(cs[k]) && ((in >= 0 && cs[k].in == in) || (out >= 0 && cs[k].out == out)))
+                    pick = k;
+            for (int k = 0; k < (int)cs.size() && pick < 0; ++k)
+                if (compat(cs[k])) pick = k;
+            if (pick < 0) {
+                cs.push_back(C{-1, -1, (int)tbs->size()});
+                tbs->push_back({});
+                tb_rank->push_back(r);
+                pick = (int)cs.size() - 1;
+            }
+            if (in >= 0) cs[pick].in = in;
+            if (out >= 0) cs[pick].out = out;
+            (*tbs)[cs[pick].id].push_back(i);
+        }
+    }
+}
+
+void pack_state_based(const ccl_schedule& s, const Timeline& tl, TBList* tbs, std::vector<int>* tb_rank)
+{
+    struct G { int rank; std::vector<char> busy; std::vector<int> instrs; int first; };
+    std::vector<int> idx(tbs->size());
+    for (size_t i = 0; i < idx.size(); ++i) idx[i] = (int)i;
+    auto first_sp = [&](int t) {
+        int f = 1 << 30;
+        for (int i : (*tbs)[t]) f = std::min(f, tl.sp_lo[i]);
+        return f;
+    };
+    std::sort(idx.begin(), idx.end(), [&](int a, int b) {
+        int fa = first_sp(a), fb = first_sp(b);
+        return fa != fb ? fa < fb : a < b;
+    });
+    std::vector<G> groups;
+    for (int t : idx) {
+        std::vector<char> busy(tl.nsp + 1, 0);
+        for (int i : (*tbs)[t])
+            for (int k = tl.sp_lo[i]; k <= tl.sp_hi[i]; ++k) busy[k] = 1;
+        int pick = -1;
+        for (int g = 0; g < (int)groups.size() && pick < 0; ++g) {
+            if (groups[g].rank != (*tb_rank)[t]) continue;
+            bool clash = false;
+            for (int k = 0; k <= tl.nsp && !clash; ++k) clash = busy[k] && groups[g].busy[k];
+            if (!clash) pick = g;
+        }
+        if (pick < 0) {
+            groups.push_back(G{(*tb_rank)[t], busy, (*tbs)[t], first_sp(t)});
+        } else {
+            for (int k = 0; k <= tl.nsp; ++k) groups[pick].busy[k] |= busy[k];
+            auto& v = groups[pick].instrs;
+            v.insert(v.end(), (*tbs)[t].begin(), (*tbs)[t].end());
+        }
+    }
+    // keep threadblocks grouped by rank
+    std::stable_sort(groups.begin(), groups.end(), [](const G& a, const G& b) { return a.rank < b.rank; });
+    tbs->clear();
+    tb_rank->clear();
+    for (auto& g : groups) {
+        std::sort(g.instrs.begin(), g.instrs.end(), [&](int a, int b) {
+            if (tl.sp_hi[a] != tl.sp_hi[b]) return tl.sp_hi[a] < tl.sp_hi[b];
+            return s.instrs[a].position < s.instrs[b].position;
+        });
+        tbs->push_back(g.instrs);
+        tb_rank->push_back(g.rank);
+    }
+}
+
+// segments of one threadblock program
+std::vector<std::vector<int>> make_segments(const ccl_schedule& s, const Timeline& tl,
+                                            const std::vector<int>& prog, int order,
+                                            const std::vector<std::vector<std::pair<int, bool>>>& ideps)
+{
+    std::vector<std::vector<int>> segs;
+    std::set<int> cur;
+    int cur_hi = -1;
+    for (int idx = 0; idx < (int)prog.size(); ++idx) {
+        int i = prog[idx];
+        bool cut = false;
+        if (!segs.empty()) {
+            if (order == CCL_MB_TASK) cut = true;
+            if (order == CCL_MB_SEGMENT && tl.sp_lo[i] > cur_hi + 1) cut = true;
+            for (auto& d : ideps[i])
+                if (!d.second && cur.count(d.first)) cut = true;
+        }
+        if (segs.empty() || cut) {
+            segs.push_back({});
+            cur.clear();
+            cur_hi = -1;
+        }
+        segs.back().push_back(i);
+        cur.insert(i);
+        cur_hi = std::max(cur_hi, tl.sp_hi[i]);
+    }
+    (void)s;
+    return segs;
+}
+
+struct Attempt {
+    int alloc, m, order;
+};
+
+ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList& tbs,
+                         const std::vector<int>& tb_rank, int64_t ce, int dtype,
+                         const ccl_plan_opts_t& o, int m, int order, PlanImage* img)
+{
+    const int ni = (int)s.instrs.size();
+    const int p = o.channels;
+    const int es = esize_of(dtype);
+    const int64_t ve = 16 / es;
+    const int S = o.fifo_slots;
+    const int64_t slot_elems = o.slot_bytes / es;
+    const int nT = (int)tbs.size();
+
+    std::vector<std::vector<std::pair<int, bool>>> ideps(ni);
+    for (const Dep& d : s.deps) ideps[d.to].push_back({d.from, d.exact});
+
+    img->instrs.assign((size_t)ni * p, DInstr{});
+    img->steps.clear();
+    img->links.clear();
+    img->deps.clear();
+    img->tb_begin.clear();
+    img->tb_rank.clear();
+    img->m = m;
+    img->channels = p;
+    img->mb_order = order;
+    img->S = S;
+    img->slot_bytes = o.slot_bytes;
+    img->nthreads = o.nthreads;
+    img->dtype = dtype;
+    img->esize = es;
+    img->chunk_elems = ce;
+    img->nsubpipelines = tl.nsp;
+    img->timeout_ms = o.timeout_ms;
+    img->instrument = o.instrument;
+    for (int r = 0; r < CCL_MAX_RANKS; ++r) img->scratch_used[r] = false;
+
+    // links
+    std::map<std::tuple<int, int, int>, int> link_id;
+    auto get_link = [&](int a, int b, int ch) {
+        auto key = std::make_tuple(a, b, ch);
+        auto it = link_id.find(key);
+        if (it != link_id.end()) return it->second;
+        int id = (int)img->links.size();
+        DLink L{};
+        L.slot_base = (int64_t)id * S * o.slot_bytes;
+        L.total = 0;
+        L.flag_base = id * 2 * S;
+        L.src_rank = a; L.dst_rank = b; L.channel = ch;
+        img->links.push_back(L);
+        link_id[key] = id;
+        return id;
+    };
+
+    // channel instructions
+    int64_t sched_bytes = 0;
+    for (int i = 0; i < ni; ++i) {
+        const Instr& I = s.instrs[i];
+        int64_t n = I.count * ce;
+        for (int ch = 0; ch < p; ++ch) {
+            Piece pc = split(n, ve, p, ch);
+            DInstr& D = img->instrs[(size_t)i * p + ch];
+            D.kind = I.kind;
+            D.dtype = dtype;
+            D.link_in = I.xfer_in >= 0 ? get_link(s.xfers[I.xfer_in].src_rank, I.rank, ch) : -1;
+            D.link_out = I.xfer_out >= 0 ? get_link(I.rank, s.xfers[I.xfer_out].dst_rank, ch) : -1;
+            D.src_rank = I.src.rank; D.src_buf = I.src.valid() ? I.src.buf : -1;
+            D.loc_rank = I.loc.rank; D.loc_buf = I.loc.valid() ? I.loc.buf : -1;
+            D.dst_rank = I.dst.rank; D.dst_buf = I.dst.valid() ? I.dst.buf : -1;
+            D.src_off = I.src.valid() ? I.src.off * ce + pc.off : 0;
+            D.loc_off = I.loc.valid() ? I.loc.off * ce + pc.off : 0;
+            D.dst_off = I.dst.valid() ? I.dst.off * ce + pc.off : 0;
+            D.nelem = pc.len;
+            sched_bytes += kind_bytes_factor(I.kind) * pc.len * es;
+            for (const Range* rg : {&I.src, &I.loc, &I.dst})
+                if (rg->valid() && rg->buf == CCL_BUF_SCRATCH) img->scratch_used[rg->rank] = true;
+        }
+    }
+    img->schedule_bytes = sched_bytes;
+
+    // threadblock programs -> steps
+    const int ntb = nT * p;
+    img->ntb = ntb;
+    std::vector<int> dev_tb_of((size_t)ni * p, -1);
+    std::vector<std::vector<int>> step_of((size_t)ni * p, std::vector<int>(m, -1));
+    for (int ch = 0; ch < p; ++ch) {
+        for (int t = 0; t < nT; ++t) {
+            int dtb = ch * nT + t;
+            img->tb_begin.push_back((int)img->steps.size());
+            img->tb_rank.push_back(tb_rank[t]);
+            auto segs = make_segments(s, tl, tbs[t], order, ideps);
+            for (auto& seg : segs) {
+                for (int mb = 0; mb < m; ++mb) {
+                    for (int i : seg) {
+                        int ci = i * p + ch;
+                        dev_tb_of[ci] = dtb;
+                        const DInstr& D = img->instrs[ci];
+                        Piece pc = split(D.nelem, ve, m, mb);
+                        DStep st{};
+                        st.instr = ci;
+                        st.mb = mb;
+                        st.elem_off = pc.off;
+                        st.nelem = pc.len;
+                        st.seq_in = st.seq_out = 0;
+                        bool linked = D.link_in >= 0 || D.link_out >= 0;
+                        st.nslots = linked ? (int32_t)std::max<int64_t>(1, (pc.len + slot_elems - 1) / slot_elems) : 0;
+                        st.dep_begin = 0;
+                        st.dep_count = 0;
+                        st.signal = -1;
+                        st.flags = 0;
+                        step_of[ci][mb] = (int)img->steps.size();
+                        img->steps.push_back(st);
+                    }
+                }
+            }
+        }
+    }
+    img->tb_begin.push_back((int)img->steps.size());
+
+    // sequence numbers per link, in the sending threadblock's order
+    {
+        std::vector<std::vector<std::pair<int, int>>> senders(img->links.size());  // (step, tb)
+        for (int tb = 0; tb < ntb; ++tb)
+            for (int k = img->tb_begin[tb]; k < img->tb_begin[tb + 1]; ++k) {
+                const DInstr& D = img->instrs[img->steps[k].instr];
+                if (D.link_out >= 0) senders[D.link_out].push_back({k, tb});
+            }
+        for (size_t L = 0; L < senders.size(); ++L) {
+            auto& v = senders[L];
+            bool single = true;
+            for (auto& e : v) single = single && e.second == v[0].second;
+            if (!single) {
+                std::stable_sort(v.begin(), v.end(), [&](const std::pair<int, int>& a, const std::pair<int, int>& b) {
+                    int ia = a.first - img->tb_begin[a.second], ib = b.first - img->tb_begin[b.second];
+                    return ia != ib ? ia < ib : a.second < b.second;
+                });
+            }
+            int64_t seq = 0;
+            for (auto& e : v) {
+                DStep& st = img->steps[e.first];
+                st.seq_out = seq;
+                seq += st.nslots;
+            }
+            img->links[L].total = seq;
+        }
+        // receivers take the sender's numbers
+        for (int i = 0; i < ni; ++i) {
+            const Instr& I = s.instrs[i];
+            if (I.xfer_in < 0) continue;
+            int snd = s.xfers[I.xfer_in].send_instr;
+            for (int ch = 0; ch < p; ++ch)
+                for (int mb = 0; mb < m; ++mb) {
+                    DStep& r = img->steps[step_of[(size_t)i * p + ch][mb]];
+                    const DStep& w = img->steps[step_of[(size_t)snd * p + ch][mb]];
+                    if (r.nslots != w.nslots || r.nelem != w.nelem)
+                        return fail(CCL_ERR_INTERNAL, "sender and receiver pieces disagree");
+                    r.seq_in = w.seq_out;
+                }
+        }
+    }
+
+    // dependencies across threadblocks -> counters
+    {
+        std::vector<int> counter_of((size_t)ni * p, -1);
+        auto counter = [&](int ci) {
+            if (counter_of[ci] < 0) counter_of[ci] = img->ncounters++;
+            return counter_of[ci];
+        };
+        img->ncounters = 0;
+        std::vector<std::vector<DDep>> waits(img->steps.size());
+        for (const Dep& d : s.deps) {
+            for (int ch = 0; ch < p; ++ch) {
+                int cb = d.to * p + ch;
+                if (d.exact) {
+                    int ca = d.from * p + ch;
+                    if (dev_tb_of[ca] == dev_tb_of[cb]) continue;
+                    for (int mb = 0; mb < m; ++mb)
+                        waits[step_of[cb][mb]].push_back(DDep{counter(ca), 0, mb + 1});
+                } else {
+                    // all micro-batches of every channel of `from`; the first
+                    // step of `to` (micro-batch 0) waits, later ones follow it
+                    for (int ch2 = 0; ch2 < p; ++ch2) {
+                        int ca = d.from * p + ch2;
+                        if (dev_tb_of[ca] == dev_tb_of[cb]) continue;
+                        waits[step_of[cb][0]].push_back(DDep{counter(ca), 0, (int64_t)m});
+                    }
+                }
+            }
+        }
+        for (size_t k = 0; k < img->steps.size(); ++k) {
+            auto& w = waits[k];
+            std::sort(w.begin(), w.end(), [](const DDep& a, const DDep& b) {
+                return a.counter != b.counter ? a.counter < b.counter : a.value > b.value;
+            });
+            std::vector<DDep> u;
+            for (auto& e : w)
+                if (u.empty() || u.back().counter != e.counter) u.push_back(e);
+            img->steps[k].dep_begin = (int32_t)img->deps.size();
+            img->steps[k].dep_count = (int32_t)u.size();
+            img->deps.insert(img->deps.end(), u.begin(), u.end());
+        }
+        for (size_t k = 0; k < img->steps.size(); ++k) {
+            int ci = img->steps[k].instr;
+            img->steps[k].signal = counter_of[ci];
+        }
+    }
+    img->fifo_bytes = (int64_t)img->links.size() * S * o.slot_bytes;
+    return CCL_OK;
+}
+
+}  // namespace
+
+bool simulate_plan(const PlanImage& img, std::string* why)
+{
+    const int ntb = img.ntb;
+    const int S = img.S;
+    std::vector<int64_t> flags((size_t)img.links.size() * 2 * S, 0);
+    std::vector<int64_t> counters(img.ncounters, 0);
+    std::vector<int> si(ntb), slot(ntb, 0);
+    std::vector<char> deps_ok(ntb, 0);
+    for (int t = 0; t < ntb; ++t) si[t] = img.tb_begin[t];
+    int finished = 0;
+    for (int t = 0; t < ntb; ++t)
+        if (si[t] == img.tb_begin[t + 1]) ++finished;
+    while (finished < ntb) {
+        bool progress = false;
+        for (int t = 0; t < ntb; ++t) {
+            while (si[t] < img.tb_begin[t + 1]) {
+                const DStep& st = img.steps[si[t]];
+                const DInstr& D = img.instrs[st.instr];
+                if (!deps_ok[t]) {
+                    bool ok = true;
+                    for (int k = 0; k < st.dep_count && ok; ++k) {
+                        const DDep& d = img.deps[st.dep_begin + k];
+                        ok = counters[d.counter] >= d.value;
+                    }
+                    if (!ok) break;
+                    deps_ok[t] = 1;
+                }
+                bool blocked = false;
+                while (slot[t] < st.nslots) {
+                    int64_t sin = st.seq_in + slot[t], sout = st.seq_out + slot[t];
+                    if (D.link_in >= 0) {
+                        const DLink& L = img.links[D.link_in];
+                        if (flags[L.flag_base + sin % S] < sin + 1) { blocked = true; break; }
+                    }
+                    if (D.link_out >= 0) {
+                        const DLink& L = img.links[D.link_out];
+                        if (flags[L.flag_base + S + sout % S] < sout - S + 1) { blocked = true; break; }
+                    }
+                    if (D.link_in >= 0) {
+                        const DLink& L = img.links[D.link_in];
+                        flags[L.flag_base + S + sin % S] = sin + 1;
+                    }
+                    if (D.link_out >= 0) {
+                        const DLink& L = img.links[D.link_out];
+                        flags[L.flag_base + sout % S] = sout + 1;
+                    }
+                    ++slot[t];
+                    progress = true;
+                }
+                if (blocked) break;
+                if (st.signal >= 0) counters[st.signal] = std::max<int64_t>(counters[st.signal], st.mb + 1);
+                ++si[t];
+                slot[t] = 0;
+                deps_ok[t] = 0;
+                progress = true;
+                if (si[t] == img.tb_begin[t + 1]) ++finished;
+            }
+        }
+        if (!progress) {
+            if (why) {
+                for (int t = 0; t < ntb; ++t) {
+                    if (si[t] == img.tb_begin[t + 1]) continue;
+                    const DStep& st = img.steps[si[t]];
+                    const DInstr& D = img.instrs[st.instr];
+                    *why = "threadblock " + std::to_string(t) + " (rank " + std::to_string(img.tb_rank[t]) +
+                           ") stuck at step " + std::to_string(si[t] - img.tb_begin[t]) + " kind " +
+                           std::to_string(D.kind) + " micro-batch " + std::to_string(st.mb) + " slot " +
+                           std::to_string(slot[t]) + " of " + std::to_string(st.nslots);
+                    break;
+                }
+            }
+            return false;
+        }
+    }
+    return true;
+}
+
+ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const ccl_plan_opts_t& o,
+                        PlanImage* img)
+{
+    if (ce <= 0) return fail(CCL_ERR_INVALID_ARG, "chunk_elems must be positive");
+    if (dtype < CCL_F32 || dtype > CCL_I32) return fail(CCL_ERR_INVALID_ARG, "unknown dtype");
+    if (o.channels < 1 || o.channels > 256) return fail(CCL_ERR_INVALID_ARG, "channels must be in 1..256");
+    if (o.nthreads < 64 || o.nthreads > 1024 || o.nthreads % 32)
+        return fail(CCL_ERR_INVALID_ARG, "nthreads must be a multiple of 32 in 64..1024");
+    if (o.slot_bytes < 16 || o.slot_bytes % 16) return fail(CCL_ERR_INVALID_ARG, "slot_bytes must be a positive multiple of 16");
+    if (o.fifo_slots < 2 || o.fifo_slots > 64) return fail(CCL_ERR_INVALID_ARG, "fifo_slots must be in 2..64");
+    if (o.microbatches < 0 || o.microbatches > 65536) return fail(CCL_ERR_INVALID_ARG, "microbatches out of range");
+    if (o.scheduler != CCL_SCHED_RR && o.scheduler != CCL_SCHED_HPDS) return fail(CCL_ERR_INVALID_ARG, "unknown scheduler");
+    if (o.tb_alloc != CCL_TB_CONNECTION && o.tb_alloc != CCL_TB_PACKED) return fail(CCL_ERR_INVALID_ARG, "unknown tb_alloc");
+    if (o.mb_order < CCL_MB_AUTO || o.mb_order > CCL_MB_SEGMENT) return fail(CCL_ERR_INVALID_ARG, "unknown mb_order");
+    if (o.timeout_ms <= 0) return fail(CCL_ERR_INVALID_ARG, "timeout_ms must be positive");
+
+    const int es = esize_of(dtype);
+    Timeline tl;
+    ccl_status_t st = build_timeline(s, o.scheduler, &tl);
+    if (st != CCL_OK) return st;
+
+    TBList conn;
+    std::vector<int> conn_rank;
+    allocate_connection(s, tl, &conn, &conn_rank);
+    TBList packed = conn;
+    std::vector<int> packed_rank = conn_rank;
+    if (o.tb_alloc == CCL_TB_PACKED) pack_state_based(s, tl, &packed, &packed_rank);
+
+    // micro-batch candidates
+    int64_t max_slots = 1;
+    for (const Instr& I : s.instrs) {
+        if (I.xfer_in < 0 && I.xfer_out < 0) continue;
+        int64_t n = I.count * ce;
+        int64_t per_ch = (n + o.channels - 1) / o.channels;
+        max_slots = std::max<int64_t>(max_slots, (per_ch * es + o.slot_bytes - 1) / o.slot_bytes);
+    }
+    int64_t half = std::max(1, o.fifo_slots / 2);
+    int m_small = (int)std::min<int64_t>(4096, (max_slots + half - 1) / half);
+    std::vector<int> ms;
+    if (o.microbatches > 0) ms.push_back(o.microbatches);
+    else { ms.push_back(1); if (m_small > 1) ms.push_back(m_small); }
+    std::vector<int> orders;
+    if (o.mb_order == CCL_MB_AUTO) orders = {CCL_MB_SEGMENT, CCL_MB_ALGO};
+    else orders = {o.mb_order};
+    std::vector<int> allocs;
+    if (o.tb_alloc == CCL_TB_PACKED) allocs = {CCL_TB_PACKED, CCL_TB_CONNECTION};
+    else allocs = {CCL_TB_CONNECTION};
+
+    std::string first_why;
+    for (int alloc : allocs) {
+        const TBList& tbs = alloc == CCL_TB_PACKED ? packed : conn;
+        const std::vector<int>& tr = alloc == CCL_TB_PACKED ? packed_rank : conn_rank;
+        for (int m : ms) {
+            for (int order : orders) {
+                PlanImage cand;
+                st = build_image(s, tl, tbs, tr, ce, dtype, o, m, order, &cand);
+                if (st != CCL_OK) return st;
+                std::string why;
+                if (simulate_plan(cand, &why)) {
+                    *img = std::move(cand);
+                    img->ntb_connection = (int)conn.size() * o.channels;
+                    goto done;
+                }
+                if (first_why.empty())
+                    first_why = "m=" + std::to_string(m) + " order=" + std::to_string(order) + ": " + why;
+            }
+        }
+    }
+    return fail(CCL_ERR_DEADLOCK, "threadblock programs cannot finish with " + std::to_string(o.fifo_slots) +
+                                      " FIFO slots of " + std::to_string(o.slot_bytes) + " bytes (" + first_why + ")");
+done:
+    // byte accounting of the source program
+    {
+        std::vector<std::vector<char>> rd(s.nranks, std::vector<char>(std::max(1, s.nchunks[0]), 0));
+        std::vector<std::vector<char>> wr(s.nranks, std::vector<char>(std::max(1, s.nchunks[1]), 0));
+        for (const ccl_op_t& op : s.ops) {
+            if (op.src_buf == CCL_BUF_IN)
+                for (int k = 0; k < op.count; ++k) rd[op.src_rank][op.src_off + k] = 1;
+            if (op.dst_buf == CCL_BUF_OUT)
+                for (int k = 0; k < op.count; ++k) wr[op.dst_rank][op.dst_off + k] = 1;
+        }
+        int64_t c = 0;
+        for (int r = 0; r < s.nranks; ++r) {
+            for (char v : rd[r]) c += v;
+            for (char v : wr[r]) c += v;
+        }
+        img->min_bytes = c * ce * es;
+    }
+    img->in_elems = (int64_t)s.nchunks[0] * ce;
+    img->out_elems = (int64_t)s.nchunks[1] * ce;
+    img->scratch_elems = (int64_t)s.nchunks[2] * ce;
+    {
+        double R = s.nranks;
+        int64_t in_b = img->in_elems * es, out_b = img->out_elems * es;
+        switch (s.builtin) {
+        case CCL_RING_ALLREDUCE:
+        case CCL_HIER_ALLREDUCE: img->data_bytes_per_rank = in_b; img->busbw_factor = 2.0 * (R - 1) / R; break;
+        case CCL_RING_ALLGATHER: img->data_bytes_per_rank = out_b; img->busbw_factor = (R - 1) / R; break;
+        case CCL_RING_REDUCESCATTER: img->data_bytes_per_rank = in_b; img->busbw_factor = (R - 1) / R; break;
+        case CCL_ALLTOALL_2PHASE: img->data_bytes_per_rank = in_b; img->busbw_factor = (R - 1) / R; break;
+        case CCL_ALLTONEXT: img->data_bytes_per_rank = in_b; img->busbw_factor = 1.0; break;
+        default: img->data_bytes_per_rank = in_b; img->busbw_factor = 0.0; break;
+        }
+    }
+    return CCL_OK;
+}
+
+}  // namespace ccl

@@ -1,0 +1,817 @@
+// C ABI entry points, device plan management and the executor kernel.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "ccl_executor.cuh"
+#include "ccl_internal.h"
+#include "ccl_plan.h"
+
+// ======================================================================
+// errors
+// ======================================================================
+namespace ccl {
+static thread_local std::string g_detail;
+void set_error(const std::string& msg) { g_detail = msg; }
+ccl_status_t fail(ccl_status_t st, const std::string& msg)
+{
+    g_detail = msg;
+    return st;
+}
+static ccl_status_t cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(e == cudaErrorMemoryAllocation ? CCL_ERR_OOM : CCL_ERR_CUDA,
+                std::string(what) + ": " + cudaGetErrorString(e));
+}
+}  // namespace ccl
+
+#define CUDA_TRY(call, what)                                        \
+    do {                                                            \
+        cudaError_t _e = (call);                                    \
+        if (_e != cudaSuccess) return ccl::cuda_fail(_e, what);     \
+    } while (0)
+
+// ======================================================================
+// device code
+// ======================================================================
+namespace ccl {
+
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(unsigned long long* p, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long gtimer()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait by one thread: returns false when the limit passes or
+// another threadblock has already failed.
+__device__ __forceinline__ bool wait_geq(const unsigned long long* p, unsigned long long v, const KParams& P,
+                                         int si, int reason, unsigned long long& waited)
+{
+    if (ld_acquire(p) >= v) return true;
+    unsigned long long t0 = gtimer();
+    unsigned spins = 0;
+    while (true) {
+        if (ld_acquire(p) >= v) break;
+        ++spins;
+        if ((spins & 15) == 0) {
+            if (*(volatile int*)P.status != 0) return false;
+            unsigned long long now = gtimer();
+            if (now - t0 > P.timeout_ns) {
+                if (atomicCAS(P.status, 0, (int)CCL_ERR_TIMEOUT) == 0) {
+                    P.status[1] = blockIdx.x;
+                    P.status[2] = si;
+                    P.status[3] = reason;
+                }
+                return false;
+            }
+        }
+        if (spins > 64) __nanosleep(64);
+    }
+    waited += gtimer() - t0;
+    return true;
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t add2(uint32_t a, uint32_t b);
+
+template <>
+__device__ __forceinline__ uint32_t add2<CCL_F32>(uint32_t a, uint32_t b)
+{
+    return __float_as_uint(__uint_as_float(a) + __uint_as_float(b));
+}
+template <>
+__device__ __forceinline__ uint32_t add2<CCL_I32>(uint32_t a, uint32_t b)
+{
+    return a + b;  // modulo 2^32
+}
+template <>
+__device__ __forceinline__ uint32_t add2<CCL_BF16>(uint32_t a, uint32_t b)
+{
+    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
+    __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
+    float2 fx = __bfloat1622float2(x), fy = __bfloat1622float2(y);
+    __nv_bfloat162 r = __floats2bfloat162_rn(fx.x + fy.x, fx.y + fy.y);
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+template <>
+__device__ __forceinline__ uint32_t add2<CCL_F16>(uint32_t a, uint32_t b)
+{
+    __half2 x = *reinterpret_cast<__half2*>(&a);
+    __half2 y = *reinterpret_cast<__half2*>(&b);
+    float2 fx = __half22float2(x), fy = __half22float2(y);
+    __half2 r = __floats2half2_rn(fx.x + fy.x, fx.y + fy.y);
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 vadd(uint4 a, uint4 b)
+{
+    return make_uint4(add2<DT>(a.x, b.x), add2<DT>(a.y, b.y), add2<DT>(a.z, b.z), add2<DT>(a.w, b.w));
+}
+
+__device__ __forceinline__ uint4 vload(const uint4* p, bool stream) { return stream ? __ldcs(p) : __ldcg(p); }
+__device__ __forceinline__ void vstore(uint4* p, uint4 v, bool stream)
+{
+    if (stream) __stcs(p, v); else __stcg(p, v);
+}
+
+// 16-byte path: nv vectors; full tiles keep U vectors per operand in flight
+// per thread, the remainder goes one vector per thread.
+template <bool RED, int DT>
+__device__ __forceinline__ void move_vec(const uint4* a, bool as, const uint4* b, bool bs, uint4* o1, bool o1s,
+                                         uint4* o2, int64_t nv)
+{
+    constexpr int U = 4;
+    const int T = blockDim.x;
+    int64_t i = threadIdx.x;
+    const int64_t full = nv - (int64_t)(U - 1) * T;
+    for (; i < full; i += (int64_t)U * T) {
+        uint4 va[U], vb[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            va[u] = vload(a + i + u * T, as);
+            if (RED) vb[u] = vload(b + i + u * T, bs);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            uint4 r = va[u];
+            if (RED) r = vadd<DT>(va[u], vb[u]);
+            vstore(o1 + i + u * T, r, o1s);
+            if (o2) vstore(o2 + i + u * T, r, false);
+        }
+    }
+    for (; i < nv; i += T) {
+        uint4 r = vload(a + i, as);
+        if (RED) r = vadd<DT>(r, vload(b + i, bs));
+        vstore(o1 + i, r, o1s);
+        if (o2) vstore(o2 + i, r, false);
+    }
+}
+
+// element path (unaligned operands or the tail of a piece)
+template <bool RED, int DT>
+__device__ void move_elem(const char* a, const char* b, char* o1, char* o2, int64_t lo, int64_t hi)
+{
+    constexpr int ES = (DT == CCL_BF16 || DT == CCL_F16) ? 2 : 4;
+    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+        if (ES == 4) {
+            uint32_t x = __ldcg(reinterpret_cast<const unsigned int*>(a) + i);
+            if (RED) x = add2<DT>(x, __ldcg(reinterpret_cast<const unsigned int*>(b) + i));
+            if (o1) __stcg(reinterpret_cast<unsigned int*>(o1) + i, x);
+            if (o2) __stcg(reinterpret_cast<unsigned int*>(o2) + i, x);
+        } else {
+            uint32_t x = __ldcg(reinterpret_cast<const unsigned short*>(a) + i);
+            if (RED) {
+                uint32_t y = __ldcg(reinterpret_cast<const unsigned short*>(b) + i);
+                x = add2<DT>(x, y) & 0xffffu;  // low half holds the element
+            }
+            if (o1) __stcg(reinterpret_cast<unsigned short*>(o1) + i, (unsigned short)x);
+            if (o2) __stcg(reinterpret_cast<unsigned short*>(o2) + i, (unsigned short)x);
+        }
+    }
+}
+
+template <bool RED, int DT>
+__device__ __forceinline__ void move(const char* a, bool as, const char* b, bool bs, char* o1, bool o1s, char* o2,
+                                     int64_t n)
+{
+    constexpr int ES = (DT == CCL_BF16 || DT == CCL_F16) ? 2 : 4;
+    constexpr int VE = 16 / ES;
+    uintptr_t al = (uintptr_t)a | (uintptr_t)o1 | (uintptr_t)o2 | (RED ? (uintptr_t)b : 0);
+    int64_t nv = 0;
+    if ((al & 15) == 0) {
+        nv = n / VE;
+        move_vec<RED, DT>(reinterpret_cast<const uint4*>(a), as, reinterpret_cast<const uint4*>(b), bs,
+                          reinterpret_cast<uint4*>(o1), o1s, reinterpret_cast<uint4*>(o2), nv);
+    }
+    if (nv * VE < n) move_elem<RED, DT>(a, b, o1, o2, nv * VE, n);
+}
+
+template <int DT>
+__device__ __forceinline__ void move_dt(bool red, const char* a, bool as, const char* b, bool bs, char* o1,
+                                        bool o1s, char* o2, int64_t n)
+{
+    if (red) move<true, DT>(a, as, b, bs, o1, o1s, o2, n);
+    else move<false, DT>(a, as, b, bs, o1, o1s, o2, n);
+}
+
+// Operands of one slot, prepared by thread 0 for the whole CTA.
+struct SlotOp {
+    const char* a;      // data in: incoming slot or source buffer
+    const char* b;      // local operand of a reduce
+    char* o1;           // destination buffer, or the outgoing slot
+    char* o2;           // outgoing slot when a destination is also written
+    long long n;        // elements
+    int red;            // reduce (1) or copy (0)
+    int dtype;
+    int as, bs, o1s;    // streaming cache hints per operand
+    int abort;
+    int nslots;
+};
+
+// State of the current step, kept in shared memory and used by thread 0
+// only, so that it does not occupy registers of the data-moving threads.
+struct LeadState {
+    DStep st;
+    DInstr in;
+    unsigned long long t_start, waited, base_in, base_out;
+    const DLink* Lin;
+    const DLink* Lout;
+    long long slot_elems;
+    int es;
+};
+
+__global__ void __launch_bounds__(1024, 1) ccl_exec_kernel(const __grid_constant__ KParams P)
+{
+    __shared__ SlotOp op;
+    __shared__ LeadState L;
+    const int b0 = P.tb_begin[blockIdx.x], b1 = P.tb_begin[blockIdx.x + 1];
+    const bool leader = threadIdx.x == 0;
+    DStep& st = L.st;
+    DInstr& in = L.in;
+    unsigned long long& t_start = L.t_start;
+    unsigned long long& waited = L.waited;
+    unsigned long long& base_in = L.base_in;
+    unsigned long long& base_out = L.base_out;
+    const DLink*& Lin = L.Lin;
+    const DLink*& Lout = L.Lout;
+    long long& slot_elems = L.slot_elems;
+    int& es = L.es;
+    for (int si = b0; si < b1; ++si) {
+        if (leader) {
+            t_start = gtimer();
+            waited = 0;
+            st = P.steps[si];
+            in = P.instrs[st.instr];
+            int ok = 1;
+            for (int k = 0; k < st.dep_count && ok; ++k) {
+                const DDep d = P.deps[st.dep_begin + k];
+                ok = wait_geq(P.counters + d.counter, (unsigned long long)(P.exec * P.m + d.value), P, si, WAIT_DEP,
+                              waited);
+            }
+            es = (in.dtype == CCL_BF16 || in.dtype == CCL_F16) ? 2 : 4;
+            Lin = in.link_in >= 0 ? P.links + in.link_in : nullptr;
+            Lout = in.link_out >= 0 ? P.links + in.link_out : nullptr;
+            base_in = Lin ? (unsigned long long)(P.exec * Lin->total) : 0;
+            base_out = Lout ? (unsigned long long)(P.exec * Lout->total) : 0;
+            slot_elems = (Lin || Lout) ? P.slot_bytes / es : (st.nelem > 0 ? st.nelem : 1);
+            op.nslots = st.nslots > 0 ? st.nslots : 1;
+            op.abort = !ok;
+            op.red = (in.kind == CCL_I_REDUCE || in.kind == CCL_I_RRC || in.kind == CCL_I_RRS || in.kind == CCL_I_RRCS);
+            op.dtype = in.dtype;
+        }
+        __syncthreads();
+        if (op.abort) return;
+        const int nslots = op.nslots;
+        for (int k = 0; k < nslots; ++k) {
+            if (leader) {
+                const long long e0 = (long long)k * slot_elems;
+                long long n = st.nelem - e0;
+                if (n > slot_elems) n = slot_elems;
+                if (n < 0) n = 0;
+                const unsigned long long sin = base_in + st.seq_in + k;
+                const unsigned long long sout = base_out + st.seq_out + k;
+                int ok = 1;
+                if (Lin) ok = wait_geq(P.flags + Lin->flag_base + (int)(sin % P.S), sin + 1, P, si, WAIT_FULL, waited);
+                if (ok && Lout && sout + 1 > (unsigned long long)P.S)
+                    ok = wait_geq(P.flags + Lout->flag_base + P.S + (int)(sout % P.S), sout + 1 - P.S, P, si,
+                                  WAIT_FREE, waited);
+                const long long eo = (st.elem_off + e0) * es;
+                const char* srcp = in.src_buf >= 0 ? P.bufs[in.src_buf][in.src_rank] + in.src_off * es + eo : nullptr;
+                const char* locp = in.loc_buf >= 0 ? P.bufs[in.loc_buf][in.loc_rank] + in.loc_off * es + eo : nullptr;
+                char* dstp = in.dst_buf >= 0 ? P.bufs[in.dst_buf][in.dst_rank] + in.dst_off * es + eo : nullptr;
+                char* slot_out = Lout ? P.fifo + Lout->slot_base + (long long)(sout % P.S) * P.slot_bytes : nullptr;
+                if (Lin && in.kind != CCL_I_REDUCE) {
+                    op.a = P.fifo + Lin->slot_base + (long long)(sin % P.S) * P.slot_bytes;
+                    op.as = 0;
+                } else {
+                    op.a = srcp;
+                    op.as = in.src_buf == CCL_BUF_IN;
+                }
+                op.b = locp;
+                op.bs = in.loc_buf == CCL_BUF_IN;
+                if (dstp) {
+                    op.o1 = dstp;
+                    op.o1s = in.dst_buf == CCL_BUF_OUT;
+                    op.o2 = slot_out;
+                } else {
+                    op.o1 = slot_out;
+                    op.o1s = 0;
+                    op.o2 = nullptr;
+                }
+                op.n = n;
+                op.abort = !ok;
+            }
+            __syncthreads();
+            if (op.abort) return;
+            {
+                const char* a = op.a;
+                const char* b = op.b;
+                char* o1 = op.o1;
+                char* o2 = op.o2;
+                const long long n = op.n;
+                const bool as = op.as, bs = op.bs, o1s = op.o1s, red = op.red;
+                if (n > 0) {
+                    switch (op.dtype) {
+                    case CCL_F32: move_dt<CCL_F32>(red, a, as, b, bs, o1, o1s, o2, n); break;
+                    case CCL_BF16: move_dt<CCL_BF16>(red, a, as, b, bs, o1, o1s, o2, n); break;
+                    case CCL_F16: move_dt<CCL_F16>(red, a, as, b, bs, o1, o1s, o2, n); break;
+                    default: move_dt<CCL_I32>(red, a, as, b, bs, o1, o1s, o2, n); break;
+                    }
+                }
+            }
+            __syncthreads();
+            if (leader) {
+                __threadfence();
+                if (!(st.flags & 1)) {
+                    const unsigned long long sin = base_in + st.seq_in + k;
+                    const unsigned long long sout = base_out + st.seq_out + k;
+                    if (Lin) st_release(P.flags + Lin->flag_base + P.S + (int)(sin % P.S), sin + 1);
+                    if (Lout) st_release(P.flags + Lout->flag_base + (int)(sout % P.S), sout + 1);
+                }
+            }
+        }
+        if (leader) {
+            if (st.signal >= 0) st_release(P.counters + st.signal, (unsigned long long)(P.exec * P.m + st.mb + 1));
+            if (P.timeline) {
+                unsigned long long* tl = P.timeline + 3ll * si;
+                tl[0] = t_start;
+                tl[1] = waited;
+                tl[2] = gtimer();
+            }
+        }
+    }
+}
+
+}  // namespace ccl
+
+// ======================================================================
+// host plan
+// ======================================================================
+struct ccl_plan {
+    ccl::PlanImage img;
+    int device = 0;
+    int nranks = 0;
+    char* d_blob = nullptr;
+    unsigned long long* d_flags = nullptr;    // links * 2S, then counters
+    char* d_fifo = nullptr;
+    int* d_status = nullptr;
+    unsigned long long* d_timeline = nullptr;
+    char* d_scratch[CCL_MAX_RANKS] = {};
+    size_t flags_count = 0;
+    long long exec = 0;
+    int64_t device_bytes = 0;
+    double compile_ms = 0;
+    ccl::KParams kp{};
+};
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+ccl_plan_opts_t merged_opts(const ccl_plan_opts_t* opts)
+{
+    ccl_plan_opts_t o;
+    ccl_plan_opts_default(&o);
+    o.nthreads = 512;
+    if (opts) {
+        if (opts->channels) o.channels = opts->channels;
+        if (opts->nthreads) o.nthreads = opts->nthreads;
+        if (opts->slot_bytes) o.slot_bytes = opts->slot_bytes;
+        if (opts->fifo_slots) o.fifo_slots = opts->fifo_slots;
+        o.microbatches = opts->microbatches;
+        o.scheduler = opts->scheduler;
+        o.tb_alloc = opts->tb_alloc;
+        o.mb_order = opts->mb_order;
+        if (opts->timeout_ms) o.timeout_ms = opts->timeout_ms;
+        o.instrument = opts->instrument;
+    }
+    return o;
+}
+
+void fill_stats(const ccl::PlanImage& img, ccl_plan_stats_t* st)
+{
+    std::memset(st, 0, sizeof(*st));
+    st->schedule_bytes = img.schedule_bytes;
+    st->min_bytes = img.min_bytes;
+    st->data_bytes_per_rank = img.data_bytes_per_rank;
+    st->busbw_factor = img.busbw_factor;
+    st->nthreadblocks = img.ntb;
+    st->nthreadblocks_connection = img.ntb_connection;
+    st->nsteps = (int32_t)img.steps.size();
+    st->ninstr = (int32_t)img.instrs.size();
+    st->nlinks = (int32_t)img.links.size();
+    st->nsubpipelines = img.nsubpipelines;
+    st->microbatches = img.m;
+    st->mb_order = img.mb_order;
+    st->channels = img.channels;
+    st->nthreads = img.nthreads;
+    st->fifo_slots = img.S;
+    st->slot_bytes = img.slot_bytes;
+    st->fifo_bytes = img.fifo_bytes;
+}
+
+void free_plan(ccl_plan* p)
+{
+    if (!p) return;
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(p->device);
+    cudaFree(p->d_blob);
+    cudaFree(p->d_flags);
+    cudaFree(p->d_fifo);
+    cudaFree(p->d_status);
+    cudaFree(p->d_timeline);
+    for (int r = 0; r < CCL_MAX_RANKS; ++r) cudaFree(p->d_scratch[r]);
+    cudaSetDevice(prev);
+    delete p;
+}
+
+ccl_status_t reset_flags(ccl_plan* p, cudaStream_t s)
+{
+    if (p->flags_count)
+        CUDA_TRY(cudaMemsetAsync(p->d_flags, 0, p->flags_count * sizeof(unsigned long long), s), "reset flags");
+    CUDA_TRY(cudaMemsetAsync(p->d_status, 0, 4 * sizeof(int), s), "reset status");
+    p->exec = 0;
+    return CCL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ccl_version(void) { return "ccl-gb300 0.1 (sm_103a)"; }
+
+const char* ccl_error_string(ccl_status_t s)
+{
+    switch (s) {
+    case CCL_OK: return "ok";
+    case CCL_ERR_INVALID_ARG: return "invalid argument";
+    case CCL_ERR_CYCLE: return "dependency cycle";
+    case CCL_ERR_DEADLOCK: return "deadlock";
+    case CCL_ERR_RACE: return "data race";
+    case CCL_ERR_UNSUPPORTED: return "unsupported";
+    case CCL_ERR_OOM: return "out of device memory";
+    case CCL_ERR_CUDA: return "CUDA error";
+    case CCL_ERR_TIMEOUT: return "device wait timed out";
+    case CCL_ERR_INTERNAL: return "internal error";
+    }
+    return "unknown status";
+}
+
+const char* ccl_last_error_detail(void) { return ccl::g_detail.c_str(); }
+
+void ccl_plan_opts_default(ccl_plan_opts_t* o)
+{
+    if (!o) return;
+    o->channels = 1;
+    o->nthreads = 0;  // 0: 512, halved until all threadblocks are co-resident
+    o->slot_bytes = 128 * 1024;
+    o->fifo_slots = 4;
+    o->microbatches = 0;
+    o->scheduler = CCL_SCHED_HPDS;
+    o->tb_alloc = CCL_TB_CONNECTION;
+    o->mb_order = CCL_MB_AUTO;
+    o->timeout_ms = 2000;
+    o->instrument = 0;
+}
+
+ccl_status_t ccl_schedule_compile(const ccl_op_t* ops, int32_t nops, int32_t nranks, const int32_t nchunks[3],
+                                  int32_t fuse, ccl_schedule_t* out)
+{
+    if (!out || !nchunks) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    auto* s = new ccl_schedule();
+    ccl_status_t st = ccl::compile_program(ops, nops, nranks, nchunks, fuse != 0, s);
+    if (st != CCL_OK) { delete s; return st; }
+    *out = s;
+    return CCL_OK;
+}
+
+ccl_status_t ccl_schedule_builtin(int32_t kind, int32_t nranks, int32_t group_size, uint32_t flags,
+                                  ccl_schedule_t* out)
+{
+    if (!out) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    std::vector<ccl_op_t> ops;
+    int32_t nch[3] = {0, 0, 0};
+    ccl_status_t st = ccl::builtin_program(kind, nranks, group_size, flags, &ops, nch);
+    if (st != CCL_OK) return st;
+    auto* s = new ccl_schedule();
+    st = ccl::compile_program(ops.data(), (int)ops.size(), nranks, nch, (flags & CCL_FLAG_NOFUSE) == 0, s);
+    if (st != CCL_OK) { delete s; return st; }
+    s->builtin = kind;
+    s->group_size = group_size;
+    *out = s;
+    return CCL_OK;
+}
+
+ccl_status_t ccl_schedule_info(ccl_schedule_t s, ccl_schedule_info_t* info)
+{
+    if (!s || !info) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    std::memset(info, 0, sizeof(*info));
+    info->nranks = s->nranks;
+    for (int b = 0; b < 3; ++b) info->nchunks[b] = s->nchunks[b];
+    info->nops = (int32_t)s->ops.size();
+    info->ninstr = (int32_t)s->instrs.size();
+    info->ntransfers = (int32_t)s->xfers.size();
+    int64_t bytes = 0;
+    for (const auto& I : s->instrs) {
+        info->kind_count[I.kind]++;
+        bytes += ccl::kind_bytes_factor(I.kind) * I.count;
+    }
+    info->bytes_per_chunk_elem_x_esize = bytes;
+    info->builtin = s->builtin;
+    info->group_size = s->group_size;
+    return CCL_OK;
+}
+
+ccl_status_t ccl_schedule_get_ops(ccl_schedule_t s, ccl_op_t* ops, int32_t cap, int32_t* n)
+{
+    if (!s || !n) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    *n = (int32_t)s->ops.size();
+    if (cap < *n || (*n && !ops)) return ccl::fail(CCL_ERR_INVALID_ARG, "capacity too small");
+    std::copy(s->ops.begin(), s->ops.end(), ops);
+    return CCL_OK;
+}
+
+ccl_status_t ccl_schedule_get_instrs(ccl_schedule_t s, ccl_instr_info_t* out, int32_t cap, int32_t* n)
+{
+    if (!s || !n) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    *n = (int32_t)s->instrs.size();
+    if (cap < *n || (*n && !out)) return ccl::fail(CCL_ERR_INVALID_ARG, "capacity too small");
+    for (int i = 0; i < *n; ++i) {
+        const ccl::Instr& I = s->instrs[i];
+        ccl_instr_info_t& o = out[i];
+        o.kind = I.kind;
+        o.rank = I.rank;
+        o.src_rank = I.src.rank; o.src_buf = I.src.buf; o.src_off = (int32_t)I.src.off;
+        o.loc_rank = I.loc.rank; o.loc_buf = I.loc.buf; o.loc_off = (int32_t)I.loc.off;
+        o.dst_rank = I.dst.rank; o.dst_buf = I.dst.buf; o.dst_off = (int32_t)I.dst.off;
+        o.count = (int32_t)I.count;
+        o.peer_in = I.xfer_in >= 0 ? s->xfers[I.xfer_in].src_rank : -1;
+        o.peer_out = I.xfer_out >= 0 ? s->xfers[I.xfer_out].dst_rank : -1;
+        o.xfer_in = I.xfer_in;
+        o.xfer_out = I.xfer_out;
+        o.position = I.position;
+    }
+    return CCL_OK;
+}
+
+void ccl_schedule_destroy(ccl_schedule_t s) { delete s; }
+
+ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtype, int32_t op,
+                             const ccl_plan_opts_t* opts, ccl_plan_t* out)
+{
+    auto t0 = std::chrono::steady_clock::now();
+    if (!s || !out) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    if (op != CCL_SUM) return ccl::fail(CCL_ERR_INVALID_ARG, "only CCL_SUM is supported");
+    ccl_plan_opts_t o = merged_opts(opts);
+    int ndev = 0;
+    CUDA_TRY(cudaGetDeviceCount(&ndev), "cudaGetDeviceCount");
+    if (ndev <= 0) return ccl::fail(CCL_ERR_CUDA, "no CUDA device");
+    auto* p = new ccl_plan();
+    ccl_status_t st = ccl::build_plan(*s, chunk_elems, dtype, o, &p->img);
+    if (st != CCL_OK) { delete p; return st; }
+    cudaGetDevice(&p->device);
+    p->nranks = s->nranks;
+    ccl::PlanImage& img = p->img;
+
+    // co-residency: every threadblock of the grid must be resident at once;
+    // with the thread count left to the library, halve it until they fit
+    int nsm = 0, per_sm = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, p->device);
+    while (true) {
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ccl::ccl_exec_kernel, img.nthreads, 0);
+        if (e != cudaSuccess) { delete p; return ccl::cuda_fail(e, "occupancy query"); }
+        if ((int64_t)per_sm * nsm >= img.ntb || (opts && opts->nthreads) || img.nthreads <= 64) break;
+        img.nthreads /= 2;
+    }
+    if ((int64_t)per_sm * nsm < img.ntb) {
+        std::string msg = "plan needs " + std::to_string(img.ntb) + " co-resident threadblocks of " +
+                          std::to_string(img.nthreads) + " threads; the device holds " + std::to_string(per_sm * nsm);
+        delete p;
+        return ccl::fail(CCL_ERR_UNSUPPORTED, msg);
+    }
+
+    // one blob for the read-only tables
+    size_t o_instr = 0;
+    size_t o_steps = align_up(o_instr + img.instrs.size() * sizeof(ccl::DInstr), 256);
+    size_t o_tb = align_up(o_steps + img.steps.size() * sizeof(ccl::DStep), 256);
+    size_t o_links = align_up(o_tb + img.tb_begin.size() * sizeof(int32_t), 256);
+    size_t o_deps = align_up(o_links + img.links.size() * sizeof(ccl::DLink), 256);
+    size_t blob = align_up(o_deps + std::max<size_t>(1, img.deps.size()) * sizeof(ccl::DDep), 256);
+    std::vector<char> h(blob, 0);
+    std::memcpy(h.data() + o_instr, img.instrs.data(), img.instrs.size() * sizeof(ccl::DInstr));
+    std::memcpy(h.data() + o_steps, img.steps.data(), img.steps.size() * sizeof(ccl::DStep));
+    std::memcpy(h.data() + o_tb, img.tb_begin.data(), img.tb_begin.size() * sizeof(int32_t));
+    std::memcpy(h.data() + o_links, img.links.data(), img.links.size() * sizeof(ccl::DLink));
+    if (!img.deps.empty()) std::memcpy(h.data() + o_deps, img.deps.data(), img.deps.size() * sizeof(ccl::DDep));
+
+#define PLAN_TRY(call, what)                                               \
+    do {                                                                   \
+        cudaError_t _e = (call);                                           \
+        if (_e != cudaSuccess) { free_plan(p); return ccl::cuda_fail(_e, what); } \
+    } while (0)
+
+    PLAN_TRY(cudaMalloc(&p->d_blob, blob), "allocate plan tables");
+    PLAN_TRY(cudaMemcpy(p->d_blob, h.data(), blob, cudaMemcpyHostToDevice), "upload plan tables");
+    p->flags_count = img.links.size() * 2 * img.S + (size_t)img.ncounters;
+    PLAN_TRY(cudaMalloc(&p->d_flags, std::max<size_t>(1, p->flags_count) * sizeof(unsigned long long)), "allocate flags");
+    PLAN_TRY(cudaMalloc(&p->d_status, 4 * sizeof(int)), "allocate status");
+    if (img.fifo_bytes) PLAN_TRY(cudaMalloc(&p->d_fifo, img.fifo_bytes), "allocate link FIFOs");
+    if (img.instrument) PLAN_TRY(cudaMalloc(&p->d_timeline, img.steps.size() * 3 * sizeof(unsigned long long)), "allocate timeline");
+    int64_t scratch_bytes = img.scratch_elems * img.esize;
+    int64_t dev_bytes = blob + p->flags_count * 8 + 16 + img.fifo_bytes;
+    for (int r = 0; r < s->nranks; ++r) {
+        if (img.scratch_used[r] && scratch_bytes > 0) {
+            PLAN_TRY(cudaMalloc(&p->d_scratch[r], scratch_bytes), "allocate scratch");
+            dev_bytes += scratch_bytes;
+        }
+    }
+    if (img.instrument) dev_bytes += img.steps.size() * 24;
+    p->device_bytes = dev_bytes;
+    if (reset_flags(p, 0) != CCL_OK) { free_plan(p); return CCL_ERR_CUDA; }
+    PLAN_TRY(cudaDeviceSynchronize(), "plan upload");
+#undef PLAN_TRY
+
+    ccl::KParams& k = p->kp;
+    k.instrs = reinterpret_cast<const ccl::DInstr*>(p->d_blob + o_instr);
+    k.steps = reinterpret_cast<const ccl::DStep*>(p->d_blob + o_steps);
+    k.tb_begin = reinterpret_cast<const int32_t*>(p->d_blob + o_tb);
+    k.links = reinterpret_cast<const ccl::DLink*>(p->d_blob + o_links);
+    k.deps = reinterpret_cast<const ccl::DDep*>(p->d_blob + o_deps);
+    k.flags = p->d_flags;
+    k.counters = p->d_flags + img.links.size() * 2 * img.S;
+    k.fifo = p->d_fifo;
+    k.status = p->d_status;
+    k.timeline = p->d_timeline;
+    k.m = img.m;
+    k.slot_bytes = img.slot_bytes;
+    k.timeout_ns = (unsigned long long)img.timeout_ms * 1000000ull;
+    k.S = img.S;
+    for (int r = 0; r < CCL_MAX_RANKS; ++r) k.bufs[2][r] = p->d_scratch[r];
+    p->compile_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+    *out = p;
+    return CCL_OK;
+}
+
+ccl_status_t ccl_execute(ccl_plan_t p, void* const* in_bufs, void* const* out_bufs, void* stream)
+{
+    if (!p || !in_bufs || !out_bufs) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    const int es = p->img.esize;
+    for (int r = 0; r < p->nranks; ++r) {
+        if ((p->img.in_elems && !in_bufs[r]) || (p->img.out_elems && !out_bufs[r]))
+            return ccl::fail(CCL_ERR_INVALID_ARG, "null buffer for rank " + std::to_string(r));
+        if (((uintptr_t)in_bufs[r] | (uintptr_t)out_bufs[r]) % es)
+            return ccl::fail(CCL_ERR_INVALID_ARG, "buffer of rank " + std::to_string(r) + " is not element aligned");
+    }
+    ccl::KParams k = p->kp;
+    for (int r = 0; r < p->nranks; ++r) {
+        k.bufs[0][r] = static_cast<char*>(in_bufs[r]);
+        k.bufs[1][r] = static_cast<char*>(out_bufs[r]);
+    }
+    k.exec = p->exec;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* args[] = {&k};
+    cudaError_t e = cudaLaunchCooperativeKernel((const void*)ccl::ccl_exec_kernel, dim3(p->img.ntb),
+                                                dim3(p->img.nthreads), args, 0, s);
+    if (e != cudaSuccess) return ccl::cuda_fail(e, "executor launch");
+    p->exec += 1;
+    return CCL_OK;
+}
+
+ccl_status_t ccl_execute_host(ccl_plan_t p, const void* const* host_in, void* const* host_out,
+                              void* const* dev_in, void* const* dev_out, void* stream)
+{
+    if (!p || !host_in || !host_out || !dev_in || !dev_out) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t ib = (size_t)p->img.in_elems * p->img.esize, ob = (size_t)p->img.out_elems * p->img.esize;
+    for (int r = 0; r < p->nranks; ++r)
+        CUDA_TRY(cudaMemcpyAsync(dev_in[r], host_in[r], ib, cudaMemcpyHostToDevice, s), "copy input to device");
+    ccl_status_t st = ccl_execute(p, dev_in, dev_out, stream);
+    if (st != CCL_OK) return st;
+    for (int r = 0; r < p->nranks; ++r)
+        CUDA_TRY(cudaMemcpyAsync(host_out[r], dev_out[r], ob, cudaMemcpyDeviceToHost, s), "copy output to host");
+    return CCL_OK;
+}
+
+ccl_status_t ccl_plan_status(ccl_plan_t p)
+{
+    if (!p) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    int hs[4] = {0, 0, 0, 0};
+    CUDA_TRY(cudaMemcpy(hs, p->d_status, sizeof(hs), cudaMemcpyDeviceToHost), "read status");
+    if (hs[0] == 0) return CCL_OK;
+    static const char* reasons[] = {"?", "dependency counter", "incoming slot", "free outgoing slot"};
+    std::string msg = "threadblock " + std::to_string(hs[1]) + " (rank " +
+                      std::to_string(hs[1] >= 0 && hs[1] < (int)p->img.tb_rank.size() ? p->img.tb_rank[hs[1]] : -1) +
+                      ") gave up waiting for " + reasons[(hs[3] >= 1 && hs[3] <= 3) ? hs[3] : 0] + " at step " +
+                      std::to_string(hs[2]);
+    ccl_status_t code = (ccl_status_t)hs[0];
+    if (reset_flags(p, 0) != CCL_OK) return CCL_ERR_CUDA;
+    CUDA_TRY(cudaDeviceSynchronize(), "reset after timeout");
+    return ccl::fail(code, msg);
+}
+
+ccl_status_t ccl_plan_stats(ccl_plan_t p, ccl_plan_stats_t* st)
+{
+    if (!p || !st) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    fill_stats(p->img, st);
+    st->device_bytes = p->device_bytes;
+    st->compile_ms = p->compile_ms;
+    return CCL_OK;
+}
+
+ccl_status_t ccl_plan_check(ccl_schedule_t s, int64_t chunk_elems, int32_t dtype, const ccl_plan_opts_t* opts,
+                            ccl_plan_stats_t* st)
+{
+    auto t0 = std::chrono::steady_clock::now();
+    if (!s) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    ccl::PlanImage img;
+    ccl_status_t r = ccl::build_plan(*s, chunk_elems, dtype, merged_opts(opts), &img);
+    if (r != CCL_OK) return r;
+    if (st) {
+        fill_stats(img, st);
+        st->compile_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+    }
+    return CCL_OK;
+}
+
+ccl_status_t ccl_schedule_timeline(ccl_schedule_t s, int32_t scheduler, int32_t* xfer_sp, int32_t* nsub)
+{
+    if (!s) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    if (scheduler != CCL_SCHED_RR && scheduler != CCL_SCHED_HPDS)
+        return ccl::fail(CCL_ERR_INVALID_ARG, "unknown scheduler");
+    ccl::Timeline tl;
+    ccl_status_t r = ccl::build_timeline(*s, scheduler, &tl);
+    if (r != CCL_OK) return r;
+    if (xfer_sp) std::copy(tl.xfer_sp.begin(), tl.xfer_sp.end(), xfer_sp);
+    if (nsub) *nsub = tl.nsp;
+    return CCL_OK;
+}
+
+ccl_status_t ccl_plan_timeline(ccl_plan_t p, double* idle, int32_t cap, double* mean_idle, double* max_idle,
+                               double* span_us)
+{
+    if (!p) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    if (!p->d_timeline) return ccl::fail(CCL_ERR_INVALID_ARG, "plan was created without instrumentation");
+    const ccl::PlanImage& img = p->img;
+    if (idle && cap < img.ntb) return ccl::fail(CCL_ERR_INVALID_ARG, "capacity too small");
+    CUDA_TRY(cudaDeviceSynchronize(), "synchronize");
+    std::vector<unsigned long long> t(img.steps.size() * 3);
+    CUDA_TRY(cudaMemcpy(t.data(), p->d_timeline, t.size() * 8, cudaMemcpyDeviceToHost), "read timeline");
+    unsigned long long lo = ~0ull, hi = 0;
+    for (size_t k = 0; k < img.steps.size(); ++k) {
+        lo = std::min(lo, t[3 * k]);
+        hi = std::max(hi, t[3 * k + 2]);
+    }
+    double span = hi > lo ? (double)(hi - lo) : 1.0;
+    double sum = 0, mx = 0;
+    for (int b = 0; b < img.ntb; ++b) {
+        double busy = 0;
+        for (int k = img.tb_begin[b]; k < img.tb_begin[b + 1]; ++k) {
+            double d = (double)(t[3 * k + 2] - t[3 * k]) - (double)t[3 * k + 1];
+            busy += std::max(0.0, d);
+        }
+        double id = std::min(1.0, std::max(0.0, 1.0 - busy / span));
+        if (idle) idle[b] = id;
+        sum += id;
+        mx = std::max(mx, id);
+    }
+    if (mean_idle) *mean_idle = img.ntb ? sum / img.ntb : 0;
+    if (max_idle) *max_idle = mx;
+    if (span_us) *span_us = span / 1000.0;
+    return CCL_OK;
+}
+
+ccl_status_t ccl_plan_debug_drop_signal(ccl_plan_t p, int32_t tb, int32_t step)
+{
+    if (!p) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    ccl::PlanImage& img = p->img;
+    if (tb < 0 || tb >= img.ntb) return ccl::fail(CCL_ERR_INVALID_ARG, "threadblock out of range");
+    int k = img.tb_begin[tb] + step;
+    if (step < 0 || k >= img.tb_begin[tb + 1]) return ccl::fail(CCL_ERR_INVALID_ARG, "step out of range");
+    img.steps[k].flags |= 1;
+    ccl::DStep* dst = const_cast<ccl::DStep*>(p->kp.steps) + k;
+    CUDA_TRY(cudaMemcpy(dst, &img.steps[k], sizeof(ccl::DStep), cudaMemcpyHostToDevice), "patch step");
+    return CCL_OK;
+}
+
+void ccl_plan_destroy(ccl_plan_t p) { free_plan(p); }
+
+}  // extern "C"

@@ -1,0 +1,193 @@
+// Tuner: subspace coordinate descent over the resource parameters.
+//
+// AutoCCL report, "research method" 1-2: implementation parameters (here:
+// the threadblock allocation policy) split the search space into small
+// subspaces; inside each, the resource parameters nChannel, nThread and
+// chunk size are optimised one coordinate at a time, raising a parameter
+// while bandwidth keeps improving (bandwidth is unimodal in each of them).
+// Grids: channels {1,2,4,8,12,16,24,32,48}, threads {128,256,512,1024},
+// slot size 16 KiB .. 4 MiB in powers of two.  A probe is the median of
+// `reps` CUDA-event-timed executions after one warm-up; a point whose plan
+// cannot be built (threadblocks not co-resident, FIFO too small) scores 0.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <map>
+#include <tuple>
+#include <vector>
+
+#include "ccl_internal.h"
+
+namespace ccl {
+namespace {
+
+struct Prober {
+    ccl_schedule_t s;
+    int64_t ce;
+    int32_t dtype;
+    void* const* in;
+    void* const* out;
+    cudaStream_t stream;
+    int reps;
+    int probes = 0;
+    std::map<std::tuple<int, int, int64_t, int>, double> cache;  // -> microseconds (0 = infeasible)
+
+    double time_us(const ccl_plan_opts_t& o)
+    {
+        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+        ++probes;
+        double us = 0;
+        ccl_plan_t p = nullptr;
+        if (ccl_plan_create(s, ce, dtype, CCL_SUM, &o, &p) == CCL_OK) {
+            cudaEvent_t a, b;
+            cudaEventCreate(&a);
+            cudaEventCreate(&b);
+            std::vector<float> t;
+            bool ok = ccl_execute(p, in, out, stream) == CCL_OK;
+            for (int k = 0; k < reps && ok; ++k) {
+                cudaEventRecord(a, stream);
+                ok = ccl_execute(p, in, out, stream) == CCL_OK;
+                cudaEventRecord(b, stream);
+                cudaEventSynchronize(b);
+                float ms = 0;
+                cudaEventElapsedTime(&ms, a, b);
+                t.push_back(ms);
+            }
+            cudaStreamSynchronize(stream);
+            if (ok && ccl_plan_status(p) == CCL_OK && !t.empty()) {
+                std::sort(t.begin(), t.end());
+                us = 1000.0 * t[t.size() / 2];
+            }
+            cudaEventDestroy(a);
+            cudaEventDestroy(b);
+            ccl_plan_destroy(p);
+        }
+        cache[key] = us;
+        return us;
+    }
+};
+
+const int kChannels[] = {1, 2, 4, 8, 12, 16, 24, 32, 48};
+const int kThreads[] = {128, 256, 512, 1024};
+
+std::vector<int64_t> slot_grid()
+{
+    std::vector<int64_t> v;
+    for (int64_t b = 16 * 1024; b <= 4 * 1024 * 1024; b *= 2) v.push_back(b);
+    return v;
+}
+
+template <typename T>
+int nearest(const std::vector<T>& g, T x)
+{
+    int best = 0;
+    for (int i = 0; i < (int)g.size(); ++i)
+        if (std::llabs((long long)g[i] - (long long)x) < std::llabs((long long)g[best] - (long long)x)) best = i;
+    return best;
+}
+
+}  // namespace
+}  // namespace ccl
+
+extern "C" ccl_status_t ccl_tune(ccl_schedule_t s, int64_t chunk_elems, int32_t dtype, void* const* in_bufs,
+                                 void* const* out_bufs, void* stream, const ccl_tune_opts_t* topts,
+                                 const ccl_plan_opts_t* start, ccl_plan_opts_t* best, ccl_tune_report_t* report)
+{
+    using namespace ccl;
+    if (!s || !in_bufs || !out_bufs || !best) return fail(CCL_ERR_INVALID_ARG, "null argument");
+    ccl_tune_opts_t to{3, 5, 0.01};
+    if (topts) {
+        if (topts->max_rounds > 0) to.max_rounds = topts->max_rounds;
+        if (topts->reps > 0) to.reps = topts->reps;
+        if (topts->min_gain > 0) to.min_gain = topts->min_gain;
+    }
+    ccl_plan_opts_t base;
+    ccl_plan_opts_default(&base);
+    if (start) {
+        ccl_plan_opts_t z = *start;
+        if (z.channels) base.channels = z.channels;
+        if (z.nthreads) base.nthreads = z.nthreads;
+        if (z.slot_bytes) base.slot_bytes = z.slot_bytes;
+        if (z.fifo_slots) base.fifo_slots = z.fifo_slots;
+        base.microbatches = z.microbatches;
+        base.scheduler = z.scheduler;
+        base.tb_alloc = z.tb_alloc;
+        base.mb_order = z.mb_order;
+    }
+    Prober P{s, chunk_elems, dtype, in_bufs, out_bufs, static_cast<cudaStream_t>(stream), to.reps};
+    std::vector<int> gc(std::begin(kChannels), std::end(kChannels));
+    std::vector<int> gt(std::begin(kThreads), std::end(kThreads));
+    std::vector<int64_t> gs = slot_grid();
+
+    double default_us = P.time_us(base);
+    ccl_plan_opts_t overall = base;
+    double overall_us = default_us > 0 ? default_us : 1e30;
+
+    for (int alloc : {CCL_TB_CONNECTION, CCL_TB_PACKED}) {
+        ccl_plan_opts_t cur = base;
+        cur.tb_alloc = alloc;
+        int ic = nearest(gc, cur.channels), it = nearest(gt, cur.nthreads), is = nearest(gs, cur.slot_bytes);
+        auto eval = [&](int c, int t, int sl) {
+            ccl_plan_opts_t o = cur;
+            o.channels = gc[c];
+            o.nthreads = gt[t];
+            o.slot_bytes = gs[sl];
+            double us = P.time_us(o);
+            return us > 0 ? 1.0 / us : 0.0;  // bandwidth up to a constant
+        };
+        double bw = eval(ic, it, is);
+        for (int round = 0; round < to.max_rounds; ++round) {
+            bool moved = false;
+            for (int coord = 0; coord < 3; ++coord) {
+                int* idx = coord == 0 ? &ic : coord == 1 ? &it : &is;
+                int n = coord == 0 ? (int)gc.size() : coord == 1 ? (int)gt.size() : (int)gs.size();
+                auto at = [&](int v) {
+                    return coord == 0 ? eval(v, it, is) : coord == 1 ? eval(ic, v, is) : eval(ic, it, v);
+                };
+                // raise while bandwidth improves; if the first raise does not
+                // help, try lowering the same way
+                for (int dir : {+1, -1}) {
+                    bool any = false;
+                    while (*idx + dir >= 0 && *idx + dir < n) {
+                        double nb = at(*idx + dir);
+                        if (nb > bw * (1.0 + to.min_gain)) {
+                            *idx += dir;
+                            bw = nb;
+                            any = moved = true;
+                        } else {
+                            break;
+                        }
+                    }
+                    if (any) break;
+                }
+            }
+            if (!moved) break;
+        }
+        if (bw > 0 && 1.0 / bw < overall_us) {
+            overall_us = 1.0 / bw;
+            overall = cur;
+            overall.channels = gc[ic];
+            overall.nthreads = gt[it];
+            overall.slot_bytes = gs[is];
+        }
+    }
+    *best = overall;
+    if (report) {
+        std::memset(report, 0, sizeof(*report));
+        report->probes = P.probes;
+        report->best_us = overall_us < 1e29 ? overall_us : 0;
+        report->default_us = default_us;
+        ccl_plan_t p = nullptr;
+        if (ccl_plan_create(s, chunk_elems, dtype, CCL_SUM, &overall, &p) == CCL_OK) {
+            ccl_plan_stats_t st;
+            ccl_plan_stats(p, &st);
+            if (report->best_us > 0) report->best_gbs = st.schedule_bytes / (report->best_us * 1e3);
+            ccl_plan_destroy(p);
+        }
+    }
+    if (overall_us >= 1e29) return fail(CCL_ERR_UNSUPPORTED, "no configuration could run");
+    return CCL_OK;
+}

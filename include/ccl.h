@@ -1,0 +1,351 @@
+/*
+ * ccl.h -- C ABI of the GB300 chunk-schedule collective executor.
+ *
+ * One GPU holds R *virtual ranks*.  Each rank owns an input, an output and a
+ * scratch buffer in HBM; a "link" between two ranks is a FIFO of slots in HBM
+ * with per-slot flags, so a transfer is a device-memory copy and no byte
+ * leaves the GPU.  A collective is a chunk program (a list of copy / reduce
+ * operations on chunk ranges of those buffers) that the host compiles into
+ * per-threadblock instruction lists run by one persistent CUDA kernel.
+ *
+ * Sources of the model (cited by page title and section):
+ *   - MSCCLang report (ASPLOS '23), §III.1 "system design": chunk-oriented
+ *     programs over input/output/scratch buffers with copy and reduce; the
+ *     compiler traces dependencies into a DAG, lowers cross-rank operations
+ *     to send/recv/reduce instructions, fuses adjacent ones into
+ *     recv-reduce-copy-send style instructions, and spreads them over
+ *     channels and threadblocks by a parallelization factor; a runtime
+ *     executes the instruction lists with pipelining.
+ *   - ReSCCL report (SIGCOMM '25), §II.1-II.2: task-level execution across
+ *     micro-batches, hierarchical-priority dynamic scheduling (HPDS) into
+ *     sub-pipelines, state-based threadblock allocation.
+ *   - AutoCCL report (NSDI '25), "research method" 1-2: resource parameters
+ *     nChannel / nThread / chunk size tuned by subspace coordinate descent.
+ *
+ * Conventions for every function:
+ *   - Return CCL_OK or an error code; on error, ccl_last_error_detail()
+ *     returns a human-readable reason (thread-local, valid until the next
+ *     call on the same thread).  Output handles are left untouched on error.
+ *   - Device pointers are CUDA device addresses on the current device.  A
+ *     "stream" argument is a cudaStream_t passed as void* (NULL = legacy
+ *     default stream).
+ *   - Handles (ccl_schedule_t, ccl_plan_t) are owned by the library and freed
+ *     by their *_destroy function; nothing returned by the library must be
+ *     freed by the caller.
+ *   - Nothing here falls back to the CPU: an entry point that needs the GPU
+ *     returns CCL_ERR_CUDA when no device or no sm_103 image is usable.
+ */
+#ifndef CCL_SCHEDULE_H
+#define CCL_SCHEDULE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CCL_MAX_RANKS 64
+
+typedef enum {
+    CCL_OK = 0,
+    CCL_ERR_INVALID_ARG = 1, /* bad argument, out-of-range op, misaligned or overlapping buffers */
+    CCL_ERR_CYCLE = 2,       /* dependency cycle among compiled instructions */
+    CCL_ERR_DEADLOCK = 3,    /* threadblock programs cannot all finish with the given FIFO capacity */
+    CCL_ERR_RACE = 4,        /* two unordered accesses to one buffer range, one of them a write */
+    CCL_ERR_UNSUPPORTED = 5, /* valid request the executor cannot run (e.g. threadblocks not co-resident) */
+    CCL_ERR_OOM = 6,         /* device allocation failed */
+    CCL_ERR_CUDA = 7,        /* a CUDA runtime call failed (no device, launch failure, ...) */
+    CCL_ERR_TIMEOUT = 8,     /* a device flag wait ran out of time (reported by ccl_plan_status) */
+    CCL_ERR_INTERNAL = 9
+} ccl_status_t;
+
+typedef enum { CCL_F32 = 0, CCL_BF16 = 1, CCL_F16 = 2, CCL_I32 = 3 } ccl_dtype_t;
+typedef enum { CCL_SUM = 0 } ccl_redop_t;
+typedef enum { CCL_BUF_IN = 0, CCL_BUF_OUT = 1, CCL_BUF_SCRATCH = 2 } ccl_buf_t;
+typedef enum { CCL_OP_COPY = 0, CCL_OP_REDUCE = 1 } ccl_opcode_t;
+
+/*
+ * One chunk operation (MSCCLang report, §III.1): copy  dst := src, or
+ * reduce  dst := dst (+) src.  Offsets and counts are in chunks of the
+ * buffer kind named by *_buf (ccl_buf_t).  Layout: 8 consecutive int32.
+ * Source and destination of one operation must not overlap.
+ */
+typedef struct {
+    int32_t op;       /* ccl_opcode_t */
+    int32_t src_rank, src_buf, src_off;
+    int32_t dst_rank, dst_buf, dst_off;
+    int32_t count;    /* chunks, > 0 */
+} ccl_op_t;
+
+typedef struct ccl_schedule* ccl_schedule_t;
+typedef struct ccl_plan* ccl_plan_t;
+
+/* Built-in collective programs (ccl_schedule_builtin kinds). */
+typedef enum {
+    CCL_RING_ALLREDUCE = 0,     /* out[r] = sum_k in[k]; R chunks per buffer */
+    CCL_RING_ALLGATHER = 1,     /* out[r] = concat_s in[s]; in 1 chunk, out R chunks */
+    CCL_RING_REDUCESCATTER = 2, /* out[r] = chunk r of sum_k in[k]; in R chunks, out 1 chunk */
+    CCL_HIER_ALLREDUCE = 3,     /* R = G*ng; intra RS, inter ring AR per slice, intra AG */
+    CCL_ALLTOALL_2PHASE = 4,    /* out[d] block s = in[s] block d; R = G*ng */
+    CCL_ALLTONEXT = 5           /* out[r+1] = in[r]; cross-group pairs relayed in G parts */
+} ccl_builtin_t;
+
+#define CCL_FLAG_WRAP 1u    /* AllToNext: also send rank R-1 -> rank 0 */
+#define CCL_FLAG_NOFUSE 2u  /* compile without instruction fusion */
+
+/* Fused instruction kinds produced by the compiler (MSCCLang report,
+ * §III.1 "instruction generation" and "instruction fusion"). */
+typedef enum {
+    CCL_I_COPY = 0,      /* dst <- src (one rank) */
+    CCL_I_REDUCE = 1,    /* dst <- local (+) src (one rank) */
+    CCL_I_SEND = 2,      /* slot_out <- src */
+    CCL_I_RECV = 3,      /* dst <- slot_in */
+    CCL_I_RRC = 4,       /* dst <- local (+) slot_in           (recv-reduce-copy) */
+    CCL_I_RCS = 5,       /* dst <- slot_in; slot_out <- slot_in (recv-copy-send) */
+    CCL_I_FWD = 6,       /* slot_out <- slot_in                 (recv-send, relay) */
+    CCL_I_RRS = 7,       /* slot_out <- local (+) slot_in       (recv-reduce-send) */
+    CCL_I_RRCS = 8,      /* t <- local (+) slot_in; dst <- t; slot_out <- t */
+    CCL_I_COPY_SEND = 9, /* dst <- src; slot_out <- src */
+    CCL_I_NKINDS = 10
+} ccl_instr_kind_t;
+
+typedef struct {
+    int32_t nranks;
+    int32_t nchunks[3];          /* chunks per rank of in / out / scratch */
+    int32_t nops;                /* operations in the source program */
+    int32_t ninstr;              /* fused instructions (all ranks) */
+    int32_t ntransfers;          /* cross-rank transfers */
+    int32_t kind_count[CCL_I_NKINDS];
+    int64_t bytes_per_chunk_elem_x_esize; /* schedule bytes = this * chunk_elems * esize */
+    int32_t builtin;             /* ccl_builtin_t, or -1 for a compiled program */
+    int32_t group_size;
+} ccl_schedule_info_t;
+
+/* Per fused instruction, for inspection and tests.  Ranges are in chunks;
+ * an absent operand has rank -1. */
+typedef struct {
+    int32_t kind;                /* ccl_instr_kind_t */
+    int32_t rank;
+    int32_t src_rank, src_buf, src_off;
+    int32_t loc_rank, loc_buf, loc_off;
+    int32_t dst_rank, dst_buf, dst_off;
+    int32_t count;
+    int32_t peer_in;             /* sending rank of the received transfer, or -1 */
+    int32_t peer_out;            /* receiving rank of the sent transfer, or -1 */
+    int32_t xfer_in, xfer_out;   /* transfer ids, or -1 */
+    int32_t position;            /* program position */
+} ccl_instr_info_t;
+
+/*
+ * Compile a chunk program.  ops[0..nops) in program order; dependencies
+ * are traced from program order (read-after-write, write-after-read and
+ * write-after-write on overlapping ranges of the same rank's buffer), so the
+ * traced DAG is acyclic by construction.  fuse = 1 applies copy propagation,
+ * dead-store elimination and recv/send fusion; fuse = 0 keeps one
+ * instruction per half operation.
+ * Errors: CCL_ERR_INVALID_ARG (rank/buffer/range out of bounds, count <= 0,
+ * overlapping source and destination, nranks outside 1..CCL_MAX_RANKS).
+ */
+ccl_status_t ccl_schedule_compile(const ccl_op_t* ops, int32_t nops, int32_t nranks,
+                                  const int32_t nchunks[3], int32_t fuse, ccl_schedule_t* out);
+
+/*
+ * Generate and compile a built-in program.  group_size (G) is used by the
+ * hierarchical, AllToAll and AllToNext kinds (nranks must be a multiple of
+ * G); the ring kinds ignore it.  flags: CCL_FLAG_WRAP, CCL_FLAG_NOFUSE.
+ */
+ccl_status_t ccl_schedule_builtin(int32_t kind, int32_t nranks, int32_t group_size,
+                                  uint32_t flags, ccl_schedule_t* out);
+
+ccl_status_t ccl_schedule_info(ccl_schedule_t s, ccl_schedule_info_t* info);
+
+/* Copy the source program (ops) or the fused instructions into caller
+ * arrays of capacity cap; *n receives the full count (CCL_ERR_INVALID_ARG if
+ * cap is too small, after setting *n). */
+ccl_status_t ccl_schedule_get_ops(ccl_schedule_t s, ccl_op_t* ops, int32_t cap, int32_t* n);
+ccl_status_t ccl_schedule_get_instrs(ccl_schedule_t s, ccl_instr_info_t* out, int32_t cap,
+                                     int32_t* n);
+
+void ccl_schedule_destroy(ccl_schedule_t s);
+
+/* Scheduling policies for ccl_plan_opts_t. */
+typedef enum { CCL_SCHED_RR = 0, CCL_SCHED_HPDS = 1 } ccl_scheduler_t;
+typedef enum { CCL_TB_CONNECTION = 0, CCL_TB_PACKED = 1 } ccl_tb_alloc_t;
+typedef enum { CCL_MB_AUTO = 0, CCL_MB_ALGO = 1, CCL_MB_TASK = 2, CCL_MB_SEGMENT = 3 } ccl_mb_order_t;
+
+/*
+ * Execution parameters of a plan (zero fields take the defaults written by
+ * ccl_plan_opts_default).
+ *   channels    : parallelization factor; every chunk range is split into
+ *                 `channels` contiguous 16-byte-granular pieces, each with its
+ *                 own links and threadblocks (MSCCLang report, §III.1, §IV.1).
+ *   nthreads    : threads per threadblock (64..1024, multiple of 32); 0 =
+ *                 512, halved until every threadblock can be co-resident.
+ *   slot_bytes  : FIFO slot size (multiple of 16).
+ *   fifo_slots  : slots per link FIFO (>= 2).
+ *   microbatches: pieces every channel range is cut into; 0 = the smallest
+ *                 count that keeps a piece within half of a FIFO.
+ *   scheduler   : CCL_SCHED_RR (program-order list scheduling) or
+ *                 CCL_SCHED_HPDS (ReSCCL report, §II.2).
+ *   tb_alloc    : CCL_TB_CONNECTION (one threadblock per (in-link, out-link)
+ *                 connection) or CCL_TB_PACKED (connections never active in
+ *                 the same sub-pipeline share a threadblock).
+ *   mb_order    : order of micro-batches inside a threadblock program:
+ *                 ALGO = micro-batch outermost; TASK = each instruction runs
+ *                 all micro-batches before the next (task-level execution);
+ *                 SEGMENT = task-level between idle gaps of the threadblock,
+ *                 micro-batch-major inside; AUTO = SEGMENT, falling back to
+ *                 ALGO when SEGMENT cannot finish.
+ *   timeout_ms  : limit of every device flag wait.
+ *   instrument  : 1 = record per-step global-timer stamps (ccl_plan_timeline).
+ */
+typedef struct {
+    int32_t channels;
+    int32_t nthreads;
+    int64_t slot_bytes;
+    int32_t fifo_slots;
+    int32_t microbatches;
+    int32_t scheduler;
+    int32_t tb_alloc;
+    int32_t mb_order;
+    int32_t timeout_ms;
+    int32_t instrument;
+} ccl_plan_opts_t;
+
+void ccl_plan_opts_default(ccl_plan_opts_t* o);
+
+/*
+ * Build an executable plan for `chunk_elems` elements per chunk.  Rank r's
+ * input buffer then holds nchunks[0] * chunk_elems elements, its output
+ * nchunks[1] * chunk_elems.  Allocates (library-owned, on the current
+ * device): link FIFOs and flags, scratch for ranks whose scratch is touched,
+ * and the instruction tables.  Validates the threadblock programs by
+ * simulating them (CCL_ERR_DEADLOCK) and checks that all threadblocks can be
+ * co-resident (CCL_ERR_UNSUPPORTED).  dtype: ccl_dtype_t; op: CCL_SUM.
+ */
+ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtype, int32_t op,
+                             const ccl_plan_opts_t* opts, ccl_plan_t* out);
+
+/*
+ * Run the plan on `stream` (asynchronous).  in_bufs[r] / out_bufs[r] are
+ * device pointers to rank r's input / output (16-byte alignment gives the
+ * vector path; any element-aligned pointer is accepted).  An input may equal
+ * its rank's output only if the program never reads that rank's input after
+ * writing its output; other overlaps between buffers are the caller's
+ * responsibility.  Launch errors return CCL_ERR_CUDA; a device timeout is
+ * reported later by ccl_plan_status.  A plan must not run concurrently with
+ * itself (one stream at a time).
+ */
+ccl_status_t ccl_execute(ccl_plan_t p, void* const* in_bufs, void* const* out_bufs, void* stream);
+
+/*
+ * End-to-end form: copy host_in[r] (host memory; pinned gives asynchronous
+ * copies) to dev_in[r], run the plan, copy dev_out[r] back to host_out[r],
+ * all on `stream`.  The caller synchronizes the stream before reading
+ * host_out.
+ */
+ccl_status_t ccl_execute_host(ccl_plan_t p, const void* const* host_in, void* const* host_out,
+                              void* const* dev_in, void* const* dev_out, void* stream);
+
+/*
+ * Status of the last execution, to call after synchronizing its stream:
+ * CCL_OK, or CCL_ERR_TIMEOUT when a flag wait ran out (the detail names the
+ * threadblock and step).  After a timeout the plan's flags are reset so the
+ * plan can run again.
+ */
+ccl_status_t ccl_plan_status(ccl_plan_t p);
+
+typedef struct {
+    int64_t schedule_bytes;      /* bytes read + written by all fused instructions per execution */
+    int64_t min_bytes;           /* inputs read once + outputs written once */
+    int64_t data_bytes_per_rank; /* message size used for algBW (per builtin kind) */
+    double busbw_factor;         /* nccl-tests convention: algBW -> busBW */
+    int32_t nthreadblocks;       /* threadblocks in the launch */
+    int32_t nthreadblocks_connection; /* count under one-threadblock-per-connection */
+    int32_t nsteps;              /* (instruction, micro-batch) steps over all threadblocks */
+    int32_t ninstr;              /* channel instructions */
+    int32_t nlinks;              /* link FIFOs */
+    int32_t nsubpipelines;       /* sub-pipelines of the scheduler's timeline */
+    int32_t microbatches;
+    int32_t mb_order;            /* order actually used */
+    int32_t channels, nthreads, fifo_slots;
+    int64_t slot_bytes;
+    int64_t fifo_bytes;          /* device bytes of all link FIFOs */
+    int64_t device_bytes;        /* all device memory owned by the plan */
+    double compile_ms;           /* host time of ccl_plan_create */
+} ccl_plan_stats_t;
+
+ccl_status_t ccl_plan_stats(ccl_plan_t p, ccl_plan_stats_t* st);
+
+/*
+ * Run the planner and its deadlock simulation on the host only (no device
+ * memory, no GPU needed) and report what ccl_plan_create would build.
+ * Returns the same validation errors as ccl_plan_create except the
+ * co-residency check (CCL_ERR_UNSUPPORTED), which needs the device.
+ */
+ccl_status_t ccl_plan_check(ccl_schedule_t s, int64_t chunk_elems, int32_t dtype,
+                            const ccl_plan_opts_t* opts, ccl_plan_stats_t* st);
+
+/*
+ * Sub-pipeline timeline of a schedule (ReSCCL report, §II.2): xfer_sp[x]
+ * receives the sub-pipeline of transfer x (array of ccl_schedule_info_t
+ * .ntransfers entries, may be NULL) and *nsub the number of sub-pipelines.
+ * scheduler: CCL_SCHED_RR or CCL_SCHED_HPDS.
+ */
+ccl_status_t ccl_schedule_timeline(ccl_schedule_t s, int32_t scheduler, int32_t* xfer_sp, int32_t* nsub);
+
+/*
+ * Threadblock utilisation of the last execution of an instrumented plan
+ * (ReSCCL report, §III: mean and maximum threadblock idle rate).  For each
+ * threadblock b: busy[b] = time spent moving data, span = first start to
+ * last end over all threadblocks; idle[b] = 1 - busy[b] / span.  Arrays of
+ * capacity cap (>= nthreadblocks).  Synchronizes the device.
+ */
+ccl_status_t ccl_plan_timeline(ccl_plan_t p, double* idle, int32_t cap, double* mean_idle,
+                               double* max_idle, double* span_us);
+
+/*
+ * Test hook: make threadblock `tb` skip the flag post of its step `step`
+ * (the data is still written), so a peer's wait runs out.  Used to check
+ * that a lost signal ends in CCL_ERR_TIMEOUT with a usable device.
+ */
+ccl_status_t ccl_plan_debug_drop_signal(ccl_plan_t p, int32_t tb, int32_t step);
+
+void ccl_plan_destroy(ccl_plan_t p);
+
+/* Tuner (AutoCCL report, "research method" 2: subspace coordinate descent
+ * over nChannel, nThread, chunk size, raising each while bandwidth
+ * improves). */
+typedef struct {
+    int32_t max_rounds;          /* coordinate sweeps (default 3) */
+    int32_t reps;                /* timed executions per probe; the median is used (default 5) */
+    double min_gain;             /* relative improvement to keep moving (default 0.01) */
+} ccl_tune_opts_t;
+
+typedef struct {
+    int32_t probes;              /* configurations timed */
+    double best_us;              /* median time of the chosen configuration */
+    double best_gbs;             /* schedule bytes / best_us */
+    double default_us;           /* median time of the default configuration */
+} ccl_tune_report_t;
+
+/*
+ * Tune channels, threads and slot size for one schedule and size by timing
+ * executions on the caller's buffers (their contents are overwritten).
+ * `start` (nullable) is the first point; `best` receives the result.
+ */
+ccl_status_t ccl_tune(ccl_schedule_t s, int64_t chunk_elems, int32_t dtype,
+                      void* const* in_bufs, void* const* out_bufs, void* stream,
+                      const ccl_tune_opts_t* topts, const ccl_plan_opts_t* start,
+                      ccl_plan_opts_t* best, ccl_tune_report_t* report);
+
+const char* ccl_error_string(ccl_status_t s);
+const char* ccl_last_error_detail(void);
+const char* ccl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCL_SCHEDULE_H */

@@ -1,0 +1,44 @@
+"""The C ABI library loads and exports every function include/ccl.h declares
+(no GPU needed: nothing here launches work)."""
+import ctypes
+import os
+import re
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_\s\*]*?\b(ccl_[A-Za-z0-9_]+)\s*\(", text, re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("ccl_schedule_compile", "ccl_schedule_builtin", "ccl_plan_create", "ccl_execute",
+                 "ccl_execute_host", "ccl_plan_status", "ccl_plan_stats", "ccl_tune", "ccl_plan_destroy",
+                 "ccl_schedule_destroy", "ccl_error_string", "ccl_last_error_detail"):
+        assert must in names, must
+
+
+def test_library_exports_every_declared_symbol():
+    import collective_communication_schedule_gb300 as ccl
+    lib = ctypes.CDLL(ccl.LIB_PATH)
+    missing = [n for n in sorted(declared_functions()) if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_host_only_calls_work_without_a_gpu():
+    import collective_communication_schedule_gb300 as ccl
+    assert "sm_103a" in ccl.version()
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 8)
+    assert s.info().nranks == 8
+    st = s.check(1024, ccl.F32, channels=2)
+    assert st.nthreadblocks == 16
+    assert ccl.lib.ccl_error_string(3) == b"deadlock"

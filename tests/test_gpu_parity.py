@@ -1,0 +1,114 @@
+"""GPU executor vs the oracle, bit for bit (fixed reduction order).
+
+Sizes span several slots, channels and micro-batches, with ragged element
+counts (unaligned chunk starts, element tails) as well as the aligned
+workload shapes.  Every expected value comes from ``oracle``.
+"""
+import numpy as np
+import pytest
+
+from gpu_helpers import assert_bitexact, run_case
+
+pytestmark = pytest.mark.gpu
+
+F32, BF16, F16, I32 = 0, 1, 2, 3
+DIST = {F32: "normal", BF16: "normal", F16: "uniform", I32: "int"}
+
+
+@pytest.fixture(scope="module")
+def ccl():
+    import collective_communication_schedule_gb300 as m
+    return m
+
+
+# (kind, R, G)
+BUILTINS = [(0, 8, 0), (1, 8, 0), (2, 8, 0), (3, 16, 8), (4, 32, 8), (5, 24, 8),
+            (0, 3, 0), (2, 5, 0), (3, 4, 2), (4, 4, 2), (5, 6, 3)]
+
+
+@pytest.mark.parametrize("kind,R,G", BUILTINS)
+@pytest.mark.parametrize("dtype", [F32, BF16, F16, I32])
+def test_builtin_small_bitexact(ccl, kind, R, G, dtype):
+    got, want, _ = run_case(ccl, kind, R, G, 1000, dtype, DIST[dtype], 7)
+    assert_bitexact(got, want)
+
+
+@pytest.mark.parametrize("ce", [1, 7, 33, 4093])
+@pytest.mark.parametrize("dtype", [BF16, F32])
+def test_ragged_sizes(ccl, ce, dtype):
+    """Chunk sizes that leave element tails and unaligned chunk starts."""
+    for kind, R, G in [(0, 8, 0), (3, 4, 2), (5, 6, 3)]:
+        got, want, _ = run_case(ccl, kind, R, G, ce, dtype, DIST[dtype], 11, channels=2)
+        assert_bitexact(got, want)
+
+
+@pytest.mark.parametrize("channels", [1, 2, 3, 4])
+@pytest.mark.parametrize("mb", [0, 1, 5])
+def test_channels_and_microbatches_do_not_change_bits(ccl, channels, mb):
+    # many slots per piece: 64 KiB chunks, 16 KiB slots
+    got, want, plan = run_case(ccl, 0, 8, 0, 16384, BF16, "normal", 1, channels=channels, microbatches=mb,
+                               slot_bytes=16384, fifo_slots=4)
+    assert_bitexact(got, want)
+    assert plan.stats().channels == channels
+
+
+@pytest.mark.parametrize("sched", [0, 1])
+@pytest.mark.parametrize("alloc", [0, 1])
+@pytest.mark.parametrize("order", [0, 1, 3])
+def test_scheduler_allocation_order(ccl, sched, alloc, order):
+    for kind, R, G in [(3, 16, 8), (4, 8, 4), (5, 12, 4)]:
+        got, want, _ = run_case(ccl, kind, R, G, 2048, F32, "normal", 2, scheduler=sched, tb_alloc=alloc,
+                                mb_order=order, microbatches=4, slot_bytes=4096)
+        assert_bitexact(got, want)
+
+
+def test_unfused_equals_fused(ccl):
+    for kind, R, G in [(0, 8, 0), (2, 8, 0), (3, 16, 8), (5, 24, 8)]:
+        got, want, _ = run_case(ccl, kind, R, G, 512, BF16, "normal", 3, fuse=False)
+        assert_bitexact(got, want)
+
+
+def test_config0_ring_allreduce_fp32_and_int32(ccl):
+    """R = 8, 262144 elements per rank (8 chunks of 32768), seed 0."""
+    got, want, _ = run_case(ccl, 0, 8, 0, 32768, F32, "uniform", 0)
+    assert_bitexact(got, want)
+    got, want, _ = run_case(ccl, 0, 8, 0, 32768, I32, "int", 0)
+    assert_bitexact(got, want)
+
+
+@pytest.mark.parametrize("kbytes", [32, 64, 128, 256, 512, 1024, 2048, 3072])
+@pytest.mark.parametrize("channels", [1, 4])
+def test_config1_allgather_reducescatter_sweep(ccl, kbytes, channels):
+    R = 8
+    ce = kbytes * 1024 // 2 // R          # bf16 elements per chunk
+    for kind in (1, 2):
+        got, want, _ = run_case(ccl, kind, R, 0, ce, BF16, "normal", 1, channels=channels)
+        assert_bitexact(got, want)
+
+
+def test_alltonext_wrap_and_untouched_rank0(ccl):
+    got, want, _ = run_case(ccl, 5, 12, 4, 300, F32, "normal", 4, wrap=True)
+    assert_bitexact(got, want)
+    got, want, _ = run_case(ccl, 5, 12, 4, 300, F32, "normal", 4, wrap=False)
+    assert_bitexact(got, want)
+    assert np.all(np.ascontiguousarray(got[0]).view(np.uint8) == 0xA5)
+
+
+def test_repeated_executions_reuse_flags(ccl):
+    """Sequence numbers continue across executions without a reset."""
+    import torch
+    import datagen
+    import oracle
+    from gpu_helpers import oracle_program, to_device, empty_outputs, to_host
+    s = ccl.Schedule.builtin(0, 8, 0)
+    plan = ccl.Plan(s, 4096, BF16, slot_bytes=2048, fifo_slots=3, channels=2)
+    ops, nch = oracle_program(0, 8)
+    for it in range(5):
+        ins = datagen.rank_inputs(100 + it, "normal", 8, 8 * 4096, BF16)
+        d_in = to_device(ins, BF16)
+        d_out = empty_outputs(8, 8 * 4096, BF16)
+        plan.execute(d_in, d_out)
+        torch.cuda.synchronize()
+        plan.status()
+        want, _, _ = oracle.run(ops, 8, nch, 4096, BF16, ins)
+        assert_bitexact(to_host(d_out, BF16), want)
