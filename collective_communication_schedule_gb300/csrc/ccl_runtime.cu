@@ -688,6 +688,7 @@ ccl_status_t ccl_execute(ccl_plan_t p, void* const* in_bufs, void* const* out_bu
     }
     k.exec = p->exec;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->img.ntb == 0) return CCL_OK;  // empty program: nothing to move
     void* args[] = {&k};
     cudaError_t e = cudaLaunchCooperativeKernel((const void*)ccl::ccl_exec_kernel, dim3(p->img.ntb),
                                                 dim3(p->img.nthreads), args, 0, s);
