@@ -39,7 +39,7 @@ MiB = 1 << 20
 # name, kind, R, G, dtype, bytes per chunk, dist, seed, plan options
 SUITE = [
     ("hier_ar", 3, 16, 8, 0, 4 * MiB, "normal", 2, dict(channels=8, microbatches=16)),
-    ("a2a", 4, 32, 8, 2, 1 * MiB, "uniform", 3, dict(channels=2)),
+    ("a2a", 4, 32, 8, 2, 1 * MiB, "uniform", 3, dict(channels=2, slot_bytes=32768)),
     ("ring_bf16", 0, 8, 0, 1, 32 * MiB, "normal", 4, dict(channels=24)),
     ("ring_f32", 0, 8, 0, 0, 32 * MiB, "normal", 4, dict(channels=24)),
     ("a2n", 5, 24, 8, 0, 16 * MiB, "normal", 4, dict(channels=2)),

@@ -15,17 +15,20 @@
 //     connection).  PACKED (state-based): connection threadblocks of a rank
 //     whose sets of active sub-pipelines are disjoint are merged.
 //  3. Program order inside a threadblock: by sub-pipeline, then program
-//     position.  Micro-batch order: ALGO (micro-batch outermost), TASK (an
-//     instruction runs all its micro-batches before the next: task-level
-//     execution) or SEGMENT (task-level across idle gaps of the threadblock,
-//     micro-batch-major between them).  A dependency on a partly overlapping
-//     range inside the current segment always starts a new segment.
+//     position.  The program is cut into segments, each run micro-batch-major
+//     (for every micro-batch, every instruction of the segment) -- the
+//     pipelining of MSCCLang's runtime -- and the segments one after the
+//     other, which is ReSCCL's task-level execution.  ALGO cuts only where the
+//     epoch changes (a whole-instruction dependency lies between), SEGMENT also
+//     at idle gaps of the threadblock's timeline, TASK before every
+//     instruction.
 //  4. Geometry.  Every instruction range is split into `channels` pieces and
 //     every channel piece into `m` micro-batch pieces, both in 16-byte units
 //     (the element tail goes to the last piece); a piece moves through the
 //     link FIFO in slots of `slot_bytes`.
-//  5. Link sequence numbers are assigned in the sending threadblock's order;
-//     a receiver waits for the sequence number of the piece it needs, so the
+//  5. A link FIFO joins one sending threadblock to one receiving threadblock
+//     (one per connection and channel).  Sequence numbers follow the sender's
+//     order; a receiver waits for the number of the piece it needs, so the
 //     flags are per slot and no piece is read out of turn.
 //  6. Dependencies between instructions in different threadblocks become
 //     counter waits (per micro-batch when the ranges are identical, on the
@@ -34,6 +37,8 @@
 //     cannot finish is rejected.
 #include <algorithm>
 #include <chrono>
+#include <cstdio>
+#include <cstdlib>
 #include <map>
 #include <set>
 #include <string>
@@ -249,33 +254,49 @@ void pack_state_based(const ccl_schedule& s, const Timeline& tl, TBList* tbs, st
     }
 }
 
+// Epoch of every instruction: the largest number of whole-instruction
+// dependencies (partly overlapping ranges) on a path into it, following
+// same-rank dependencies and transfers.  Such a dependency needs every
+// micro-batch of its producer, so a micro-batch-major segment never spans two
+// epochs; because the epoch is a property of the instruction, both ends of a
+// link agree on where their segments break.
+std::vector<int> epochs(const ccl_schedule& s)
+{
+    const int ni = (int)s.instrs.size();
+    std::vector<std::vector<std::pair<int, int>>> out(ni);   // (to, weight)
+    std::vector<int> indeg(ni, 0), ep(ni, 0);
+    for (const Dep& d : s.deps) { out[d.from].push_back({d.to, d.exact ? 0 : 1}); ++indeg[d.to]; }
+    for (const Xfer& x : s.xfers) { out[x.send_instr].push_back({x.recv_instr, 0}); ++indeg[x.recv_instr]; }
+    std::vector<int> q;
+    for (int i = 0; i < ni; ++i)
+        if (!indeg[i]) q.push_back(i);
+    for (size_t h = 0; h < q.size(); ++h) {
+        int i = q[h];
+        for (auto& e : out[i]) {
+            ep[e.first] = std::max(ep[e.first], ep[i] + e.second);
+            if (--indeg[e.first] == 0) q.push_back(e.first);
+        }
+    }
+    return ep;
+}
+
 // segments of one threadblock program
-std::vector<std::vector<int>> make_segments(const ccl_schedule& s, const Timeline& tl,
-                                            const std::vector<int>& prog, int order,
-                                            const std::vector<std::vector<std::pair<int, bool>>>& ideps)
+std::vector<std::vector<int>> make_segments(const Timeline& tl, const std::vector<int>& prog, int order,
+                                            const std::vector<int>& ep)
 {
     std::vector<std::vector<int>> segs;
-    std::set<int> cur;
-    int cur_hi = -1;
-    for (int idx = 0; idx < (int)prog.size(); ++idx) {
-        int i = prog[idx];
-        bool cut = false;
-        if (!segs.empty()) {
-            if (order == CCL_MB_TASK) cut = true;
-            if (order == CCL_MB_SEGMENT && tl.sp_lo[i] > cur_hi + 1) cut = true;
-            for (auto& d : ideps[i])
-                if (!d.second && cur.count(d.first)) cut = true;
-        }
-        if (segs.empty() || cut) {
+    int cur_hi = -1, cur_ep = -1;
+    for (int i : prog) {
+        bool cut = segs.empty() || ep[i] != cur_ep || order == CCL_MB_TASK ||
+                   (order == CCL_MB_SEGMENT && tl.sp_lo[i] > cur_hi + 1);
+        if (cut) {
             segs.push_back({});
-            cur.clear();
             cur_hi = -1;
+            cur_ep = ep[i];
         }
         segs.back().push_back(i);
-        cur.insert(i);
         cur_hi = std::max(cur_hi, tl.sp_hi[i]);
     }
-    (void)s;
     return segs;
 }
 
@@ -295,8 +316,7 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     const int64_t slot_elems = o.slot_bytes / es;
     const int nT = (int)tbs.size();
 
-    std::vector<std::vector<std::pair<int, bool>>> ideps(ni);
-    for (const Dep& d : s.deps) ideps[d.to].push_back({d.from, d.exact});
+    const std::vector<int> ep = epochs(s);
 
     img->instrs.assign((size_t)ni * p, DInstr{});
     img->steps.clear();
@@ -318,10 +338,19 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     img->instrument = o.instrument;
     for (int r = 0; r < CCL_MAX_RANKS; ++r) img->scratch_used[r] = false;
 
-    // links
-    std::map<std::tuple<int, int, int>, int> link_id;
-    auto get_link = [&](int a, int b, int ch) {
-        auto key = std::make_tuple(a, b, ch);
+    // threadblock of every channel instruction: device threadblock
+    // ch * nT + t runs channel ch of rank-level threadblock t
+    const int ntb = nT * p;
+    std::vector<int> dev_tb_of((size_t)ni * p, -1);
+    for (int t = 0; t < nT; ++t)
+        for (int i : tbs[t])
+            for (int ch = 0; ch < p; ++ch) dev_tb_of[(size_t)i * p + ch] = ch * nT + t;
+
+    // one FIFO per (sending threadblock, receiving threadblock): every link
+    // has a single producer and a single consumer
+    std::map<std::pair<int, int>, int> link_id;
+    auto get_link = [&](int a, int b, int ch, int stb, int rtb) {
+        auto key = std::make_pair(stb, rtb);
         auto it = link_id.find(key);
         if (it != link_id.end()) return it->second;
         int id = (int)img->links.size();
@@ -345,8 +374,20 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
             DInstr& D = img->instrs[(size_t)i * p + ch];
             D.kind = I.kind;
             D.dtype = dtype;
-            D.link_in = I.xfer_in >= 0 ? get_link(s.xfers[I.xfer_in].src_rank, I.rank, ch) : -1;
-            D.link_out = I.xfer_out >= 0 ? get_link(I.rank, s.xfers[I.xfer_out].dst_rank, ch) : -1;
+            if (I.xfer_in >= 0) {
+                const Xfer& X = s.xfers[I.xfer_in];
+                D.link_in = get_link(X.src_rank, I.rank, ch, dev_tb_of[(size_t)X.send_instr * p + ch],
+                                     dev_tb_of[(size_t)i * p + ch]);
+            } else {
+                D.link_in = -1;
+            }
+            if (I.xfer_out >= 0) {
+                const Xfer& X = s.xfers[I.xfer_out];
+                D.link_out = get_link(I.rank, X.dst_rank, ch, dev_tb_of[(size_t)i * p + ch],
+                                      dev_tb_of[(size_t)X.recv_instr * p + ch]);
+            } else {
+                D.link_out = -1;
+            }
             D.src_rank = I.src.rank; D.src_buf = I.src.valid() ? I.src.buf : -1;
             D.loc_rank = I.loc.rank; D.loc_buf = I.loc.valid() ? I.loc.buf : -1;
             D.dst_rank = I.dst.rank; D.dst_buf = I.dst.valid() ? I.dst.buf : -1;
@@ -362,21 +403,17 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     img->schedule_bytes = sched_bytes;
 
     // threadblock programs -> steps
-    const int ntb = nT * p;
     img->ntb = ntb;
-    std::vector<int> dev_tb_of((size_t)ni * p, -1);
     std::vector<std::vector<int>> step_of((size_t)ni * p, std::vector<int>(m, -1));
     for (int ch = 0; ch < p; ++ch) {
         for (int t = 0; t < nT; ++t) {
-            int dtb = ch * nT + t;
             img->tb_begin.push_back((int)img->steps.size());
             img->tb_rank.push_back(tb_rank[t]);
-            auto segs = make_segments(s, tl, tbs[t], order, ideps);
+            auto segs = make_segments(tl, tbs[t], order, ep);
             for (auto& seg : segs) {
                 for (int mb = 0; mb < m; ++mb) {
                     for (int i : seg) {
                         int ci = i * p + ch;
-                        dev_tb_of[ci] = dtb;
                         const DInstr& D = img->instrs[ci];
                         Piece pc = split(D.nelem, ve, m, mb);
                         DStep st{};
@@ -552,6 +589,30 @@ bool simulate_plan(const PlanImage& img, std::string* why)
             }
         }
         if (!progress) {
+            if (std::getenv("CCL_LOG_LEVEL") && std::atoi(std::getenv("CCL_LOG_LEVEL")) >= 2) {
+                for (int t = 0; t < ntb; ++t) {
+                    if (si[t] == img.tb_begin[t + 1]) continue;
+                    const DStep& st = img.steps[si[t]];
+                    const DInstr& D = img.instrs[st.instr];
+                    std::fprintf(stderr, "[ccl] stuck tb %d step %d instr %d kind %d mb %d slot %d/%d deps_ok %d",
+                                 t, si[t] - img.tb_begin[t], st.instr, D.kind, st.mb, slot[t], st.nslots, deps_ok[t]);
+                    if (!deps_ok[t])
+                        for (int k = 0; k < st.dep_count; ++k) {
+                            const DDep& d = img.deps[st.dep_begin + k];
+                            if (counters[d.counter] < d.value)
+                                std::fprintf(stderr, " dep(c%d>=%lld have %lld)", d.counter, (long long)d.value,
+                                             (long long)counters[d.counter]);
+                        }
+                    if (D.link_in >= 0)
+                        std::fprintf(stderr, " in(L%d seq %lld full %lld)", D.link_in, (long long)(st.seq_in + slot[t]),
+                                     (long long)flags[img.links[D.link_in].flag_base + (st.seq_in + slot[t]) % S]);
+                    if (D.link_out >= 0)
+                        std::fprintf(stderr, " out(L%d seq %lld consumed %lld)", D.link_out,
+                                     (long long)(st.seq_out + slot[t]),
+                                     (long long)flags[img.links[D.link_out].flag_base + S + (st.seq_out + slot[t]) % S]);
+                    std::fprintf(stderr, "\n");
+                }
+            }
             if (why) {
                 for (int t = 0; t < ntb; ++t) {
                     if (si[t] == img.tb_begin[t + 1]) continue;
@@ -569,6 +630,33 @@ bool simulate_plan(const PlanImage& img, std::string* why)
     }
     return true;
 }
+
+namespace {
+
+int log_level()
+{
+    const char* v = std::getenv("CCL_LOG_LEVEL");
+    return v ? std::atoi(v) : 0;
+}
+
+void dump_programs(const ccl_schedule& s, const Timeline& tl, const TBList& tbs, const std::vector<int>& tr, int m,
+                   int order)
+{
+    static const char* kn[] = {"copy", "reduce", "send", "recv", "rrc", "rcs", "fwd", "rrs", "rrcs", "copy_send"};
+    std::fprintf(stderr, "[ccl] m=%d order=%d threadblocks=%zu sub-pipelines=%d\n", m, order, tbs.size(), tl.nsp);
+    for (size_t t = 0; t < tbs.size(); ++t) {
+        std::fprintf(stderr, "[ccl] tb %zu rank %d:", t, tr[t]);
+        for (int i : tbs[t]) {
+            const Instr& I = s.instrs[i];
+            int pin = I.xfer_in >= 0 ? s.xfers[I.xfer_in].src_rank : -1;
+            int pout = I.xfer_out >= 0 ? s.xfers[I.xfer_out].dst_rank : -1;
+            std::fprintf(stderr, " %s(i%d %d>%d sp%d-%d)", kn[I.kind], i, pin, pout, tl.sp_lo[i], tl.sp_hi[i]);
+        }
+        std::fprintf(stderr, "\n");
+    }
+}
+
+}  // namespace
 
 ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const ccl_plan_opts_t& o,
                         PlanImage* img)
@@ -609,10 +697,12 @@ ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const 
     int64_t half = std::max(1, o.fifo_slots / 2);
     int m_small = (int)std::min<int64_t>(4096, (max_slots + half - 1) / half);
     std::vector<int> ms;
+    // small pieces first: instructions sharing a threadblock then interleave
+    // piece by piece instead of running one after the other
     if (o.microbatches > 0) ms.push_back(o.microbatches);
-    else { ms.push_back(1); if (m_small > 1) ms.push_back(m_small); }
+    else { ms.push_back(m_small); if (m_small > 1) ms.push_back(1); }
     std::vector<int> orders;
-    if (o.mb_order == CCL_MB_AUTO) orders = {CCL_MB_SEGMENT, CCL_MB_ALGO};
+    if (o.mb_order == CCL_MB_AUTO) orders = {CCL_MB_ALGO, CCL_MB_SEGMENT, CCL_MB_TASK};
     else orders = {o.mb_order};
     std::vector<int> allocs;
     if (o.tb_alloc == CCL_TB_PACKED) allocs = {CCL_TB_PACKED, CCL_TB_CONNECTION};
@@ -628,6 +718,7 @@ ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const 
                 st = build_image(s, tl, tbs, tr, ce, dtype, o, m, order, &cand);
                 if (st != CCL_OK) return st;
                 std::string why;
+                if (log_level() >= 2) dump_programs(s, tl, tbs, tr, m, order);
                 if (simulate_plan(cand, &why)) {
                     *img = std::move(cand);
                     img->ntb_connection = (int)conn.size() * o.channels;

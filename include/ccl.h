@@ -191,12 +191,16 @@ typedef enum { CCL_MB_AUTO = 0, CCL_MB_ALGO = 1, CCL_MB_TASK = 2, CCL_MB_SEGMENT
  *   tb_alloc    : CCL_TB_CONNECTION (one threadblock per (in-link, out-link)
  *                 connection) or CCL_TB_PACKED (connections never active in
  *                 the same sub-pipeline share a threadblock).
- *   mb_order    : order of micro-batches inside a threadblock program:
- *                 ALGO = micro-batch outermost; TASK = each instruction runs
- *                 all micro-batches before the next (task-level execution);
- *                 SEGMENT = task-level between idle gaps of the threadblock,
- *                 micro-batch-major inside; AUTO = SEGMENT, falling back to
- *                 ALGO when SEGMENT cannot finish.
+ *   mb_order    : order of micro-batches inside a threadblock program.  A
+ *                 program is cut into segments run one after the other; a
+ *                 segment runs micro-batch-major (each micro-batch through all
+ *                 of its instructions).  ALGO cuts only where a dependency on
+ *                 a partly overlapping range needs all micro-batches of its
+ *                 producer; SEGMENT also cuts at idle gaps of the
+ *                 threadblock's sub-pipeline timeline; TASK cuts before every
+ *                 instruction (each runs all its micro-batches first:
+ *                 task-level execution); AUTO tries ALGO, SEGMENT, TASK in
+ *                 that order and keeps the first that can finish.
  *   timeout_ms  : limit of every device flag wait.
  *   instrument  : 1 = record per-step global-timer stamps (ccl_plan_timeline).
  */
