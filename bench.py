@@ -113,10 +113,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def build_suite(ccl, torch, datagen, with_host=False):
+def selected_suite(args):
+    """The suite, or a subset (--only) at reduced chunk size (--scale) for
+    profiling captures."""
+    out = []
+    only = set(args.only.split(",")) if getattr(args, "only", None) else None
+    for row in SUITE:
+        if only and row[0] not in only:
+            continue
+        name, kind, R, G, dt, chunk_bytes, dist, seed, opts = row
+        scale = getattr(args, "scale", 1.0) or 1.0
+        cb = max(16, int(chunk_bytes * scale) // 16 * 16)
+        out.append((name, kind, R, G, dt, cb, dist, seed, opts))
+    return out
+
+
+def build_suite(ccl, torch, datagen, args, with_host=False):
     import numpy as np
     items = []
-    for name, kind, R, G, dt, chunk_bytes, dist, seed, opts in SUITE:
+    for name, kind, R, G, dt, chunk_bytes, dist, seed, opts in selected_suite(args):
         ce = chunk_bytes // ESIZE[dt]
         sched = ccl.Schedule.builtin(kind, R, G)
         plan = ccl.Plan(sched, ce, dt, **opts)
@@ -145,7 +160,7 @@ def run_gpu(args):
     import datagen
 
     peak, peak_kind = peaks()
-    items = build_suite(ccl, torch, datagen, with_host=True)
+    items = build_suite(ccl, torch, datagen, args, with_host=True)
     stream = torch.cuda.current_stream()
     # warm-up
     for _ in range(args.warmup):
@@ -236,7 +251,8 @@ def run_gpu(args):
                                "8x256MiB bf16 & f32 (24 ch) + AllToNext 24x128MiB f32 + AG/RS 8x3MiB bf16 + "
                                "ring AR 8x1MiB f32",
                    "parallelism": "R virtual ranks on one GPU", "l2": "step working set ~19 GiB > L2 (no flush)",
-                   "schedule_bytes_per_step": sched_bytes},
+                   "schedule_bytes_per_step": sched_bytes,
+                   **({"subset": args.only, "scale": args.scale} if (args.only or args.scale != 1.0) else {})},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 3), "traffic": None,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -321,7 +337,7 @@ def run_reference(args):
         return None
     import collective_communication_schedule_gb300 as ccl  # only for byte counts via host planning
     items = []
-    for name, kind, R, G, dt, chunk_bytes, dist, seed, opts in SUITE:
+    for name, kind, R, G, dt, chunk_bytes, dist, seed, opts in selected_suite(args):
         ce = chunk_bytes // ESIZE[dt]
         sch = ccl.Schedule.builtin(kind, R, G)
         st = sch.check(ce, dt, **opts)
@@ -347,6 +363,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="", help="comma-separated subset of the suite (profiling)")
+    ap.add_argument("--scale", type=float, default=1.0, help="chunk size factor (profiling)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
