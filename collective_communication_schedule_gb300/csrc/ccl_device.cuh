@@ -1,0 +1,185 @@
+// Device helpers shared by the executor kernels: gpu-scope flag access,
+// bounded waits, and the 16-byte vector copy / reduce bodies.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "ccl_executor.cuh"
+
+namespace ccl {
+
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(unsigned long long* p, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long gtimer()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait by one thread: returns false when the limit passes or
+// another threadblock has already failed (status[0] != 0).  On timeout the
+// first failing threadblock records (code, block, step, reason) in status.
+__device__ __forceinline__ bool wait_geq(const unsigned long long* p, unsigned long long v, int* status,
+                                         unsigned long long timeout_ns, int si, int reason,
+                                         unsigned long long& waited)
+{
+    if (ld_acquire(p) >= v) return true;
+    unsigned long long t0 = gtimer();
+    unsigned spins = 0;
+    while (true) {
+        if (ld_acquire(p) >= v) break;
+        ++spins;
+        if ((spins & 15) == 0) {
+            if (*(volatile int*)status != 0) return false;
+            unsigned long long now = gtimer();
+            if (now - t0 > timeout_ns) {
+                if (atomicCAS(status, 0, (int)CCL_ERR_TIMEOUT) == 0) {
+                    status[1] = blockIdx.x;
+                    status[2] = si;
+                    status[3] = reason;
+                }
+                return false;
+            }
+        }
+        if (spins > 64) __nanosleep(64);
+    }
+    waited += gtimer() - t0;
+    return true;
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t add2(uint32_t a, uint32_t b);
+
+template <>
+__device__ __forceinline__ uint32_t add2<CCL_F32>(uint32_t a, uint32_t b)
+{
+    return __float_as_uint(__uint_as_float(a) + __uint_as_float(b));
+}
+template <>
+__device__ __forceinline__ uint32_t add2<CCL_I32>(uint32_t a, uint32_t b)
+{
+    return a + b;  // modulo 2^32
+}
+template <>
+__device__ __forceinline__ uint32_t add2<CCL_BF16>(uint32_t a, uint32_t b)
+{
+    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
+    __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
+    float2 fx = __bfloat1622float2(x), fy = __bfloat1622float2(y);
+    __nv_bfloat162 r = __floats2bfloat162_rn(fx.x + fy.x, fx.y + fy.y);
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+template <>
+__device__ __forceinline__ uint32_t add2<CCL_F16>(uint32_t a, uint32_t b)
+{
+    __half2 x = *reinterpret_cast<__half2*>(&a);
+    __half2 y = *reinterpret_cast<__half2*>(&b);
+    float2 fx = __half22float2(x), fy = __half22float2(y);
+    __half2 r = __floats2half2_rn(fx.x + fy.x, fx.y + fy.y);
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 vadd(uint4 a, uint4 b)
+{
+    return make_uint4(add2<DT>(a.x, b.x), add2<DT>(a.y, b.y), add2<DT>(a.z, b.z), add2<DT>(a.w, b.w));
+}
+
+__device__ __forceinline__ uint4 vload(const uint4* p, bool stream) { return stream ? __ldcs(p) : __ldcg(p); }
+__device__ __forceinline__ void vstore(uint4* p, uint4 v, bool stream)
+{
+    if (stream) __stcs(p, v); else __stcg(p, v);
+}
+
+// 16-byte path: nv vectors; full tiles keep U vectors per operand in flight
+// per thread, the remainder goes one vector per thread.
+template <bool RED, int DT>
+__device__ __forceinline__ void move_vec(const uint4* a, bool as, const uint4* b, bool bs, uint4* o1, bool o1s,
+                                         uint4* o2, int64_t nv)
+{
+    constexpr int U = 4;
+    const int T = blockDim.x;
+    int64_t i = threadIdx.x;
+    const int64_t full = nv - (int64_t)(U - 1) * T;
+    for (; i < full; i += (int64_t)U * T) {
+        uint4 va[U], vb[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            va[u] = vload(a + i + u * T, as);
+            if (RED) vb[u] = vload(b + i + u * T, bs);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            uint4 r = va[u];
+            if (RED) r = vadd<DT>(va[u], vb[u]);
+            vstore(o1 + i + u * T, r, o1s);
+            if (o2) vstore(o2 + i + u * T, r, false);
+        }
+    }
+    for (; i < nv; i += T) {
+        uint4 r = vload(a + i, as);
+        if (RED) r = vadd<DT>(r, vload(b + i, bs));
+        vstore(o1 + i, r, o1s);
+        if (o2) vstore(o2 + i, r, false);
+    }
+}
+
+// element path (unaligned operands or the tail of a piece)
+template <bool RED, int DT>
+__device__ void move_elem(const char* a, const char* b, char* o1, char* o2, int64_t lo, int64_t hi)
+{
+    constexpr int ES = (DT == CCL_BF16 || DT == CCL_F16) ? 2 : 4;
+    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+        if (ES == 4) {
+            uint32_t x = __ldcg(reinterpret_cast<const unsigned int*>(a) + i);
+            if (RED) x = add2<DT>(x, __ldcg(reinterpret_cast<const unsigned int*>(b) + i));
+            if (o1) __stcg(reinterpret_cast<unsigned int*>(o1) + i, x);
+            if (o2) __stcg(reinterpret_cast<unsigned int*>(o2) + i, x);
+        } else {
+            uint32_t x = __ldcg(reinterpret_cast<const unsigned short*>(a) + i);
+            if (RED) {
+                uint32_t y = __ldcg(reinterpret_cast<const unsigned short*>(b) + i);
+                x = add2<DT>(x, y) & 0xffffu;  // low half holds the element
+            }
+            if (o1) __stcg(reinterpret_cast<unsigned short*>(o1) + i, (unsigned short)x);
+            if (o2) __stcg(reinterpret_cast<unsigned short*>(o2) + i, (unsigned short)x);
+        }
+    }
+}
+
+template <bool RED, int DT>
+__device__ __forceinline__ void move(const char* a, bool as, const char* b, bool bs, char* o1, bool o1s, char* o2,
+                                     int64_t n)
+{
+    constexpr int ES = (DT == CCL_BF16 || DT == CCL_F16) ? 2 : 4;
+    constexpr int VE = 16 / ES;
+    uintptr_t al = (uintptr_t)a | (uintptr_t)o1 | (uintptr_t)o2 | (RED ? (uintptr_t)b : 0);
+    int64_t nv = 0;
+    if ((al & 15) == 0) {
+        nv = n / VE;
+        move_vec<RED, DT>(reinterpret_cast<const uint4*>(a), as, reinterpret_cast<const uint4*>(b), bs,
+                          reinterpret_cast<uint4*>(o1), o1s, reinterpret_cast<uint4*>(o2), nv);
+    }
+    if (nv * VE < n) move_elem<RED, DT>(a, b, o1, o2, nv * VE, n);
+}
+
+template <int DT>
+__device__ __forceinline__ void move_dt(bool red, const char* a, bool as, const char* b, bool bs, char* o1,
+                                        bool o1s, char* o2, int64_t n)
+{
+    if (red) move<true, DT>(a, as, b, bs, o1, o1s, o2, n);
+    else move<false, DT>(a, as, b, bs, o1, o1s, o2, n);
+}
+
+}  // namespace ccl
