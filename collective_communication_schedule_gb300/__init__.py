@@ -112,6 +112,7 @@ def _load():
         "ccl_plan_debug_drop_signal": [P, I32_, I32_],
         "ccl_plan_check": [P, I64_, I32_, ctypes.POINTER(PlanOpts), ctypes.POINTER(PlanStats)],
         "ccl_schedule_timeline": [P, I32_, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
+        "ccl_allreduce_ring_noalloc": [ctypes.POINTER(P), ctypes.POINTER(P), I32_, I64_, I32_, I32_, P],
         "ccl_tune": [P, I64_, I32_, ctypes.POINTER(P), ctypes.POINTER(P), P, ctypes.POINTER(TuneOpts),
                      ctypes.POINTER(PlanOpts), ctypes.POINTER(PlanOpts), ctypes.POINTER(TuneReport)],
     }
@@ -293,6 +294,12 @@ def tune(schedule: Schedule, chunk_elems, dtype, inputs, outputs, stream=None, s
                         ctypes.byref(to), ctypes.byref(start) if start is not None else None, ctypes.byref(best),
                         ctypes.byref(rep)))
     return best, rep
+
+
+def allreduce_ring_noalloc(inputs, outputs, chunk_elems, dtype, channels=0, stream=None):
+    """Ring AllReduce with no device allocation (static scratch; see ccl.h)."""
+    _check(lib.ccl_allreduce_ring_noalloc(_ptrs(inputs), _ptrs(outputs), len(inputs), chunk_elems, dtype,
+                                          channels, _stream(stream)))
 
 
 def version() -> str:

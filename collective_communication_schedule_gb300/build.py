@@ -17,8 +17,9 @@ LIB = os.path.join(HERE, "libccl.so")
 ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["ccl_runtime.cu", "ccl_compiler.cpp", "ccl_builtin.cpp", "ccl_planner.cpp", "ccl_tuner.cpp"]
-HEADERS = ["ccl_internal.h", "ccl_plan.h", "ccl_executor.cuh"]
+SOURCES = ["ccl_runtime.cu", "ccl_static.cu", "ccl_compiler.cpp", "ccl_builtin.cpp", "ccl_planner.cpp",
+           "ccl_tuner.cpp"]
+HEADERS = ["ccl_internal.h", "ccl_plan.h", "ccl_executor.cuh", "ccl_device.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

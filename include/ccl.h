@@ -344,6 +344,38 @@ ccl_status_t ccl_tune(ccl_schedule_t s, int64_t chunk_elems, int32_t dtype,
                       const ccl_tune_opts_t* topts, const ccl_plan_opts_t* start,
                       ccl_plan_opts_t* best, ccl_tune_report_t* report);
 
+/*
+ * Ring AllReduce that allocates nothing.  The pages have no counterpart of
+ * this call; it is here for callers that must not allocate device memory when
+ * they run a collective (all device memory already reserved by a framework
+ * allocator, no room for the device-wide synchronisation a cudaMalloc may
+ * cause mid-step, or a policy of no allocation after start-up).
+ *
+ * Computes out_bufs[r] = sum_k in_bufs[k] for r < nranks, each rank buffer
+ * holding nranks * chunk_elems elements of `dtype`, with the same fused ring
+ * program and therefore the same reduction order (bit for bit) as a plan
+ * built from ccl_schedule_builtin(CCL_RING_ALLREDUCE).  channels: 0 picks
+ * min(8, 64 / nranks).
+ *
+ * Memory: the link FIFOs (4 slots of 32 KiB per link), flags and a status
+ * word live in one file-scope device array of 8 MiB + 4160 bytes that every
+ * GPU loading this library holds until the process exits.  nranks * channels
+ * may not exceed 64 links (CCL_ERR_INVALID_ARG otherwise).  No cudaMalloc,
+ * cudaFree or other allocating call is made, on the host or the device.
+ *
+ * The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress (once per device, that device current); make that
+ * first call before any stream capture.  Every call clears the flags on
+ * `stream` and launches one cooperative kernel; all calls share the array,
+ * so calls whose executions overlap on the GPU (other streams, other host
+ * threads) race and corrupt each other: serialise them.  A device wait that
+ * runs out of time (2 s) leaves the outputs incomplete; this call does not
+ * report it (use the plan API when that matters).
+ * Returns CCL_OK, CCL_ERR_INVALID_ARG, CCL_ERR_UNSUPPORTED or CCL_ERR_CUDA.
+ */
+ccl_status_t ccl_allreduce_ring_noalloc(void* const* in_bufs, void* const* out_bufs, int32_t nranks,
+                                        int64_t chunk_elems, int32_t dtype, int32_t channels, void* stream);
+
 const char* ccl_error_string(ccl_status_t s);
 const char* ccl_last_error_detail(void);
 const char* ccl_version(void);
