@@ -106,11 +106,10 @@ __device__ __forceinline__ void vstore(uint4* p, uint4 v, bool stream)
 // per thread, the remainder goes one vector per thread.
 template <bool RED, int DT>
 __device__ __forceinline__ void move_vec(const uint4* a, bool as, const uint4* b, bool bs, uint4* o1, bool o1s,
-                                         uint4* o2, int64_t nv)
+                                         uint4* o2, int64_t nv, int tid, int T)
 {
     constexpr int U = 4;
-    const int T = blockDim.x;
-    int64_t i = threadIdx.x;
+    int64_t i = tid;
     const int64_t full = nv - (int64_t)(U - 1) * T;
     for (; i < full; i += (int64_t)U * T) {
         uint4 va[U], vb[U];
@@ -137,10 +136,10 @@ __device__ __forceinline__ void move_vec(const uint4* a, bool as, const uint4* b
 
 // element path (unaligned operands or the tail of a piece)
 template <bool RED, int DT>
-__device__ void move_elem(const char* a, const char* b, char* o1, char* o2, int64_t lo, int64_t hi)
+__device__ void move_elem(const char* a, const char* b, char* o1, char* o2, int64_t lo, int64_t hi, int tid, int T)
 {
     constexpr int ES = (DT == CCL_BF16 || DT == CCL_F16) ? 2 : 4;
-    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+    for (int64_t i = lo + tid; i < hi; i += T) {
         if (ES == 4) {
             uint32_t x = __ldcg(reinterpret_cast<const unsigned int*>(a) + i);
             if (RED) x = add2<DT>(x, __ldcg(reinterpret_cast<const unsigned int*>(b) + i));
@@ -160,7 +159,7 @@ __device__ void move_elem(const char* a, const char* b, char* o1, char* o2, int6
 
 template <bool RED, int DT>
 __device__ __forceinline__ void move(const char* a, bool as, const char* b, bool bs, char* o1, bool o1s, char* o2,
-                                     int64_t n)
+                                     int64_t n, int tid, int T)
 {
     constexpr int ES = (DT == CCL_BF16 || DT == CCL_F16) ? 2 : 4;
     constexpr int VE = 16 / ES;
@@ -169,17 +168,54 @@ __device__ __forceinline__ void move(const char* a, bool as, const char* b, bool
     if ((al & 15) == 0) {
         nv = n / VE;
         move_vec<RED, DT>(reinterpret_cast<const uint4*>(a), as, reinterpret_cast<const uint4*>(b), bs,
-                          reinterpret_cast<uint4*>(o1), o1s, reinterpret_cast<uint4*>(o2), nv);
+                          reinterpret_cast<uint4*>(o1), o1s, reinterpret_cast<uint4*>(o2), nv, tid, T);
     }
-    if (nv * VE < n) move_elem<RED, DT>(a, b, o1, o2, nv * VE, n);
+    if (nv * VE < n) move_elem<RED, DT>(a, b, o1, o2, nv * VE, n, tid, T);
 }
 
+// copy or reduce n elements, shared by threads [0, T) of the caller (tid)
+template <int DT>
+__device__ __forceinline__ void move_part(bool red, const char* a, bool as, const char* b, bool bs, char* o1,
+                                          bool o1s, char* o2, int64_t n, int tid, int T)
+{
+    if (red) move<true, DT>(a, as, b, bs, o1, o1s, o2, n, tid, T);
+    else move<false, DT>(a, as, b, bs, o1, o1s, o2, n, tid, T);
+}
+
+// the whole CTA moves the data
 template <int DT>
 __device__ __forceinline__ void move_dt(bool red, const char* a, bool as, const char* b, bool bs, char* o1,
                                         bool o1s, char* o2, int64_t n)
 {
-    if (red) move<true, DT>(a, as, b, bs, o1, o1s, o2, n);
-    else move<false, DT>(a, as, b, bs, o1, o1s, o2, n);
+    move_part<DT>(red, a, as, b, bs, o1, o1s, o2, n, threadIdx.x, blockDim.x);
+}
+
+// ---------------------------------------------------------------- mbarriers
+__device__ __forceinline__ unsigned smem_addr(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, int count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// arrive (release at CTA scope)
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+// non-blocking test of the phase with the given parity (acquire at CTA scope)
+__device__ __forceinline__ bool mbar_test(unsigned long long* bar, unsigned parity)
+{
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 
 }  // namespace ccl

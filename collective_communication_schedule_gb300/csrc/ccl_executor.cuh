@@ -38,6 +38,6 @@ struct KParams {
     char* bufs[3][CCL_MAX_RANKS];
 };
 
-enum WaitReason : int { WAIT_DEP = 1, WAIT_FULL = 2, WAIT_FREE = 3 };
+enum WaitReason : int { WAIT_DEP = 1, WAIT_FULL = 2, WAIT_FREE = 3, WAIT_DONE = 4 };
 
 }  // namespace ccl

@@ -39,7 +39,8 @@ struct DStep {
     int32_t dep_begin;  // waits: deps[dep_begin .. dep_begin + dep_count)
     int32_t dep_count;
     int32_t signal;     // counter to post after the step, or -1
-    int32_t flags;      // bit 0: do not post link flags (debug hook)
+    int32_t flags;      // bit 0: do not post link flags (debug hook); bit 1: depends on an
+                        // earlier step of the same threadblock (drain in-flight slots first)
     int32_t pad;
 };
 static_assert(sizeof(DStep) == 64, "DStep layout");

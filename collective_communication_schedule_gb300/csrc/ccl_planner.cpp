@@ -491,6 +491,11 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
         for (const Dep& d : s.deps) {
             for (int ch = 0; ch < p; ++ch) {
                 int cb = d.to * p + ch;
+                // a producer in the same threadblock: its slots must have
+                // left the data warps before this instruction starts
+                for (int ch2 = 0; ch2 < p; ++ch2)
+                    if (dev_tb_of[(size_t)d.from * p + ch2] == dev_tb_of[cb])
+                        for (int mb = 0; mb < m; ++mb) img->steps[step_of[cb][mb]].flags |= 2;
                 if (d.exact) {
                     int ca = d.from * p + ch;
                     if (dev_tb_of[ca] == dev_tb_of[cb]) continue;

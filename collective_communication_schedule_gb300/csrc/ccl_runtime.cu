@@ -42,154 +42,302 @@ static ccl_status_t cuda_fail(cudaError_t e, const char* what)
 // ======================================================================
 namespace ccl {
 
-// Operands of one slot, prepared by thread 0 for the whole CTA.
+// ----------------------------------------------------------------------
+// Warp-specialised executor.
+//
+// Lane 0 of warp 0 (the control thread) walks the threadblock program: it
+// reads each step, waits (bounded) for dependency counters and for the
+// incoming slot to be full / the outgoing slot to be free, computes the
+// slot's operand addresses and hands them to the data warps through a ring
+// of kQ shared-memory descriptors guarded by mbarriers ("ready").  The data
+// warps (warps 1..) move every slot with 16-byte loads and stores and
+// arrive on a second mbarrier ("done").  When a slot is done the control
+// thread posts its consumed / full flags with gpu-scope release stores (the
+// data warps' stores reach it through the CTA-scope release/acquire of the
+// mbarrier), and the step's dependency counter after its last slot.  The
+// control thread runs up to kQ slots ahead and keeps releasing finished
+// slots while it spins on an outside flag, so it never holds a finished
+// slot while it waits and the data warps never wait on a barrier for flags.
+// ----------------------------------------------------------------------
+constexpr int kQ = 4;
+
 struct SlotOp {
     const char* a;      // data in: incoming slot or source buffer
     const char* b;      // local operand of a reduce
     char* o1;           // destination buffer, or the outgoing slot
     char* o2;           // outgoing slot when a destination is also written
     long long n;        // elements
-    int red;            // reduce (1) or copy (0)
-    int dtype;
-    int as, bs, o1s;    // streaming cache hints per operand
-    int abort;
-    int nslots;
+    int red, dtype;
+    int as, bs, o1s;    // streaming cache hints
+    int cmd;            // 0 move, 1 end, 2 abort
 };
 
-// State of the current step, kept in shared memory and used by thread 0
-// only, so that it does not occupy registers of the data-moving threads.
-struct LeadState {
-    DStep st;
-    DInstr in;
-    unsigned long long t_start, waited, base_in, base_out;
-    const DLink* Lin;
-    const DLink* Lout;
-    long long slot_elems;
-    int es;
+struct Release {
+    unsigned long long* consumed;  // flag to post, or null
+    unsigned long long* full;
+    unsigned long long* counter;
+    unsigned long long consumed_v, full_v, counter_v;
+    unsigned long long t_start, waited;
+    int si;
+    int last;                      // last slot of its step
 };
 
-__global__ void __launch_bounds__(1024, 1) ccl_exec_kernel(const __grid_constant__ KParams P)
+struct CtlShared {
+    SlotOp op[kQ];
+    Release rel[kQ];
+    unsigned long long ready[kQ];
+    unsigned long long done[kQ];
+};
+
+// control-thread state
+struct Ctl {
+    const KParams* P;
+    CtlShared* sh;
+    int head, tail;                // slots [tail, head) handed out, not yet released
+};
+
+__device__ __forceinline__ void ctl_release(Ctl& c, const Release& r)
 {
-    __shared__ SlotOp op;
-    __shared__ LeadState L;
-    const int b0 = P.tb_begin[blockIdx.x], b1 = P.tb_begin[blockIdx.x + 1];
-    const bool leader = threadIdx.x == 0;
-    DStep& st = L.st;
-    DInstr& in = L.in;
-    unsigned long long& t_start = L.t_start;
-    unsigned long long& waited = L.waited;
-    unsigned long long& base_in = L.base_in;
-    unsigned long long& base_out = L.base_out;
-    const DLink*& Lin = L.Lin;
-    const DLink*& Lout = L.Lout;
-    long long& slot_elems = L.slot_elems;
-    int& es = L.es;
-    for (int si = b0; si < b1; ++si) {
-        if (leader) {
-            t_start = gtimer();
-            waited = 0;
-            st = P.steps[si];
-            in = P.instrs[st.instr];
-            int ok = 1;
-            for (int k = 0; k < st.dep_count && ok; ++k) {
-                const DDep d = P.deps[st.dep_begin + k];
-                ok = wait_geq(P.counters + d.counter, (unsigned long long)(P.exec * P.m + d.value), P.status, P.timeout_ns, si, WAIT_DEP,
-                              waited);
-            }
-            es = (in.dtype == CCL_BF16 || in.dtype == CCL_F16) ? 2 : 4;
-            Lin = in.link_in >= 0 ? P.links + in.link_in : nullptr;
-            Lout = in.link_out >= 0 ? P.links + in.link_out : nullptr;
-            base_in = Lin ? (unsigned long long)(P.exec * Lin->total) : 0;
-            base_out = Lout ? (unsigned long long)(P.exec * Lout->total) : 0;
-            slot_elems = (Lin || Lout) ? P.slot_bytes / es : (st.nelem > 0 ? st.nelem : 1);
-            op.nslots = st.nslots > 0 ? st.nslots : 1;
-            op.abort = !ok;
-            op.red = (in.kind == CCL_I_REDUCE || in.kind == CCL_I_RRC || in.kind == CCL_I_RRS || in.kind == CCL_I_RRCS);
-            op.dtype = in.dtype;
+    if (r.consumed) st_release(r.consumed, r.consumed_v);
+    if (r.full) st_release(r.full, r.full_v);
+    if (r.last) {
+        if (r.counter) st_release(r.counter, r.counter_v);
+        if (c.P->timeline) {
+            unsigned long long* tl = c.P->timeline + 3ll * r.si;
+            tl[0] = r.t_start;
+            tl[1] = r.waited;
+            tl[2] = gtimer();
         }
-        __syncthreads();
-        if (op.abort) return;
-        const int nslots = op.nslots;
-        for (int k = 0; k < nslots; ++k) {
-            if (leader) {
-                const long long e0 = (long long)k * slot_elems;
-                long long n = st.nelem - e0;
-                if (n > slot_elems) n = slot_elems;
-                if (n < 0) n = 0;
-                const unsigned long long sin = base_in + st.seq_in + k;
-                const unsigned long long sout = base_out + st.seq_out + k;
-                int ok = 1;
-                if (Lin)
-                    ok = wait_geq(P.flags + Lin->flag_base + (int)(sin % P.S), sin + 1, P.status, P.timeout_ns, si,
-                                  WAIT_FULL, waited);
-                if (ok && Lout && sout + 1 > (unsigned long long)P.S)
-                    ok = wait_geq(P.flags + Lout->flag_base + P.S + (int)(sout % P.S), sout + 1 - P.S, P.status,
-                                  P.timeout_ns, si, WAIT_FREE, waited);
-                const long long eo = (st.elem_off + e0) * es;
-                const char* srcp = in.src_buf >= 0 ? P.bufs[in.src_buf][in.src_rank] + in.src_off * es + eo : nullptr;
-                const char* locp = in.loc_buf >= 0 ? P.bufs[in.loc_buf][in.loc_rank] + in.loc_off * es + eo : nullptr;
-                char* dstp = in.dst_buf >= 0 ? P.bufs[in.dst_buf][in.dst_rank] + in.dst_off * es + eo : nullptr;
-                char* slot_out = Lout ? P.fifo + Lout->slot_base + (long long)(sout % P.S) * P.slot_bytes : nullptr;
-                if (Lin && in.kind != CCL_I_REDUCE) {
-                    op.a = P.fifo + Lin->slot_base + (long long)(sin % P.S) * P.slot_bytes;
-                    op.as = 0;
-                } else {
-                    op.a = srcp;
-                    op.as = in.src_buf == CCL_BUF_IN;
+    }
+}
+
+// release every finished slot in order, without blocking
+__device__ __forceinline__ void ctl_drain(Ctl& c)
+{
+    while (c.tail < c.head) {
+        const int q = c.tail % kQ;
+        if (!mbar_test(&c.sh->done[q], (unsigned)((c.tail / kQ) & 1))) break;
+        ctl_release(c, c.sh->rel[q]);
+        ++c.tail;
+    }
+}
+
+// wait for the oldest handed-out slot (the data warps depend on nothing
+// outside the CTA, so this ends; bounded anyway)
+__device__ __forceinline__ bool ctl_drain_one(Ctl& c, int si)
+{
+    const int q = c.tail % kQ;
+    const unsigned par = (unsigned)((c.tail / kQ) & 1);
+    unsigned long long t0 = 0;
+    unsigned spins = 0;
+    while (!mbar_test(&c.sh->done[q], par)) {
+        if ((++spins & 255) == 0) {
+            unsigned long long now = gtimer();
+            if (!t0) t0 = now;
+            else if (now - t0 > c.P->timeout_ns) {
+                if (atomicCAS(c.P->status, 0, (int)CCL_ERR_TIMEOUT) == 0) {
+                    c.P->status[1] = blockIdx.x;
+                    c.P->status[2] = si;
+                    c.P->status[3] = WAIT_DONE;
                 }
-                op.b = locp;
-                op.bs = in.loc_buf == CCL_BUF_IN;
-                if (dstp) {
-                    op.o1 = dstp;
-                    op.o1s = in.dst_buf == CCL_BUF_OUT;
-                    op.o2 = slot_out;
-                } else {
-                    op.o1 = slot_out;
-                    op.o1s = 0;
-                    op.o2 = nullptr;
-                }
-                op.n = n;
-                op.abort = !ok;
-            }
-            __syncthreads();
-            if (op.abort) return;
-            {
-                const char* a = op.a;
-                const char* b = op.b;
-                char* o1 = op.o1;
-                char* o2 = op.o2;
-                const long long n = op.n;
-                const bool as = op.as, bs = op.bs, o1s = op.o1s, red = op.red;
-                if (n > 0) {
-                    switch (op.dtype) {
-                    case CCL_F32: move_dt<CCL_F32>(red, a, as, b, bs, o1, o1s, o2, n); break;
-                    case CCL_BF16: move_dt<CCL_BF16>(red, a, as, b, bs, o1, o1s, o2, n); break;
-                    case CCL_F16: move_dt<CCL_F16>(red, a, as, b, bs, o1, o1s, o2, n); break;
-                    default: move_dt<CCL_I32>(red, a, as, b, bs, o1, o1s, o2, n); break;
-                    }
-                }
-            }
-            __syncthreads();
-            if (leader) {
-                __threadfence();
-                if (!(st.flags & 1)) {
-                    const unsigned long long sin = base_in + st.seq_in + k;
-                    const unsigned long long sout = base_out + st.seq_out + k;
-                    if (Lin) st_release(P.flags + Lin->flag_base + P.S + (int)(sin % P.S), sin + 1);
-                    if (Lout) st_release(P.flags + Lout->flag_base + (int)(sout % P.S), sout + 1);
-                }
-            }
-        }
-        if (leader) {
-            if (st.signal >= 0) st_release(P.counters + st.signal, (unsigned long long)(P.exec * P.m + st.mb + 1));
-            if (P.timeline) {
-                unsigned long long* tl = P.timeline + 3ll * si;
-                tl[0] = t_start;
-                tl[1] = waited;
-                tl[2] = gtimer();
+                return false;
             }
         }
     }
+    ctl_release(c, c.sh->rel[q]);
+    ++c.tail;
+    return true;
+}
+
+// bounded wait on a flag of another threadblock; finished slots keep being
+// released meanwhile
+__device__ bool ctl_wait(Ctl& c, const unsigned long long* p, unsigned long long v, int si, int reason,
+                         unsigned long long& waited)
+{
+    if (ld_acquire(p) >= v) return true;
+    unsigned long long t0 = gtimer();
+    unsigned spins = 0;
+    while (ld_acquire(p) < v) {
+        ctl_drain(c);
+        ++spins;
+        if ((spins & 15) == 0) {
+            if (*(volatile int*)c.P->status != 0) return false;
+            if (gtimer() - t0 > c.P->timeout_ns) {
+                if (atomicCAS(c.P->status, 0, (int)CCL_ERR_TIMEOUT) == 0) {
+                    c.P->status[1] = blockIdx.x;
+                    c.P->status[2] = si;
+                    c.P->status[3] = reason;
+                }
+                return false;
+            }
+        }
+        if (spins > 64) __nanosleep(32);
+    }
+    waited += gtimer() - t0;
+    return true;
+}
+
+__device__ __forceinline__ void ctl_publish_cmd(Ctl& c, int cmd)
+{
+    const int q = c.head % kQ;
+    c.sh->op[q].cmd = cmd;
+    mbar_arrive(&c.sh->ready[q]);
+}
+
+__device__ void control_thread(const KParams& P, CtlShared* sh, int b0, int b1)
+{
+    Ctl c{&P, sh, 0, 0};
+    for (int si = b0; si < b1; ++si) {
+        const DStep st = P.steps[si];
+        const DInstr in = P.instrs[st.instr];
+        const unsigned long long t_start = gtimer();
+        unsigned long long waited = 0;
+        if (st.flags & 2) {
+            // reads or writes what an earlier step of this threadblock touched
+            while (c.tail < c.head)
+                if (!ctl_drain_one(c, si)) {
+                    ctl_publish_cmd(c, 2);
+                    return;
+                }
+        }
+        for (int k = 0; k < st.dep_count; ++k) {
+            const DDep d = P.deps[st.dep_begin + k];
+            if (!ctl_wait(c, P.counters + d.counter, (unsigned long long)(P.exec * P.m + d.value), si, WAIT_DEP,
+                          waited)) {
+                ctl_publish_cmd(c, 2);
+                return;
+            }
+        }
+        const int es = (in.dtype == CCL_BF16 || in.dtype == CCL_F16) ? 2 : 4;
+        const DLink* Lin = in.link_in >= 0 ? P.links + in.link_in : nullptr;
+        const DLink* Lout = in.link_out >= 0 ? P.links + in.link_out : nullptr;
+        const unsigned long long base_in = Lin ? (unsigned long long)(P.exec * Lin->total) : 0;
+        const unsigned long long base_out = Lout ? (unsigned long long)(P.exec * Lout->total) : 0;
+        const long long slot_elems = (Lin || Lout) ? P.slot_bytes / es : (st.nelem > 0 ? st.nelem : 1);
+        const int nslots = st.nslots > 0 ? st.nslots : 1;
+        const bool red = in.kind == CCL_I_REDUCE || in.kind == CCL_I_RRC || in.kind == CCL_I_RRS || in.kind == CCL_I_RRCS;
+        const char* srcb = in.src_buf >= 0 ? P.bufs[in.src_buf][in.src_rank] + (in.src_off + st.elem_off) * es : nullptr;
+        const char* locb = in.loc_buf >= 0 ? P.bufs[in.loc_buf][in.loc_rank] + (in.loc_off + st.elem_off) * es : nullptr;
+        char* dstb = in.dst_buf >= 0 ? P.bufs[in.dst_buf][in.dst_rank] + (in.dst_off + st.elem_off) * es : nullptr;
+        for (int k = 0; k < nslots; ++k) {
+            if (c.head - c.tail == kQ && !ctl_drain_one(c, si)) {
+                ctl_publish_cmd(c, 2);
+                return;
+            }
+            const unsigned long long sin = base_in + st.seq_in + k;
+            const unsigned long long sout = base_out + st.seq_out + k;
+            int ok = 1;
+            if (Lin) ok = ctl_wait(c, P.flags + Lin->flag_base + (int)(sin % P.S), sin + 1, si, WAIT_FULL, waited);
+            if (ok && Lout && sout + 1 > (unsigned long long)P.S)
+                ok = ctl_wait(c, P.flags + Lout->flag_base + P.S + (int)(sout % P.S), sout + 1 - P.S, si, WAIT_FREE,
+                              waited);
+            if (!ok) {
+                ctl_publish_cmd(c, 2);
+                return;
+            }
+            const long long e0 = (long long)k * slot_elems;
+            long long n = st.nelem - e0;
+            if (n > slot_elems) n = slot_elems;
+            if (n < 0) n = 0;
+            const int q = c.head % kQ;
+            char* slot_out = Lout ? P.fifo + Lout->slot_base + (long long)(sout % P.S) * P.slot_bytes : nullptr;
+            SlotOp& op = sh->op[q];
+            if (Lin && in.kind != CCL_I_REDUCE) {
+                op.a = P.fifo + Lin->slot_base + (long long)(sin % P.S) * P.slot_bytes;
+                op.as = 0;
+            } else {
+                op.a = srcb + e0 * es;
+                op.as = in.src_buf == CCL_BUF_IN;
+            }
+            op.b = locb ? locb + e0 * es : nullptr;
+            op.bs = in.loc_buf == CCL_BUF_IN;
+            if (dstb) {
+                op.o1 = dstb + e0 * es;
+                op.o1s = in.dst_buf == CCL_BUF_OUT;
+                op.o2 = slot_out;
+            } else {
+                op.o1 = slot_out;
+                op.o1s = 0;
+                op.o2 = nullptr;
+            }
+            op.n = n;
+            op.red = red;
+            op.dtype = in.dtype;
+            op.cmd = 0;
+            Release& r = sh->rel[q];
+            const bool post = !(st.flags & 1);
+            r.consumed = (Lin && post) ? P.flags + Lin->flag_base + P.S + (int)(sin % P.S) : nullptr;
+            r.consumed_v = sin + 1;
+            r.full = (Lout && post) ? P.flags + Lout->flag_base + (int)(sout % P.S) : nullptr;
+            r.full_v = sout + 1;
+            r.last = k == nslots - 1;
+            r.counter = st.signal >= 0 ? P.counters + st.signal : nullptr;
+            r.counter_v = (unsigned long long)(P.exec * P.m + st.mb + 1);
+            r.si = si;
+            r.t_start = t_start;
+            r.waited = waited;
+            mbar_arrive(&sh->ready[q]);
+            ++c.head;
+            ctl_drain(c);
+        }
+    }
+    while (c.tail < c.head)
+        if (!ctl_drain_one(c, b1 - 1)) break;
+    ctl_publish_cmd(c, 1);
+}
+
+__device__ void data_warps(const KParams& P, CtlShared* sh)
+{
+    const int tid = threadIdx.x - 32;
+    const int T = blockDim.x - 32;
+    const int lane = threadIdx.x & 31;
+    for (int j = 0;; ++j) {
+        const int q = j % kQ;
+        const unsigned par = (unsigned)((j / kQ) & 1);
+        unsigned spins = 0;
+        unsigned long long t0 = 0;
+        while (!mbar_test(&sh->ready[q], par)) {
+            if ((++spins & 255) == 0) {
+                unsigned long long now = gtimer();
+                if (!t0) t0 = now;
+                // the control thread waits at most timeout_ns per flag; give it
+                // a generous margin before giving up on it
+                else if (now - t0 > 4 * P.timeout_ns) return;
+            }
+            if (spins > 32) __nanosleep(20);
+        }
+        const SlotOp op = sh->op[q];
+        if (op.cmd != 0) return;
+        if (op.n > 0) {
+            switch (op.dtype) {
+            case CCL_F32: move_part<CCL_F32>(op.red, op.a, op.as, op.b, op.bs, op.o1, op.o1s, op.o2, op.n, tid, T); break;
+            case CCL_BF16: move_part<CCL_BF16>(op.red, op.a, op.as, op.b, op.bs, op.o1, op.o1s, op.o2, op.n, tid, T); break;
+            case CCL_F16: move_part<CCL_F16>(op.red, op.a, op.as, op.b, op.bs, op.o1, op.o1s, op.o2, op.n, tid, T); break;
+            default: move_part<CCL_I32>(op.red, op.a, op.as, op.b, op.bs, op.o1, op.o1s, op.o2, op.n, tid, T); break;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->done[q]);
+    }
+}
+
+__global__ void __launch_bounds__(1024, 1) ccl_exec_kernel(const __grid_constant__ KParams P)
+{
+    __shared__ CtlShared sh;
+    const int b0 = P.tb_begin[blockIdx.x], b1 = P.tb_begin[blockIdx.x + 1];
+    const int nwarps = blockDim.x / 32;
+    if (threadIdx.x == 0) {
+        for (int q = 0; q < kQ; ++q) {
+            mbar_init(&sh.ready[q], 1);
+            mbar_init(&sh.done[q], nwarps - 1);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        if (threadIdx.x == 0) control_thread(P, &sh, b0, b1);
+        return;
+    }
+    data_warps(P, &sh);
 }
 
 }  // namespace ccl
@@ -551,10 +699,11 @@ ccl_status_t ccl_plan_status(ccl_plan_t p)
     int hs[4] = {0, 0, 0, 0};
     CUDA_TRY(cudaMemcpy(hs, p->d_status, sizeof(hs), cudaMemcpyDeviceToHost), "read status");
     if (hs[0] == 0) return CCL_OK;
-    static const char* reasons[] = {"?", "dependency counter", "incoming slot", "free outgoing slot"};
+    static const char* reasons[] = {"?", "dependency counter", "incoming slot", "free outgoing slot",
+                                    "its own data warps"};
     std::string msg = "threadblock " + std::to_string(hs[1]) + " (rank " +
                       std::to_string(hs[1] >= 0 && hs[1] < (int)p->img.tb_rank.size() ? p->img.tb_rank[hs[1]] : -1) +
-                      ") gave up waiting for " + reasons[(hs[3] >= 1 && hs[3] <= 3) ? hs[3] : 0] + " at step " +
+                      ") gave up waiting for " + reasons[(hs[3] >= 1 && hs[3] <= 4) ? hs[3] : 0] + " at step " +
                       std::to_string(hs[2]);
     ccl_status_t code = (ccl_status_t)hs[0];
     if (reset_flags(p, 0) != CCL_OK) return CCL_ERR_CUDA;

@@ -1,0 +1,117 @@
+"""GPU runtime behaviour: bounded waits, instrumentation, tuner, host-buffer
+path, and full-size parity in the benchmark's launch configurations."""
+import numpy as np
+import pytest
+
+from gpu_helpers import assert_bitexact, empty_outputs, oracle_program, run_case, to_device, to_host
+
+pytestmark = pytest.mark.gpu
+
+F32, BF16, F16, I32 = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def ccl():
+    import collective_communication_schedule_gb300 as m
+    return m
+
+
+def test_lost_signal_times_out_and_device_stays_usable(ccl):
+    """A plan patched to skip one flag post: the waiting threadblock gives up
+    after 50 ms, the status reads CCL_ERR_TIMEOUT, and the GPU then runs a
+    fresh plan correctly (host-made fault, no device fault)."""
+    import torch
+    import datagen
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 4)
+    plan = ccl.Plan(s, 1024, F32, timeout_ms=50)
+    plan.debug_drop_signal(0, 0)
+    ins = to_device(datagen.rank_inputs(0, "normal", 4, 4 * 1024, F32), F32)
+    outs = empty_outputs(4, 4 * 1024, F32)
+    plan.execute(ins, outs)
+    torch.cuda.synchronize()
+    with pytest.raises(ccl.CclError) as ei:
+        plan.status()
+    assert ei.value.code == 8
+    assert "gave up waiting" in ei.value.detail
+    got, want, _ = run_case(ccl, 0, 4, 0, 1024, F32, "normal", 0)
+    assert_bitexact(got, want)
+
+
+def test_timeline_reports_idle_fractions(ccl):
+    import torch
+    import datagen
+    s = ccl.Schedule.builtin(ccl.HIER_ALLREDUCE, 16, 8)
+    plan = ccl.Plan(s, 65536, F32, channels=2, microbatches=4, instrument=1)
+    ins = to_device(datagen.rank_inputs(2, "normal", 16, 16 * 65536, F32), F32)
+    outs = empty_outputs(16, 16 * 65536, F32)
+    plan.execute(ins, outs)
+    torch.cuda.synchronize()
+    plan.status()
+    tl = plan.timeline()
+    st = plan.stats()
+    assert len(tl["idle"]) == st.nthreadblocks
+    assert all(0.0 <= x <= 1.0 for x in tl["idle"])
+    assert tl["mean_idle"] <= tl["max_idle"] + 1e-12 and tl["span_us"] > 0
+
+
+def test_tuner_returns_a_configuration_that_runs(ccl):
+    import torch
+    import datagen
+    import oracle
+    R, ce = 8, 32768
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, R)
+    host = datagen.rank_inputs(0, "uniform", R, R * ce, F32)
+    ins = to_device(host, F32)
+    outs = empty_outputs(R, R * ce, F32)
+    best, rep = ccl.tune(s, ce, F32, ins, outs, max_rounds=1, reps=3)
+    assert rep.probes >= 2 and rep.best_us > 0
+    assert rep.best_us <= rep.default_us * 1.10 + 5.0
+    plan = ccl.Plan(s, ce, F32, opts=best)
+    outs = empty_outputs(R, R * ce, F32)
+    plan.execute(ins, outs)
+    torch.cuda.synchronize()
+    plan.status()
+    ops, nch = oracle_program(0, R)
+    want, _, _ = oracle.run(ops, R, nch, ce, F32, host)
+    assert_bitexact(to_host(outs, F32), want)
+
+
+def test_execute_host_round_trip(ccl):
+    import torch
+    import datagen
+    import oracle
+    R, G, ce = 8, 4, 5000
+    s = ccl.Schedule.builtin(ccl.ALLTOALL_2PHASE, R, G)
+    plan = ccl.Plan(s, ce, F16, channels=2)
+    host = datagen.rank_inputs(3, "uniform", R, R * ce, F16)
+    h_in = [torch.from_numpy(a.view(np.int16)).pin_memory() for a in host]
+    h_out = [torch.empty(R * ce, dtype=torch.int16).pin_memory() for _ in range(R)]
+    d_in = [torch.empty(R * ce, dtype=torch.int16, device="cuda") for _ in range(R)]
+    d_out = [torch.empty(R * ce, dtype=torch.int16, device="cuda") for _ in range(R)]
+    plan.execute_host(h_in, h_out, d_in, d_out)
+    torch.cuda.synchronize()
+    plan.status()
+    ops, nch = oracle_program(4, R, G)
+    want, _, _ = oracle.run(ops, R, nch, ce, F16, host)
+    assert_bitexact([t.numpy().view(np.uint16) for t in h_out], want)
+
+
+def _bench_rows():
+    import bench
+    return bench.SUITE
+
+
+@pytest.mark.parametrize("row", range(8))
+def test_full_size_benchmark_configurations(ccl, row):
+    """Every collective of the benchmark at its full size and plan options;
+    the oracle computes 64 sampled in-chunk columns exactly, and the
+    copy collectives are also compared in full."""
+    import torch
+    name, kind, R, G, dt, chunk_bytes, dist, seed, opts = _bench_rows()[row]
+    ce = chunk_bytes // {0: 4, 1: 2, 2: 2, 3: 4}[dt]
+    rng = np.random.default_rng(12345 + row)
+    cols = np.unique(np.concatenate([[0, ce - 1], rng.integers(0, ce, 62)]))
+    got, want, plan = run_case(ccl, kind, R, G, ce, dt, dist, seed, sampled=cols, **opts)
+    assert_bitexact(got, want)
+    del got, want, plan
+    torch.cuda.empty_cache()
