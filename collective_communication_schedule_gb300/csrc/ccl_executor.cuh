@@ -19,8 +19,7 @@
 namespace ccl {
 
 struct KParams {
-    const DInstr* instrs;
-    const DStep* steps;
+    const DRec* recs;
     const int32_t* tb_begin;
     const DLink* links;
     const DDep* deps;

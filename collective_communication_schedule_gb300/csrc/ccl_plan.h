@@ -45,6 +45,18 @@ struct DStep {
 };
 static_assert(sizeof(DStep) == 64, "DStep layout");
 
+// Everything the executor needs for one step, denormalised (one 128-byte
+// record per step, so the control warp prefetches a step with one load).
+struct DRec {
+    int32_t kind, dtype, link_in, link_out;
+    int32_t src_buf, src_rank, loc_buf, loc_rank, dst_buf, dst_rank;
+    int32_t nslots, dep_begin, dep_count, signal, mb, flags;
+    int64_t src_off, loc_off, dst_off;   // element offsets of this piece
+    int64_t nelem, seq_in, seq_out;
+    int64_t pad[2];
+};
+static_assert(sizeof(DRec) == 128, "DRec layout");
+
 struct DLink {
     int64_t slot_base;  // byte offset of slot 0 in the FIFO pool
     int64_t total;      // slot sequences per execution
@@ -62,6 +74,7 @@ struct DDep {
 struct PlanImage {
     std::vector<DInstr> instrs;
     std::vector<DStep> steps;
+    std::vector<DRec> recs;          // built from instrs + steps at the end of planning
     std::vector<int32_t> tb_begin;   // ntb + 1
     std::vector<DLink> links;
     std::vector<DDep> deps;

@@ -300,6 +300,26 @@ std::vector<std::vector<int>> make_segments(const Timeline& tl, const std::vecto
     return segs;
 }
 
+void fill_records(PlanImage* img)
+{
+    img->recs.assign(img->steps.size(), DRec{});
+    for (size_t k = 0; k < img->steps.size(); ++k) {
+        const DStep& st = img->steps[k];
+        const DInstr& in = img->instrs[st.instr];
+        DRec& r = img->recs[k];
+        r.kind = in.kind; r.dtype = in.dtype; r.link_in = in.link_in; r.link_out = in.link_out;
+        r.src_buf = in.src_buf; r.src_rank = in.src_rank;
+        r.loc_buf = in.loc_buf; r.loc_rank = in.loc_rank;
+        r.dst_buf = in.dst_buf; r.dst_rank = in.dst_rank;
+        r.nslots = st.nslots; r.dep_begin = st.dep_begin; r.dep_count = st.dep_count;
+        r.signal = st.signal; r.mb = st.mb; r.flags = st.flags;
+        r.src_off = in.src_off + st.elem_off;
+        r.loc_off = in.loc_off + st.elem_off;
+        r.dst_off = in.dst_off + st.elem_off;
+        r.nelem = st.nelem; r.seq_in = st.seq_in; r.seq_out = st.seq_out;
+    }
+}
+
 struct Attempt {
     int alloc, m, order;
 };
@@ -530,6 +550,7 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
         }
     }
     img->fifo_bytes = (int64_t)img->links.size() * S * o.slot_bytes;
+    fill_records(img);
     return CCL_OK;
 }
 
@@ -669,8 +690,8 @@ ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const 
     if (ce <= 0) return fail(CCL_ERR_INVALID_ARG, "chunk_elems must be positive");
     if (dtype < CCL_F32 || dtype > CCL_I32) return fail(CCL_ERR_INVALID_ARG, "unknown dtype");
     if (o.channels < 1 || o.channels > 256) return fail(CCL_ERR_INVALID_ARG, "channels must be in 1..256");
-    if (o.nthreads < 64 || o.nthreads > 1024 || o.nthreads % 32)
-        return fail(CCL_ERR_INVALID_ARG, "nthreads must be a multiple of 32 in 64..1024");
+    if (o.nthreads < 96 || o.nthreads > 1024 || o.nthreads % 32)
+        return fail(CCL_ERR_INVALID_ARG, "nthreads must be a multiple of 32 in 96..1024");
     if (o.slot_bytes < 16 || o.slot_bytes % 16) return fail(CCL_ERR_INVALID_ARG, "slot_bytes must be a positive multiple of 16");
     if (o.fifo_slots < 2 || o.fifo_slots > 64) return fail(CCL_ERR_INVALID_ARG, "fifo_slots must be in 2..64");
     if (o.microbatches < 0 || o.microbatches > 65536) return fail(CCL_ERR_INVALID_ARG, "microbatches out of range");

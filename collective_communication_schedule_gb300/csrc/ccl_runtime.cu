@@ -43,23 +43,27 @@ static ccl_status_t cuda_fail(cudaError_t e, const char* what)
 namespace ccl {
 
 // ----------------------------------------------------------------------
-// Warp-specialised executor.
+// Warp-specialised executor.  Three roles per CTA:
 //
-// Lane 0 of warp 0 (the control thread) walks the threadblock program: it
-// reads each step, waits (bounded) for dependency counters and for the
-// incoming slot to be full / the outgoing slot to be free, computes the
-// slot's operand addresses and hands them to the data warps through a ring
-// of kQ shared-memory descriptors guarded by mbarriers ("ready").  The data
-// warps (warps 1..) move every slot with 16-byte loads and stores and
-// arrive on a second mbarrier ("done").  When a slot is done the control
-// thread posts its consumed / full flags with gpu-scope release stores (the
-// data warps' stores reach it through the CTA-scope release/acquire of the
-// mbarrier), and the step's dependency counter after its last slot.  The
-// control thread runs up to kQ slots ahead and keeps releasing finished
-// slots while it spins on an outside flag, so it never holds a finished
-// slot while it waits and the data warps never wait on a barrier for flags.
+//  * issuer (warp 0, lane 0) walks the threadblock program.  For every slot
+//    it waits (bounded) for the step's dependency counters, the incoming
+//    slot to be full and the outgoing slot to be free -- both flags polled
+//    with relaxed loads in one round trip, then one acquire fence -- and
+//    hands the slot's operand addresses to the data warps through a ring of
+//    kQ shared-memory descriptors guarded by mbarriers ("ready").  The next
+//    step's 128-byte record is prefetched while the current one runs.
+//  * data warps (warps 2..) move each slot with 16-byte loads and stores and
+//    arrive on "done".
+//  * releaser (warp 1, lane 0) takes finished slots in order, issues one
+//    release fence per batch and then posts the consumed / full flags and the
+//    step's dependency counter with relaxed stores, and frees the descriptor
+//    ("freed").  The data warps' stores reach it through the CTA-scope
+//    release / acquire of the mbarrier, so the gpu-scope fence covers them.
+//
+// The issuer can run kQ slots ahead of the data warps, and releases never
+// wait behind the issuer's waits on other threadblocks.
 // ----------------------------------------------------------------------
-constexpr int kQ = 4;
+constexpr int kQ = 8;
 
 struct SlotOp {
     const char* a;      // data in: incoming slot or source buffer
@@ -83,177 +87,160 @@ struct Release {
 };
 
 struct CtlShared {
+    DRec rec[2];
     SlotOp op[kQ];
     Release rel[kQ];
     unsigned long long ready[kQ];
     unsigned long long done[kQ];
+    unsigned long long freed[kQ];
 };
 
-// control-thread state
-struct Ctl {
-    const KParams* P;
-    CtlShared* sh;
-    int head, tail;                // slots [tail, head) handed out, not yet released
-};
-
-__device__ __forceinline__ void ctl_release(Ctl& c, const Release& r)
+__device__ __forceinline__ void record_timeout(const KParams& P, int si, int reason)
 {
-    if (r.consumed) st_release(r.consumed, r.consumed_v);
-    if (r.full) st_release(r.full, r.full_v);
-    if (r.last) {
-        if (r.counter) st_release(r.counter, r.counter_v);
-        if (c.P->timeline) {
-            unsigned long long* tl = c.P->timeline + 3ll * r.si;
-            tl[0] = r.t_start;
-            tl[1] = r.waited;
-            tl[2] = gtimer();
-        }
+    if (atomicCAS(P.status, 0, (int)CCL_ERR_TIMEOUT) == 0) {
+        P.status[1] = blockIdx.x;
+        P.status[2] = si;
+        P.status[3] = reason;
     }
 }
 
-// release every finished slot in order, without blocking
-__device__ __forceinline__ void ctl_drain(Ctl& c)
+// bounded wait on an mbarrier phase inside the CTA
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned par, unsigned long long limit_ns)
 {
-    while (c.tail < c.head) {
-        const int q = c.tail % kQ;
-        if (!mbar_test(&c.sh->done[q], (unsigned)((c.tail / kQ) & 1))) break;
-        ctl_release(c, c.sh->rel[q]);
-        ++c.tail;
-    }
-}
-
-// wait for the oldest handed-out slot (the data warps depend on nothing
-// outside the CTA, so this ends; bounded anyway)
-__device__ __forceinline__ bool ctl_drain_one(Ctl& c, int si)
-{
-    const int q = c.tail % kQ;
-    const unsigned par = (unsigned)((c.tail / kQ) & 1);
-    unsigned long long t0 = 0;
     unsigned spins = 0;
-    while (!mbar_test(&c.sh->done[q], par)) {
-        if ((++spins & 255) == 0) {
+    unsigned long long t0 = 0;
+    while (!mbar_test(bar, par)) {
+        if ((++spins & 127) == 0) {
             unsigned long long now = gtimer();
             if (!t0) t0 = now;
-            else if (now - t0 > c.P->timeout_ns) {
-                if (atomicCAS(c.P->status, 0, (int)CCL_ERR_TIMEOUT) == 0) {
-                    c.P->status[1] = blockIdx.x;
-                    c.P->status[2] = si;
-                    c.P->status[3] = WAIT_DONE;
-                }
-                return false;
-            }
+            else if (now - t0 > limit_ns) return false;
         }
+        if (spins > 32) __nanosleep(20);
     }
-    ctl_release(c, c.sh->rel[q]);
-    ++c.tail;
     return true;
 }
 
-// bounded wait on a flag of another threadblock; finished slots keep being
-// released meanwhile
-__device__ bool ctl_wait(Ctl& c, const unsigned long long* p, unsigned long long v, int si, int reason,
-                         unsigned long long& waited)
+// bounded wait until *a >= va and *b >= vb (b may be null), polled with
+// relaxed loads issued together, followed by one acquire fence
+__device__ bool wait_flags(const KParams& P, const unsigned long long* a, unsigned long long va,
+                           const unsigned long long* b, unsigned long long vb, int si, int reason,
+                           unsigned long long& waited)
 {
-    if (ld_acquire(p) >= v) return true;
-    unsigned long long t0 = gtimer();
+    unsigned long long t0 = 0;
     unsigned spins = 0;
-    while (ld_acquire(p) < v) {
-        ctl_drain(c);
+    while (true) {
+        unsigned long long x = a ? ld_relaxed(a) : ~0ull;
+        unsigned long long y = b ? ld_relaxed(b) : ~0ull;
+        if (x >= va && y >= vb) break;
+        if (!t0) t0 = gtimer();
         ++spins;
         if ((spins & 15) == 0) {
-            if (*(volatile int*)c.P->status != 0) return false;
-            if (gtimer() - t0 > c.P->timeout_ns) {
-                if (atomicCAS(c.P->status, 0, (int)CCL_ERR_TIMEOUT) == 0) {
-                    c.P->status[1] = blockIdx.x;
-                    c.P->status[2] = si;
-                    c.P->status[3] = reason;
-                }
+            if (*(volatile int*)P.status != 0) return false;
+            if (gtimer() - t0 > P.timeout_ns) {
+                record_timeout(P, si, (a && x < va) ? reason : WAIT_FREE);
                 return false;
             }
         }
         if (spins > 64) __nanosleep(32);
     }
-    waited += gtimer() - t0;
+    fence_acq_rel_gpu();
+    if (t0) waited += gtimer() - t0;
     return true;
 }
 
-__device__ __forceinline__ void ctl_publish_cmd(Ctl& c, int cmd)
+__device__ __forceinline__ void prefetch_rec(DRec* dst, const DRec* src)
 {
-    const int q = c.head % kQ;
-    c.sh->op[q].cmd = cmd;
-    mbar_arrive(&c.sh->ready[q]);
+    const unsigned d = smem_addr(dst);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + 16 * k), "l"((const char*)src + 16 * k)
+                     : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-__device__ void control_thread(const KParams& P, CtlShared* sh, int b0, int b1)
+__device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
 {
-    Ctl c{&P, sh, 0, 0};
+    int head = 0;
+    auto publish_cmd = [&](int cmd) {
+        const int q = head % kQ;
+        if (head >= kQ) mbar_wait(&sh->freed[q], (unsigned)(((head / kQ) - 1) & 1), 4 * P.timeout_ns);
+        sh->op[q].cmd = cmd;
+        mbar_arrive(&sh->ready[q]);
+    };
+    // step records are double-buffered in shared memory: the record of the
+    // next step is copied asynchronously (cp.async) while this one runs
+    if (b0 < b1) prefetch_rec(&sh->rec[b0 & 1], P.recs + b0);
     for (int si = b0; si < b1; ++si) {
-        const DStep st = P.steps[si];
-        const DInstr in = P.instrs[st.instr];
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        const DRec& st = sh->rec[si & 1];
+        if (si + 1 < b1) prefetch_rec(&sh->rec[(si + 1) & 1], P.recs + si + 1);
         const unsigned long long t_start = gtimer();
         unsigned long long waited = 0;
         if (st.flags & 2) {
-            // reads or writes what an earlier step of this threadblock touched
-            while (c.tail < c.head)
-                if (!ctl_drain_one(c, si)) {
-                    ctl_publish_cmd(c, 2);
-                    return;
-                }
-        }
-        for (int k = 0; k < st.dep_count; ++k) {
-            const DDep d = P.deps[st.dep_begin + k];
-            if (!ctl_wait(c, P.counters + d.counter, (unsigned long long)(P.exec * P.m + d.value), si, WAIT_DEP,
-                          waited)) {
-                ctl_publish_cmd(c, 2);
+            // reads or writes what an earlier step of this threadblock
+            // touched: let every handed-out slot finish first
+            if (head > 0 && !mbar_wait(&sh->freed[(head - 1) % kQ], (unsigned)(((head - 1) / kQ) & 1),
+                                       4 * P.timeout_ns)) {
+                record_timeout(P, si, WAIT_DONE);
+                publish_cmd(2);
                 return;
             }
         }
-        const int es = (in.dtype == CCL_BF16 || in.dtype == CCL_F16) ? 2 : 4;
-        const DLink* Lin = in.link_in >= 0 ? P.links + in.link_in : nullptr;
-        const DLink* Lout = in.link_out >= 0 ? P.links + in.link_out : nullptr;
+        for (int k = 0; k < st.dep_count; ++k) {
+            const DDep d = P.deps[st.dep_begin + k];
+            if (!wait_flags(P, P.counters + d.counter, (unsigned long long)(P.exec * P.m + d.value), nullptr, 0, si,
+                            WAIT_DEP, waited)) {
+                publish_cmd(2);
+                return;
+            }
+        }
+        const int es = (st.dtype == CCL_BF16 || st.dtype == CCL_F16) ? 2 : 4;
+        const DLink* Lin = st.link_in >= 0 ? P.links + st.link_in : nullptr;
+        const DLink* Lout = st.link_out >= 0 ? P.links + st.link_out : nullptr;
         const unsigned long long base_in = Lin ? (unsigned long long)(P.exec * Lin->total) : 0;
         const unsigned long long base_out = Lout ? (unsigned long long)(P.exec * Lout->total) : 0;
         const long long slot_elems = (Lin || Lout) ? P.slot_bytes / es : (st.nelem > 0 ? st.nelem : 1);
         const int nslots = st.nslots > 0 ? st.nslots : 1;
-        const bool red = in.kind == CCL_I_REDUCE || in.kind == CCL_I_RRC || in.kind == CCL_I_RRS || in.kind == CCL_I_RRCS;
-        const char* srcb = in.src_buf >= 0 ? P.bufs[in.src_buf][in.src_rank] + (in.src_off + st.elem_off) * es : nullptr;
-        const char* locb = in.loc_buf >= 0 ? P.bufs[in.loc_buf][in.loc_rank] + (in.loc_off + st.elem_off) * es : nullptr;
-        char* dstb = in.dst_buf >= 0 ? P.bufs[in.dst_buf][in.dst_rank] + (in.dst_off + st.elem_off) * es : nullptr;
+        const int red = st.kind == CCL_I_REDUCE || st.kind == CCL_I_RRC || st.kind == CCL_I_RRS || st.kind == CCL_I_RRCS;
+        const char* srcb = st.src_buf >= 0 ? P.bufs[st.src_buf][st.src_rank] + st.src_off * es : nullptr;
+        const char* locb = st.loc_buf >= 0 ? P.bufs[st.loc_buf][st.loc_rank] + st.loc_off * es : nullptr;
+        char* dstb = st.dst_buf >= 0 ? P.bufs[st.dst_buf][st.dst_rank] + st.dst_off * es : nullptr;
+        const bool post = !(st.flags & 1);
         for (int k = 0; k < nslots; ++k) {
-            if (c.head - c.tail == kQ && !ctl_drain_one(c, si)) {
-                ctl_publish_cmd(c, 2);
+            const int q = head % kQ;
+            if (head >= kQ && !mbar_wait(&sh->freed[q], (unsigned)(((head / kQ) - 1) & 1), 4 * P.timeout_ns)) {
+                record_timeout(P, si, WAIT_DONE);
+                publish_cmd(2);
                 return;
             }
             const unsigned long long sin = base_in + st.seq_in + k;
             const unsigned long long sout = base_out + st.seq_out + k;
-            int ok = 1;
-            if (Lin) ok = ctl_wait(c, P.flags + Lin->flag_base + (int)(sin % P.S), sin + 1, si, WAIT_FULL, waited);
-            if (ok && Lout && sout + 1 > (unsigned long long)P.S)
-                ok = ctl_wait(c, P.flags + Lout->flag_base + P.S + (int)(sout % P.S), sout + 1 - P.S, si, WAIT_FREE,
-                              waited);
-            if (!ok) {
-                ctl_publish_cmd(c, 2);
+            const bool need_free = Lout && sout + 1 > (unsigned long long)P.S;
+            if ((Lin || need_free) &&
+                !wait_flags(P, Lin ? P.flags + Lin->flag_base + (int)(sin % P.S) : nullptr, sin + 1,
+                            need_free ? P.flags + Lout->flag_base + P.S + (int)(sout % P.S) : nullptr,
+                            sout + 1 - P.S, si, WAIT_FULL, waited)) {
+                publish_cmd(2);
                 return;
             }
             const long long e0 = (long long)k * slot_elems;
             long long n = st.nelem - e0;
             if (n > slot_elems) n = slot_elems;
             if (n < 0) n = 0;
-            const int q = c.head % kQ;
             char* slot_out = Lout ? P.fifo + Lout->slot_base + (long long)(sout % P.S) * P.slot_bytes : nullptr;
             SlotOp& op = sh->op[q];
-            if (Lin && in.kind != CCL_I_REDUCE) {
+            if (Lin && st.kind != CCL_I_REDUCE) {
                 op.a = P.fifo + Lin->slot_base + (long long)(sin % P.S) * P.slot_bytes;
                 op.as = 0;
             } else {
                 op.a = srcb + e0 * es;
-                op.as = in.src_buf == CCL_BUF_IN;
+                op.as = st.src_buf == CCL_BUF_IN;
             }
             op.b = locb ? locb + e0 * es : nullptr;
-            op.bs = in.loc_buf == CCL_BUF_IN;
+            op.bs = st.loc_buf == CCL_BUF_IN;
             if (dstb) {
                 op.o1 = dstb + e0 * es;
-                op.o1s = in.dst_buf == CCL_BUF_OUT;
+                op.o1s = st.dst_buf == CCL_BUF_OUT;
                 op.o2 = slot_out;
             } else {
                 op.o1 = slot_out;
@@ -262,10 +249,9 @@ __device__ void control_thread(const KParams& P, CtlShared* sh, int b0, int b1)
             }
             op.n = n;
             op.red = red;
-            op.dtype = in.dtype;
+            op.dtype = st.dtype;
             op.cmd = 0;
             Release& r = sh->rel[q];
-            const bool post = !(st.flags & 1);
             r.consumed = (Lin && post) ? P.flags + Lin->flag_base + P.S + (int)(sin % P.S) : nullptr;
             r.consumed_v = sin + 1;
             r.full = (Lout && post) ? P.flags + Lout->flag_base + (int)(sout % P.S) : nullptr;
@@ -277,35 +263,58 @@ __device__ void control_thread(const KParams& P, CtlShared* sh, int b0, int b1)
             r.t_start = t_start;
             r.waited = waited;
             mbar_arrive(&sh->ready[q]);
-            ++c.head;
-            ctl_drain(c);
+            ++head;
         }
     }
-    while (c.tail < c.head)
-        if (!ctl_drain_one(c, b1 - 1)) break;
-    ctl_publish_cmd(c, 1);
+    publish_cmd(1);
+}
+
+__device__ void releaser(const KParams& P, CtlShared* sh)
+{
+    const unsigned long long limit = 4 * P.timeout_ns;
+    for (int j = 0;;) {
+        int q = j % kQ;
+        unsigned par = (unsigned)((j / kQ) & 1);
+        if (!mbar_wait(&sh->ready[q], par, limit)) return;
+        if (sh->op[q].cmd != 0) return;
+        if (!mbar_wait(&sh->done[q], par, limit)) return;
+        // batch every further slot that is already finished
+        int n = 1;
+        while (n < kQ) {
+            const int q2 = (j + n) % kQ;
+            const unsigned p2 = (unsigned)(((j + n) / kQ) & 1);
+            if (!mbar_test(&sh->ready[q2], p2) || sh->op[q2].cmd != 0 || !mbar_test(&sh->done[q2], p2)) break;
+            ++n;
+        }
+        fence_acq_rel_gpu();
+        for (int i = 0; i < n; ++i) {
+            const Release& r = sh->rel[(j + i) % kQ];
+            if (r.consumed) st_relaxed(r.consumed, r.consumed_v);
+            if (r.full) st_relaxed(r.full, r.full_v);
+            if (r.last) {
+                if (r.counter) st_relaxed(r.counter, r.counter_v);
+                if (P.timeline) {
+                    unsigned long long* tl = P.timeline + 3ll * r.si;
+                    tl[0] = r.t_start;
+                    tl[1] = r.waited;
+                    tl[2] = gtimer();
+                }
+            }
+        }
+        for (int i = 0; i < n; ++i) mbar_arrive(&sh->freed[(j + i) % kQ]);
+        j += n;
+    }
 }
 
 __device__ void data_warps(const KParams& P, CtlShared* sh)
 {
-    const int tid = threadIdx.x - 32;
-    const int T = blockDim.x - 32;
+    const int tid = threadIdx.x - 64;
+    const int T = blockDim.x - 64;
     const int lane = threadIdx.x & 31;
+    const unsigned long long limit = 4 * P.timeout_ns;
     for (int j = 0;; ++j) {
         const int q = j % kQ;
-        const unsigned par = (unsigned)((j / kQ) & 1);
-        unsigned spins = 0;
-        unsigned long long t0 = 0;
-        while (!mbar_test(&sh->ready[q], par)) {
-            if ((++spins & 255) == 0) {
-                unsigned long long now = gtimer();
-                if (!t0) t0 = now;
-                // the control thread waits at most timeout_ns per flag; give it
-                // a generous margin before giving up on it
-                else if (now - t0 > 4 * P.timeout_ns) return;
-            }
-            if (spins > 32) __nanosleep(20);
-        }
+        if (!mbar_wait(&sh->ready[q], (unsigned)((j / kQ) & 1), limit)) return;
         const SlotOp op = sh->op[q];
         if (op.cmd != 0) return;
         if (op.n > 0) {
@@ -323,18 +332,23 @@ __device__ void data_warps(const KParams& P, CtlShared* sh)
 
 __global__ void __launch_bounds__(1024, 1) ccl_exec_kernel(const __grid_constant__ KParams P)
 {
-    __shared__ CtlShared sh;
+    __shared__ __align__(16) CtlShared sh;
     const int b0 = P.tb_begin[blockIdx.x], b1 = P.tb_begin[blockIdx.x + 1];
     const int nwarps = blockDim.x / 32;
     if (threadIdx.x == 0) {
         for (int q = 0; q < kQ; ++q) {
             mbar_init(&sh.ready[q], 1);
-            mbar_init(&sh.done[q], nwarps - 1);
+            mbar_init(&sh.done[q], nwarps - 2);
+            mbar_init(&sh.freed[q], 1);
         }
     }
     __syncthreads();
     if (threadIdx.x < 32) {
-        if (threadIdx.x == 0) control_thread(P, &sh, b0, b1);
+        if (threadIdx.x == 0) issuer(P, &sh, b0, b1);
+        return;
+    }
+    if (threadIdx.x < 64) {
+        if (threadIdx.x == 32) releaser(P, &sh);
         return;
     }
     data_warps(P, &sh);
@@ -580,8 +594,8 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
         if (e == cudaSuccess)
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ccl::ccl_exec_kernel, img.nthreads, 0);
         if (e != cudaSuccess) { delete p; return ccl::cuda_fail(e, "occupancy query"); }
-        if ((int64_t)per_sm * nsm >= img.ntb || (opts && opts->nthreads) || img.nthreads <= 64) break;
-        img.nthreads /= 2;
+        if ((int64_t)per_sm * nsm >= img.ntb || (opts && opts->nthreads) || img.nthreads <= 128) break;
+        img.nthreads = img.nthreads / 2 >= 128 ? img.nthreads / 2 : 128;
     }
     if ((int64_t)per_sm * nsm < img.ntb) {
         std::string msg = "plan needs " + std::to_string(img.ntb) + " co-resident threadblocks of " +
@@ -591,15 +605,13 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
     }
 
     // one blob for the read-only tables
-    size_t o_instr = 0;
-    size_t o_steps = align_up(o_instr + img.instrs.size() * sizeof(ccl::DInstr), 256);
-    size_t o_tb = align_up(o_steps + img.steps.size() * sizeof(ccl::DStep), 256);
+    size_t o_recs = 0;
+    size_t o_tb = align_up(o_recs + img.recs.size() * sizeof(ccl::DRec), 256);
     size_t o_links = align_up(o_tb + img.tb_begin.size() * sizeof(int32_t), 256);
     size_t o_deps = align_up(o_links + img.links.size() * sizeof(ccl::DLink), 256);
     size_t blob = align_up(o_deps + std::max<size_t>(1, img.deps.size()) * sizeof(ccl::DDep), 256);
     std::vector<char> h(blob, 0);
-    std::memcpy(h.data() + o_instr, img.instrs.data(), img.instrs.size() * sizeof(ccl::DInstr));
-    std::memcpy(h.data() + o_steps, img.steps.data(), img.steps.size() * sizeof(ccl::DStep));
+    std::memcpy(h.data() + o_recs, img.recs.data(), img.recs.size() * sizeof(ccl::DRec));
     std::memcpy(h.data() + o_tb, img.tb_begin.data(), img.tb_begin.size() * sizeof(int32_t));
     std::memcpy(h.data() + o_links, img.links.data(), img.links.size() * sizeof(ccl::DLink));
     if (!img.deps.empty()) std::memcpy(h.data() + o_deps, img.deps.data(), img.deps.size() * sizeof(ccl::DDep));
@@ -632,8 +644,7 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
 #undef PLAN_TRY
 
     ccl::KParams& k = p->kp;
-    k.instrs = reinterpret_cast<const ccl::DInstr*>(p->d_blob + o_instr);
-    k.steps = reinterpret_cast<const ccl::DStep*>(p->d_blob + o_steps);
+    k.recs = reinterpret_cast<const ccl::DRec*>(p->d_blob + o_recs);
     k.tb_begin = reinterpret_cast<const int32_t*>(p->d_blob + o_tb);
     k.links = reinterpret_cast<const ccl::DLink*>(p->d_blob + o_links);
     k.deps = reinterpret_cast<const ccl::DDep*>(p->d_blob + o_deps);
@@ -790,8 +801,9 @@ ccl_status_t ccl_plan_debug_drop_signal(ccl_plan_t p, int32_t tb, int32_t step)
     int k = img.tb_begin[tb] + step;
     if (step < 0 || k >= img.tb_begin[tb + 1]) return ccl::fail(CCL_ERR_INVALID_ARG, "step out of range");
     img.steps[k].flags |= 1;
-    ccl::DStep* dst = const_cast<ccl::DStep*>(p->kp.steps) + k;
-    CUDA_TRY(cudaMemcpy(dst, &img.steps[k], sizeof(ccl::DStep), cudaMemcpyHostToDevice), "patch step");
+    img.recs[k].flags |= 1;
+    ccl::DRec* dst = const_cast<ccl::DRec*>(p->kp.recs) + k;
+    CUDA_TRY(cudaMemcpy(dst, &img.recs[k], sizeof(ccl::DRec), cudaMemcpyHostToDevice), "patch step");
     return CCL_OK;
 }
 

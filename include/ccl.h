@@ -180,8 +180,10 @@ typedef enum { CCL_MB_AUTO = 0, CCL_MB_ALGO = 1, CCL_MB_TASK = 2, CCL_MB_SEGMENT
  *   channels    : parallelization factor; every chunk range is split into
  *                 `channels` contiguous 16-byte-granular pieces, each with its
  *                 own links and threadblocks (MSCCLang report, §III.1, §IV.1).
- *   nthreads    : threads per threadblock (64..1024, multiple of 32); 0 =
- *                 512, halved until every threadblock can be co-resident.
+ *   nthreads    : threads per threadblock (96..1024, multiple of 32: one
+ *                 issuing warp, one releasing warp, the rest move data);
+ *                 0 = 512, halved (down to 128) until every threadblock can
+ *                 be co-resident.
  *   slot_bytes  : FIFO slot size (multiple of 16).
  *   fifo_slots  : slots per link FIFO (>= 2).
  *   microbatches: pieces every channel range is cut into; 0 = the smallest
