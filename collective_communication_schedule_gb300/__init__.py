@@ -66,7 +66,7 @@ class PlanOpts(ctypes.Structure):
     _fields_ = [("channels", ctypes.c_int32), ("nthreads", ctypes.c_int32), ("slot_bytes", ctypes.c_int64),
                 ("fifo_slots", ctypes.c_int32), ("microbatches", ctypes.c_int32), ("scheduler", ctypes.c_int32),
                 ("tb_alloc", ctypes.c_int32), ("mb_order", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
-                ("instrument", ctypes.c_int32)]
+                ("instrument", ctypes.c_int32), ("tile_bytes", ctypes.c_int64)]
 
 
 class PlanStats(ctypes.Structure):
@@ -77,7 +77,8 @@ class PlanStats(ctypes.Structure):
                 ("nsubpipelines", ctypes.c_int32), ("microbatches", ctypes.c_int32), ("mb_order", ctypes.c_int32),
                 ("channels", ctypes.c_int32), ("nthreads", ctypes.c_int32), ("fifo_slots", ctypes.c_int32),
                 ("slot_bytes", ctypes.c_int64), ("fifo_bytes", ctypes.c_int64), ("device_bytes", ctypes.c_int64),
-                ("compile_ms", ctypes.c_double)]
+                ("compile_ms", ctypes.c_double), ("tile_bytes", ctypes.c_int64), ("stages", ctypes.c_int32),
+                ("pad", ctypes.c_int32)]
 
 
 class TuneOpts(ctypes.Structure):

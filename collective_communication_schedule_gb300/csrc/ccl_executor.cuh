@@ -32,8 +32,9 @@ struct KParams {
     long long m;
     long long slot_bytes;
     unsigned long long timeout_ns;
+    long long tile_bytes;          // bytes per tile handed to the data path
     int S;
-    int pad;
+    int ns;                        // shared-memory stages of the bulk path (0: off)
     char* bufs[3][CCL_MAX_RANKS];
 };
 

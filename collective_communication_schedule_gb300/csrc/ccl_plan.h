@@ -84,6 +84,8 @@ struct PlanImage {
     int32_t nthreads = 512;
     int32_t S = 4;
     int64_t slot_bytes = 0;
+    int64_t tile_bytes = 0;          // tile of the data path
+    int32_t ns = 0;                  // shared-memory stages of the bulk path (set at plan creation)
     int64_t fifo_bytes = 0;
     int32_t m = 1;
     int32_t channels = 1;

@@ -349,6 +349,7 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     img->mb_order = order;
     img->S = S;
     img->slot_bytes = o.slot_bytes;
+    img->tile_bytes = o.tile_bytes;
     img->nthreads = o.nthreads;
     img->dtype = dtype;
     img->esize = es;
@@ -690,8 +691,10 @@ ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const 
     if (ce <= 0) return fail(CCL_ERR_INVALID_ARG, "chunk_elems must be positive");
     if (dtype < CCL_F32 || dtype > CCL_I32) return fail(CCL_ERR_INVALID_ARG, "unknown dtype");
     if (o.channels < 1 || o.channels > 256) return fail(CCL_ERR_INVALID_ARG, "channels must be in 1..256");
-    if (o.nthreads < 96 || o.nthreads > 1024 || o.nthreads % 32)
-        return fail(CCL_ERR_INVALID_ARG, "nthreads must be a multiple of 32 in 96..1024");
+    if (o.nthreads < 128 || o.nthreads > 1024 || o.nthreads % 32)
+        return fail(CCL_ERR_INVALID_ARG, "nthreads must be a multiple of 32 in 128..1024");
+    if (o.tile_bytes < 16 || o.tile_bytes % 16 || o.tile_bytes > 65536)
+        return fail(CCL_ERR_INVALID_ARG, "tile_bytes must be a multiple of 16 in 16..65536");
     if (o.slot_bytes < 16 || o.slot_bytes % 16) return fail(CCL_ERR_INVALID_ARG, "slot_bytes must be a positive multiple of 16");
     if (o.fifo_slots < 2 || o.fifo_slots > 64) return fail(CCL_ERR_INVALID_ARG, "fifo_slots must be in 2..64");
     if (o.microbatches < 0 || o.microbatches > 65536) return fail(CCL_ERR_INVALID_ARG, "microbatches out of range");

@@ -43,27 +43,29 @@ static ccl_status_t cuda_fail(cudaError_t e, const char* what)
 namespace ccl {
 
 // ----------------------------------------------------------------------
-// Warp-specialised executor.  Three roles per CTA:
+// Warp-specialised executor.  Four roles per CTA:
 //
-//  * issuer (warp 0, lane 0) walks the threadblock program.  For every slot
-//    it waits (bounded) for the step's dependency counters, the incoming
+//  * issuer (warp 0, lane 0) walks the threadblock program.  Per FIFO slot
+//    it waits (bounded) for the step's dependency counters, for the incoming
 //    slot to be full and the outgoing slot to be free -- both flags polled
 //    with relaxed loads in one round trip, then one acquire fence -- and
-//    hands the slot's operand addresses to the data warps through a ring of
+//    hands the slot out as tiles of at most `tile` bytes through a ring of
 //    kQ shared-memory descriptors guarded by mbarriers ("ready").  The next
-//    step's 128-byte record is prefetched while the current one runs.
-//  * data warps (warps 2..) move each slot with 16-byte loads and stores and
-//    arrive on "done".
-//  * releaser (warp 1, lane 0) takes finished slots in order, issues one
-//    release fence per batch and then posts the consumed / full flags and the
-//    step's dependency counter with relaxed stores, and frees the descriptor
-//    ("freed").  The data warps' stores reach it through the CTA-scope
-//    release / acquire of the mbarrier, so the gpu-scope fence covers them.
-//
-// The issuer can run kQ slots ahead of the data warps, and releases never
-// wait behind the issuer's waits on other threadblocks.
+//    step's 128-byte record is prefetched with cp.async.
+//  * TMA thread (warp 2, lane 0) moves every 16-byte-aligned tile with bulk
+//    copies: global -> shared stage (mbarrier complete_tx), then shared ->
+//    global to the destination and/or the outgoing slot (bulk groups).  Up to
+//    `ns` tiles are in flight; a tile's stage is reused once its stores have
+//    read it, and a tile counts as done once its stores are complete.
+//  * data warps (warps 3..) add the two operands of reduce tiles in shared
+//    memory, and move unaligned tiles with 16-byte / element loads and stores.
+//  * releaser (warp 1, lane 0) takes finished tiles in order, issues one
+//    release fence per batch and posts the flags and counters carried by a
+//    slot's last tile with relaxed stores, then frees the descriptor.
 // ----------------------------------------------------------------------
-constexpr int kQ = 8;
+constexpr int kQ = 16;     // tile descriptors in flight
+constexpr int kNSMax = 8;  // shared-memory stages
+constexpr int kRetireDepth = 2;
 
 struct SlotOp {
     const char* a;      // data in: incoming slot or source buffer
@@ -72,7 +74,8 @@ struct SlotOp {
     char* o2;           // outgoing slot when a destination is also written
     long long n;        // elements
     int red, dtype;
-    int as, bs, o1s;    // streaming cache hints
+    int as, bs, o1s;    // streaming cache hints (register path)
+    int bulk;           // moved by the TMA thread
     int cmd;            // 0 move, 1 end, 2 abort
 };
 
@@ -83,7 +86,7 @@ struct Release {
     unsigned long long consumed_v, full_v, counter_v;
     unsigned long long t_start, waited;
     int si;
-    int last;                      // last slot of its step
+    int last;                      // last tile of its step
 };
 
 struct CtlShared {
@@ -91,8 +94,11 @@ struct CtlShared {
     SlotOp op[kQ];
     Release rel[kQ];
     unsigned long long ready[kQ];
-    unsigned long long done[kQ];
+    unsigned long long done_g[kQ];      // data warps finished an unaligned tile
+    unsigned long long done_b[kQ];      // TMA thread finished a bulk tile
     unsigned long long freed[kQ];
+    unsigned long long full[kNSMax];    // stage loaded
+    unsigned long long computed[kNSMax];// reduce stage summed
 };
 
 __device__ __forceinline__ void record_timeout(const KParams& P, int si, int reason)
@@ -120,7 +126,7 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned par,
     return true;
 }
 
-// bounded wait until *a >= va and *b >= vb (b may be null), polled with
+// bounded wait until *a >= va and *b >= vb (either may be null), polled with
 // relaxed loads issued together, followed by one acquire fence
 __device__ bool wait_flags(const KParams& P, const unsigned long long* a, unsigned long long va,
                            const unsigned long long* b, unsigned long long vb, int si, int reason,
@@ -158,17 +164,18 @@ __device__ __forceinline__ void prefetch_rec(DRec* dst, const DRec* src)
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
+__device__ __forceinline__ bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
 __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
 {
     int head = 0;
+    const unsigned long long limit = 4 * P.timeout_ns;
     auto publish_cmd = [&](int cmd) {
         const int q = head % kQ;
-        if (head >= kQ) mbar_wait(&sh->freed[q], (unsigned)(((head / kQ) - 1) & 1), 4 * P.timeout_ns);
+        if (head >= kQ) mbar_wait(&sh->freed[q], (unsigned)(((head / kQ) - 1) & 1), limit);
         sh->op[q].cmd = cmd;
         mbar_arrive(&sh->ready[q]);
     };
-    // step records are double-buffered in shared memory: the record of the
-    // next step is copied asynchronously (cp.async) while this one runs
     if (b0 < b1) prefetch_rec(&sh->rec[b0 & 1], P.recs + b0);
     for (int si = b0; si < b1; ++si) {
         asm volatile("cp.async.wait_all;" ::: "memory");
@@ -176,15 +183,13 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
         if (si + 1 < b1) prefetch_rec(&sh->rec[(si + 1) & 1], P.recs + si + 1);
         const unsigned long long t_start = gtimer();
         unsigned long long waited = 0;
-        if (st.flags & 2) {
-            // reads or writes what an earlier step of this threadblock
-            // touched: let every handed-out slot finish first
-            if (head > 0 && !mbar_wait(&sh->freed[(head - 1) % kQ], (unsigned)(((head - 1) / kQ) & 1),
-                                       4 * P.timeout_ns)) {
-                record_timeout(P, si, WAIT_DONE);
-                publish_cmd(2);
-                return;
-            }
+        if ((st.flags & 2) && head > 0 &&
+            !mbar_wait(&sh->freed[(head - 1) % kQ], (unsigned)(((head - 1) / kQ) & 1), limit)) {
+            // reads or writes what an earlier step of this threadblock touched:
+            // every handed-out tile must be finished first
+            record_timeout(P, si, WAIT_DONE);
+            publish_cmd(2);
+            return;
         }
         for (int k = 0; k < st.dep_count; ++k) {
             const DDep d = P.deps[st.dep_begin + k];
@@ -199,20 +204,19 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
         const DLink* Lout = st.link_out >= 0 ? P.links + st.link_out : nullptr;
         const unsigned long long base_in = Lin ? (unsigned long long)(P.exec * Lin->total) : 0;
         const unsigned long long base_out = Lout ? (unsigned long long)(P.exec * Lout->total) : 0;
-        const long long slot_elems = (Lin || Lout) ? P.slot_bytes / es : (st.nelem > 0 ? st.nelem : 1);
-        const int nslots = st.nslots > 0 ? st.nslots : 1;
+        const long long slot_elems = P.slot_bytes / es;
+        const long long tile_elems = P.tile_bytes / es;
+        const bool linked = Lin || Lout;
+        // FIFO slots of a linked step; local steps are cut into tiles directly
+        const long long nslots = linked ? (st.nslots > 0 ? st.nslots : 1)
+                                        : (st.nelem > 0 ? (st.nelem + tile_elems - 1) / tile_elems : 1);
+        const long long span = linked ? slot_elems : tile_elems;
         const int red = st.kind == CCL_I_REDUCE || st.kind == CCL_I_RRC || st.kind == CCL_I_RRS || st.kind == CCL_I_RRCS;
         const char* srcb = st.src_buf >= 0 ? P.bufs[st.src_buf][st.src_rank] + st.src_off * es : nullptr;
         const char* locb = st.loc_buf >= 0 ? P.bufs[st.loc_buf][st.loc_rank] + st.loc_off * es : nullptr;
         char* dstb = st.dst_buf >= 0 ? P.bufs[st.dst_buf][st.dst_rank] + st.dst_off * es : nullptr;
         const bool post = !(st.flags & 1);
-        for (int k = 0; k < nslots; ++k) {
-            const int q = head % kQ;
-            if (head >= kQ && !mbar_wait(&sh->freed[q], (unsigned)(((head / kQ) - 1) & 1), 4 * P.timeout_ns)) {
-                record_timeout(P, si, WAIT_DONE);
-                publish_cmd(2);
-                return;
-            }
+        for (long long k = 0; k < nslots; ++k) {
             const unsigned long long sin = base_in + st.seq_in + k;
             const unsigned long long sout = base_out + st.seq_out + k;
             const bool need_free = Lout && sout + 1 > (unsigned long long)P.S;
@@ -223,47 +227,66 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
                 publish_cmd(2);
                 return;
             }
-            const long long e0 = (long long)k * slot_elems;
+            const long long e0 = k * span;
             long long n = st.nelem - e0;
-            if (n > slot_elems) n = slot_elems;
+            if (n > span) n = span;
             if (n < 0) n = 0;
+            const char* slot_in = Lin ? P.fifo + Lin->slot_base + (long long)(sin % P.S) * P.slot_bytes : nullptr;
             char* slot_out = Lout ? P.fifo + Lout->slot_base + (long long)(sout % P.S) * P.slot_bytes : nullptr;
-            SlotOp& op = sh->op[q];
-            if (Lin && st.kind != CCL_I_REDUCE) {
-                op.a = P.fifo + Lin->slot_base + (long long)(sin % P.S) * P.slot_bytes;
-                op.as = 0;
-            } else {
-                op.a = srcb + e0 * es;
-                op.as = st.src_buf == CCL_BUF_IN;
+            const long long ntiles = n > 0 ? (n + tile_elems - 1) / tile_elems : 1;
+            for (long long u = 0; u < ntiles; ++u) {
+                const int q = head % kQ;
+                if (head >= kQ && !mbar_wait(&sh->freed[q], (unsigned)(((head / kQ) - 1) & 1), limit)) {
+                    record_timeout(P, si, WAIT_DONE);
+                    publish_cmd(2);
+                    return;
+                }
+                const long long t0 = u * tile_elems;
+                long long tn = n - t0;
+                if (tn > tile_elems) tn = tile_elems;
+                if (tn < 0) tn = 0;
+                const long long off = (e0 + t0) * es;   // byte offset in the step's buffers
+                const long long soff = t0 * es;         // byte offset in the slot
+                SlotOp& op = sh->op[q];
+                if (Lin && st.kind != CCL_I_REDUCE) {
+                    op.a = slot_in + soff;
+                    op.as = 0;
+                } else {
+                    op.a = srcb + off;
+                    op.as = st.src_buf == CCL_BUF_IN;
+                }
+                op.b = locb ? locb + off : nullptr;
+                op.bs = st.loc_buf == CCL_BUF_IN;
+                if (dstb) {
+                    op.o1 = dstb + off;
+                    op.o1s = st.dst_buf == CCL_BUF_OUT;
+                    op.o2 = slot_out ? slot_out + soff : nullptr;
+                } else {
+                    op.o1 = slot_out + soff;
+                    op.o1s = 0;
+                    op.o2 = nullptr;
+                }
+                op.n = tn;
+                op.red = red;
+                op.dtype = st.dtype;
+                op.bulk = P.ns > 0 && tn > 0 && ((tn * es) & 15) == 0 && aligned16(op.a) && aligned16(op.o1) &&
+                          (!op.o2 || aligned16(op.o2)) && (!red || aligned16(op.b));
+                op.cmd = 0;
+                Release& r = sh->rel[q];
+                const bool last_tile = u == ntiles - 1;
+                r.consumed = (Lin && post && last_tile) ? P.flags + Lin->flag_base + P.S + (int)(sin % P.S) : nullptr;
+                r.consumed_v = sin + 1;
+                r.full = (Lout && post && last_tile) ? P.flags + Lout->flag_base + (int)(sout % P.S) : nullptr;
+                r.full_v = sout + 1;
+                r.last = last_tile && k == nslots - 1;
+                r.counter = st.signal >= 0 ? P.counters + st.signal : nullptr;
+                r.counter_v = (unsigned long long)(P.exec * P.m + st.mb + 1);
+                r.si = si;
+                r.t_start = t_start;
+                r.waited = waited;
+                mbar_arrive(&sh->ready[q]);
+                ++head;
             }
-            op.b = locb ? locb + e0 * es : nullptr;
-            op.bs = st.loc_buf == CCL_BUF_IN;
-            if (dstb) {
-                op.o1 = dstb + e0 * es;
-                op.o1s = st.dst_buf == CCL_BUF_OUT;
-                op.o2 = slot_out;
-            } else {
-                op.o1 = slot_out;
-                op.o1s = 0;
-                op.o2 = nullptr;
-            }
-            op.n = n;
-            op.red = red;
-            op.dtype = st.dtype;
-            op.cmd = 0;
-            Release& r = sh->rel[q];
-            r.consumed = (Lin && post) ? P.flags + Lin->flag_base + P.S + (int)(sin % P.S) : nullptr;
-            r.consumed_v = sin + 1;
-            r.full = (Lout && post) ? P.flags + Lout->flag_base + (int)(sout % P.S) : nullptr;
-            r.full_v = sout + 1;
-            r.last = k == nslots - 1;
-            r.counter = st.signal >= 0 ? P.counters + st.signal : nullptr;
-            r.counter_v = (unsigned long long)(P.exec * P.m + st.mb + 1);
-            r.si = si;
-            r.t_start = t_start;
-            r.waited = waited;
-            mbar_arrive(&sh->ready[q]);
-            ++head;
         }
     }
     publish_cmd(1);
@@ -277,13 +300,14 @@ __device__ void releaser(const KParams& P, CtlShared* sh)
         unsigned par = (unsigned)((j / kQ) & 1);
         if (!mbar_wait(&sh->ready[q], par, limit)) return;
         if (sh->op[q].cmd != 0) return;
-        if (!mbar_wait(&sh->done[q], par, limit)) return;
-        // batch every further slot that is already finished
+        if (!mbar_wait(sh->op[q].bulk ? &sh->done_b[q] : &sh->done_g[q], par, limit)) return;
+        // batch every further tile that is already finished
         int n = 1;
         while (n < kQ) {
             const int q2 = (j + n) % kQ;
             const unsigned p2 = (unsigned)(((j + n) / kQ) & 1);
-            if (!mbar_test(&sh->ready[q2], p2) || sh->op[q2].cmd != 0 || !mbar_test(&sh->done[q2], p2)) break;
+            if (!mbar_test(&sh->ready[q2], p2) || sh->op[q2].cmd != 0) break;
+            if (!mbar_test(sh->op[q2].bulk ? &sh->done_b[q2] : &sh->done_g[q2], p2)) break;
             ++n;
         }
         fence_acq_rel_gpu();
@@ -306,17 +330,145 @@ __device__ void releaser(const KParams& P, CtlShared* sh)
     }
 }
 
-__device__ void data_warps(const KParams& P, CtlShared* sh)
+// TMA thread: bulk copies of aligned tiles through the shared-memory stages
+__device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stages)
 {
-    const int tid = threadIdx.x - 64;
-    const int T = blockDim.x - 64;
+    const int NS = P.ns;
+    const long long T2 = 2 * P.tile_bytes;   // stage = operand a | operand b
+    const unsigned long long limit = 4 * P.timeout_ns;
+    struct Fly { int q, s, red, tnum; char* o1; char* o2; unsigned bytes; };
+    Fly fly[kNSMax];
+    int stage_grp[kNSMax];
+    for (int i = 0; i < kNSMax; ++i) stage_grp[i] = -1;
+    int cq[kNSMax + 1] = {};  // tiles stored, waiting for their stores to complete
+    int cg[kNSMax + 1] = {};
+    int c_head = 0, c_tail = 0;
+    int j = 0, t = 0, g = 0, f_head = 0, f_tail = 0;
+    bool ended = false;
+    auto retire = [&](int depth) {
+        // all but the newest `depth` store groups are complete
+        bulk_wait(depth);
+        bool any = false;
+        while (c_tail < c_head && cg[c_tail % (kNSMax + 1)] < g - depth) {
+            if (!any) { fence_proxy_async_global(); any = true; }
+            mbar_arrive(&sh->done_b[cq[c_tail % (kNSMax + 1)]]);
+            ++c_tail;
+        }
+    };
+    // leave only when no bulk copy still reads or writes this CTA's shared
+    // memory: wait (bounded) for every issued load, then for every store
+    auto leave = [&]() {
+        for (int i = f_tail; i < f_head; ++i) {
+            const Fly& e = fly[i % kNSMax];
+            mbar_wait(&sh->full[e.s], (unsigned)((e.tnum / NS) & 1), P.timeout_ns);
+        }
+        bulk_wait(0);
+    };
+    auto stage_wait = [&](unsigned long long* bar, unsigned par) {
+        unsigned spins = 0;
+        unsigned long long t0 = 0;
+        while (!mbar_test(bar, par)) {
+            if ((++spins & 127) == 0) {
+                if (*(volatile int*)P.status != 0) return false;
+                unsigned long long now = gtimer();
+                if (!t0) t0 = now;
+                else if (now - t0 > limit) return false;
+            }
+            if (spins > 32) __nanosleep(20);
+        }
+        return true;
+    };
+    while (true) {
+        // 1. start loads of newly handed-out aligned tiles while a stage is free
+        while (!ended && f_head - f_tail < NS) {
+            const int q = j % kQ;
+            if (!mbar_test(&sh->ready[q], (unsigned)((j / kQ) & 1))) break;
+            const SlotOp& op = sh->op[q];
+            if (op.cmd != 0) { ended = true; break; }
+            if (!op.bulk) { ++j; continue; }
+            const int s = t % NS;
+            if (stage_grp[s] >= 0) bulk_wait_read(g - stage_grp[s] - 1);
+            const int es = (op.dtype == CCL_BF16 || op.dtype == CCL_F16) ? 2 : 4;
+            const unsigned bytes = (unsigned)(op.n * es);
+            unsigned char* A = stages + s * T2;
+            fence_proxy_async_global();
+            mbar_arrive_expect_tx(&sh->full[s], op.red ? 2 * bytes : bytes);
+            bulk_load(A, op.a, bytes, &sh->full[s]);
+            if (op.red) bulk_load(A + P.tile_bytes, op.b, bytes, &sh->full[s]);
+            fly[f_head % kNSMax] = Fly{q, s, op.red, t, op.o1, op.o2, bytes};
+            ++f_head;
+            ++t;
+            ++j;
+        }
+        if (f_tail < f_head) {
+            // 2. store the oldest tile once loaded (copy) or summed (reduce)
+            const Fly e = fly[f_tail % kNSMax];
+            const unsigned par = (unsigned)((e.tnum / NS) & 1);
+            if (!stage_wait(e.red ? &sh->computed[e.s] : &sh->full[e.s], par)) {
+                leave();
+                return;
+            }
+            const unsigned char* A = stages + e.s * T2;
+            bulk_store(e.o1, A, e.bytes);
+            if (e.o2) bulk_store(e.o2, A, e.bytes);
+            bulk_commit();
+            stage_grp[e.s] = g;
+            cq[c_head % (kNSMax + 1)] = e.q;
+            cg[c_head % (kNSMax + 1)] = g;
+            ++c_head;
+            ++g;
+            ++f_tail;
+            if (c_head - c_tail > kRetireDepth) retire(kRetireDepth);
+        } else {
+            // 3. nothing in flight: finish every store, then wait for work
+            retire(0);
+            if (ended) return;
+            if (!stage_wait(&sh->ready[j % kQ], (unsigned)((j / kQ) & 1))) {
+                leave();
+                return;
+            }
+        }
+    }
+}
+
+__device__ void data_warps(const KParams& P, CtlShared* sh, unsigned char* stages)
+{
+    const int tid = threadIdx.x - 96;
+    const int T = blockDim.x - 96;
     const int lane = threadIdx.x & 31;
     const unsigned long long limit = 4 * P.timeout_ns;
+    const long long T2 = 2 * P.tile_bytes;
+    int t = 0;   // aligned tiles seen (same numbering as the TMA thread)
     for (int j = 0;; ++j) {
         const int q = j % kQ;
         if (!mbar_wait(&sh->ready[q], (unsigned)((j / kQ) & 1), limit)) return;
         const SlotOp op = sh->op[q];
         if (op.cmd != 0) return;
+        if (op.bulk) {
+            const int tn = t++;
+            const int s = tn % P.ns;
+            if (!op.red) {
+                // keep the stage's "computed" phases one per tile
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh->computed[s]);
+                continue;
+            }
+            if (!mbar_wait(&sh->full[s], (unsigned)((tn / P.ns) & 1), limit)) return;
+            uint4* A = reinterpret_cast<uint4*>(stages + s * T2);
+            const uint4* B = reinterpret_cast<const uint4*>(stages + s * T2 + P.tile_bytes);
+            const int es = (op.dtype == CCL_BF16 || op.dtype == CCL_F16) ? 2 : 4;
+            const int nv = (int)(op.n * es / 16);
+            switch (op.dtype) {
+            case CCL_F32: for (int v = tid; v < nv; v += T) A[v] = vadd<CCL_F32>(A[v], B[v]); break;
+            case CCL_BF16: for (int v = tid; v < nv; v += T) A[v] = vadd<CCL_BF16>(A[v], B[v]); break;
+            case CCL_F16: for (int v = tid; v < nv; v += T) A[v] = vadd<CCL_F16>(A[v], B[v]); break;
+            default: for (int v = tid; v < nv; v += T) A[v] = vadd<CCL_I32>(A[v], B[v]); break;
+            }
+            fence_proxy_async_smem();   // the sums are read next by bulk stores
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh->computed[s]);
+            continue;
+        }
         if (op.n > 0) {
             switch (op.dtype) {
             case CCL_F32: move_part<CCL_F32>(op.red, op.a, op.as, op.b, op.bs, op.o1, op.o1s, op.o2, op.n, tid, T); break;
@@ -326,32 +478,40 @@ __device__ void data_warps(const KParams& P, CtlShared* sh)
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->done[q]);
+        if (lane == 0) mbar_arrive(&sh->done_g[q]);
     }
 }
 
 __global__ void __launch_bounds__(1024, 1) ccl_exec_kernel(const __grid_constant__ KParams P)
 {
     __shared__ __align__(16) CtlShared sh;
+    extern __shared__ __align__(128) unsigned char stages[];
     const int b0 = P.tb_begin[blockIdx.x], b1 = P.tb_begin[blockIdx.x + 1];
     const int nwarps = blockDim.x / 32;
     if (threadIdx.x == 0) {
         for (int q = 0; q < kQ; ++q) {
             mbar_init(&sh.ready[q], 1);
-            mbar_init(&sh.done[q], nwarps - 2);
+            mbar_init(&sh.done_g[q], nwarps - 3);
+            mbar_init(&sh.done_b[q], 1);
             mbar_init(&sh.freed[q], 1);
         }
+        for (int s = 0; s < kNSMax; ++s) {
+            mbar_init(&sh.full[s], 1);
+            mbar_init(&sh.computed[s], nwarps - 3);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
-        if (threadIdx.x == 0) issuer(P, &sh, b0, b1);
+    const int warp = threadIdx.x >> 5;
+    if (warp < 3) {
+        if ((threadIdx.x & 31) == 0) {
+            if (warp == 0) issuer(P, &sh, b0, b1);
+            else if (warp == 1) releaser(P, &sh);
+            else if (P.ns > 0) tma_thread(P, &sh, stages);
+        }
         return;
     }
-    if (threadIdx.x < 64) {
-        if (threadIdx.x == 32) releaser(P, &sh);
-        return;
-    }
-    data_warps(P, &sh);
+    data_warps(P, &sh, stages);
 }
 
 }  // namespace ccl
@@ -396,6 +556,7 @@ ccl_plan_opts_t merged_opts(const ccl_plan_opts_t* opts)
         o.mb_order = opts->mb_order;
         if (opts->timeout_ms) o.timeout_ms = opts->timeout_ms;
         o.instrument = opts->instrument;
+        if (opts->tile_bytes) o.tile_bytes = opts->tile_bytes;
     }
     return o;
 }
@@ -420,6 +581,8 @@ void fill_stats(const ccl::PlanImage& img, ccl_plan_stats_t* st)
     st->fifo_slots = img.S;
     st->slot_bytes = img.slot_bytes;
     st->fifo_bytes = img.fifo_bytes;
+    st->tile_bytes = img.tile_bytes;
+    st->stages = img.ns;
 }
 
 void free_plan(ccl_plan* p)
@@ -485,6 +648,7 @@ void ccl_plan_opts_default(ccl_plan_opts_t* o)
     o->mb_order = CCL_MB_AUTO;
     o->timeout_ms = 2000;
     o->instrument = 0;
+    o->tile_bytes = 16 * 1024;
 }
 
 ccl_status_t ccl_schedule_compile(const ccl_op_t* ops, int32_t nops, int32_t nranks, const int32_t nchunks[3],
@@ -587,16 +751,37 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
     ccl::PlanImage& img = p->img;
 
     // co-residency: every threadblock of the grid must be resident at once;
-    // with the thread count left to the library, halve it until they fit
-    int nsm = 0, per_sm = 0;
+    // with the thread count left to the library, halve it until they fit.
+    // Shared-memory stages of the bulk path take what the SM has left for
+    // the threadblocks it must hold.
+    int nsm = 0, per_sm = 0, smem_sm = 0, smem_optin = 0;
     cudaError_t e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, p->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, p->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
+    cudaFuncAttributes fa{};
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, ccl::ccl_exec_kernel);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(ccl::ccl_exec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_optin - (int)fa.sharedSizeBytes);
+    if (e != cudaSuccess) { delete p; return ccl::cuda_fail(e, "device attributes"); }
+    const int need_sm = nsm > 0 ? (img.ntb + nsm - 1) / nsm : 1;
+    int budget = smem_sm / std::max(1, need_sm) - (int)fa.sharedSizeBytes - 1024;
+    budget = std::min(budget, smem_optin - (int)fa.sharedSizeBytes);
+    int ns = img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / (2 * img.tile_bytes)) : 0;
+    if (ns < 2) ns = 0;
     while (true) {
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ccl::ccl_exec_kernel, img.nthreads, 0);
+        size_t dyn = (size_t)ns * 2 * img.tile_bytes;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ccl::ccl_exec_kernel, img.nthreads, dyn);
         if (e != cudaSuccess) { delete p; return ccl::cuda_fail(e, "occupancy query"); }
-        if ((int64_t)per_sm * nsm >= img.ntb || (opts && opts->nthreads) || img.nthreads <= 128) break;
+        if ((int64_t)per_sm * nsm >= img.ntb) break;
+        if (ns > 2) { --ns; continue; }
+        if (ns > 0) { ns = 0; continue; }
+        if ((opts && opts->nthreads) || img.nthreads <= 128) break;
         img.nthreads = img.nthreads / 2 >= 128 ? img.nthreads / 2 : 128;
+        ns = img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / (2 * img.tile_bytes)) : 0;
+        if (ns < 2) ns = 0;
     }
+    img.ns = ns;
     if ((int64_t)per_sm * nsm < img.ntb) {
         std::string msg = "plan needs " + std::to_string(img.ntb) + " co-resident threadblocks of " +
                           std::to_string(img.nthreads) + " threads; the device holds " + std::to_string(per_sm * nsm);
@@ -655,6 +840,8 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
     k.timeline = p->d_timeline;
     k.m = img.m;
     k.slot_bytes = img.slot_bytes;
+    k.tile_bytes = img.tile_bytes;
+    k.ns = img.ns;
     k.timeout_ns = (unsigned long long)img.timeout_ms * 1000000ull;
     k.S = img.S;
     for (int r = 0; r < CCL_MAX_RANKS; ++r) k.bufs[2][r] = p->d_scratch[r];
@@ -683,7 +870,8 @@ ccl_status_t ccl_execute(ccl_plan_t p, void* const* in_bufs, void* const* out_bu
     if (p->img.ntb == 0) return CCL_OK;  // empty program: nothing to move
     void* args[] = {&k};
     cudaError_t e = cudaLaunchCooperativeKernel((const void*)ccl::ccl_exec_kernel, dim3(p->img.ntb),
-                                                dim3(p->img.nthreads), args, 0, s);
+                                                dim3(p->img.nthreads), args,
+                                                (size_t)p->img.ns * 2 * p->img.tile_bytes, s);
     if (e != cudaSuccess) return ccl::cuda_fail(e, "executor launch");
     p->exec += 1;
     return CCL_OK;

@@ -180,8 +180,9 @@ typedef enum { CCL_MB_AUTO = 0, CCL_MB_ALGO = 1, CCL_MB_TASK = 2, CCL_MB_SEGMENT
  *   channels    : parallelization factor; every chunk range is split into
  *                 `channels` contiguous 16-byte-granular pieces, each with its
  *                 own links and threadblocks (MSCCLang report, §III.1, §IV.1).
- *   nthreads    : threads per threadblock (96..1024, multiple of 32: one
- *                 issuing warp, one releasing warp, the rest move data);
+ *   nthreads    : threads per threadblock (128..1024, multiple of 32: an
+ *                 issuing, a releasing and a bulk-copy warp, the rest move
+ *                 or add data);
  *                 0 = 512, halved (down to 128) until every threadblock can
  *                 be co-resident.
  *   slot_bytes  : FIFO slot size (multiple of 16).
@@ -205,6 +206,9 @@ typedef enum { CCL_MB_AUTO = 0, CCL_MB_ALGO = 1, CCL_MB_TASK = 2, CCL_MB_SEGMENT
  *                 that order and keeps the first that can finish.
  *   timeout_ms  : limit of every device flag wait.
  *   instrument  : 1 = record per-step global-timer stamps (ccl_plan_timeline).
+ *   tile_bytes  : the executor moves a slot in tiles of this size (multiple of
+ *                 16, <= 64 KiB); 16-byte-aligned tiles go through shared
+ *                 memory with bulk (TMA) copies, others through registers.
  */
 typedef struct {
     int32_t channels;
@@ -217,6 +221,7 @@ typedef struct {
     int32_t mb_order;
     int32_t timeout_ms;
     int32_t instrument;
+    int64_t tile_bytes;
 } ccl_plan_opts_t;
 
 void ccl_plan_opts_default(ccl_plan_opts_t* o);
@@ -280,6 +285,9 @@ typedef struct {
     int64_t fifo_bytes;          /* device bytes of all link FIFOs */
     int64_t device_bytes;        /* all device memory owned by the plan */
     double compile_ms;           /* host time of ccl_plan_create */
+    int64_t tile_bytes;          /* tile of the data path */
+    int32_t stages;              /* shared-memory stages of the bulk path (0: registers only) */
+    int32_t pad;
 } ccl_plan_stats_t;
 
 ccl_status_t ccl_plan_stats(ccl_plan_t p, ccl_plan_stats_t* st);
