@@ -339,7 +339,11 @@ __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stage
     struct Fly { int q, s, red, tnum; char* o1; char* o2; unsigned bytes; };
     Fly fly[kNSMax];
     int stage_grp[kNSMax];
-    for (int i = 0; i < kNSMax; ++i) stage_grp[i] = -1;
+    int red_uses[kNSMax];     // reduce tiles stored from each stage (parity of "computed")
+    for (int i = 0; i < kNSMax; ++i) {
+        stage_grp[i] = -1;
+        red_uses[i] = 0;
+    }
     int cq[kNSMax + 1] = {};  // tiles stored, waiting for their stores to complete
     int cg[kNSMax + 1] = {};
     int c_head = 0, c_tail = 0;
@@ -403,7 +407,8 @@ __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stage
         if (f_tail < f_head) {
             // 2. store the oldest tile once loaded (copy) or summed (reduce)
             const Fly e = fly[f_tail % kNSMax];
-            const unsigned par = (unsigned)((e.tnum / NS) & 1);
+            const unsigned par = e.red ? (unsigned)(red_uses[e.s] & 1) : (unsigned)((e.tnum / NS) & 1);
+            if (e.red) ++red_uses[e.s];
             if (!stage_wait(e.red ? &sh->computed[e.s] : &sh->full[e.s], par)) {
                 leave();
                 return;
@@ -445,14 +450,12 @@ __device__ void data_warps(const KParams& P, CtlShared* sh, unsigned char* stage
         const SlotOp op = sh->op[q];
         if (op.cmd != 0) return;
         if (op.bulk) {
+            // the TMA thread moves copy tiles alone; a reduce tile is summed
+            // here once its stage is loaded ("computed" completes once per
+            // reduce tile of the stage)
             const int tn = t++;
             const int s = tn % P.ns;
-            if (!op.red) {
-                // keep the stage's "computed" phases one per tile
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh->computed[s]);
-                continue;
-            }
+            if (!op.red) continue;
             if (!mbar_wait(&sh->full[s], (unsigned)((tn / P.ns) & 1), limit)) return;
             uint4* A = reinterpret_cast<uint4*>(stages + s * T2);
             const uint4* B = reinterpret_cast<const uint4*>(stages + s * T2 + P.tile_bytes);
