@@ -52,16 +52,22 @@ namespace ccl {
 //    hands the slot out as tiles of at most `tile` bytes through a ring of
 //    kQ shared-memory descriptors guarded by mbarriers ("ready").  The next
 //    step's 128-byte record is prefetched with cp.async.
-//  * TMA thread (warp 2, lane 0) moves every 16-byte-aligned tile with bulk
-//    copies: global -> shared stage (mbarrier complete_tx), then shared ->
-//    global to the destination and/or the outgoing slot (bulk groups).  Up to
-//    `ns` tiles are in flight; a tile's stage is reused once its stores have
-//    read it, and a tile counts as done once its stores are complete.
-//  * data warps (warps 3..) add the two operands of reduce tiles in shared
-//    memory, and move unaligned tiles with 16-byte / element loads and stores.
+//  * TMA thread (warp 2, lane 0) moves every 16-byte-aligned *copy* tile
+//    with bulk copies: global -> shared stage (mbarrier complete_tx), then
+//    shared -> global to the destination and/or the outgoing slot (bulk
+//    groups).  Up to `ns` tiles are in flight; a stage is reused once its
+//    stores have read it, and a tile counts as done once its stores are
+//    complete.
+//  * data warps (warps 3..) move the other tiles (every reduce, and copies
+//    that are not 16-byte aligned) with 16-byte / element loads and stores.
 //  * releaser (warp 1, lane 0) takes finished tiles in order, issues one
 //    release fence per batch and posts the flags and counters carried by a
 //    slot's last tile with relaxed stores, then frees the descriptor.
+//
+// Both the TMA thread and the data warps acknowledge every descriptor (the
+// one that moves a tile once it is moved, the other as soon as it has seen
+// that the tile is not its own), and a descriptor is reused only after both
+// acknowledgements, so no role ever misses a descriptor.
 // ----------------------------------------------------------------------
 constexpr int kQ = 16;     // tile descriptors in flight
 constexpr int kNSMax = 8;  // shared-memory stages
@@ -94,11 +100,10 @@ struct CtlShared {
     SlotOp op[kQ];
     Release rel[kQ];
     unsigned long long ready[kQ];
-    unsigned long long done_g[kQ];      // data warps finished an unaligned tile
-    unsigned long long done_b[kQ];      // TMA thread finished a bulk tile
+    unsigned long long done_g[kQ];      // data warps are through with the descriptor
+    unsigned long long done_b[kQ];      // the TMA thread is through with the descriptor
     unsigned long long freed[kQ];
     unsigned long long full[kNSMax];    // stage loaded
-    unsigned long long computed[kNSMax];// reduce stage summed
 };
 
 __device__ __forceinline__ void record_timeout(const KParams& P, int si, int reason)
@@ -269,8 +274,8 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
                 op.n = tn;
                 op.red = red;
                 op.dtype = st.dtype;
-                op.bulk = P.ns > 0 && tn > 0 && ((tn * es) & 15) == 0 && aligned16(op.a) && aligned16(op.o1) &&
-                          (!op.o2 || aligned16(op.o2)) && (!red || aligned16(op.b));
+                op.bulk = P.ns > 0 && !red && tn > 0 && ((tn * es) & 15) == 0 && aligned16(op.a) &&
+                          aligned16(op.o1) && (!op.o2 || aligned16(op.o2));
                 op.cmd = 0;
                 Release& r = sh->rel[q];
                 const bool last_tile = u == ntiles - 1;
@@ -300,14 +305,14 @@ __device__ void releaser(const KParams& P, CtlShared* sh)
         unsigned par = (unsigned)((j / kQ) & 1);
         if (!mbar_wait(&sh->ready[q], par, limit)) return;
         if (sh->op[q].cmd != 0) return;
-        if (!mbar_wait(sh->op[q].bulk ? &sh->done_b[q] : &sh->done_g[q], par, limit)) return;
+        if (!mbar_wait(&sh->done_g[q], par, limit) || !mbar_wait(&sh->done_b[q], par, limit)) return;
         // batch every further tile that is already finished
         int n = 1;
         while (n < kQ) {
             const int q2 = (j + n) % kQ;
             const unsigned p2 = (unsigned)(((j + n) / kQ) & 1);
             if (!mbar_test(&sh->ready[q2], p2) || sh->op[q2].cmd != 0) break;
-            if (!mbar_test(sh->op[q2].bulk ? &sh->done_b[q2] : &sh->done_g[q2], p2)) break;
+            if (!mbar_test(&sh->done_g[q2], p2) || !mbar_test(&sh->done_b[q2], p2)) break;
             ++n;
         }
         fence_acq_rel_gpu();
@@ -330,20 +335,17 @@ __device__ void releaser(const KParams& P, CtlShared* sh)
     }
 }
 
-// TMA thread: bulk copies of aligned tiles through the shared-memory stages
+// TMA thread: bulk copies of aligned copy tiles through the shared-memory
+// stages; every other descriptor is acknowledged at once
 __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stages)
 {
     const int NS = P.ns;
-    const long long T2 = 2 * P.tile_bytes;   // stage = operand a | operand b
+    const long long TB = P.tile_bytes;
     const unsigned long long limit = 4 * P.timeout_ns;
-    struct Fly { int q, s, red, tnum; char* o1; char* o2; unsigned bytes; };
+    struct Fly { int q, s, tnum; char* o1; char* o2; unsigned bytes; };
     Fly fly[kNSMax];
     int stage_grp[kNSMax];
-    int red_uses[kNSMax];     // reduce tiles stored from each stage (parity of "computed")
-    for (int i = 0; i < kNSMax; ++i) {
-        stage_grp[i] = -1;
-        red_uses[i] = 0;
-    }
+    for (int i = 0; i < kNSMax; ++i) stage_grp[i] = -1;
     int cq[kNSMax + 1] = {};  // tiles stored, waiting for their stores to complete
     int cg[kNSMax + 1] = {};
     int c_head = 0, c_tail = 0;
@@ -368,7 +370,7 @@ __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stage
         }
         bulk_wait(0);
     };
-    auto stage_wait = [&](unsigned long long* bar, unsigned par) {
+    auto wait_ready = [&](unsigned long long* bar, unsigned par) {
         unsigned spins = 0;
         unsigned long long t0 = 0;
         while (!mbar_test(bar, par)) {
@@ -383,37 +385,39 @@ __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stage
         return true;
     };
     while (true) {
-        // 1. start loads of newly handed-out aligned tiles while a stage is free
+        // 1. start loads of newly handed-out tiles while a stage is free
         while (!ended && f_head - f_tail < NS) {
             const int q = j % kQ;
             if (!mbar_test(&sh->ready[q], (unsigned)((j / kQ) & 1))) break;
             const SlotOp& op = sh->op[q];
             if (op.cmd != 0) { ended = true; break; }
-            if (!op.bulk) { ++j; continue; }
+            if (!op.bulk) {
+                // not ours: acknowledge right away
+                mbar_arrive(&sh->done_b[q]);
+                ++j;
+                continue;
+            }
             const int s = t % NS;
             if (stage_grp[s] >= 0) bulk_wait_read(g - stage_grp[s] - 1);
             const int es = (op.dtype == CCL_BF16 || op.dtype == CCL_F16) ? 2 : 4;
             const unsigned bytes = (unsigned)(op.n * es);
-            unsigned char* A = stages + s * T2;
+            unsigned char* A = stages + s * TB;
             fence_proxy_async_global();
-            mbar_arrive_expect_tx(&sh->full[s], op.red ? 2 * bytes : bytes);
+            mbar_arrive_expect_tx(&sh->full[s], bytes);
             bulk_load(A, op.a, bytes, &sh->full[s]);
-            if (op.red) bulk_load(A + P.tile_bytes, op.b, bytes, &sh->full[s]);
-            fly[f_head % kNSMax] = Fly{q, s, op.red, t, op.o1, op.o2, bytes};
+            fly[f_head % kNSMax] = Fly{q, s, t, op.o1, op.o2, bytes};
             ++f_head;
             ++t;
             ++j;
         }
         if (f_tail < f_head) {
-            // 2. store the oldest tile once loaded (copy) or summed (reduce)
+            // 2. store the oldest tile once its load has landed
             const Fly e = fly[f_tail % kNSMax];
-            const unsigned par = e.red ? (unsigned)(red_uses[e.s] & 1) : (unsigned)((e.tnum / NS) & 1);
-            if (e.red) ++red_uses[e.s];
-            if (!stage_wait(e.red ? &sh->computed[e.s] : &sh->full[e.s], par)) {
+            if (!wait_ready(&sh->full[e.s], (unsigned)((e.tnum / NS) & 1))) {
                 leave();
                 return;
             }
-            const unsigned char* A = stages + e.s * T2;
+            const unsigned char* A = stages + e.s * TB;
             bulk_store(e.o1, A, e.bytes);
             if (e.o2) bulk_store(e.o2, A, e.bytes);
             bulk_commit();
@@ -428,7 +432,7 @@ __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stage
             // 3. nothing in flight: finish every store, then wait for work
             retire(0);
             if (ended) return;
-            if (!stage_wait(&sh->ready[j % kQ], (unsigned)((j / kQ) & 1))) {
+            if (!wait_ready(&sh->ready[j % kQ], (unsigned)((j / kQ) & 1))) {
                 leave();
                 return;
             }
@@ -436,43 +440,18 @@ __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stage
     }
 }
 
-__device__ void data_warps(const KParams& P, CtlShared* sh, unsigned char* stages)
+__device__ void data_warps(const KParams& P, CtlShared* sh)
 {
     const int tid = threadIdx.x - 96;
     const int T = blockDim.x - 96;
     const int lane = threadIdx.x & 31;
     const unsigned long long limit = 4 * P.timeout_ns;
-    const long long T2 = 2 * P.tile_bytes;
-    int t = 0;   // aligned tiles seen (same numbering as the TMA thread)
     for (int j = 0;; ++j) {
         const int q = j % kQ;
         if (!mbar_wait(&sh->ready[q], (unsigned)((j / kQ) & 1), limit)) return;
         const SlotOp op = sh->op[q];
         if (op.cmd != 0) return;
-        if (op.bulk) {
-            // the TMA thread moves copy tiles alone; a reduce tile is summed
-            // here once its stage is loaded ("computed" completes once per
-            // reduce tile of the stage)
-            const int tn = t++;
-            const int s = tn % P.ns;
-            if (!op.red) continue;
-            if (!mbar_wait(&sh->full[s], (unsigned)((tn / P.ns) & 1), limit)) return;
-            uint4* A = reinterpret_cast<uint4*>(stages + s * T2);
-            const uint4* B = reinterpret_cast<const uint4*>(stages + s * T2 + P.tile_bytes);
-            const int es = (op.dtype == CCL_BF16 || op.dtype == CCL_F16) ? 2 : 4;
-            const int nv = (int)(op.n * es / 16);
-            switch (op.dtype) {
-            case CCL_F32: for (int v = tid; v < nv; v += T) A[v] = vadd<CCL_F32>(A[v], B[v]); break;
-            case CCL_BF16: for (int v = tid; v < nv; v += T) A[v] = vadd<CCL_BF16>(A[v], B[v]); break;
-            case CCL_F16: for (int v = tid; v < nv; v += T) A[v] = vadd<CCL_F16>(A[v], B[v]); break;
-            default: for (int v = tid; v < nv; v += T) A[v] = vadd<CCL_I32>(A[v], B[v]); break;
-            }
-            fence_proxy_async_smem();   // the sums are read next by bulk stores
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh->computed[s]);
-            continue;
-        }
-        if (op.n > 0) {
+        if (!op.bulk && op.n > 0) {
             switch (op.dtype) {
             case CCL_F32: move_part<CCL_F32>(op.red, op.a, op.as, op.b, op.bs, op.o1, op.o1s, op.o2, op.n, tid, T); break;
             case CCL_BF16: move_part<CCL_BF16>(op.red, op.a, op.as, op.b, op.bs, op.o1, op.o1s, op.o2, op.n, tid, T); break;
@@ -498,10 +477,7 @@ __global__ void __launch_bounds__(1024, 1) ccl_exec_kernel(const __grid_constant
             mbar_init(&sh.done_b[q], 1);
             mbar_init(&sh.freed[q], 1);
         }
-        for (int s = 0; s < kNSMax; ++s) {
-            mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.computed[s], nwarps - 3);
-        }
+        for (int s = 0; s < kNSMax; ++s) mbar_init(&sh.full[s], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -510,11 +486,11 @@ __global__ void __launch_bounds__(1024, 1) ccl_exec_kernel(const __grid_constant
         if ((threadIdx.x & 31) == 0) {
             if (warp == 0) issuer(P, &sh, b0, b1);
             else if (warp == 1) releaser(P, &sh);
-            else if (P.ns > 0) tma_thread(P, &sh, stages);
+            else tma_thread(P, &sh, stages);
         }
         return;
     }
-    data_warps(P, &sh, stages);
+    data_warps(P, &sh);
 }
 
 }  // namespace ccl
@@ -770,10 +746,10 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
     const int need_sm = nsm > 0 ? (img.ntb + nsm - 1) / nsm : 1;
     int budget = smem_sm / std::max(1, need_sm) - (int)fa.sharedSizeBytes - 1024;
     budget = std::min(budget, smem_optin - (int)fa.sharedSizeBytes);
-    int ns = img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / (2 * img.tile_bytes)) : 0;
+    int ns = img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / img.tile_bytes) : 0;
     if (ns < 2) ns = 0;
     while (true) {
-        size_t dyn = (size_t)ns * 2 * img.tile_bytes;
+        size_t dyn = (size_t)ns * img.tile_bytes;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ccl::ccl_exec_kernel, img.nthreads, dyn);
         if (e != cudaSuccess) { delete p; return ccl::cuda_fail(e, "occupancy query"); }
         if ((int64_t)per_sm * nsm >= img.ntb) break;
@@ -781,7 +757,7 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
         if (ns > 0) { ns = 0; continue; }
         if ((opts && opts->nthreads) || img.nthreads <= 128) break;
         img.nthreads = img.nthreads / 2 >= 128 ? img.nthreads / 2 : 128;
-        ns = img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / (2 * img.tile_bytes)) : 0;
+        ns = img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / img.tile_bytes) : 0;
         if (ns < 2) ns = 0;
     }
     img.ns = ns;
@@ -874,7 +850,7 @@ ccl_status_t ccl_execute(ccl_plan_t p, void* const* in_bufs, void* const* out_bu
     void* args[] = {&k};
     cudaError_t e = cudaLaunchCooperativeKernel((const void*)ccl::ccl_exec_kernel, dim3(p->img.ntb),
                                                 dim3(p->img.nthreads), args,
-                                                (size_t)p->img.ns * 2 * p->img.tile_bytes, s);
+                                                (size_t)p->img.ns * p->img.tile_bytes, s);
     if (e != cudaSuccess) return ccl::cuda_fail(e, "executor launch");
     p->exec += 1;
     return CCL_OK;
