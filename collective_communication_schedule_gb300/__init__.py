@@ -27,6 +27,7 @@ FLAG_WRAP, FLAG_NOFUSE = 1, 2
 SCHED_RR, SCHED_HPDS = 0, 1
 TB_CONNECTION, TB_PACKED = 0, 1
 MB_AUTO, MB_ALGO, MB_TASK, MB_SEGMENT = 0, 1, 2, 3
+LINK_FIFO, LINK_DIRECT = 0, 1
 KIND_NAMES = ["copy", "reduce", "send", "recv", "rrc", "rcs", "fwd", "rrs", "rrcs", "copy_send"]
 DTYPE_NAMES = {F32: "f32", BF16: "bf16", F16: "f16", I32: "i32"}
 ESIZE = {F32: 4, BF16: 2, F16: 2, I32: 4}
@@ -66,7 +67,8 @@ class PlanOpts(ctypes.Structure):
     _fields_ = [("channels", ctypes.c_int32), ("nthreads", ctypes.c_int32), ("slot_bytes", ctypes.c_int64),
                 ("fifo_slots", ctypes.c_int32), ("microbatches", ctypes.c_int32), ("scheduler", ctypes.c_int32),
                 ("tb_alloc", ctypes.c_int32), ("mb_order", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
-                ("instrument", ctypes.c_int32), ("tile_bytes", ctypes.c_int64)]
+                ("instrument", ctypes.c_int32), ("tile_bytes", ctypes.c_int64), ("bulk", ctypes.c_int32),
+                ("link_mode", ctypes.c_int32)]
 
 
 class PlanStats(ctypes.Structure):

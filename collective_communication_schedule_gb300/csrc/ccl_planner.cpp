@@ -184,6 +184,9 @@ void allocate_connection(const ccl_schedule& s, const Timeline& tl, TBList* tbs,
             const Instr& I = s.instrs[i];
             int in = I.xfer_in >= 0 ? s.xfers[I.xfer_in].src_rank : -1;
             int out = I.xfer_out >= 0 ? s.xfers[I.xfer_out].dst_rank : -1;
+            // a copy into another rank's buffer (direct transport) is a
+            // connection of its own to that rank
+            if (I.kind == CCL_I_COPY && I.dst.valid() && I.dst.rank != I.rank) out = CCL_MAX_RANKS + I.dst.rank;
             auto compat = [&](const C& c) {
                 return (in < 0 || c.in < 0 || c.in == in) && (out < 0 || c.out < 0 || c.out == out);
             };
@@ -350,6 +353,8 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     img->S = S;
     img->slot_bytes = o.slot_bytes;
     img->tile_bytes = o.tile_bytes;
+    img->bulk = o.bulk;
+    img->link_mode = o.link_mode;
     img->nthreads = o.nthreads;
     img->dtype = dtype;
     img->esize = es;
@@ -685,7 +690,65 @@ void dump_programs(const ccl_schedule& s, const Timeline& tl, const TBList& tbs,
 
 }  // namespace
 
-ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const ccl_plan_opts_t& o,
+// Direct transport: a plain send from a buffer whose transfer ends in a plain
+// receive into a buffer becomes one copy run by the sender's threadblock
+// straight into the receiver's destination; the receive disappears and
+// every dependency on it moves to the copy.  Nothing is staged in a FIFO.
+ccl_schedule direct_transport(const ccl_schedule& s, int* ndirect)
+{
+    ccl_schedule d = s;
+    const int ni = (int)s.instrs.size();
+    std::vector<int> redirect(ni);
+    for (int i = 0; i < ni; ++i) redirect[i] = i;
+    std::vector<char> drop_x(s.xfers.size(), 0), drop_i(ni, 0);
+    int n = 0;
+    for (size_t x = 0; x < s.xfers.size(); ++x) {
+        const Xfer& X = s.xfers[x];
+        const Instr& snd = s.instrs[X.send_instr];
+        const Instr& rcv = s.instrs[X.recv_instr];
+        if (snd.kind != CCL_I_SEND || rcv.kind != CCL_I_RECV) continue;
+        Instr& c = d.instrs[X.send_instr];
+        c.kind = CCL_I_COPY;
+        c.dst = rcv.dst;
+        c.xfer_out = -1;
+        drop_x[x] = 1;
+        drop_i[X.recv_instr] = 1;
+        redirect[X.recv_instr] = X.send_instr;
+        ++n;
+    }
+    *ndirect = n;
+    if (!n) return d;
+    // renumber instructions and transfers
+    std::vector<int> inew(ni, -1), xnew(s.xfers.size(), -1);
+    std::vector<Instr> instrs;
+    for (int i = 0; i < ni; ++i)
+        if (!drop_i[i]) { inew[i] = (int)instrs.size(); instrs.push_back(d.instrs[i]); }
+    std::vector<Xfer> xfers;
+    for (size_t x = 0; x < s.xfers.size(); ++x)
+        if (!drop_x[x]) { xnew[x] = (int)xfers.size(); xfers.push_back(s.xfers[x]); }
+    for (auto& I : instrs) {
+        if (I.xfer_in >= 0) I.xfer_in = xnew[I.xfer_in];
+        if (I.xfer_out >= 0) I.xfer_out = xnew[I.xfer_out];
+    }
+    for (auto& X : xfers) {
+        X.send_instr = inew[X.send_instr];
+        X.recv_instr = inew[X.recv_instr];
+    }
+    std::set<std::tuple<int, int, int>> seen;
+    std::vector<Dep> deps;
+    for (const Dep& e : s.deps) {
+        int a = inew[redirect[e.from]], b = inew[redirect[e.to]];
+        if (a < 0 || b < 0 || a == b) continue;
+        if (!seen.insert(std::make_tuple(a, b, e.exact ? 1 : 0)).second) continue;
+        deps.push_back(Dep{a, b, e.exact});
+    }
+    d.instrs = std::move(instrs);
+    d.xfers = std::move(xfers);
+    d.deps = std::move(deps);
+    return d;
+}
+
+ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, const ccl_plan_opts_t& o,
                         PlanImage* img)
 {
     if (ce <= 0) return fail(CCL_ERR_INVALID_ARG, "chunk_elems must be positive");
@@ -693,6 +756,7 @@ ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const 
     if (o.channels < 1 || o.channels > 256) return fail(CCL_ERR_INVALID_ARG, "channels must be in 1..256");
     if (o.nthreads < 128 || o.nthreads > 1024 || o.nthreads % 32)
         return fail(CCL_ERR_INVALID_ARG, "nthreads must be a multiple of 32 in 128..1024");
+    if (o.bulk != 0 && o.bulk != 1) return fail(CCL_ERR_INVALID_ARG, "bulk must be 0 or 1");
     if (o.tile_bytes < 16 || o.tile_bytes % 16 || o.tile_bytes > 65536)
         return fail(CCL_ERR_INVALID_ARG, "tile_bytes must be a multiple of 16 in 16..65536");
     if (o.slot_bytes < 16 || o.slot_bytes % 16) return fail(CCL_ERR_INVALID_ARG, "slot_bytes must be a positive multiple of 16");
@@ -703,6 +767,10 @@ ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const 
     if (o.mb_order < CCL_MB_AUTO || o.mb_order > CCL_MB_SEGMENT) return fail(CCL_ERR_INVALID_ARG, "unknown mb_order");
     if (o.timeout_ms <= 0) return fail(CCL_ERR_INVALID_ARG, "timeout_ms must be positive");
 
+    if (o.link_mode != CCL_LINK_FIFO && o.link_mode != CCL_LINK_DIRECT)
+        return fail(CCL_ERR_INVALID_ARG, "unknown link_mode");
+    int ndirect = 0;
+    const ccl_schedule s = o.link_mode == CCL_LINK_DIRECT ? direct_transport(s_in, &ndirect) : s_in;
     const int es = esize_of(dtype);
     Timeline tl;
     ccl_status_t st = build_timeline(s, o.scheduler, &tl);
@@ -761,6 +829,7 @@ ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const 
     return fail(CCL_ERR_DEADLOCK, "threadblock programs cannot finish with " + std::to_string(o.fifo_slots) +
                                       " FIFO slots of " + std::to_string(o.slot_bytes) + " bytes (" + first_why + ")");
 done:
+    img->ndirect = ndirect;
     // byte accounting of the source program
     {
         std::vector<std::vector<char>> rd(s.nranks, std::vector<char>(std::max(1, s.nchunks[0]), 0));

@@ -71,7 +71,8 @@ namespace ccl {
 // ----------------------------------------------------------------------
 constexpr int kQ = 16;     // tile descriptors in flight
 constexpr int kNSMax = 8;  // shared-memory stages
-constexpr int kRetireDepth = 2;
+constexpr int kRetireDepth = 7;   // store groups left in flight when retiring
+constexpr int kCQ = 16;           // stored tiles awaiting completion (> kRetireDepth)
 
 struct SlotOp {
     const char* a;      // data in: incoming slot or source buffer
@@ -346,8 +347,8 @@ __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stage
     Fly fly[kNSMax];
     int stage_grp[kNSMax];
     for (int i = 0; i < kNSMax; ++i) stage_grp[i] = -1;
-    int cq[kNSMax + 1] = {};  // tiles stored, waiting for their stores to complete
-    int cg[kNSMax + 1] = {};
+    int cq[kCQ] = {};         // tiles stored, waiting for their stores to complete
+    int cg[kCQ] = {};
     int c_head = 0, c_tail = 0;
     int j = 0, t = 0, g = 0, f_head = 0, f_tail = 0;
     bool ended = false;
@@ -355,9 +356,9 @@ __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stage
         // all but the newest `depth` store groups are complete
         bulk_wait(depth);
         bool any = false;
-        while (c_tail < c_head && cg[c_tail % (kNSMax + 1)] < g - depth) {
+        while (c_tail < c_head && cg[c_tail % kCQ] < g - depth) {
             if (!any) { fence_proxy_async_global(); any = true; }
-            mbar_arrive(&sh->done_b[cq[c_tail % (kNSMax + 1)]]);
+            mbar_arrive(&sh->done_b[cq[c_tail % kCQ]]);
             ++c_tail;
         }
     };
@@ -402,7 +403,7 @@ __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stage
             const int es = (op.dtype == CCL_BF16 || op.dtype == CCL_F16) ? 2 : 4;
             const unsigned bytes = (unsigned)(op.n * es);
             unsigned char* A = stages + s * TB;
-            fence_proxy_async_global();
+            if (!op.as) fence_proxy_async_global();   // reads data another CTA published
             mbar_arrive_expect_tx(&sh->full[s], bytes);
             bulk_load(A, op.a, bytes, &sh->full[s]);
             fly[f_head % kNSMax] = Fly{q, s, t, op.o1, op.o2, bytes};
@@ -422,8 +423,8 @@ __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stage
             if (e.o2) bulk_store(e.o2, A, e.bytes);
             bulk_commit();
             stage_grp[e.s] = g;
-            cq[c_head % (kNSMax + 1)] = e.q;
-            cg[c_head % (kNSMax + 1)] = g;
+            cq[c_head % kCQ] = e.q;
+            cg[c_head % kCQ] = g;
             ++c_head;
             ++g;
             ++f_tail;
@@ -536,6 +537,8 @@ ccl_plan_opts_t merged_opts(const ccl_plan_opts_t* opts)
         if (opts->timeout_ms) o.timeout_ms = opts->timeout_ms;
         o.instrument = opts->instrument;
         if (opts->tile_bytes) o.tile_bytes = opts->tile_bytes;
+        o.bulk = opts->bulk;
+        o.link_mode = opts->link_mode;
     }
     return o;
 }
@@ -628,6 +631,8 @@ void ccl_plan_opts_default(ccl_plan_opts_t* o)
     o->timeout_ms = 2000;
     o->instrument = 0;
     o->tile_bytes = 16 * 1024;
+    o->bulk = 0;
+    o->link_mode = CCL_LINK_DIRECT;
 }
 
 ccl_status_t ccl_schedule_compile(const ccl_op_t* ops, int32_t nops, int32_t nranks, const int32_t nchunks[3],
@@ -746,7 +751,7 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
     const int need_sm = nsm > 0 ? (img.ntb + nsm - 1) / nsm : 1;
     int budget = smem_sm / std::max(1, need_sm) - (int)fa.sharedSizeBytes - 1024;
     budget = std::min(budget, smem_optin - (int)fa.sharedSizeBytes);
-    int ns = img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / img.tile_bytes) : 0;
+    int ns = img.bulk && img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / img.tile_bytes) : 0;
     if (ns < 2) ns = 0;
     while (true) {
         size_t dyn = (size_t)ns * img.tile_bytes;
@@ -757,7 +762,7 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
         if (ns > 0) { ns = 0; continue; }
         if ((opts && opts->nthreads) || img.nthreads <= 128) break;
         img.nthreads = img.nthreads / 2 >= 128 ? img.nthreads / 2 : 128;
-        ns = img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / img.tile_bytes) : 0;
+        ns = img.bulk && img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / img.tile_bytes) : 0;
         if (ns < 2) ns = 0;
     }
     img.ns = ns;

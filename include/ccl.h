@@ -173,6 +173,7 @@ void ccl_schedule_destroy(ccl_schedule_t s);
 typedef enum { CCL_SCHED_RR = 0, CCL_SCHED_HPDS = 1 } ccl_scheduler_t;
 typedef enum { CCL_TB_CONNECTION = 0, CCL_TB_PACKED = 1 } ccl_tb_alloc_t;
 typedef enum { CCL_MB_AUTO = 0, CCL_MB_ALGO = 1, CCL_MB_TASK = 2, CCL_MB_SEGMENT = 3 } ccl_mb_order_t;
+typedef enum { CCL_LINK_FIFO = 0, CCL_LINK_DIRECT = 1 } ccl_link_mode_t;
 
 /*
  * Execution parameters of a plan (zero fields take the defaults written by
@@ -207,8 +208,15 @@ typedef enum { CCL_MB_AUTO = 0, CCL_MB_ALGO = 1, CCL_MB_TASK = 2, CCL_MB_SEGMENT
  *   timeout_ms  : limit of every device flag wait.
  *   instrument  : 1 = record per-step global-timer stamps (ccl_plan_timeline).
  *   tile_bytes  : the executor moves a slot in tiles of this size (multiple of
- *                 16, <= 64 KiB); 16-byte-aligned tiles go through shared
- *                 memory with bulk (TMA) copies, others through registers.
+ *                 16, <= 64 KiB).
+ *   bulk        : 1 = move 16-byte-aligned copy tiles through shared memory
+ *                 with bulk (TMA) copies; 0 = registers for every tile.
+ *   link_mode   : transport of a transfer (AutoCCL report: implementation
+ *                 parameter "transport").  CCL_LINK_FIFO stages every
+ *                 transfer in the link FIFO; CCL_LINK_DIRECT lets a plain
+ *                 send from a buffer write straight into the receiver's
+ *                 destination buffer (one copy, no FIFO) and keeps FIFOs for
+ *                 transfers that are forwarded or reduced.
  */
 typedef struct {
     int32_t channels;
@@ -222,6 +230,8 @@ typedef struct {
     int32_t timeout_ms;
     int32_t instrument;
     int64_t tile_bytes;
+    int32_t bulk;
+    int32_t link_mode;
 } ccl_plan_opts_t;
 
 void ccl_plan_opts_default(ccl_plan_opts_t* o);

@@ -112,3 +112,15 @@ def test_repeated_executions_reuse_flags(ccl):
         plan.status()
         want, _, _ = oracle.run(ops, 8, nch, 4096, BF16, ins)
         assert_bitexact(to_host(d_out, BF16), want)
+
+
+@pytest.mark.parametrize("link_mode", [0, 1])
+@pytest.mark.parametrize("bulk", [0, 1])
+@pytest.mark.parametrize("kind,R,G", [(0, 8, 0), (1, 8, 0), (2, 5, 0), (3, 16, 8), (4, 32, 8), (5, 24, 8), (5, 6, 3)])
+def test_transport_and_data_path_do_not_change_bits(ccl, kind, R, G, link_mode, bulk):
+    """FIFO vs direct transport, register vs bulk (TMA) tiles, with a ragged
+    chunk so unaligned tiles take the register path inside the same plan."""
+    for ce, dtype in ((4096, BF16), (1003, F32)):
+        got, want, _ = run_case(ccl, kind, R, G, ce, dtype, DIST[dtype], 21, link_mode=link_mode, bulk=bulk,
+                                tile_bytes=4096, slot_bytes=8192)
+        assert_bitexact(got, want)
