@@ -304,9 +304,15 @@ __device__ void releaser(const KParams& P, CtlShared* sh)
     for (int j = 0;;) {
         int q = j % kQ;
         unsigned par = (unsigned)((j / kQ) & 1);
-        if (!mbar_wait(&sh->ready[q], par, limit)) return;
+        if (!mbar_wait(&sh->ready[q], par, limit)) {
+            record_timeout(P, -1, WAIT_DONE);
+            return;
+        }
         if (sh->op[q].cmd != 0) return;
-        if (!mbar_wait(&sh->done_g[q], par, limit) || !mbar_wait(&sh->done_b[q], par, limit)) return;
+        if (!mbar_wait(&sh->done_g[q], par, limit) || !mbar_wait(&sh->done_b[q], par, limit)) {
+            record_timeout(P, -1, WAIT_DONE);
+            return;
+        }
         // batch every further tile that is already finished
         int n = 1;
         while (n < kQ) {
@@ -341,6 +347,18 @@ __device__ void releaser(const KParams& P, CtlShared* sh)
 __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stages)
 {
     const int NS = P.ns;
+    if (NS == 0) {
+        // bulk path off: acknowledge every descriptor as it comes
+        for (int j = 0;; ++j) {
+            const int q = j % kQ;
+            if (!mbar_wait(&sh->ready[q], (unsigned)((j / kQ) & 1), 4 * P.timeout_ns)) {
+                record_timeout(P, -1, WAIT_DONE);
+                return;
+            }
+            if (sh->op[q].cmd != 0) return;
+            mbar_arrive(&sh->done_b[q]);
+        }
+    }
     const long long TB = P.tile_bytes;
     const unsigned long long limit = 4 * P.timeout_ns;
     struct Fly { int q, s, tnum; char* o1; char* o2; unsigned bytes; };
@@ -385,7 +403,12 @@ __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stage
         }
         return true;
     };
+    unsigned iter = 0;
     while (true) {
+        if ((++iter & 63) == 0 && *(volatile int*)P.status != 0) {
+            leave();
+            return;
+        }
         // 1. start loads of newly handed-out tiles while a stage is free
         while (!ended && f_head - f_tail < NS) {
             const int q = j % kQ;
@@ -415,6 +438,7 @@ __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stage
             // 2. store the oldest tile once its load has landed
             const Fly e = fly[f_tail % kNSMax];
             if (!wait_ready(&sh->full[e.s], (unsigned)((e.tnum / NS) & 1))) {
+                record_timeout(P, -1, WAIT_DONE);
                 leave();
                 return;
             }
@@ -434,6 +458,7 @@ __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stage
             retire(0);
             if (ended) return;
             if (!wait_ready(&sh->ready[j % kQ], (unsigned)((j / kQ) & 1))) {
+                record_timeout(P, -1, WAIT_DONE);
                 leave();
                 return;
             }
@@ -449,7 +474,10 @@ __device__ void data_warps(const KParams& P, CtlShared* sh)
     const unsigned long long limit = 4 * P.timeout_ns;
     for (int j = 0;; ++j) {
         const int q = j % kQ;
-        if (!mbar_wait(&sh->ready[q], (unsigned)((j / kQ) & 1), limit)) return;
+        if (!mbar_wait(&sh->ready[q], (unsigned)((j / kQ) & 1), limit)) {
+            if (lane == 0) record_timeout(P, -1, WAIT_DONE);
+            return;
+        }
         const SlotOp op = sh->op[q];
         if (op.cmd != 0) return;
         if (!op.bulk && op.n > 0) {
