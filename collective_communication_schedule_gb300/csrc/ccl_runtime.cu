@@ -211,7 +211,8 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
         const unsigned long long base_in = Lin ? (unsigned long long)(P.exec * Lin->total) : 0;
         const unsigned long long base_out = Lout ? (unsigned long long)(P.exec * Lout->total) : 0;
         const long long slot_elems = P.slot_bytes / es;
-        const long long tile_elems = P.tile_bytes / es;
+        // tiles exist for the bulk path; the register path takes a slot whole
+        const long long tile_elems = (P.ns > 0 ? P.tile_bytes : P.slot_bytes) / es;
         const bool linked = Lin || Lout;
         // FIFO slots of a linked step; local steps are cut into tiles directly
         const long long nslots = linked ? (st.nslots > 0 ? st.nslots : 1)
