@@ -121,7 +121,7 @@ template <bool RED, int DT>
 __device__ __forceinline__ void move_vec(const uint4* a, bool as, const uint4* b, bool bs, uint4* o1, bool o1s,
                                          uint4* o2, int64_t nv, int tid, int T)
 {
-    constexpr int U = 4;
+    constexpr int U = 4;   // vectors in flight per operand per thread
     int64_t i = tid;
     const int64_t full = nv - (int64_t)(U - 1) * T;
     for (; i < full; i += (int64_t)U * T) {
