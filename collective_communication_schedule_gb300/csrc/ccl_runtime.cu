@@ -160,6 +160,48 @@ __device__ bool wait_flags(const KParams& P, const unsigned long long* a, unsign
     return true;
 }
 
+// Batched form for consecutive slots k .. k+bmax-1 of one step: the flags of
+// all of them are polled with relaxed loads in one round trip; returns how
+// many leading slots are ready (>= 1), after one acquire fence, or 0 when the
+// wait for the first one fails.
+constexpr int kBatch = 4;
+__device__ int wait_slots(const KParams& P, const DLink* Lin, const DLink* Lout, unsigned long long sin0,
+                          unsigned long long sout0, int bmax, int si, unsigned long long& waited)
+{
+    unsigned long long t0 = 0;
+    unsigned spins = 0;
+    while (true) {
+        unsigned long long x[kBatch], y[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            x[i] = ~0ull;
+            y[i] = ~0ull;
+            if (i < bmax) {
+                if (Lin) x[i] = ld_relaxed(P.flags + Lin->flag_base + (int)((sin0 + i) % P.S));
+                if (Lout && sout0 + i + 1 > (unsigned long long)P.S)
+                    y[i] = ld_relaxed(P.flags + Lout->flag_base + P.S + (int)((sout0 + i) % P.S));
+            }
+        }
+        int b = 0;
+        while (b < bmax && x[b] >= sin0 + b + 1 && y[b] >= sout0 + b + 1 - P.S) ++b;
+        if (b > 0) {
+            fence_acq_rel_gpu();
+            if (t0) waited += gtimer() - t0;
+            return b;
+        }
+        if (!t0) t0 = gtimer();
+        ++spins;
+        if ((spins & 15) == 0) {
+            if (*(volatile int*)P.status != 0) return 0;
+            if (gtimer() - t0 > P.timeout_ns) {
+                record_timeout(P, si, x[0] < sin0 + 1 ? WAIT_FULL : WAIT_FREE);
+                return 0;
+            }
+        }
+        if (spins > 64) __nanosleep(32);
+    }
+}
+
 __device__ __forceinline__ void prefetch_rec(DRec* dst, const DRec* src)
 {
     const unsigned d = smem_addr(dst);
@@ -223,17 +265,19 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
         const char* locb = st.loc_buf >= 0 ? P.bufs[st.loc_buf][st.loc_rank] + st.loc_off * es : nullptr;
         char* dstb = st.dst_buf >= 0 ? P.bufs[st.dst_buf][st.dst_rank] + st.dst_off * es : nullptr;
         const bool post = !(st.flags & 1);
+        int ready_slots = 0;   // slots whose flags were already seen ready
         for (long long k = 0; k < nslots; ++k) {
             const unsigned long long sin = base_in + st.seq_in + k;
             const unsigned long long sout = base_out + st.seq_out + k;
-            const bool need_free = Lout && sout + 1 > (unsigned long long)P.S;
-            if ((Lin || need_free) &&
-                !wait_flags(P, Lin ? P.flags + Lin->flag_base + (int)(sin % P.S) : nullptr, sin + 1,
-                            need_free ? P.flags + Lout->flag_base + P.S + (int)(sout % P.S) : nullptr,
-                            sout + 1 - P.S, si, WAIT_FULL, waited)) {
-                publish_cmd(2);
-                return;
+            if (linked && ready_slots == 0) {
+                const int bmax = (int)((nslots - k) < kBatch ? (nslots - k) : kBatch);
+                ready_slots = wait_slots(P, Lin, Lout, sin, sout, bmax, si, waited);
+                if (ready_slots == 0) {
+                    publish_cmd(2);
+                    return;
+                }
             }
+            if (linked) --ready_slots;
             const long long e0 = k * span;
             long long n = st.nelem - e0;
             if (n > span) n = span;
