@@ -68,7 +68,7 @@ class PlanOpts(ctypes.Structure):
                 ("fifo_slots", ctypes.c_int32), ("microbatches", ctypes.c_int32), ("scheduler", ctypes.c_int32),
                 ("tb_alloc", ctypes.c_int32), ("mb_order", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("instrument", ctypes.c_int32), ("tile_bytes", ctypes.c_int64), ("bulk", ctypes.c_int32),
-                ("link_mode", ctypes.c_int32)]
+                ("link_mode", ctypes.c_int32), ("channel_scaling", ctypes.c_int32), ("pad", ctypes.c_int32)]
 
 
 class PlanStats(ctypes.Structure):

@@ -89,6 +89,7 @@ struct PlanImage {
     int32_t bulk = 0;                // bulk path requested
     int32_t link_mode = 0;
     int32_t ndirect = 0;             // transfers turned into direct copies
+    int32_t channel_scaling = 0;
     int64_t fifo_bytes = 0;
     int32_t m = 1;
     int32_t channels = 1;

@@ -323,6 +323,23 @@ void fill_records(PlanImage* img)
     }
 }
 
+// Parallelization factor of every instruction: `p` for all, or (scaled)
+// proportional to the instruction's size, at least 1, so that small
+// instructions do not claim as many threadblocks as large ones.  Both ends
+// of a transfer have the same size and therefore the same factor.
+std::vector<int> channel_counts(const ccl_schedule& s, int p, int scaled)
+{
+    std::vector<int> pc(s.instrs.size(), p);
+    if (!scaled) return pc;
+    int64_t cmax = 1;
+    for (const Instr& I : s.instrs) cmax = std::max<int64_t>(cmax, I.count);
+    for (size_t i = 0; i < s.instrs.size(); ++i) {
+        int64_t v = (p * s.instrs[i].count + cmax / 2) / cmax;
+        pc[i] = (int)std::max<int64_t>(1, std::min<int64_t>(p, v));
+    }
+    return pc;
+}
+
 struct Attempt {
     int alloc, m, order;
 };
@@ -340,6 +357,7 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     const int nT = (int)tbs.size();
 
     const std::vector<int> ep = epochs(s);
+    const std::vector<int> pc = channel_counts(s, p, o.channel_scaling);
 
     img->instrs.assign((size_t)ni * p, DInstr{});
     img->steps.clear();
@@ -364,13 +382,24 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     img->instrument = o.instrument;
     for (int r = 0; r < CCL_MAX_RANKS; ++r) img->scratch_used[r] = false;
 
-    // threadblock of every channel instruction: device threadblock
-    // ch * nT + t runs channel ch of rank-level threadblock t
-    const int ntb = nT * p;
+    // threadblock of every channel instruction: channel ch of rank-level
+    // threadblock t is a device threadblock when some instruction of t has
+    // that channel; device threadblocks are numbered channel-major
+    std::vector<int> tb_of_tc((size_t)nT * p, -1), tb_t, tb_ch;
+    for (int ch = 0; ch < p; ++ch)
+        for (int t = 0; t < nT; ++t) {
+            bool any = false;
+            for (int i : tbs[t]) any = any || pc[i] > ch;
+            if (!any) continue;
+            tb_of_tc[(size_t)t * p + ch] = (int)tb_t.size();
+            tb_t.push_back(t);
+            tb_ch.push_back(ch);
+        }
+    const int ntb = (int)tb_t.size();
     std::vector<int> dev_tb_of((size_t)ni * p, -1);
     for (int t = 0; t < nT; ++t)
         for (int i : tbs[t])
-            for (int ch = 0; ch < p; ++ch) dev_tb_of[(size_t)i * p + ch] = ch * nT + t;
+            for (int ch = 0; ch < pc[i]; ++ch) dev_tb_of[(size_t)i * p + ch] = tb_of_tc[(size_t)t * p + ch];
 
     // one FIFO per (sending threadblock, receiving threadblock): every link
     // has a single producer and a single consumer
@@ -395,8 +424,8 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     for (int i = 0; i < ni; ++i) {
         const Instr& I = s.instrs[i];
         int64_t n = I.count * ce;
-        for (int ch = 0; ch < p; ++ch) {
-            Piece pc = split(n, ve, p, ch);
+        for (int ch = 0; ch < pc[i]; ++ch) {
+            Piece pce = split(n, ve, pc[i], ch);
             DInstr& D = img->instrs[(size_t)i * p + ch];
             D.kind = I.kind;
             D.dtype = dtype;
@@ -417,11 +446,11 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
             D.src_rank = I.src.rank; D.src_buf = I.src.valid() ? I.src.buf : -1;
             D.loc_rank = I.loc.rank; D.loc_buf = I.loc.valid() ? I.loc.buf : -1;
             D.dst_rank = I.dst.rank; D.dst_buf = I.dst.valid() ? I.dst.buf : -1;
-            D.src_off = I.src.valid() ? I.src.off * ce + pc.off : 0;
-            D.loc_off = I.loc.valid() ? I.loc.off * ce + pc.off : 0;
-            D.dst_off = I.dst.valid() ? I.dst.off * ce + pc.off : 0;
-            D.nelem = pc.len;
-            sched_bytes += kind_bytes_factor(I.kind) * pc.len * es;
+            D.src_off = I.src.valid() ? I.src.off * ce + pce.off : 0;
+            D.loc_off = I.loc.valid() ? I.loc.off * ce + pce.off : 0;
+            D.dst_off = I.dst.valid() ? I.dst.off * ce + pce.off : 0;
+            D.nelem = pce.len;
+            sched_bytes += kind_bytes_factor(I.kind) * pce.len * es;
             for (const Range* rg : {&I.src, &I.loc, &I.dst})
                 if (rg->valid() && rg->buf == CCL_BUF_SCRATCH) img->scratch_used[rg->rank] = true;
         }
@@ -431,11 +460,15 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     // threadblock programs -> steps
     img->ntb = ntb;
     std::vector<std::vector<int>> step_of((size_t)ni * p, std::vector<int>(m, -1));
-    for (int ch = 0; ch < p; ++ch) {
-        for (int t = 0; t < nT; ++t) {
+    for (int dtb = 0; dtb < ntb; ++dtb) {
+        {
+            const int t = tb_t[dtb], ch = tb_ch[dtb];
             img->tb_begin.push_back((int)img->steps.size());
             img->tb_rank.push_back(tb_rank[t]);
-            auto segs = make_segments(tl, tbs[t], order, ep);
+            std::vector<int> prog;
+            for (int i : tbs[t])
+                if (pc[i] > ch) prog.push_back(i);
+            auto segs = make_segments(tl, prog, order, ep);
             for (auto& seg : segs) {
                 for (int mb = 0; mb < m; ++mb) {
                     for (int i : seg) {
@@ -494,7 +527,7 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
             const Instr& I = s.instrs[i];
             if (I.xfer_in < 0) continue;
             int snd = s.xfers[I.xfer_in].send_instr;
-            for (int ch = 0; ch < p; ++ch)
+            for (int ch = 0; ch < pc[i]; ++ch)
                 for (int mb = 0; mb < m; ++mb) {
                     DStep& r = img->steps[step_of[(size_t)i * p + ch][mb]];
                     const DStep& w = img->steps[step_of[(size_t)snd * p + ch][mb]];
@@ -515,14 +548,14 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
         img->ncounters = 0;
         std::vector<std::vector<DDep>> waits(img->steps.size());
         for (const Dep& d : s.deps) {
-            for (int ch = 0; ch < p; ++ch) {
+            for (int ch = 0; ch < pc[d.to]; ++ch) {
                 int cb = d.to * p + ch;
                 // a producer in the same threadblock: its slots must have
                 // left the data warps before this instruction starts
-                for (int ch2 = 0; ch2 < p; ++ch2)
+                for (int ch2 = 0; ch2 < pc[d.from]; ++ch2)
                     if (dev_tb_of[(size_t)d.from * p + ch2] == dev_tb_of[cb])
                         for (int mb = 0; mb < m; ++mb) img->steps[step_of[cb][mb]].flags |= 2;
-                if (d.exact) {
+                if (d.exact && pc[d.from] == pc[d.to]) {
                     int ca = d.from * p + ch;
                     if (dev_tb_of[ca] == dev_tb_of[cb]) continue;
                     for (int mb = 0; mb < m; ++mb)
@@ -530,7 +563,7 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
                 } else {
                     // all micro-batches of every channel of `from`; the first
                     // step of `to` (micro-batch 0) waits, later ones follow it
-                    for (int ch2 = 0; ch2 < p; ++ch2) {
+                    for (int ch2 = 0; ch2 < pc[d.from]; ++ch2) {
                         int ca = d.from * p + ch2;
                         if (dev_tb_of[ca] == dev_tb_of[cb]) continue;
                         waits[step_of[cb][0]].push_back(DDep{counter(ca), 0, (int64_t)m});
@@ -757,6 +790,8 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
     if (o.nthreads < 128 || o.nthreads > 1024 || o.nthreads % 32)
         return fail(CCL_ERR_INVALID_ARG, "nthreads must be a multiple of 32 in 128..1024");
     if (o.bulk != 0 && o.bulk != 1) return fail(CCL_ERR_INVALID_ARG, "bulk must be 0 or 1");
+    if (o.channel_scaling != 0 && o.channel_scaling != 1)
+        return fail(CCL_ERR_INVALID_ARG, "channel_scaling must be 0 or 1");
     if (o.tile_bytes < 16 || o.tile_bytes % 16 || o.tile_bytes > 65536)
         return fail(CCL_ERR_INVALID_ARG, "tile_bytes must be a multiple of 16 in 16..65536");
     if (o.slot_bytes < 16 || o.slot_bytes % 16) return fail(CCL_ERR_INVALID_ARG, "slot_bytes must be a positive multiple of 16");
@@ -785,10 +820,12 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
 
     // micro-batch candidates
     int64_t max_slots = 1;
-    for (const Instr& I : s.instrs) {
+    const std::vector<int> pcs = channel_counts(s, o.channels, o.channel_scaling);
+    for (size_t i = 0; i < s.instrs.size(); ++i) {
+        const Instr& I = s.instrs[i];
         if (I.xfer_in < 0 && I.xfer_out < 0) continue;
         int64_t n = I.count * ce;
-        int64_t per_ch = (n + o.channels - 1) / o.channels;
+        int64_t per_ch = (n + pcs[i] - 1) / pcs[i];
         max_slots = std::max<int64_t>(max_slots, (per_ch * es + o.slot_bytes - 1) / o.slot_bytes);
     }
     int64_t half = std::max(1, o.fifo_slots / 2);
@@ -819,6 +856,7 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
                 if (simulate_plan(cand, &why)) {
                     *img = std::move(cand);
                     img->ntb_connection = (int)conn.size() * o.channels;
+                    img->channel_scaling = o.channel_scaling;
                     goto done;
                 }
                 if (first_why.empty())

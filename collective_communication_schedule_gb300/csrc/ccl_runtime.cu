@@ -612,6 +612,7 @@ ccl_plan_opts_t merged_opts(const ccl_plan_opts_t* opts)
         if (opts->tile_bytes) o.tile_bytes = opts->tile_bytes;
         o.bulk = opts->bulk;
         o.link_mode = opts->link_mode;
+        o.channel_scaling = opts->channel_scaling;
     }
     return o;
 }
@@ -706,6 +707,8 @@ void ccl_plan_opts_default(ccl_plan_opts_t* o)
     o->tile_bytes = 16 * 1024;
     o->bulk = 0;
     o->link_mode = CCL_LINK_DIRECT;
+    o->channel_scaling = 1;
+    o->pad = 0;
 }
 
 ccl_status_t ccl_schedule_compile(const ccl_op_t* ops, int32_t nops, int32_t nranks, const int32_t nchunks[3],

@@ -120,6 +120,7 @@ extern "C" ccl_status_t ccl_tune(ccl_schedule_t s, int64_t chunk_elems, int32_t 
         if (z.timeout_ms) base.timeout_ms = z.timeout_ms;
         base.bulk = z.bulk;
         base.link_mode = z.link_mode;
+        base.channel_scaling = z.channel_scaling;
     }
     if (!base.nthreads) base.nthreads = 512;
     Prober P{s, chunk_elems, dtype, in_bufs, out_bufs, static_cast<cudaStream_t>(stream), to.reps};

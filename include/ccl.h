@@ -211,6 +211,10 @@ typedef enum { CCL_LINK_FIFO = 0, CCL_LINK_DIRECT = 1 } ccl_link_mode_t;
  *                 16, <= 64 KiB).
  *   bulk        : 1 = move 16-byte-aligned copy tiles through shared memory
  *                 with bulk (TMA) copies; 0 = registers for every tile.
+ *   channel_scaling: 1 = an instruction gets a parallelization factor
+ *                 proportional to its size (at most `channels`, at least 1),
+ *                 so small transfers do not occupy as many threadblocks as
+ *                 large ones; 0 = every instruction gets `channels`.
  *   link_mode   : transport of a transfer (AutoCCL report: implementation
  *                 parameter "transport").  CCL_LINK_FIFO stages every
  *                 transfer in the link FIFO; CCL_LINK_DIRECT lets a plain
@@ -232,6 +236,8 @@ typedef struct {
     int64_t tile_bytes;
     int32_t bulk;
     int32_t link_mode;
+    int32_t channel_scaling;
+    int32_t pad;
 } ccl_plan_opts_t;
 
 void ccl_plan_opts_default(ccl_plan_opts_t* o);
