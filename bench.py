@@ -41,13 +41,13 @@ SUITE = [
     # parameters the workload fixes are kept (24 channels, 16 micro-batches,
     # 1 channel, <= 4 channels); the others are the best measured settings
     ("hier_ar", 3, 16, 8, 0, 4 * MiB, "normal", 2,
-     dict(channels=8, microbatches=16, tb_alloc=1, slot_bytes=65536)),
+     dict(channels=16, microbatches=16, tb_alloc=1, slot_bytes=65536)),
     ("a2a", 4, 32, 8, 2, 1 * MiB, "uniform", 3,
-     dict(channels=2, link_mode=1, bulk=1, nthreads=128, tile_bytes=16384)),
+     dict(channels=2, link_mode=1, bulk=1, nthreads=128, tile_bytes=16384, channel_scaling=0)),
     ("ring_bf16", 0, 8, 0, 1, 32 * MiB, "normal", 4, dict(channels=24, slot_bytes=131072)),
     ("ring_f32", 0, 8, 0, 0, 32 * MiB, "normal", 4, dict(channels=24, slot_bytes=131072)),
     ("a2n", 5, 24, 8, 0, 16 * MiB, "normal", 4,
-     dict(channels=8, link_mode=1, bulk=1, nthreads=128, tile_bytes=16384, slot_bytes=131072)),
+     dict(channels=16, link_mode=1, nthreads=256, slot_bytes=131072, channel_scaling=1)),
     ("ag_3m", 1, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4)),
     ("rs_3m", 2, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4)),
     ("ar_1m", 0, 8, 0, 0, 1 * MiB // 8, "uniform", 0, dict(channels=1)),
