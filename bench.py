@@ -57,6 +57,40 @@ NAMES = {0: "f32", 1: "bf16", 2: "f16", 3: "i32"}
 METRIC = "effective HBM GB/s & busBW per collective vs GB300 HBM roofline, 1 GPU"
 
 
+def sources_hash():
+    """Hash of the executor / planner sources and of the suite: the DRAM
+    traffic recorded in profiles/ holds only for this exact combination."""
+    import glob
+    import hashlib
+    csrc = os.path.join(ROOT, "collective_communication_schedule_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
+                   glob.glob(os.path.join(csrc, "*.cpp")) + glob.glob(os.path.join(csrc, "*.h")),
+                   key=os.path.basename)
+    h = hashlib.sha256()
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update(repr(SUITE).encode())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel, planner or suite changed since it was captured."""
+    try:
+        kv = {}
+        with open(os.path.join(ROOT, "profiles", "roofline_traffic.txt")) as f:
+            for line in f:
+                if line.strip() and not line.startswith("#"):
+                    k, v = line.split()
+                    kv[k] = v
+        if kv.get("sources_sha256_16") != sources_hash():
+            return None
+        return int(kv["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -259,7 +293,10 @@ def run_gpu(args):
                    "schedule_bytes_per_step": sched_bytes,
                    **({"subset": args.only, "scale": args.scale} if (args.only or args.scale != 1.0) else {})},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 3), "traffic": None,
+                     "frac": round(achieved / peak, 3),
+                     "traffic": recorded_traffic() if not (args.only or args.scale != 1.0) else None,
+                     "traffic_unit": "bytes per launch (ncu dram read+write, profiles/roofline_traffic.txt)",
+                     "algorithmic_bytes_per_launch": sched_bytes // len(items),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},
         "e2e": {"value": round(sched_bytes / (e2e_ms * 1e6), 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
