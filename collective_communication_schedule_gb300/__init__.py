@@ -92,6 +92,9 @@ class TuneReport(ctypes.Structure):
                 ("default_us", ctypes.c_double)]
 
 
+PROBE_FN = ctypes.CFUNCTYPE(ctypes.c_double, ctypes.c_void_p, ctypes.POINTER(PlanOpts))
+
+
 def _load():
     if not os.path.exists(_LIB_PATH):
         raise ImportError(f"{_LIB_PATH} is missing: build it with "
@@ -132,6 +135,10 @@ def _load():
     for name in ("ccl_last_error_detail", "ccl_version"):
         getattr(L, name).restype = ctypes.c_char_p
         getattr(L, name).argtypes = []
+    L.ccl_tune_search.restype = ctypes.c_int
+    L.ccl_tune_search.argtypes = [ctypes.POINTER(PlanOpts), ctypes.POINTER(TuneOpts), PROBE_FN, P,
+                                  ctypes.POINTER(PlanOpts), ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(ctypes.c_int32)]
     L.ccl_error_string.restype = ctypes.c_char_p
     L.ccl_error_string.argtypes = [ctypes.c_int]
     return L
@@ -303,6 +310,18 @@ def allreduce_ring_noalloc(inputs, outputs, chunk_elems, dtype, channels=0, stre
     """Ring AllReduce with no device allocation (static scratch; see ccl.h)."""
     _check(lib.ccl_allreduce_ring_noalloc(_ptrs(inputs), _ptrs(outputs), len(inputs), chunk_elems, dtype,
                                           channels, _stream(stream)))
+
+
+def tune_search(probe, start: PlanOpts | None = None, max_rounds=3, min_gain=0.01):
+    """Run the tuner's search with a Python probe(opts) -> bandwidth."""
+    cb = PROBE_FN(lambda user, o: float(probe(o.contents)))
+    best = PlanOpts()
+    bw = ctypes.c_double()
+    n = ctypes.c_int32()
+    to = TuneOpts(max_rounds, 1, min_gain)
+    _check(lib.ccl_tune_search(ctypes.byref(start) if start is not None else None, ctypes.byref(to), cb, None,
+                               ctypes.byref(best), ctypes.byref(bw), ctypes.byref(n)))
+    return best, bw.value, n.value
 
 
 def version() -> str:

@@ -92,12 +92,15 @@ int nearest(const std::vector<T>& g, T x)
 }  // namespace
 }  // namespace ccl
 
-extern "C" ccl_status_t ccl_tune(ccl_schedule_t s, int64_t chunk_elems, int32_t dtype, void* const* in_bufs,
-                                 void* const* out_bufs, void* stream, const ccl_tune_opts_t* topts,
-                                 const ccl_plan_opts_t* start, ccl_plan_opts_t* best, ccl_tune_report_t* report)
+// Subspace coordinate descent over (channels, threads, slot size) for each
+// threadblock-allocation policy; `probe` returns the bandwidth of a point
+// (any unit, 0 = infeasible).
+extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_tune_opts_t* topts,
+                                        double (*probe)(void* user, const ccl_plan_opts_t* o), void* user,
+                                        ccl_plan_opts_t* best, double* best_bw, int32_t* probes)
 {
     using namespace ccl;
-    if (!s || !in_bufs || !out_bufs || !best) return fail(CCL_ERR_INVALID_ARG, "null argument");
+    if (!probe || !best) return fail(CCL_ERR_INVALID_ARG, "null argument");
     ccl_tune_opts_t to{3, 5, 0.01};
     if (topts) {
         if (topts->max_rounds > 0) to.max_rounds = topts->max_rounds;
@@ -123,15 +126,23 @@ extern "C" ccl_status_t ccl_tune(ccl_schedule_t s, int64_t chunk_elems, int32_t 
         base.channel_scaling = z.channel_scaling;
     }
     if (!base.nthreads) base.nthreads = 512;
-    Prober P{s, chunk_elems, dtype, in_bufs, out_bufs, static_cast<cudaStream_t>(stream), to.reps};
     std::vector<int> gc(std::begin(kChannels), std::end(kChannels));
     std::vector<int> gt(std::begin(kThreads), std::end(kThreads));
     std::vector<int64_t> gs = slot_grid();
-
-    double default_us = P.time_us(base);
+    std::map<std::tuple<int, int, int64_t, int>, double> cache;
+    int nprobe = 0;
+    auto measure = [&](const ccl_plan_opts_t& o) {
+        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+        ++nprobe;
+        double bw = probe(user, &o);
+        if (!(bw > 0)) bw = 0;
+        cache[key] = bw;
+        return bw;
+    };
     ccl_plan_opts_t overall = base;
-    double overall_us = default_us > 0 ? default_us : 1e30;
-
+    double overall_bw = measure(base);
     for (int alloc : {CCL_TB_CONNECTION, CCL_TB_PACKED}) {
         ccl_plan_opts_t cur = base;
         cur.tb_alloc = alloc;
@@ -141,8 +152,7 @@ extern "C" ccl_status_t ccl_tune(ccl_schedule_t s, int64_t chunk_elems, int32_t 
             o.channels = gc[c];
             o.nthreads = gt[t];
             o.slot_bytes = gs[sl];
-            double us = P.time_us(o);
-            return us > 0 ? 1.0 / us : 0.0;  // bandwidth up to a constant
+            return measure(o);
         };
         double bw = eval(ic, it, is);
         for (int round = 0; round < to.max_rounds; ++round) {
@@ -172,8 +182,8 @@ extern "C" ccl_status_t ccl_tune(ccl_schedule_t s, int64_t chunk_elems, int32_t 
             }
             if (!moved) break;
         }
-        if (bw > 0 && 1.0 / bw < overall_us) {
-            overall_us = 1.0 / bw;
+        if (bw > overall_bw) {
+            overall_bw = bw;
             overall = cur;
             overall.channels = gc[ic];
             overall.nthreads = gt[it];
@@ -181,19 +191,59 @@ extern "C" ccl_status_t ccl_tune(ccl_schedule_t s, int64_t chunk_elems, int32_t 
         }
     }
     *best = overall;
+    if (best_bw) *best_bw = overall_bw;
+    if (probes) *probes = nprobe;
+    if (!(overall_bw > 0)) return fail(CCL_ERR_UNSUPPORTED, "no configuration could run");
+    return CCL_OK;
+}
+
+namespace {
+double gpu_probe(void* user, const ccl_plan_opts_t* o)
+{
+    auto* P = static_cast<ccl::Prober*>(user);
+    double us = P->time_us(*o);
+    return us > 0 ? 1.0 / us : 0.0;
+}
+}  // namespace
+
+extern "C" ccl_status_t ccl_tune(ccl_schedule_t s, int64_t chunk_elems, int32_t dtype, void* const* in_bufs,
+                                 void* const* out_bufs, void* stream, const ccl_tune_opts_t* topts,
+                                 const ccl_plan_opts_t* start, ccl_plan_opts_t* best, ccl_tune_report_t* report)
+{
+    using namespace ccl;
+    if (!s || !in_bufs || !out_bufs || !best) return fail(CCL_ERR_INVALID_ARG, "null argument");
+    ccl_tune_opts_t to{3, 5, 0.01};
+    if (topts) {
+        if (topts->max_rounds > 0) to.max_rounds = topts->max_rounds;
+        if (topts->reps > 0) to.reps = topts->reps;
+        if (topts->min_gain > 0) to.min_gain = topts->min_gain;
+    }
+    Prober P{s, chunk_elems, dtype, in_bufs, out_bufs, static_cast<cudaStream_t>(stream), to.reps};
+    ccl_plan_opts_t base;
+    ccl_plan_opts_default(&base);
+    if (start) base = *start;
+    if (!base.nthreads) base.nthreads = 512;
+    if (!base.channels) base.channels = 1;
+    if (!base.slot_bytes) base.slot_bytes = 128 * 1024;
+    if (!base.fifo_slots) base.fifo_slots = 4;
+    if (!base.tile_bytes) base.tile_bytes = 16 * 1024;
+    if (!base.timeout_ms) base.timeout_ms = 2000;
+    double default_us = P.time_us(base);
+    double bw = 0;
+    int32_t probes = 0;
+    ccl_status_t st = ccl_tune_search(&base, &to, gpu_probe, &P, best, &bw, &probes);
     if (report) {
         std::memset(report, 0, sizeof(*report));
         report->probes = P.probes;
-        report->best_us = overall_us < 1e29 ? overall_us : 0;
+        report->best_us = bw > 0 ? 1.0 / bw : 0;
         report->default_us = default_us;
         ccl_plan_t p = nullptr;
-        if (ccl_plan_create(s, chunk_elems, dtype, CCL_SUM, &overall, &p) == CCL_OK) {
-            ccl_plan_stats_t st;
-            ccl_plan_stats(p, &st);
-            if (report->best_us > 0) report->best_gbs = st.schedule_bytes / (report->best_us * 1e3);
+        if (st == CCL_OK && ccl_plan_create(s, chunk_elems, dtype, CCL_SUM, best, &p) == CCL_OK) {
+            ccl_plan_stats_t ps;
+            ccl_plan_stats(p, &ps);
+            if (report->best_us > 0) report->best_gbs = ps.schedule_bytes / (report->best_us * 1e3);
             ccl_plan_destroy(p);
         }
     }
-    if (overall_us >= 1e29) return fail(CCL_ERR_UNSUPPORTED, "no configuration could run");
-    return CCL_OK;
+    return st;
 }

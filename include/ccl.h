@@ -402,6 +402,18 @@ ccl_status_t ccl_tune(ccl_schedule_t s, int64_t chunk_elems, int32_t dtype,
 ccl_status_t ccl_allreduce_ring_noalloc(void* const* in_bufs, void* const* out_bufs, int32_t nranks,
                                         int64_t chunk_elems, int32_t dtype, int32_t channels, void* stream);
 
+/*
+ * The search of ccl_tune on its own: subspace coordinate descent driven by a
+ * caller-supplied probe that returns the bandwidth of a configuration (any
+ * unit, <= 0 = cannot run).  start (nullable) is the first point; best gets
+ * the winner, *best_bw its bandwidth, *probes the number of distinct
+ * configurations probed.  Host only; no device is touched unless the probe
+ * does.
+ */
+ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_tune_opts_t* topts,
+                             double (*probe)(void* user, const ccl_plan_opts_t* o), void* user,
+                             ccl_plan_opts_t* best, double* best_bw, int32_t* probes);
+
 const char* ccl_error_string(ccl_status_t s);
 const char* ccl_last_error_detail(void);
 const char* ccl_version(void);

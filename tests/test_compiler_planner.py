@@ -1,0 +1,347 @@
+"""Host-side pins of the compiler, planner and tuner (no GPU).
+
+* closed-form instruction mixes and schedule bytes of the built-in programs;
+* fused instruction lists interpreted here (a plain reading of each fused
+  kind's definition) and compared bit for bit with the oracle, for the
+  built-ins and for random chunk programs, with fusion on and off;
+* sub-pipeline constraints of RR and HPDS; threadblock packing; direct
+  transport; deadlock rejection; argument validation;
+* the tuner's coordinate descent on synthetic unimodal bandwidth surfaces.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import datagen
+import oracle
+from oracle import schedules as OS
+
+ccl = pytest.importorskip("collective_communication_schedule_gb300")
+
+F32, BF16, F16, I32 = 0, 1, 2, 3
+KIND = {n: i for i, n in enumerate(ccl.KIND_NAMES)}
+ORACLE_GEN = {0: ("ring_allreduce", lambda R, G: (R,)), 1: ("ring_allgather", lambda R, G: (R,)),
+              2: ("ring_reducescatter", lambda R, G: (R,)), 3: ("hier_allreduce", lambda R, G: (G, R // G)),
+              4: ("alltoall_two_phase", lambda R, G: (G, R // G)), 5: ("alltonext", lambda R, G: (G, R // G))}
+
+
+# --------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("R", [2, 3, 8, 16])
+def test_ring_allreduce_instruction_mix_and_bytes(R):
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, R)
+    per_rank = {}
+    for ins in s.instrs():
+        per_rank.setdefault(ins["rank"], []).append(ccl.KIND_NAMES[ins["kind"]])
+    for r in range(R):
+        k = sorted(per_rank[r])
+        want = sorted(["send"] + ["rrs"] * (R - 2) + ["rrcs"] + ["rcs"] * (R - 2) + ["recv"])
+        assert k == want
+    # R ranks x N (6 - 4/R) bytes, N = R chunks of one element-byte
+    assert s.info().bytes_per_chunk_elem_x_esize == R * R * (6 * R - 4) // R
+
+
+@pytest.mark.parametrize("R", [2, 4, 8])
+def test_allgather_and_reducescatter_bytes(R):
+    for kind in (ccl.RING_ALLGATHER, ccl.RING_REDUCESCATTER):
+        s = ccl.Schedule.builtin(kind, R)
+        assert s.info().bytes_per_chunk_elem_x_esize == R * (3 * R - 1)
+
+
+def test_hierarchical_alltoall_alltonext_bytes():
+    # hierarchical, G = 8, 2 groups: 6.125 x (16 chunks) per rank, 16 ranks
+    assert ccl.Schedule.builtin(ccl.HIER_ALLREDUCE, 16, 8).info().bytes_per_chunk_elem_x_esize == 16 * 98
+    # two-phase AllToAll, R = 32, G = 8: 216 blocks per rank
+    assert ccl.Schedule.builtin(ccl.ALLTOALL_2PHASE, 32, 8).info().bytes_per_chunk_elem_x_esize == 32 * 216
+    # AllToNext, 3 groups of 8: 21 direct pairs x 4 x 8 parts + 2 relayed pairs
+    # x (two 2-hop parts of 6 + six 3-hop parts of 8, relays fused to recv-send)
+    assert ccl.Schedule.builtin(ccl.ALLTONEXT, 24, 8).info().bytes_per_chunk_elem_x_esize == 21 * 32 + 2 * 60
+
+
+def test_unfused_program_has_only_halves():
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 8, 0, ccl.FLAG_NOFUSE)
+    kinds = {ccl.KIND_NAMES[i["kind"]] for i in s.instrs()}
+    assert kinds <= {"copy", "reduce", "send", "recv", "rrc"}
+    # every transfer costs send 2n + receive 2n (or 3n when it reduces)
+    fused = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 8).info().bytes_per_chunk_elem_x_esize
+    assert s.info().bytes_per_chunk_elem_x_esize > fused
+
+
+# ------------------------------------------- fused-instruction interpretation
+
+def _add(a, b, dtype):
+    if dtype == F32:
+        return (a.astype(np.float32) + b.astype(np.float32)).astype(np.float32)
+    if dtype == I32:
+        return (a.astype(np.int64) + b.astype(np.int64)).astype(np.int32)
+    if dtype == BF16:
+        return oracle.add_bf16(a, b)
+    return oracle.add_f16(a, b)
+
+
+def interpret_fused(instrs, R, nchunks, ce, dtype, inputs):
+    """Run fused instructions: every rank in position order, a receiving
+    instruction once its transfer has been sent."""
+    st = datagen.STORAGE[dtype]
+    bufs = {}
+    for r in range(R):
+        bufs[(r, 0)] = np.asarray(inputs[r], st).copy()
+        bufs[(r, 1)] = np.full(nchunks[1] * ce * datagen.ESIZE[dtype], 0xA5, np.uint8).view(st)
+        bufs[(r, 2)] = np.full(max(nchunks[2], 0) * ce * datagen.ESIZE[dtype], 0xA5, np.uint8).view(st)
+
+    def rng(rank, buf, off, cnt):
+        return bufs[(rank, buf)][off * ce:(off + cnt) * ce]
+
+    slots = {}
+    by_rank = {}
+    for i in instrs:
+        by_rank.setdefault(i["rank"], []).append(i)
+    for v in by_rank.values():
+        v.sort(key=lambda x: x["position"])
+    pc = {r: 0 for r in by_rank}
+    remaining = len(instrs)
+    while remaining:
+        moved = False
+        for r, lst in by_rank.items():
+            while pc[r] < len(lst):
+                ins = lst[pc[r]]
+                if ins["xfer_in"] >= 0 and ins["xfer_in"] not in slots:
+                    break
+                k = ccl.KIND_NAMES[ins["kind"]]
+                cnt = ins["count"]
+                src = rng(ins["src_rank"], ins["src_buf"], ins["src_off"], cnt) if ins["src_rank"] >= 0 else None
+                loc = rng(ins["loc_rank"], ins["loc_buf"], ins["loc_off"], cnt) if ins["loc_rank"] >= 0 else None
+                inc = slots.pop(ins["xfer_in"]) if ins["xfer_in"] >= 0 else None
+                if k in ("copy", "copy_send"):
+                    val = src.copy()
+                elif k == "reduce":
+                    val = _add(loc, src, dtype)
+                elif k == "send":
+                    val = src.copy()
+                elif k in ("recv", "rcs", "fwd"):
+                    val = inc
+                elif k in ("rrc", "rrs", "rrcs"):
+                    val = _add(loc, inc, dtype)
+                else:
+                    raise AssertionError(k)
+                if ins["dst_rank"] >= 0:
+                    rng(ins["dst_rank"], ins["dst_buf"], ins["dst_off"], cnt)[:] = val
+                if ins["xfer_out"] >= 0:
+                    slots[ins["xfer_out"]] = val.copy()
+                pc[r] += 1
+                remaining -= 1
+                moved = True
+        assert moved, "fused program cannot make progress"
+    return [bufs[(r, 1)] for r in range(R)]
+
+
+@pytest.mark.parametrize("kind,R,G", [(0, 8, 0), (0, 3, 0), (1, 8, 0), (2, 8, 0), (2, 5, 0), (3, 16, 8), (3, 6, 3),
+                                      (4, 8, 4), (4, 32, 8), (5, 24, 8), (5, 6, 2)])
+@pytest.mark.parametrize("fuse", [True, False])
+def test_fused_builtins_equal_oracle(kind, R, G, fuse):
+    dtype, ce = BF16, 5
+    s = ccl.Schedule.builtin(kind, R, G, 0 if fuse else ccl.FLAG_NOFUSE)
+    name, args = ORACLE_GEN[kind]
+    ops, nch = OS.BUILTINS[name](*args(R, G))
+    assert tuple(s.info().nchunks) == tuple(nch)
+    ins = datagen.rank_inputs(7, "normal", R, nch[0] * ce, dtype)
+    got = interpret_fused(s.instrs(), R, nch, ce, dtype, ins)
+    want, _, _ = oracle.run(ops, R, nch, ce, dtype, ins)
+    for r in range(R):
+        assert np.array_equal(got[r].view(np.uint8), want[r].view(np.uint8)), f"rank {r}"
+
+
+def random_program(seed, R=3, C=4, nops=40):
+    rng = np.random.default_rng(seed)
+    ops = []
+    while len(ops) < nops:
+        op = int(rng.integers(0, 2))
+        sr, dr = int(rng.integers(0, R)), int(rng.integers(0, R))
+        sb = int(rng.choice([0, 1, 2]))
+        db = int(rng.choice([1, 2]))          # never write inputs
+        cnt = int(rng.integers(1, 3))
+        so, do = int(rng.integers(0, C - cnt + 1)), int(rng.integers(0, C - cnt + 1))
+        if sr == dr and sb == db and so < do + cnt and do < so + cnt:
+            continue
+        ops.append((op, sr, sb, so, dr, db, do, cnt))
+    return ops, (C, C, C)
+
+
+@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("fuse", [True, False])
+def test_random_programs_fused_equal_oracle(seed, fuse):
+    ops, nch = random_program(seed)
+    R, ce = 3, 3
+    s = ccl.Schedule.compile(ops, R, nch, fuse=fuse)
+    ins = datagen.rank_inputs(seed, "int", R, nch[0] * ce, I32)
+    # scratch starts as the sentinel on both sides; reads of it are part of
+    # the program, so both must start from the same bytes
+    got = interpret_fused(s.instrs(), R, nch, ce, I32, ins)
+    want, _, _ = oracle.run(np.array(ops), R, nch, ce, I32, ins)
+    for r in range(R):
+        assert np.array_equal(got[r], want[r])
+    ins = datagen.rank_inputs(seed, "normal", R, nch[0] * ce, F16)
+    got = interpret_fused(s.instrs(), R, nch, ce, F16, ins)
+    want, _, _ = oracle.run(np.array(ops), R, nch, ce, F16, ins)
+    for r in range(R):
+        assert np.array_equal(got[r], want[r])
+
+
+@pytest.mark.parametrize("bad", [
+    [(0, 0, 0, 0, 0, 0, 0, 1)],            # overlapping source and destination
+    [(0, 0, 0, 3, 1, 1, 0, 2)],            # source range outside the buffer
+    [(0, 5, 0, 0, 1, 1, 0, 1)],            # rank out of range
+    [(0, 0, 0, 0, 1, 1, 0, 0)],            # empty count
+    [(9, 0, 0, 0, 1, 1, 0, 1)],            # unknown opcode
+    [(0, 0, 4, 0, 1, 1, 0, 1)],            # unknown buffer kind
+])
+def test_invalid_programs_are_rejected(bad):
+    with pytest.raises(ccl.CclError) as e:
+        ccl.Schedule.compile(bad, 2, (4, 4, 0))
+    assert e.value.code == 1
+
+
+# ------------------------------------------------------------------ planner
+
+@pytest.mark.parametrize("kind,R,G", [(0, 8, 0), (3, 16, 8), (4, 32, 8), (5, 24, 8), (1, 8, 0)])
+@pytest.mark.parametrize("sched", [ccl.SCHED_RR, ccl.SCHED_HPDS])
+def test_subpipelines_respect_links_and_dependencies(kind, R, G, sched):
+    s = ccl.Schedule.builtin(kind, R, G)
+    sp, nsub = s.timeline(sched)
+    instrs = s.instrs()
+    # transfers: (sender, receiver) of each transfer id
+    ends = {}
+    for i in instrs:
+        if i["xfer_out"] >= 0:
+            ends.setdefault(i["xfer_out"], {})["snd"] = i
+        if i["xfer_in"] >= 0:
+            ends.setdefault(i["xfer_in"], {})["rcv"] = i
+    seen = {}
+    for x, e in ends.items():
+        link = (e["snd"]["rank"], e["rcv"]["rank"])
+        assert (sp[x], link) not in seen, "two transfers on one link in one sub-pipeline"
+        seen[(sp[x], link)] = x
+        # a forwarded transfer comes after the one it forwards
+        if e["snd"]["xfer_in"] >= 0:
+            assert sp[x] > sp[e["snd"]["xfer_in"]]
+    assert 0 <= min(sp) and max(sp) < nsub
+
+
+def test_hpds_prioritises_least_scheduled_chunks():
+    """Chunk 0 fans out from rank 0 on three links while chunk 1 takes one
+    link; both then want link 1->2.  Round-robin keeps program order (chunk
+    0 first); HPDS serves the chunk with fewer scheduled tasks (chunk 1)."""
+    ops = [(0, 0, 0, 0, 1, 2, 0, 1), (0, 0, 0, 0, 2, 2, 0, 1), (0, 0, 0, 0, 3, 2, 0, 1),
+           (0, 3, 0, 1, 1, 2, 1, 1),
+           (0, 1, 2, 0, 2, 1, 0, 1), (0, 1, 2, 1, 2, 1, 1, 1)]
+    s = ccl.Schedule.compile(ops, 4, (2, 2, 2))
+    assert s.timeline(ccl.SCHED_RR) == ([0, 0, 0, 0, 1, 2], 3)
+    assert s.timeline(ccl.SCHED_HPDS) == ([0, 0, 0, 0, 2, 1], 3)
+    # the ring keeps its 2 (R - 1) steps under both
+    r = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 8)
+    assert r.timeline(ccl.SCHED_HPDS)[1] == r.timeline(ccl.SCHED_RR)[1] == 2 * (8 - 1)
+
+
+@pytest.mark.parametrize("kind,R,G", [(0, 8, 0), (3, 16, 8), (4, 32, 8), (5, 24, 8)])
+def test_state_based_packing_never_adds_threadblocks(kind, R, G):
+    s = ccl.Schedule.builtin(kind, R, G)
+    a = s.check(1024, F32, tb_alloc=ccl.TB_CONNECTION, link_mode=ccl.LINK_FIFO, channel_scaling=0)
+    b = s.check(1024, F32, tb_alloc=ccl.TB_PACKED, link_mode=ccl.LINK_FIFO, channel_scaling=0)
+    assert b.nthreadblocks <= a.nthreadblocks
+    assert b.nthreadblocks_connection == a.nthreadblocks
+
+
+def test_packing_merges_idle_inter_group_threadblocks():
+    s = ccl.Schedule.builtin(ccl.HIER_ALLREDUCE, 16, 8)
+    a = s.check(1024, F32, tb_alloc=ccl.TB_CONNECTION, microbatches=4, channel_scaling=0)
+    b = s.check(1024, F32, tb_alloc=ccl.TB_PACKED, microbatches=4, channel_scaling=0)
+    assert b.nthreadblocks == a.nthreadblocks // 2
+
+
+def test_direct_transport_removes_fifos_from_alltoall():
+    s = ccl.Schedule.builtin(ccl.ALLTOALL_2PHASE, 32, 8)
+    fifo = s.check(1024, F16, link_mode=ccl.LINK_FIFO)
+    direct = s.check(1024, F16, link_mode=ccl.LINK_DIRECT)
+    assert direct.nlinks == 0 and fifo.nlinks > 0
+    # per rank (G = 8, 4 groups): 7 peers x 4 blocks in the intra-group
+    # phase, 3 peers x 8 blocks in the inter-group phase, 4 blocks copied
+    # locally.  A FIFO transfer costs 4 bytes per element byte (staging
+    # write + read), a direct one 2, like a copy.
+    blk = 1024 * 2
+    sent, copied = 32 * (7 * 4 + 3 * 8), 32 * 4
+    assert fifo.schedule_bytes == blk * (4 * sent + 2 * copied)
+    assert direct.schedule_bytes == blk * 2 * (sent + copied)
+
+
+def test_channel_scaling_gives_small_instructions_fewer_threadblocks():
+    s = ccl.Schedule.builtin(ccl.ALLTONEXT, 24, 8)
+    flat = s.check(4096, F32, channels=8, channel_scaling=0)
+    scaled = s.check(4096, F32, channels=8, channel_scaling=1)
+    assert scaled.nthreadblocks < flat.nthreadblocks
+    assert scaled.schedule_bytes == flat.schedule_bytes
+
+
+def test_task_order_ring_with_big_pieces_is_rejected_as_deadlock():
+    """Each ring step must run all its micro-batches before the next, while
+    the neighbour does the same: with a piece larger than the FIFO nobody can
+    finish; the simulator rejects the plan instead of launching it."""
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 4)
+    with pytest.raises(ccl.CclError) as e:
+        s.check(65536, F32, mb_order=ccl.MB_TASK, microbatches=1, slot_bytes=4096, fifo_slots=2)
+    assert e.value.code == 3
+    st = s.check(65536, F32, mb_order=ccl.MB_AUTO, slot_bytes=4096, fifo_slots=2)
+    assert st.microbatches > 1
+
+
+def test_plan_options_are_validated():
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 4)
+    for kw in (dict(channels=300), dict(nthreads=100), dict(slot_bytes=24), dict(fifo_slots=1),
+               dict(tile_bytes=70000), dict(link_mode=5), dict(scheduler=7)):
+        with pytest.raises(ccl.CclError) as e:
+            s.check(1024, F32, **kw)
+        assert e.value.code == 1, kw
+    with pytest.raises(ccl.CclError):
+        s.check(0, F32)
+
+
+def test_channels_split_in_16_byte_units_and_keep_bytes():
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 8)
+    base = s.check(1000, BF16, channels=1)
+    for p in (2, 3, 7):
+        st = s.check(1000, BF16, channels=p, channel_scaling=0)
+        assert st.schedule_bytes == base.schedule_bytes
+        assert st.nthreadblocks == 8 * p
+
+
+# -------------------------------------------------------------------- tuner
+
+def _surface(peak):
+    c0, t0, s0 = peak
+
+    def f(o):
+        return math.exp(-(math.log2(o.channels) - math.log2(c0)) ** 2 - (math.log2(o.nthreads) - math.log2(t0)) ** 2
+                        - (math.log2(o.slot_bytes) - math.log2(s0)) ** 2)
+    return f
+
+
+@pytest.mark.parametrize("peak", [(12, 256, 1 << 18), (1, 1024, 1 << 14), (48, 128, 1 << 22), (4, 512, 1 << 17)])
+def test_coordinate_descent_reaches_the_peak_of_unimodal_surfaces(peak):
+    best, bw, n = ccl.tune_search(_surface(peak))
+    assert (best.channels, best.nthreads, best.slot_bytes) == peak
+    assert bw == pytest.approx(1.0)
+    assert n < 9 * 4 * 9 // 2      # far fewer probes than the full grid (per subspace)
+
+
+def test_coordinate_descent_treats_infeasible_points_as_zero():
+    f = _surface((24, 512, 1 << 17))
+
+    def g(o):
+        return 0.0 if o.channels > 16 else f(o)   # too many threadblocks
+    best, bw, n = ccl.tune_search(g)
+    assert best.channels == 16 and bw > 0
+
+
+def test_coordinate_descent_plateau_stops_early():
+    best, bw, n = ccl.tune_search(lambda o: 1.0)
+    assert bw == 1.0 and n <= 20
