@@ -68,7 +68,7 @@ class PlanOpts(ctypes.Structure):
                 ("fifo_slots", ctypes.c_int32), ("microbatches", ctypes.c_int32), ("scheduler", ctypes.c_int32),
                 ("tb_alloc", ctypes.c_int32), ("mb_order", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("instrument", ctypes.c_int32), ("tile_bytes", ctypes.c_int64), ("bulk", ctypes.c_int32),
-                ("link_mode", ctypes.c_int32), ("channel_scaling", ctypes.c_int32), ("pad", ctypes.c_int32)]
+                ("link_mode", ctypes.c_int32), ("channel_scaling", ctypes.c_int32), ("mb_window", ctypes.c_int32)]
 
 
 class PlanStats(ctypes.Structure):
@@ -80,7 +80,7 @@ class PlanStats(ctypes.Structure):
                 ("channels", ctypes.c_int32), ("nthreads", ctypes.c_int32), ("fifo_slots", ctypes.c_int32),
                 ("slot_bytes", ctypes.c_int64), ("fifo_bytes", ctypes.c_int64), ("device_bytes", ctypes.c_int64),
                 ("compile_ms", ctypes.c_double), ("tile_bytes", ctypes.c_int64), ("stages", ctypes.c_int32),
-                ("pad", ctypes.c_int32)]
+                ("mb_window", ctypes.c_int32)]
 
 
 class TuneOpts(ctypes.Structure):
@@ -115,6 +115,8 @@ def _load():
         "ccl_plan_stats": [P, ctypes.POINTER(PlanStats)],
         "ccl_plan_timeline": [P, ctypes.POINTER(ctypes.c_double), I32_, ctypes.POINTER(ctypes.c_double),
                               ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
+        "ccl_plan_timeline_raw": [P, ctypes.POINTER(ctypes.c_uint64), I64_, ctypes.POINTER(ctypes.c_int32), I32_,
+                                  ctypes.POINTER(ctypes.c_int64)],
         "ccl_plan_debug_drop_signal": [P, I32_, I32_],
         "ccl_plan_check": [P, I64_, I32_, ctypes.POINTER(PlanOpts), ctypes.POINTER(PlanStats)],
         "ccl_schedule_timeline": [P, I32_, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
@@ -284,6 +286,19 @@ class Plan:
         _check(lib.ccl_plan_timeline(self._h, idle, st.nthreadblocks, ctypes.byref(mean), ctypes.byref(mx),
                                      ctypes.byref(span)))
         return {"idle": list(idle), "mean_idle": mean.value, "max_idle": mx.value, "span_us": span.value}
+
+    def timeline_raw(self):
+        """(start_ns, waited_ns, end_ns) per step as an (nsteps, 3) uint64 array,
+        and the first step of every threadblock (ntb + 1 entries)."""
+        import numpy as np
+        st = self.stats()
+        n = ctypes.c_int64()
+        tb = (ctypes.c_int32 * (st.nthreadblocks + 1))()
+        _check(lib.ccl_plan_timeline_raw(self._h, None, 0, tb, st.nthreadblocks + 1, ctypes.byref(n)))
+        buf = np.zeros(3 * n.value, dtype=np.uint64)
+        _check(lib.ccl_plan_timeline_raw(self._h, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), buf.size, tb,
+                                         st.nthreadblocks + 1, None))
+        return buf.reshape(-1, 3), list(tb)
 
     def debug_drop_signal(self, tb, step):
         _check(lib.ccl_plan_debug_drop_signal(self._h, tb, step))

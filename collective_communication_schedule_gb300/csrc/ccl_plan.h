@@ -39,9 +39,9 @@ struct DStep {
     int32_t dep_begin;  // waits: deps[dep_begin .. dep_begin + dep_count)
     int32_t dep_count;
     int32_t signal;     // counter to post after the step, or -1
-    int32_t flags;      // bit 0: do not post link flags (debug hook); bit 1: depends on an
-                        // earlier step of the same threadblock (drain in-flight slots first)
-    int32_t pad;
+    int32_t flags;      // bit 0: do not post link flags (debug hook)
+    int32_t drain;      // latest earlier step of the same threadblock whose tiles must be
+                        // finished before this step starts (global step index), or -1
 };
 static_assert(sizeof(DStep) == 64, "DStep layout");
 
@@ -53,7 +53,8 @@ struct DRec {
     int32_t nslots, dep_begin, dep_count, signal, mb, flags;
     int64_t src_off, loc_off, dst_off;   // element offsets of this piece
     int64_t nelem, seq_in, seq_out;
-    int64_t pad[2];
+    int32_t drain, pad0;
+    int64_t pad1;
 };
 static_assert(sizeof(DRec) == 128, "DRec layout");
 
@@ -94,6 +95,7 @@ struct PlanImage {
     int32_t m = 1;
     int32_t channels = 1;
     int32_t mb_order = CCL_MB_ALGO;
+    int32_t mb_window = 1;           // micro-batches interleaved per instruction inside a segment
     int32_t nsubpipelines = 0;
     int32_t ntb_connection = 0;
     int32_t dtype = CCL_F32;

@@ -21,7 +21,11 @@
 //     other, which is ReSCCL's task-level execution.  ALGO cuts only where the
 //     epoch changes (a whole-instruction dependency lies between), SEGMENT also
 //     at idle gaps of the threadblock's timeline, TASK before every
-//     instruction.
+//     instruction.  Inside a segment the micro-batches may be taken in
+//     windows of w: every instruction of the segment in turn runs the w
+//     micro-batches of the window, so a threadblock holds w independent
+//     pieces of one instruction while the piece its next instruction needs
+//     is still upstream (w = 1: strictly micro-batch-major).
 //  4. Geometry.  Every instruction range is split into `channels` pieces and
 //     every channel piece into `m` micro-batch pieces, both in 16-byte units
 //     (the element tail goes to the last piece); a piece moves through the
@@ -315,7 +319,7 @@ void fill_records(PlanImage* img)
         r.loc_buf = in.loc_buf; r.loc_rank = in.loc_rank;
         r.dst_buf = in.dst_buf; r.dst_rank = in.dst_rank;
         r.nslots = st.nslots; r.dep_begin = st.dep_begin; r.dep_count = st.dep_count;
-        r.signal = st.signal; r.mb = st.mb; r.flags = st.flags;
+        r.signal = st.signal; r.mb = st.mb; r.flags = st.flags; r.drain = st.drain;
         r.src_off = in.src_off + st.elem_off;
         r.loc_off = in.loc_off + st.elem_off;
         r.dst_off = in.dst_off + st.elem_off;
@@ -346,7 +350,7 @@ struct Attempt {
 
 ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList& tbs,
                          const std::vector<int>& tb_rank, int64_t ce, int dtype,
-                         const ccl_plan_opts_t& o, int m, int order, PlanImage* img)
+                         const ccl_plan_opts_t& o, int m, int order, int window, PlanImage* img)
 {
     const int ni = (int)s.instrs.size();
     const int p = o.channels;
@@ -368,6 +372,7 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     img->m = m;
     img->channels = p;
     img->mb_order = order;
+    img->mb_window = window;
     img->S = S;
     img->slot_bytes = o.slot_bytes;
     img->tile_bytes = o.tile_bytes;
@@ -469,9 +474,11 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
             for (int i : tbs[t])
                 if (pc[i] > ch) prog.push_back(i);
             auto segs = make_segments(tl, prog, order, ep);
+            // window by window; inside a window instruction-major
             for (auto& seg : segs) {
-                for (int mb = 0; mb < m; ++mb) {
-                    for (int i : seg) {
+                for (int w0 = 0; w0 < m; w0 += window) {
+                    const int w1 = std::min(m, w0 + window);
+                    for (int i : seg) for (int mb = w0; mb < w1; ++mb) {
                         int ci = i * p + ch;
                         const DInstr& D = img->instrs[ci];
                         Piece pc = split(D.nelem, ve, m, mb);
@@ -487,6 +494,7 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
                         st.dep_count = 0;
                         st.signal = -1;
                         st.flags = 0;
+                        st.drain = -1;
                         step_of[ci][mb] = (int)img->steps.size();
                         img->steps.push_back(st);
                     }
@@ -550,11 +558,24 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
         for (const Dep& d : s.deps) {
             for (int ch = 0; ch < pc[d.to]; ++ch) {
                 int cb = d.to * p + ch;
-                // a producer in the same threadblock: its slots must have
-                // left the data warps before this instruction starts
-                for (int ch2 = 0; ch2 < pc[d.from]; ++ch2)
-                    if (dev_tb_of[(size_t)d.from * p + ch2] == dev_tb_of[cb])
-                        for (int mb = 0; mb < m; ++mb) img->steps[step_of[cb][mb]].flags |= 2;
+                // a producer in the same threadblock comes earlier in its
+                // program; its tiles must have left the data path before the
+                // consumer starts: the same micro-batch of the same channel
+                // when the ranges are identical, every piece otherwise
+                const bool same_range = d.exact && pc[d.from] == pc[d.to];
+                for (int ch2 = 0; ch2 < pc[d.from]; ++ch2) {
+                    const int ca2 = d.from * p + ch2;
+                    if (dev_tb_of[ca2] != dev_tb_of[cb] || (same_range && ch2 != ch)) continue;
+                    int all = -1;
+                    for (int mb = 0; mb < m; ++mb) all = std::max(all, step_of[ca2][mb]);
+                    for (int mb = 0; mb < m; ++mb) {
+                        DStep& c = img->steps[step_of[cb][mb]];
+                        const int need = same_range ? step_of[ca2][mb] : all;
+                        if (need >= step_of[cb][mb])
+                            return fail(CCL_ERR_DEADLOCK, "a producer follows its consumer in one threadblock");
+                        c.drain = std::max(c.drain, need);
+                    }
+                }
                 if (d.exact && pc[d.from] == pc[d.to]) {
                     int ca = d.from * p + ch;
                     if (dev_tb_of[ca] == dev_tb_of[cb]) continue;
@@ -800,6 +821,7 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
     if (o.scheduler != CCL_SCHED_RR && o.scheduler != CCL_SCHED_HPDS) return fail(CCL_ERR_INVALID_ARG, "unknown scheduler");
     if (o.tb_alloc != CCL_TB_CONNECTION && o.tb_alloc != CCL_TB_PACKED) return fail(CCL_ERR_INVALID_ARG, "unknown tb_alloc");
     if (o.mb_order < CCL_MB_AUTO || o.mb_order > CCL_MB_SEGMENT) return fail(CCL_ERR_INVALID_ARG, "unknown mb_order");
+    if (o.mb_window < 0 || o.mb_window > 65536) return fail(CCL_ERR_INVALID_ARG, "mb_window out of range");
     if (o.timeout_ms <= 0) return fail(CCL_ERR_INVALID_ARG, "timeout_ms must be positive");
 
     if (o.link_mode != CCL_LINK_FIFO && o.link_mode != CCL_LINK_DIRECT)
@@ -847,11 +869,22 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
         const TBList& tbs = alloc == CCL_TB_PACKED ? packed : conn;
         const std::vector<int>& tr = alloc == CCL_TB_PACKED ? packed_rank : conn_rank;
         for (int m : ms) {
-            for (int order : orders) {
+            std::vector<int> wins;
+            if (o.mb_window > 0) wins.push_back(std::min(m, o.mb_window));
+            else {
+                const int w = std::max(1, std::min(m, o.fifo_slots - 1));
+                wins.push_back(w);
+                if (w > 1) wins.push_back(1);
+            }
+            for (int order : orders) for (int window : wins) {
                 PlanImage cand;
-                st = build_image(s, tl, tbs, tr, ce, dtype, o, m, order, &cand);
-                if (st != CCL_OK) return st;
+                st = build_image(s, tl, tbs, tr, ce, dtype, o, m, order, window, &cand);
                 std::string why;
+                if (st == CCL_ERR_DEADLOCK) {
+                    if (first_why.empty()) first_why = ccl_last_error_detail();
+                    continue;
+                }
+                if (st != CCL_OK) return st;
                 if (log_level() >= 2) dump_programs(s, tl, tbs, tr, m, order);
                 if (simulate_plan(cand, &why)) {
                     *img = std::move(cand);
@@ -860,7 +893,8 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
                     goto done;
                 }
                 if (first_why.empty())
-                    first_why = "m=" + std::to_string(m) + " order=" + std::to_string(order) + ": " + why;
+                    first_why = "m=" + std::to_string(m) + " order=" + std::to_string(order) +
+                                " window=" + std::to_string(window) + ": " + why;
             }
         }
     }
@@ -868,6 +902,18 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
                                       " FIFO slots of " + std::to_string(o.slot_bytes) + " bytes (" + first_why + ")");
 done:
     img->ndirect = ndirect;
+    if (log_level() >= 1) {
+        size_t drains = 0, waiting = 0;
+        for (const DStep& d : img->steps) {
+            drains += d.drain >= 0;
+            waiting += d.dep_count > 0;
+        }
+        std::fprintf(stderr,
+                     "[ccl] plan: %d threadblocks, %zu steps, m=%d order=%d window=%d, %zu steps follow an earlier "
+                     "step of their threadblock, %zu steps wait on %zu counters\n",
+                     img->ntb, img->steps.size(), img->m, img->mb_order, img->mb_window, drains, waiting,
+                     img->deps.size());
+    }
     // byte accounting of the source program
     {
         std::vector<std::vector<char>> rd(s.nranks, std::vector<char>(std::max(1, s.nchunks[0]), 0));

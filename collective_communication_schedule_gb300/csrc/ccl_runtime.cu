@@ -73,6 +73,11 @@ constexpr int kQ = 16;     // tile descriptors in flight
 constexpr int kNSMax = 8;  // shared-memory stages
 constexpr int kRetireDepth = 7;   // store groups left in flight when retiring
 constexpr int kCQ = 16;           // stored tiles awaiting completion (> kRetireDepth)
+// last descriptor of each of the latest kHist steps; every step hands out at
+// least one descriptor and descriptors are freed in order, so a step further
+// back than kQ + 1 steps is finished whenever the issuer runs
+constexpr int kHist = 32;
+static_assert(kHist > kQ, "history must reach past the descriptor ring");
 
 struct SlotOp {
     const char* a;      // data in: incoming slot or source buffer
@@ -105,6 +110,7 @@ struct CtlShared {
     unsigned long long done_b[kQ];      // the TMA thread is through with the descriptor
     unsigned long long freed[kQ];
     unsigned long long full[kNSMax];    // stage loaded
+    int last_head[kHist];               // issuer only: last descriptor of step si % kHist
 };
 
 __device__ __forceinline__ void record_timeout(const KParams& P, int si, int reason)
@@ -231,13 +237,16 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
         if (si + 1 < b1) prefetch_rec(&sh->rec[(si + 1) & 1], P.recs + si + 1);
         const unsigned long long t_start = gtimer();
         unsigned long long waited = 0;
-        if ((st.flags & 2) && head > 0 &&
-            !mbar_wait(&sh->freed[(head - 1) % kQ], (unsigned)(((head - 1) / kQ) & 1), limit)) {
-            // reads or writes what an earlier step of this threadblock touched:
-            // every handed-out tile must be finished first
-            record_timeout(P, si, WAIT_DONE);
-            publish_cmd(2);
-            return;
+        if (st.drain >= 0 && si - st.drain < kHist) {
+            // reads or writes what an earlier step of this threadblock
+            // touched: that step's last tile (and so, freed in order, all of
+            // its tiles) must be finished first
+            const int h = sh->last_head[st.drain % kHist];
+            if (h >= head - kQ && !mbar_wait(&sh->freed[h % kQ], (unsigned)((h / kQ) & 1), limit)) {
+                record_timeout(P, si, WAIT_DONE);
+                publish_cmd(2);
+                return;
+            }
         }
         for (int k = 0; k < st.dep_count; ++k) {
             const DDep d = P.deps[st.dep_begin + k];
@@ -339,6 +348,7 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
                 ++head;
             }
         }
+        sh->last_head[si % kHist] = head - 1;
     }
     publish_cmd(1);
 }
@@ -613,6 +623,7 @@ ccl_plan_opts_t merged_opts(const ccl_plan_opts_t* opts)
         o.bulk = opts->bulk;
         o.link_mode = opts->link_mode;
         o.channel_scaling = opts->channel_scaling;
+        o.mb_window = opts->mb_window;
     }
     return o;
 }
@@ -639,6 +650,7 @@ void fill_stats(const ccl::PlanImage& img, ccl_plan_stats_t* st)
     st->fifo_bytes = img.fifo_bytes;
     st->tile_bytes = img.tile_bytes;
     st->stages = img.ns;
+    st->mb_window = img.mb_window;
 }
 
 void free_plan(ccl_plan* p)
@@ -708,7 +720,7 @@ void ccl_plan_opts_default(ccl_plan_opts_t* o)
     o->bulk = 0;
     o->link_mode = CCL_LINK_DIRECT;
     o->channel_scaling = 1;
-    o->pad = 0;
+    o->mb_window = 0;
 }
 
 ccl_status_t ccl_schedule_compile(const ccl_op_t* ops, int32_t nops, int32_t nranks, const int32_t nchunks[3],
@@ -1025,11 +1037,29 @@ ccl_status_t ccl_plan_timeline(ccl_plan_t p, double* idle, int32_t cap, double* 
     double span = hi > lo ? (double)(hi - lo) : 1.0;
     double sum = 0, mx = 0;
     for (int b = 0; b < img.ntb; ++b) {
-        double busy = 0;
+        // steps of one threadblock overlap (the issuer runs ahead of the data
+        // path): busy time is the length of the union of the intervals from
+        // the end of each step's waits to the post of its last tile
+        std::vector<std::pair<unsigned long long, unsigned long long>> iv;
         for (int k = img.tb_begin[b]; k < img.tb_begin[b + 1]; ++k) {
-            double d = (double)(t[3 * k + 2] - t[3 * k]) - (double)t[3 * k + 1];
-            busy += std::max(0.0, d);
+            const unsigned long long s0 = t[3 * k] + t[3 * k + 1], s1 = t[3 * k + 2];
+            if (s1 > s0) iv.emplace_back(s0, s1);
         }
+        std::sort(iv.begin(), iv.end());
+        double busy = 0;
+        unsigned long long cur0 = 0, cur1 = 0;
+        bool open = false;
+        for (const auto& e : iv) {
+            if (open && e.first <= cur1) {
+                cur1 = std::max(cur1, e.second);
+                continue;
+            }
+            if (open) busy += (double)(cur1 - cur0);
+            cur0 = e.first;
+            cur1 = e.second;
+            open = true;
+        }
+        if (open) busy += (double)(cur1 - cur0);
         double id = std::min(1.0, std::max(0.0, 1.0 - busy / span));
         if (idle) idle[b] = id;
         sum += id;
@@ -1038,6 +1068,24 @@ ccl_status_t ccl_plan_timeline(ccl_plan_t p, double* idle, int32_t cap, double* 
     if (mean_idle) *mean_idle = img.ntb ? sum / img.ntb : 0;
     if (max_idle) *max_idle = mx;
     if (span_us) *span_us = span / 1000.0;
+    return CCL_OK;
+}
+
+ccl_status_t ccl_plan_timeline_raw(ccl_plan_t p, uint64_t* stamps, int64_t cap, int32_t* tb_begin,
+                                   int32_t tb_cap, int64_t* nsteps)
+{
+    if (!p) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    const ccl::PlanImage& img = p->img;
+    if (nsteps) *nsteps = (int64_t)img.steps.size();
+    if (tb_begin) {
+        if (tb_cap < img.ntb + 1) return ccl::fail(CCL_ERR_INVALID_ARG, "threadblock capacity too small");
+        for (int b = 0; b <= img.ntb; ++b) tb_begin[b] = img.tb_begin[b];
+    }
+    if (!stamps) return CCL_OK;
+    if (!p->d_timeline) return ccl::fail(CCL_ERR_INVALID_ARG, "plan was created without instrumentation");
+    if (cap < 3 * (int64_t)img.steps.size()) return ccl::fail(CCL_ERR_INVALID_ARG, "capacity too small");
+    CUDA_TRY(cudaDeviceSynchronize(), "synchronize");
+    CUDA_TRY(cudaMemcpy(stamps, p->d_timeline, img.steps.size() * 3 * 8, cudaMemcpyDeviceToHost), "read timeline");
     return CCL_OK;
 }
 

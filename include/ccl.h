@@ -205,6 +205,15 @@ typedef enum { CCL_LINK_FIFO = 0, CCL_LINK_DIRECT = 1 } ccl_link_mode_t;
  *                 instruction (each runs all its micro-batches first:
  *                 task-level execution); AUTO tries ALGO, SEGMENT, TASK in
  *                 that order and keeps the first that can finish.
+ *   mb_window   : micro-batches a segment interleaves.  The segment runs its
+ *                 micro-batches in windows of this many: each instruction
+ *                 of the segment in turn takes every micro-batch of the
+ *                 window, so a step has up to mb_window - 1 independent
+ *                 pieces ahead of it in its own threadblock while the piece
+ *                 it depends on is still in flight upstream.  1 = one
+ *                 micro-batch at a time through the whole segment; 0 =
+ *                 auto: min(m, fifo_slots - 1) first, then 1, keeping the
+ *                 first that can finish.
  *   timeout_ms  : limit of every device flag wait.
  *   instrument  : 1 = record per-step global-timer stamps (ccl_plan_timeline).
  *   tile_bytes  : the executor moves a slot in tiles of this size (multiple of
@@ -237,7 +246,7 @@ typedef struct {
     int32_t bulk;
     int32_t link_mode;
     int32_t channel_scaling;
-    int32_t pad;
+    int32_t mb_window;
 } ccl_plan_opts_t;
 
 void ccl_plan_opts_default(ccl_plan_opts_t* o);
@@ -303,7 +312,7 @@ typedef struct {
     double compile_ms;           /* host time of ccl_plan_create */
     int64_t tile_bytes;          /* tile of the data path */
     int32_t stages;              /* shared-memory stages of the bulk path (0: registers only) */
-    int32_t pad;
+    int32_t mb_window;           /* micro-batch window actually used */
 } ccl_plan_stats_t;
 
 ccl_status_t ccl_plan_stats(ccl_plan_t p, ccl_plan_stats_t* st);
@@ -328,12 +337,27 @@ ccl_status_t ccl_schedule_timeline(ccl_schedule_t s, int32_t scheduler, int32_t*
 /*
  * Threadblock utilisation of the last execution of an instrumented plan
  * (ReSCCL report, §III: mean and maximum threadblock idle rate).  For each
- * threadblock b: busy[b] = time spent moving data, span = first start to
- * last end over all threadblocks; idle[b] = 1 - busy[b] / span.  Arrays of
- * capacity cap (>= nthreadblocks).  Synchronizes the device.
+ * threadblock b: busy[b] = length of the union, over its steps, of the
+ * interval from the end of the step's waits to the post of its last tile
+ * (steps of one threadblock overlap); span = first start to last end over
+ * all threadblocks; idle[b] = 1 - busy[b] / span.  Arrays of capacity cap
+ * (>= nthreadblocks).  Synchronizes the device.
  */
 ccl_status_t ccl_plan_timeline(ccl_plan_t p, double* idle, int32_t cap, double* mean_idle,
                                double* max_idle, double* span_us);
+
+/*
+ * Raw stamps of the last execution of an instrumented plan, three per step
+ * in threadblock-program order: the global-timer time (ns) the issuer took
+ * the step up, the ns it spent waiting for dependency counters and FIFO
+ * flags, and the time the last tile's flags were posted.  stamps: capacity
+ * cap (>= 3 * nsteps) or NULL; tb_begin: capacity tb_cap (>= nthreadblocks
+ * + 1) or NULL, the first step of every threadblock; *nsteps (may be NULL)
+ * receives the step count.  With stamps non-NULL the plan must have been
+ * created with instrument = 1; synchronizes the device.
+ */
+ccl_status_t ccl_plan_timeline_raw(ccl_plan_t p, uint64_t* stamps, int64_t cap, int32_t* tb_begin,
+                                   int32_t tb_cap, int64_t* nsteps);
 
 /*
  * Test hook: make threadblock `tb` skip the flag post of its step `step`

@@ -345,3 +345,27 @@ def test_coordinate_descent_treats_infeasible_points_as_zero():
 def test_coordinate_descent_plateau_stops_early():
     best, bw, n = ccl.tune_search(lambda o: 1.0)
     assert bw == 1.0 and n <= 20
+
+
+def test_microbatch_window_is_used_when_the_fifo_holds_it():
+    s = ccl.Schedule.builtin(ccl.HIER_ALLREDUCE, 16, 8)
+    kw = dict(channels=2, microbatches=8, tb_alloc=ccl.TB_PACKED, slot_bytes=65536, mb_order=ccl.MB_ALGO)
+    assert s.check(65536, F32, fifo_slots=4, mb_window=1, **kw).mb_window == 1
+    # auto: min(m, fifo_slots - 1)
+    assert s.check(65536, F32, fifo_slots=4, mb_window=0, **kw).mb_window == 3
+    assert s.check(65536, F32, fifo_slots=9, mb_window=0, **kw).mb_window == 8
+    # same steps and bytes in another order
+    a = s.check(65536, F32, fifo_slots=9, mb_window=1, **kw)
+    b = s.check(65536, F32, fifo_slots=9, mb_window=8, **kw)
+    assert (a.nsteps, a.schedule_bytes) == (b.nsteps, b.schedule_bytes)
+
+
+def test_microbatch_window_larger_than_the_fifo_is_rejected():
+    """A ring step that must send a whole window before its neighbour reads
+    any of it needs window + 1 slots per link."""
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 4)
+    with pytest.raises(ccl.CclError) as e:
+        s.check(65536, F32, microbatches=8, mb_window=8, fifo_slots=4, slot_bytes=32768, mb_order=ccl.MB_ALGO)
+    assert e.value.code == 3
+    st = s.check(65536, F32, microbatches=8, mb_window=8, fifo_slots=9, slot_bytes=32768, mb_order=ccl.MB_ALGO)
+    assert st.mb_window == 8

@@ -124,3 +124,16 @@ def test_transport_and_data_path_do_not_change_bits(ccl, kind, R, G, link_mode, 
         got, want, _ = run_case(ccl, kind, R, G, ce, dtype, DIST[dtype], 21, link_mode=link_mode, bulk=bulk,
                                 tile_bytes=4096, slot_bytes=8192)
         assert_bitexact(got, want)
+
+
+@pytest.mark.parametrize("window", [1, 2, 3, 8])
+@pytest.mark.parametrize("order", [1, 3])
+def test_microbatch_windows_do_not_change_bits(ccl, window, order):
+    """Micro-batches interleaved per instruction in windows of 1..8, with
+    FIFOs deep enough for the window (pieces of one slot)."""
+    for kind, R, G in [(3, 16, 8), (0, 8, 0), (5, 12, 4), (2, 5, 0)]:
+        got, want, plan = run_case(ccl, kind, R, G, 4096, F32, "normal", 5, microbatches=8, mb_order=order,
+                                   mb_window=window, fifo_slots=window + 1 if window > 1 else 4, slot_bytes=4096,
+                                   tb_alloc=1, link_mode=0)
+        assert_bitexact(got, want)
+        assert plan.stats().mb_window in (window, 1)
