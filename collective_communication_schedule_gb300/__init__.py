@@ -288,17 +288,18 @@ class Plan:
         return {"idle": list(idle), "mean_idle": mean.value, "max_idle": mx.value, "span_us": span.value}
 
     def timeline_raw(self):
-        """(start_ns, waited_ns, end_ns) per step as an (nsteps, 3) uint64 array,
-        and the first step of every threadblock (ntb + 1 entries)."""
+        """(start, waited, first tile handed out, last tile done, posted) in ns
+        per step as an (nsteps, 5) uint64 array, and the first step of every
+        threadblock (ntb + 1 entries)."""
         import numpy as np
         st = self.stats()
         n = ctypes.c_int64()
         tb = (ctypes.c_int32 * (st.nthreadblocks + 1))()
         _check(lib.ccl_plan_timeline_raw(self._h, None, 0, tb, st.nthreadblocks + 1, ctypes.byref(n)))
-        buf = np.zeros(3 * n.value, dtype=np.uint64)
+        buf = np.zeros(5 * n.value, dtype=np.uint64)
         _check(lib.ccl_plan_timeline_raw(self._h, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), buf.size, tb,
                                          st.nthreadblocks + 1, None))
-        return buf.reshape(-1, 3), list(tb)
+        return buf.reshape(-1, 5), list(tb)
 
     def debug_drop_signal(self, tb, step):
         _check(lib.ccl_plan_debug_drop_signal(self._h, tb, step))

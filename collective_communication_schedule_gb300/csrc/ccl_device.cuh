@@ -139,11 +139,25 @@ __device__ __forceinline__ void move_vec(const uint4* a, bool as, const uint4* b
             if (o2) vstore(o2 + i + u * T, r, false);
         }
     }
-    for (; i < nv; i += T) {
-        uint4 r = vload(a + i, as);
-        if (RED) r = vadd<DT>(r, vload(b + i, bs));
-        vstore(o1 + i, r, o1s);
-        if (o2) vstore(o2 + i, r, false);
+    // what is left of this thread's vectors (at most U - 1) in one round:
+    // all of its loads in flight together instead of one round trip each
+    // (loads past the end re-read the last vector and are not used)
+    if (i < nv) {
+        uint4 va[U - 1], vb[U - 1];
+#pragma unroll
+        for (int u = 0; u < U - 1; ++u) {
+            const int64_t j = i + u * T < nv ? i + u * T : nv - 1;
+            va[u] = vload(a + j, as);
+            if (RED) vb[u] = vload(b + j, bs);
+        }
+#pragma unroll
+        for (int u = 0; u < U - 1; ++u)
+            if (i + u * T < nv) {
+                uint4 r = va[u];
+                if (RED) r = vadd<DT>(va[u], vb[u]);
+                vstore(o1 + i + u * T, r, o1s);
+                if (o2) vstore(o2 + i + u * T, r, false);
+            }
     }
 }
 
@@ -277,6 +291,21 @@ __device__ __forceinline__ void bulk_wait(int n)
 // shared memory)
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// test of the phase with the given parity that may suspend the thread for a
+// short, hardware-chosen time while the phase is incomplete (acquire at CTA
+// scope); false when the phase has not completed yet
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, unsigned parity)
+{
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 
 // non-blocking test of the phase with the given parity (acquire at CTA scope)
 __device__ __forceinline__ bool mbar_test(unsigned long long* bar, unsigned parity)

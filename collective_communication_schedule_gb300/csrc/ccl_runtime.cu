@@ -96,13 +96,16 @@ struct Release {
     unsigned long long* full;
     unsigned long long* counter;
     unsigned long long consumed_v, full_v, counter_v;
-    unsigned long long t_start, waited;
+    unsigned long long t_start, waited, t_pub;
     int si;
     int last;                      // last tile of its step
 };
 
+// steps whose first-slot flags the issuer polls in one round trip
+constexpr int kLook = 4;
+
 struct CtlShared {
-    DRec rec[2];
+    DRec rec[2 * kLook];                // two batches of step records (prefetched one batch ahead)
     SlotOp op[kQ];
     Release rel[kQ];
     unsigned long long ready[kQ];
@@ -122,18 +125,15 @@ __device__ __forceinline__ void record_timeout(const KParams& P, int si, int rea
     }
 }
 
-// bounded wait on an mbarrier phase inside the CTA
+// bounded wait on an mbarrier phase inside the CTA: try_wait suspends the
+// thread in hardware until the phase completes or a short time passes
 __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned par, unsigned long long limit_ns)
 {
-    unsigned spins = 0;
     unsigned long long t0 = 0;
-    while (!mbar_test(bar, par)) {
-        if ((++spins & 127) == 0) {
-            unsigned long long now = gtimer();
-            if (!t0) t0 = now;
-            else if (now - t0 > limit_ns) return false;
-        }
-        if (spins > 32) __nanosleep(20);
+    while (!mbar_try_wait(bar, par)) {
+        const unsigned long long now = gtimer();
+        if (!t0) t0 = now;
+        else if (now - t0 > limit_ns) return false;
     }
     return true;
 }
@@ -215,7 +215,74 @@ __device__ __forceinline__ void prefetch_rec(DRec* dst, const DRec* src)
     for (int k = 0; k < 8; ++k)
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + 16 * k), "l"((const char*)src + 16 * k)
                      : "memory");
-    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// flag word and value that say the first FIFO slot of a step may be read
+// (incoming slot full) or written (outgoing slot consumed S sequences ago)
+struct SlotCond {
+    const unsigned long long* in;
+    const unsigned long long* out;
+    unsigned long long vin, vout;
+};
+
+__device__ __forceinline__ SlotCond first_slot_cond(const KParams& P, const DRec& st)
+{
+    SlotCond c{nullptr, nullptr, 0, 0};
+    if (st.link_in >= 0) {
+        const DLink& L = P.links[st.link_in];
+        const unsigned long long s = (unsigned long long)(P.exec * L.total) + st.seq_in;
+        c.in = P.flags + L.flag_base + (int)(s % P.S);
+        c.vin = s + 1;
+    }
+    if (st.link_out >= 0) {
+        const DLink& L = P.links[st.link_out];
+        const unsigned long long s = (unsigned long long)(P.exec * L.total) + st.seq_out;
+        if (s + 1 > (unsigned long long)P.S) {
+            c.out = P.flags + L.flag_base + P.S + (int)(s % P.S);
+            c.vout = s + 1 - P.S;
+        }
+    }
+    return c;
+}
+
+// Poll the first-slot flags of steps [s0, s1) (records in the ring, no
+// dependency counters) with relaxed loads issued together; returns the end
+// of the leading run of ready steps (> s0) after one acquire fence, or -1
+// when the wait for step s0 fails.
+__device__ int poll_steps(const KParams& P, const CtlShared* sh, int s0, int s1, unsigned long long& waited)
+{
+    SlotCond c[kLook];
+    const int n = s1 - s0;
+#pragma unroll
+    for (int i = 0; i < kLook; ++i)
+        c[i] = i < n ? first_slot_cond(P, sh->rec[(s0 + i) % (2 * kLook)]) : SlotCond{nullptr, nullptr, 0, 0};
+    unsigned long long t0 = 0;
+    unsigned spins = 0;
+    while (true) {
+        unsigned long long x[kLook], y[kLook];
+#pragma unroll
+        for (int i = 0; i < kLook; ++i) {
+            x[i] = c[i].in ? ld_relaxed(c[i].in) : ~0ull;
+            y[i] = c[i].out ? ld_relaxed(c[i].out) : ~0ull;
+        }
+        int r = 0;
+        while (r < n && x[r] >= c[r].vin && y[r] >= c[r].vout) ++r;
+        if (r > 0) {
+            fence_acq_rel_gpu();
+            if (t0) waited += gtimer() - t0;
+            return s0 + r;
+        }
+        if (!t0) t0 = gtimer();
+        ++spins;
+        if ((spins & 15) == 0) {
+            if (*(volatile int*)P.status != 0) return -1;
+            if (gtimer() - t0 > P.timeout_ns) {
+                record_timeout(P, s0, x[0] < c[0].vin ? WAIT_FULL : WAIT_FREE);
+                return -1;
+            }
+        }
+        if (spins > 64) __nanosleep(32);
+    }
 }
 
 __device__ __forceinline__ bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
@@ -230,13 +297,35 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
         sh->op[q].cmd = cmd;
         mbar_arrive(&sh->ready[q]);
     };
-    if (b0 < b1) prefetch_rec(&sh->rec[b0 & 1], P.recs + b0);
+    // records arrive in batches of kLook, one batch ahead: [rec_ready,
+    // rec_end) is in flight, everything below rec_ready is in shared memory
+    int rec_ready = b0, rec_end = b0;
+    auto request = [&](int from) {
+        rec_end = from + kLook < b1 ? from + kLook : b1;
+        for (int j = from; j < rec_end; ++j) prefetch_rec(&sh->rec[j % (2 * kLook)], P.recs + j);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    if (b0 < b1) request(b0);
+    int cleared = b0;   // steps below: first-slot flags seen ready (and fenced)
     for (int si = b0; si < b1; ++si) {
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        const DRec& st = sh->rec[si & 1];
-        if (si + 1 < b1) prefetch_rec(&sh->rec[(si + 1) & 1], P.recs + si + 1);
+        if (si >= rec_ready) {
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            rec_ready = rec_end;
+            if (rec_end < b1) request(rec_end);
+        }
+        const DRec& st = sh->rec[si % (2 * kLook)];
         const unsigned long long t_start = gtimer();
-        unsigned long long waited = 0;
+        unsigned long long waited = 0, t_pub = 0;
+        if (si >= cleared && st.dep_count == 0) {
+            // one round trip for the next steps that wait on FIFO flags only
+            int s1 = si + 1;
+            while (s1 < rec_ready && s1 < si + kLook && sh->rec[s1 % (2 * kLook)].dep_count == 0) ++s1;
+            cleared = poll_steps(P, sh, si, s1, waited);
+            if (cleared < 0) {
+                publish_cmd(2);
+                return;
+            }
+        }
         if (st.drain >= 0 && si - st.drain < kHist) {
             // reads or writes what an earlier step of this threadblock
             // touched: that step's last tile (and so, freed in order, all of
@@ -274,7 +363,7 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
         const char* locb = st.loc_buf >= 0 ? P.bufs[st.loc_buf][st.loc_rank] + st.loc_off * es : nullptr;
         char* dstb = st.dst_buf >= 0 ? P.bufs[st.dst_buf][st.dst_rank] + st.dst_off * es : nullptr;
         const bool post = !(st.flags & 1);
-        int ready_slots = 0;   // slots whose flags were already seen ready
+        int ready_slots = si < cleared ? 1 : 0;   // slots whose flags were already seen ready
         for (long long k = 0; k < nslots; ++k) {
             const unsigned long long sin = base_in + st.seq_in + k;
             const unsigned long long sout = base_out + st.seq_out + k;
@@ -342,8 +431,10 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
                 r.counter = st.signal >= 0 ? P.counters + st.signal : nullptr;
                 r.counter_v = (unsigned long long)(P.exec * P.m + st.mb + 1);
                 r.si = si;
+                if (P.timeline && !t_pub) t_pub = gtimer();
                 r.t_start = t_start;
                 r.waited = waited;
+                r.t_pub = t_pub;
                 mbar_arrive(&sh->ready[q]);
                 ++head;
             }
@@ -377,6 +468,7 @@ __device__ void releaser(const KParams& P, CtlShared* sh)
             if (!mbar_test(&sh->done_g[q2], p2) || !mbar_test(&sh->done_b[q2], p2)) break;
             ++n;
         }
+        const unsigned long long t_done = P.timeline ? gtimer() : 0;
         fence_acq_rel_gpu();
         for (int i = 0; i < n; ++i) {
             const Release& r = sh->rel[(j + i) % kQ];
@@ -385,10 +477,12 @@ __device__ void releaser(const KParams& P, CtlShared* sh)
             if (r.last) {
                 if (r.counter) st_relaxed(r.counter, r.counter_v);
                 if (P.timeline) {
-                    unsigned long long* tl = P.timeline + 3ll * r.si;
+                    unsigned long long* tl = P.timeline + 5ll * r.si;
                     tl[0] = r.t_start;
                     tl[1] = r.waited;
-                    tl[2] = gtimer();
+                    tl[2] = r.t_pub;
+                    tl[3] = t_done;
+                    tl[4] = gtimer();
                 }
             }
         }
@@ -839,10 +933,11 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
     const int need_sm = nsm > 0 ? (img.ntb + nsm - 1) / nsm : 1;
     int budget = smem_sm / std::max(1, need_sm) - (int)fa.sharedSizeBytes - 1024;
     budget = std::min(budget, smem_optin - (int)fa.sharedSizeBytes);
-    int ns = img.bulk && img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / img.tile_bytes) : 0;
+    const int64_t stage_bytes = img.tile_bytes;
+    int ns = img.bulk && img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / stage_bytes) : 0;
     if (ns < 2) ns = 0;
     while (true) {
-        size_t dyn = (size_t)ns * img.tile_bytes;
+        size_t dyn = (size_t)ns * stage_bytes;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ccl::ccl_exec_kernel, img.nthreads, dyn);
         if (e != cudaSuccess) { delete p; return ccl::cuda_fail(e, "occupancy query"); }
         if ((int64_t)per_sm * nsm >= img.ntb) break;
@@ -850,7 +945,7 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
         if (ns > 0) { ns = 0; continue; }
         if ((opts && opts->nthreads) || img.nthreads <= 128) break;
         img.nthreads = img.nthreads / 2 >= 128 ? img.nthreads / 2 : 128;
-        ns = img.bulk && img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / img.tile_bytes) : 0;
+        ns = img.bulk && img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / stage_bytes) : 0;
         if (ns < 2) ns = 0;
     }
     img.ns = ns;
@@ -885,7 +980,7 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
     PLAN_TRY(cudaMalloc(&p->d_flags, std::max<size_t>(1, p->flags_count) * sizeof(unsigned long long)), "allocate flags");
     PLAN_TRY(cudaMalloc(&p->d_status, 4 * sizeof(int)), "allocate status");
     if (img.fifo_bytes) PLAN_TRY(cudaMalloc(&p->d_fifo, img.fifo_bytes), "allocate link FIFOs");
-    if (img.instrument) PLAN_TRY(cudaMalloc(&p->d_timeline, img.steps.size() * 3 * sizeof(unsigned long long)), "allocate timeline");
+    if (img.instrument) PLAN_TRY(cudaMalloc(&p->d_timeline, img.steps.size() * 5 * sizeof(unsigned long long)), "allocate timeline");
     int64_t scratch_bytes = img.scratch_elems * img.esize;
     int64_t dev_bytes = blob + p->flags_count * 8 + 16 + img.fifo_bytes;
     for (int r = 0; r < s->nranks; ++r) {
@@ -1027,12 +1122,12 @@ ccl_status_t ccl_plan_timeline(ccl_plan_t p, double* idle, int32_t cap, double* 
     const ccl::PlanImage& img = p->img;
     if (idle && cap < img.ntb) return ccl::fail(CCL_ERR_INVALID_ARG, "capacity too small");
     CUDA_TRY(cudaDeviceSynchronize(), "synchronize");
-    std::vector<unsigned long long> t(img.steps.size() * 3);
+    std::vector<unsigned long long> t(img.steps.size() * 5);
     CUDA_TRY(cudaMemcpy(t.data(), p->d_timeline, t.size() * 8, cudaMemcpyDeviceToHost), "read timeline");
     unsigned long long lo = ~0ull, hi = 0;
     for (size_t k = 0; k < img.steps.size(); ++k) {
-        lo = std::min(lo, t[3 * k]);
-        hi = std::max(hi, t[3 * k + 2]);
+        lo = std::min(lo, t[5 * k]);
+        hi = std::max(hi, t[5 * k + 4]);
     }
     double span = hi > lo ? (double)(hi - lo) : 1.0;
     double sum = 0, mx = 0;
@@ -1042,7 +1137,7 @@ ccl_status_t ccl_plan_timeline(ccl_plan_t p, double* idle, int32_t cap, double* 
         // the end of each step's waits to the post of its last tile
         std::vector<std::pair<unsigned long long, unsigned long long>> iv;
         for (int k = img.tb_begin[b]; k < img.tb_begin[b + 1]; ++k) {
-            const unsigned long long s0 = t[3 * k] + t[3 * k + 1], s1 = t[3 * k + 2];
+            const unsigned long long s0 = t[5 * k] + t[5 * k + 1], s1 = t[5 * k + 4];
             if (s1 > s0) iv.emplace_back(s0, s1);
         }
         std::sort(iv.begin(), iv.end());
@@ -1083,9 +1178,9 @@ ccl_status_t ccl_plan_timeline_raw(ccl_plan_t p, uint64_t* stamps, int64_t cap, 
     }
     if (!stamps) return CCL_OK;
     if (!p->d_timeline) return ccl::fail(CCL_ERR_INVALID_ARG, "plan was created without instrumentation");
-    if (cap < 3 * (int64_t)img.steps.size()) return ccl::fail(CCL_ERR_INVALID_ARG, "capacity too small");
+    if (cap < 5 * (int64_t)img.steps.size()) return ccl::fail(CCL_ERR_INVALID_ARG, "capacity too small");
     CUDA_TRY(cudaDeviceSynchronize(), "synchronize");
-    CUDA_TRY(cudaMemcpy(stamps, p->d_timeline, img.steps.size() * 3 * 8, cudaMemcpyDeviceToHost), "read timeline");
+    CUDA_TRY(cudaMemcpy(stamps, p->d_timeline, img.steps.size() * 5 * 8, cudaMemcpyDeviceToHost), "read timeline");
     return CCL_OK;
 }
 

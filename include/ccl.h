@@ -347,11 +347,13 @@ ccl_status_t ccl_plan_timeline(ccl_plan_t p, double* idle, int32_t cap, double* 
                                double* max_idle, double* span_us);
 
 /*
- * Raw stamps of the last execution of an instrumented plan, three per step
+ * Raw stamps of the last execution of an instrumented plan, five per step
  * in threadblock-program order: the global-timer time (ns) the issuer took
- * the step up, the ns it spent waiting for dependency counters and FIFO
- * flags, and the time the last tile's flags were posted.  stamps: capacity
- * cap (>= 3 * nsteps) or NULL; tb_begin: capacity tb_cap (>= nthreadblocks
+ * the step up; the ns it spent waiting for dependency counters and FIFO
+ * flags; the time it handed out the step's first tile; the time the
+ * releasing warp saw the step's last tile finished (before its release
+ * fence); the time that tile's flags were posted.  stamps: capacity cap
+ * (>= 5 * nsteps) or NULL; tb_begin: capacity tb_cap (>= nthreadblocks
  * + 1) or NULL, the first step of every threadblock; *nsteps (may be NULL)
  * receives the step count.  With stamps non-NULL the plan must have been
  * created with instrument = 1; synchronizes the device.
