@@ -43,11 +43,12 @@ SUITE = [
     ("hier_ar", 3, 16, 8, 0, 4 * MiB, "normal", 2,
      dict(channels=8, microbatches=16, tb_alloc=1, slot_bytes=65536, fifo_slots=5, mb_window=4)),
     ("a2a", 4, 32, 8, 2, 1 * MiB, "uniform", 3,
-     dict(channels=2, link_mode=1, bulk=1, nthreads=128, tile_bytes=16384, channel_scaling=0)),
+     dict(channels=4, link_mode=1, bulk=1, tile_bytes=16384, channel_scaling=0, tb_alloc=1)),
     ("ring_bf16", 0, 8, 0, 1, 32 * MiB, "normal", 4, dict(channels=24, slot_bytes=131072)),
     ("ring_f32", 0, 8, 0, 0, 32 * MiB, "normal", 4, dict(channels=24, slot_bytes=131072)),
+    # relay hops as plain direct copies (no fusion into FIFO forwards)
     ("a2n", 5, 24, 8, 0, 16 * MiB, "normal", 4,
-     dict(channels=16, link_mode=1, nthreads=256, slot_bytes=131072, channel_scaling=1)),
+     dict(fuse=False, channels=8, link_mode=1, microbatches=8, tb_alloc=1, channel_scaling=0)),
     ("ag_3m", 1, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4)),
     ("rs_3m", 2, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4)),
     ("ar_1m", 0, 8, 0, 0, 1 * MiB // 8, "uniform", 0, dict(channels=1)),
@@ -152,6 +153,14 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def schedule_and_opts(ccl, kind, R, G, opts):
+    """The built-in schedule of a suite row (the row's `fuse` key chooses
+    the compiler's fusion) and the remaining plan options."""
+    opts = dict(opts)
+    fuse = opts.pop("fuse", True)
+    return ccl.Schedule.builtin(kind, R, G, 0 if fuse else ccl.FLAG_NOFUSE), opts
+
+
 def selected_suite(args):
     """The suite, or a subset (--only) at reduced chunk size (--scale) for
     profiling captures."""
@@ -172,8 +181,8 @@ def build_suite(ccl, torch, datagen, args, with_host=False):
     items = []
     for name, kind, R, G, dt, chunk_bytes, dist, seed, opts in selected_suite(args):
         ce = chunk_bytes // ESIZE[dt]
-        sched = ccl.Schedule.builtin(kind, R, G)
-        plan = ccl.Plan(sched, ce, dt, **opts)
+        sched, popts = schedule_and_opts(ccl, kind, R, G, opts)
+        plan = ccl.Plan(sched, ce, dt, **popts)
         st = plan.stats()
         nin, nout = plan.in_elems, plan.out_elems
         tdt = {0: torch.float32, 1: torch.int16, 2: torch.int16, 3: torch.int32}[dt]
@@ -381,8 +390,8 @@ def run_reference(args):
     items = []
     for name, kind, R, G, dt, chunk_bytes, dist, seed, opts in selected_suite(args):
         ce = chunk_bytes // ESIZE[dt]
-        sch = ccl.Schedule.builtin(kind, R, G)
-        st = sch.check(ce, dt, **opts)
+        sch, popts = schedule_and_opts(ccl, kind, R, G, opts)
+        st = sch.check(ce, dt, **popts)
         nin = sch.info().nchunks[0] * ce
         items.append(dict(name=name, kind=kind, R=R, G=G, dt=dt, ce=ce, stats=st, dist=dist, seed=seed, nin=nin))
     cb = None

@@ -83,6 +83,13 @@ class PlanStats(ctypes.Structure):
                 ("mb_window", ctypes.c_int32)]
 
 
+class StepInfo(ctypes.Structure):
+    _fields_ = [("tb", ctypes.c_int32), ("kind", ctypes.c_int32), ("rank", ctypes.c_int32), ("channel", ctypes.c_int32),
+                ("mb", ctypes.c_int32), ("link_in", ctypes.c_int32), ("link_out", ctypes.c_int32),
+                ("nslots", ctypes.c_int32), ("dep_count", ctypes.c_int32), ("drain", ctypes.c_int32),
+                ("nelem", ctypes.c_int64)]
+
+
 class TuneOpts(ctypes.Structure):
     _fields_ = [("max_rounds", ctypes.c_int32), ("reps", ctypes.c_int32), ("min_gain", ctypes.c_double)]
 
@@ -117,6 +124,7 @@ def _load():
                               ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
         "ccl_plan_timeline_raw": [P, ctypes.POINTER(ctypes.c_uint64), I64_, ctypes.POINTER(ctypes.c_int32), I32_,
                                   ctypes.POINTER(ctypes.c_int64)],
+        "ccl_plan_steps": [P, ctypes.POINTER(StepInfo), I64_, ctypes.POINTER(ctypes.c_int64)],
         "ccl_plan_debug_drop_signal": [P, I32_, I32_],
         "ccl_plan_check": [P, I64_, I32_, ctypes.POINTER(PlanOpts), ctypes.POINTER(PlanStats)],
         "ccl_schedule_timeline": [P, I32_, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
@@ -300,6 +308,14 @@ class Plan:
         _check(lib.ccl_plan_timeline_raw(self._h, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), buf.size, tb,
                                          st.nthreadblocks + 1, None))
         return buf.reshape(-1, 5), list(tb)
+
+    def steps(self):
+        """Every step of the plan in threadblock-program order, as dicts."""
+        n = ctypes.c_int64()
+        _check(lib.ccl_plan_steps(self._h, None, 0, ctypes.byref(n)))
+        arr = (StepInfo * max(1, n.value))()
+        _check(lib.ccl_plan_steps(self._h, arr, n.value, ctypes.byref(n)))
+        return [{f: getattr(s, f) for f, _ in StepInfo._fields_} for s in arr[:n.value]]
 
     def debug_drop_signal(self, tb, step):
         _check(lib.ccl_plan_debug_drop_signal(self._h, tb, step))

@@ -1184,6 +1184,35 @@ ccl_status_t ccl_plan_timeline_raw(ccl_plan_t p, uint64_t* stamps, int64_t cap, 
     return CCL_OK;
 }
 
+ccl_status_t ccl_plan_steps(ccl_plan_t p, ccl_step_info_t* out, int64_t cap, int64_t* n)
+{
+    if (!p) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    const ccl::PlanImage& img = p->img;
+    const int64_t ns = (int64_t)img.steps.size();
+    if (n) *n = ns;
+    if (!out) return CCL_OK;
+    if (cap < ns) return ccl::fail(CCL_ERR_INVALID_ARG, "capacity too small");
+    const int ch = img.channels > 0 ? img.channels : 1;
+    for (int b = 0; b < img.ntb; ++b)
+        for (int k = img.tb_begin[b]; k < img.tb_begin[b + 1]; ++k) {
+            const ccl::DStep& s = img.steps[k];
+            const ccl::DInstr& d = img.instrs[s.instr];
+            ccl_step_info_t& o = out[k];
+            o.tb = b;
+            o.kind = d.kind;
+            o.rank = img.tb_rank[b];
+            o.channel = s.instr % ch;
+            o.mb = s.mb;
+            o.link_in = d.link_in;
+            o.link_out = d.link_out;
+            o.nslots = s.nslots;
+            o.dep_count = s.dep_count;
+            o.drain = s.drain;
+            o.nelem = s.nelem;
+        }
+    return CCL_OK;
+}
+
 ccl_status_t ccl_plan_debug_drop_signal(ccl_plan_t p, int32_t tb, int32_t step)
 {
     if (!p) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");

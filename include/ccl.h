@@ -361,6 +361,29 @@ ccl_status_t ccl_plan_timeline(ccl_plan_t p, double* idle, int32_t cap, double* 
 ccl_status_t ccl_plan_timeline_raw(ccl_plan_t p, uint64_t* stamps, int64_t cap, int32_t* tb_begin,
                                    int32_t tb_cap, int64_t* nsteps);
 
+/* One step of a threadblock program: one channel piece of one fused
+ * instruction for one micro-batch. */
+typedef struct {
+    int32_t tb;          /* threadblock that runs it */
+    int32_t kind;        /* CCL_I_* */
+    int32_t rank;        /* rank the threadblock serves */
+    int32_t channel;
+    int32_t mb;          /* micro-batch */
+    int32_t link_in;     /* incoming link FIFO of the plan, or -1 */
+    int32_t link_out;    /* outgoing link FIFO, or -1 */
+    int32_t nslots;      /* FIFO slots the piece occupies (0: no link) */
+    int32_t dep_count;   /* counters waited on before it starts */
+    int32_t drain;       /* earlier step of the same threadblock it follows, or -1 */
+    int64_t nelem;       /* elements of the piece */
+} ccl_step_info_t;
+
+/*
+ * The steps of a plan in threadblock-program order (the order of the stamps
+ * of ccl_plan_timeline_raw).  out: capacity cap, or NULL to ask for *n only.
+ * CCL_ERR_INVALID_ARG when cap is too small (after setting *n).
+ */
+ccl_status_t ccl_plan_steps(ccl_plan_t p, ccl_step_info_t* out, int64_t cap, int64_t* n);
+
 /*
  * Test hook: make threadblock `tb` skip the flag post of its step `step`
  * (the data is still written), so a peer's wait runs out.  Used to check

@@ -115,3 +115,24 @@ def test_full_size_benchmark_configurations(ccl, row):
     assert_bitexact(got, want)
     del got, want, plan
     torch.cuda.empty_cache()
+
+
+def test_plan_steps_match_the_timeline(ccl):
+    """Step introspection lines up with the raw stamps: same count, threadblock
+    boundaries, and every step posted no earlier than it started."""
+    import torch
+    import datagen
+    s = ccl.Schedule.builtin(ccl.ALLTONEXT, 6, 3)
+    plan = ccl.Plan(s, 4096, F32, channels=2, instrument=1)
+    ins = to_device(datagen.rank_inputs(1, "normal", 6, 6 * 4096, F32), F32)
+    outs = empty_outputs(6, 6 * 4096, F32)
+    plan.execute(ins, outs)
+    torch.cuda.synchronize()
+    plan.status()
+    steps = plan.steps()
+    stamps, tb = plan.timeline_raw()
+    assert len(steps) == plan.stats().nsteps == stamps.shape[0]
+    for b in range(len(tb) - 1):
+        assert all(st["tb"] == b for st in steps[tb[b]:tb[b + 1]])
+    assert np.all(stamps[:, 4] >= stamps[:, 0])
+    assert all(st["nelem"] >= 0 and st["kind"] in range(len(ccl.KIND_NAMES)) for st in steps)
