@@ -291,14 +291,14 @@ def run_gpu(args):
         "warmup": args.warmup,
         "ms_per_step": round(step_ms, 4),
         "higher_is_better": True,
-        "scaling": "replicas only",
+        "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32/bf16/f16 (per collective)",
         "data": "synthetic (numpy PCG64 seeds 0-4)",
         "config": {"workload": "collective suite: hier AR 16x64MiB f32 + two-phase A2A 32x32MiB f16 + ring AR "
                                "8x256MiB bf16 & f32 (24 ch) + AllToNext 24x128MiB f32 + AG/RS 8x3MiB bf16 + "
                                "ring AR 8x1MiB f32",
-                   "parallelism": "R virtual ranks on one GPU", "l2": "step working set ~19 GiB > L2 (no flush)",
+                   "parallelism": "replicas only (R virtual ranks per GPU, no cross-GPU exchange)", "l2": "step working set ~19 GiB > L2 (no flush)",
                    "schedule_bytes_per_step": sched_bytes,
                    **({"subset": args.only, "scale": args.scale} if (args.only or args.scale != 1.0) else {})},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -398,7 +398,7 @@ def run_reference(args):
     for _ in range(args.warmup + args.steps):
         cb = cpu_baseline(items, args.cpu_seconds, divisor=1024)
     return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "replicas only",
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32/bf16/f16 (per collective)", "data": "synthetic (numpy PCG64 seeds 0-4)",
             "config": {"workload": "collective suite (same as the GPU arm), each step a 1/1024 sample of in-chunk offsets"},
             "cpu_baseline": cb,
