@@ -872,7 +872,10 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
             std::vector<int> wins;
             if (o.mb_window > 0) wins.push_back(std::min(m, o.mb_window));
             else {
-                const int w = std::max(1, std::min(m, o.fifo_slots - 1));
+                // double buffering: a window's slots and the next window's
+                // fit in the FIFO together, so neighbours do not run in
+                // lockstep
+                const int w = std::max(1, std::min(m, o.fifo_slots / 2));
                 wins.push_back(w);
                 if (w > 1) wins.push_back(1);
             }

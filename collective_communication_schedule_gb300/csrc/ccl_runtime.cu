@@ -138,28 +138,42 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned par,
     return true;
 }
 
-// bounded wait until *a >= va and *b >= vb (either may be null), polled with
-// relaxed loads issued together, followed by one acquire fence
-__device__ bool wait_flags(const KParams& P, const unsigned long long* a, unsigned long long va,
-                           const unsigned long long* b, unsigned long long vb, int si, int reason,
-                           unsigned long long& waited)
+// Bounded wait until every dependency counter of a step reaches its value:
+// up to kDepBatch counters polled with relaxed loads issued together per
+// round trip, one acquire fence at the end.
+constexpr int kDepBatch = 8;
+__device__ bool wait_deps(const KParams& P, const DDep* deps, int n, int si, unsigned long long& waited)
 {
+    const unsigned long long base = (unsigned long long)(P.exec * P.m);
     unsigned long long t0 = 0;
-    unsigned spins = 0;
-    while (true) {
-        unsigned long long x = a ? ld_relaxed(a) : ~0ull;
-        unsigned long long y = b ? ld_relaxed(b) : ~0ull;
-        if (x >= va && y >= vb) break;
-        if (!t0) t0 = gtimer();
-        ++spins;
-        if ((spins & 15) == 0) {
-            if (*(volatile int*)P.status != 0) return false;
-            if (gtimer() - t0 > P.timeout_ns) {
-                record_timeout(P, si, (a && x < va) ? reason : WAIT_FREE);
-                return false;
-            }
+    for (int k0 = 0; k0 < n; k0 += kDepBatch) {
+        const int nb = n - k0 < kDepBatch ? n - k0 : kDepBatch;
+        const unsigned long long* c[kDepBatch];
+        unsigned long long v[kDepBatch];
+#pragma unroll
+        for (int i = 0; i < kDepBatch; ++i) {
+            const DDep d = deps[k0 + (i < nb ? i : 0)];
+            c[i] = P.counters + d.counter;
+            v[i] = base + d.value;
         }
-        if (spins > 64) __nanosleep(32);
+        unsigned spins = 0;
+        while (true) {
+            bool ok = true;
+#pragma unroll
+            for (int i = 0; i < kDepBatch; ++i)
+                if (i < nb && ld_relaxed(c[i]) < v[i]) ok = false;
+            if (ok) break;
+            if (!t0) t0 = gtimer();
+            ++spins;
+            if ((spins & 15) == 0) {
+                if (*(volatile int*)P.status != 0) return false;
+                if (gtimer() - t0 > P.timeout_ns) {
+                    record_timeout(P, si, WAIT_DEP);
+                    return false;
+                }
+            }
+            if (spins > 64) __nanosleep(32);
+        }
     }
     fence_acq_rel_gpu();
     if (t0) waited += gtimer() - t0;
@@ -337,13 +351,9 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
                 return;
             }
         }
-        for (int k = 0; k < st.dep_count; ++k) {
-            const DDep d = P.deps[st.dep_begin + k];
-            if (!wait_flags(P, P.counters + d.counter, (unsigned long long)(P.exec * P.m + d.value), nullptr, 0, si,
-                            WAIT_DEP, waited)) {
-                publish_cmd(2);
-                return;
-            }
+        if (st.dep_count > 0 && !wait_deps(P, P.deps + st.dep_begin, st.dep_count, si, waited)) {
+            publish_cmd(2);
+            return;
         }
         const int es = (st.dtype == CCL_BF16 || st.dtype == CCL_F16) ? 2 : 4;
         const DLink* Lin = st.link_in >= 0 ? P.links + st.link_in : nullptr;

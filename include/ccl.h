@@ -212,8 +212,9 @@ typedef enum { CCL_LINK_FIFO = 0, CCL_LINK_DIRECT = 1 } ccl_link_mode_t;
  *                 pieces ahead of it in its own threadblock while the piece
  *                 it depends on is still in flight upstream.  1 = one
  *                 micro-batch at a time through the whole segment; 0 =
- *                 auto: min(m, fifo_slots - 1) first, then 1, keeping the
- *                 first that can finish.
+ *                 auto: min(m, fifo_slots / 2) first (a window and the next
+ *                 one fit in the FIFO together), then 1, keeping the first
+ *                 that can finish.
  *   timeout_ms  : limit of every device flag wait.
  *   instrument  : 1 = record per-step global-timer stamps (ccl_plan_timeline).
  *   tile_bytes  : the executor moves a slot in tiles of this size (multiple of

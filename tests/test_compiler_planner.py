@@ -351,9 +351,10 @@ def test_microbatch_window_is_used_when_the_fifo_holds_it():
     s = ccl.Schedule.builtin(ccl.HIER_ALLREDUCE, 16, 8)
     kw = dict(channels=2, microbatches=8, tb_alloc=ccl.TB_PACKED, slot_bytes=65536, mb_order=ccl.MB_ALGO)
     assert s.check(65536, F32, fifo_slots=4, mb_window=1, **kw).mb_window == 1
-    # auto: min(m, fifo_slots - 1)
-    assert s.check(65536, F32, fifo_slots=4, mb_window=0, **kw).mb_window == 3
-    assert s.check(65536, F32, fifo_slots=9, mb_window=0, **kw).mb_window == 8
+    # auto: min(m, fifo_slots / 2)
+    assert s.check(65536, F32, fifo_slots=4, mb_window=0, **kw).mb_window == 2
+    assert s.check(65536, F32, fifo_slots=9, mb_window=0, **kw).mb_window == 4
+    assert s.check(65536, F32, fifo_slots=32, mb_window=0, **kw).mb_window == 8
     # same steps and bytes in another order
     a = s.check(65536, F32, fifo_slots=9, mb_window=1, **kw)
     b = s.check(65536, F32, fifo_slots=9, mb_window=8, **kw)
