@@ -217,6 +217,32 @@ __device__ __forceinline__ void move_dt(bool red, const char* a, bool as, const 
     move_part<DT>(red, a, as, b, bs, o1, o1s, o2, n, threadIdx.x, blockDim.x);
 }
 
+// ---------------------------------------------------------------- LL lines
+// An LL line is one 64-bit word: 4 data bytes in the low half, the flag of
+// its FIFO slot (sequence number + 1, low 32 bits) in the high half.  Lines
+// are written and read as elements of 16-byte vectors; each 64-bit element
+// is an aligned scalar access and therefore single-copy atomic, so a reader
+// that sees the flag sees the data beside it.  Volatile accesses bypass L1.
+__device__ __forceinline__ void ll_load2(const void* p, unsigned long long& x, unsigned long long& y)
+{
+    asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "l"(p) : "memory");
+}
+__device__ __forceinline__ void ll_store2(void* p, unsigned long long x, unsigned long long y)
+{
+    asm volatile("st.volatile.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(x), "l"(y) : "memory");
+}
+__device__ __forceinline__ unsigned long long ll_line(unsigned data, unsigned flag)
+{
+    return ((unsigned long long)flag << 32) | data;
+}
+// the 16 data bytes of vector i as four lines (32 bytes) at p + 32 i
+__device__ __forceinline__ void ll_store_vec(char* p, long long i, uint4 r, unsigned flag)
+{
+    char* q = p + 32 * i;
+    ll_store2(q, ll_line(r.x, flag), ll_line(r.y, flag));
+    ll_store2(q + 16, ll_line(r.z, flag), ll_line(r.w, flag));
+}
+
 // ---------------------------------------------------------------- mbarriers
 __device__ __forceinline__ unsigned smem_addr(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
 

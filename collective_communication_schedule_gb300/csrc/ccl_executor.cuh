@@ -27,14 +27,16 @@ struct KParams {
     unsigned long long* counters;
     char* fifo;
     int* status;                   // [0] code, [1] threadblock, [2] step, [3] reason
-    unsigned long long* timeline;  // 3 stamps per step, or null
+    unsigned long long* timeline;  // 5 stamps per step, or null
     long long exec;
     long long m;
-    long long slot_bytes;
+    long long slot_bytes;          // data bytes of a slot
+    long long slot_stride;         // bytes a slot occupies (2 x slot_bytes for LL)
     unsigned long long timeout_ns;
     long long tile_bytes;          // bytes per tile handed to the data path
     int S;
     int ns;                        // shared-memory stages of the bulk path (0: off)
+    int ll;                        // FIFO slots hold LL lines (data + flag per 64 bits)
     char* bufs[3][CCL_MAX_RANKS];
 };
 

@@ -53,16 +53,18 @@ struct DRec {
     int32_t nslots, dep_begin, dep_count, signal, mb, flags;
     int64_t src_off, loc_off, dst_off;   // element offsets of this piece
     int64_t nelem, seq_in, seq_out;
-    int32_t drain, pad0;
-    int64_t pad1;
+    int32_t drain;
+    int32_t seq_in_mod, seq_out_mod;   // seq_in % S, seq_out % S (slot index arithmetic in 32 bits)
+    int32_t pad0;
 };
 static_assert(sizeof(DRec) == 128, "DRec layout");
 
 struct DLink {
-    int64_t slot_base;  // byte offset of slot 0 in the FIFO pool
+    int64_t slot_base;  // byte offset of slot 0 in the FIFO pool (slots of slot_stride bytes)
     int64_t total;      // slot sequences per execution
     int32_t flag_base;  // full flags at [flag_base, +S), consumed at [flag_base+S, +S)
-    int32_t src_rank, dst_rank, channel;
+    int32_t src_rank, dst_rank;
+    int32_t total_mod;  // total % S
 };
 static_assert(sizeof(DLink) == 32, "DLink layout");
 
@@ -96,6 +98,7 @@ struct PlanImage {
     int32_t channels = 1;
     int32_t mb_order = CCL_MB_ALGO;
     int32_t mb_window = 1;           // micro-batches interleaved per instruction inside a segment
+    int32_t protocol = 0;            // CCL_PROTO_*: LL slots take 2 x slot_bytes
     int32_t nsubpipelines = 0;
     int32_t ntb_connection = 0;
     int32_t dtype = CCL_F32;

@@ -324,6 +324,8 @@ void fill_records(PlanImage* img)
         r.loc_off = in.loc_off + st.elem_off;
         r.dst_off = in.dst_off + st.elem_off;
         r.nelem = st.nelem; r.seq_in = st.seq_in; r.seq_out = st.seq_out;
+        r.seq_in_mod = (int32_t)(st.seq_in % img->S);
+        r.seq_out_mod = (int32_t)(st.seq_out % img->S);
     }
 }
 
@@ -373,7 +375,10 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     img->channels = p;
     img->mb_order = order;
     img->mb_window = window;
+    img->protocol = o.protocol;
     img->S = S;
+    // an LL slot carries slot_bytes of data in twice as many bytes of lines
+    const int64_t slot_stride = o.protocol == CCL_PROTO_LL ? 2 * o.slot_bytes : o.slot_bytes;
     img->slot_bytes = o.slot_bytes;
     img->tile_bytes = o.tile_bytes;
     img->bulk = o.bulk;
@@ -415,10 +420,10 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
         if (it != link_id.end()) return it->second;
         int id = (int)img->links.size();
         DLink L{};
-        L.slot_base = (int64_t)id * S * o.slot_bytes;
+        L.slot_base = (int64_t)id * S * slot_stride;
         L.total = 0;
         L.flag_base = id * 2 * S;
-        L.src_rank = a; L.dst_rank = b; L.channel = ch;
+        L.src_rank = a; L.dst_rank = b; L.total_mod = 0;
         img->links.push_back(L);
         link_id[key] = id;
         return id;
@@ -529,6 +534,7 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
                 seq += st.nslots;
             }
             img->links[L].total = seq;
+            img->links[L].total_mod = (int32_t)(seq % S);
         }
         // receivers take the sender's numbers
         for (int i = 0; i < ni; ++i) {
@@ -609,7 +615,7 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
             img->steps[k].signal = counter_of[ci];
         }
     }
-    img->fifo_bytes = (int64_t)img->links.size() * S * o.slot_bytes;
+    img->fifo_bytes = (int64_t)img->links.size() * S * slot_stride;
     fill_records(img);
     return CCL_OK;
 }
@@ -822,6 +828,9 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
     if (o.tb_alloc != CCL_TB_CONNECTION && o.tb_alloc != CCL_TB_PACKED) return fail(CCL_ERR_INVALID_ARG, "unknown tb_alloc");
     if (o.mb_order < CCL_MB_AUTO || o.mb_order > CCL_MB_SEGMENT) return fail(CCL_ERR_INVALID_ARG, "unknown mb_order");
     if (o.mb_window < 0 || o.mb_window > 65536) return fail(CCL_ERR_INVALID_ARG, "mb_window out of range");
+    if (o.protocol != CCL_PROTO_SIMPLE && o.protocol != CCL_PROTO_LL) return fail(CCL_ERR_INVALID_ARG, "unknown protocol");
+    if (o.protocol == CCL_PROTO_LL && (ce * esize_of(dtype)) % 16)
+        return fail(CCL_ERR_UNSUPPORTED, "the LL protocol needs chunks of a multiple of 16 bytes");
     if (o.timeout_ms <= 0) return fail(CCL_ERR_INVALID_ARG, "timeout_ms must be positive");
 
     if (o.link_mode != CCL_LINK_FIFO && o.link_mode != CCL_LINK_DIRECT)

@@ -89,6 +89,8 @@ struct SlotOp {
     int as, bs, o1s;    // streaming cache hints (register path)
     int bulk;           // moved by the TMA thread
     int cmd;            // 0 move, 1 end, 2 abort
+    int a_ll, o1_ll, o2_ll;   // operand is an LL slot
+    unsigned fin, fout;       // flag of the incoming / outgoing LL slot
 };
 
 struct Release {
@@ -186,8 +188,10 @@ __device__ bool wait_deps(const KParams& P, const DDep* deps, int n, int si, uns
 // wait for the first one fails.
 constexpr int kBatch = 4;
 __device__ int wait_slots(const KParams& P, const DLink* Lin, const DLink* Lout, unsigned long long sin0,
-                          unsigned long long sout0, int bmax, int si, unsigned long long& waited)
+                          unsigned long long sout0, unsigned in_idx0, unsigned out_idx0, int bmax, int si,
+                          unsigned long long& waited)
 {
+    const unsigned S = (unsigned)P.S;
     unsigned long long t0 = 0;
     unsigned spins = 0;
     while (true) {
@@ -197,9 +201,11 @@ __device__ int wait_slots(const KParams& P, const DLink* Lin, const DLink* Lout,
             x[i] = ~0ull;
             y[i] = ~0ull;
             if (i < bmax) {
-                if (Lin) x[i] = ld_relaxed(P.flags + Lin->flag_base + (int)((sin0 + i) % P.S));
-                if (Lout && sout0 + i + 1 > (unsigned long long)P.S)
-                    y[i] = ld_relaxed(P.flags + Lout->flag_base + P.S + (int)((sout0 + i) % P.S));
+                unsigned ii = in_idx0 + i, io = out_idx0 + i;   // slot indices: i < kBatch, S >= 2
+                while (ii >= S) ii -= S;
+                while (io >= S) io -= S;
+                if (Lin && !P.ll) x[i] = ld_relaxed(P.flags + Lin->flag_base + ii);
+                if (Lout && sout0 + i + 1 > (unsigned long long)P.S) y[i] = ld_relaxed(P.flags + Lout->flag_base + S + io);
             }
         }
         int b = 0;
@@ -239,20 +245,28 @@ struct SlotCond {
     unsigned long long vin, vout;
 };
 
-__device__ __forceinline__ SlotCond first_slot_cond(const KParams& P, const DRec& st)
+// slot index (sequence % S) of a step's first slot on link L, in 32 bits:
+// (exec * total + seq) % S from exec % S, total % S and seq % S
+__device__ __forceinline__ unsigned slot_index(unsigned exec_mod, const DLink& L, int seq_mod, unsigned S)
+{
+    return (exec_mod * (unsigned)L.total_mod + (unsigned)seq_mod) % S;
+}
+
+__device__ __forceinline__ SlotCond first_slot_cond(const KParams& P, const DRec& st, unsigned exec_mod)
 {
     SlotCond c{nullptr, nullptr, 0, 0};
-    if (st.link_in >= 0) {
+    const unsigned S = (unsigned)P.S;
+    if (st.link_in >= 0 && !P.ll) {   // LL: the data path polls the lines
         const DLink& L = P.links[st.link_in];
         const unsigned long long s = (unsigned long long)(P.exec * L.total) + st.seq_in;
-        c.in = P.flags + L.flag_base + (int)(s % P.S);
+        c.in = P.flags + L.flag_base + slot_index(exec_mod, L, st.seq_in_mod, S);
         c.vin = s + 1;
     }
     if (st.link_out >= 0) {
         const DLink& L = P.links[st.link_out];
         const unsigned long long s = (unsigned long long)(P.exec * L.total) + st.seq_out;
         if (s + 1 > (unsigned long long)P.S) {
-            c.out = P.flags + L.flag_base + P.S + (int)(s % P.S);
+            c.out = P.flags + L.flag_base + S + slot_index(exec_mod, L, st.seq_out_mod, S);
             c.vout = s + 1 - P.S;
         }
     }
@@ -263,13 +277,14 @@ __device__ __forceinline__ SlotCond first_slot_cond(const KParams& P, const DRec
 // dependency counters) with relaxed loads issued together; returns the end
 // of the leading run of ready steps (> s0) after one acquire fence, or -1
 // when the wait for step s0 fails.
-__device__ int poll_steps(const KParams& P, const CtlShared* sh, int s0, int s1, unsigned long long& waited)
+__device__ int poll_steps(const KParams& P, const CtlShared* sh, int s0, int s1, unsigned exec_mod,
+                          unsigned long long& waited)
 {
     SlotCond c[kLook];
     const int n = s1 - s0;
 #pragma unroll
     for (int i = 0; i < kLook; ++i)
-        c[i] = i < n ? first_slot_cond(P, sh->rec[(s0 + i) % (2 * kLook)]) : SlotCond{nullptr, nullptr, 0, 0};
+        c[i] = i < n ? first_slot_cond(P, sh->rec[(s0 + i) % (2 * kLook)], exec_mod) : SlotCond{nullptr, nullptr, 0, 0};
     unsigned long long t0 = 0;
     unsigned spins = 0;
     while (true) {
@@ -321,6 +336,10 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
     };
     if (b0 < b1) request(b0);
     int cleared = b0;   // steps below: first-slot flags seen ready (and fenced)
+    // slot indices in 32-bit arithmetic: no 64-bit division on the way to a
+    // step (the issuer is one thread; a 64-bit modulo is a long routine)
+    const unsigned S = (unsigned)P.S;
+    const unsigned exec_mod = (unsigned)(P.exec % P.S);
     for (int si = b0; si < b1; ++si) {
         if (si >= rec_ready) {
             asm volatile("cp.async.wait_all;" ::: "memory");
@@ -334,7 +353,7 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
             // one round trip for the next steps that wait on FIFO flags only
             int s1 = si + 1;
             while (s1 < rec_ready && s1 < si + kLook && sh->rec[s1 % (2 * kLook)].dep_count == 0) ++s1;
-            cleared = poll_steps(P, sh, si, s1, waited);
+            cleared = poll_steps(P, sh, si, s1, exec_mod, waited);
             if (cleared < 0) {
                 publish_cmd(2);
                 return;
@@ -360,13 +379,19 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
         const DLink* Lout = st.link_out >= 0 ? P.links + st.link_out : nullptr;
         const unsigned long long base_in = Lin ? (unsigned long long)(P.exec * Lin->total) : 0;
         const unsigned long long base_out = Lout ? (unsigned long long)(P.exec * Lout->total) : 0;
-        const long long slot_elems = P.slot_bytes / es;
+        const int esh = es == 2 ? 1 : 2;
+        const long long slot_elems = P.slot_bytes >> esh;
         // tiles exist for the bulk path; the register path takes a slot whole
-        const long long tile_elems = (P.ns > 0 ? P.tile_bytes : P.slot_bytes) / es;
+        const long long tile_elems = (P.ns > 0 ? P.tile_bytes : P.slot_bytes) >> esh;
         const bool linked = Lin || Lout;
         // FIFO slots of a linked step; local steps are cut into tiles directly
-        const long long nslots = linked ? (st.nslots > 0 ? st.nslots : 1)
-                                        : (st.nelem > 0 ? (st.nelem + tile_elems - 1) / tile_elems : 1);
+        long long nslots = linked ? (st.nslots > 0 ? st.nslots : 1) : 1;
+        if (!linked && st.nelem > 0)
+            nslots = st.nelem + tile_elems - 1 < 0xffffffffll
+                         ? (unsigned)(st.nelem + tile_elems - 1) / (unsigned)tile_elems
+                         : (st.nelem + tile_elems - 1) / tile_elems;
+        unsigned in_idx = Lin ? slot_index(exec_mod, *Lin, st.seq_in_mod, S) : 0;
+        unsigned out_idx = Lout ? slot_index(exec_mod, *Lout, st.seq_out_mod, S) : 0;
         const long long span = linked ? slot_elems : tile_elems;
         const int red = st.kind == CCL_I_REDUCE || st.kind == CCL_I_RRC || st.kind == CCL_I_RRS || st.kind == CCL_I_RRCS;
         const char* srcb = st.src_buf >= 0 ? P.bufs[st.src_buf][st.src_rank] + st.src_off * es : nullptr;
@@ -379,7 +404,7 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
             const unsigned long long sout = base_out + st.seq_out + k;
             if (linked && ready_slots == 0) {
                 const int bmax = (int)((nslots - k) < kBatch ? (nslots - k) : kBatch);
-                ready_slots = wait_slots(P, Lin, Lout, sin, sout, bmax, si, waited);
+                ready_slots = wait_slots(P, Lin, Lout, sin, sout, in_idx, out_idx, bmax, si, waited);
                 if (ready_slots == 0) {
                     publish_cmd(2);
                     return;
@@ -390,9 +415,11 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
             long long n = st.nelem - e0;
             if (n > span) n = span;
             if (n < 0) n = 0;
-            const char* slot_in = Lin ? P.fifo + Lin->slot_base + (long long)(sin % P.S) * P.slot_bytes : nullptr;
-            char* slot_out = Lout ? P.fifo + Lout->slot_base + (long long)(sout % P.S) * P.slot_bytes : nullptr;
-            const long long ntiles = n > 0 ? (n + tile_elems - 1) / tile_elems : 1;
+            const char* slot_in = Lin ? P.fifo + Lin->slot_base + (long long)in_idx * P.slot_stride : nullptr;
+            char* slot_out = Lout ? P.fifo + Lout->slot_base + (long long)out_idx * P.slot_stride : nullptr;
+            const long long lls = P.ll ? 2 : 1;   // slot bytes per data byte
+            // n <= slot_elems: 32-bit division
+            const long long ntiles = n > 0 ? (long long)((unsigned)(n + tile_elems - 1) / (unsigned)tile_elems) : 1;
             for (long long u = 0; u < ntiles; ++u) {
                 const int q = head % kQ;
                 if (head >= kQ && !mbar_wait(&sh->freed[q], (unsigned)(((head / kQ) - 1) & 1), limit)) {
@@ -407,9 +434,11 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
                 const long long off = (e0 + t0) * es;   // byte offset in the step's buffers
                 const long long soff = t0 * es;         // byte offset in the slot
                 SlotOp& op = sh->op[q];
+                op.a_ll = op.o1_ll = op.o2_ll = 0;
                 if (Lin && st.kind != CCL_I_REDUCE) {
-                    op.a = slot_in + soff;
+                    op.a = slot_in + lls * soff;
                     op.as = 0;
+                    op.a_ll = P.ll;
                 } else {
                     op.a = srcb + off;
                     op.as = st.src_buf == CCL_BUF_IN;
@@ -419,23 +448,28 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
                 if (dstb) {
                     op.o1 = dstb + off;
                     op.o1s = st.dst_buf == CCL_BUF_OUT;
-                    op.o2 = slot_out ? slot_out + soff : nullptr;
+                    op.o2 = slot_out ? slot_out + lls * soff : nullptr;
+                    op.o2_ll = slot_out && P.ll;
                 } else {
-                    op.o1 = slot_out + soff;
+                    op.o1 = slot_out + lls * soff;
                     op.o1s = 0;
                     op.o2 = nullptr;
+                    op.o1_ll = P.ll;
                 }
+                op.fin = (unsigned)(sin + 1);
+                op.fout = (unsigned)(sout + 1);
                 op.n = tn;
                 op.red = red;
                 op.dtype = st.dtype;
                 op.bulk = P.ns > 0 && !red && tn > 0 && ((tn * es) & 15) == 0 && aligned16(op.a) &&
-                          aligned16(op.o1) && (!op.o2 || aligned16(op.o2));
+                          aligned16(op.o1) && (!op.o2 || aligned16(op.o2)) && !op.a_ll && !op.o1_ll && !op.o2_ll;
                 op.cmd = 0;
                 Release& r = sh->rel[q];
                 const bool last_tile = u == ntiles - 1;
-                r.consumed = (Lin && post && last_tile) ? P.flags + Lin->flag_base + P.S + (int)(sin % P.S) : nullptr;
+                r.consumed = (Lin && post && last_tile) ? P.flags + Lin->flag_base + S + in_idx : nullptr;
                 r.consumed_v = sin + 1;
-                r.full = (Lout && post && last_tile) ? P.flags + Lout->flag_base + (int)(sout % P.S) : nullptr;
+                // LL slots carry their flags in the lines
+                r.full = (Lout && post && last_tile && !P.ll) ? P.flags + Lout->flag_base + out_idx : nullptr;
                 r.full_v = sout + 1;
                 r.last = last_tile && k == nslots - 1;
                 r.counter = st.signal >= 0 ? P.counters + st.signal : nullptr;
@@ -448,6 +482,8 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
                 mbar_arrive(&sh->ready[q]);
                 ++head;
             }
+            if (++in_idx == S) in_idx = 0;
+            if (++out_idx == S) out_idx = 0;
         }
         sh->last_head[si % kHist] = head - 1;
     }
@@ -625,6 +661,97 @@ __device__ void tma_thread(const KParams& P, CtlShared* sh, unsigned char* stage
     }
 }
 
+// Copy or reduce a tile of which some operand is an LL slot (16-byte
+// multiples, every pointer 16-byte aligned: the plan guarantees it).  An LL
+// source is polled line by line until every line carries the slot's flag;
+// LL destinations get the data with the outgoing slot's flag.  Returns false
+// when a wait gives up (time limit, or another role recorded a failure).
+template <bool RED, int DT>
+__device__ __forceinline__ bool move_ll(const SlotOp& op, int tid, int T, unsigned long long timeout_ns,
+                                        const int* status)
+{
+    constexpr int ES = (DT == CCL_BF16 || DT == CCL_F16) ? 2 : 4;
+    const long long nv = op.n * ES / 16;
+    const char* a = op.a;
+    const uint4* a16 = reinterpret_cast<const uint4*>(a);
+    const uint4* b16 = reinterpret_cast<const uint4*>(op.b);
+    const bool a_ll = op.a_ll, o1_ll = op.o1_ll, o2_ll = op.o2_ll, as = op.as, bs = op.bs, o1s = op.o1s;
+    char* o1 = op.o1;
+    char* o2 = op.o2;
+    const unsigned fin = op.fin, fout = op.fout;
+    // two vectors in flight per thread: i and i + T
+    for (long long i = tid; i < nv; i += 2ll * T) {
+        const long long j1 = i + T < nv ? i + T : nv - 1;   // past the end: re-read, never used
+        uint4 va0, va1, vb0, vb1;
+        if (a_ll) {
+            unsigned long long p0, p1, p2, p3, q0, q1, q2, q3;
+            ll_load2(a + 32 * i, p0, p1);
+            ll_load2(a + 32 * i + 16, p2, p3);
+            ll_load2(a + 32 * j1, q0, q1);
+            ll_load2(a + 32 * j1 + 16, q2, q3);
+            if (RED) {
+                vb0 = vload(b16 + i, bs);
+                vb1 = vload(b16 + j1, bs);
+            }
+            unsigned long long t0 = 0;
+            unsigned spins = 0;
+            while (true) {
+                const bool r0 = (unsigned)(p0 >> 32) == fin && (unsigned)(p1 >> 32) == fin &&
+                                (unsigned)(p2 >> 32) == fin && (unsigned)(p3 >> 32) == fin;
+                const bool r1 = (unsigned)(q0 >> 32) == fin && (unsigned)(q1 >> 32) == fin &&
+                                (unsigned)(q2 >> 32) == fin && (unsigned)(q3 >> 32) == fin;
+                if (r0 && r1) break;
+                const unsigned long long now = gtimer();
+                if (!t0) t0 = now;
+                else if (now - t0 > timeout_ns) return false;
+                if ((++spins & 63) == 0 && *(const volatile int*)status != 0) return false;
+                if (!r0) {
+                    ll_load2(a + 32 * i, p0, p1);
+                    ll_load2(a + 32 * i + 16, p2, p3);
+                }
+                if (!r1) {
+                    ll_load2(a + 32 * j1, q0, q1);
+                    ll_load2(a + 32 * j1 + 16, q2, q3);
+                }
+            }
+            va0 = make_uint4((unsigned)p0, (unsigned)p1, (unsigned)p2, (unsigned)p3);
+            va1 = make_uint4((unsigned)q0, (unsigned)q1, (unsigned)q2, (unsigned)q3);
+        } else {
+            va0 = vload(a16 + i, as);
+            va1 = vload(a16 + j1, as);
+            if (RED) {
+                vb0 = vload(b16 + i, bs);
+                vb1 = vload(b16 + j1, bs);
+            }
+        }
+        const uint4 r0 = RED ? vadd<DT>(va0, vb0) : va0;
+        if (o1_ll) ll_store_vec(o1, i, r0, fout);
+        else vstore(reinterpret_cast<uint4*>(o1) + i, r0, o1s);
+        if (o2) {
+            if (o2_ll) ll_store_vec(o2, i, r0, fout);
+            else vstore(reinterpret_cast<uint4*>(o2) + i, r0, false);
+        }
+        if (i + T < nv) {
+            const uint4 r1 = RED ? vadd<DT>(va1, vb1) : va1;
+            if (o1_ll) ll_store_vec(o1, i + T, r1, fout);
+            else vstore(reinterpret_cast<uint4*>(o1) + i + T, r1, o1s);
+            if (o2) {
+                if (o2_ll) ll_store_vec(o2, i + T, r1, fout);
+                else vstore(reinterpret_cast<uint4*>(o2) + i + T, r1, false);
+            }
+        }
+    }
+    return true;
+}
+
+template <int DT>
+__device__ __forceinline__ bool move_ll_dt(const SlotOp& op, int tid, int T, const KParams& P)
+{
+    return op.red ? move_ll<true, DT>(op, tid, T, P.timeout_ns, P.status)
+                  : move_ll<false, DT>(op, tid, T, P.timeout_ns, P.status);
+}
+
+template <bool LL>
 __device__ void data_warps(const KParams& P, CtlShared* sh)
 {
     const int tid = threadIdx.x - 96;
@@ -637,9 +764,22 @@ __device__ void data_warps(const KParams& P, CtlShared* sh)
             if (lane == 0) record_timeout(P, -1, WAIT_DONE);
             return;
         }
-        const SlotOp op = sh->op[q];
+        // the descriptor stays put until every data warp acknowledged it
+        const SlotOp& op = sh->op[q];
         if (op.cmd != 0) return;
-        if (!op.bulk && op.n > 0) {
+        if (LL && (op.a_ll || op.o1_ll || op.o2_ll)) {
+            // after a recorded failure the tile is only acknowledged
+            if (op.n > 0 && *(volatile int*)P.status == 0) {
+                bool ok;
+                switch (op.dtype) {
+                case CCL_F32: ok = move_ll_dt<CCL_F32>(op, tid, T, P); break;
+                case CCL_BF16: ok = move_ll_dt<CCL_BF16>(op, tid, T, P); break;
+                case CCL_F16: ok = move_ll_dt<CCL_F16>(op, tid, T, P); break;
+                default: ok = move_ll_dt<CCL_I32>(op, tid, T, P); break;
+                }
+                if (!ok) record_timeout(P, -1, WAIT_FULL);
+            }
+        } else if (!op.bulk && op.n > 0) {
             switch (op.dtype) {
             case CCL_F32: move_part<CCL_F32>(op.red, op.a, op.as, op.b, op.bs, op.o1, op.o1s, op.o2, op.n, tid, T); break;
             case CCL_BF16: move_part<CCL_BF16>(op.red, op.a, op.as, op.b, op.bs, op.o1, op.o1s, op.o2, op.n, tid, T); break;
@@ -652,7 +792,12 @@ __device__ void data_warps(const KParams& P, CtlShared* sh)
     }
 }
 
-__global__ void __launch_bounds__(1024, 1) ccl_exec_kernel(const __grid_constant__ KParams P)
+// one instantiation per FIFO protocol: only plans with LL slots carry the
+// LL data path; they run without the bulk path, with at most 512 threads
+// and so twice the registers per thread
+constexpr int kMaxThreadsLL = 512;
+template <bool LL>
+__global__ void __launch_bounds__(LL ? kMaxThreadsLL : 1024, 1) ccl_exec_kernel(const __grid_constant__ KParams P)
 {
     __shared__ __align__(16) CtlShared sh;
     extern __shared__ __align__(128) unsigned char stages[];
@@ -678,7 +823,15 @@ __global__ void __launch_bounds__(1024, 1) ccl_exec_kernel(const __grid_constant
         }
         return;
     }
-    data_warps(P, &sh);
+    data_warps<LL>(P, &sh);
+}
+
+template __global__ void ccl_exec_kernel<false>(const __grid_constant__ KParams P);
+template __global__ void ccl_exec_kernel<true>(const __grid_constant__ KParams P);
+
+const void* exec_kernel(int protocol)
+{
+    return protocol == CCL_PROTO_LL ? (const void*)ccl_exec_kernel<true> : (const void*)ccl_exec_kernel<false>;
 }
 
 }  // namespace ccl
@@ -728,6 +881,7 @@ ccl_plan_opts_t merged_opts(const ccl_plan_opts_t* opts)
         o.link_mode = opts->link_mode;
         o.channel_scaling = opts->channel_scaling;
         o.mb_window = opts->mb_window;
+        o.protocol = opts->protocol;
     }
     return o;
 }
@@ -755,6 +909,7 @@ void fill_stats(const ccl::PlanImage& img, ccl_plan_stats_t* st)
     st->tile_bytes = img.tile_bytes;
     st->stages = img.ns;
     st->mb_window = img.mb_window;
+    st->protocol = img.protocol;
 }
 
 void free_plan(ccl_plan* p)
@@ -778,6 +933,10 @@ ccl_status_t reset_flags(ccl_plan* p, cudaStream_t s)
     if (p->flags_count)
         CUDA_TRY(cudaMemsetAsync(p->d_flags, 0, p->flags_count * sizeof(unsigned long long), s), "reset flags");
     CUDA_TRY(cudaMemsetAsync(p->d_status, 0, 4 * sizeof(int), s), "reset status");
+    // LL lines carry sequence numbers as well: sequences that start over
+    // must not meet lines of an earlier run
+    if (p->img.protocol == CCL_PROTO_LL && p->d_fifo)
+        CUDA_TRY(cudaMemsetAsync(p->d_fifo, 0, p->img.fifo_bytes, s), "clear LL slots");
     p->exec = 0;
     return CCL_OK;
 }
@@ -825,6 +984,8 @@ void ccl_plan_opts_default(ccl_plan_opts_t* o)
     o->link_mode = CCL_LINK_DIRECT;
     o->channel_scaling = 1;
     o->mb_window = 0;
+    o->protocol = CCL_PROTO_SIMPLE;
+    o->pad = 0;
 }
 
 ccl_status_t ccl_schedule_compile(const ccl_op_t* ops, int32_t nops, int32_t nranks, const int32_t nchunks[3],
@@ -935,27 +1096,37 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, p->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
     cudaFuncAttributes fa{};
-    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, ccl::ccl_exec_kernel);
+    const void* kfn = ccl::exec_kernel(img.protocol);
+    if (img.protocol == CCL_PROTO_LL && img.nthreads > ccl::kMaxThreadsLL) {
+        if (opts && opts->nthreads) {
+            delete p;
+            return ccl::fail(CCL_ERR_INVALID_ARG, "plans with the LL protocol use at most 512 threads");
+        }
+        img.nthreads = ccl::kMaxThreadsLL;
+    }
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kfn);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(ccl::ccl_exec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  smem_optin - (int)fa.sharedSizeBytes);
     if (e != cudaSuccess) { delete p; return ccl::cuda_fail(e, "device attributes"); }
     const int need_sm = nsm > 0 ? (img.ntb + nsm - 1) / nsm : 1;
     int budget = smem_sm / std::max(1, need_sm) - (int)fa.sharedSizeBytes - 1024;
     budget = std::min(budget, smem_optin - (int)fa.sharedSizeBytes);
     const int64_t stage_bytes = img.tile_bytes;
-    int ns = img.bulk && img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / stage_bytes) : 0;
+    // LL plans move every tile through registers
+    const bool can_bulk = img.bulk && img.protocol != CCL_PROTO_LL && img.tile_bytes > 0;
+    int ns = can_bulk ? (int)std::min<int64_t>(8, budget / stage_bytes) : 0;
     if (ns < 2) ns = 0;
     while (true) {
         size_t dyn = (size_t)ns * stage_bytes;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ccl::ccl_exec_kernel, img.nthreads, dyn);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, img.nthreads, dyn);
         if (e != cudaSuccess) { delete p; return ccl::cuda_fail(e, "occupancy query"); }
         if ((int64_t)per_sm * nsm >= img.ntb) break;
         if (ns > 2) { --ns; continue; }
         if (ns > 0) { ns = 0; continue; }
         if ((opts && opts->nthreads) || img.nthreads <= 128) break;
         img.nthreads = img.nthreads / 2 >= 128 ? img.nthreads / 2 : 128;
-        ns = img.bulk && img.tile_bytes > 0 ? (int)std::min<int64_t>(8, budget / stage_bytes) : 0;
+        ns = can_bulk ? (int)std::min<int64_t>(8, budget / stage_bytes) : 0;
         if (ns < 2) ns = 0;
     }
     img.ns = ns;
@@ -1017,6 +1188,8 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
     k.timeline = p->d_timeline;
     k.m = img.m;
     k.slot_bytes = img.slot_bytes;
+    k.ll = img.protocol == CCL_PROTO_LL;
+    k.slot_stride = k.ll ? 2 * img.slot_bytes : img.slot_bytes;
     k.tile_bytes = img.tile_bytes;
     k.ns = img.ns;
     k.timeout_ns = (unsigned long long)img.timeout_ms * 1000000ull;
@@ -1036,6 +1209,9 @@ ccl_status_t ccl_execute(ccl_plan_t p, void* const* in_bufs, void* const* out_bu
             return ccl::fail(CCL_ERR_INVALID_ARG, "null buffer for rank " + std::to_string(r));
         if (((uintptr_t)in_bufs[r] | (uintptr_t)out_bufs[r]) % es)
             return ccl::fail(CCL_ERR_INVALID_ARG, "buffer of rank " + std::to_string(r) + " is not element aligned");
+        if (p->img.protocol == CCL_PROTO_LL && ((uintptr_t)in_bufs[r] | (uintptr_t)out_bufs[r]) % 16)
+            return ccl::fail(CCL_ERR_INVALID_ARG, "the LL protocol needs 16-byte aligned buffers (rank " +
+                                                      std::to_string(r) + ")");
     }
     ccl::KParams k = p->kp;
     for (int r = 0; r < p->nranks; ++r) {
@@ -1046,7 +1222,7 @@ ccl_status_t ccl_execute(ccl_plan_t p, void* const* in_bufs, void* const* out_bu
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p->img.ntb == 0) return CCL_OK;  // empty program: nothing to move
     void* args[] = {&k};
-    cudaError_t e = cudaLaunchCooperativeKernel((const void*)ccl::ccl_exec_kernel, dim3(p->img.ntb),
+    cudaError_t e = cudaLaunchCooperativeKernel(ccl::exec_kernel(p->img.protocol), dim3(p->img.ntb),
                                                 dim3(p->img.nthreads), args,
                                                 (size_t)p->img.ns * p->img.tile_bytes, s);
     if (e != cudaSuccess) return ccl::cuda_fail(e, "executor launch");

@@ -1,8 +1,8 @@
 // Tuner: subspace coordinate descent over the resource parameters.
 //
 // AutoCCL report, "research method" 1-2: implementation parameters (here:
-// the threadblock allocation policy) split the search space into small
-// subspaces; inside each, the resource parameters nChannel, nThread and
+// the threadblock allocation policy and the FIFO protocol) split the search
+// space into small subspaces; inside each, the resource parameters nChannel, nThread and
 // chunk size are optimised one coordinate at a time, raising a parameter
 // while bandwidth keeps improving (bandwidth is unimodal in each of them).
 // Grids: channels {1,2,4,8,12,16,24,32,48}, threads {128,256,512,1024},
@@ -31,11 +31,11 @@ struct Prober {
     cudaStream_t stream;
     int reps;
     int probes = 0;
-    std::map<std::tuple<int, int, int64_t, int>, double> cache;  // -> microseconds (0 = infeasible)
+    std::map<std::tuple<int, int, int64_t, int, int>, double> cache;  // -> microseconds (0 = infeasible)
 
     double time_us(const ccl_plan_opts_t& o)
     {
-        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc);
+        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
         ++probes;
@@ -125,15 +125,16 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
         base.link_mode = z.link_mode;
         base.channel_scaling = z.channel_scaling;
         base.mb_window = z.mb_window;
+        base.protocol = z.protocol;
     }
     if (!base.nthreads) base.nthreads = 512;
     std::vector<int> gc(std::begin(kChannels), std::end(kChannels));
     std::vector<int> gt(std::begin(kThreads), std::end(kThreads));
     std::vector<int64_t> gs = slot_grid();
-    std::map<std::tuple<int, int, int64_t, int>, double> cache;
+    std::map<std::tuple<int, int, int64_t, int, int>, double> cache;
     int nprobe = 0;
     auto measure = [&](const ccl_plan_opts_t& o) {
-        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc);
+        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
         ++nprobe;
@@ -144,9 +145,10 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
     };
     ccl_plan_opts_t overall = base;
     double overall_bw = measure(base);
-    for (int alloc : {CCL_TB_CONNECTION, CCL_TB_PACKED}) {
+    for (int sub = 0; sub < 4; ++sub) {
         ccl_plan_opts_t cur = base;
-        cur.tb_alloc = alloc;
+        cur.tb_alloc = sub & 1 ? CCL_TB_PACKED : CCL_TB_CONNECTION;
+        cur.protocol = sub & 2 ? CCL_PROTO_LL : CCL_PROTO_SIMPLE;
         int ic = nearest(gc, cur.channels), it = nearest(gt, cur.nthreads), is = nearest(gs, cur.slot_bytes);
         auto eval = [&](int c, int t, int sl) {
             ccl_plan_opts_t o = cur;

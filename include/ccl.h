@@ -174,6 +174,7 @@ typedef enum { CCL_SCHED_RR = 0, CCL_SCHED_HPDS = 1 } ccl_scheduler_t;
 typedef enum { CCL_TB_CONNECTION = 0, CCL_TB_PACKED = 1 } ccl_tb_alloc_t;
 typedef enum { CCL_MB_AUTO = 0, CCL_MB_ALGO = 1, CCL_MB_TASK = 2, CCL_MB_SEGMENT = 3 } ccl_mb_order_t;
 typedef enum { CCL_LINK_FIFO = 0, CCL_LINK_DIRECT = 1 } ccl_link_mode_t;
+typedef enum { CCL_PROTO_SIMPLE = 0, CCL_PROTO_LL = 1 } ccl_protocol_t;
 
 /*
  * Execution parameters of a plan (zero fields take the defaults written by
@@ -215,6 +216,19 @@ typedef enum { CCL_LINK_FIFO = 0, CCL_LINK_DIRECT = 1 } ccl_link_mode_t;
  *                 auto: min(m, fifo_slots / 2) first (a window and the next
  *                 one fit in the FIFO together), then 1, keeping the first
  *                 that can finish.
+ *   protocol    : FIFO signalling (AutoCCL report: implementation parameter
+ *                 "protocol"; MSCCLang report §III.1 runtime protocols).
+ *                 CCL_PROTO_SIMPLE: a slot is published by a flag after its
+ *                 data (release fence on the sender, flag poll and acquire
+ *                 fence on the receiver).  CCL_PROTO_LL: every 4 data bytes
+ *                 travel in one 64-bit line with the slot's flag in the high
+ *                 half, written and polled with 64-bit accesses (single-copy
+ *                 atomic), so the receiver's data path reads the data as soon
+ *                 as it lands, with no fence or flag round trip in between;
+ *                 a slot occupies 2 x slot_bytes.  LL needs chunk sizes that
+ *                 are multiples of 16 bytes, 16-byte aligned buffers and at
+ *                 most 512 threads (bulk copies are off); it suits the
+ *                 latency-bound sizes.
  *   timeout_ms  : limit of every device flag wait.
  *   instrument  : 1 = record per-step global-timer stamps (ccl_plan_timeline).
  *   tile_bytes  : the executor moves a slot in tiles of this size (multiple of
@@ -248,6 +262,8 @@ typedef struct {
     int32_t link_mode;
     int32_t channel_scaling;
     int32_t mb_window;
+    int32_t protocol;
+    int32_t pad;
 } ccl_plan_opts_t;
 
 void ccl_plan_opts_default(ccl_plan_opts_t* o);
@@ -314,6 +330,8 @@ typedef struct {
     int64_t tile_bytes;          /* tile of the data path */
     int32_t stages;              /* shared-memory stages of the bulk path (0: registers only) */
     int32_t mb_window;           /* micro-batch window actually used */
+    int32_t protocol;            /* CCL_PROTO_* */
+    int32_t pad;
 } ccl_plan_stats_t;
 
 ccl_status_t ccl_plan_stats(ccl_plan_t p, ccl_plan_stats_t* st);
@@ -453,9 +471,11 @@ ccl_status_t ccl_allreduce_ring_noalloc(void* const* in_bufs, void* const* out_b
                                         int64_t chunk_elems, int32_t dtype, int32_t channels, void* stream);
 
 /*
- * The search of ccl_tune on its own: subspace coordinate descent driven by a
- * caller-supplied probe that returns the bandwidth of a configuration (any
- * unit, <= 0 = cannot run).  start (nullable) is the first point; best gets
+ * The search of ccl_tune on its own (AutoCCL report, research method 1-2):
+ * the implementation parameters threadblock policy x protocol make four
+ * subspaces; in each, coordinate descent over channels, threads and slot
+ * size, driven by a caller-supplied probe that returns the bandwidth of a
+ * configuration (any unit, <= 0 = cannot run).  start (nullable) is the first point; best gets
  * the winner, *best_bw its bandwidth, *probes the number of distinct
  * configurations probed.  Host only; no device is touched unless the probe
  * does.

@@ -343,8 +343,10 @@ def test_coordinate_descent_treats_infeasible_points_as_zero():
 
 
 def test_coordinate_descent_plateau_stops_early():
+    # four subspaces (policy x protocol): on a flat surface each tries one
+    # step up and one down per coordinate (at most 6 probes), plus the start
     best, bw, n = ccl.tune_search(lambda o: 1.0)
-    assert bw == 1.0 and n <= 20
+    assert bw == 1.0 and n <= 1 + 4 * 6
 
 
 def test_microbatch_window_is_used_when_the_fifo_holds_it():
@@ -370,3 +372,30 @@ def test_microbatch_window_larger_than_the_fifo_is_rejected():
     assert e.value.code == 3
     st = s.check(65536, F32, microbatches=8, mb_window=8, fifo_slots=9, slot_bytes=32768, mb_order=ccl.MB_ALGO)
     assert st.mb_window == 8
+
+
+def test_ll_protocol_doubles_fifo_bytes_and_needs_16_byte_chunks():
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 8)
+    simple = s.check(4096, BF16, protocol=ccl.PROTO_SIMPLE, slot_bytes=16384)
+    ll = s.check(4096, BF16, protocol=ccl.PROTO_LL, slot_bytes=16384)
+    assert ll.protocol == ccl.PROTO_LL and simple.protocol == ccl.PROTO_SIMPLE
+    assert ll.fifo_bytes == 2 * simple.fifo_bytes
+    assert ll.schedule_bytes == simple.schedule_bytes
+    with pytest.raises(ccl.CclError) as e:
+        s.check(4093, BF16, protocol=ccl.PROTO_LL)      # 8186-byte chunks
+    assert e.value.code == 5
+    with pytest.raises(ccl.CclError) as e:
+        s.check(4096, BF16, protocol=7)
+    assert e.value.code == 1
+
+
+def test_coordinate_descent_visits_both_protocols():
+    seen = set()
+
+    def f(o):
+        seen.add(o.protocol)
+        return (2.0 if o.protocol == ccl.PROTO_LL else 1.0) * _surface((4, 256, 1 << 16))(o)
+    best, bw, n = ccl.tune_search(f)
+    assert seen == {ccl.PROTO_SIMPLE, ccl.PROTO_LL}
+    assert best.protocol == ccl.PROTO_LL and bw == pytest.approx(2.0)
+    assert (best.channels, best.nthreads, best.slot_bytes) == (4, 256, 1 << 16)

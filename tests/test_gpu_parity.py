@@ -137,3 +137,36 @@ def test_microbatch_windows_do_not_change_bits(ccl, window, order):
                                    tb_alloc=1, link_mode=0)
         assert_bitexact(got, want)
         assert plan.stats().mb_window in (window, 1)
+
+
+@pytest.mark.parametrize("kind,R,G", BUILTINS)
+@pytest.mark.parametrize("dtype", [F32, BF16, F16, I32])
+def test_ll_protocol_bitexact(ccl, kind, R, G, dtype):
+    """Inline-flag slots: chunks of a multiple of 16 bytes, several slots and
+    channels, FIFO and direct transport."""
+    for lm in (0, 1):
+        got, want, plan = run_case(ccl, kind, R, G, 1024, dtype, DIST[dtype], 9, protocol=1, channels=2,
+                                   slot_bytes=2048, link_mode=lm)
+        assert_bitexact(got, want)
+        assert plan.stats().protocol == 1
+
+
+def test_ll_protocol_repeated_executions_and_windows(ccl):
+    """Line flags follow the slot sequence numbers across executions; windows
+    and micro-batches keep the bits."""
+    import torch
+    import datagen
+    import oracle
+    from gpu_helpers import oracle_program, to_device, empty_outputs, to_host
+    s = ccl.Schedule.builtin(3, 16, 8)
+    plan = ccl.Plan(s, 4096, F32, protocol=1, slot_bytes=4096, fifo_slots=8, microbatches=4, mb_window=2,
+                    tb_alloc=1)
+    ops, nch = oracle_program(3, 16, 8)
+    for it in range(4):
+        ins = datagen.rank_inputs(200 + it, "normal", 16, 16 * 4096, F32)
+        d_out = empty_outputs(16, 16 * 4096, F32)
+        plan.execute(to_device(ins, F32), d_out)
+        torch.cuda.synchronize()
+        plan.status()
+        want, _, _ = oracle.run(ops, 16, nch, 4096, F32, ins)
+        assert_bitexact(to_host(d_out, F32), want)
