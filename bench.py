@@ -161,6 +161,13 @@ def schedule_and_opts(ccl, kind, R, G, opts):
     return ccl.Schedule.builtin(kind, R, G, 0 if fuse else ccl.FLAG_NOFUSE), opts
 
 
+def barrier():
+    """Barrier across replicas (no-op on one GPU)."""
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
 def selected_suite(args):
     """The suite, or a subset (--only) at reduced chunk size (--scale) for
     profiling captures."""
@@ -226,6 +233,7 @@ def run_gpu(args):
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     time.sleep(0.3)
+    barrier()
     torch.cuda.synchronize()
     t_all0.record(stream)
     for k in range(K):
@@ -235,6 +243,7 @@ def run_gpu(args):
             ev[k][j][1].record(stream)
     t_all1.record(stream)
     torch.cuda.synchronize()
+    barrier()
     clk = clocks.stop()
     for it in items:
         it["plan"].status()
@@ -405,6 +414,153 @@ def run_reference(args):
             "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def _time_plan(torch, plan, d_in, d_out, stream, reps=5, warm=2, side=None):
+    """Median device time (ms) of `reps` executions after `warm`; `side`, when
+    given, is called before each execution to queue concurrent work."""
+    ts = []
+    for k in range(warm + reps):
+        if side is not None:
+            side()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        plan.execute(d_in, d_out, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if k >= warm:
+            ts.append(a.elapsed_time(b))
+    plan.status()
+    return statistics.median(ts)
+
+
+def run_ablation(args):
+    """Scheduler (RR / HPDS) x threadblock allocation (connection / packed)
+    on the large collectives: device time, threadblocks, sub-pipelines and
+    threadblock idle fractions (one JSON line per configuration)."""
+    import torch
+    import collective_communication_schedule_gb300 as ccl
+    import datagen
+    names = args.only.split(",") if args.only else ["hier_ar", "a2a", "a2n", "ring_f32"]
+    args.only = ",".join(names)
+    items = build_suite(ccl, torch, datagen, args)
+    stream = torch.cuda.current_stream()
+    for it, row in zip(items, selected_suite(args)):
+        base = dict(row[8])
+        del it["plan"]
+        for sched in (ccl.SCHED_RR, ccl.SCHED_HPDS):
+            for alloc in (ccl.TB_CONNECTION, ccl.TB_PACKED):
+                opts = dict(base, scheduler=sched, tb_alloc=alloc)
+                sch, popts = schedule_and_opts(ccl, it["kind"], it["R"], it["G"], opts)
+                rec = {"ablation": it["name"], "scheduler": ["rr", "hpds"][sched],
+                       "tb_alloc": ["connection", "packed"][alloc]}
+                try:
+                    plan = ccl.Plan(sch, it["ce"], it["dt"], **popts)
+                    ms = _time_plan(torch, plan, it["d_in"], it["d_out"], stream)
+                    st = plan.stats()
+                    del plan
+                    inst = ccl.Plan(sch, it["ce"], it["dt"], instrument=1, **popts)
+                    _time_plan(torch, inst, it["d_in"], it["d_out"], stream, reps=1, warm=1)
+                    tl = inst.timeline()
+                    del inst
+                    rec.update(us=round(ms * 1e3, 1), schedule_gbs=round(st.schedule_bytes / (ms * 1e6), 1),
+                               threadblocks=st.nthreadblocks, threadblocks_connection=st.nthreadblocks_connection,
+                               subpipelines=st.nsubpipelines, mean_idle=round(tl["mean_idle"], 3),
+                               max_idle=round(tl["max_idle"], 3))
+                except ccl.CclError as e:
+                    rec["error"] = str(e)[:120]
+                torch.cuda.empty_cache()
+                print(json.dumps(rec), flush=True)
+
+
+def run_interference(args):
+    """Interference-aware tuning: tune one collective in isolation and again
+    while a bf16 GEMM runs on a concurrent stream; time both choices under
+    the GEMM (AutoCCL report: interference of concurrent computation).
+    Also times an exhaustive grid in isolation to place the isolated tuner's
+    choice.  One JSON line."""
+    import torch
+    import collective_communication_schedule_gb300 as ccl
+    import datagen
+    name = args.only or "ring_f32"
+    args.only = name
+    it = build_suite(ccl, torch, datagen, args)[0]
+    row = selected_suite(args)[0]
+    del it["plan"]
+    stream = torch.cuda.current_stream()
+    side_stream = torch.cuda.Stream()
+    n = 8192
+    ga = torch.randn(n, n, device="cuda", dtype=torch.bfloat16)
+    gb = torch.randn(n, n, device="cuda", dtype=torch.bfloat16)
+    gc = torch.empty(n, n, device="cuda", dtype=torch.bfloat16)
+
+    def gemm():
+        with torch.cuda.stream(side_stream):
+            for _ in range(4):
+                torch.matmul(ga, gb, out=gc)
+
+    base = dict(row[8])
+    sch, popts = schedule_and_opts(ccl, it["kind"], it["R"], it["G"], base)
+    start = ccl.default_opts()
+    for k, v in popts.items():
+        setattr(start, k, v)
+
+    def make_probe(with_gemm):
+        def probe(o):
+            try:
+                plan = ccl.Plan(sch, it["ce"], it["dt"], opts=o)
+            except ccl.CclError:
+                return 0.0
+            try:
+                ms = _time_plan(torch, plan, it["d_in"], it["d_out"], stream, reps=3, warm=1,
+                                side=gemm if with_gemm else None)
+                return plan.stats().schedule_bytes / (ms * 1e6)
+            except ccl.CclError:
+                return 0.0
+            finally:
+                del plan
+                torch.cuda.synchronize()
+        return probe
+
+    iso_best, iso_bw, iso_n = ccl.tune_search(make_probe(False), start=start)
+    int_best, int_bw, int_n = ccl.tune_search(make_probe(True), start=start)
+
+    def t_us(o, with_gemm):
+        plan = ccl.Plan(sch, it["ce"], it["dt"], opts=o)
+        ms = _time_plan(torch, plan, it["d_in"], it["d_out"], stream, reps=7, warm=2,
+                        side=gemm if with_gemm else None)
+        del plan
+        return round(ms * 1e3, 1)
+
+    def cfg(o):
+        return {"channels": o.channels, "nthreads": o.nthreads, "slot_bytes": o.slot_bytes,
+                "tb_alloc": o.tb_alloc, "protocol": o.protocol}
+
+    # exhaustive grid in isolation (the tuner's resource grid, both policies,
+    # flag protocol), best point
+    grid_best, grid_us, grid_n = None, None, 0
+    for alloc in (ccl.TB_CONNECTION, ccl.TB_PACKED):
+        for ch in (1, 2, 4, 8, 12, 16, 24, 32, 48):
+            for nt in (128, 256, 512, 1024):
+                for sl in (16384, 32768, 65536, 131072, 262144, 524288, 1048576):
+                    o = ccl.default_opts()
+                    for k, v in popts.items():
+                        setattr(o, k, v)
+                    o.tb_alloc, o.channels, o.nthreads, o.slot_bytes = alloc, ch, nt, sl
+                    bw = make_probe(False)(o)
+                    grid_n += 1
+                    if bw > 0 and (grid_us is None or it["stats"].schedule_bytes / (bw * 1e3) < grid_us):
+                        grid_us = it["stats"].schedule_bytes / (bw * 1e3)
+                        grid_best = cfg(o)
+    out = {"interference": name, "gemm": f"bf16 {n}x{n}x{n}, 4 per execution on a concurrent stream",
+           "isolated_tuned": cfg(iso_best), "interference_tuned": cfg(int_best),
+           "probes": {"isolated": iso_n, "interference": int_n, "grid": grid_n},
+           "us": {"isolated_cfg_alone": t_us(iso_best, False), "isolated_cfg_with_gemm": t_us(iso_best, True),
+                  "interference_cfg_with_gemm": t_us(int_best, True), "default_cfg_alone": t_us(start, False),
+                  "grid_best_alone": round(grid_us, 1) if grid_us else None},
+           "grid_best": grid_best}
+    out["gain_under_interference"] = round(out["us"]["isolated_cfg_with_gemm"] / out["us"]["interference_cfg_with_gemm"], 3)
+    print(json.dumps(out))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -416,7 +572,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma-separated subset of the suite (profiling)")
     ap.add_argument("--scale", type=float, default=1.0, help="chunk size factor (profiling)")
+    ap.add_argument("--ablation", action="store_true", help="scheduler x threadblock allocation table")
+    ap.add_argument("--interference", action="store_true",
+                    help="tune one collective (--only, default ring_f32) alone and beside a bf16 GEMM")
     args = ap.parse_args()
+    if args.ablation or args.interference:
+        import torch
+        torch.cuda.set_device(0)
+        run_ablation(args) if args.ablation else run_interference(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
