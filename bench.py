@@ -43,7 +43,7 @@ SUITE = [
     ("hier_ar", 3, 16, 8, 0, 4 * MiB, "normal", 2,
      dict(channels=8, microbatches=16, tb_alloc=1, slot_bytes=65536, fifo_slots=8, mb_window=4)),
     ("a2a", 4, 32, 8, 2, 1 * MiB, "uniform", 3,
-     dict(channels=4, link_mode=1, bulk=1, tile_bytes=16384, channel_scaling=0, tb_alloc=1)),
+     dict(channels=8, link_mode=1, channel_scaling=0, tb_alloc=2, tb_budget=256)),
     ("ring_bf16", 0, 8, 0, 1, 32 * MiB, "normal", 4, dict(channels=24, slot_bytes=131072)),
     ("ring_f32", 0, 8, 0, 0, 32 * MiB, "normal", 4, dict(channels=24, slot_bytes=131072)),
     # relay hops as plain direct copies (no fusion into FIFO forwards)
@@ -273,18 +273,31 @@ def run_gpu(args):
     avg_launch_ms = kern_ms_total / (K * len(items))
     achieved = (sched_bytes / len(items)) / (avg_launch_ms * 1e6)
 
-    # end to end through the C ABI with host buffers (H2D + execute + D2H)
+    # end to end through the C ABI with host buffers (H2D + execute + D2H per
+    # collective).  The collectives of a step are independent, so they
+    # alternate over two streams: one collective's output copies overlap the
+    # next one's input copies (host<->device copies run in both directions
+    # at once).
     Ke = max(1, min(K, args.e2e_steps))
     h2d = sum(it["plan"].in_elems * ESIZE[it["dt"]] * it["R"] for it in items)
     d2h = sum(it["plan"].out_elems * ESIZE[it["dt"]] * it["R"] for it in items)
-    for it in items:   # one warm pass
-        it["plan"].execute_host(it["h_in"], it["h_out"], it["d_in"], it["d_out"], stream)
+    e2e_streams = [stream, torch.cuda.Stream()]
+
+    def e2e_pass():
+        for j, it in enumerate(items):
+            s = e2e_streams[j % 2]
+            it["plan"].execute_host(it["h_in"], it["h_out"], it["d_in"], it["d_out"], s)
+
+    e2e_pass()   # warm
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    e2e_streams[1].wait_event(e0)
     for _ in range(Ke):
-        for it in items:
-            it["plan"].execute_host(it["h_in"], it["h_out"], it["d_in"], it["d_out"], stream)
+        e2e_pass()
+    joined = torch.cuda.Event()
+    joined.record(e2e_streams[1])
+    stream.wait_event(joined)
     e1.record(stream)
     torch.cuda.synchronize()
     for it in items:
@@ -561,6 +574,48 @@ def run_interference(args):
     print(json.dumps(out))
 
 
+def run_alltoallv(args):
+    """Second workload: uneven AllToAll of a mixture-of-experts layer.  32
+    ranks (one expert each), 4096 tokens per rank of 4096 bf16 values (one
+    8 KiB chunk per token), Zipf(1.2) expert popularity (datagen recipe,
+    seed 3).  One JSON line per plan configuration."""
+    import numpy as np
+    import torch
+    import collective_communication_schedule_gb300 as ccl
+    import datagen
+    R, tokens, hidden = 32, int(4096 * args.scale), 4096
+    counts = datagen.alltoallv_counts(3, R, tokens)
+    sch = ccl.Schedule.alltoallv(counts)
+    nin, nout = sch.info().nchunks[0] * hidden, sch.info().nchunks[1] * hidden
+    rng = np.random.default_rng(3)
+    d_in = [torch.from_numpy(datagen.draw(rng, "normal", nin, ccl.BF16).view(np.int16)).cuda() for _ in range(R)]
+    d_out = [torch.empty(nout, dtype=torch.int16, device="cuda") for _ in range(R)]
+    stream = torch.cuda.current_stream()
+    peak, _ = peaks()
+    # channels in proportion to a pair's size (channel_scaling): the hot
+    # expert's pairs get many threadblocks, the small pairs one
+    # balanced allocation: a rank's direct copies binned into a few large
+    # threadblocks instead of one small threadblock per pair
+    configs = [dict(link_mode=1, tb_alloc=1, channels=4, bulk=1)] + \
+              [dict(link_mode=1, tb_alloc=2, channels=c, channel_scaling=0, tb_budget=b)
+               for c in (2, 4, 8) for b in (256, 512)]
+    for o in configs:
+        rec = {"workload": "alltoallv", "ranks": R, "tokens_per_rank": tokens, "chunk_bytes": hidden * 2,
+               "max_in_chunks": int(counts.sum(1).max()), "max_out_chunks": int(counts.sum(0).max()), "opts": o}
+        try:
+            plan = ccl.Plan(sch, hidden, ccl.BF16, **o)
+            ms = _time_plan(torch, plan, d_in, d_out, stream, reps=args.steps, warm=args.warmup)
+            st = plan.stats()
+            rec.update(us=round(ms * 1e3, 1), schedule_gbs=round(st.schedule_bytes / (ms * 1e6), 1),
+                       frac_of_peak=round(st.schedule_bytes / (ms * 1e6) / peak, 3),
+                       min_bytes_gbs=round(st.min_bytes / (ms * 1e6), 1), threadblocks=st.nthreadblocks,
+                       nthreads=st.nthreads)
+            del plan
+        except ccl.CclError as e:
+            rec["error"] = str(e)[:120]
+        print(json.dumps(rec), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -575,11 +630,17 @@ def main():
     ap.add_argument("--ablation", action="store_true", help="scheduler x threadblock allocation table")
     ap.add_argument("--interference", action="store_true",
                     help="tune one collective (--only, default ring_f32) alone and beside a bf16 GEMM")
+    ap.add_argument("--alltoallv", action="store_true", help="second workload: uneven (MoE) AllToAll")
     args = ap.parse_args()
-    if args.ablation or args.interference:
+    if args.ablation or args.interference or args.alltoallv:
         import torch
         torch.cuda.set_device(0)
-        run_ablation(args) if args.ablation else run_interference(args)
+        if args.ablation:
+            run_ablation(args)
+        elif args.interference:
+            run_interference(args)
+        else:
+            run_alltoallv(args)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -22,10 +22,10 @@ _LIB_PATH = os.path.join(_HERE, "libccl.so")
 F32, BF16, F16, I32 = 0, 1, 2, 3
 IN, OUT, SCRATCH = 0, 1, 2
 COPY, REDUCE = 0, 1
-RING_ALLREDUCE, RING_ALLGATHER, RING_REDUCESCATTER, HIER_ALLREDUCE, ALLTOALL_2PHASE, ALLTONEXT = range(6)
+RING_ALLREDUCE, RING_ALLGATHER, RING_REDUCESCATTER, HIER_ALLREDUCE, ALLTOALL_2PHASE, ALLTONEXT, ALLTOALLV = range(7)
 FLAG_WRAP, FLAG_NOFUSE = 1, 2
 SCHED_RR, SCHED_HPDS = 0, 1
-TB_CONNECTION, TB_PACKED = 0, 1
+TB_CONNECTION, TB_PACKED, TB_BALANCED = 0, 1, 2
 MB_AUTO, MB_ALGO, MB_TASK, MB_SEGMENT = 0, 1, 2, 3
 LINK_FIFO, LINK_DIRECT = 0, 1
 PROTO_SIMPLE, PROTO_LL = 0, 1
@@ -70,7 +70,7 @@ class PlanOpts(ctypes.Structure):
                 ("tb_alloc", ctypes.c_int32), ("mb_order", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("instrument", ctypes.c_int32), ("tile_bytes", ctypes.c_int64), ("bulk", ctypes.c_int32),
                 ("link_mode", ctypes.c_int32), ("channel_scaling", ctypes.c_int32), ("mb_window", ctypes.c_int32),
-                ("protocol", ctypes.c_int32), ("pad", ctypes.c_int32)]
+                ("protocol", ctypes.c_int32), ("tb_budget", ctypes.c_int32)]
 
 
 class PlanStats(ctypes.Structure):
@@ -114,6 +114,7 @@ def _load():
         "ccl_schedule_compile": [ctypes.POINTER(Op), I32_, I32_, ctypes.POINTER(ctypes.c_int32), I32_,
                                  ctypes.POINTER(P)],
         "ccl_schedule_builtin": [I32_, I32_, I32_, U32_, ctypes.POINTER(P)],
+        "ccl_schedule_alltoallv": [I32_, ctypes.POINTER(ctypes.c_int32), U32_, ctypes.POINTER(P)],
         "ccl_schedule_info": [P, ctypes.POINTER(ScheduleInfo)],
         "ccl_schedule_get_ops": [P, ctypes.POINTER(Op), I32_, ctypes.POINTER(ctypes.c_int32)],
         "ccl_schedule_get_instrs": [P, ctypes.POINTER(InstrInfo), I32_, ctypes.POINTER(ctypes.c_int32)],
@@ -198,6 +199,19 @@ class Schedule:
     def builtin(cls, kind, nranks, group_size=0, flags=0):
         h = ctypes.c_void_p()
         _check(lib.ccl_schedule_builtin(kind, nranks, group_size, flags, ctypes.byref(h)))
+        return cls(h.value)
+
+    @classmethod
+    def alltoallv(cls, counts, flags=0):
+        """Uneven AllToAll: ``counts[s][d]`` chunks from rank s to rank d
+        (``ccl_schedule_alltoallv``)."""
+        rows = [[int(c) for c in row] for row in counts]
+        R = len(rows)
+        if any(len(r) != R for r in rows):
+            raise ValueError("counts must be square")
+        arr = (ctypes.c_int32 * max(1, R * R))(*[c for r in rows for c in r])
+        h = ctypes.c_void_p()
+        _check(lib.ccl_schedule_alltoallv(R, arr, flags, ctypes.byref(h)))
         return cls(h.value)
 
     @classmethod

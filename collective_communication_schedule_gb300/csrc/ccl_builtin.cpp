@@ -17,6 +17,9 @@
 //  * AllToNext (MSCCLang report, §II and §IV.4): out[r+1] = in[r]; a pair
 //    crossing a group boundary is split into G parts, part j relayed through
 //    local rank j on both sides so every link of both groups carries a share.
+//  * Uneven AllToAll (per-pair sizes, MoE token exchange): one copy per
+//    non-empty (source, destination) pair, in shift order.
+#include <algorithm>
 #include <string>
 
 #include "ccl_internal.h"
@@ -150,6 +153,51 @@ void alltonext(int G, int ng, bool wrap, std::vector<ccl_op_t>& v)
 }
 
 }  // namespace
+
+ccl_status_t alltoallv_program(int R, const int32_t* counts, std::vector<ccl_op_t>* ops, int32_t nchunks[3])
+{
+    if (R < 1 || R > CCL_MAX_RANKS)
+        return fail(CCL_ERR_INVALID_ARG, "nranks must be in 1.." + std::to_string(CCL_MAX_RANKS));
+    if (!counts) return fail(CCL_ERR_INVALID_ARG, "null counts");
+    // block offsets: rank s's input in destination order, rank d's output
+    // in source order
+    std::vector<int64_t> in_off((size_t)R * R), out_off((size_t)R * R);
+    int64_t max_in = 0, max_out = 0, total = 0;
+    for (int s = 0; s < R; ++s) {
+        int64_t o = 0;
+        for (int d = 0; d < R; ++d) {
+            const int32_t c = counts[(size_t)s * R + d];
+            if (c < 0) return fail(CCL_ERR_INVALID_ARG, "negative count");
+            in_off[(size_t)s * R + d] = o;
+            o += c;
+        }
+        max_in = std::max(max_in, o);
+        total += o;
+    }
+    for (int d = 0; d < R; ++d) {
+        int64_t o = 0;
+        for (int s = 0; s < R; ++s) {
+            out_off[(size_t)s * R + d] = o;
+            o += counts[(size_t)s * R + d];
+        }
+        max_out = std::max(max_out, o);
+    }
+    if (total == 0) return fail(CCL_ERR_INVALID_ARG, "no chunk to move");
+    if (max_in > (1 << 30) || max_out > (1 << 30)) return fail(CCL_ERR_INVALID_ARG, "per-rank total above 2^30 chunks");
+    ops->clear();
+    for (int k = 0; k < R; ++k)
+        for (int s = 0; s < R; ++s) {
+            const int d = (s + k) % R;
+            const int32_t c = counts[(size_t)s * R + d];
+            if (c > 0)
+                ops->push_back(mk(CP, s, IN, (int)in_off[(size_t)s * R + d], d, OUT,
+                                  (int)out_off[(size_t)s * R + d], c));
+        }
+    nchunks[0] = (int32_t)max_in;
+    nchunks[1] = (int32_t)max_out;
+    nchunks[2] = 0;
+    return CCL_OK;
+}
 
 ccl_status_t builtin_program(int kind, int R, int G, uint32_t flags, std::vector<ccl_op_t>* ops,
                              int32_t nchunks[3])

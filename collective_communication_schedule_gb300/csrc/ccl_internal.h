@@ -82,5 +82,7 @@ ccl_status_t compile_program(const ccl_op_t* ops, int nops, int nranks, const in
                              bool fuse, ccl_schedule* s);
 ccl_status_t builtin_program(int kind, int nranks, int G, uint32_t flags,
                              std::vector<ccl_op_t>* ops, int32_t nchunks[3]);
+// uneven AllToAll: counts[s * R + d] chunks from s to d
+ccl_status_t alltoallv_program(int R, const int32_t* counts, std::vector<ccl_op_t>* ops, int32_t nchunks[3]);
 
 }  // namespace ccl

@@ -261,6 +261,58 @@ void pack_state_based(const ccl_schedule& s, const Timeline& tl, TBList* tbs, st
     }
 }
 
+// Balanced allocation: threadblocks of a rank that run only link-free
+// instructions (local copies, direct copies: no FIFO, so any number of them
+// may share a threadblock in program order) are merged into at most `cap`
+// threadblocks, largest first into the least loaded (bytes in chunk units).
+void balance_linkfree(const ccl_schedule& s, const Timeline& tl, TBList* tbs, std::vector<int>* tb_rank, int cap)
+{
+    struct B { int rank; std::vector<int> instrs; int64_t load; };
+    std::vector<B> out;
+    std::map<int, std::vector<int>> free_tbs;   // rank -> link-free threadblocks
+    for (size_t t = 0; t < tbs->size(); ++t) {
+        bool link_free = true;
+        for (int i : (*tbs)[t]) link_free = link_free && s.instrs[i].xfer_in < 0 && s.instrs[i].xfer_out < 0;
+        if (link_free) free_tbs[(*tb_rank)[t]].push_back((int)t);
+        else out.push_back(B{(*tb_rank)[t], (*tbs)[t], 0});
+    }
+    for (auto& kv : free_tbs) {
+        std::vector<int>& v = kv.second;
+        if ((int)v.size() <= cap) {
+            for (int t : v) out.push_back(B{kv.first, (*tbs)[t], 0});
+            continue;
+        }
+        auto weight = [&](int t) {
+            int64_t w = 0;
+            for (int i : (*tbs)[t]) w += s.instrs[i].count;
+            return w;
+        };
+        std::stable_sort(v.begin(), v.end(), [&](int a, int b) { return weight(a) > weight(b); });
+        std::vector<B> bins(cap, B{kv.first, {}, 0});
+        for (int t : v) {
+            int k = 0;
+            for (int b = 1; b < cap; ++b)
+                if (bins[b].load < bins[k].load) k = b;
+            bins[k].instrs.insert(bins[k].instrs.end(), (*tbs)[t].begin(), (*tbs)[t].end());
+            bins[k].load += weight(t);
+        }
+        for (auto& b : bins) {
+            std::sort(b.instrs.begin(), b.instrs.end(), [&](int a, int c) {
+                if (tl.sp_hi[a] != tl.sp_hi[c]) return tl.sp_hi[a] < tl.sp_hi[c];
+                return s.instrs[a].position < s.instrs[c].position;
+            });
+            out.push_back(std::move(b));
+        }
+    }
+    std::stable_sort(out.begin(), out.end(), [](const B& a, const B& b) { return a.rank < b.rank; });
+    tbs->clear();
+    tb_rank->clear();
+    for (auto& b : out) {
+        tbs->push_back(std::move(b.instrs));
+        tb_rank->push_back(b.rank);
+    }
+}
+
 // Epoch of every instruction: the largest number of whole-instruction
 // dependencies (partly overlapping ranges) on a path into it, following
 // same-rank dependencies and transfers.  Such a dependency needs every
@@ -825,7 +877,9 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
     if (o.fifo_slots < 2 || o.fifo_slots > 64) return fail(CCL_ERR_INVALID_ARG, "fifo_slots must be in 2..64");
     if (o.microbatches < 0 || o.microbatches > 65536) return fail(CCL_ERR_INVALID_ARG, "microbatches out of range");
     if (o.scheduler != CCL_SCHED_RR && o.scheduler != CCL_SCHED_HPDS) return fail(CCL_ERR_INVALID_ARG, "unknown scheduler");
-    if (o.tb_alloc != CCL_TB_CONNECTION && o.tb_alloc != CCL_TB_PACKED) return fail(CCL_ERR_INVALID_ARG, "unknown tb_alloc");
+    if (o.tb_alloc != CCL_TB_CONNECTION && o.tb_alloc != CCL_TB_PACKED && o.tb_alloc != CCL_TB_BALANCED)
+        return fail(CCL_ERR_INVALID_ARG, "unknown tb_alloc");
+    if (o.tb_budget < 0) return fail(CCL_ERR_INVALID_ARG, "tb_budget must not be negative");
     if (o.mb_order < CCL_MB_AUTO || o.mb_order > CCL_MB_SEGMENT) return fail(CCL_ERR_INVALID_ARG, "unknown mb_order");
     if (o.mb_window < 0 || o.mb_window > 65536) return fail(CCL_ERR_INVALID_ARG, "mb_window out of range");
     if (o.protocol != CCL_PROTO_SIMPLE && o.protocol != CCL_PROTO_LL) return fail(CCL_ERR_INVALID_ARG, "unknown protocol");
@@ -847,7 +901,11 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
     allocate_connection(s, tl, &conn, &conn_rank);
     TBList packed = conn;
     std::vector<int> packed_rank = conn_rank;
-    if (o.tb_alloc == CCL_TB_PACKED) pack_state_based(s, tl, &packed, &packed_rank);
+    if (o.tb_alloc == CCL_TB_PACKED || o.tb_alloc == CCL_TB_BALANCED) pack_state_based(s, tl, &packed, &packed_rank);
+    if (o.tb_alloc == CCL_TB_BALANCED) {
+        const int budget = o.tb_budget > 0 ? o.tb_budget : 256;
+        balance_linkfree(s, tl, &packed, &packed_rank, std::max(1, budget / std::max(1, s.nranks * o.channels)));
+    }
 
     // micro-batch candidates
     int64_t max_slots = 1;
@@ -870,7 +928,7 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
     if (o.mb_order == CCL_MB_AUTO) orders = {CCL_MB_ALGO, CCL_MB_SEGMENT, CCL_MB_TASK};
     else orders = {o.mb_order};
     std::vector<int> allocs;
-    if (o.tb_alloc == CCL_TB_PACKED) allocs = {CCL_TB_PACKED, CCL_TB_CONNECTION};
+    if (o.tb_alloc == CCL_TB_PACKED || o.tb_alloc == CCL_TB_BALANCED) allocs = {CCL_TB_PACKED, CCL_TB_CONNECTION};
     else allocs = {CCL_TB_CONNECTION};
 
     std::string first_why;
@@ -955,6 +1013,7 @@ done:
         case CCL_RING_ALLGATHER: img->data_bytes_per_rank = out_b; img->busbw_factor = (R - 1) / R; break;
         case CCL_RING_REDUCESCATTER: img->data_bytes_per_rank = in_b; img->busbw_factor = (R - 1) / R; break;
         case CCL_ALLTOALL_2PHASE: img->data_bytes_per_rank = in_b; img->busbw_factor = (R - 1) / R; break;
+        case CCL_ALLTOALLV: img->data_bytes_per_rank = in_b; img->busbw_factor = (R - 1) / R; break;
         case CCL_ALLTONEXT: img->data_bytes_per_rank = in_b; img->busbw_factor = 1.0; break;
         default: img->data_bytes_per_rank = in_b; img->busbw_factor = 0.0; break;
         }

@@ -882,6 +882,7 @@ ccl_plan_opts_t merged_opts(const ccl_plan_opts_t* opts)
         o.channel_scaling = opts->channel_scaling;
         o.mb_window = opts->mb_window;
         o.protocol = opts->protocol;
+        o.tb_budget = opts->tb_budget;
     }
     return o;
 }
@@ -985,7 +986,7 @@ void ccl_plan_opts_default(ccl_plan_opts_t* o)
     o->channel_scaling = 1;
     o->mb_window = 0;
     o->protocol = CCL_PROTO_SIMPLE;
-    o->pad = 0;
+    o->tb_budget = 0;
 }
 
 ccl_status_t ccl_schedule_compile(const ccl_op_t* ops, int32_t nops, int32_t nranks, const int32_t nchunks[3],
@@ -1012,6 +1013,22 @@ ccl_status_t ccl_schedule_builtin(int32_t kind, int32_t nranks, int32_t group_si
     if (st != CCL_OK) { delete s; return st; }
     s->builtin = kind;
     s->group_size = group_size;
+    *out = s;
+    return CCL_OK;
+}
+
+ccl_status_t ccl_schedule_alltoallv(int32_t nranks, const int32_t* counts, uint32_t flags, ccl_schedule_t* out)
+{
+    if (!out) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    std::vector<ccl_op_t> ops;
+    int32_t nch[3] = {0, 0, 0};
+    ccl_status_t st = ccl::alltoallv_program(nranks, counts, &ops, nch);
+    if (st != CCL_OK) return st;
+    auto* s = new ccl_schedule();
+    st = ccl::compile_program(ops.data(), (int)ops.size(), nranks, nch, (flags & CCL_FLAG_NOFUSE) == 0, s);
+    if (st != CCL_OK) { delete s; return st; }
+    s->builtin = CCL_ALLTOALLV;
+    s->group_size = 0;
     *out = s;
     return CCL_OK;
 }

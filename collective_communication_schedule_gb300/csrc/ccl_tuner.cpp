@@ -126,6 +126,7 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
         base.channel_scaling = z.channel_scaling;
         base.mb_window = z.mb_window;
         base.protocol = z.protocol;
+        base.tb_budget = z.tb_budget;
     }
     if (!base.nthreads) base.nthreads = 512;
     std::vector<int> gc(std::begin(kChannels), std::end(kChannels));

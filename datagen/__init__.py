@@ -76,3 +76,17 @@ def to_f64(a: np.ndarray, dtype: int) -> np.ndarray:
     if dtype == BF16:
         return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     raise ValueError(dtype)
+
+
+def alltoallv_counts(seed: int, nranks: int, tokens_per_rank: int, skew: float = 1.2) -> np.ndarray:
+    """Token routing of a mixture-of-experts layer with one expert per rank:
+    expert popularity follows a Zipf law of exponent ``skew`` over a random
+    order of the experts (fresh generator from ``seed``), and every rank
+    draws the destinations of its ``tokens_per_rank`` tokens from it
+    (multinomial).  Returns counts[s][d] (int32, rows sum to
+    tokens_per_rank)."""
+    rng = np.random.default_rng(seed)
+    weight = 1.0 / np.arange(1, nranks + 1, dtype=np.float64) ** skew
+    p = weight[rng.permutation(nranks)]
+    p /= p.sum()
+    return np.stack([rng.multinomial(tokens_per_rank, p) for _ in range(nranks)]).astype(np.int32)

@@ -88,7 +88,8 @@ typedef enum {
     CCL_RING_REDUCESCATTER = 2, /* out[r] = chunk r of sum_k in[k]; in R chunks, out 1 chunk */
     CCL_HIER_ALLREDUCE = 3,     /* R = G*ng; intra RS, inter ring AR per slice, intra AG */
     CCL_ALLTOALL_2PHASE = 4,    /* out[d] block s = in[s] block d; R = G*ng */
-    CCL_ALLTONEXT = 5           /* out[r+1] = in[r]; cross-group pairs relayed in G parts */
+    CCL_ALLTONEXT = 5,          /* out[r+1] = in[r]; cross-group pairs relayed in G parts */
+    CCL_ALLTOALLV = 6           /* uneven AllToAll: built by ccl_schedule_alltoallv only */
 } ccl_builtin_t;
 
 #define CCL_FLAG_WRAP 1u    /* AllToNext: also send rank R-1 -> rank 0 */
@@ -158,6 +159,22 @@ ccl_status_t ccl_schedule_compile(const ccl_op_t* ops, int32_t nops, int32_t nra
 ccl_status_t ccl_schedule_builtin(int32_t kind, int32_t nranks, int32_t group_size,
                                   uint32_t flags, ccl_schedule_t* out);
 
+/*
+ * Uneven AllToAll (MoE-style token exchange; a variant with per-pair sizes
+ * of the AllToAll of the MSCCLang report §IV.3): counts[s * nranks + d] >= 0
+ * chunks go from rank s to rank d.  Rank s's input holds its blocks for
+ * d = 0, 1, ... in that order (sizes counts[s][d]); rank d's output holds
+ * the blocks from s = 0, 1, ... in that order.  Every rank's buffers are as
+ * long as the longest rank's (in: max_s sum_d counts[s][d] chunks, out:
+ * max_d sum_s counts[s][d]); the tail of a shorter output is not written.
+ * One copy per non-empty pair, issued in shift order (d = s + k) so that
+ * each round of the program touches distinct links.  flags: CCL_FLAG_NOFUSE.
+ * Errors: CCL_ERR_INVALID_ARG (nranks out of range, a negative count, no
+ * chunk to move, a per-rank total above 2^30 chunks).
+ */
+ccl_status_t ccl_schedule_alltoallv(int32_t nranks, const int32_t* counts, uint32_t flags,
+                                    ccl_schedule_t* out);
+
 ccl_status_t ccl_schedule_info(ccl_schedule_t s, ccl_schedule_info_t* info);
 
 /* Copy the source program (ops) or the fused instructions into caller
@@ -171,7 +188,7 @@ void ccl_schedule_destroy(ccl_schedule_t s);
 
 /* Scheduling policies for ccl_plan_opts_t. */
 typedef enum { CCL_SCHED_RR = 0, CCL_SCHED_HPDS = 1 } ccl_scheduler_t;
-typedef enum { CCL_TB_CONNECTION = 0, CCL_TB_PACKED = 1 } ccl_tb_alloc_t;
+typedef enum { CCL_TB_CONNECTION = 0, CCL_TB_PACKED = 1, CCL_TB_BALANCED = 2 } ccl_tb_alloc_t;
 typedef enum { CCL_MB_AUTO = 0, CCL_MB_ALGO = 1, CCL_MB_TASK = 2, CCL_MB_SEGMENT = 3 } ccl_mb_order_t;
 typedef enum { CCL_LINK_FIFO = 0, CCL_LINK_DIRECT = 1 } ccl_link_mode_t;
 typedef enum { CCL_PROTO_SIMPLE = 0, CCL_PROTO_LL = 1 } ccl_protocol_t;
@@ -194,8 +211,14 @@ typedef enum { CCL_PROTO_SIMPLE = 0, CCL_PROTO_LL = 1 } ccl_protocol_t;
  *   scheduler   : CCL_SCHED_RR (program-order list scheduling) or
  *                 CCL_SCHED_HPDS (ReSCCL report, §II.2).
  *   tb_alloc    : CCL_TB_CONNECTION (one threadblock per (in-link, out-link)
- *                 connection) or CCL_TB_PACKED (connections never active in
- *                 the same sub-pipeline share a threadblock).
+ *                 connection), CCL_TB_PACKED (connections never active in
+ *                 the same sub-pipeline share a threadblock), or
+ *                 CCL_TB_BALANCED (packed, then the threadblocks of a rank
+ *                 that run only link-free instructions -- local copies and
+ *                 direct copies, which need no FIFO -- are merged into at most
+ *                 max(1, tb_budget / (nranks x channels)) threadblocks by
+ *                 largest-first bin packing on their bytes; for AllToAll-like
+ *                 programs with many small pairs).
  *   mb_order    : order of micro-batches inside a threadblock program.  A
  *                 program is cut into segments run one after the other; a
  *                 segment runs micro-batch-major (each micro-batch through all
@@ -263,7 +286,7 @@ typedef struct {
     int32_t channel_scaling;
     int32_t mb_window;
     int32_t protocol;
-    int32_t pad;
+    int32_t tb_budget;   /* CCL_TB_BALANCED: threadblocks to aim for (0: 256) */
 } ccl_plan_opts_t;
 
 void ccl_plan_opts_default(ccl_plan_opts_t* o);

@@ -30,6 +30,10 @@ Readings (the pages name these algorithms but do not spell them out):
   through local rank j of the source group and local rank j of the
   destination group, so that every link of the two groups carries a share.
   No wrap-around unless ``wrap`` is set.
+* uneven AllToAll (per-pair sizes, the token exchange of a mixture-of-
+  experts layer; a variant of the AllToAll of the MSCCLang report, §IV.3):
+  rank s lays out its blocks by destination, rank d receives them ordered by
+  source; every pair is one direct copy.
 """
 from __future__ import annotations
 
@@ -178,6 +182,27 @@ def alltonext(G: int, ng: int, wrap: bool = False):
             for a, b in zip(stops[:-1], stops[1:]):
                 ops.append((COPY, a[0], a[1], a[2], b[0], b[1], b[2], 1))
     return _arr(ops), (G, G, 2)
+
+
+def alltoallv(counts):
+    """``counts[s][d]`` chunks from rank s to rank d.  Input of s: blocks for
+    d = 0, 1, ... back to back; output of d: blocks from s = 0, 1, ... back
+    to back; buffers as long as the longest rank's."""
+    c = np.asarray(counts, dtype=np.int64)
+    R = c.shape[0]
+    ops = []
+    # source-major program order (any order gives the same result: every
+    # pair writes its own output range and reads only inputs)
+    for s in range(R):
+        for d in range(R):
+            if c[s, d] == 0:
+                continue
+            src_off = int(c[s, :d].sum())
+            dst_off = int(c[:s, d].sum())
+            ops.append((COPY, s, IN, src_off, d, OUT, dst_off, int(c[s, d])))
+    nin = int(c.sum(axis=1).max())
+    nout = int(c.sum(axis=0).max())
+    return _arr(ops), (nin, nout, 0)
 
 
 BUILTINS = {

@@ -399,3 +399,24 @@ def test_coordinate_descent_visits_both_protocols():
     assert seen == {ccl.PROTO_SIMPLE, ccl.PROTO_LL}
     assert best.protocol == ccl.PROTO_LL and bw == pytest.approx(2.0)
     assert (best.channels, best.nthreads, best.slot_bytes) == (4, 256, 1 << 16)
+
+
+def test_balanced_allocation_merges_link_free_threadblocks():
+    """Direct copies need no FIFO: a rank's copy threadblocks are binned into
+    at most budget / (ranks x channels) threadblocks; bytes and steps keep."""
+    counts = datagen.alltoallv_counts(3, 32, 512)
+    s = ccl.Schedule.alltoallv(counts)
+    kw = dict(link_mode=ccl.LINK_DIRECT, channels=4, channel_scaling=0)
+    packed = s.check(1024, BF16, tb_alloc=ccl.TB_PACKED, **kw)
+    bal = s.check(1024, BF16, tb_alloc=ccl.TB_BALANCED, tb_budget=256, **kw)
+    assert packed.nthreadblocks > 900
+    assert bal.nthreadblocks == 256          # 2 per rank x 4 channels x 32 ranks
+    assert (bal.schedule_bytes, bal.nsteps) == (packed.schedule_bytes, packed.nsteps)
+    assert s.check(1024, BF16, tb_alloc=ccl.TB_BALANCED, tb_budget=512, **kw).nthreadblocks == 512
+    # threadblocks with FIFO links are left as packed
+    h = ccl.Schedule.builtin(ccl.HIER_ALLREDUCE, 16, 8)
+    a = h.check(65536, F32, tb_alloc=ccl.TB_PACKED, microbatches=4)
+    b = h.check(65536, F32, tb_alloc=ccl.TB_BALANCED, microbatches=4, tb_budget=16)
+    assert a.nthreadblocks == b.nthreadblocks
+    with pytest.raises(ccl.CclError):
+        s.check(1024, BF16, tb_alloc=3)

@@ -170,3 +170,54 @@ def test_ll_protocol_repeated_executions_and_windows(ccl):
         plan.status()
         want, _, _ = oracle.run(ops, 16, nch, 4096, F32, ins)
         assert_bitexact(to_host(d_out, F32), want)
+
+
+@pytest.mark.parametrize("R,tokens,seed", [(4, 64, 1), (8, 96, 2), (32, 48, 3)])
+@pytest.mark.parametrize("dtype", [F32, BF16, I32])
+@pytest.mark.parametrize("link_mode", [0, 1])
+def test_alltoallv_bitexact(ccl, R, tokens, seed, dtype, link_mode):
+    """Skewed token routing (one chunk = one token's vector); outputs shorter
+    than the longest keep their untouched tail."""
+    import torch
+    import datagen
+    import oracle
+    from oracle import schedules as OS
+    from gpu_helpers import to_device, empty_outputs, to_host
+    counts = datagen.alltoallv_counts(seed, R, tokens)
+    ce = 96 if dtype == BF16 else 80
+    s = ccl.Schedule.alltoallv(counts)
+    plan = ccl.Plan(s, ce, dtype, channels=2, link_mode=link_mode, tb_alloc=1)
+    ops, nch = OS.alltoallv(counts)
+    ins = datagen.rank_inputs(seed, DIST[dtype], R, nch[0] * ce, dtype)
+    d_out = empty_outputs(R, nch[1] * ce, dtype)
+    plan.execute(to_device(ins, dtype), d_out)
+    torch.cuda.synchronize()
+    plan.status()
+    want, _, _ = oracle.run(ops, R, nch, ce, dtype, ins)
+    assert_bitexact(to_host(d_out, dtype), want)
+
+
+@pytest.mark.parametrize("budget", [64, 256])
+def test_balanced_allocation_bitexact(ccl, budget):
+    """Link-free threadblocks merged by bin packing: uneven and two-phase
+    AllToAll, AllToNext with unfused direct relays."""
+    import torch
+    import datagen
+    import oracle
+    from oracle import schedules as OS
+    from gpu_helpers import to_device, empty_outputs, to_host
+    counts = datagen.alltoallv_counts(4, 16, 64)
+    s = ccl.Schedule.alltoallv(counts)
+    plan = ccl.Plan(s, 128, BF16, channels=4, link_mode=1, tb_alloc=2, tb_budget=budget, channel_scaling=1)
+    ops, nch = OS.alltoallv(counts)
+    ins = datagen.rank_inputs(4, "normal", 16, nch[0] * 128, BF16)
+    d_out = empty_outputs(16, nch[1] * 128, BF16)
+    plan.execute(to_device(ins, BF16), d_out)
+    torch.cuda.synchronize()
+    plan.status()
+    want, _, _ = oracle.run(ops, 16, nch, 128, BF16, ins)
+    assert_bitexact(to_host(d_out, BF16), want)
+    for kind, R, G, fuse in [(4, 32, 8, True), (5, 24, 8, False), (4, 8, 4, True)]:
+        got, want, _ = run_case(ccl, kind, R, G, 1000, F32, "normal", 6, fuse=fuse, link_mode=1, tb_alloc=2,
+                                tb_budget=budget, channels=2, microbatches=4)
+        assert_bitexact(got, want)
