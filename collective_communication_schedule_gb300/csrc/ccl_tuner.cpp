@@ -1,8 +1,9 @@
 // Tuner: subspace coordinate descent over the resource parameters.
 //
 // AutoCCL report, "research method" 1-2: implementation parameters (here:
-// the threadblock allocation policy and the FIFO protocol) split the search
-// space into small subspaces; inside each, the resource parameters nChannel, nThread and
+// the threadblock allocation policy -- one per connection, or packed and
+// balanced -- and the FIFO protocol) split the search space into small
+// subspaces; inside each, the resource parameters nChannel, nThread and
 // chunk size are optimised one coordinate at a time, raising a parameter
 // while bandwidth keeps improving (bandwidth is unimodal in each of them).
 // Grids: channels {1,2,4,8,12,16,24,32,48}, threads {128,256,512,1024},
@@ -148,7 +149,9 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
     double overall_bw = measure(base);
     for (int sub = 0; sub < 4; ++sub) {
         ccl_plan_opts_t cur = base;
-        cur.tb_alloc = sub & 1 ? CCL_TB_PACKED : CCL_TB_CONNECTION;
+        // balanced = packed plus merged link-free threadblocks (the same as
+        // packed when every threadblock has a FIFO link)
+        cur.tb_alloc = sub & 1 ? CCL_TB_BALANCED : CCL_TB_CONNECTION;
         cur.protocol = sub & 2 ? CCL_PROTO_LL : CCL_PROTO_SIMPLE;
         int ic = nearest(gc, cur.channels), it = nearest(gt, cur.nthreads), is = nearest(gs, cur.slot_bytes);
         auto eval = [&](int c, int t, int sl) {
