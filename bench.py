@@ -161,6 +161,26 @@ def schedule_and_opts(ccl, kind, R, G, opts):
     return ccl.Schedule.builtin(kind, R, G, 0 if fuse else ccl.FLAG_NOFUSE), opts
 
 
+def combine_replicas(res, world, device=None):
+    """Whole-job line of N replicas: step times are the maximum over ranks
+    (device and end-to-end), values count the bytes of every replica."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([res["ms_per_step"], res["e2e"]["ms_per_step"]], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms, e2e_ms = float(t[0].item()), float(t[1].item())
+    out = dict(res)
+    sb = res["config"]["schedule_bytes_per_step"]
+    out["ms_per_step"] = round(ms, 4)
+    out["value"] = round(sb * world / (ms * 1e6), 1)
+    out["n_gpus"] = world
+    out["e2e"] = dict(res["e2e"], ms_per_step=round(e2e_ms, 3), value=round(sb * world / (e2e_ms * 1e6), 1),
+                      h2d_bytes_per_step=res["e2e"]["h2d_bytes_per_step"] * world,
+                      d2h_bytes_per_step=res["e2e"]["d2h_bytes_per_step"] * world)
+    out["gpu_launches"] = res["gpu_launches"] * world
+    return out
+
+
 def barrier():
     """Barrier across replicas (no-op on one GPU)."""
     import torch.distributed as dist
@@ -656,13 +676,8 @@ def main():
         local = int(os.environ.get("LOCAL_RANK", "0"))
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
-        res = run_gpu(args)
-        t = torch.tensor([res["ms_per_step"]], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        res = combine_replicas(run_gpu(args), world, device="cuda")
         if rank == 0:
-            res["ms_per_step"] = float(t.item())
-            res["value"] = round(res["config"]["schedule_bytes_per_step"] * world / (t.item() * 1e6), 1)
-            res["n_gpus"] = world
             print(json.dumps(res))
         dist.destroy_process_group()
         return

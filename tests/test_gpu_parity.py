@@ -221,3 +221,32 @@ def test_balanced_allocation_bitexact(ccl, budget):
         got, want, _ = run_case(ccl, kind, R, G, 1000, F32, "normal", 6, fuse=fuse, link_mode=1, tb_alloc=2,
                                 tb_budget=budget, channels=2, microbatches=4)
         assert_bitexact(got, want)
+
+
+@pytest.mark.parametrize("kind,R,G", [(0, 1, 0), (0, 2, 0), (1, 1, 0), (1, 2, 0), (2, 1, 0), (2, 2, 0),
+                                      (3, 2, 1), (4, 2, 1), (5, 2, 1), (5, 2, 2)])
+@pytest.mark.parametrize("dtype", [F32, BF16])
+def test_trivial_rank_counts(ccl, kind, R, G, dtype):
+    got, want, _ = run_case(ccl, kind, R, G, 777, dtype, DIST[dtype], 13)
+    assert_bitexact(got, want)
+
+
+@pytest.mark.parametrize("dtype", [F32, BF16, F16])
+def test_two_rank_allreduce_equals_torch_add(ccl, dtype):
+    """R = 2: every output element is one rounded addition, so the result is
+    torch's own elementwise add of the two inputs, bit for bit."""
+    import torch
+    import datagen
+    from gpu_helpers import to_device, empty_outputs
+    tdt = {F32: torch.float32, BF16: torch.bfloat16, F16: torch.float16}[dtype]
+    ce = 4096
+    ins = datagen.rank_inputs(21, DIST[dtype], 2, 2 * ce, dtype)
+    d_in = to_device(ins, dtype)
+    d_out = empty_outputs(2, 2 * ce, dtype)
+    plan = ccl.Plan(ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 2), ce, dtype, channels=2)
+    plan.execute(d_in, d_out)
+    torch.cuda.synchronize()
+    plan.status()
+    ref = (d_in[0].view(tdt) + d_in[1].view(tdt)).view(d_in[0].dtype)
+    for r in range(2):
+        assert torch.equal(d_out[r], ref), f"rank {r}"
