@@ -295,29 +295,31 @@ def run_gpu(args):
 
     # end to end through the C ABI with host buffers (H2D + execute + D2H per
     # collective).  The collectives of a step are independent, so they
-    # alternate over two streams: one collective's output copies overlap the
-    # next one's input copies (host<->device copies run in both directions
-    # at once).
+    # rotate over a few streams (each plan always on the same one): input
+    # copies of the next collectives overlap the output copies of earlier
+    # ones (host<->device copies run in both directions at once).
     Ke = max(1, min(K, args.e2e_steps))
     h2d = sum(it["plan"].in_elems * ESIZE[it["dt"]] * it["R"] for it in items)
     d2h = sum(it["plan"].out_elems * ESIZE[it["dt"]] * it["R"] for it in items)
-    e2e_streams = [stream, torch.cuda.Stream()]
+    e2e_streams = [stream] + [torch.cuda.Stream() for _ in range(max(1, args.e2e_streams) - 1)]
 
     def e2e_pass():
         for j, it in enumerate(items):
-            s = e2e_streams[j % 2]
+            s = e2e_streams[j % len(e2e_streams)]
             it["plan"].execute_host(it["h_in"], it["h_out"], it["d_in"], it["d_out"], s)
 
     e2e_pass()   # warm
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    e2e_streams[1].wait_event(e0)
+    for s in e2e_streams[1:]:
+        s.wait_event(e0)
     for _ in range(Ke):
         e2e_pass()
-    joined = torch.cuda.Event()
-    joined.record(e2e_streams[1])
-    stream.wait_event(joined)
+    for s in e2e_streams[1:]:
+        joined = torch.cuda.Event()
+        joined.record(s)
+        stream.wait_event(joined)
     e1.record(stream)
     torch.cuda.synchronize()
     for it in items:
@@ -351,7 +353,8 @@ def run_gpu(args):
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},
         "e2e": {"value": round(sched_bytes / (e2e_ms * 1e6), 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3), "steps": Ke},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3), "steps": Ke,
+                "streams": len(e2e_streams)},
         "gpu_launches": K * len(items),
         "clocks": clk,
         "per_collective": per,
@@ -643,6 +646,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-streams", type=int, default=2,
+                    help="streams the end-to-end leg rotates over (2 measured best: 477 GB/s vs 389 with 4)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma-separated subset of the suite (profiling)")
