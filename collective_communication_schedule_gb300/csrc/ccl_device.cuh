@@ -316,7 +316,6 @@ __device__ __forceinline__ void bulk_wait(int n)
 // order generic-proxy and async-proxy accesses (global memory / this CTA's
 // shared memory)
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // test of the phase with the given parity that may suspend the thread for a
 // short, hardware-chosen time while the phase is incomplete (acquire at CTA
