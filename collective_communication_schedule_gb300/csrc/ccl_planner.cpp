@@ -909,12 +909,14 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
 
     // micro-batch candidates
     int64_t max_slots = 1;
+    int64_t max_per_ch = 0;   // elements of the largest linked channel range
     const std::vector<int> pcs = channel_counts(s, o.channels, o.channel_scaling);
     for (size_t i = 0; i < s.instrs.size(); ++i) {
         const Instr& I = s.instrs[i];
         if (I.xfer_in < 0 && I.xfer_out < 0) continue;
         int64_t n = I.count * ce;
         int64_t per_ch = (n + pcs[i] - 1) / pcs[i];
+        max_per_ch = std::max(max_per_ch, per_ch);
         max_slots = std::max<int64_t>(max_slots, (per_ch * es + o.slot_bytes - 1) / o.slot_bytes);
     }
     int64_t half = std::max(1, o.fifo_slots / 2);
@@ -941,8 +943,12 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
             else {
                 // double buffering: a window's slots and the next window's
                 // fit in the FIFO together, so neighbours do not run in
-                // lockstep
-                const int w = std::max(1, std::min(m, o.fifo_slots / 2));
+                // lockstep (a piece takes ceil(per-channel range / m) bytes
+                // in slots)
+                const int64_t piece_slots =
+                    std::max<int64_t>(1, (max_per_ch + m - 1) / m * es / o.slot_bytes +
+                                             ((max_per_ch + m - 1) / m * es % o.slot_bytes ? 1 : 0));
+                const int w = (int)std::max<int64_t>(1, std::min<int64_t>(m, o.fifo_slots / (2 * piece_slots)));
                 wins.push_back(w);
                 if (w > 1) wins.push_back(1);
             }

@@ -236,9 +236,9 @@ typedef enum { CCL_PROTO_SIMPLE = 0, CCL_PROTO_LL = 1 } ccl_protocol_t;
  *                 pieces ahead of it in its own threadblock while the piece
  *                 it depends on is still in flight upstream.  1 = one
  *                 micro-batch at a time through the whole segment; 0 =
- *                 auto: min(m, fifo_slots / 2) first (a window and the next
- *                 one fit in the FIFO together), then 1, keeping the first
- *                 that can finish.
+ *                 auto: min(m, fifo_slots / (2 x slots per piece)) first (a
+ *                 window and the next one fit in the FIFO together), then 1,
+ *                 keeping the first that can finish.
  *   protocol    : FIFO signalling (AutoCCL report: implementation parameter
  *                 "protocol"; MSCCLang report §III.1 runtime protocols).
  *                 CCL_PROTO_SIMPLE: a slot is published by a flag after its

@@ -353,10 +353,16 @@ def test_microbatch_window_is_used_when_the_fifo_holds_it():
     s = ccl.Schedule.builtin(ccl.HIER_ALLREDUCE, 16, 8)
     kw = dict(channels=2, microbatches=8, tb_alloc=ccl.TB_PACKED, slot_bytes=65536, mb_order=ccl.MB_ALGO)
     assert s.check(65536, F32, fifo_slots=4, mb_window=1, **kw).mb_window == 1
-    # auto: min(m, fifo_slots / 2)
+    # auto: min(m, fifo_slots / (2 x slots per piece)); here a piece is one
+    # slot (65536 elements / 2 channels / 8 micro-batches x 4 bytes = 16 KiB)
     assert s.check(65536, F32, fifo_slots=4, mb_window=0, **kw).mb_window == 2
     assert s.check(65536, F32, fifo_slots=9, mb_window=0, **kw).mb_window == 4
     assert s.check(65536, F32, fifo_slots=32, mb_window=0, **kw).mb_window == 8
+    # pieces of two slots: five slots hold no double-buffered window of 2
+    r = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 8)
+    big = dict(channels=24, microbatches=6, slot_bytes=131072, mb_order=ccl.MB_ALGO)
+    assert r.check(32 << 20 >> 2, F32, fifo_slots=5, mb_window=0, **big).mb_window == 1
+    assert r.check(32 << 20 >> 2, F32, fifo_slots=8, mb_window=0, **big).mb_window == 2
     # same steps and bytes in another order
     a = s.check(65536, F32, fifo_slots=9, mb_window=1, **kw)
     b = s.check(65536, F32, fifo_slots=9, mb_window=8, **kw)
