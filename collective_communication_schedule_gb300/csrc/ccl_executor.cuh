@@ -1,13 +1,14 @@
-// Persistent executor kernel: one CTA per threadblock program.
+// Kernel parameters of the persistent executor: one CTA per threadblock
+// program, every rank's buffers and every link FIFO in this GPU's memory.
 //
-// Each CTA walks its list of (instruction, micro-batch) steps.  For every
-// FIFO slot of a step, thread 0 waits (bounded) until the incoming slot is
-// full and the outgoing slot is free, the CTA moves the slot's data with
-// 16-byte vector loads and stores (several in flight per thread), and thread
-// 0 posts the consumed / full flags with gpu-scope release semantics.  The
-// flag protocol stands in for the inter-GPU links of the pages' runtimes
-// (MSCCLang report, §III.1 runtime; ReSCCL report, §II.2 kernel generation):
-// every rank's buffers and every link FIFO live in this GPU's HBM.
+// Each CTA walks its list of (instruction, micro-batch) steps with four
+// roles (issuer, releaser, bulk-copy thread, data warps; see
+// ccl_runtime.cu).  Per FIFO slot the issuer waits (bounded) until the
+// incoming slot is full and the outgoing slot is free, the data path moves
+// the slot's data with 16-byte accesses, and the releaser posts the
+// consumed / full flags after a gpu-scope release fence.  The flag protocol
+// stands in for the inter-GPU links of the pages' runtimes (MSCCLang
+// report, §III.1 runtime; ReSCCL report, §II.2 kernel generation).
 #pragma once
 
 #include <cuda_bf16.h>

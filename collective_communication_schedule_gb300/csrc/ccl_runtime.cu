@@ -45,13 +45,17 @@ namespace ccl {
 // ----------------------------------------------------------------------
 // Warp-specialised executor.  Four roles per CTA:
 //
-//  * issuer (warp 0, lane 0) walks the threadblock program.  Per FIFO slot
-//    it waits (bounded) for the step's dependency counters, for the incoming
-//    slot to be full and the outgoing slot to be free -- both flags polled
-//    with relaxed loads in one round trip, then one acquire fence -- and
-//    hands the slot out as tiles of at most `tile` bytes through a ring of
-//    kQ shared-memory descriptors guarded by mbarriers ("ready").  The next
-//    step's 128-byte record is prefetched with cp.async.
+//  * issuer (warp 0, lane 0) walks the threadblock program.  Step records
+//    (128 bytes each) arrive by cp.async in batches of kLook, one batch
+//    ahead.  It waits (bounded) for a step's dependency counters and for the
+//    first slot of up to kLook coming steps -- incoming slot full, outgoing
+//    slot free -- polling all those flags with relaxed loads in one round
+//    trip, then one acquire fence; later slots of a step are polled kBatch
+//    at a time.  A step that follows an earlier step of its own threadblock
+//    waits only for that step's last tile.  Slots are handed out as tiles
+//    of at most `tile` bytes through a ring of kQ shared-memory descriptors
+//    guarded by mbarriers ("ready").  Slot indices are computed in 32 bits
+//    from residues the plan precomputes (no 64-bit division on one thread).
 //  * TMA thread (warp 2, lane 0) moves every 16-byte-aligned *copy* tile
 //    with bulk copies: global -> shared stage (mbarrier complete_tx), then
 //    shared -> global to the destination and/or the outgoing slot (bulk
@@ -59,7 +63,9 @@ namespace ccl {
 //    stores have read it, and a tile counts as done once its stores are
 //    complete.
 //  * data warps (warps 3..) move the other tiles (every reduce, and copies
-//    that are not 16-byte aligned) with 16-byte / element loads and stores.
+//    that are not 16-byte aligned) with 16-byte / element loads and stores;
+//    in the LL instantiation they also poll incoming LL lines and write
+//    outgoing lines with the slot's flag.
 //  * releaser (warp 1, lane 0) takes finished tiles in order, issues one
 //    release fence per batch and posts the flags and counters carried by a
 //    slot's last tile with relaxed stores, then frees the descriptor.
