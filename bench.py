@@ -301,12 +301,23 @@ def run_gpu(args):
     Ke = max(1, min(K, args.e2e_steps))
     h2d = sum(it["plan"].in_elems * ESIZE[it["dt"]] * it["R"] for it in items)
     d2h = sum(it["plan"].out_elems * ESIZE[it["dt"]] * it["R"] for it in items)
-    e2e_streams = [stream] + [torch.cuda.Stream() for _ in range(max(1, args.e2e_streams) - 1)]
+    if args.e2e_mode == "pipeline":
+        # ccl_execute_host_async: every input copy on one stream, every
+        # kernel on the launching stream, every output copy on a third, so
+        # the copy engines of both directions stay busy across collectives
+        e2e_streams = [stream, torch.cuda.Stream(), torch.cuda.Stream()]
 
-    def e2e_pass():
-        for j, it in enumerate(items):
-            s = e2e_streams[j % len(e2e_streams)]
-            it["plan"].execute_host(it["h_in"], it["h_out"], it["d_in"], it["d_out"], s)
+        def e2e_pass():
+            for it in items:
+                it["plan"].execute_host_async(it["h_in"], it["h_out"], it["d_in"], it["d_out"], e2e_streams[1],
+                                              stream, e2e_streams[2])
+    else:
+        e2e_streams = [stream] + [torch.cuda.Stream() for _ in range(max(1, args.e2e_streams) - 1)]
+
+        def e2e_pass():
+            for j, it in enumerate(items):
+                s = e2e_streams[j % len(e2e_streams)]
+                it["plan"].execute_host(it["h_in"], it["h_out"], it["d_in"], it["d_out"], s)
 
     e2e_pass()   # warm
     torch.cuda.synchronize()
@@ -354,7 +365,7 @@ def run_gpu(args):
                      else "fallback 6.8 TB/s"},
         "e2e": {"value": round(sched_bytes / (e2e_ms * 1e6), 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3), "steps": Ke,
-                "streams": len(e2e_streams)},
+                "mode": args.e2e_mode, "streams": len(e2e_streams)},
         "gpu_launches": K * len(items),
         "clocks": clk,
         "per_collective": per,
@@ -646,6 +657,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-mode", default="pipeline", choices=["pipeline", "streams"],
+                    help="pipeline: ccl_execute_host_async over copy-in / compute / copy-out streams; "
+                         "streams: ccl_execute_host rotating over --e2e-streams")
     ap.add_argument("--e2e-streams", type=int, default=2,
                     help="streams the end-to-end leg rotates over (2 measured best: 477 GB/s vs 389 with 4)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)

@@ -121,6 +121,8 @@ def _load():
         "ccl_plan_create": [P, I64_, I32_, I32_, ctypes.POINTER(PlanOpts), ctypes.POINTER(P)],
         "ccl_execute": [P, ctypes.POINTER(P), ctypes.POINTER(P), P],
         "ccl_execute_host": [P, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P), P],
+        "ccl_execute_host_async": [P, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P), P, P,
+                                   P],
         "ccl_plan_status": [P],
         "ccl_plan_stats": [P, ctypes.POINTER(PlanStats)],
         "ccl_plan_timeline": [P, ctypes.POINTER(ctypes.c_double), I32_, ctypes.POINTER(ctypes.c_double),
@@ -290,6 +292,14 @@ class Plan:
 
     def execute(self, inputs, outputs, stream=None):
         _check(lib.ccl_execute(self._h, _ptrs(inputs), _ptrs(outputs), _stream(stream)))
+
+    def execute_host_async(self, host_in, host_out, dev_in, dev_out, copy_in_stream, compute_stream,
+                           copy_out_stream):
+        """Input copies, kernel and output copies on three streams
+        (``ccl_execute_host_async``)."""
+        _check(lib.ccl_execute_host_async(self._h, _ptrs(host_in), _ptrs(host_out), _ptrs(dev_in), _ptrs(dev_out),
+                                          _stream(copy_in_stream), _stream(compute_stream),
+                                          _stream(copy_out_stream)))
 
     def execute_host(self, host_in, host_out, dev_in, dev_out, stream=None):
         _check(lib.ccl_execute_host(self._h, _ptrs(host_in), _ptrs(host_out), _ptrs(dev_in), _ptrs(dev_out),

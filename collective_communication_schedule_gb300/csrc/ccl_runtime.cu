@@ -860,6 +860,10 @@ struct ccl_plan {
     int64_t device_bytes = 0;
     double compile_ms = 0;
     ccl::KParams kp{};
+    // overlapped host round trip: input copies done, kernel done, output
+    // copies done (created on first use)
+    cudaEvent_t ev_in = nullptr, ev_k = nullptr, ev_out = nullptr;
+    bool pipe_started = false;
 };
 
 namespace {
@@ -931,6 +935,8 @@ void free_plan(ccl_plan* p)
     cudaFree(p->d_status);
     cudaFree(p->d_timeline);
     for (int r = 0; r < CCL_MAX_RANKS; ++r) cudaFree(p->d_scratch[r]);
+    for (cudaEvent_t e : {p->ev_in, p->ev_k, p->ev_out})
+        if (e) cudaEventDestroy(e);
     cudaSetDevice(prev);
     delete p;
 }
@@ -1265,6 +1271,36 @@ ccl_status_t ccl_execute_host(ccl_plan_t p, const void* const* host_in, void* co
     if (st != CCL_OK) return st;
     for (int r = 0; r < p->nranks; ++r)
         CUDA_TRY(cudaMemcpyAsync(host_out[r], dev_out[r], ob, cudaMemcpyDeviceToHost, s), "copy output to host");
+    return CCL_OK;
+}
+
+ccl_status_t ccl_execute_host_async(ccl_plan_t p, const void* const* host_in, void* const* host_out,
+                                    void* const* dev_in, void* const* dev_out, void* copy_in_stream,
+                                    void* compute_stream, void* copy_out_stream)
+{
+    if (!p || !host_in || !host_out || !dev_in || !dev_out) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
+    cudaStream_t si = static_cast<cudaStream_t>(copy_in_stream);
+    cudaStream_t sc = static_cast<cudaStream_t>(compute_stream);
+    cudaStream_t so = static_cast<cudaStream_t>(copy_out_stream);
+    for (cudaEvent_t* e : {&p->ev_in, &p->ev_k, &p->ev_out})
+        if (!*e) CUDA_TRY(cudaEventCreateWithFlags(e, cudaEventDisableTiming), "create pipeline event");
+    const size_t ib = (size_t)p->img.in_elems * p->img.esize, ob = (size_t)p->img.out_elems * p->img.esize;
+    // the previous call's kernel must be done reading the device inputs
+    if (p->pipe_started) CUDA_TRY(cudaStreamWaitEvent(si, p->ev_k, 0), "order input copies");
+    for (int r = 0; r < p->nranks; ++r)
+        CUDA_TRY(cudaMemcpyAsync(dev_in[r], host_in[r], ib, cudaMemcpyHostToDevice, si), "copy input to device");
+    CUDA_TRY(cudaEventRecord(p->ev_in, si), "record input copies");
+    CUDA_TRY(cudaStreamWaitEvent(sc, p->ev_in, 0), "order kernel after input copies");
+    // and the previous call's output copies done reading the device outputs
+    if (p->pipe_started) CUDA_TRY(cudaStreamWaitEvent(sc, p->ev_out, 0), "order kernel after output copies");
+    ccl_status_t st = ccl_execute(p, dev_in, dev_out, sc);
+    if (st != CCL_OK) return st;
+    CUDA_TRY(cudaEventRecord(p->ev_k, sc), "record kernel");
+    CUDA_TRY(cudaStreamWaitEvent(so, p->ev_k, 0), "order output copies");
+    for (int r = 0; r < p->nranks; ++r)
+        CUDA_TRY(cudaMemcpyAsync(host_out[r], dev_out[r], ob, cudaMemcpyDeviceToHost, so), "copy output to host");
+    CUDA_TRY(cudaEventRecord(p->ev_out, so), "record output copies");
+    p->pipe_started = true;
     return CCL_OK;
 }
 

@@ -325,6 +325,22 @@ ccl_status_t ccl_execute_host(ccl_plan_t p, const void* const* host_in, void* co
                               void* const* dev_in, void* const* dev_out, void* stream);
 
 /*
+ * End-to-end form over three streams, for pipelining several plans: the
+ * input copies go on copy_in_stream, the kernel on compute_stream after them,
+ * the output copies on copy_out_stream after the kernel (events owned by the
+ * plan, created on its first such call).  Host-to-device and device-to-host
+ * copies then overlap across plans that share the three streams.  A later
+ * call with the same plan orders its input copies after this call's kernel
+ * and its kernel after this call's output copies, so the plan's device
+ * buffers may be reused from call to call; mixing this call with
+ * ccl_execute on the same buffers needs the caller's own ordering.  The
+ * caller synchronizes copy_out_stream before reading host_out.
+ */
+ccl_status_t ccl_execute_host_async(ccl_plan_t p, const void* const* host_in, void* const* host_out,
+                                    void* const* dev_in, void* const* dev_out, void* copy_in_stream,
+                                    void* compute_stream, void* copy_out_stream);
+
+/*
  * Status of the last execution, to call after synchronizing its stream:
  * CCL_OK, or CCL_ERR_TIMEOUT when a flag wait ran out (the detail names the
  * threadblock and step).  After a timeout the plan's flags are reset so the

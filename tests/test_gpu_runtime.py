@@ -136,3 +136,38 @@ def test_plan_steps_match_the_timeline(ccl):
         assert all(st["tb"] == b for st in steps[tb[b]:tb[b + 1]])
     assert np.all(stamps[:, 4] >= stamps[:, 0])
     assert all(st["nelem"] >= 0 and st["kind"] in range(len(ccl.KIND_NAMES)) for st in steps)
+
+
+def test_execute_host_async_pipelines_two_plans_and_reuses_buffers(ccl):
+    """Two plans share copy-in / compute / copy-out streams; each runs twice
+    on the same device buffers with new host inputs (the plan's events order
+    the second round after the first)."""
+    import torch
+    import datagen
+    import oracle
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    s_comp = torch.cuda.current_stream()
+    cases = []
+    for kind, R, G, dt, ce in [(0, 8, 0, F32, 8192), (4, 8, 4, F16, 4096)]:
+        plan = ccl.Plan(ccl.Schedule.builtin(kind, R, G), ce, dt, channels=2)
+        tdt = torch.float32 if dt == F32 else torch.int16
+        d_in = [torch.empty(plan.in_elems, dtype=tdt, device="cuda") for _ in range(R)]
+        d_out = [torch.empty(plan.out_elems, dtype=tdt, device="cuda") for _ in range(R)]
+        cases.append((kind, R, G, dt, ce, plan, tdt, d_in, d_out))
+    for rnd in range(2):
+        results = []
+        for kind, R, G, dt, ce, plan, tdt, d_in, d_out in cases:
+            host = datagen.rank_inputs(40 + rnd, "uniform", R, plan.in_elems, dt)
+            h_in = [torch.from_numpy(a.view(np.int16) if dt != F32 else a).pin_memory() for a in host]
+            h_out = [torch.empty(plan.out_elems, dtype=tdt).pin_memory() for _ in range(R)]
+            plan.execute_host_async(h_in, h_out, d_in, d_out, s_in, s_comp, s_out)
+            # the pinned host tensors must outlive the copies torch cannot see
+            results.append((kind, R, G, dt, ce, plan, host, h_out, h_in))
+        s_out.synchronize()
+        torch.cuda.synchronize()
+        for kind, R, G, dt, ce, plan, host, h_out, _ in results:
+            plan.status()
+            ops, nch = oracle_program(kind, R, G)
+            want, _, _ = oracle.run(ops, R, nch, ce, dt, host)
+            got = [t.numpy().view(np.uint16) if dt != F32 else t.numpy() for t in h_out]
+            assert_bitexact(got, want)
