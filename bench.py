@@ -225,7 +225,7 @@ def build_suite(ccl, torch, datagen, args, with_host=False):
                 h_in.append(t.pin_memory())
                 h_out.append(torch.empty(nout, dtype=tdt).pin_memory())
         items.append(dict(name=name, kind=kind, R=R, G=G, dt=dt, ce=ce, plan=plan, stats=st, d_in=d_in,
-                          d_out=d_out, h_in=h_in, h_out=h_out, dist=dist, seed=seed))
+                          d_out=d_out, h_in=h_in, h_out=h_out, dist=dist, seed=seed, opts=opts))
     return items
 
 
@@ -285,9 +285,40 @@ def run_gpu(args):
             "schedule_gbs": round(gbs, 1), "min_bytes_gbs": round(st.min_bytes / (mean_ms * 1e6), 1),
             "frac_of_peak": round(gbs / peak, 3), "min_bytes_frac": round(st.min_bytes / (mean_ms * 1e6) / peak, 3),
             "algbw_gbs": round(algbw, 1), "busbw_gbs": round(algbw * st.busbw_factor, 1),
-            "threadblocks": st.nthreadblocks, "channels": st.channels, "microbatches": st.microbatches,
+            "frac_of_nominal_8tbs": round(gbs / 8000.0, 3),
+            "threadblocks": st.nthreadblocks, "threadblocks_connection": st.nthreadblocks_connection,
+            "channels": st.channels, "microbatches": st.microbatches,
             "slot_bytes": st.slot_bytes, "nthreads": st.nthreads,
         })
+    # outside the timed region: threadblock idle fractions (instrumented
+    # plan) and, for collectives whose buffers fit in L2, the time with L2
+    # flushed before every execution (flush outside the events)
+    if not args.no_extras:
+        l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+        flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device="cuda")
+        for rec, it in zip(per, items):
+            sched, popts = schedule_and_opts(ccl, it["kind"], it["R"], it["G"], it["opts"])
+            inst = ccl.Plan(sched, it["ce"], it["dt"], instrument=1, **popts)
+            inst.execute(it["d_in"], it["d_out"], stream)
+            torch.cuda.synchronize()
+            inst.status()
+            tl = inst.timeline()
+            rec["mean_idle"], rec["max_idle"] = round(tl["mean_idle"], 3), round(tl["max_idle"], 3)
+            del inst
+            footprint = it["R"] * (it["plan"].in_elems + it["plan"].out_elems) * ESIZE[it["dt"]]
+            if footprint < l2:
+                ts = []
+                for _ in range(10):
+                    flush.zero_()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    it["plan"].execute(it["d_in"], it["d_out"], stream)
+                    b.record(stream)
+                    torch.cuda.synchronize()
+                    ts.append(a.elapsed_time(b))
+                it["plan"].status()
+                rec["l2_flushed_median_us"] = round(statistics.median(ts) * 1e3, 2)
+        del flush
     step_ms = total_ms / K
     value = sched_bytes / (step_ms * 1e6)
     avg_launch_ms = kern_ms_total / (K * len(items))
@@ -664,6 +695,7 @@ def main():
                     help="streams the end-to-end leg rotates over (2 measured best: 477 GB/s vs 389 with 4)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip idle fractions and L2-flushed timings")
     ap.add_argument("--only", default="", help="comma-separated subset of the suite (profiling)")
     ap.add_argument("--scale", type=float, default=1.0, help="chunk size factor (profiling)")
     ap.add_argument("--ablation", action="store_true", help="scheduler x threadblock allocation table")
