@@ -41,7 +41,7 @@ SUITE = [
     # parameters the workload fixes are kept (24 channels, 16 micro-batches,
     # 1 channel, <= 4 channels); the others are the best measured settings
     ("hier_ar", 3, 16, 8, 0, 4 * MiB, "normal", 2,
-     dict(channels=8, microbatches=16, tb_alloc=1, slot_bytes=65536, fifo_slots=8, mb_window=4)),
+     dict(channels=9, microbatches=16, tb_alloc=1, slot_bytes=65536, fifo_slots=8, mb_window=4)),
     ("a2a", 4, 32, 8, 2, 1 * MiB, "uniform", 3,
      dict(channels=8, link_mode=1, channel_scaling=0, tb_alloc=2, tb_budget=256)),
     ("ring_bf16", 0, 8, 0, 1, 32 * MiB, "normal", 4, dict(channels=24, slot_bytes=131072)),
