@@ -48,7 +48,7 @@ SUITE = [
     ("ring_f32", 0, 8, 0, 0, 32 * MiB, "normal", 4, dict(channels=24, slot_bytes=131072)),
     # relay hops as plain direct copies (no fusion into FIFO forwards)
     ("a2n", 5, 24, 8, 0, 16 * MiB, "normal", 4,
-     dict(fuse=False, channels=8, link_mode=1, microbatches=8, tb_alloc=1, channel_scaling=0)),
+     dict(fuse=False, channels=16, link_mode=1, microbatches=8, tb_alloc=2, tb_budget=304, channel_scaling=0)),
     ("ag_3m", 1, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4)),
     ("rs_3m", 2, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4)),
     ("ar_1m", 0, 8, 0, 0, 1 * MiB // 8, "uniform", 0, dict(channels=1)),

@@ -261,45 +261,53 @@ void pack_state_based(const ccl_schedule& s, const Timeline& tl, TBList* tbs, st
     }
 }
 
-// Balanced allocation: threadblocks of a rank that run only link-free
-// instructions (local copies, direct copies: no FIFO, so any number of them
-// may share a threadblock in program order) are merged into at most `cap`
-// threadblocks, largest first into the least loaded (bytes in chunk units).
+// Balanced allocation: threadblocks that run only link-free instructions
+// (local copies, direct copies: no FIFO, so any number of them may share a
+// threadblock) are merged into at most `cap` threadblocks, largest first into
+// the least loaded (bytes in chunk units).  A link-free instruction needs no
+// particular rank's threadblock, so the bins take threadblocks of every rank;
+// inside a bin instructions run by sub-pipeline (a dependent task always has
+// a later one), then program position.  The rank of a merged threadblock is
+// that of its largest part (reporting only).
 void balance_linkfree(const ccl_schedule& s, const Timeline& tl, TBList* tbs, std::vector<int>* tb_rank, int cap)
 {
-    struct B { int rank; std::vector<int> instrs; int64_t load; };
+    struct B { int rank; std::vector<int> instrs; int64_t load; int64_t top; };
     std::vector<B> out;
-    std::map<int, std::vector<int>> free_tbs;   // rank -> link-free threadblocks
+    std::vector<int> free_tbs;
     for (size_t t = 0; t < tbs->size(); ++t) {
         bool link_free = true;
         for (int i : (*tbs)[t]) link_free = link_free && s.instrs[i].xfer_in < 0 && s.instrs[i].xfer_out < 0;
-        if (link_free) free_tbs[(*tb_rank)[t]].push_back((int)t);
-        else out.push_back(B{(*tb_rank)[t], (*tbs)[t], 0});
+        if (link_free) free_tbs.push_back((int)t);
+        else out.push_back(B{(*tb_rank)[t], (*tbs)[t], 0, 0});
     }
-    for (auto& kv : free_tbs) {
-        std::vector<int>& v = kv.second;
-        if ((int)v.size() <= cap) {
-            for (int t : v) out.push_back(B{kv.first, (*tbs)[t], 0});
-            continue;
-        }
-        auto weight = [&](int t) {
-            int64_t w = 0;
-            for (int i : (*tbs)[t]) w += s.instrs[i].count;
-            return w;
-        };
-        std::stable_sort(v.begin(), v.end(), [&](int a, int b) { return weight(a) > weight(b); });
-        std::vector<B> bins(cap, B{kv.first, {}, 0});
-        for (int t : v) {
+    auto weight = [&](int t) {
+        int64_t w = 0;
+        for (int i : (*tbs)[t]) w += s.instrs[i].count;
+        return w;
+    };
+    if ((int)free_tbs.size() <= cap) {
+        for (int t : free_tbs) out.push_back(B{(*tb_rank)[t], (*tbs)[t], 0, 0});
+    } else {
+        std::stable_sort(free_tbs.begin(), free_tbs.end(), [&](int a, int b) { return weight(a) > weight(b); });
+        std::vector<B> bins(cap, B{-1, {}, 0, 0});
+        for (int t : free_tbs) {
             int k = 0;
             for (int b = 1; b < cap; ++b)
                 if (bins[b].load < bins[k].load) k = b;
+            const int64_t w = weight(t);
             bins[k].instrs.insert(bins[k].instrs.end(), (*tbs)[t].begin(), (*tbs)[t].end());
-            bins[k].load += weight(t);
+            bins[k].load += w;
+            if (w > bins[k].top) {
+                bins[k].top = w;
+                bins[k].rank = (*tb_rank)[t];
+            }
         }
         for (auto& b : bins) {
             std::sort(b.instrs.begin(), b.instrs.end(), [&](int a, int c) {
                 if (tl.sp_hi[a] != tl.sp_hi[c]) return tl.sp_hi[a] < tl.sp_hi[c];
-                return s.instrs[a].position < s.instrs[c].position;
+                if (s.instrs[a].position != s.instrs[c].position)
+                    return s.instrs[a].position < s.instrs[c].position;
+                return a < c;
             });
             out.push_back(std::move(b));
         }
@@ -904,7 +912,7 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
     if (o.tb_alloc == CCL_TB_PACKED || o.tb_alloc == CCL_TB_BALANCED) pack_state_based(s, tl, &packed, &packed_rank);
     if (o.tb_alloc == CCL_TB_BALANCED) {
         const int budget = o.tb_budget > 0 ? o.tb_budget : 256;
-        balance_linkfree(s, tl, &packed, &packed_rank, std::max(1, budget / std::max(1, s.nranks * o.channels)));
+        balance_linkfree(s, tl, &packed, &packed_rank, std::max(1, budget / std::max(1, o.channels)));
     }
 
     // micro-batch candidates

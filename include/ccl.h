@@ -213,12 +213,13 @@ typedef enum { CCL_PROTO_SIMPLE = 0, CCL_PROTO_LL = 1 } ccl_protocol_t;
  *   tb_alloc    : CCL_TB_CONNECTION (one threadblock per (in-link, out-link)
  *                 connection), CCL_TB_PACKED (connections never active in
  *                 the same sub-pipeline share a threadblock), or
- *                 CCL_TB_BALANCED (packed, then the threadblocks of a rank
- *                 that run only link-free instructions -- local copies and
- *                 direct copies, which need no FIFO -- are merged into at most
- *                 max(1, tb_budget / (nranks x channels)) threadblocks by
+ *                 CCL_TB_BALANCED (packed, then the threadblocks that run
+ *                 only link-free instructions -- local copies and direct
+ *                 copies, which need no FIFO and no particular rank's
+ *                 threadblock -- are merged into at most
+ *                 max(1, tb_budget / channels) threadblocks of any rank by
  *                 largest-first bin packing on their bytes; for AllToAll-like
- *                 programs with many small pairs).
+ *                 programs with many small or uneven pairs).
  *   mb_order    : order of micro-batches inside a threadblock program.  A
  *                 program is cut into segments run one after the other; a
  *                 segment runs micro-batch-major (each micro-batch through all
