@@ -49,7 +49,9 @@ SUITE = [
     # relay hops as plain direct copies (no fusion into FIFO forwards)
     ("a2n", 5, 24, 8, 0, 16 * MiB, "normal", 4,
      dict(fuse=False, channels=16, link_mode=1, microbatches=8, tb_alloc=2, tb_budget=304, channel_scaling=0)),
-    ("ag_3m", 1, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4)),
+    ("ag_3m", 1, 8, 0, 1, 3 * MiB // 8, "normal", 1,
+     # every hop a direct copy into the next rank's output (no FIFO)
+     dict(fuse=False, channels=4, link_mode=1)),
     ("rs_3m", 2, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4)),
     ("ar_1m", 0, 8, 0, 0, 1 * MiB // 8, "uniform", 0, dict(channels=1)),
 ]
