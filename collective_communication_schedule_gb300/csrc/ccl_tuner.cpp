@@ -2,8 +2,8 @@
 //
 // AutoCCL report, "research method" 1-2: implementation parameters (here:
 // the threadblock allocation policy -- one per connection, or packed and
-// balanced -- and the FIFO protocol) split the search space into small
-// subspaces; inside each, the resource parameters nChannel, nThread and
+// balanced --, the FIFO protocol and the transport) split the search space
+// into small subspaces; inside each, the resource parameters nChannel, nThread and
 // chunk size are optimised one coordinate at a time, raising a parameter
 // while bandwidth keeps improving (bandwidth is unimodal in each of them).
 // Grids: channels {1,2,4,8,12,16,24,32,48}, threads {128,256,512,1024},
@@ -32,11 +32,11 @@ struct Prober {
     cudaStream_t stream;
     int reps;
     int probes = 0;
-    std::map<std::tuple<int, int, int64_t, int, int>, double> cache;  // -> microseconds (0 = infeasible)
+    std::map<std::tuple<int, int, int64_t, int, int, int>, double> cache;  // -> microseconds (0 = infeasible)
 
     double time_us(const ccl_plan_opts_t& o)
     {
-        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol);
+        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol, o.link_mode);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
         ++probes;
@@ -133,10 +133,10 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
     std::vector<int> gc(std::begin(kChannels), std::end(kChannels));
     std::vector<int> gt(std::begin(kThreads), std::end(kThreads));
     std::vector<int64_t> gs = slot_grid();
-    std::map<std::tuple<int, int, int64_t, int, int>, double> cache;
+    std::map<std::tuple<int, int, int64_t, int, int, int>, double> cache;
     int nprobe = 0;
     auto measure = [&](const ccl_plan_opts_t& o) {
-        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol);
+        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol, o.link_mode);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
         ++nprobe;
@@ -147,12 +147,13 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
     };
     ccl_plan_opts_t overall = base;
     double overall_bw = measure(base);
-    for (int sub = 0; sub < 4; ++sub) {
+    for (int sub = 0; sub < 8; ++sub) {
         ccl_plan_opts_t cur = base;
         // balanced = packed plus merged link-free threadblocks (the same as
         // packed when every threadblock has a FIFO link)
         cur.tb_alloc = sub & 1 ? CCL_TB_BALANCED : CCL_TB_CONNECTION;
         cur.protocol = sub & 2 ? CCL_PROTO_LL : CCL_PROTO_SIMPLE;
+        cur.link_mode = sub & 4 ? CCL_LINK_DIRECT : CCL_LINK_FIFO;
         int ic = nearest(gc, cur.channels), it = nearest(gt, cur.nthreads), is = nearest(gs, cur.slot_bytes);
         auto eval = [&](int c, int t, int sl) {
             ccl_plan_opts_t o = cur;

@@ -513,7 +513,8 @@ ccl_status_t ccl_allreduce_ring_noalloc(void* const* in_bufs, void* const* out_b
 /*
  * The search of ccl_tune on its own (AutoCCL report, research method 1-2):
  * the implementation parameters threadblock policy (connection / balanced)
- * x protocol (simple / LL) make four subspaces; in each, coordinate descent over channels, threads and slot
+ * x protocol (simple / LL) x transport (FIFO / direct) make eight
+ * subspaces; in each, coordinate descent over channels, threads and slot
  * size, driven by a caller-supplied probe that returns the bandwidth of a
  * configuration (any unit, <= 0 = cannot run).  start (nullable) is the first point; best gets
  * the winner, *best_bw its bandwidth, *probes the number of distinct

@@ -343,10 +343,11 @@ def test_coordinate_descent_treats_infeasible_points_as_zero():
 
 
 def test_coordinate_descent_plateau_stops_early():
-    # four subspaces (policy x protocol): on a flat surface each tries one
-    # step up and one down per coordinate (at most 6 probes), plus the start
+    # eight subspaces (policy x protocol x transport): on a flat surface each
+    # tries one step up and one down per coordinate (at most 6 probes), plus
+    # the start
     best, bw, n = ccl.tune_search(lambda o: 1.0)
-    assert bw == 1.0 and n <= 1 + 4 * 6
+    assert bw == 1.0 and n <= 1 + 8 * 6
 
 
 def test_microbatch_window_is_used_when_the_fifo_holds_it():
@@ -426,3 +427,15 @@ def test_balanced_allocation_merges_link_free_threadblocks():
     assert a.nthreadblocks == b.nthreadblocks
     with pytest.raises(ccl.CclError):
         s.check(1024, BF16, tb_alloc=3)
+
+
+def test_coordinate_descent_visits_both_transports():
+    seen = set()
+
+    def f(o):
+        seen.add((o.link_mode, o.tb_alloc, o.protocol))
+        return (1.5 if o.link_mode == ccl.LINK_DIRECT else 1.0) * _surface((8, 512, 1 << 17))(o)
+    best, bw, n = ccl.tune_search(f)
+    assert {m for m, _, _ in seen} == {ccl.LINK_FIFO, ccl.LINK_DIRECT}
+    assert len(seen) == 8
+    assert best.link_mode == ccl.LINK_DIRECT and bw == pytest.approx(1.5)
