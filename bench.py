@@ -13,7 +13,10 @@ synthetic inputs resident in HBM:
   ar_1m     ring AllReduce, R=8, fp32, 1 MiB/rank, 1 channel
 
 value = schedule bytes of the step (bytes every fused instruction reads and
-writes, FIFO staging included) / device time of the step.  The step's working
+writes, FIFO staging included) / device time of the step.  A schedule that
+moves fewer bytes (direct transport, unchained copy hops) lowers the step
+time and the byte count together; collective_min_bytes_gbs (each input read
+once, each output written once, per second) does not depend on that choice.  The step's working
 set (~19 GiB) is far larger than L2, so consecutive collectives evict each
 other; no separate flush.
 
@@ -39,13 +42,20 @@ MiB = 1 << 20
 # name, kind, R, G, dtype, bytes per chunk, dist, seed, plan options
 SUITE = [
     # parameters the workload fixes are kept (24 channels, 16 micro-batches,
-    # 1 channel, <= 4 channels); the others are the best measured settings
+    # 1 channel, <= 4 channels); the others are the best measured settings.
+    # fuse="nochain": reductions fused, copy-only receives left unchained so
+    # that direct transport makes each all-gather hop one plain copy
     ("hier_ar", 3, 16, 8, 0, 4 * MiB, "normal", 2,
-     dict(channels=9, microbatches=16, tb_alloc=1, slot_bytes=65536, fifo_slots=8, mb_window=4)),
+     dict(fuse="nochain", link_mode=1, channels=9, microbatches=16, tb_alloc=1, slot_bytes=65536, fifo_slots=8,
+          mb_window=4)),
     ("a2a", 4, 32, 8, 2, 1 * MiB, "uniform", 3,
      dict(channels=8, link_mode=1, channel_scaling=0, tb_alloc=2, tb_budget=256)),
-    ("ring_bf16", 0, 8, 0, 1, 32 * MiB, "normal", 4, dict(channels=24, slot_bytes=131072)),
-    ("ring_f32", 0, 8, 0, 0, 32 * MiB, "normal", 4, dict(channels=24, slot_bytes=131072)),
+    ("ring_bf16", 0, 8, 0, 1, 32 * MiB, "normal", 4,
+     dict(fuse="nochain", link_mode=1, channels=24, slot_bytes=131072, microbatches=12, fifo_slots=4, tb_alloc=2,
+          tb_budget=192)),
+    ("ring_f32", 0, 8, 0, 0, 32 * MiB, "normal", 4,
+     dict(fuse="nochain", link_mode=1, channels=24, slot_bytes=131072, microbatches=12, fifo_slots=4, tb_alloc=2,
+          tb_budget=192)),
     # relay hops as plain direct copies (no fusion into FIFO forwards)
     ("a2n", 5, 24, 8, 0, 16 * MiB, "normal", 4,
      dict(fuse=False, channels=16, link_mode=1, microbatches=8, tb_alloc=2, tb_budget=304, channel_scaling=0)),
@@ -53,7 +63,8 @@ SUITE = [
      # every hop a direct copy into the next rank's output (no FIFO)
      dict(fuse=False, channels=4, link_mode=1)),
     ("rs_3m", 2, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4)),
-    ("ar_1m", 0, 8, 0, 0, 1 * MiB // 8, "uniform", 0, dict(channels=1)),
+    ("ar_1m", 0, 8, 0, 0, 1 * MiB // 8, "uniform", 0, dict(fuse="nochain", link_mode=1, channels=1, tb_alloc=2,
+                                                            tb_budget=16)),
 ]
 ESIZE = {0: 4, 1: 2, 2: 2, 3: 4}
 NAMES = {0: "f32", 1: "bf16", 2: "f16", 3: "i32"}
@@ -157,10 +168,12 @@ class ClockSampler:
 
 def schedule_and_opts(ccl, kind, R, G, opts):
     """The built-in schedule of a suite row (the row's `fuse` key chooses
-    the compiler's fusion) and the remaining plan options."""
+    the compiler's fusion: True, False or "nochain") and the remaining plan
+    options."""
     opts = dict(opts)
     fuse = opts.pop("fuse", True)
-    return ccl.Schedule.builtin(kind, R, G, 0 if fuse else ccl.FLAG_NOFUSE), opts
+    flags = ccl.FLAG_NOCHAIN_COPIES if fuse == "nochain" else (0 if fuse else ccl.FLAG_NOFUSE)
+    return ccl.Schedule.builtin(kind, R, G, flags), opts
 
 
 def combine_replicas(res, world, device=None):
@@ -323,6 +336,7 @@ def run_gpu(args):
         del flush
     step_ms = total_ms / K
     value = sched_bytes / (step_ms * 1e6)
+    min_bytes = sum(it["stats"].min_bytes for it in items)
     avg_launch_ms = kern_ms_total / (K * len(items))
     achieved = (sched_bytes / len(items)) / (avg_launch_ms * 1e6)
 
@@ -388,6 +402,7 @@ def run_gpu(args):
                                "ring AR 8x1MiB f32",
                    "parallelism": "replicas only (R virtual ranks per GPU, no cross-GPU exchange)", "l2": "step working set ~19 GiB > L2 (no flush)",
                    "schedule_bytes_per_step": sched_bytes,
+                   "collective_min_bytes_per_step": min_bytes,
                    **({"subset": args.only, "scale": args.scale} if (args.only or args.scale != 1.0) else {})},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 3),
@@ -399,6 +414,10 @@ def run_gpu(args):
         "e2e": {"value": round(sched_bytes / (e2e_ms * 1e6), 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3), "steps": Ke,
                 "mode": args.e2e_mode, "streams": len(e2e_streams)},
+        # bytes every collective must move at least (each input read once,
+        # each output written once) per second of the step: unlike `value`,
+        # independent of the schedule's transport and fusion choices
+        "collective_min_bytes_gbs": round(min_bytes / (step_ms * 1e6), 1),
         "gpu_launches": K * len(items),
         "clocks": clk,
         "per_collective": per,

@@ -23,7 +23,8 @@ F32, BF16, F16, I32 = 0, 1, 2, 3
 IN, OUT, SCRATCH = 0, 1, 2
 COPY, REDUCE = 0, 1
 RING_ALLREDUCE, RING_ALLGATHER, RING_REDUCESCATTER, HIER_ALLREDUCE, ALLTOALL_2PHASE, ALLTONEXT, ALLTOALLV = range(7)
-FLAG_WRAP, FLAG_NOFUSE = 1, 2
+FLAG_WRAP, FLAG_NOFUSE, FLAG_NOCHAIN_COPIES = 1, 2, 4
+FUSE_NONE, FUSE_FULL, FUSE_NOCHAIN = 0, 1, 2
 SCHED_RR, SCHED_HPDS = 0, 1
 TB_CONNECTION, TB_PACKED, TB_BALANCED = 0, 1, 2
 MB_AUTO, MB_ALGO, MB_TASK, MB_SEGMENT = 0, 1, 2, 3
@@ -219,12 +220,14 @@ class Schedule:
     @classmethod
     def compile(cls, ops, nranks, nchunks, fuse=True):
         """``ops``: iterable of 8-int rows (op, src_rank, src_buf, src_off,
-        dst_rank, dst_buf, dst_off, count)."""
+        dst_rank, dst_buf, dst_off, count).  ``fuse``: a bool, or one of
+        FUSE_NONE / FUSE_FULL / FUSE_NOCHAIN."""
         rows = [tuple(int(v) for v in r) for r in ops]
         arr = (Op * max(1, len(rows)))(*[Op(*r) for r in rows])
         nch = (ctypes.c_int32 * 3)(*[int(c) for c in nchunks])
         h = ctypes.c_void_p()
-        _check(lib.ccl_schedule_compile(arr, len(rows), nranks, nch, 1 if fuse else 0, ctypes.byref(h)))
+        mode = int(fuse) if not isinstance(fuse, bool) else (FUSE_FULL if fuse else FUSE_NONE)
+        _check(lib.ccl_schedule_compile(arr, len(rows), nranks, nch, mode, ctypes.byref(h)))
         return cls(h.value)
 
     def info(self) -> ScheduleInfo:

@@ -96,6 +96,7 @@ struct ValueInfo {
 
 class Fuser {
 public:
+    bool chain_copies = true;  // R3 also chains receives that only copy
     std::vector<Half> h;
     std::vector<std::vector<int>> per_rank;  // indices into h, sorted by pos
 
@@ -179,7 +180,7 @@ public:
                     }
                 }
                 // R3: receive chaining
-                if (W.recv_x >= 0 && W.send_x < 0) {
+                if (W.recv_x >= 0 && W.send_x < 0 && (chain_copies || W.recv_reduce)) {
                     for (int xi : vi.consumers) {
                         Half& X = h[xi];
                         if (!send_only(X) || !X.src.same(W.dst)) continue;
@@ -195,6 +196,16 @@ public:
     }
 };
 
+}  // namespace
+
+int fuse_mode(uint32_t flags)
+{
+    if (flags & CCL_FLAG_NOFUSE) return CCL_FUSE_NONE;
+    return (flags & CCL_FLAG_NOCHAIN_COPIES) ? CCL_FUSE_NOCHAIN : CCL_FUSE_FULL;
+}
+
+namespace {
+
 int kind_of(const Half& x)
 {
     if (x.recv_x < 0 && x.send_x < 0) return x.local_reduce ? CCL_I_REDUCE : CCL_I_COPY;
@@ -207,7 +218,7 @@ int kind_of(const Half& x)
 }  // namespace
 
 ccl_status_t compile_program(const ccl_op_t* ops, int nops, int nranks, const int32_t nchunks[3],
-                             bool fuse, ccl_schedule* s)
+                             int fuse, ccl_schedule* s)
 {
     if (nranks < 1 || nranks > CCL_MAX_RANKS)
         return fail(CCL_ERR_INVALID_ARG, "nranks must be in 1.." + std::to_string(CCL_MAX_RANKS));
@@ -266,7 +277,8 @@ ccl_status_t compile_program(const ccl_op_t* ops, int nops, int nranks, const in
         }
     }
     F.index(nranks);
-    if (fuse) {
+    F.chain_copies = fuse != CCL_FUSE_NOCHAIN;
+    if (fuse != CCL_FUSE_NONE) {
         int guard = 0;
         while (F.step()) {
             F.index(nranks);

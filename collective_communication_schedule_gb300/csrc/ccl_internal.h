@@ -78,8 +78,10 @@ int64_t kind_bytes_factor(int kind);   // bytes moved per element byte
 bool kind_reads_slot(int kind);
 bool kind_writes_slot(int kind);
 bool kind_is_reduce(int kind);
+// fuse: CCL_FUSE_NONE, CCL_FUSE_FULL or CCL_FUSE_NOCHAIN
 ccl_status_t compile_program(const ccl_op_t* ops, int nops, int nranks, const int32_t nchunks[3],
-                             bool fuse, ccl_schedule* s);
+                             int fuse, ccl_schedule* s);
+int fuse_mode(uint32_t flags);
 ccl_status_t builtin_program(int kind, int nranks, int G, uint32_t flags,
                              std::vector<ccl_op_t>* ops, int32_t nchunks[3]);
 // uneven AllToAll: counts[s * R + d] chunks from s to d

@@ -1006,7 +1006,10 @@ ccl_status_t ccl_schedule_compile(const ccl_op_t* ops, int32_t nops, int32_t nra
 {
     if (!out || !nchunks) return ccl::fail(CCL_ERR_INVALID_ARG, "null argument");
     auto* s = new ccl_schedule();
-    ccl_status_t st = ccl::compile_program(ops, nops, nranks, nchunks, fuse != 0, s);
+    ccl_status_t st = ccl::compile_program(ops, nops, nranks, nchunks,
+                                           fuse == CCL_FUSE_NOCHAIN ? CCL_FUSE_NOCHAIN
+                                                                    : (fuse != 0 ? CCL_FUSE_FULL : CCL_FUSE_NONE),
+                                           s);
     if (st != CCL_OK) { delete s; return st; }
     *out = s;
     return CCL_OK;
@@ -1021,7 +1024,7 @@ ccl_status_t ccl_schedule_builtin(int32_t kind, int32_t nranks, int32_t group_si
     ccl_status_t st = ccl::builtin_program(kind, nranks, group_size, flags, &ops, nch);
     if (st != CCL_OK) return st;
     auto* s = new ccl_schedule();
-    st = ccl::compile_program(ops.data(), (int)ops.size(), nranks, nch, (flags & CCL_FLAG_NOFUSE) == 0, s);
+    st = ccl::compile_program(ops.data(), (int)ops.size(), nranks, nch, ccl::fuse_mode(flags), s);
     if (st != CCL_OK) { delete s; return st; }
     s->builtin = kind;
     s->group_size = group_size;
@@ -1037,7 +1040,7 @@ ccl_status_t ccl_schedule_alltoallv(int32_t nranks, const int32_t* counts, uint3
     ccl_status_t st = ccl::alltoallv_program(nranks, counts, &ops, nch);
     if (st != CCL_OK) return st;
     auto* s = new ccl_schedule();
-    st = ccl::compile_program(ops.data(), (int)ops.size(), nranks, nch, (flags & CCL_FLAG_NOFUSE) == 0, s);
+    st = ccl::compile_program(ops.data(), (int)ops.size(), nranks, nch, ccl::fuse_mode(flags), s);
     if (st != CCL_OK) { delete s; return st; }
     s->builtin = CCL_ALLTOALLV;
     s->group_size = 0;

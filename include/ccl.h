@@ -94,6 +94,18 @@ typedef enum {
 
 #define CCL_FLAG_WRAP 1u    /* AllToNext: also send rank R-1 -> rank 0 */
 #define CCL_FLAG_NOFUSE 2u  /* compile without instruction fusion */
+/* Fuse as usual but leave a received value that is only copied on (no
+ * reduction) as a receive into its buffer plus a send from it, instead of
+ * chaining the two into one receive-copy-send; reductions keep their fused
+ * forms.  With direct transport each such hop is then one plain copy into
+ * the next rank's buffer (the all-gather half of a ring or hierarchical
+ * AllReduce). */
+#define CCL_FLAG_NOCHAIN_COPIES 4u
+
+/* Fusion modes of ccl_schedule_compile's `fuse` argument. */
+#define CCL_FUSE_NONE 0
+#define CCL_FUSE_FULL 1
+#define CCL_FUSE_NOCHAIN 2  /* as CCL_FLAG_NOCHAIN_COPIES */
 
 /* Fused instruction kinds produced by the compiler (MSCCLang report,
  * §III.1 "instruction generation" and "instruction fusion"). */
@@ -142,8 +154,10 @@ typedef struct {
  * Compile a chunk program.  ops[0..nops) in program order; dependencies
  * are traced from program order (read-after-write, write-after-read and
  * write-after-write on overlapping ranges of the same rank's buffer), so the
- * traced DAG is acyclic by construction.  fuse = 1 applies copy propagation,
- * dead-store elimination and recv/send fusion; fuse = 0 keeps one
+ * traced DAG is acyclic by construction.  fuse = CCL_FUSE_FULL (or any
+ * value other than the two below) applies copy propagation, dead-store
+ * elimination and recv/send fusion; CCL_FUSE_NOCHAIN does the same except
+ * chaining a copy-only receive into its send; CCL_FUSE_NONE (0) keeps one
  * instruction per half operation.
  * Errors: CCL_ERR_INVALID_ARG (rank/buffer/range out of bounds, count <= 0,
  * overlapping source and destination, nranks outside 1..CCL_MAX_RANKS).
@@ -154,7 +168,8 @@ ccl_status_t ccl_schedule_compile(const ccl_op_t* ops, int32_t nops, int32_t nra
 /*
  * Generate and compile a built-in program.  group_size (G) is used by the
  * hierarchical, AllToAll and AllToNext kinds (nranks must be a multiple of
- * G); the ring kinds ignore it.  flags: CCL_FLAG_WRAP, CCL_FLAG_NOFUSE.
+ * G); the ring kinds ignore it.  flags: CCL_FLAG_WRAP, CCL_FLAG_NOFUSE,
+ * CCL_FLAG_NOCHAIN_COPIES (NOFUSE wins when both are set).
  */
 ccl_status_t ccl_schedule_builtin(int32_t kind, int32_t nranks, int32_t group_size,
                                   uint32_t flags, ccl_schedule_t* out);
@@ -168,7 +183,8 @@ ccl_status_t ccl_schedule_builtin(int32_t kind, int32_t nranks, int32_t group_si
  * long as the longest rank's (in: max_s sum_d counts[s][d] chunks, out:
  * max_d sum_s counts[s][d]); the tail of a shorter output is not written.
  * One copy per non-empty pair, issued in shift order (d = s + k) so that
- * each round of the program touches distinct links.  flags: CCL_FLAG_NOFUSE.
+ * each round of the program touches distinct links.  flags: CCL_FLAG_NOFUSE,
+ * CCL_FLAG_NOCHAIN_COPIES.
  * Errors: CCL_ERR_INVALID_ARG (nranks out of range, a negative count, no
  * chunk to move, a per-rank total above 2^30 chunks).
  */

@@ -57,12 +57,17 @@ def to_host(ts, dtype):
 
 
 def run_case(ccl, kind, R, G, ce, dtype, dist, seed, wrap=False, fuse=True, sampled=None, **opts):
-    """Run the built-in collective on the GPU and the oracle on the CPU.
+    """Run the built-in collective on the GPU and the oracle on the CPU
+    (``fuse``: True, False or "nochain" for copy receives left unchained).
     Returns (gpu_outputs, oracle_outputs, plan); with ``sampled`` (array of
     in-chunk offsets) the oracle computes only those columns and the GPU
     outputs are reduced to the same columns."""
     import torch
-    flags = (ccl.FLAG_WRAP if wrap else 0) | (0 if fuse else ccl.FLAG_NOFUSE)
+    flags = ccl.FLAG_WRAP if wrap else 0
+    if fuse == "nochain":
+        flags |= ccl.FLAG_NOCHAIN_COPIES
+    elif not fuse:
+        flags |= ccl.FLAG_NOFUSE
     sched = ccl.Schedule.builtin(kind, R, G, flags)
     plan = ccl.Plan(sched, ce, dtype, **opts)
     ops, nch = oracle_program(kind, R, G, wrap)

@@ -138,10 +138,11 @@ def interpret_fused(instrs, R, nchunks, ce, dtype, inputs):
 
 @pytest.mark.parametrize("kind,R,G", [(0, 8, 0), (0, 3, 0), (1, 8, 0), (2, 8, 0), (2, 5, 0), (3, 16, 8), (3, 6, 3),
                                       (4, 8, 4), (4, 32, 8), (5, 24, 8), (5, 6, 2)])
-@pytest.mark.parametrize("fuse", [True, False])
+@pytest.mark.parametrize("fuse", [True, False, "nochain"])
 def test_fused_builtins_equal_oracle(kind, R, G, fuse):
     dtype, ce = BF16, 5
-    s = ccl.Schedule.builtin(kind, R, G, 0 if fuse else ccl.FLAG_NOFUSE)
+    flags = ccl.FLAG_NOCHAIN_COPIES if fuse == "nochain" else (0 if fuse else ccl.FLAG_NOFUSE)
+    s = ccl.Schedule.builtin(kind, R, G, flags)
     name, args = ORACLE_GEN[kind]
     ops, nch = OS.BUILTINS[name](*args(R, G))
     assert tuple(s.info().nchunks) == tuple(nch)
@@ -150,6 +151,33 @@ def test_fused_builtins_equal_oracle(kind, R, G, fuse):
     want, _, _ = oracle.run(ops, R, nch, ce, dtype, ins)
     for r in range(R):
         assert np.array_equal(got[r].view(np.uint8), want[r].view(np.uint8)), f"rank {r}"
+
+
+def test_nochain_keeps_copy_receives_apart():
+    """Ring AllReduce: full fusion chains every all-gather hop into a
+    receive-copy-send; without copy chaining each middle hop stays a receive
+    plus a send, while the reduce-scatter half keeps its fused reduce forms.
+    Under direct transport the copy hops then become plain copies."""
+    for R in (3, 8):
+        nochain = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, R, 0, ccl.FLAG_NOCHAIN_COPIES)
+        per_rank = {}
+        for ins in nochain.instrs():
+            per_rank.setdefault(ins["rank"], []).append(ccl.KIND_NAMES[ins["kind"]])
+        for r in range(R):
+            want = ["send"] + ["rrs"] * (R - 2) + ["rrcs"] + ["recv", "send"] * (R - 2) + ["recv"]
+            assert sorted(per_rank[r]) == sorted(want)
+        # same bytes in FIFO mode: (R-2) chunks per rank move 2 bytes (recv)
+        # + 2 (send) instead of 3 (rcs) and one more read of the output
+        full = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, R)
+        nf = full.info().bytes_per_chunk_elem_x_esize
+        nn = nochain.info().bytes_per_chunk_elem_x_esize
+        assert nn == nf + R * (R - 2)
+        # direct transport: a middle hop is one copy into the next rank's
+        # output (2 bytes per element byte) instead of a receive-copy-send (3)
+        ce, es = 64, 4
+        st_full = full.check(ce, F32, link_mode=ccl.LINK_DIRECT)
+        st_nochain = nochain.check(ce, F32, link_mode=ccl.LINK_DIRECT)
+        assert st_nochain.schedule_bytes == st_full.schedule_bytes - R * (R - 2) * ce * es
 
 
 def random_program(seed, R=3, C=4, nops=40):
@@ -169,7 +197,7 @@ def random_program(seed, R=3, C=4, nops=40):
 
 
 @pytest.mark.parametrize("seed", range(12))
-@pytest.mark.parametrize("fuse", [True, False])
+@pytest.mark.parametrize("fuse", [True, False, ccl.FUSE_NOCHAIN])
 def test_random_programs_fused_equal_oracle(seed, fuse):
     ops, nch = random_program(seed)
     R, ce = 3, 3

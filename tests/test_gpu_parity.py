@@ -68,6 +68,16 @@ def test_unfused_equals_fused(ccl):
         assert_bitexact(got, want)
 
 
+@pytest.mark.parametrize("link_mode", [0, 1])
+def test_nochain_copies_bitexact(ccl, link_mode):
+    """Reductions fused, copy receives unchained: under direct transport every
+    all-gather hop is a plain copy into the next rank's buffer."""
+    for kind, R, G, dtype in [(0, 8, 0, BF16), (3, 16, 8, F32), (1, 8, 0, BF16), (5, 24, 8, F32), (0, 3, 0, F16)]:
+        got, want, _ = run_case(ccl, kind, R, G, 1000, dtype, DIST[dtype], 8, fuse="nochain", link_mode=link_mode,
+                                channels=2, microbatches=3, slot_bytes=4096, tb_alloc=2 if link_mode else 0)
+        assert_bitexact(got, want)
+
+
 def test_config0_ring_allreduce_fp32_and_int32(ccl):
     """R = 8, 262144 elements per rank (8 chunks of 32768), seed 0."""
     got, want, _ = run_case(ccl, 0, 8, 0, 32768, F32, "uniform", 0)
