@@ -47,11 +47,11 @@ namespace ccl {
 //
 //  * issuer (warp 0, lane 0) walks the threadblock program.  Step records
 //    (128 bytes each) arrive by cp.async in batches of kLook, one batch
-//    ahead.  It waits (bounded) for a step's dependency counters and for the
-//    first slot of up to kLook coming steps -- incoming slot full, outgoing
-//    slot free -- polling all those flags with relaxed loads in one round
-//    trip, then one acquire fence; later slots of a step are polled kBatch
-//    at a time.  A step that follows an earlier step of its own threadblock
+//    ahead.  It waits (bounded) for the first slot of up to kLook coming
+//    steps -- incoming slot full, outgoing slot free -- and for their first
+//    kDepPoll dependency counters, polling all those words with relaxed
+//    loads in one round trip, then one acquire fence; later slots of a step
+//    are polled kBatch at a time, further counters one step at a time.  A step that follows an earlier step of its own threadblock
 //    waits only for that step's last tile.  Slots are handed out as tiles
 //    of at most `tile` bytes through a ring of kQ shared-memory descriptors
 //    guarded by mbarriers ("ready").  Slot indices are computed in 32 bits
@@ -109,8 +109,10 @@ struct Release {
     int last;                      // last tile of its step
 };
 
-// steps whose first-slot flags the issuer polls in one round trip
+// steps whose first-slot flags and first kDepPoll dependency counters the
+// issuer polls in one round trip
 constexpr int kLook = 4;
+constexpr int kDepPoll = 2;
 
 struct CtlShared {
     DRec rec[2 * kLook];                // two batches of step records (prefetched one batch ahead)
@@ -122,6 +124,8 @@ struct CtlShared {
     unsigned long long freed[kQ];
     unsigned long long full[kNSMax];    // stage loaded
     int last_head[kHist];               // issuer only: last descriptor of step si % kHist
+    const unsigned long long* poll_ptr[kLook * (2 + kDepPoll)];   // issuer only: polled words
+    unsigned long long poll_want[kLook * (2 + kDepPoll)];         // and their targets
 };
 
 __device__ __forceinline__ void record_timeout(const KParams& P, int si, int reason)
@@ -279,29 +283,61 @@ __device__ __forceinline__ SlotCond first_slot_cond(const KParams& P, const DRec
     return c;
 }
 
-// Poll the first-slot flags of steps [s0, s1) (records in the ring, no
-// dependency counters) with relaxed loads issued together; returns the end
-// of the leading run of ready steps (> s0) after one acquire fence, or -1
-// when the wait for step s0 fails.
-__device__ int poll_steps(const KParams& P, const CtlShared* sh, int s0, int s1, unsigned exec_mod,
+// Poll the conditions of steps [s0, s1) (records in the ring) -- the first
+// FIFO slot's flags and the first kDepPoll dependency counters of each --
+// with relaxed loads issued together; returns the end of the leading run of
+// ready steps (> s0) after one acquire fence, or -1 when the wait for step
+// s0 fails.  Counters of a step beyond kDepPoll are left to wait_deps.
+__device__ int poll_steps(const KParams& P, CtlShared* sh, int s0, int s1, unsigned exec_mod,
                           unsigned long long& waited)
 {
-    SlotCond c[kLook];
+    constexpr int kC = 2 + kDepPoll;   // conditions per step
     const int n = s1 - s0;
+    const unsigned long long base = (unsigned long long)(P.exec * P.m);
+    // condition words and targets go to shared memory (the issuer's
+    // registers are capped with the rest of the kernel's)
 #pragma unroll
-    for (int i = 0; i < kLook; ++i)
-        c[i] = i < n ? first_slot_cond(P, sh->rec[(s0 + i) % (2 * kLook)], exec_mod) : SlotCond{nullptr, nullptr, 0, 0};
+    for (int i = 0; i < kLook; ++i) {
+        const unsigned long long** ptr = sh->poll_ptr + i * kC;
+        unsigned long long* want = sh->poll_want + i * kC;
+        if (i >= n) {
+            for (int k = 0; k < kC; ++k) ptr[k] = nullptr;
+            continue;
+        }
+        const DRec& st = sh->rec[(s0 + i) % (2 * kLook)];
+        const SlotCond c = first_slot_cond(P, st, exec_mod);
+        ptr[0] = c.in;
+        want[0] = c.vin;
+        ptr[1] = c.out;
+        want[1] = c.vout;
+        for (int k = 0; k < kDepPoll; ++k) {
+            if (k < st.dep_count) {
+                const DDep d = P.deps[st.dep_begin + k];
+                ptr[2 + k] = P.counters + d.counter;
+                want[2 + k] = base + d.value;
+            } else {
+                ptr[2 + k] = nullptr;
+            }
+        }
+    }
     unsigned long long t0 = 0;
     unsigned spins = 0;
     while (true) {
-        unsigned long long x[kLook], y[kLook];
+        unsigned long long x[kLook * kC];
 #pragma unroll
-        for (int i = 0; i < kLook; ++i) {
-            x[i] = c[i].in ? ld_relaxed(c[i].in) : ~0ull;
-            y[i] = c[i].out ? ld_relaxed(c[i].out) : ~0ull;
+        for (int k = 0; k < kLook * kC; ++k) {
+            const unsigned long long* q = sh->poll_ptr[k];
+            x[k] = q ? ld_relaxed(q) : ~0ull;
         }
         int r = 0;
-        while (r < n && x[r] >= c[r].vin && y[r] >= c[r].vout) ++r;
+        bool ok = true;
+#pragma unroll
+        for (int i = 0; i < kLook; ++i) {
+#pragma unroll
+            for (int k = 0; k < kC; ++k)
+                if (x[i * kC + k] < sh->poll_want[i * kC + k]) ok = false;
+            if (ok && i < n) r = i + 1;
+        }
         if (r > 0) {
             fence_acq_rel_gpu();
             if (t0) waited += gtimer() - t0;
@@ -312,7 +348,9 @@ __device__ int poll_steps(const KParams& P, const CtlShared* sh, int s0, int s1,
         if ((spins & 15) == 0) {
             if (*(volatile int*)P.status != 0) return -1;
             if (gtimer() - t0 > P.timeout_ns) {
-                record_timeout(P, s0, x[0] < c[0].vin ? WAIT_FULL : WAIT_FREE);
+                record_timeout(P, s0, x[0] < sh->poll_want[0]   ? WAIT_FULL
+                                      : x[1] < sh->poll_want[1] ? WAIT_FREE
+                                                                : WAIT_DEP);
                 return -1;
             }
         }
@@ -355,10 +393,10 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
         const DRec& st = sh->rec[si % (2 * kLook)];
         const unsigned long long t_start = gtimer();
         unsigned long long waited = 0, t_pub = 0;
-        if (si >= cleared && st.dep_count == 0) {
-            // one round trip for the next steps that wait on FIFO flags only
-            int s1 = si + 1;
-            while (s1 < rec_ready && s1 < si + kLook && sh->rec[s1 % (2 * kLook)].dep_count == 0) ++s1;
+        if (si >= cleared) {
+            // one round trip for the first-slot flags and dependency
+            // counters of the next steps whose records are here
+            const int s1 = rec_ready < si + kLook ? rec_ready : si + kLook;
             cleared = poll_steps(P, sh, si, s1, exec_mod, waited);
             if (cleared < 0) {
                 publish_cmd(2);
@@ -376,7 +414,8 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
                 return;
             }
         }
-        if (st.dep_count > 0 && !wait_deps(P, P.deps + st.dep_begin, st.dep_count, si, waited)) {
+        if (st.dep_count > kDepPoll &&
+            !wait_deps(P, P.deps + st.dep_begin + kDepPoll, st.dep_count - kDepPoll, si, waited)) {
             publish_cmd(2);
             return;
         }
