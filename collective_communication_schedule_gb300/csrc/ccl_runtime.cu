@@ -517,7 +517,7 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
                 r.full = (Lout && post && last_tile && !P.ll) ? P.flags + Lout->flag_base + out_idx : nullptr;
                 r.full_v = sout + 1;
                 r.last = last_tile && k == nslots - 1;
-                r.counter = st.signal >= 0 ? P.counters + st.signal : nullptr;
+                r.counter = (st.signal >= 0 && post) ? P.counters + st.signal : nullptr;
                 r.counter_v = (unsigned long long)(P.exec * P.m + st.mb + 1);
                 r.si = si;
                 if (P.timeline && !t_pub) t_pub = gtimer();

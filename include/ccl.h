@@ -460,9 +460,10 @@ typedef struct {
 ccl_status_t ccl_plan_steps(ccl_plan_t p, ccl_step_info_t* out, int64_t cap, int64_t* n);
 
 /*
- * Test hook: make threadblock `tb` skip the flag post of its step `step`
- * (the data is still written), so a peer's wait runs out.  Used to check
- * that a lost signal ends in CCL_ERR_TIMEOUT with a usable device.
+ * Test hook: make threadblock `tb` skip the FIFO flag posts and the
+ * dependency-counter post of its step `step` (the data is still written),
+ * so a peer's wait runs out.  Used to check that a lost signal ends in
+ * CCL_ERR_TIMEOUT with a usable device.
  */
 ccl_status_t ccl_plan_debug_drop_signal(ccl_plan_t p, int32_t tb, int32_t step);
 

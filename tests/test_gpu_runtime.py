@@ -37,6 +37,34 @@ def test_lost_signal_times_out_and_device_stays_usable(ccl):
     assert_bitexact(got, want)
 
 
+def test_lost_counter_times_out_and_device_stays_usable(ccl):
+    """Direct copies signal dependency counters instead of FIFO flags: a
+    threadblock of link-free copies that posts none of its counters makes its
+    dependents give up after 50 ms; the GPU then runs a fresh plan."""
+    import torch
+    import datagen
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 4, 0, ccl.FLAG_NOCHAIN_COPIES)
+    plan = ccl.Plan(s, 1024, F32, timeout_ms=50, link_mode=ccl.LINK_DIRECT, tb_alloc=ccl.TB_CONNECTION)
+    steps = plan.steps()
+    by_tb = {}
+    for k, st in enumerate(steps):
+        by_tb.setdefault(int(st["tb"]), []).append(st)
+    free = [tb for tb, lst in by_tb.items() if all(x["link_in"] < 0 and x["link_out"] < 0 for x in lst)]
+    assert free, "the plan has a threadblock of direct copies"
+    for i in range(len(by_tb[free[0]])):
+        plan.debug_drop_signal(free[0], i)
+    ins = to_device(datagen.rank_inputs(1, "normal", 4, 4 * 1024, F32), F32)
+    outs = empty_outputs(4, 4 * 1024, F32)
+    plan.execute(ins, outs)
+    torch.cuda.synchronize()
+    with pytest.raises(ccl.CclError) as ei:
+        plan.status()
+    assert ei.value.code == 8
+    assert "gave up waiting" in ei.value.detail
+    got, want, _ = run_case(ccl, 0, 4, 0, 1024, F32, "normal", 1, fuse="nochain", link_mode=ccl.LINK_DIRECT)
+    assert_bitexact(got, want)
+
+
 def test_timeline_reports_idle_fractions(ccl):
     import torch
     import datagen
