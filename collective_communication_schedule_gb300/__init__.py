@@ -30,6 +30,7 @@ TB_CONNECTION, TB_PACKED, TB_BALANCED = 0, 1, 2
 MB_AUTO, MB_ALGO, MB_TASK, MB_SEGMENT = 0, 1, 2, 3
 LINK_FIFO, LINK_DIRECT = 0, 1
 PROTO_SIMPLE, PROTO_LL = 0, 1
+ENGINE_PIPELINED, ENGINE_SEQUENTIAL = 0, 1
 KIND_NAMES = ["copy", "reduce", "send", "recv", "rrc", "rcs", "fwd", "rrs", "rrcs", "copy_send"]
 DTYPE_NAMES = {F32: "f32", BF16: "bf16", F16: "f16", I32: "i32"}
 ESIZE = {F32: 4, BF16: 2, F16: 2, I32: 4}
@@ -71,7 +72,7 @@ class PlanOpts(ctypes.Structure):
                 ("tb_alloc", ctypes.c_int32), ("mb_order", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("instrument", ctypes.c_int32), ("tile_bytes", ctypes.c_int64), ("bulk", ctypes.c_int32),
                 ("link_mode", ctypes.c_int32), ("channel_scaling", ctypes.c_int32), ("mb_window", ctypes.c_int32),
-                ("protocol", ctypes.c_int32), ("tb_budget", ctypes.c_int32)]
+                ("protocol", ctypes.c_int32), ("tb_budget", ctypes.c_int32), ("engine", ctypes.c_int32)]
 
 
 class PlanStats(ctypes.Structure):
@@ -83,7 +84,7 @@ class PlanStats(ctypes.Structure):
                 ("channels", ctypes.c_int32), ("nthreads", ctypes.c_int32), ("fifo_slots", ctypes.c_int32),
                 ("slot_bytes", ctypes.c_int64), ("fifo_bytes", ctypes.c_int64), ("device_bytes", ctypes.c_int64),
                 ("compile_ms", ctypes.c_double), ("tile_bytes", ctypes.c_int64), ("stages", ctypes.c_int32),
-                ("mb_window", ctypes.c_int32), ("protocol", ctypes.c_int32), ("pad", ctypes.c_int32)]
+                ("mb_window", ctypes.c_int32), ("protocol", ctypes.c_int32), ("engine", ctypes.c_int32)]
 
 
 class StepInfo(ctypes.Structure):

@@ -90,6 +90,7 @@ struct PlanImage {
     int64_t tile_bytes = 0;          // tile of the data path
     int32_t ns = 0;                  // shared-memory stages of the bulk path (set at plan creation)
     int32_t bulk = 0;                // bulk path requested
+    int32_t engine = 0;              // CCL_ENGINE_*
     int32_t link_mode = 0;
     int32_t ndirect = 0;             // transfers turned into direct copies
     int32_t channel_scaling = 0;

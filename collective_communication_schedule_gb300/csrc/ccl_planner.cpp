@@ -441,7 +441,8 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     const int64_t slot_stride = o.protocol == CCL_PROTO_LL ? 2 * o.slot_bytes : o.slot_bytes;
     img->slot_bytes = o.slot_bytes;
     img->tile_bytes = o.tile_bytes;
-    img->bulk = o.bulk;
+    img->bulk = o.engine == CCL_ENGINE_SEQUENTIAL ? 0 : o.bulk;
+    img->engine = o.engine;
     img->link_mode = o.link_mode;
     img->nthreads = o.nthreads;
     img->dtype = dtype;
@@ -877,6 +878,10 @@ ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, con
     if (o.nthreads < 128 || o.nthreads > 1024 || o.nthreads % 32)
         return fail(CCL_ERR_INVALID_ARG, "nthreads must be a multiple of 32 in 128..1024");
     if (o.bulk != 0 && o.bulk != 1) return fail(CCL_ERR_INVALID_ARG, "bulk must be 0 or 1");
+    if (o.engine != CCL_ENGINE_PIPELINED && o.engine != CCL_ENGINE_SEQUENTIAL)
+        return fail(CCL_ERR_INVALID_ARG, "engine must be CCL_ENGINE_PIPELINED or CCL_ENGINE_SEQUENTIAL");
+    if (o.engine == CCL_ENGINE_SEQUENTIAL && o.protocol == CCL_PROTO_LL)
+        return fail(CCL_ERR_UNSUPPORTED, "the sequential engine has no LL data path");
     if (o.channel_scaling != 0 && o.channel_scaling != 1)
         return fail(CCL_ERR_INVALID_ARG, "channel_scaling must be 0 or 1");
     if (o.tile_bytes < 16 || o.tile_bytes % 16 || o.tile_bytes > 65536)

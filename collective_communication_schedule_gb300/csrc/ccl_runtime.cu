@@ -874,8 +874,133 @@ __global__ void __launch_bounds__(LL ? kMaxThreadsLL : 1024, 1) ccl_exec_kernel(
 template __global__ void ccl_exec_kernel<false>(const __grid_constant__ KParams P);
 template __global__ void ccl_exec_kernel<true>(const __grid_constant__ KParams P);
 
-const void* exec_kernel(int protocol)
+// ----------------------------------------------------------------------
+// Sequential engine: one CTA per threadblock program, no warp roles.  Thread
+// 0 reads a step's record, waits (bounded) for its dependency counters and,
+// slot by slot, for the FIFO flags; every thread of the CTA moves the slot;
+// after a CTA barrier thread 0 issues the gpu-scope release fence and posts
+// the slot's flags (and, after the last slot, the step's counter).  Steps run
+// strictly one after another, so a step needs no drain of an earlier one.
+// Fewer hand-offs per step than the warp-specialised pipeline, and all warps
+// move data; no overlap of one step's waits with another step's data.
+// ----------------------------------------------------------------------
+struct SeqShared {
+    DRec rec;
+    int abort;
+};
+
+__global__ void __launch_bounds__(1024, 1) ccl_exec_seq_kernel(const __grid_constant__ KParams P)
 {
+    __shared__ __align__(16) SeqShared sh;
+    const int tid = threadIdx.x, T = blockDim.x;
+    const int b0 = P.tb_begin[blockIdx.x], b1 = P.tb_begin[blockIdx.x + 1];
+    const unsigned S = (unsigned)P.S;
+    const unsigned exec_mod = (unsigned)(P.exec % P.S);
+    const DRec& st = sh.rec;
+    for (int si = b0; si < b1; ++si) {
+        unsigned long long t_start = 0, waited = 0;
+        if (tid == 0) {
+            if (P.timeline) t_start = gtimer();
+            sh.rec = P.recs[si];
+            int ok = *(volatile int*)P.status == 0;
+            if (ok && sh.rec.dep_count > 0)
+                ok = wait_deps(P, P.deps + sh.rec.dep_begin, sh.rec.dep_count, si, waited);
+            sh.abort = !ok;
+        }
+        __syncthreads();
+        if (sh.abort) return;
+        const int es = (st.dtype == CCL_BF16 || st.dtype == CCL_F16) ? 2 : 4;
+        const int esh = es == 2 ? 1 : 2;
+        const DLink* Lin = st.link_in >= 0 ? P.links + st.link_in : nullptr;
+        const DLink* Lout = st.link_out >= 0 ? P.links + st.link_out : nullptr;
+        const unsigned long long base_in = Lin ? (unsigned long long)(P.exec * Lin->total) : 0;
+        const unsigned long long base_out = Lout ? (unsigned long long)(P.exec * Lout->total) : 0;
+        const long long slot_elems = P.slot_bytes >> esh;
+        const bool linked = Lin || Lout;
+        long long nslots = linked ? (st.nslots > 0 ? st.nslots : 1) : 1;
+        if (!linked && st.nelem > 0) nslots = (st.nelem + slot_elems - 1) / slot_elems;
+        unsigned in_idx = Lin ? slot_index(exec_mod, *Lin, st.seq_in_mod, S) : 0;
+        unsigned out_idx = Lout ? slot_index(exec_mod, *Lout, st.seq_out_mod, S) : 0;
+        const int red = st.kind == CCL_I_REDUCE || st.kind == CCL_I_RRC || st.kind == CCL_I_RRS || st.kind == CCL_I_RRCS;
+        const char* srcb = st.src_buf >= 0 ? P.bufs[st.src_buf][st.src_rank] + st.src_off * es : nullptr;
+        const char* locb = st.loc_buf >= 0 ? P.bufs[st.loc_buf][st.loc_rank] + st.loc_off * es : nullptr;
+        char* dstb = st.dst_buf >= 0 ? P.bufs[st.dst_buf][st.dst_rank] + st.dst_off * es : nullptr;
+        const bool post = !(st.flags & 1);
+        unsigned long long t_pub = 0, t_done = 0;
+        for (long long k = 0; k < nslots; ++k) {
+            const unsigned long long sin = base_in + st.seq_in + k;
+            const unsigned long long sout = base_out + st.seq_out + k;
+            if (linked) {
+                if (tid == 0) sh.abort = wait_slots(P, Lin, Lout, sin, sout, in_idx, out_idx, 1, si, waited) == 0;
+                __syncthreads();
+                if (sh.abort) return;
+            }
+            if (tid == 0 && P.timeline && k == 0) t_pub = gtimer();
+            const long long e0 = k * slot_elems;
+            long long n = st.nelem - e0;
+            if (n > slot_elems) n = slot_elems;
+            if (n < 0) n = 0;
+            const char* slot_in = Lin ? P.fifo + Lin->slot_base + (long long)in_idx * P.slot_stride : nullptr;
+            char* slot_out = Lout ? P.fifo + Lout->slot_base + (long long)out_idx * P.slot_stride : nullptr;
+            const char* a;
+            bool as = false;
+            if (Lin && st.kind != CCL_I_REDUCE) {
+                a = slot_in;
+            } else {
+                a = srcb + e0 * es;
+                as = st.src_buf == CCL_BUF_IN;
+            }
+            const char* b = locb ? locb + e0 * es : nullptr;
+            const bool bs = st.loc_buf == CCL_BUF_IN;
+            char* o1;
+            char* o2 = nullptr;
+            bool o1s = false;
+            if (dstb) {
+                o1 = dstb + e0 * es;
+                o1s = st.dst_buf == CCL_BUF_OUT;
+                o2 = slot_out;
+            } else {
+                o1 = slot_out;
+            }
+            if (n > 0) {
+                switch (st.dtype) {
+                case CCL_F32: move_part<CCL_F32>(red, a, as, b, bs, o1, o1s, o2, n, tid, T); break;
+                case CCL_BF16: move_part<CCL_BF16>(red, a, as, b, bs, o1, o1s, o2, n, tid, T); break;
+                case CCL_F16: move_part<CCL_F16>(red, a, as, b, bs, o1, o1s, o2, n, tid, T); break;
+                default: move_part<CCL_I32>(red, a, as, b, bs, o1, o1s, o2, n, tid, T); break;
+                }
+            }
+            __syncthreads();
+            if (tid == 0) {
+                if (P.timeline && k == nslots - 1) t_done = gtimer();
+                // every thread's stores were observed at the barrier; the
+                // fence makes them visible at gpu scope before the flags
+                fence_acq_rel_gpu();
+                if (Lin && post) st_relaxed(P.flags + Lin->flag_base + S + in_idx, sin + 1);
+                if (Lout && post) st_relaxed(P.flags + Lout->flag_base + out_idx, sout + 1);
+                if (k == nslots - 1) {
+                    if (st.signal >= 0 && post)
+                        st_relaxed(P.counters + st.signal, (unsigned long long)(P.exec * P.m + st.mb + 1));
+                    if (P.timeline) {
+                        unsigned long long* tl = P.timeline + 5ll * si;
+                        tl[0] = t_start;
+                        tl[1] = waited;
+                        tl[2] = t_pub;
+                        tl[3] = t_done;
+                        tl[4] = gtimer();
+                    }
+                }
+            }
+            if (++in_idx == S) in_idx = 0;
+            if (++out_idx == S) out_idx = 0;
+        }
+        __syncthreads();   // the record is read again by thread 0 for the next step
+    }
+}
+
+const void* exec_kernel(int protocol, int engine)
+{
+    if (engine == CCL_ENGINE_SEQUENTIAL) return (const void*)ccl_exec_seq_kernel;
     return protocol == CCL_PROTO_LL ? (const void*)ccl_exec_kernel<true> : (const void*)ccl_exec_kernel<false>;
 }
 
@@ -932,6 +1057,7 @@ ccl_plan_opts_t merged_opts(const ccl_plan_opts_t* opts)
         o.mb_window = opts->mb_window;
         o.protocol = opts->protocol;
         o.tb_budget = opts->tb_budget;
+        o.engine = opts->engine;
     }
     return o;
 }
@@ -960,6 +1086,7 @@ void fill_stats(const ccl::PlanImage& img, ccl_plan_stats_t* st)
     st->stages = img.ns;
     st->mb_window = img.mb_window;
     st->protocol = img.protocol;
+    st->engine = img.engine;
 }
 
 void free_plan(ccl_plan* p)
@@ -1038,6 +1165,7 @@ void ccl_plan_opts_default(ccl_plan_opts_t* o)
     o->mb_window = 0;
     o->protocol = CCL_PROTO_SIMPLE;
     o->tb_budget = 0;
+    o->engine = CCL_ENGINE_PIPELINED;
 }
 
 ccl_status_t ccl_schedule_compile(const ccl_op_t* ops, int32_t nops, int32_t nranks, const int32_t nchunks[3],
@@ -1167,7 +1295,7 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, p->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
     cudaFuncAttributes fa{};
-    const void* kfn = ccl::exec_kernel(img.protocol);
+    const void* kfn = ccl::exec_kernel(img.protocol, img.engine);
     if (img.protocol == CCL_PROTO_LL && img.nthreads > ccl::kMaxThreadsLL) {
         if (opts && opts->nthreads) {
             delete p;
@@ -1293,7 +1421,7 @@ ccl_status_t ccl_execute(ccl_plan_t p, void* const* in_bufs, void* const* out_bu
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p->img.ntb == 0) return CCL_OK;  // empty program: nothing to move
     void* args[] = {&k};
-    cudaError_t e = cudaLaunchCooperativeKernel(ccl::exec_kernel(p->img.protocol), dim3(p->img.ntb),
+    cudaError_t e = cudaLaunchCooperativeKernel(ccl::exec_kernel(p->img.protocol, p->img.engine), dim3(p->img.ntb),
                                                 dim3(p->img.nthreads), args,
                                                 (size_t)p->img.ns * p->img.tile_bytes, s);
     if (e != cudaSuccess) return ccl::cuda_fail(e, "executor launch");

@@ -2,7 +2,9 @@
 //
 // AutoCCL report, "research method" 1-2: implementation parameters (here:
 // the threadblock allocation policy -- one per connection, or packed and
-// balanced --, the FIFO protocol and the transport) split the search space
+// balanced --, the FIFO protocol, the transport and the execution engine --
+// pipelined or sequential; the sequential engine has no LL path, so twelve
+// subspaces in all) split the search space
 // into small subspaces; inside each, the resource parameters nChannel, nThread and
 // chunk size are optimised one coordinate at a time, raising a parameter
 // while bandwidth keeps improving (bandwidth is unimodal in each of them).
@@ -32,11 +34,11 @@ struct Prober {
     cudaStream_t stream;
     int reps;
     int probes = 0;
-    std::map<std::tuple<int, int, int64_t, int, int, int>, double> cache;  // -> microseconds (0 = infeasible)
+    std::map<std::tuple<int, int, int64_t, int, int, int, int>, double> cache;  // -> microseconds (0 = infeasible)
 
     double time_us(const ccl_plan_opts_t& o)
     {
-        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol, o.link_mode);
+        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol, o.link_mode, o.engine);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
         ++probes;
@@ -128,15 +130,16 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
         base.mb_window = z.mb_window;
         base.protocol = z.protocol;
         base.tb_budget = z.tb_budget;
+        base.engine = z.engine;
     }
     if (!base.nthreads) base.nthreads = 512;
     std::vector<int> gc(std::begin(kChannels), std::end(kChannels));
     std::vector<int> gt(std::begin(kThreads), std::end(kThreads));
     std::vector<int64_t> gs = slot_grid();
-    std::map<std::tuple<int, int, int64_t, int, int, int>, double> cache;
+    std::map<std::tuple<int, int, int64_t, int, int, int, int>, double> cache;
     int nprobe = 0;
     auto measure = [&](const ccl_plan_opts_t& o) {
-        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol, o.link_mode);
+        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol, o.link_mode, o.engine);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
         ++nprobe;
@@ -147,13 +150,15 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
     };
     ccl_plan_opts_t overall = base;
     double overall_bw = measure(base);
-    for (int sub = 0; sub < 8; ++sub) {
+    for (int sub = 0; sub < 16; ++sub) {
+        if ((sub & 2) && (sub & 8)) continue;   // LL on the sequential engine: no such path
         ccl_plan_opts_t cur = base;
         // balanced = packed plus merged link-free threadblocks (the same as
         // packed when every threadblock has a FIFO link)
         cur.tb_alloc = sub & 1 ? CCL_TB_BALANCED : CCL_TB_CONNECTION;
         cur.protocol = sub & 2 ? CCL_PROTO_LL : CCL_PROTO_SIMPLE;
         cur.link_mode = sub & 4 ? CCL_LINK_DIRECT : CCL_LINK_FIFO;
+        cur.engine = sub & 8 ? CCL_ENGINE_SEQUENTIAL : CCL_ENGINE_PIPELINED;
         int ic = nearest(gc, cur.channels), it = nearest(gt, cur.nthreads), is = nearest(gs, cur.slot_bytes);
         auto eval = [&](int c, int t, int sl) {
             ccl_plan_opts_t o = cur;

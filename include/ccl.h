@@ -209,6 +209,11 @@ typedef enum { CCL_MB_AUTO = 0, CCL_MB_ALGO = 1, CCL_MB_TASK = 2, CCL_MB_SEGMENT
 typedef enum { CCL_LINK_FIFO = 0, CCL_LINK_DIRECT = 1 } ccl_link_mode_t;
 typedef enum { CCL_PROTO_SIMPLE = 0, CCL_PROTO_LL = 1 } ccl_protocol_t;
 
+typedef enum {
+    CCL_ENGINE_PIPELINED = 0,    /* warp-specialised CTAs (issuer, data warps, releaser) */
+    CCL_ENGINE_SEQUENTIAL = 1    /* one step at a time, every thread moves data */
+} ccl_engine_t;
+
 /*
  * Execution parameters of a plan (zero fields take the defaults written by
  * ccl_plan_opts_default).
@@ -279,6 +284,15 @@ typedef enum { CCL_PROTO_SIMPLE = 0, CCL_PROTO_LL = 1 } ccl_protocol_t;
  *                 proportional to its size (at most `channels`, at least 1),
  *                 so small transfers do not occupy as many threadblocks as
  *                 large ones; 0 = every instruction gets `channels`.
+ *   engine      : CCL_ENGINE_PIPELINED (default): warp-specialised CTAs --
+ *                 one issuing thread polls the flags of coming steps and
+ *                 hands slots to the data warps through shared-memory
+ *                 descriptors, one releasing thread posts flags -- so the
+ *                 waits of a step overlap the data of earlier ones.
+ *                 CCL_ENGINE_SEQUENTIAL: a CTA runs its steps one after
+ *                 another; thread 0 waits, every thread moves the slot, a CTA
+ *                 barrier, thread 0 fences and posts.  Fewer hand-offs per
+ *                 step (for the latency-bound sizes); no bulk copies, no LL.
  *   link_mode   : transport of a transfer (AutoCCL report: implementation
  *                 parameter "transport").  CCL_LINK_FIFO stages every
  *                 transfer in the link FIFO; CCL_LINK_DIRECT lets a plain
@@ -304,6 +318,7 @@ typedef struct {
     int32_t mb_window;
     int32_t protocol;
     int32_t tb_budget;   /* CCL_TB_BALANCED: threadblocks to aim for (0: 256) */
+    int32_t engine;      /* CCL_ENGINE_* */
 } ccl_plan_opts_t;
 
 void ccl_plan_opts_default(ccl_plan_opts_t* o);
@@ -387,7 +402,7 @@ typedef struct {
     int32_t stages;              /* shared-memory stages of the bulk path (0: registers only) */
     int32_t mb_window;           /* micro-batch window actually used */
     int32_t protocol;            /* CCL_PROTO_* */
-    int32_t pad;
+    int32_t engine;              /* CCL_ENGINE_* */
 } ccl_plan_stats_t;
 
 ccl_status_t ccl_plan_stats(ccl_plan_t p, ccl_plan_stats_t* st);
@@ -530,8 +545,9 @@ ccl_status_t ccl_allreduce_ring_noalloc(void* const* in_bufs, void* const* out_b
 /*
  * The search of ccl_tune on its own (AutoCCL report, research method 1-2):
  * the implementation parameters threadblock policy (connection / balanced)
- * x protocol (simple / LL) x transport (FIFO / direct) make eight
- * subspaces; in each, coordinate descent over channels, threads and slot
+ * x protocol (simple / LL) x transport (FIFO / direct) x engine (pipelined
+ * / sequential; no LL on the sequential engine) make twelve subspaces; in
+ * each, coordinate descent over channels, threads and slot
  * size, driven by a caller-supplied probe that returns the bandwidth of a
  * configuration (any unit, <= 0 = cannot run).  start (nullable) is the first point; best gets
  * the winner, *best_bw its bandwidth, *probes the number of distinct

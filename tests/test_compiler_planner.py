@@ -358,7 +358,9 @@ def test_coordinate_descent_reaches_the_peak_of_unimodal_surfaces(peak):
     best, bw, n = ccl.tune_search(_surface(peak))
     assert (best.channels, best.nthreads, best.slot_bytes) == peak
     assert bw == pytest.approx(1.0)
-    assert n < 9 * 4 * 9 // 2      # far fewer probes than the full grid (per subspace)
+    # twelve subspaces (policy x protocol x transport x engine, no LL on the
+    # sequential engine), each probing far fewer points than its 324-point grid
+    assert n <= 12 * 24
 
 
 def test_coordinate_descent_treats_infeasible_points_as_zero():
@@ -371,11 +373,18 @@ def test_coordinate_descent_treats_infeasible_points_as_zero():
 
 
 def test_coordinate_descent_plateau_stops_early():
-    # eight subspaces (policy x protocol x transport): on a flat surface each
-    # tries one step up and one down per coordinate (at most 6 probes), plus
-    # the start
-    best, bw, n = ccl.tune_search(lambda o: 1.0)
-    assert bw == 1.0 and n <= 1 + 8 * 6
+    # twelve subspaces (policy x protocol x transport x engine, minus LL on
+    # the sequential engine): on a flat surface each tries one step up and
+    # one down per coordinate (at most 6 probes), plus the start
+    seen = set()
+
+    def flat(o):
+        seen.add((o.tb_alloc, o.protocol, o.link_mode, o.engine))
+        return 1.0
+    best, bw, n = ccl.tune_search(flat)
+    assert bw == 1.0 and n <= 1 + 12 * 6
+    assert len(seen) == 12
+    assert (ccl.PROTO_LL, ccl.ENGINE_SEQUENTIAL) not in {(p, e) for _, p, _, e in seen}
 
 
 def test_microbatch_window_is_used_when_the_fifo_holds_it():
@@ -424,6 +433,19 @@ def test_ll_protocol_doubles_fifo_bytes_and_needs_16_byte_chunks():
     assert e.value.code == 1
 
 
+def test_engine_option_is_validated():
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 8)
+    assert s.check(4096, F32).engine == ccl.ENGINE_PIPELINED
+    st = s.check(4096, F32, engine=ccl.ENGINE_SEQUENTIAL, bulk=1)
+    assert st.engine == ccl.ENGINE_SEQUENTIAL and st.schedule_bytes == s.check(4096, F32).schedule_bytes
+    with pytest.raises(ccl.CclError) as e:
+        s.check(4096, F32, engine=2)
+    assert e.value.code == 1
+    with pytest.raises(ccl.CclError) as e:
+        s.check(4096, F32, engine=ccl.ENGINE_SEQUENTIAL, protocol=ccl.PROTO_LL)
+    assert e.value.code == 5
+
+
 def test_coordinate_descent_visits_both_protocols():
     seen = set()
 
@@ -434,6 +456,14 @@ def test_coordinate_descent_visits_both_protocols():
     assert seen == {ccl.PROTO_SIMPLE, ccl.PROTO_LL}
     assert best.protocol == ccl.PROTO_LL and bw == pytest.approx(2.0)
     assert (best.channels, best.nthreads, best.slot_bytes) == (4, 256, 1 << 16)
+
+
+def test_coordinate_descent_picks_the_faster_engine():
+    def f(o):
+        return (1.5 if o.engine == ccl.ENGINE_SEQUENTIAL else 1.0) * _surface((2, 512, 1 << 15))(o)
+    best, bw, n = ccl.tune_search(f)
+    assert best.engine == ccl.ENGINE_SEQUENTIAL and best.protocol == ccl.PROTO_SIMPLE
+    assert bw == pytest.approx(1.5)
 
 
 def test_balanced_allocation_merges_link_free_threadblocks():

@@ -69,6 +69,41 @@ def test_unfused_equals_fused(ccl):
 
 
 @pytest.mark.parametrize("link_mode", [0, 1])
+def test_sequential_engine_bitexact(ccl, link_mode):
+    """The sequential engine (one step at a time, every thread moving data)
+    on every built-in: ragged chunks, several slots per piece, micro-batches
+    and windows, FIFO and direct transport, fused and unfused programs."""
+    cases = [(0, 8, 0, 4099, F32, True), (0, 5, 0, 1000, BF16, "nochain"), (1, 8, 0, 3001, F16, True),
+             (2, 8, 0, 777, BF16, True), (3, 16, 8, 2048, F32, "nochain"), (4, 8, 4, 1000, F16, True),
+             (5, 24, 8, 1500, F32, False), (0, 8, 0, 1000, I32, True)]
+    for kind, R, G, ce, dtype, fuse in cases:
+        got, want, plan = run_case(ccl, kind, R, G, ce, dtype, DIST[dtype], 21, fuse=fuse, link_mode=link_mode,
+                                   engine=ccl.ENGINE_SEQUENTIAL, channels=2, microbatches=3, slot_bytes=4096)
+        assert plan.stats().engine == ccl.ENGINE_SEQUENTIAL
+        assert_bitexact(got, want)
+
+
+def test_sequential_engine_repeated_executions(ccl):
+    """Flags and counters carry the execution number: five executions of one
+    plan (slot indices wrap differently each time) stay bit-exact."""
+    import torch
+    import datagen
+    import oracle
+    from gpu_helpers import oracle_program, to_device, empty_outputs, to_host
+    s = ccl.Schedule.builtin(0, 8, 0)
+    plan = ccl.Plan(s, 3000, BF16, engine=ccl.ENGINE_SEQUENTIAL, slot_bytes=2048, fifo_slots=3, microbatches=2)
+    ops, nch = oracle_program(0, 8, 0, False)
+    for rep in range(5):
+        ins = datagen.rank_inputs(30 + rep, "normal", 8, nch[0] * 3000, BF16)
+        d_out = empty_outputs(8, nch[1] * 3000, BF16)
+        plan.execute(to_device(ins, BF16), d_out)
+        torch.cuda.synchronize()
+        plan.status()
+        want, _, _ = oracle.run(ops, 8, nch, 3000, BF16, ins)
+        assert_bitexact(to_host(d_out, BF16), want)
+
+
+@pytest.mark.parametrize("link_mode", [0, 1])
 def test_nochain_copies_bitexact(ccl, link_mode):
     """Reductions fused, copy receives unchained: under direct transport every
     all-gather hop is a plain copy into the next rank's buffer."""
