@@ -1,0 +1,49 @@
+"""The benchmark suite's plans, checked on the host (no GPU).
+
+Every row of the suite plans with its own options; the ring rows' schedule
+bytes equal the closed form of a ring AllReduce whose all-gather hops are
+direct copies; every plan fits the co-residency limit of the executor's
+cooperative launch; the kernel each row launches is the one named in the
+benchmark line.
+"""
+import pytest
+
+ccl = pytest.importorskip("collective_communication_schedule_gb300")
+bench = pytest.importorskip("bench")
+
+MiB = 1 << 20
+
+
+def _plan(row):
+    name, kind, R, G, dt, cb, dist, seed, opts = row
+    s, po = bench.schedule_and_opts(ccl, kind, R, G, opts)
+    return s, s.check(cb // bench.ESIZE[dt], dt, **po), po
+
+
+@pytest.mark.parametrize("row", bench.SUITE, ids=[r[0] for r in bench.SUITE])
+def test_every_row_plans_within_two_ctas_per_sm(row):
+    s, st, po = _plan(row)
+    assert 0 < st.nthreadblocks <= 2 * 152
+    assert st.schedule_bytes >= st.min_bytes > 0
+    assert st.engine == po.get("engine", 0)
+    assert bench.kernel_name(st) == ("ccl_exec_seq_kernel" if st.engine == 1 else "ccl_exec_kernel<0>")
+
+
+@pytest.mark.parametrize("name", ["ring_bf16", "ring_f32", "ar_1m"])
+def test_ring_rows_match_the_closed_form(name):
+    """Ring AllReduce over R ranks of N bytes each: R N (6 - 4/R) schedule
+    bytes fully fused through FIFOs; leaving the R - 2 middle all-gather hops
+    of every chunk unchained and direct saves one byte per element byte on
+    each of them: N (R - 2) in all."""
+    row = [r for r in bench.SUITE if r[0] == name][0]
+    _, kind, R, G, dt, cb, dist, seed, opts = row
+    assert opts.get("fuse") == "nochain" and opts.get("link_mode") == 1
+    N = R * cb                       # R chunks of cb bytes per rank
+    _, st, _ = _plan(row)
+    assert st.schedule_bytes == R * N * 6 - 4 * N - N * (R - 2)
+    assert st.min_bytes == 2 * R * N
+
+
+def test_small_rows_run_sequential_and_large_rows_pipelined():
+    engines = {r[0]: r[8].get("engine", 0) for r in bench.SUITE}
+    assert {n for n, e in engines.items() if e == 1} == {"ag_3m", "rs_3m", "ar_1m"}
