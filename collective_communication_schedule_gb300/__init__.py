@@ -193,6 +193,20 @@ def default_opts() -> PlanOpts:
     return o
 
 
+_OPT_NAMES = frozenset(f[0] for f in PlanOpts._fields_)
+
+
+def _with_opts(opts, kw) -> PlanOpts:
+    """Library defaults (or ``opts``) with keyword overrides; an unknown
+    keyword is an error rather than a silently ignored attribute."""
+    o = opts if opts is not None else default_opts()
+    for k, v in kw.items():
+        if k not in _OPT_NAMES:
+            raise TypeError(f"unknown plan option {k!r}")
+        setattr(o, k, v)
+    return o
+
+
 class Schedule:
     """A compiled chunk program (``ccl_schedule_t``)."""
 
@@ -260,9 +274,7 @@ class Schedule:
 
     def check(self, chunk_elems, dtype, opts: PlanOpts | None = None, **kw) -> PlanStats:
         """Plan on the host only (deadlock simulation included, no GPU)."""
-        o = opts if opts is not None else default_opts()
-        for k, v in kw.items():
-            setattr(o, k, v)
+        o = _with_opts(opts, kw)
         st = PlanStats()
         _check(lib.ccl_plan_check(self._h, chunk_elems, dtype, ctypes.byref(o), ctypes.byref(st)))
         return st
@@ -278,9 +290,7 @@ class Plan:
     """An executable plan (``ccl_plan_t``) on the current CUDA device."""
 
     def __init__(self, schedule: Schedule, chunk_elems: int, dtype: int, opts: PlanOpts | None = None, **kw):
-        o = opts if opts is not None else default_opts()
-        for k, v in kw.items():
-            setattr(o, k, v)
+        o = _with_opts(opts, kw)
         self.schedule = schedule
         self.opts = o
         self.dtype = dtype

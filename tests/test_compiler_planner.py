@@ -433,6 +433,12 @@ def test_ll_protocol_doubles_fifo_bytes_and_needs_16_byte_chunks():
     assert e.value.code == 1
 
 
+def test_unknown_plan_option_is_an_error():
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 8)
+    with pytest.raises(TypeError):
+        s.check(4096, F32, channel=4)        # misspelt "channels"
+
+
 def test_engine_option_is_validated():
     s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 8)
     assert s.check(4096, F32).engine == ccl.ENGINE_PIPELINED
