@@ -73,8 +73,9 @@ METRIC = "effective HBM GB/s & busBW per collective vs GB300 HBM roofline, 1 GPU
 
 
 def sources_hash():
-    """Hash of the executor / planner sources and of the suite: the DRAM
-    traffic recorded in profiles/ holds only for this exact combination."""
+    """Hash of the executor / planner sources and of the suite rows that run
+    on the pipelined kernel (the launches whose DRAM traffic profiles/
+    records): the recorded traffic holds only for this exact combination."""
     import glob
     import hashlib
     csrc = os.path.join(ROOT, "collective_communication_schedule_gb300", "csrc")
@@ -85,13 +86,14 @@ def sources_hash():
     for f in files:
         with open(f, "rb") as fh:
             h.update(fh.read())
-    h.update(repr(SUITE).encode())
+    h.update(repr([r for r in SUITE if r[8].get("engine", 0) != 1]).encode())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel, planner or suite changed since it was captured."""
+def recorded_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when it records another kernel or when the sources or the suite
+    changed since it was captured."""
     try:
         kv = {}
         with open(os.path.join(ROOT, "profiles", "roofline_traffic.txt")) as f:
@@ -99,7 +101,7 @@ def recorded_traffic():
                 if line.strip() and not line.startswith("#"):
                     k, v = line.split()
                     kv[k] = v
-        if kv.get("sources_sha256_16") != sources_hash():
+        if kv.get("sources_sha256_16") != sources_hash() or kv.get("kernel") != kernel:
             return None
         return int(kv["traffic_bytes_per_launch"])
     except Exception:
@@ -423,7 +425,7 @@ def run_gpu(args):
                    **({"subset": args.only, "scale": args.scale} if (args.only or args.scale != 1.0) else {})},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 3), "kernels": kernels,
-                     "traffic": recorded_traffic() if not (args.only or args.scale != 1.0) else None,
+                     "traffic": recorded_traffic(dom) if not (args.only or args.scale != 1.0) else None,
                      "traffic_unit": "bytes per launch (ncu dram read+write, profiles/roofline_traffic.txt)",
                      "algorithmic_bytes_per_launch": bytes_dom // n_dom,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
