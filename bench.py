@@ -721,6 +721,77 @@ def run_alltoallv(args):
         print(json.dumps(rec), flush=True)
 
 
+def hier_allgather_program(G, ng):
+    """A user chunk program for the hierarchical AllGather of the HetCCL
+    summary ("hierarchical algorithm design and pipelined execution"): an
+    in-group step, a cross-group step and a final in-group step, the
+    cross-group transfers overlapping the in-group work.  Groups of G ranks
+    stand for the clusters.  Every rank places its block and copies it, from
+    its input, to the rank with its local index in every other group; then
+    ring rounds inside every group carry each block on from the rank it
+    entered the group at.  One chunk in per rank, R = G * ng chunks out.
+    Rows: (op, src_rank, src_buf, src_off, dst_rank, dst_buf, dst_off, count)."""
+    R = G * ng
+    ops = []
+    for r in range(R):
+        ops.append((0, r, 0, 0, r, 1, r, 1))
+        for h in range(ng):
+            if h != r // G:
+                ops.append((0, r, 0, 0, h * G + r % G, 1, r, 1))
+    for k in range(G - 1):           # ring round k inside every group
+        for h in range(ng):
+            for blk in range(R):     # entered group h at local index blk % G
+                a = h * G + (blk % G + k) % G
+                b = h * G + (blk % G + k + 1) % G
+                ops.append((0, a, 1, blk, b, 1, blk, 1))
+    return ops, (1, R, 0)
+
+
+def run_hier_allgather(args):
+    """NEXT workload: hierarchical AllGather, 16 ranks as 2 groups x 8, bf16,
+    4 MiB in and 64 MiB out per rank (normal(0,1), seed 5), against the flat
+    ring AllGather on the same ranks and bytes.  One JSON line per plan."""
+    import numpy as np
+    import torch
+    import collective_communication_schedule_gb300 as ccl
+    import datagen
+    G, ng = 8, 2
+    R = G * ng
+    ce = int(2 * MiB * args.scale)            # bf16 elements per chunk (4 MiB)
+    rng = np.random.default_rng(5)
+    d_in = [torch.from_numpy(datagen.draw(rng, "normal", ce, ccl.BF16).view(np.int16)).cuda() for _ in range(R)]
+    d_out = [torch.empty(R * ce, dtype=torch.int16, device="cuda") for _ in range(R)]
+    stream = torch.cuda.current_stream()
+    peak, _ = peaks()
+    ops, nch = hier_allgather_program(G, ng)
+    hier = ccl.Schedule.compile(ops, R, nch, fuse=False)
+    flat = ccl.Schedule.builtin(ccl.RING_ALLGATHER, R, 0, ccl.FLAG_NOFUSE)
+    flat_fused = ccl.Schedule.builtin(ccl.RING_ALLGATHER, R)
+    direct = dict(channels=8, link_mode=1)
+    balanced = dict(channels=8, link_mode=1, tb_alloc=2, tb_budget=304)
+    # unfused with direct copies: every hop one copy into the next rank's
+    # output (the hierarchical program fused through FIFOs needs more slots
+    # and threadblocks than fit); the flat ring also fused through FIFOs
+    runs = [("hierarchical", False, hier, direct), ("hierarchical", False, hier, balanced),
+            ("flat ring", False, flat, direct), ("flat ring", False, flat, balanced),
+            ("flat ring", True, flat_fused, dict(channels=8))]
+    for name, fuse, sched, o in runs:
+        rec = {"workload": "allgather", "algorithm": name, "ranks": R, "groups": ng,
+               "out_bytes_per_rank": R * ce * 2, "fuse": fuse, "opts": o}
+        try:
+            plan = ccl.Plan(sched, ce, ccl.BF16, **o)
+            ms = _time_plan(torch, plan, d_in, d_out, stream, reps=args.steps, warm=args.warmup)
+            st = plan.stats()
+            rec.update(us=round(ms * 1e3, 1), schedule_gbs=round(st.schedule_bytes / (ms * 1e6), 1),
+                       frac_of_peak=round(st.schedule_bytes / (ms * 1e6) / peak, 3),
+                       algbw_gbs=round(R * ce * 2 / (ms * 1e6), 1),   # output bytes per rank
+                       min_bytes_gbs=round(st.min_bytes / (ms * 1e6), 1), threadblocks=st.nthreadblocks)
+            del plan
+        except ccl.CclError as e:
+            rec["error"] = str(e)[:120]
+        print(json.dumps(rec), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -742,14 +813,18 @@ def main():
     ap.add_argument("--interference", action="store_true",
                     help="tune one collective (--only, default ring_f32) alone and beside a bf16 GEMM")
     ap.add_argument("--alltoallv", action="store_true", help="second workload: uneven (MoE) AllToAll")
+    ap.add_argument("--hier-allgather", action="store_true",
+                    help="hierarchical AllGather (in-group, cross-group, in-group) against the flat ring")
     args = ap.parse_args()
-    if args.ablation or args.interference or args.alltoallv:
+    if args.ablation or args.interference or args.alltoallv or args.hier_allgather:
         import torch
         torch.cuda.set_device(0)
         if args.ablation:
             run_ablation(args)
         elif args.interference:
             run_interference(args)
+        elif args.hier_allgather:
+            run_hier_allgather(args)
         else:
             run_alltoallv(args)
         return

@@ -30,6 +30,15 @@ Readings (the pages name these algorithms but do not spell them out):
   through local rank j of the source group and local rank j of the
   destination group, so that every link of the two groups carries a share.
   No wrap-around unless ``wrap`` is set.
+* hierarchical AllGather (HetCCL summary, "hierarchical algorithm design
+  and pipelined execution": an in-cluster step, a cross-cluster step, a
+  final in-cluster step, the cross-cluster transfers overlapping the
+  in-cluster work): groups of G ranks stand for the clusters.  (1) ring
+  AllGather of a group's own blocks inside the group; (2) rank (g, i)
+  copies its block to local rank i of every other group -- it reads only
+  the input, so it runs beside (1); (3) inside group h every block received
+  in (2) circulates the group ring starting from the rank that received it.
+  Every block crosses into each other group exactly once.
 * uneven AllToAll (per-pair sizes, the token exchange of a mixture-of-
   experts layer; a variant of the AllToAll of the MSCCLang report, §IV.3):
   rank s lays out its blocks by destination, rank d receives them ordered by
@@ -205,6 +214,38 @@ def alltoallv(counts):
     return _arr(ops), (nin, nout, 0)
 
 
+def hier_allgather(G: int, ng: int):
+    """out[r] = in[0] ++ in[1] ++ ... ++ in[R-1] over R = G * ng ranks, one
+    chunk per rank in, R chunks out (block s at chunk s)."""
+    R = G * ng
+    ops = []
+    rank = lambda g, i: g * G + i   # noqa: E731
+    # (1) in-group ring AllGather of the group's own blocks
+    for g in range(ng):
+        for i in range(G):
+            b = rank(g, i)
+            ops.append((COPY, b, IN, 0, b, OUT, b, 1))
+            for k in range(G - 1):
+                ops.append((COPY, rank(g, (i + k) % G), OUT, b, rank(g, (i + k + 1) % G), OUT, b, 1))
+    # (2) cross-group: same local index, every other group, from the input
+    for g in range(ng):
+        for i in range(G):
+            b = rank(g, i)
+            for h in range(ng):
+                if h != g:
+                    ops.append((COPY, b, IN, 0, rank(h, i), OUT, b, 1))
+    # (3) in group h, the block of (g, i) circulates from rank (h, i)
+    for h in range(ng):
+        for g in range(ng):
+            if g == h:
+                continue
+            for i in range(G):
+                b = rank(g, i)
+                for k in range(G - 1):
+                    ops.append((COPY, rank(h, (i + k) % G), OUT, b, rank(h, (i + k + 1) % G), OUT, b, 1))
+    return _arr(ops), (1, R, 0)
+
+
 BUILTINS = {
     "ring_allreduce": ring_allreduce,
     "ring_allgather": ring_allgather,
@@ -212,4 +253,5 @@ BUILTINS = {
     "hier_allreduce": hier_allreduce,
     "alltoall_two_phase": alltoall_two_phase,
     "alltonext": alltonext,
+    "hier_allgather": hier_allgather,
 }

@@ -68,6 +68,35 @@ def test_unfused_equals_fused(ccl):
         assert_bitexact(got, want)
 
 
+# fused through FIFOs the program needs round-robin task order with 4 slots
+# (the HPDS order deadlocks below 16 slots; the planner rejects it)
+@pytest.mark.parametrize("fuse,opts", [(True, dict(channels=2, scheduler=0)), (False, dict(channels=2, link_mode=1)),
+                                       (False, dict(channels=3, link_mode=1, tb_alloc=2, tb_budget=24)),
+                                       (True, dict(channels=2, engine=1, microbatches=2, scheduler=0))])
+def test_hier_allgather_program_bitexact(ccl, fuse, opts):
+    """The benchmark's hierarchical AllGather user program (16 ranks as 2
+    groups of 8), compiled through ccl_schedule_compile, against the oracle's
+    own program: ragged chunk (unaligned starts, element tail)."""
+    import torch
+    import bench
+    import datagen
+    import oracle
+    from oracle import schedules as OS
+    from gpu_helpers import to_device, empty_outputs, to_host
+    G, ng, ce = 8, 2, 5001
+    R = G * ng
+    ops, nch = bench.hier_allgather_program(G, ng)
+    plan = ccl.Plan(ccl.Schedule.compile(ops, R, nch, fuse=fuse), ce, BF16, slot_bytes=16384, **opts)
+    ins = datagen.rank_inputs(5, "normal", R, ce, BF16)
+    d_out = empty_outputs(R, R * ce, BF16)
+    plan.execute(to_device(ins, BF16), d_out)
+    torch.cuda.synchronize()
+    plan.status()
+    ref_ops, _ = OS.hier_allgather(G, ng)
+    want, _, _ = oracle.run(ref_ops, R, nch, ce, BF16, ins)
+    assert_bitexact(to_host(d_out, BF16), want)
+
+
 @pytest.mark.parametrize("link_mode", [0, 1])
 def test_sequential_engine_bitexact(ccl, link_mode):
     """The sequential engine (one step at a time, every thread moving data)
