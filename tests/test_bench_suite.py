@@ -47,3 +47,19 @@ def test_ring_rows_match_the_closed_form(name):
 def test_small_rows_run_sequential_and_large_rows_pipelined():
     engines = {r[0]: r[8].get("engine", 0) for r in bench.SUITE}
     assert {n for n, e in engines.items() if e == 1} == {"ag_3m", "rs_3m", "ar_1m"}
+
+
+def test_hier_allgather_benchmark_plans_fit():
+    """The --hier-allgather runs: the hierarchical program and the flat ring,
+    unfused with direct copies (one copy per hop: schedule bytes = collective
+    minimum), plan within the co-residency limit at the benchmark's size."""
+    G, ng = 8, 2
+    R, ce = G * ng, 2 * MiB
+    ops, nch = bench.hier_allgather_program(G, ng)
+    hier = ccl.Schedule.compile(ops, R, nch, fuse=False)
+    flat = ccl.Schedule.builtin(ccl.RING_ALLGATHER, R, 0, ccl.FLAG_NOFUSE)
+    for s in (hier, flat):
+        for o in (dict(channels=8, link_mode=1), dict(channels=8, link_mode=1, tb_alloc=2, tb_budget=304)):
+            st = s.check(ce, 1, **o)
+            assert st.nthreadblocks <= 2 * 152
+            assert st.schedule_bytes == st.min_bytes == 2 * R * R * ce * 2
