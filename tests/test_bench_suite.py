@@ -51,8 +51,10 @@ def test_small_rows_run_sequential_and_large_rows_pipelined():
 
 def test_hier_allgather_benchmark_plans_fit():
     """The --hier-allgather runs: the hierarchical program and the flat ring,
-    unfused with direct copies (one copy per hop: schedule bytes = collective
-    minimum), plan within the co-residency limit at the benchmark's size."""
+    unfused with direct copies, plan within the co-residency limit at the
+    benchmark's size and move the same bytes: every one of the R x R output
+    chunks is written once by one copy that reads one chunk (2 R^2 chunks),
+    against the collective minimum of R input and R^2 output chunks."""
     G, ng = 8, 2
     R, ce = G * ng, 2 * MiB
     ops, nch = bench.hier_allgather_program(G, ng)
@@ -62,4 +64,5 @@ def test_hier_allgather_benchmark_plans_fit():
         for o in (dict(channels=8, link_mode=1), dict(channels=8, link_mode=1, tb_alloc=2, tb_budget=304)):
             st = s.check(ce, 1, **o)
             assert st.nthreadblocks <= 2 * 152
-            assert st.schedule_bytes == st.min_bytes == 2 * R * R * ce * 2
+            assert st.schedule_bytes == 2 * R * R * ce * 2
+            assert st.min_bytes == (R + R * R) * ce * 2
