@@ -42,3 +42,33 @@ def test_host_only_calls_work_without_a_gpu():
     st = s.check(1024, ccl.F32, channels=2)
     assert st.nthreadblocks == 16
     assert ccl.lib.ccl_error_string(3) == b"deadlock"
+
+
+def test_binding_structs_match_the_header_layout(tmp_path):
+    """Every ctypes structure of the binding has the size and field offsets of
+    its C counterpart, as gcc lays it out from include/ccl.h."""
+    import shutil
+    import subprocess
+    import pytest
+    import collective_communication_schedule_gb300 as ccl
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc:
+        pytest.skip("no C compiler")
+    pairs = [(ccl.Op, "ccl_op_t"), (ccl.ScheduleInfo, "ccl_schedule_info_t"), (ccl.InstrInfo, "ccl_instr_info_t"),
+             (ccl.PlanOpts, "ccl_plan_opts_t"), (ccl.PlanStats, "ccl_plan_stats_t"), (ccl.StepInfo, "ccl_step_info_t"),
+             (ccl.TuneOpts, "ccl_tune_opts_t"), (ccl.TuneReport, "ccl_tune_report_t")]
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "ccl.h"', "int main(void) {"]
+    want = []
+    for cls, cname in pairs:
+        lines.append(f'    printf("%zu\\n", sizeof({cname}));')
+        want.append(ctypes.sizeof(cls))
+        for f in cls._fields_:
+            lines.append(f'    printf("%zu\\n", offsetof({cname}, {f[0]}));')
+            want.append(getattr(cls, f[0]).offset)
+    lines += ["    return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    assert got == want
