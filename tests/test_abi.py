@@ -72,3 +72,28 @@ def test_binding_structs_match_the_header_layout(tmp_path):
     subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
     got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
     assert got == want
+
+
+def test_binding_constants_match_the_header():
+    """Every CCL_* constant of the header that the binding re-exports (same
+    name without the prefix) has the header's value."""
+    import collective_communication_schedule_gb300 as ccl
+    vals = {}
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", fn)).read(), flags=re.S)
+        for m in re.finditer(r"#define\s+CCL_([A-Z0-9_]+)\s+(\d+)u?\b", text):
+            vals[m.group(1)] = int(m.group(2))
+        for m in re.finditer(r"\bCCL_([A-Z0-9_]+)\s*=\s*(-?\d+)", text):
+            vals[m.group(1)] = int(m.group(2))
+    checked = 0
+    for name, v in vals.items():
+        if hasattr(ccl, name) and isinstance(getattr(ccl, name), int):
+            assert getattr(ccl, name) == v, name
+            checked += 1
+    assert checked >= 20
+    # instruction kind names are indexed by the header's CCL_I_* values
+    for i, name in enumerate(ccl.KIND_NAMES):
+        assert vals["I_" + name.upper()] == i, name
+    assert vals["I_NKINDS"] == len(ccl.KIND_NAMES)
