@@ -73,20 +73,29 @@ METRIC = "effective HBM GB/s & busBW per collective vs GB300 HBM roofline, 1 GPU
 
 
 def sources_hash():
-    """Hash of the executor / planner sources and of the suite rows that run
-    on the pipelined kernel (the launches whose DRAM traffic profiles/
-    records): the recorded traffic holds only for this exact combination."""
+    """Key of the DRAM traffic recorded in profiles/: the executor and planner
+    sources, the suite rows that run on the pipelined kernel (the launches
+    the traffic covers) and the instruction lists the compiler makes of
+    them.  The compiler's source stands in only through its output, so a
+    compiler change that leaves these schedules alone keeps the record."""
     import glob
     import hashlib
+    import collective_communication_schedule_gb300 as ccl
     csrc = os.path.join(ROOT, "collective_communication_schedule_gb300", "csrc")
     files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
                    glob.glob(os.path.join(csrc, "*.cpp")) + glob.glob(os.path.join(csrc, "*.h")),
                    key=os.path.basename)
     h = hashlib.sha256()
     for f in files:
+        if os.path.basename(f) == "ccl_compiler.cpp":
+            continue
         with open(f, "rb") as fh:
             h.update(fh.read())
-    h.update(repr([r for r in SUITE if r[8].get("engine", 0) != 1]).encode())
+    rows = [r for r in SUITE if r[8].get("engine", 0) != 1]
+    h.update(repr(rows).encode())
+    for name, kind, R, G, dt, cb, dist, seed, opts in rows:
+        sched, _ = schedule_and_opts(ccl, kind, R, G, opts)
+        h.update(repr([tuple(sorted(d.items())) for d in sched.instrs()]).encode())
     return h.hexdigest()[:16]
 
 

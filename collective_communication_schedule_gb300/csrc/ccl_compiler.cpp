@@ -97,6 +97,7 @@ struct ValueInfo {
 class Fuser {
 public:
     bool chain_copies = true;  // R3 also chains receives that only copy
+    std::vector<int> xfer_dst; // receiving rank of every transfer
     std::vector<Half> h;
     std::vector<std::vector<int>> per_rank;  // indices into h, sorted by pos
 
@@ -145,6 +146,37 @@ public:
         return true;
     }
 
+    // Moving X's send up to W (R2, R3) changes the order of the sends on the
+    // link W.rank -> dst.  The planner orders a threadblock's steps by their
+    // dependencies, so that is harmless unless a send to dst between the two
+    // positions must itself follow W: then the moved send would overtake it
+    // on the link while its receiver still takes them in program order.
+    // True when no alive half of W's rank strictly between W and X depends
+    // on W (transitively, through overlapping buffer ranges on that rank) and
+    // sends to dst.
+    bool can_move_send_up(int w, int xpos, int dst)
+    {
+        const Half& W = h[w];
+        std::vector<const Half*> dep{&W};
+        auto reads = [](const Half& a, const Range& r) { return a.src.overlaps(r) || a.loc.overlaps(r); };
+        for (int x : per_rank[W.rank]) {
+            const Half& y = h[x];
+            if (!y.alive || y.pos <= W.pos || y.pos >= xpos) continue;
+            bool d = false;
+            for (const Half* z : dep) {
+                if ((z->dst.valid() && (reads(y, z->dst) || y.dst.overlaps(z->dst))) ||
+                    (y.dst.valid() && reads(*z, y.dst))) {
+                    d = true;
+                    break;
+                }
+            }
+            if (!d) continue;
+            if (y.send_x >= 0 && xfer_dst[y.send_x] == dst) return false;
+            dep.push_back(&y);
+        }
+        return true;
+    }
+
     bool step()
     {
         for (auto& lst : per_rank) {
@@ -173,6 +205,8 @@ public:
                             X.src = W.src;
                             W.alive = false;
                         } else {
+                            // the send moves up to W's position
+                            if (!can_move_send_up(w, X.pos, xfer_dst[X.send_x])) continue;
                             W.send_x = X.send_x;
                             X.alive = false;
                         }
@@ -184,6 +218,8 @@ public:
                     for (int xi : vi.consumers) {
                         Half& X = h[xi];
                         if (!send_only(X) || !X.src.same(W.dst)) continue;
+                        // the send moves up to W's position
+                        if (!can_move_send_up(w, X.pos, xfer_dst[X.send_x])) continue;
                         W.send_x = X.send_x;
                         X.alive = false;
                         if (vi.consumers.size() == 1 && !vi.liveout) W.dst = Range();
@@ -267,6 +303,7 @@ ccl_status_t compile_program(const ccl_op_t* ops, int nops, int nranks, const in
             t.chunk_id = o.src_off;
             t.op_index = i;
             xf.push_back(t);
+            F.xfer_dst.push_back(o.dst_rank);
             Half snd;
             snd.rank = o.src_rank; snd.pos = i; snd.count = o.count; snd.send_x = id; snd.src = S;
             Half rcv;

@@ -180,6 +180,25 @@ def test_nochain_keeps_copy_receives_apart():
         assert st_nochain.schedule_bytes == st_full.schedule_bytes - R * (R - 2) * ce * es
 
 
+def test_fusion_keeps_the_order_of_dependent_sends_on_a_link():
+    """Rank 0 receives a reduction (op 0) and later sends two ranges of its
+    result to rank 1 (ops 1 and 2); rank 1 takes op 1 before op 2 (op 2
+    reduces into the range op 1 wrote).  Chaining op 2's send into the
+    receive of op 0 would put it on the link ahead of op 1's send, which
+    must follow op 0; the compiler leaves that send where it is, and the
+    program plans in every fusion mode with the oracle's result."""
+    ops = [(1, 1, 0, 0, 0, 1, 0, 3), (0, 0, 1, 0, 1, 2, 2, 1), (1, 0, 1, 0, 1, 2, 0, 3)]
+    nch = (3, 3, 3)
+    want, _, _ = oracle.run(np.array(ops, np.int32), 2, nch, 4, I32,
+                            datagen.rank_inputs(1, "int", 2, 12, I32))
+    for fuse in (ccl.FUSE_FULL, ccl.FUSE_NOCHAIN, ccl.FUSE_NONE):
+        s = ccl.Schedule.compile(ops, 2, nch, fuse=fuse)
+        s.check(64, F32)
+        got = interpret_fused(s.instrs(), 2, nch, 4, I32, datagen.rank_inputs(1, "int", 2, 12, I32))
+        for r in range(2):
+            assert np.array_equal(got[r], want[r])
+
+
 def random_program(seed, R=3, C=4, nops=40):
     rng = np.random.default_rng(seed)
     ops = []
