@@ -452,6 +452,21 @@ def test_ll_protocol_doubles_fifo_bytes_and_needs_16_byte_chunks():
     assert e.value.code == 1
 
 
+def test_degenerate_sizes_and_programs():
+    """An empty program plans to no threadblock (executing it launches
+    nothing); a zero-element chunk is rejected; a one-element chunk plans
+    (the element path carries it)."""
+    empty = ccl.Schedule.compile([], 2, (1, 1, 0))
+    st = empty.check(16, F32)
+    assert (st.nthreadblocks, st.nsteps, st.schedule_bytes) == (0, 0, 0)
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 8)
+    with pytest.raises(ccl.CclError) as e:
+        s.check(0, F32)
+    assert e.value.code == 1
+    one = s.check(1, BF16)
+    assert one.schedule_bytes == 8 * 8 * (6 * 8 - 4) // 8 * 2   # R N (6 - 4/R), N = 8 chunks of 2 bytes
+
+
 def test_unknown_plan_option_is_an_error():
     s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 8)
     with pytest.raises(TypeError):
