@@ -84,7 +84,8 @@ class PlanStats(ctypes.Structure):
                 ("channels", ctypes.c_int32), ("nthreads", ctypes.c_int32), ("fifo_slots", ctypes.c_int32),
                 ("slot_bytes", ctypes.c_int64), ("fifo_bytes", ctypes.c_int64), ("device_bytes", ctypes.c_int64),
                 ("compile_ms", ctypes.c_double), ("tile_bytes", ctypes.c_int64), ("stages", ctypes.c_int32),
-                ("mb_window", ctypes.c_int32), ("protocol", ctypes.c_int32), ("engine", ctypes.c_int32)]
+                ("mb_window", ctypes.c_int32), ("protocol", ctypes.c_int32), ("engine", ctypes.c_int32),
+                ("fuse", ctypes.c_int32)]
 
 
 class StepInfo(ctypes.Structure):

@@ -101,11 +101,22 @@ public:
     std::vector<Half> h;
     std::vector<std::vector<int>> per_rank;  // indices into h, sorted by pos
 
+    std::vector<std::vector<int>> per_pos;   // alive halves at each program position
+    std::vector<int> sender;                 // alive half that sends each transfer
+
     void index(int nranks)
     {
         per_rank.assign(nranks, {});
-        for (int i = 0; i < (int)h.size(); ++i)
-            if (h[i].alive) per_rank[h[i].rank].push_back(i);
+        int npos = 0;
+        for (const Half& x : h) npos = std::max(npos, x.pos + 1);
+        per_pos.assign(npos, {});
+        sender.assign(xfer_dst.size(), -1);
+        for (int i = 0; i < (int)h.size(); ++i) {
+            if (!h[i].alive) continue;
+            per_rank[h[i].rank].push_back(i);
+            per_pos[h[i].pos].push_back(i);
+            if (h[i].send_x >= 0) sender[h[i].send_x] = i;
+        }
         for (auto& v : per_rank)
             std::sort(v.begin(), v.end(), [&](int a, int b) { return h[a].pos < h[b].pos; });
     }
@@ -152,27 +163,45 @@ public:
     // positions must itself follow W: then the moved send would overtake it
     // on the link while its receiver still takes them in program order.
     // True when no alive half of W's rank strictly between W and X depends
-    // on W (transitively, through overlapping buffer ranges on that rank) and
-    // sends to dst.
+    // on W and sends to dst.  "Depends" is the closure of two edges, followed
+    // over every rank: a later half of the same rank that touches a range
+    // the other half wrote (or writes a range it read), and the receiving
+    // half of a transfer whose sending half depends on W -- so a chain that
+    // leaves W's rank through a transfer and comes back counts too.  Both
+    // edges only go forward in program position, so one pass over the
+    // positions between W and X finds the closure.
     bool can_move_send_up(int w, int xpos, int dst)
     {
         const Half& W = h[w];
-        std::vector<const Half*> dep{&W};
         auto reads = [](const Half& a, const Range& r) { return a.src.overlaps(r) || a.loc.overlaps(r); };
-        for (int x : per_rank[W.rank]) {
-            const Half& y = h[x];
-            if (!y.alive || y.pos <= W.pos || y.pos >= xpos) continue;
-            bool d = false;
-            for (const Half* z : dep) {
-                if ((z->dst.valid() && (reads(y, z->dst) || y.dst.overlaps(z->dst))) ||
-                    (y.dst.valid() && reads(*z, y.dst))) {
-                    d = true;
-                    break;
+        auto touches = [&](const Half& y, const Half& z) {   // y later than z on z's rank
+            return (z.dst.valid() && (reads(y, z.dst) || y.dst.overlaps(z.dst))) ||
+                   (y.dst.valid() && reads(z, y.dst));
+        };
+        std::vector<char> is_dep(h.size(), 0);
+        std::vector<std::vector<int>> dep_of_rank(per_rank.size());
+        is_dep[w] = 1;
+        dep_of_rank[W.rank].push_back(w);
+        for (int p = W.pos; p < xpos && p < (int)per_pos.size(); ++p) {
+            // a position holds one operation: its send half (possibly moved
+            // into an earlier half) and its receive half; two rounds let a
+            // receive see its sender's verdict at the same position
+            for (int round = 0; round < 2; ++round) {
+                for (int x : per_pos[p]) {
+                    if (is_dep[x]) continue;
+                    const Half& y = h[x];
+                    bool d = y.recv_x >= 0 && sender[y.recv_x] >= 0 && is_dep[sender[y.recv_x]];
+                    for (size_t k = 0; !d && k < dep_of_rank[y.rank].size(); ++k) {
+                        const Half& z = h[dep_of_rank[y.rank][k]];
+                        d = z.pos < y.pos && touches(y, z);
+                    }
+                    if (!d) continue;
+                    if (y.rank == W.rank && y.pos > W.pos && y.send_x >= 0 && xfer_dst[y.send_x] == dst)
+                        return false;
+                    is_dep[x] = 1;
+                    dep_of_rank[y.rank].push_back(x);
                 }
             }
-            if (!d) continue;
-            if (y.send_x >= 0 && xfer_dst[y.send_x] == dst) return false;
-            dep.push_back(&y);
         }
         return true;
     }
@@ -280,6 +309,7 @@ ccl_status_t compile_program(const ccl_op_t* ops, int nops, int nranks, const in
     }
 
     s->nranks = nranks;
+    s->fuse = fuse;
     for (int b = 0; b < 3; ++b) s->nchunks[b] = nchunks[b];
     s->ops.assign(ops, ops + nops);
 

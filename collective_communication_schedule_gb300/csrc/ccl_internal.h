@@ -66,6 +66,7 @@ struct ccl_schedule {
     int32_t nchunks[3] = {0, 0, 0};
     int32_t builtin = -1;
     int32_t group_size = 0;
+    int32_t fuse = CCL_FUSE_FULL;     // fusion mode the instructions were compiled with
     std::vector<ccl_op_t> ops;
     std::vector<ccl::Instr> instrs;   // sorted by (rank, position)
     std::vector<ccl::Xfer> xfers;

@@ -114,10 +114,13 @@ struct PlanImage {
     int64_t in_elems = 0, out_elems = 0;
     int32_t timeout_ms = 2000;
     int32_t instrument = 0;
+    int32_t fuse = CCL_FUSE_FULL;    // fusion mode of the instructions planned
 };
 
 struct Timeline {
-    std::vector<int> sp_lo, sp_hi;   // per instruction
+    std::vector<int> sp_lo, sp_hi;   // per instruction: first and last sub-pipeline of its tasks
+    std::vector<int> sp_key;         // per instruction: sub-pipeline that orders it in its threadblock
+    bool split = false;              // dependencies wait only for the effect task of a fused instruction
     std::vector<int> xfer_sp;        // per transfer
     int nsp = 0;
 };

@@ -68,7 +68,23 @@ int esize_of(int dt) { return (dt == CCL_BF16 || dt == CCL_F16) ? 2 : 4; }
 
 }  // namespace
 
-ccl_status_t build_timeline(const ccl_schedule& s, int scheduler, Timeline* tl)
+namespace {
+
+int log_level()
+{
+    const char* v = std::getenv("CCL_LOG_LEVEL");
+    return v ? std::atoi(v) : 0;
+}
+
+// One pass of the list scheduler.  split = false: a task waits for every
+// task of each instruction its instructions depend on.  split = true: it
+// waits only for the task that carries the buffer effects of that
+// instruction -- its receive when it has one (a fused receive-...-send
+// reads and writes its buffers when the data arrives; its send only passes
+// that data on), else its send, else the local task -- so a dependent of a
+// fused receive need not wait for the forwarded transfer, whose receiver
+// may itself wait for the dependent.
+ccl_status_t timeline_pass(const ccl_schedule& s, int scheduler, bool split, Timeline* tl)
 {
     const int ni = (int)s.instrs.size();
     const int nx = (int)s.xfers.size();
@@ -86,17 +102,34 @@ ccl_status_t build_timeline(const ccl_schedule& s, int scheduler, Timeline* tl)
         itasks[X.send_instr].push_back(x);
         itasks[X.recv_instr].push_back(x);
     }
+    // local task of every instruction without a transfer, and in the split
+    // model also of a copy-send: its local copy is its buffer effect
+    std::vector<int> local_task(ni, -1);
     for (int i = 0; i < ni; ++i) {
-        if (!itasks[i].empty()) continue;
-        itasks[i].push_back((int)tasks.size());
-        tasks.push_back(T{s.instrs[i].position, -1, -1, (int)s.instrs[i].src.off, {}});
+        const Instr& I = s.instrs[i];
+        const bool copy_part = split && I.xfer_in < 0 && I.xfer_out >= 0 && I.dst.valid();
+        if (!itasks[i].empty() && !copy_part) continue;
+        local_task[i] = (int)tasks.size();
+        itasks[i].push_back(local_task[i]);
+        tasks.push_back(T{I.position, -1, -1, (int)I.src.off, {}});
     }
     std::vector<std::vector<int>> ideps(ni);
     for (const Dep& d : s.deps) ideps[d.to].push_back(d.from);
+    auto effect_task = [&](int j) {
+        const Instr& J = s.instrs[j];
+        if (J.xfer_in >= 0) return J.xfer_in;
+        return local_task[j] >= 0 ? local_task[j] : J.xfer_out;
+    };
     auto add_preds_of = [&](int t, int instr) {
-        for (int j : ideps[instr])
+        for (int j : ideps[instr]) {
+            if (split) {
+                const int u = effect_task(j);
+                if (u != t) tasks[t].preds.push_back(u);
+                continue;
+            }
             for (int u : itasks[j])
                 if (u != t) tasks[t].preds.push_back(u);
+        }
     };
     for (int x = 0; x < nx; ++x) {
         const Xfer& X = s.xfers[x];
@@ -104,9 +137,11 @@ ccl_status_t build_timeline(const ccl_schedule& s, int scheduler, Timeline* tl)
         add_preds_of(x, X.recv_instr);
         int y = s.instrs[X.send_instr].xfer_in;
         if (y >= 0) tasks[x].preds.push_back(y);
+        // the send of a copy-send passes on what its local copy reads
+        if (local_task[X.send_instr] >= 0) tasks[x].preds.push_back(local_task[X.send_instr]);
     }
     for (int i = 0; i < ni; ++i)
-        if (s.instrs[i].xfer_in < 0 && s.instrs[i].xfer_out < 0) add_preds_of(itasks[i][0], i);
+        if (local_task[i] >= 0) add_preds_of(local_task[i], i);
     for (auto& t : tasks) {
         std::sort(t.preds.begin(), t.preds.end());
         t.preds.erase(std::unique(t.preds.begin(), t.preds.end()), t.preds.end());
@@ -127,7 +162,26 @@ ccl_status_t build_timeline(const ccl_schedule& s, int scheduler, Timeline* tl)
                 if (tasks[u].sp < 0 || tasks[u].sp >= sp) { ok = false; break; }
             if (ok) ready.push_back(t);
         }
-        if (ready.empty()) return fail(CCL_ERR_CYCLE, "dependency cycle among compiled instructions");
+        if (ready.empty()) {
+            if (split && log_level() >= 2) {
+                // the tasks left and the predecessors they still wait for
+                for (int t = 0; t < nt; ++t) {
+                    if (tasks[t].sp >= 0) continue;
+                    std::fprintf(stderr, "[ccl] task %d (%s %d>%d, instructions", t, t < nx ? "transfer" : "local",
+                                 tasks[t].a, tasks[t].b);
+                    for (int i = 0; i < ni; ++i)
+                        for (int u : itasks[i])
+                            if (u == t)
+                                std::fprintf(stderr, " %d:k%d:r%d:p%d", i, s.instrs[i].kind, s.instrs[i].rank,
+                                             s.instrs[i].position);
+                    std::fprintf(stderr, ") waits for");
+                    for (int u : tasks[t].preds)
+                        if (tasks[u].sp < 0) std::fprintf(stderr, " %d", u);
+                    std::fprintf(stderr, "\n");
+                }
+            }
+            return fail(CCL_ERR_CYCLE, "dependency cycle among compiled instructions");
+        }
         if (scheduler == CCL_SCHED_HPDS) {
             std::stable_sort(ready.begin(), ready.end(), [&](int a, int b) {
                 int ca = times[tasks[a].chunk], cb = times[tasks[b].chunk];
@@ -158,12 +212,30 @@ ccl_status_t build_timeline(const ccl_schedule& s, int scheduler, Timeline* tl)
     for (int x = 0; x < nx; ++x) tl->xfer_sp[x] = tasks[x].sp;
     tl->sp_lo.assign(ni, 1 << 30);
     tl->sp_hi.assign(ni, -1);
-    for (int i = 0; i < ni; ++i)
+    tl->sp_key.assign(ni, 0);
+    for (int i = 0; i < ni; ++i) {
         for (int t : itasks[i]) {
             tl->sp_lo[i] = std::min(tl->sp_lo[i], tasks[t].sp);
             tl->sp_hi[i] = std::max(tl->sp_hi[i], tasks[t].sp);
         }
+        // program order inside a threadblock: a dependent's tasks all come
+        // after the tasks it waits for, so this key never puts a consumer
+        // before its producer
+        tl->sp_key[i] = split ? tasks[effect_task(i)].sp : tl->sp_hi[i];
+    }
+    tl->split = split;
     return CCL_OK;
+}
+
+}  // namespace
+
+ccl_status_t build_timeline(const ccl_schedule& s, int scheduler, Timeline* tl)
+{
+    // whole instructions as the unit first; the finer model only when the
+    // coarse one sees a cycle through a fused receive-...-send
+    ccl_status_t st = timeline_pass(s, scheduler, false, tl);
+    if (st != CCL_ERR_CYCLE) return st;
+    return timeline_pass(s, scheduler, true, tl);
 }
 
 namespace {
@@ -179,7 +251,7 @@ void allocate_connection(const ccl_schedule& s, const Timeline& tl, TBList* tbs,
     for (int r = 0; r < s.nranks; ++r) {
         auto& v = byrank[r];
         std::sort(v.begin(), v.end(), [&](int a, int b) {
-            if (tl.sp_hi[a] != tl.sp_hi[b]) return tl.sp_hi[a] < tl.sp_hi[b];
+            if (tl.sp_key[a] != tl.sp_key[b]) return tl.sp_key[a] < tl.sp_key[b];
             return s.instrs[a].position < s.instrs[b].position;
         });
         struct C { int in, out, id; };
@@ -253,7 +325,7 @@ void pack_state_based(const ccl_schedule& s, const Timeline& tl, TBList* tbs, st
     tb_rank->clear();
     for (auto& g : groups) {
         std::sort(g.instrs.begin(), g.instrs.end(), [&](int a, int b) {
-            if (tl.sp_hi[a] != tl.sp_hi[b]) return tl.sp_hi[a] < tl.sp_hi[b];
+            if (tl.sp_key[a] != tl.sp_key[b]) return tl.sp_key[a] < tl.sp_key[b];
             return s.instrs[a].position < s.instrs[b].position;
         });
         tbs->push_back(g.instrs);
@@ -304,7 +376,7 @@ void balance_linkfree(const ccl_schedule& s, const Timeline& tl, TBList* tbs, st
         }
         for (auto& b : bins) {
             std::sort(b.instrs.begin(), b.instrs.end(), [&](int a, int c) {
-                if (tl.sp_hi[a] != tl.sp_hi[c]) return tl.sp_hi[a] < tl.sp_hi[c];
+                if (tl.sp_key[a] != tl.sp_key[c]) return tl.sp_key[a] < tl.sp_key[c];
                 if (s.instrs[a].position != s.instrs[c].position)
                     return s.instrs[a].position < s.instrs[c].position;
                 return a < c;
@@ -786,12 +858,6 @@ bool simulate_plan(const PlanImage& img, std::string* why)
 
 namespace {
 
-int log_level()
-{
-    const char* v = std::getenv("CCL_LOG_LEVEL");
-    return v ? std::atoi(v) : 0;
-}
-
 void dump_programs(const ccl_schedule& s, const Timeline& tl, const TBList& tbs, const std::vector<int>& tr, int m,
                    int order)
 {
@@ -869,8 +935,10 @@ ccl_schedule direct_transport(const ccl_schedule& s, int* ndirect)
     return d;
 }
 
-ccl_status_t build_plan(const ccl_schedule& s_in, int64_t ce, int32_t dtype, const ccl_plan_opts_t& o,
-                        PlanImage* img)
+namespace {
+
+ccl_status_t build_plan_one(const ccl_schedule& s_in, int64_t ce, int32_t dtype, const ccl_plan_opts_t& o,
+                            PlanImage* img)
 {
     if (ce <= 0) return fail(CCL_ERR_INVALID_ARG, "chunk_elems must be positive");
     if (dtype < CCL_F32 || dtype > CCL_I32) return fail(CCL_ERR_INVALID_ARG, "unknown dtype");
@@ -1037,7 +1105,39 @@ done:
         default: img->data_bytes_per_rank = in_b; img->busbw_factor = 0.0; break;
         }
     }
+    img->fuse = s.fuse;
     return CCL_OK;
+}
+
+}  // namespace
+
+// Fusion moves a send into the step that produces its data, so a fused
+// program keeps more transfers in flight on a link than its unfused form and
+// can need more FIFO slots, or a task order the timeline cannot build, where
+// the unfused program plans.  Both compute the same values, so a fused
+// schedule that cannot be planned with the given options is planned from the
+// same program compiled with less fusion (full -> copy receives unchained ->
+// none); the plan reports the mode it used.
+ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const ccl_plan_opts_t& o,
+                        PlanImage* img)
+{
+    ccl_status_t st = build_plan_one(s, ce, dtype, o, img);
+    if ((st != CCL_ERR_CYCLE && st != CCL_ERR_DEADLOCK) || s.fuse == CCL_FUSE_NONE) return st;
+    const std::string first = ccl_last_error_detail();
+    for (int mode : {CCL_FUSE_NOCHAIN, CCL_FUSE_NONE}) {
+        if (mode == s.fuse || (s.fuse == CCL_FUSE_NOCHAIN && mode != CCL_FUSE_NONE)) continue;
+        ccl_schedule less;
+        if (compile_program(s.ops.data(), (int)s.ops.size(), s.nranks, s.nchunks, mode, &less) != CCL_OK) break;
+        less.builtin = s.builtin;
+        less.group_size = s.group_size;
+        if (build_plan_one(less, ce, dtype, o, img) == CCL_OK) {
+            if (log_level() >= 1)
+                std::fprintf(stderr, "[ccl] fused schedule did not plan (%s); planned with fusion mode %d\n",
+                             first.c_str(), mode);
+            return CCL_OK;
+        }
+    }
+    return fail(st, first);
 }
 
 }  // namespace ccl

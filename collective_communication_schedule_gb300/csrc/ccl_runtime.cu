@@ -1087,6 +1087,7 @@ void fill_stats(const ccl::PlanImage& img, ccl_plan_stats_t* st)
     st->mb_window = img.mb_window;
     st->protocol = img.protocol;
     st->engine = img.engine;
+    st->fuse = img.fuse;
 }
 
 void free_plan(ccl_plan* p)

@@ -331,6 +331,11 @@ void ccl_plan_opts_default(ccl_plan_opts_t* o);
  * and the instruction tables.  Validates the threadblock programs by
  * simulating them (CCL_ERR_DEADLOCK) and checks that all threadblocks can be
  * co-resident (CCL_ERR_UNSUPPORTED).  dtype: ccl_dtype_t; op: CCL_SUM.
+ * A fused schedule whose instructions cannot be planned with these options
+ * (a fused send keeps more transfers in flight on a link than the FIFO
+ * holds, or no task order exists) is planned from the same program compiled
+ * with less fusion (copy receives unchained, then none): same results, more
+ * bytes; ccl_plan_stats reports the mode used.
  */
 ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtype, int32_t op,
                              const ccl_plan_opts_t* opts, ccl_plan_t* out);
@@ -403,6 +408,8 @@ typedef struct {
     int32_t mb_window;           /* micro-batch window actually used */
     int32_t protocol;            /* CCL_PROTO_* */
     int32_t engine;              /* CCL_ENGINE_* */
+    int32_t fuse;                /* CCL_FUSE_* mode of the instructions planned (less than the
+                                    schedule's when its fused form could not be planned) */
 } ccl_plan_stats_t;
 
 ccl_status_t ccl_plan_stats(ccl_plan_t p, ccl_plan_stats_t* st);

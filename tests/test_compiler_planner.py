@@ -199,6 +199,90 @@ def test_fusion_keeps_the_order_of_dependent_sends_on_a_link():
             assert np.array_equal(got[r], want[r])
 
 
+def test_send_is_not_chained_past_a_dependent_round_trip():
+    """Rank 0 receives out[0] (op 0), sends it to rank 2 (op 2), which sends
+    it back into rank 0's scratch (op 3); op 4 sends that scratch on to rank
+    1 and op 5 reduces rank 0's out[0] into the same range of rank 1.  Op
+    4's send depends on op 0 only through the round trip over rank 2; moving
+    op 5's send up into op 0's receive would put it ahead of op 4's on the
+    link 0 -> 1, although rank 1 takes op 4 first.  The compiler keeps op 4's
+    send ahead and the program plans in every fusion mode with the oracle's
+    result."""
+    ops = [(0, 1, 0, 0, 0, 1, 0, 1), (0, 0, 1, 0, 0, 2, 1, 1), (0, 0, 2, 1, 2, 1, 0, 1),
+           (0, 2, 1, 0, 0, 2, 0, 1), (0, 0, 2, 0, 1, 1, 1, 1), (1, 0, 1, 0, 1, 1, 1, 1)]
+    nch, R = (3, 3, 3), 3
+    ins = datagen.rank_inputs(4, "int", R, 12, I32)
+    want, _, _ = oracle.run(np.array(ops, np.int32), R, nch, 4, I32, ins)
+    for fuse in (ccl.FUSE_FULL, ccl.FUSE_NOCHAIN, ccl.FUSE_NONE):
+        s = ccl.Schedule.compile(ops, R, nch, fuse=fuse)
+        ins0 = [i for i in s.instrs() if i["rank"] == 0]
+        pos_of = {i["xfer_out"]: i["position"] for i in ins0 if i["xfer_out"] >= 0}
+        # transfers are numbered by their operation: op 4 -> 3, op 5 -> 4
+        assert pos_of[3] < pos_of[4]
+        for link_mode in (ccl.LINK_FIFO, ccl.LINK_DIRECT):
+            st = s.check(64, F32, link_mode=link_mode)
+            assert st.fuse == fuse
+        got = interpret_fused(s.instrs(), R, nch, 4, I32, ins)
+        for r in range(R):
+            assert np.array_equal(got[r], want[r])
+
+
+# Random programs (seeded fuzzing of the compiler) that the fused modes once
+# failed to plan although their unfused form planned: cycles of the
+# timeline through a fused receive-...-send or a copy-send whose send half
+# waits on the receiver side for a dependent of its buffer effect (first
+# three), and fused programs whose moved sends keep more transfers in flight
+# on a link than 4 FIFO slots hold (last two: planned from a less fused form).
+FUZZED = [
+    (5, 2, [(1, 3, 1, 0, 1, 2, 0, 2), (0, 0, 1, 0, 4, 1, 0, 1), (0, 0, 2, 0, 3, 1, 0, 2), (0, 1, 1, 1, 2, 1, 1, 1),
+            (1, 2, 2, 0, 4, 1, 1, 1), (0, 1, 0, 1, 0, 2, 0, 1), (0, 4, 1, 0, 0, 2, 0, 1), (1, 4, 1, 0, 4, 2, 0, 2),
+            (0, 3, 1, 1, 0, 2, 0, 1), (1, 3, 1, 1, 2, 2, 0, 1), (1, 0, 2, 0, 3, 1, 0, 2), (1, 3, 2, 0, 4, 2, 1, 1),
+            (0, 2, 0, 0, 4, 2, 0, 2), (0, 4, 1, 1, 3, 2, 0, 1), (0, 3, 2, 0, 2, 2, 1, 1)]),
+    (2, 2, [(1, 0, 0, 1, 0, 1, 1, 1), (0, 1, 2, 0, 1, 1, 0, 1), (1, 0, 0, 0, 1, 1, 1, 1), (0, 1, 1, 0, 0, 2, 0, 1),
+            (0, 1, 1, 0, 1, 2, 0, 1), (0, 1, 0, 1, 0, 2, 1, 1), (0, 0, 2, 0, 1, 1, 0, 2), (0, 0, 2, 0, 1, 1, 0, 2),
+            (1, 0, 0, 0, 0, 1, 0, 2), (1, 0, 0, 0, 0, 2, 0, 2), (0, 0, 2, 1, 0, 1, 0, 1), (0, 0, 0, 0, 1, 1, 0, 2),
+            (1, 1, 1, 0, 1, 2, 0, 2), (1, 0, 2, 0, 1, 2, 0, 2), (1, 1, 1, 0, 0, 2, 0, 2), (1, 1, 0, 0, 0, 2, 0, 2),
+            (0, 1, 1, 0, 1, 2, 0, 1), (0, 0, 0, 1, 0, 2, 1, 1), (0, 1, 0, 1, 0, 2, 1, 1)]),
+    (4, 3, [(0, 1, 0, 0, 1, 2, 0, 3), (0, 0, 2, 0, 3, 1, 0, 3), (0, 3, 2, 1, 2, 1, 2, 1), (0, 3, 1, 0, 1, 1, 0, 3),
+            (1, 2, 1, 1, 1, 1, 0, 2), (1, 1, 0, 0, 0, 1, 0, 3), (0, 3, 1, 0, 3, 2, 0, 3), (0, 1, 2, 0, 1, 1, 0, 2),
+            (0, 0, 2, 0, 1, 1, 0, 2), (0, 1, 2, 0, 0, 2, 0, 3), (0, 0, 2, 1, 2, 2, 1, 1), (0, 2, 0, 0, 0, 2, 0, 3),
+            (1, 0, 1, 0, 1, 2, 0, 2), (1, 3, 2, 1, 2, 2, 1, 1), (0, 0, 1, 1, 2, 2, 2, 1), (1, 3, 1, 0, 1, 2, 1, 2),
+            (0, 1, 2, 0, 3, 1, 0, 3), (1, 1, 2, 0, 3, 2, 0, 3), (1, 2, 0, 0, 2, 1, 0, 2), (1, 0, 1, 0, 3, 2, 0, 2),
+            (1, 1, 1, 0, 3, 1, 0, 3), (0, 3, 1, 2, 0, 1, 0, 1), (0, 2, 1, 1, 0, 2, 0, 2), (1, 3, 0, 1, 1, 2, 1, 1),
+            (1, 1, 0, 0, 0, 1, 1, 2), (0, 0, 2, 0, 0, 1, 1, 1), (0, 1, 0, 1, 2, 1, 1, 2), (0, 1, 0, 2, 3, 1, 0, 1),
+            (0, 0, 2, 0, 2, 2, 0, 3)]),
+    (2, 1, [(0, 1, 2, 0, 1, 1, 0, 1), (1, 0, 2, 0, 1, 1, 0, 1), (0, 0, 1, 0, 1, 1, 0, 1), (1, 0, 1, 0, 1, 1, 0, 1),
+            (1, 1, 2, 0, 0, 1, 0, 1), (0, 1, 0, 0, 1, 2, 0, 1), (1, 1, 2, 0, 0, 1, 0, 1), (1, 0, 2, 0, 1, 2, 0, 1),
+            (1, 0, 0, 0, 0, 2, 0, 1), (1, 1, 0, 0, 0, 1, 0, 1), (1, 1, 1, 0, 0, 2, 0, 1), (1, 1, 0, 0, 1, 2, 0, 1),
+            (0, 0, 0, 0, 0, 1, 0, 1), (0, 1, 0, 0, 0, 2, 0, 1), (1, 0, 2, 0, 1, 2, 0, 1), (1, 1, 0, 0, 1, 1, 0, 1),
+            (0, 0, 1, 0, 0, 2, 0, 1)]),
+    (2, 1, [(1, 1, 1, 0, 0, 1, 0, 1), (0, 0, 1, 0, 1, 1, 0, 1), (0, 1, 2, 0, 0, 2, 0, 1), (1, 0, 1, 0, 1, 2, 0, 1),
+            (0, 1, 2, 0, 1, 1, 0, 1), (0, 1, 0, 0, 1, 2, 0, 1), (1, 1, 0, 0, 0, 2, 0, 1), (0, 1, 0, 0, 1, 2, 0, 1),
+            (1, 1, 2, 0, 0, 1, 0, 1), (0, 0, 1, 0, 0, 2, 0, 1), (0, 0, 0, 0, 0, 1, 0, 1), (1, 0, 2, 0, 1, 1, 0, 1),
+            (1, 1, 2, 0, 0, 1, 0, 1), (1, 1, 2, 0, 0, 2, 0, 1), (1, 1, 1, 0, 0, 2, 0, 1), (1, 1, 1, 0, 0, 1, 0, 1),
+            (0, 1, 0, 0, 0, 1, 0, 1), (1, 0, 2, 0, 1, 1, 0, 1), (1, 1, 1, 0, 1, 2, 0, 1), (0, 0, 0, 0, 1, 2, 0, 1),
+            (1, 1, 2, 0, 0, 1, 0, 1)]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(FUZZED)))
+@pytest.mark.parametrize("fuse", [ccl.FUSE_FULL, ccl.FUSE_NOCHAIN])
+def test_fuzzed_programs_plan_in_fused_modes(case, fuse):
+    R, C, ops = FUZZED[case]
+    nch = (C, C, C)
+    s = ccl.Schedule.compile(ops, R, nch, fuse=fuse)
+    for link_mode in (ccl.LINK_FIFO, ccl.LINK_DIRECT):
+        st = s.check(64, F32, link_mode=link_mode)
+        assert st.fuse in (fuse, ccl.FUSE_NOCHAIN, ccl.FUSE_NONE)
+        if case < 3:
+            assert st.fuse == fuse      # planned as compiled (split timeline)
+    ins = datagen.rank_inputs(case, "int", R, C * 3, I32)
+    got = interpret_fused(s.instrs(), R, nch, 3, I32, ins)
+    want, _, _ = oracle.run(np.array(ops, np.int32), R, nch, 3, I32, ins)
+    for r in range(R):
+        assert np.array_equal(got[r], want[r])
+
+
 def random_program(seed, R=3, C=4, nops=40):
     rng = np.random.default_rng(seed)
     ops = []
@@ -329,16 +413,20 @@ def test_channel_scaling_gives_small_instructions_fewer_threadblocks():
     assert scaled.schedule_bytes == flat.schedule_bytes
 
 
-def test_task_order_ring_with_big_pieces_is_rejected_as_deadlock():
-    """Each ring step must run all its micro-batches before the next, while
-    the neighbour does the same: with a piece larger than the FIFO nobody can
-    finish; the simulator rejects the plan instead of launching it."""
+def test_task_order_ring_with_big_pieces_plans_unfused():
+    """Each fused ring step (receive, reduce, send on) must move a whole
+    piece while its neighbour does the same: with a piece larger than the
+    FIFO no fused step can finish, so the planner plans the program from its
+    unfused compilation (sends and receives in steps of their own), which
+    can; with micro-batches the fused form plans as compiled."""
     s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 4)
-    with pytest.raises(ccl.CclError) as e:
-        s.check(65536, F32, mb_order=ccl.MB_TASK, microbatches=1, slot_bytes=4096, fifo_slots=2)
-    assert e.value.code == 3
+    kw = dict(mb_order=ccl.MB_TASK, microbatches=1, slot_bytes=4096, fifo_slots=2)
+    st = s.check(65536, F32, **kw)
+    assert st.fuse == ccl.FUSE_NONE
+    unfused = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 4, 0, ccl.FLAG_NOFUSE).check(65536, F32, **kw)
+    assert st.schedule_bytes == unfused.schedule_bytes
     st = s.check(65536, F32, mb_order=ccl.MB_AUTO, slot_bytes=4096, fifo_slots=2)
-    assert st.microbatches > 1
+    assert st.microbatches > 1 and st.fuse == ccl.FUSE_FULL
 
 
 def test_plan_options_are_validated():
@@ -426,15 +514,17 @@ def test_microbatch_window_is_used_when_the_fifo_holds_it():
     assert (a.nsteps, a.schedule_bytes) == (b.nsteps, b.schedule_bytes)
 
 
-def test_microbatch_window_larger_than_the_fifo_is_rejected():
-    """A ring step that must send a whole window before its neighbour reads
-    any of it needs window + 1 slots per link."""
+def test_microbatch_window_larger_than_the_fifo_plans_unfused():
+    """A fused ring step that must send a whole window before its neighbour
+    reads any of it needs window + 1 slots per link: with fewer the fused
+    form cannot finish and the program is planned unfused (its receives and
+    sends in steps of their own), with enough slots it is planned fused."""
     s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 4)
-    with pytest.raises(ccl.CclError) as e:
-        s.check(65536, F32, microbatches=8, mb_window=8, fifo_slots=4, slot_bytes=32768, mb_order=ccl.MB_ALGO)
-    assert e.value.code == 3
-    st = s.check(65536, F32, microbatches=8, mb_window=8, fifo_slots=9, slot_bytes=32768, mb_order=ccl.MB_ALGO)
-    assert st.mb_window == 8
+    kw = dict(microbatches=8, mb_window=8, slot_bytes=32768, mb_order=ccl.MB_ALGO)
+    st = s.check(65536, F32, fifo_slots=4, **kw)
+    assert st.fuse == ccl.FUSE_NONE and st.mb_window == 8
+    st = s.check(65536, F32, fifo_slots=9, **kw)
+    assert st.mb_window == 8 and st.fuse == ccl.FUSE_FULL
 
 
 def test_ll_protocol_doubles_fifo_bytes_and_needs_16_byte_chunks():
