@@ -38,6 +38,7 @@ struct KParams {
     int S;
     int ns;                        // shared-memory stages of the bulk path (0: off)
     int ll;                        // FIFO slots hold LL lines (data + flag per 64 bits)
+    int stream_in;                 // inputs share no memory with outputs: streaming loads allowed
     char* bufs[3][CCL_MAX_RANKS];
 };
 

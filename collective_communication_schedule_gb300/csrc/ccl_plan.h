@@ -12,6 +12,9 @@ namespace ccl {
 // operand buffer classes (select cache hints in the kernel)
 enum : int32_t { OPB_NONE = -1 };
 
+// DStep / DRec flags
+enum : int32_t { STEP_NOPOST = 1, STEP_SRC_STREAM = 2, STEP_LOC_STREAM = 4 };
+
 // One channel instruction.  Offsets are element offsets of the channel
 // range inside the rank's buffer; a missing operand has buf = -1.
 struct DInstr {
@@ -39,7 +42,8 @@ struct DStep {
     int32_t dep_begin;  // waits: deps[dep_begin .. dep_begin + dep_count)
     int32_t dep_count;
     int32_t signal;     // counter to post after the step, or -1
-    int32_t flags;      // bit 0: do not post link flags (debug hook)
+    int32_t flags;      // bit 0: do not post link flags (debug hook); bits 1 / 2: the source /
+                        // local operand is an input buffer no instruction writes (streaming loads)
     int32_t drain;      // latest earlier step of the same threadblock whose tiles must be
                         // finished before this step starts (global step index), or -1
 };

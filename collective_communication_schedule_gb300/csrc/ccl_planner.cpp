@@ -600,6 +600,21 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     }
     img->schedule_bytes = sched_bytes;
 
+    // Inputs that some instruction writes (a program may write into an
+    // input buffer): their reads must see data other threadblocks wrote
+    // during the execution, so they take no streaming (L1-allocating) load
+    // and a bulk copy from them is ordered after generic-proxy writes; inputs
+    // nobody writes are read once and streamed.
+    std::vector<char> in_written(s.nranks, 0);
+    for (const Instr& I : s.instrs)
+        if (I.dst.valid() && I.dst.buf == CCL_BUF_IN) in_written[I.dst.rank] = 1;
+    auto stream_bits = [&](const DInstr& D) {
+        int32_t f = 0;
+        if (D.src_buf == CCL_BUF_IN && !in_written[D.src_rank]) f |= STEP_SRC_STREAM;
+        if (D.loc_buf == CCL_BUF_IN && !in_written[D.loc_rank]) f |= STEP_LOC_STREAM;
+        return f;
+    };
+
     // threadblock programs -> steps
     img->ntb = ntb;
     std::vector<std::vector<int>> step_of((size_t)ni * p, std::vector<int>(m, -1));
@@ -631,7 +646,7 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
                         st.dep_begin = 0;
                         st.dep_count = 0;
                         st.signal = -1;
-                        st.flags = 0;
+                        st.flags = stream_bits(D);
                         st.drain = -1;
                         step_of[ci][mb] = (int)img->steps.size();
                         img->steps.push_back(st);

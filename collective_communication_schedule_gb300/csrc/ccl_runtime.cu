@@ -442,7 +442,7 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
         const char* srcb = st.src_buf >= 0 ? P.bufs[st.src_buf][st.src_rank] + st.src_off * es : nullptr;
         const char* locb = st.loc_buf >= 0 ? P.bufs[st.loc_buf][st.loc_rank] + st.loc_off * es : nullptr;
         char* dstb = st.dst_buf >= 0 ? P.bufs[st.dst_buf][st.dst_rank] + st.dst_off * es : nullptr;
-        const bool post = !(st.flags & 1);
+        const bool post = !(st.flags & STEP_NOPOST);
         int ready_slots = si < cleared ? 1 : 0;   // slots whose flags were already seen ready
         for (long long k = 0; k < nslots; ++k) {
             const unsigned long long sin = base_in + st.seq_in + k;
@@ -486,10 +486,10 @@ __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
                     op.a_ll = P.ll;
                 } else {
                     op.a = srcb + off;
-                    op.as = st.src_buf == CCL_BUF_IN;
+                    op.as = (st.flags & STEP_SRC_STREAM) && P.stream_in;
                 }
                 op.b = locb ? locb + off : nullptr;
-                op.bs = st.loc_buf == CCL_BUF_IN;
+                op.bs = (st.flags & STEP_LOC_STREAM) && P.stream_in;
                 if (dstb) {
                     op.o1 = dstb + off;
                     op.o1s = st.dst_buf == CCL_BUF_OUT;
@@ -925,7 +925,7 @@ __global__ void __launch_bounds__(1024, 1) ccl_exec_seq_kernel(const __grid_cons
         const char* srcb = st.src_buf >= 0 ? P.bufs[st.src_buf][st.src_rank] + st.src_off * es : nullptr;
         const char* locb = st.loc_buf >= 0 ? P.bufs[st.loc_buf][st.loc_rank] + st.loc_off * es : nullptr;
         char* dstb = st.dst_buf >= 0 ? P.bufs[st.dst_buf][st.dst_rank] + st.dst_off * es : nullptr;
-        const bool post = !(st.flags & 1);
+        const bool post = !(st.flags & STEP_NOPOST);
         unsigned long long t_pub = 0, t_done = 0;
         for (long long k = 0; k < nslots; ++k) {
             const unsigned long long sin = base_in + st.seq_in + k;
@@ -948,10 +948,10 @@ __global__ void __launch_bounds__(1024, 1) ccl_exec_seq_kernel(const __grid_cons
                 a = slot_in;
             } else {
                 a = srcb + e0 * es;
-                as = st.src_buf == CCL_BUF_IN;
+                as = (st.flags & STEP_SRC_STREAM) && P.stream_in;
             }
             const char* b = locb ? locb + e0 * es : nullptr;
-            const bool bs = st.loc_buf == CCL_BUF_IN;
+            const bool bs = (st.flags & STEP_LOC_STREAM) && P.stream_in;
             char* o1;
             char* o2 = nullptr;
             bool o1s = false;
@@ -1418,6 +1418,18 @@ ccl_status_t ccl_execute(ccl_plan_t p, void* const* in_bufs, void* const* out_bu
         k.bufs[0][r] = static_cast<char*>(in_bufs[r]);
         k.bufs[1][r] = static_cast<char*>(out_bufs[r]);
     }
+    // an input that shares memory with an output (in-place AllReduce) is
+    // written during the execution: no streaming loads from inputs then
+    k.stream_in = 1;
+    {
+        const size_t ib = (size_t)p->img.in_elems * es, ob = (size_t)p->img.out_elems * es;
+        for (int r = 0; r < p->nranks && k.stream_in && ib; ++r)
+            for (int q = 0; q < p->nranks && ob; ++q) {
+                const char* a = static_cast<const char*>(in_bufs[r]);
+                const char* b = static_cast<const char*>(out_bufs[q]);
+                if (a < b + ob && b < a + ib) { k.stream_in = 0; break; }
+            }
+    }
     k.exec = p->exec;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p->img.ntb == 0) return CCL_OK;  // empty program: nothing to move
@@ -1636,8 +1648,8 @@ ccl_status_t ccl_plan_debug_drop_signal(ccl_plan_t p, int32_t tb, int32_t step)
     if (tb < 0 || tb >= img.ntb) return ccl::fail(CCL_ERR_INVALID_ARG, "threadblock out of range");
     int k = img.tb_begin[tb] + step;
     if (step < 0 || k >= img.tb_begin[tb + 1]) return ccl::fail(CCL_ERR_INVALID_ARG, "step out of range");
-    img.steps[k].flags |= 1;
-    img.recs[k].flags |= 1;
+    img.steps[k].flags |= ccl::STEP_NOPOST;
+    img.recs[k].flags |= ccl::STEP_NOPOST;
     ccl::DRec* dst = const_cast<ccl::DRec*>(p->kp.recs) + k;
     CUDA_TRY(cudaMemcpy(dst, &img.recs[k], sizeof(ccl::DRec), cudaMemcpyHostToDevice), "patch step");
     return CCL_OK;

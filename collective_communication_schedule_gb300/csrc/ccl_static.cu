@@ -45,6 +45,7 @@ struct StaticParams {
     unsigned char* scratch;   // device address of g_ring_scratch
     long long chunk_elems;
     int nranks, channels, dtype;
+    int stream_in;            // inputs share no memory with outputs: streaming loads allowed
 };
 
 __host__ __device__ inline void piece(long long n, long long ve, long long parts, long long k, long long* off,
@@ -127,13 +128,13 @@ __global__ void __launch_bounds__(512, 2) ring_static_kernel(const __grid_consta
                 const char* b = red ? P.in[r] + (base + e0) * es : nullptr;
                 char* o1 = has_dst ? P.out[r] + (base + e0) * es : slot_out;
                 char* o2 = has_dst && wr ? slot_out : nullptr;
-                const bool as = !rd;
+                const bool as = !rd && P.stream_in, bs = P.stream_in;
                 if (n > 0) {
                     switch (P.dtype) {
-                    case CCL_F32: move_dt<CCL_F32>(red, a, as, b, true, o1, has_dst, o2, n); break;
-                    case CCL_BF16: move_dt<CCL_BF16>(red, a, as, b, true, o1, has_dst, o2, n); break;
-                    case CCL_F16: move_dt<CCL_F16>(red, a, as, b, true, o1, has_dst, o2, n); break;
-                    default: move_dt<CCL_I32>(red, a, as, b, true, o1, has_dst, o2, n); break;
+                    case CCL_F32: move_dt<CCL_F32>(red, a, as, b, bs, o1, has_dst, o2, n); break;
+                    case CCL_BF16: move_dt<CCL_BF16>(red, a, as, b, bs, o1, has_dst, o2, n); break;
+                    case CCL_F16: move_dt<CCL_F16>(red, a, as, b, bs, o1, has_dst, o2, n); break;
+                    default: move_dt<CCL_I32>(red, a, as, b, bs, o1, has_dst, o2, n); break;
                     }
                 }
                 __syncthreads();
@@ -214,6 +215,16 @@ extern "C" ccl_status_t ccl_allreduce_ring_noalloc(void* const* in_bufs, void* c
         P.in[r] = static_cast<char*>(in_bufs[r]);
         P.out[r] = static_cast<char*>(out_bufs[r]);
     }
+    // an in-place call (an input shares memory with an output) takes no
+    // streaming loads from its inputs
+    P.stream_in = 1;
+    const size_t bytes = (size_t)nranks * chunk_elems * es;
+    for (int r = 0; r < nranks && P.stream_in; ++r)
+        for (int q = 0; q < nranks; ++q) {
+            const char* a = static_cast<const char*>(in_bufs[r]);
+            const char* b = static_cast<const char*>(out_bufs[q]);
+            if (a < b + bytes && b < a + bytes) { P.stream_in = 0; break; }
+        }
     P.scratch = scratch;
     P.chunk_elems = chunk_elems;
     P.nranks = nranks;

@@ -531,19 +531,23 @@ ccl_status_t ccl_tune(ccl_schedule_t s, int64_t chunk_elems, int32_t dtype,
  * min(8, 64 / nranks).
  *
  * Memory: the link FIFOs (4 slots of 32 KiB per link), flags and a status
- * word live in one file-scope device array of 8 MiB + 4160 bytes that every
- * GPU loading this library holds until the process exits.  nranks * channels
- * may not exceed 64 links (CCL_ERR_INVALID_ARG otherwise).  No cudaMalloc,
- * cudaFree or other allocating call is made, on the host or the device.
+ * word live in one file-scope device array of 8 MiB + 4160 bytes.  The
+ * device backs it when it loads the library's device code: with CUDA's
+ * default lazy module loading that is the first call of this function on
+ * each device (at library load only when modules load eagerly); from then
+ * on that GPU holds it until the process exits.  nranks * channels may not
+ * exceed 64 links (CCL_ERR_INVALID_ARG otherwise).  This call makes no
+ * cudaMalloc, cudaFree or other allocating call, on the host or the device.
  *
- * The first call on a device looks up the array's device address with
+ * The first call on a device also looks up the array's device address with
  * cudaGetSymbolAddress (once per device, that device current); make that
- * first call before any stream capture.  Every call clears the flags on
- * `stream` and launches one cooperative kernel; all calls share the array,
- * so calls whose executions overlap on the GPU (other streams, other host
- * threads) race and corrupt each other: serialise them.  A device wait that
- * runs out of time (2 s) leaves the outputs incomplete; this call does not
- * report it (use the plan API when that matters).
+ * first call before any stream capture, and outside any latency-critical
+ * step.  Every call clears the flags on `stream` and launches one
+ * cooperative kernel; all calls share the array, so calls whose executions
+ * overlap on the GPU (other streams, other host threads) race and corrupt
+ * each other: serialise them.  in_bufs[r] may equal out_bufs[r] (in place).
+ * A device wait that runs out of time (2 s) leaves the outputs incomplete;
+ * this call does not report it (use the plan API when that matters).
  * Returns CCL_OK, CCL_ERR_INVALID_ARG, CCL_ERR_UNSUPPORTED or CCL_ERR_CUDA.
  */
 ccl_status_t ccl_allreduce_ring_noalloc(void* const* in_bufs, void* const* out_bufs, int32_t nranks,

@@ -151,7 +151,7 @@ def test_config0_ring_allreduce_fp32_and_int32(ccl):
 
 
 @pytest.mark.parametrize("kbytes", [32, 64, 128, 256, 512, 1024, 2048, 3072])
-@pytest.mark.parametrize("channels", [1, 4])
+@pytest.mark.parametrize("channels", [1, 2, 3, 4])
 def test_config1_allgather_reducescatter_sweep(ccl, kbytes, channels):
     R = 8
     ce = kbytes * 1024 // 2 // R          # bf16 elements per chunk
@@ -324,3 +324,68 @@ def test_two_rank_allreduce_equals_torch_add(ccl, dtype):
     ref = (d_in[0].view(tdt) + d_in[1].view(tdt)).view(d_in[0].dtype)
     for r in range(2):
         assert torch.equal(d_out[r], ref), f"rank {r}"
+
+
+# A user program that writes input buffers: rank 0's input chunk 2 is
+# written by a copy from rank 1 and a reduction from rank 2 (threadblocks of
+# other ranks), then read by rank 0's threadblock for rank 3 and rank 1;
+# rank 0 also overwrites its own input chunk 1 and sends it on; rank 3 copies
+# its output back into its input and reduces that into rank 2.
+WRITES_INPUTS = [(0, 1, 0, 0, 0, 0, 2, 1), (1, 2, 0, 1, 0, 0, 2, 1), (0, 0, 0, 2, 3, 1, 0, 1),
+                 (1, 0, 0, 2, 1, 1, 1, 1), (0, 0, 0, 0, 0, 0, 1, 1), (0, 0, 0, 1, 2, 1, 0, 1),
+                 (0, 3, 1, 0, 3, 0, 0, 1), (1, 3, 0, 0, 2, 1, 1, 1), (1, 1, 0, 2, 3, 1, 1, 1)]
+
+
+@pytest.mark.parametrize("fuse", [True, False, 2])
+@pytest.mark.parametrize("opts", [dict(link_mode=0), dict(link_mode=1), dict(link_mode=1, bulk=1, tile_bytes=4096),
+                                  dict(link_mode=0, engine=1), dict(link_mode=1, tb_alloc=2, channels=3)])
+def test_program_that_writes_inputs_bitexact(ccl, fuse, opts):
+    """Inputs written during the execution by other ranks' threadblocks and
+    read afterwards on third ranks: the reads see the written values (no
+    streaming load of a stale line, bulk copies ordered after the writes);
+    outputs and the written inputs equal the oracle's."""
+    import torch
+    import datagen
+    import oracle
+    from gpu_helpers import to_device, empty_outputs, to_host
+    R, nch, ce = 4, (3, 2, 1), 6007
+    ops = np.array(WRITES_INPUTS, np.int32)
+    plan = ccl.Plan(ccl.Schedule.compile(WRITES_INPUTS, R, nch, fuse=fuse), ce, F32, slot_bytes=8192,
+                    **dict(dict(channels=2), **opts))
+    for rep in range(2):
+        ins = datagen.rank_inputs(40 + rep, "normal", R, nch[0] * ce, F32)
+        d_in = to_device(ins, F32)
+        d_out = empty_outputs(R, nch[1] * ce, F32)
+        plan.execute(d_in, d_out)
+        torch.cuda.synchronize()
+        plan.status()
+        want_out, _, want_in = oracle.run(ops, R, nch, ce, F32, ins)
+        assert_bitexact(to_host(d_out, F32), want_out)
+        assert_bitexact(to_host(d_in, F32), want_in)
+
+
+@pytest.mark.parametrize("fuse", [True, "nochain"])
+@pytest.mark.parametrize("opts", [dict(link_mode=0), dict(link_mode=1, tb_alloc=2), dict(link_mode=1, bulk=1),
+                                  dict(engine=1), dict(protocol=1)])
+@pytest.mark.parametrize("dtype", [F32, BF16])
+def test_inplace_ring_allreduce_bitexact(ccl, fuse, opts, dtype):
+    """In-place ring AllReduce (each rank's input is its output): the ring
+    program reads a rank's input chunk before it writes that output chunk,
+    so the result is the out-of-place oracle's, bit for bit."""
+    import torch
+    import datagen
+    import oracle
+    from gpu_helpers import oracle_program, to_device, to_host
+    R = 8
+    ce = 4096 if opts.get("protocol") else 3001
+    flags = ccl.FLAG_NOCHAIN_COPIES if fuse == "nochain" else 0
+    plan = ccl.Plan(ccl.Schedule.builtin(ccl.RING_ALLREDUCE, R, 0, flags), ce, dtype, channels=2, slot_bytes=8192,
+                    **opts)
+    ops, nch = oracle_program(0, R)
+    ins = datagen.rank_inputs(17, DIST[dtype], R, R * ce, dtype)
+    d = to_device(ins, dtype)
+    plan.execute(d, d)
+    torch.cuda.synchronize()
+    plan.status()
+    want, _, _ = oracle.run(ops, R, nch, ce, dtype, ins)
+    assert_bitexact(to_host(d, dtype), want)
