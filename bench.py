@@ -455,6 +455,33 @@ def run_gpu(args):
     return out
 
 
+ORACLE_PROGRAMS = {0: ("ring_allreduce", lambda R, G: (R,)), 1: ("ring_allgather", lambda R, G: (R,)),
+                   2: ("ring_reducescatter", lambda R, G: (R,)), 3: ("hier_allreduce", lambda R, G: (G, R // G)),
+                   4: ("alltoall_two_phase", lambda R, G: (G, R // G)), 5: ("alltonext", lambda R, G: (G, R // G))}
+# the plan option defaults the suite rows rely on (ccl_plan_opts_default):
+# direct transport unless a row asks for FIFOs
+DEFAULT_LINK_MODE = 1
+
+
+def oracle_program(kind, R, G):
+    """The oracle's own program of a built-in collective: (ops, nchunks)."""
+    from oracle import schedules as OS
+    nm, a = ORACLE_PROGRAMS[kind]
+    return OS.BUILTINS[nm](*a(R, G))
+
+
+def oracle_bytes(kind, R, G, dt, ce, opts):
+    """Schedule bytes and collective-minimum bytes of one execution of a
+    suite row, counted by the oracle from its own program (fused-instruction
+    semantics, the row's fusion mode and transport)."""
+    from oracle import bytes as OB
+    ops, nch = oracle_program(kind, R, G)
+    fuse = opts.get("fuse", True)
+    mode = "nochain" if fuse == "nochain" else ("full" if fuse else "none")
+    direct = opts.get("link_mode", DEFAULT_LINK_MODE) == 1
+    return (OB.schedule_bytes(ops, R, nch, ce, dt, mode, direct), OB.min_bytes(ops, R, nch, ce, dt))
+
+
 def _oracle_inputs(it):
     """Host copies of the inputs: the GPU arm's pinned buffers, or a fresh
     draw with the same recipe (reference arm)."""
@@ -475,15 +502,10 @@ def cpu_baseline(items, budget_s, divisor=None):
     three timed repetitions take about ``budget_s`` seconds."""
     import numpy as np
     import oracle
-    from oracle import schedules as OS
-    names = {0: ("ring_allreduce", lambda R, G: (R,)), 1: ("ring_allgather", lambda R, G: (R,)),
-             2: ("ring_reducescatter", lambda R, G: (R,)), 3: ("hier_allreduce", lambda R, G: (G, R // G)),
-             4: ("alltoall_two_phase", lambda R, G: (G, R // G)), 5: ("alltonext", lambda R, G: (G, R // G))}
     oracle.build()
     prepared = []
     for it in items:
-        nm, a = names[it["kind"]]
-        ops, nch = OS.BUILTINS[nm](*a(it["R"], it["G"]))
+        ops, nch = oracle_program(it["kind"], it["R"], it["G"])
         prepared.append((it, ops, nch, _oracle_inputs(it)))
 
     def one_pass(div, reps):
@@ -499,7 +521,8 @@ def cpu_baseline(items, budget_s, divisor=None):
                 oracle.run(ops, it["R"], nch, cols, it["dt"], cols_in)
                 ts.append(time.perf_counter() - t0)
             t_total += statistics.median(ts)
-            bytes_total += it["stats"].schedule_bytes * cols / ce
+            # the oracle's own count of the row's schedule bytes on the sample
+            bytes_total += oracle_bytes(it["kind"], it["R"], it["G"], it["dt"], cols, it["opts"])[0]
             sampled.append(f"{it['name']}:{cols}/{ce}")
         return t_total, bytes_total, sampled
 
@@ -522,14 +545,14 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return None
-    import collective_communication_schedule_gb300 as ccl  # only for byte counts via host planning
+    # nothing of the product runs here: programs, inputs and byte counts
+    # all come from the oracle and datagen
     items = []
     for name, kind, R, G, dt, chunk_bytes, dist, seed, opts in selected_suite(args):
         ce = chunk_bytes // ESIZE[dt]
-        sch, popts = schedule_and_opts(ccl, kind, R, G, opts)
-        st = sch.check(ce, dt, **popts)
-        nin = sch.info().nchunks[0] * ce
-        items.append(dict(name=name, kind=kind, R=R, G=G, dt=dt, ce=ce, stats=st, dist=dist, seed=seed, nin=nin))
+        _, nch = oracle_program(kind, R, G)
+        items.append(dict(name=name, kind=kind, R=R, G=G, dt=dt, ce=ce, dist=dist, seed=seed, nin=nch[0] * ce,
+                          opts=opts))
     cb = None
     for _ in range(args.warmup + args.steps):
         cb = cpu_baseline(items, args.cpu_seconds, divisor=1024)

@@ -1,0 +1,157 @@
+"""The oracle's byte accounting (``oracle.bytes``), pinned to closed forms
+derived by hand from the collective programs and the fused-instruction costs
+(copy 2, send 2, recv 2, reduce / rrc / rcs / rrs / copy-send 3, rrcs 4,
+recv-send 2 bytes per element byte), then compared with the product's own
+count for every benchmark row."""
+import numpy as np
+import pytest
+
+from oracle import bytes as OB
+from oracle import schedules as OS
+
+F32, BF16, F16, I32 = 0, 1, 2, 3
+
+
+@pytest.mark.parametrize("R", [2, 3, 5, 8])
+def test_ring_allreduce_closed_forms(R):
+    """Per rank, n = chunk bytes.  Full fusion: send 2 + (R-2) rrs 3 +
+    rrcs 4 + (R-2) rcs 3 + recv 2 = 6R - 4.  Copy receives unchained: the
+    all-gather is R-1 receives and R-2 sends of 2: 3R + 4R - 6 = 7R - 6;
+    with direct transport the R-2 send/receive pairs between plain ends are
+    copies of 2: 3R + 2 + 2(R-2) = 5R - 2.  Unfused: R local copies 2,
+    R-1 reduce transfers 2 + 3, R-1 copy transfers 2 + 2 = 11R - 9."""
+    ops, nch = OS.ring_allreduce(R)
+    ce, es = 1000, 4
+    n = ce * es
+    assert OB.schedule_bytes(ops, R, nch, ce, F32, "full", direct=False) == R * (6 * R - 4) * n
+    assert OB.schedule_bytes(ops, R, nch, ce, F32, "full", direct=True) == R * (6 * R - 4) * n
+    assert OB.schedule_bytes(ops, R, nch, ce, F32, "nochain", direct=False) == R * (7 * R - 6) * n
+    assert OB.schedule_bytes(ops, R, nch, ce, F32, "nochain", direct=True) == R * (5 * R - 2) * n
+    assert OB.schedule_bytes(ops, R, nch, ce, F32, "none", direct=False) == R * (11 * R - 9) * n
+    # per rank N(6 - 4/R) with N = R n bytes per rank
+    assert OB.schedule_bytes(ops, R, nch, ce, F32) * R == R * R * n * (6 * R - 4)
+
+
+@pytest.mark.parametrize("R", [2, 4, 8])
+def test_allgather_and_reducescatter_closed_forms(R):
+    """Per rank, n = S / R: AllGather copy-send 3 + (R-2) rcs 3 + recv 2;
+    ReduceScatter send 2 + (R-2) rrs 3 + rrc 3; both 3R - 1.  AllGather
+    unfused with direct copies: the local copy and R-1 hops of 2 = 2R."""
+    for prog in (OS.ring_allgather, OS.ring_reducescatter):
+        ops, nch = prog(R)
+        assert OB.schedule_bytes(ops, R, nch, 512, BF16, "full", direct=False) == R * (3 * R - 1) * 1024
+    ops, nch = OS.ring_allgather(R)
+    assert OB.schedule_bytes(ops, R, nch, 512, BF16, "none", direct=True) == R * 2 * R * 1024
+
+
+def test_hierarchical_allreduce_closed_form():
+    """G = 8, 2 groups, M = 16 n per rank, slices of 2 chunks.  Intra
+    reduce-scatter: send 2x2 + 6 rrs 3x2 + rrc 3x2 = 46 n.  The inter-group
+    step works on single chunks, which partly overlap the slices, so nothing
+    fuses across it: send 2 + rrcs 4 (the reduced chunk is sent back) +
+    recv 2 = 8 n.  Intra all-gather: send 2x2 + 6 rcs 3x2 + recv 2x2 = 44 n.
+    98 n = 6.125 M."""
+    ops, nch = OS.hier_allreduce(8, 2)
+    n = 4096 * 4
+    assert OB.schedule_bytes(ops, 16, nch, 4096, F32, "full", direct=False) == 16 * 98 * n
+
+
+def test_two_phase_alltoall_closed_form():
+    """R = 32 = 4 x 8, one chunk per block: per rank the own block (local
+    copy 2), 7 in-group blocks (transfers 4), 24 blocks to aggregators -- 3
+    of them the rank itself (local copies 2), 21 transfers 4 -- and 24
+    blocks of phase 2 (transfers 4): 2 + 28 + 6 + 84 + 96 = 216 blocks.
+    With direct transport every transfer is a copy of 2: 2 (sent + copied)
+    = 2 * (7 + 21 + 24 + 1 + 3) = 112."""
+    ops, nch = OS.alltoall_two_phase(8, 4)
+    n = 1024 * 2
+    assert OB.schedule_bytes(ops, 32, nch, 1024, F16, "full", direct=False) == 32 * 216 * n
+    assert OB.schedule_bytes(ops, 32, nch, 1024, F16, "full", direct=True) == 32 * 112 * n
+
+
+def test_alltonext_closed_forms():
+    """R = 24 = 3 x 8, 8 parts of n per rank.  21 in-group pairs of 8 parts:
+    transfers of 4 (FIFO) or copies of 2 (direct, unfused).  The 2 pairs
+    that leave a group: parts 0 and 7 take 2 hops, parts 1..6 take 3; fused
+    through FIFOs a part costs send 2 + a recv-send 2 per relay + recv 2
+    (6 and 8), unfused with direct copies 2 per hop (4 and 6)."""
+    ops, nch = OS.alltonext(8, 3)
+    n = 1000 * 4
+    assert OB.schedule_bytes(ops, 24, nch, 1000, F32, "full", direct=False) == (21 * 8 * 4 + 2 * (2 * 6 + 6 * 8)) * n
+    assert OB.schedule_bytes(ops, 24, nch, 1000, F32, "none", direct=True) == (21 * 8 * 2 + 2 * (2 * 4 + 6 * 6)) * n
+
+
+def test_min_bytes_closed_forms():
+    """Every input chunk a program reads, read once, and every output chunk
+    it writes, written once: AllReduce R (R + R) chunks, AllGather R (1 +
+    R), AllToNext without wrap 23 senders and 23 receivers of 8 chunks."""
+    ops, nch = OS.ring_allreduce(8)
+    assert OB.min_bytes(ops, 8, nch, 100, F32) == 2 * 8 * 8 * 100 * 4
+    ops, nch = OS.ring_allgather(8)
+    assert OB.min_bytes(ops, 8, nch, 100, BF16) == (8 * 1 + 8 * 8) * 100 * 2
+    ops, nch = OS.alltonext(8, 3)          # rank 23 sends nothing, rank 0 receives nothing
+    assert OB.min_bytes(ops, 24, nch, 100, F32) == 2 * 23 * 8 * 100 * 4
+
+
+def test_planted_mistake_in_a_factor_is_caught():
+    """A wrong cost for one fused kind (a receive-reduce-copy-send counted as
+    3 instead of 4) breaks the ring closed form."""
+    ops, nch = OS.ring_allreduce(8)
+    saved = OB.FACTOR["rrcs"]
+    try:
+        OB.FACTOR["rrcs"] = 3
+        assert OB.schedule_bytes(ops, 8, nch, 10, F32, "full", direct=False) != 8 * (6 * 8 - 4) * 40
+    finally:
+        OB.FACTOR["rrcs"] = saved
+
+
+# ------------------------------------------------- against the product count
+
+ccl = pytest.importorskip("collective_communication_schedule_gb300")
+
+KIND_PROGRAM = {0: lambda R, G: OS.ring_allreduce(R), 1: lambda R, G: OS.ring_allgather(R),
+                2: lambda R, G: OS.ring_reducescatter(R), 3: lambda R, G: OS.hier_allreduce(G, R // G),
+                4: lambda R, G: OS.alltoall_two_phase(G, R // G), 5: lambda R, G: OS.alltonext(G, R // G)}
+
+
+def _fuse_name(flags):
+    return "none" if flags & ccl.FLAG_NOFUSE else ("nochain" if flags & ccl.FLAG_NOCHAIN_COPIES else "full")
+
+
+def test_oracle_count_equals_the_product_count_for_every_benchmark_row():
+    import bench
+
+    class A:
+        only, scale = "", 1.0
+    assert bench.DEFAULT_LINK_MODE == ccl.default_opts().link_mode
+    for name, kind, R, G, dt, cb, dist, seed, opts in bench.selected_suite(A):
+        sched, popts = bench.schedule_and_opts(ccl, kind, R, G, opts)
+        ce = cb // bench.ESIZE[dt]
+        st = sched.check(ce, dt, **popts)
+        # the count the CPU baseline and the reference arm use
+        assert bench.oracle_bytes(kind, R, G, dt, ce, opts) == (st.schedule_bytes, st.min_bytes), name
+        fl = {"nochain": ccl.FLAG_NOCHAIN_COPIES, False: ccl.FLAG_NOFUSE}.get(opts.get("fuse", True), 0)
+        ops, nch = KIND_PROGRAM[kind](R, G)
+        direct = popts.get("link_mode", ccl.default_opts().link_mode) == ccl.LINK_DIRECT
+        assert OB.schedule_bytes(ops, R, nch, ce, dt, _fuse_name(fl), direct) == st.schedule_bytes, name
+
+
+@pytest.mark.parametrize("kind,R,G", [(0, 8, 0), (0, 3, 0), (1, 8, 0), (2, 5, 0), (3, 16, 8), (3, 4, 2),
+                                      (4, 32, 8), (4, 8, 4), (5, 24, 8), (5, 6, 3)])
+@pytest.mark.parametrize("flags", [0, 2, 4])
+@pytest.mark.parametrize("link_mode", [0, 1])
+def test_oracle_count_equals_the_product_count_for_builtins(kind, R, G, flags, link_mode):
+    ops, nch = KIND_PROGRAM[kind](R, G)
+    st = ccl.Schedule.builtin(kind, R, G, flags).check(333, F32, link_mode=link_mode)
+    assert OB.schedule_bytes(ops, R, nch, 333, F32, _fuse_name(flags), link_mode == 1) == st.schedule_bytes
+
+
+def test_oracle_fused_kinds_equal_the_compiled_kinds():
+    """Instruction by instruction: the fused kinds the oracle derives for the
+    benchmark collectives are the kinds the compiler emits."""
+    for kind, R, G in [(0, 8, 0), (1, 8, 0), (2, 8, 0), (3, 16, 8), (4, 32, 8), (5, 24, 8)]:
+        ops, _ = KIND_PROGRAM[kind](R, G)
+        for flags in (0, 2, 4):
+            mine = sorted(k for k, *_ in OB.fused_instructions(ops, R, _fuse_name(flags)))
+            theirs = sorted(ccl.KIND_NAMES[i["kind"]] for i in ccl.Schedule.builtin(kind, R, G, flags).instrs())
+            assert mine == theirs, (kind, flags)
