@@ -411,6 +411,7 @@ def run_gpu(args):
     for it in items:
         it["plan"].status()
     e2e_ms = e0.elapsed_time(e1) / Ke
+    link = host_link(torch, items, stream)
 
     out = {
         "metric": METRIC,
@@ -441,7 +442,12 @@ def run_gpu(args):
                      else "fallback 6.8 TB/s"},
         "e2e": {"value": round(sched_bytes / (e2e_ms * 1e6), 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3), "steps": Ke,
-                "mode": args.e2e_mode, "streams": len(e2e_streams)},
+                "mode": args.e2e_mode, "streams": len(e2e_streams),
+                # the same host buffers copied alone (no kernels): the floor of
+                # ms_per_step is max(h2d, d2h) bytes / these rates
+                "host_link_gbs": link,
+                "floor_ms_from_link": round(max(h2d, d2h) / (link["both_each_way"] * 1e6), 3)
+                if link.get("both_each_way") else None},
         # bytes every collective must move at least (each input read once,
         # each output written once) per second of the step: unlike `value`,
         # independent of the schedule's transport and fusion choices
@@ -450,8 +456,169 @@ def run_gpu(args):
         "clocks": clk,
         "per_collective": per,
     }
+    if not args.no_sweep:
+        out["sweep"] = run_sweep(ccl, torch, datagen, args, peak)
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(items, args.cpu_seconds)
+    return out
+
+
+def host_link(torch, items, stream):
+    """Pinned host <-> device copy rates of the step's own buffers, with no
+    kernel: every input to the device alone, every output to the host alone,
+    and both directions at once on two streams (GB/s each way)."""
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    h2d = sum(t.numel() * t.element_size() for it in items for t in it["h_in"])
+    d2h = sum(t.numel() * t.element_size() for it in items for t in it["d_out"])
+    if not h2d or not d2h:
+        return {}
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        up.wait_event(a)
+        down.wait_event(a)
+        fn()
+        for s in (up, down):
+            e = torch.cuda.Event()
+            e.record(s)
+            stream.wait_event(e)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    def copy_in():
+        with torch.cuda.stream(up):
+            for it in items:
+                for d, h in zip(it["d_in"], it["h_in"]):
+                    d.copy_(h, non_blocking=True)
+
+    def copy_out():
+        with torch.cuda.stream(down):
+            for it in items:
+                for h, d in zip(it["h_out"], it["d_out"]):
+                    h.copy_(d, non_blocking=True)
+
+    def both():
+        copy_in()
+        copy_out()
+    t_in, t_out, t_both = timed(copy_in), timed(copy_out), timed(both)
+    return {"h2d": round(h2d / (t_in * 1e6), 1), "d2h": round(d2h / (t_out * 1e6), 1),
+            "both_each_way": round(max(h2d, d2h) / (t_both * 1e6), 1)}
+
+
+# BASELINE workload 1: ring AllGather and ReduceScatter, 8 ranks, bf16, per-rank
+# buffer (AllGather output, ReduceScatter input) 32 KiB .. 2 MiB and 3 MiB,
+# channels 1..4, normal(0,1) seed 1.  Workload 0's int32 copy: ring AllReduce
+# 8 x 1 MiB, integers in [-1000, 1000], seed 0.
+SWEEP_KIB = [32, 64, 128, 256, 512, 1024, 2048, 3072]
+TABLE_DIR = os.path.join(ROOT, "collective_communication_schedule_gb300", "tables")
+
+
+def tuned_table(ccl, torch, datagen, kind, args):
+    """The per-size tuning table of a sweep collective: the committed file
+    when there is one (and --retune is not given), else tuned now (outside
+    any timed region) and written to gpurun_out/ when that folder exists."""
+    name = {1: "ring_allgather", 2: "ring_reducescatter"}[kind]
+    path = os.path.join(TABLE_DIR, f"{name}_r8_bf16.json")
+    if os.path.exists(path) and not args.retune:
+        rows, _ = ccl.read_tune_table(path)
+        return rows, os.path.relpath(path, ROOT)
+    R = 8
+    sizes = [kib * 1024 // 2 // R for kib in SWEEP_KIB]
+    s = ccl.Schedule.builtin(kind, R)
+    nin = max(sizes) * (1 if kind == 1 else R)
+    ins = [torch.from_numpy(a.view("int16")).cuda() for a in datagen.rank_inputs(1, "normal", R, nin, 1)]
+    outs = [torch.empty(max(sizes) * (R if kind == 1 else 1), dtype=torch.int16, device="cuda") for _ in range(R)]
+    rows = ccl.tune_table(s, 1, sizes, ins, outs, max_rounds=2, reps=5, max_channels=4)
+    out_dir = os.path.join(ROOT, "gpurun_out")
+    if os.path.isdir(out_dir):
+        ccl.write_tune_table(rows, 1, os.path.join(out_dir, os.path.basename(path)),
+                             note=f"{name} R=8 bf16, channels <= 4, tuned on {torch.cuda.get_device_name()}")
+    return rows, "tuned in this run"
+
+
+def run_sweep(ccl, torch, datagen, args, peak):
+    """Workload 1's sweep (every size x channels 1-4, AllGather and
+    ReduceScatter) and workload 0's int32 copy, each with its tuned
+    configuration; median of 20 executions with warm L2 and of 10 with L2
+    flushed before each (flush outside the events), threadblock idle
+    fractions from one instrumented execution.  Measured after the timed
+    region of the step."""
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device="cuda")
+    R = 8
+
+    def measure(sched, ce, dt, opts, d_in, d_out):
+        plan = ccl.Plan(sched, ce, dt, opts=opts)
+        st = plan.stats()
+        warm = _time_plan(torch, plan, d_in, d_out, stream, reps=20, warm=3)
+        ts = []
+        for _ in range(10):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            plan.execute(d_in, d_out, stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        plan.status()
+        cold = statistics.median(ts)
+        del plan
+        o2 = ccl.PlanOpts.from_buffer_copy(opts)
+        o2.instrument = 1
+        inst = ccl.Plan(sched, ce, dt, opts=o2)
+        inst.execute(d_in, d_out, stream)
+        torch.cuda.synchronize()
+        inst.status()
+        tl = inst.timeline()
+        del inst
+        algbw = st.data_bytes_per_rank / (cold * 1e6)
+        return {"us": round(cold * 1e3, 2), "us_warm_l2": round(warm * 1e3, 2),
+                "schedule_gbs": round(st.schedule_bytes / (cold * 1e6), 1),
+                "frac_of_peak": round(st.schedule_bytes / (cold * 1e6) / peak, 4),
+                "algbw_gbs": round(algbw, 2), "busbw_gbs": round(algbw * st.busbw_factor, 2),
+                "threadblocks": st.nthreadblocks, "threadblocks_connection": st.nthreadblocks_connection,
+                "mean_idle": round(tl["mean_idle"], 3), "max_idle": round(tl["max_idle"], 3),
+                "engine": st.engine, "nthreads": st.nthreads, "slot_bytes": st.slot_bytes,
+                "link_mode": opts.link_mode, "tb_alloc": opts.tb_alloc}
+
+    out = {"note": "per-rank buffer S: AllGather output, ReduceScatter input; us = median with L2 flushed", "rows": []}
+    for kind, kname in ((1, "allgather"), (2, "reducescatter")):
+        rows, src = tuned_table(ccl, torch, datagen, kind, args)
+        out[f"{kname}_table"] = src
+        sched = ccl.Schedule.builtin(kind, R)
+        for kib in SWEEP_KIB:
+            ce = kib * 1024 // 2 // R
+            nin = ce * (1 if kind == 1 else R)
+            nout = ce * (R if kind == 1 else 1)
+            d_in = [torch.from_numpy(a.view("int16")).cuda() for a in datagen.rank_inputs(1, "normal", R, nin, 1)]
+            d_out = [torch.empty(nout, dtype=torch.int16, device="cuda") for _ in range(R)]
+            base = ccl.lookup_tune_table(rows, ce)
+            for ch in (1, 2, 3, 4):
+                o = ccl.PlanOpts.from_buffer_copy(base)
+                o.channels = ch
+                rec = {"collective": kname, "dtype": "bf16", "per_rank_kib": kib, "channels": ch}
+                try:
+                    rec.update(measure(sched, ce, 1, o, d_in, d_out))
+                except ccl.CclError as e:
+                    rec["error"] = str(e)[:100]
+                out["rows"].append(rec)
+    # workload 0's int32 copy: the ring AllReduce row's options
+    row = [r for r in SUITE if r[0] == "ar_1m"][0]
+    sched, popts = schedule_and_opts(ccl, 0, R, 0, row[8])
+    ce = 1 * MiB // 4 // R
+    d_in = [torch.from_numpy(a).cuda() for a in datagen.rank_inputs(0, "int", R, R * ce, 3)]
+    d_out = [torch.empty(R * ce, dtype=torch.int32, device="cuda") for _ in range(R)]
+    o = ccl.default_opts()
+    for k, v in popts.items():
+        setattr(o, k, v)
+    rec = {"collective": "allreduce", "dtype": "i32", "per_rank_kib": 1024, "channels": o.channels}
+    rec.update(measure(sched, ce, 3, o, d_in, d_out))
+    out["rows"].append(rec)
+    del flush
     return out
 
 
@@ -830,7 +997,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--e2e-mode", default="pipeline", choices=["pipeline", "streams"],
                     help="pipeline: ccl_execute_host_async over copy-in / compute / copy-out streams; "
                          "streams: ccl_execute_host rotating over --e2e-streams")
@@ -839,6 +1006,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip idle fractions and L2-flushed timings")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the AllGather / ReduceScatter size sweep")
+    ap.add_argument("--retune", action="store_true", help="tune the sweep's tables now instead of reading them")
     ap.add_argument("--only", default="", help="comma-separated subset of the suite (profiling)")
     ap.add_argument("--scale", type=float, default=1.0, help="chunk size factor (profiling)")
     ap.add_argument("--ablation", action="store_true", help="scheduler x threadblock allocation table")

@@ -96,12 +96,17 @@ class StepInfo(ctypes.Structure):
 
 
 class TuneOpts(ctypes.Structure):
-    _fields_ = [("max_rounds", ctypes.c_int32), ("reps", ctypes.c_int32), ("min_gain", ctypes.c_double)]
+    _fields_ = [("max_rounds", ctypes.c_int32), ("reps", ctypes.c_int32), ("min_gain", ctypes.c_double),
+                ("max_channels", ctypes.c_int32)]
 
 
 class TuneReport(ctypes.Structure):
     _fields_ = [("probes", ctypes.c_int32), ("best_us", ctypes.c_double), ("best_gbs", ctypes.c_double),
                 ("default_us", ctypes.c_double)]
+
+
+class TuneRow(ctypes.Structure):
+    _fields_ = [("chunk_elems", ctypes.c_int64), ("best", PlanOpts), ("report", TuneReport)]
 
 
 PROBE_FN = ctypes.CFUNCTYPE(ctypes.c_double, ctypes.c_void_p, ctypes.POINTER(PlanOpts))
@@ -139,6 +144,14 @@ def _load():
         "ccl_allreduce_ring_noalloc": [ctypes.POINTER(P), ctypes.POINTER(P), I32_, I64_, I32_, I32_, P],
         "ccl_tune": [P, I64_, I32_, ctypes.POINTER(P), ctypes.POINTER(P), P, ctypes.POINTER(TuneOpts),
                      ctypes.POINTER(PlanOpts), ctypes.POINTER(PlanOpts), ctypes.POINTER(TuneReport)],
+        "ccl_tune_table": [P, I32_, ctypes.POINTER(ctypes.c_int64), I32_, ctypes.POINTER(P), ctypes.POINTER(P), P,
+                           ctypes.POINTER(TuneOpts), ctypes.POINTER(PlanOpts), ctypes.POINTER(TuneRow)],
+        "ccl_tune_table_write_json": [ctypes.POINTER(TuneRow), I32_, I32_, ctypes.c_char_p, ctypes.c_char_p],
+        "ccl_tune_table_read_json": [ctypes.c_char_p, ctypes.POINTER(TuneRow), I32_, ctypes.POINTER(ctypes.c_int32),
+                                     ctypes.POINTER(ctypes.c_int32)],
+        "ccl_tune_table_lookup": [ctypes.POINTER(TuneRow), I32_, I64_, ctypes.POINTER(PlanOpts)],
+        "ccl_schedule_write_json": [P, ctypes.c_char_p],
+        "ccl_schedule_read_json": [ctypes.c_char_p, ctypes.POINTER(P)],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -273,6 +286,17 @@ class Schedule:
         _check(lib.ccl_schedule_timeline(self._h, scheduler, arr, ctypes.byref(nsub)))
         return list(arr[:n]), nsub.value
 
+    def save(self, path):
+        """Write the schedule as JSON (``ccl_schedule_write_json``)."""
+        _check(lib.ccl_schedule_write_json(self._h, os.fsencode(path)))
+
+    @classmethod
+    def load(cls, path):
+        """Read a schedule written by ``save`` (``ccl_schedule_read_json``)."""
+        h = ctypes.c_void_p()
+        _check(lib.ccl_schedule_read_json(os.fsencode(path), ctypes.byref(h)))
+        return cls(h.value)
+
     def check(self, chunk_elems, dtype, opts: PlanOpts | None = None, **kw) -> PlanStats:
         """Plan on the host only (deadlock simulation included, no GPU)."""
         o = _with_opts(opts, kw)
@@ -369,14 +393,48 @@ class Plan:
 
 
 def tune(schedule: Schedule, chunk_elems, dtype, inputs, outputs, stream=None, start: PlanOpts | None = None,
-         max_rounds=3, reps=5, min_gain=0.01):
+         max_rounds=3, reps=5, min_gain=0.01, max_channels=0):
     best = PlanOpts()
     rep = TuneReport()
-    to = TuneOpts(max_rounds, reps, min_gain)
+    to = TuneOpts(max_rounds, reps, min_gain, max_channels)
     _check(lib.ccl_tune(schedule._h, chunk_elems, dtype, _ptrs(inputs), _ptrs(outputs), _stream(stream),
                         ctypes.byref(to), ctypes.byref(start) if start is not None else None, ctypes.byref(best),
                         ctypes.byref(rep)))
     return best, rep
+
+
+def tune_table(schedule: Schedule, dtype, sizes, inputs, outputs, stream=None, start: PlanOpts | None = None,
+               max_rounds=3, reps=5, min_gain=0.01, max_channels=0):
+    """Per-size tuning (``ccl_tune_table``): a list of TuneRow, one per
+    chunk size in ``sizes``; the buffers hold the largest size."""
+    n = len(sizes)
+    arr = (ctypes.c_int64 * n)(*[int(x) for x in sizes])
+    rows = (TuneRow * n)()
+    to = TuneOpts(max_rounds, reps, min_gain, max_channels)
+    _check(lib.ccl_tune_table(schedule._h, dtype, arr, n, _ptrs(inputs), _ptrs(outputs), _stream(stream),
+                              ctypes.byref(to), ctypes.byref(start) if start is not None else None, rows))
+    return list(rows)
+
+
+def write_tune_table(rows, dtype, path, note=""):
+    arr = (TuneRow * max(1, len(rows)))(*rows)
+    _check(lib.ccl_tune_table_write_json(arr, len(rows), dtype, note.encode(), os.fsencode(path)))
+
+
+def read_tune_table(path):
+    """(rows, dtype) of a table file."""
+    n, dt = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib.ccl_tune_table_read_json(os.fsencode(path), None, 0, ctypes.byref(n), ctypes.byref(dt)))
+    rows = (TuneRow * max(1, n.value))()
+    _check(lib.ccl_tune_table_read_json(os.fsencode(path), rows, n.value, ctypes.byref(n), ctypes.byref(dt)))
+    return list(rows[:n.value]), dt.value
+
+
+def lookup_tune_table(rows, chunk_elems) -> PlanOpts:
+    arr = (TuneRow * max(1, len(rows)))(*rows)
+    o = PlanOpts()
+    _check(lib.ccl_tune_table_lookup(arr, len(rows), chunk_elems, ctypes.byref(o)))
+    return o
 
 
 def allreduce_ring_noalloc(inputs, outputs, chunk_elems, dtype, channels=0, stream=None):
@@ -391,7 +449,7 @@ def tune_search(probe, start: PlanOpts | None = None, max_rounds=3, min_gain=0.0
     best = PlanOpts()
     bw = ctypes.c_double()
     n = ctypes.c_int32()
-    to = TuneOpts(max_rounds, 1, min_gain)
+    to = TuneOpts(max_rounds, 1, min_gain, 0)
     _check(lib.ccl_tune_search(ctypes.byref(start) if start is not None else None, ctypes.byref(to), cb, None,
                                ctypes.byref(best), ctypes.byref(bw), ctypes.byref(n)))
     return best, bw.value, n.value

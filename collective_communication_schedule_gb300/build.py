@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 
 SOURCES = ["ccl_runtime.cu", "ccl_static.cu", "ccl_compiler.cpp", "ccl_builtin.cpp", "ccl_planner.cpp",
-           "ccl_tuner.cpp"]
+           "ccl_tuner.cpp", "ccl_persist.cpp"]
 HEADERS = ["ccl_internal.h", "ccl_plan.h", "ccl_executor.cuh", "ccl_device.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

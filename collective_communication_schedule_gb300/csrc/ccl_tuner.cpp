@@ -104,11 +104,12 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
 {
     using namespace ccl;
     if (!probe || !best) return fail(CCL_ERR_INVALID_ARG, "null argument");
-    ccl_tune_opts_t to{3, 5, 0.01};
+    ccl_tune_opts_t to{3, 5, 0.01, 0};
     if (topts) {
         if (topts->max_rounds > 0) to.max_rounds = topts->max_rounds;
         if (topts->reps > 0) to.reps = topts->reps;
         if (topts->min_gain > 0) to.min_gain = topts->min_gain;
+        if (topts->max_channels > 0) to.max_channels = topts->max_channels;
     }
     ccl_plan_opts_t base;
     ccl_plan_opts_default(&base);
@@ -133,7 +134,11 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
         base.engine = z.engine;
     }
     if (!base.nthreads) base.nthreads = 512;
-    std::vector<int> gc(std::begin(kChannels), std::end(kChannels));
+    std::vector<int> gc;
+    for (int c : kChannels)
+        if (!to.max_channels || c <= to.max_channels) gc.push_back(c);
+    if (to.max_channels && (gc.empty() || gc.back() != to.max_channels)) gc.push_back(to.max_channels);
+    if (to.max_channels && base.channels > to.max_channels) base.channels = to.max_channels;
     std::vector<int> gt(std::begin(kThreads), std::end(kThreads));
     std::vector<int64_t> gs = slot_grid();
     std::map<std::tuple<int, int, int64_t, int, int, int, int>, double> cache;
@@ -225,11 +230,12 @@ extern "C" ccl_status_t ccl_tune(ccl_schedule_t s, int64_t chunk_elems, int32_t 
 {
     using namespace ccl;
     if (!s || !in_bufs || !out_bufs || !best) return fail(CCL_ERR_INVALID_ARG, "null argument");
-    ccl_tune_opts_t to{3, 5, 0.01};
+    ccl_tune_opts_t to{3, 5, 0.01, 0};
     if (topts) {
         if (topts->max_rounds > 0) to.max_rounds = topts->max_rounds;
         if (topts->reps > 0) to.reps = topts->reps;
         if (topts->min_gain > 0) to.min_gain = topts->min_gain;
+        if (topts->max_channels > 0) to.max_channels = topts->max_channels;
     }
     Prober P{s, chunk_elems, dtype, in_bufs, out_bufs, static_cast<cudaStream_t>(stream), to.reps};
     ccl_plan_opts_t base;
@@ -241,6 +247,7 @@ extern "C" ccl_status_t ccl_tune(ccl_schedule_t s, int64_t chunk_elems, int32_t 
     if (!base.fifo_slots) base.fifo_slots = 4;
     if (!base.tile_bytes) base.tile_bytes = 16 * 1024;
     if (!base.timeout_ms) base.timeout_ms = 2000;
+    if (to.max_channels && base.channels > to.max_channels) base.channels = to.max_channels;
     double default_us = P.time_us(base);
     double bw = 0;
     int32_t probes = 0;
@@ -259,4 +266,25 @@ extern "C" ccl_status_t ccl_tune(ccl_schedule_t s, int64_t chunk_elems, int32_t 
         }
     }
     return st;
+}
+
+// One tuning per message size (AutoCCL report, research method 1-2: the
+// parameters are chosen per message size): rows[i] gets the configuration
+// for chunk_elems[i] elements per chunk and its report.  The buffers must
+// hold the largest size.
+extern "C" ccl_status_t ccl_tune_table(ccl_schedule_t s, int32_t dtype, const int64_t* chunk_elems, int32_t n,
+                                       void* const* in_bufs, void* const* out_bufs, void* stream,
+                                       const ccl_tune_opts_t* topts, const ccl_plan_opts_t* start,
+                                       ccl_tune_row_t* rows)
+{
+    using namespace ccl;
+    if (!s || !chunk_elems || n <= 0 || !rows) return fail(CCL_ERR_INVALID_ARG, "bad arguments");
+    for (int i = 0; i < n; ++i) {
+        std::memset(&rows[i], 0, sizeof(rows[i]));
+        rows[i].chunk_elems = chunk_elems[i];
+        ccl_status_t st = ccl_tune(s, chunk_elems[i], dtype, in_bufs, out_bufs, stream, topts, start, &rows[i].best,
+                                   &rows[i].report);
+        if (st != CCL_OK) return st;
+    }
+    return CCL_OK;
 }

@@ -498,6 +498,7 @@ typedef struct {
     int32_t max_rounds;          /* coordinate sweeps (default 3) */
     int32_t reps;                /* timed executions per probe; the median is used (default 5) */
     double min_gain;             /* relative improvement to keep moving (default 0.01) */
+    int32_t max_channels;        /* largest channel count searched (0: the whole grid) */
 } ccl_tune_opts_t;
 
 typedef struct {
@@ -568,6 +569,53 @@ ccl_status_t ccl_allreduce_ring_noalloc(void* const* in_bufs, void* const* out_b
 ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_tune_opts_t* topts,
                              double (*probe)(void* user, const ccl_plan_opts_t* o), void* user,
                              ccl_plan_opts_t* best, double* best_bw, int32_t* probes);
+
+/* One row of a per-size tuning table. */
+typedef struct {
+    int64_t chunk_elems;         /* message size of the row (elements per chunk) */
+    ccl_plan_opts_t best;        /* configuration chosen for it */
+    ccl_tune_report_t report;    /* its timings */
+} ccl_tune_row_t;
+
+/*
+ * Tune one schedule for several message sizes (AutoCCL report, research
+ * method 1-2: parameters chosen per message size): rows[i] (caller array of
+ * n) receives ccl_tune's result for chunk_elems[i].  in_bufs / out_bufs must
+ * hold the largest size (their contents are overwritten).  Stops at the
+ * first size that cannot be tuned and returns its error.
+ */
+ccl_status_t ccl_tune_table(ccl_schedule_t s, int32_t dtype, const int64_t* chunk_elems, int32_t n,
+                            void* const* in_bufs, void* const* out_bufs, void* stream,
+                            const ccl_tune_opts_t* topts, const ccl_plan_opts_t* start, ccl_tune_row_t* rows);
+
+/*
+ * Tuning tables as JSON files ("ccl-tune-table-1": dtype, a free-text note,
+ * one row per size with the chosen plan options by field name and the
+ * timings).  Reading with rows = NULL only sets *n (and *dtype); otherwise
+ * cap must be >= the row count.  Fields missing from a row take
+ * ccl_plan_opts_default's values.  Errors: CCL_ERR_INVALID_ARG (file cannot
+ * be opened or written, malformed content, capacity too small).
+ */
+ccl_status_t ccl_tune_table_write_json(const ccl_tune_row_t* rows, int32_t n, int32_t dtype, const char* note,
+                                       const char* path);
+ccl_status_t ccl_tune_table_read_json(const char* path, ccl_tune_row_t* rows, int32_t cap, int32_t* n,
+                                      int32_t* dtype);
+
+/* The options of the row whose size is nearest to chunk_elems (ratio of
+ * sizes closest to 1; the first of equals). */
+ccl_status_t ccl_tune_table_lookup(const ccl_tune_row_t* rows, int32_t n, int64_t chunk_elems,
+                                   ccl_plan_opts_t* out);
+
+/*
+ * A compiled schedule as a JSON file ("ccl-schedule-1": the source program,
+ * chunk counts, fusion mode, built-in kind and a digest of the fused
+ * instructions), for checkpointing and reuse.  Reading compiles the program
+ * again and fails with CCL_ERR_INVALID_ARG when the instructions differ from
+ * the written digest (a compiler that fuses differently), or when the file
+ * cannot be read or parsed; the new handle is the caller's to destroy.
+ */
+ccl_status_t ccl_schedule_write_json(ccl_schedule_t s, const char* path);
+ccl_status_t ccl_schedule_read_json(const char* path, ccl_schedule_t* out);
 
 const char* ccl_error_string(ccl_status_t s);
 const char* ccl_last_error_detail(void);

@@ -56,7 +56,7 @@ def test_binding_structs_match_the_header_layout(tmp_path):
         pytest.skip("no C compiler")
     pairs = [(ccl.Op, "ccl_op_t"), (ccl.ScheduleInfo, "ccl_schedule_info_t"), (ccl.InstrInfo, "ccl_instr_info_t"),
              (ccl.PlanOpts, "ccl_plan_opts_t"), (ccl.PlanStats, "ccl_plan_stats_t"), (ccl.StepInfo, "ccl_step_info_t"),
-             (ccl.TuneOpts, "ccl_tune_opts_t"), (ccl.TuneReport, "ccl_tune_report_t")]
+             (ccl.TuneOpts, "ccl_tune_opts_t"), (ccl.TuneReport, "ccl_tune_report_t"), (ccl.TuneRow, "ccl_tune_row_t")]
     lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "ccl.h"', "int main(void) {"]
     want = []
     for cls, cname in pairs:
