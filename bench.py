@@ -179,10 +179,13 @@ class ClockSampler:
 
 
 def kernel_name(stats):
-    """The executor kernel a plan launches (names as ncu lists them)."""
+    """The executor kernel a plan launches: engine, protocol and the thread
+    limit it was built for (512: eight vectors in flight per thread, 1024:
+    four)."""
+    maxt = stats.kernel_build or (512 if stats.nthreads <= 512 else 1024)
     if stats.engine == 1:
-        return "ccl_exec_seq_kernel"
-    return "ccl_exec_kernel<1>" if stats.protocol == 1 else "ccl_exec_kernel<0>"
+        return f"ccl_exec_seq_kernel<{maxt}>"
+    return "ccl_exec_kernel<LL, 512>" if stats.protocol == 1 else f"ccl_exec_kernel<simple, {maxt}>"
 
 
 def schedule_and_opts(ccl, kind, R, G, opts):
@@ -458,6 +461,11 @@ def run_gpu(args):
     }
     if not args.no_sweep:
         out["sweep"] = run_sweep(ccl, torch, datagen, args, peak)
+    if not args.no_codegen_rows and not (args.only or args.scale != 1.0):
+        # the latency-bound rows, whose steps the interpreter's record and
+        # table reads lengthen the most, run both ways (outside the timed
+        # region); `python bench.py --codegen` adds the large rows
+        out["codegen"] = run_codegen(args, rows=["ar_1m", "ag_3m", "rs_3m"], stream=stream)
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(items, args.cpu_seconds)
     return out
@@ -920,6 +928,44 @@ def run_alltoallv(args):
         print(json.dumps(rec), flush=True)
 
 
+def run_codegen(args, rows=None, stream=None):
+    """Generated against interpreted kernels (ReSCCL report, §II.2: a kernel
+    per schedule instead of an interpreter): each suite row's plan run both
+    ways on the same inputs, median of --steps executions after --warmup,
+    with the generated kernel's generation + compile time.  Returns one
+    record per row."""
+    import torch
+    import collective_communication_schedule_gb300 as ccl
+    import datagen
+    names = rows or (args.only.split(",") if args.only else ["ar_1m", "ag_3m", "rs_3m", "hier_ar"])
+    saved = args.only
+    args.only = ",".join(names)
+    items = build_suite(ccl, torch, datagen, args)
+    args.only = saved
+    stream = stream or torch.cuda.current_stream()
+    out = []
+    for it in items:
+        rec = {"row": it["name"], "engine": it["stats"].engine}
+        ms_i = _time_plan(torch, it["plan"], it["d_in"], it["d_out"], stream, reps=max(5, args.steps),
+                          warm=max(3, args.warmup))
+        rec["interpreted_us"] = round(ms_i * 1e3, 2)
+        sched, popts = schedule_and_opts(ccl, it["kind"], it["R"], it["G"], it["opts"])
+        try:
+            gen = ccl.Plan(sched, it["ce"], it["dt"], codegen=1, **popts)
+            st = gen.stats()
+            ms_g = _time_plan(torch, gen, it["d_in"], it["d_out"], stream, reps=max(5, args.steps),
+                              warm=max(3, args.warmup))
+            rec.update(generated_us=round(ms_g * 1e3, 2), speedup=round(ms_i / ms_g, 3),
+                       codegen_ms=round(st.codegen_ms, 1), threadblocks=st.nthreadblocks, steps=st.nsteps)
+            del gen
+        except ccl.CclError as e:
+            rec["error"] = str(e)[:160]
+        out.append(rec)
+        del it["plan"]
+        torch.cuda.empty_cache()
+    return out
+
+
 def hier_allgather_program(G, ng):
     """A user chunk program for the hierarchical AllGather of the HetCCL
     summary ("hierarchical algorithm design and pipelined execution"): an
@@ -1016,11 +1062,19 @@ def main():
     ap.add_argument("--alltoallv", action="store_true", help="second workload: uneven (MoE) AllToAll")
     ap.add_argument("--hier-allgather", action="store_true",
                     help="hierarchical AllGather (in-group, cross-group, in-group) against the flat ring")
+    ap.add_argument("--codegen", action="store_true",
+                    help="generated against interpreted kernels for suite rows (--only, default ar_1m, ag_3m, "
+                         "rs_3m, hier_ar)")
+    ap.add_argument("--no-codegen-rows", action="store_true",
+                    help="leave the generated-kernel comparison of the small rows out of the main line")
     args = ap.parse_args()
-    if args.ablation or args.interference or args.alltoallv or args.hier_allgather:
+    if args.ablation or args.interference or args.alltoallv or args.hier_allgather or args.codegen:
         import torch
         torch.cuda.set_device(0)
-        if args.ablation:
+        if args.codegen:
+            for rec in run_codegen(args):
+                print(json.dumps(rec), flush=True)
+        elif args.ablation:
             run_ablation(args)
         elif args.interference:
             run_interference(args)

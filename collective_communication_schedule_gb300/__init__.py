@@ -72,7 +72,8 @@ class PlanOpts(ctypes.Structure):
                 ("tb_alloc", ctypes.c_int32), ("mb_order", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("instrument", ctypes.c_int32), ("tile_bytes", ctypes.c_int64), ("bulk", ctypes.c_int32),
                 ("link_mode", ctypes.c_int32), ("channel_scaling", ctypes.c_int32), ("mb_window", ctypes.c_int32),
-                ("protocol", ctypes.c_int32), ("tb_budget", ctypes.c_int32), ("engine", ctypes.c_int32)]
+                ("protocol", ctypes.c_int32), ("tb_budget", ctypes.c_int32), ("engine", ctypes.c_int32),
+                ("codegen", ctypes.c_int32)]
 
 
 class PlanStats(ctypes.Structure):
@@ -85,7 +86,8 @@ class PlanStats(ctypes.Structure):
                 ("slot_bytes", ctypes.c_int64), ("fifo_bytes", ctypes.c_int64), ("device_bytes", ctypes.c_int64),
                 ("compile_ms", ctypes.c_double), ("tile_bytes", ctypes.c_int64), ("stages", ctypes.c_int32),
                 ("mb_window", ctypes.c_int32), ("protocol", ctypes.c_int32), ("engine", ctypes.c_int32),
-                ("fuse", ctypes.c_int32)]
+                ("fuse", ctypes.c_int32), ("kernel_build", ctypes.c_int32), ("codegen", ctypes.c_int32),
+                ("codegen_ms", ctypes.c_double)]
 
 
 class StepInfo(ctypes.Structure):
@@ -151,6 +153,8 @@ def _load():
                                      ctypes.POINTER(ctypes.c_int32)],
         "ccl_tune_table_lookup": [ctypes.POINTER(TuneRow), I32_, I64_, ctypes.POINTER(PlanOpts)],
         "ccl_schedule_write_json": [P, ctypes.c_char_p],
+        "ccl_plan_codegen_source": [P, I64_, I32_, ctypes.POINTER(PlanOpts), ctypes.c_char_p, ctypes.c_size_t,
+                                    ctypes.POINTER(ctypes.c_size_t), I32_, ctypes.POINTER(ctypes.c_int64)],
         "ccl_schedule_read_json": [ctypes.c_char_p, ctypes.POINTER(P)],
     }
     for name, args in sig.items():
@@ -296,6 +300,19 @@ class Schedule:
         h = ctypes.c_void_p()
         _check(lib.ccl_schedule_read_json(os.fsencode(path), ctypes.byref(h)))
         return cls(h.value)
+
+    def codegen_source(self, chunk_elems, dtype, compile=False, opts: PlanOpts | None = None, **kw):
+        """(source, cubin bytes or None) of the kernel a plan with codegen = 1
+        would run (``ccl_plan_codegen_source``; host only)."""
+        o = _with_opts(opts, kw)
+        n = ctypes.c_size_t()
+        cb = ctypes.c_int64()
+        _check(lib.ccl_plan_codegen_source(self._h, chunk_elems, dtype, ctypes.byref(o), None, 0, ctypes.byref(n),
+                                           0, None))
+        buf = ctypes.create_string_buffer(n.value + 1)
+        _check(lib.ccl_plan_codegen_source(self._h, chunk_elems, dtype, ctypes.byref(o), buf, n.value + 1,
+                                           ctypes.byref(n), int(bool(compile)), ctypes.byref(cb)))
+        return buf.value.decode(), (cb.value if compile else None)
 
     def check(self, chunk_elems, dtype, opts: PlanOpts | None = None, **kw) -> PlanStats:
         """Plan on the host only (deadlock simulation included, no GPU)."""

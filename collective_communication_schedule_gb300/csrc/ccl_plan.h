@@ -6,14 +6,12 @@
 #include <vector>
 
 #include "ccl_internal.h"
+#include "ccl_layout.h"
 
 namespace ccl {
 
 // operand buffer classes (select cache hints in the kernel)
 enum : int32_t { OPB_NONE = -1 };
-
-// DStep / DRec flags
-enum : int32_t { STEP_NOPOST = 1, STEP_SRC_STREAM = 2, STEP_LOC_STREAM = 4 };
 
 // One channel instruction.  Offsets are element offsets of the channel
 // range inside the rank's buffer; a missing operand has buf = -1.
@@ -49,33 +47,12 @@ struct DStep {
 };
 static_assert(sizeof(DStep) == 64, "DStep layout");
 
-// Everything the executor needs for one step, denormalised (one 128-byte
-// record per step, so the control warp prefetches a step with one load).
-struct DRec {
-    int32_t kind, dtype, link_in, link_out;
-    int32_t src_buf, src_rank, loc_buf, loc_rank, dst_buf, dst_rank;
-    int32_t nslots, dep_begin, dep_count, signal, mb, flags;
-    int64_t src_off, loc_off, dst_off;   // element offsets of this piece
-    int64_t nelem, seq_in, seq_out;
-    int32_t drain;
-    int32_t seq_in_mod, seq_out_mod;   // seq_in % S, seq_out % S (slot index arithmetic in 32 bits)
-    int32_t pad0;
-};
-static_assert(sizeof(DRec) == 128, "DRec layout");
-
-struct DLink {
-    int64_t slot_base;  // byte offset of slot 0 in the FIFO pool (slots of slot_stride bytes)
-    int64_t total;      // slot sequences per execution
-    int32_t flag_base;  // full flags at [flag_base, +S), consumed at [flag_base+S, +S)
-    int32_t src_rank, dst_rank;
-    int32_t total_mod;  // total % S
-};
-static_assert(sizeof(DLink) == 32, "DLink layout");
-
-struct DDep {
-    int32_t counter;
-    int32_t pad;
-    int64_t value;      // wait until counter >= exec * m + value
+// One segment of a threadblock program: its channel instructions in order,
+// run in windows of `window` micro-batches (each instruction takes every
+// micro-batch of a window in turn).
+struct SegInfo {
+    std::vector<int> cis;
+    int window = 1;
 };
 
 struct PlanImage {
@@ -86,6 +63,7 @@ struct PlanImage {
     std::vector<DLink> links;
     std::vector<DDep> deps;
     std::vector<int32_t> tb_rank;    // rank each threadblock serves (reporting)
+    std::vector<std::vector<SegInfo>> tb_segs;   // segments of every threadblock program
     int32_t ntb = 0;
     int32_t ncounters = 0;
     int32_t nthreads = 512;
@@ -119,6 +97,7 @@ struct PlanImage {
     int32_t timeout_ms = 2000;
     int32_t instrument = 0;
     int32_t fuse = CCL_FUSE_FULL;    // fusion mode of the instructions planned
+    int32_t kbuild = 0;              // thread limit of the kernel build launched (512 or 1024; 0: not chosen)
 };
 
 struct Timeline {

@@ -503,6 +503,7 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     img->deps.clear();
     img->tb_begin.clear();
     img->tb_rank.clear();
+    img->tb_segs.clear();
     img->m = m;
     img->channels = p;
     img->mb_order = order;
@@ -627,6 +628,13 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
             for (int i : tbs[t])
                 if (pc[i] > ch) prog.push_back(i);
             auto segs = make_segments(tl, prog, order, ep);
+            img->tb_segs.emplace_back();
+            for (auto& seg : segs) {
+                SegInfo sg;
+                for (int i : seg) sg.cis.push_back(i * p + ch);
+                sg.window = window;
+                img->tb_segs.back().push_back(std::move(sg));
+            }
             // window by window; inside a window instruction-major
             for (auto& seg : segs) {
                 for (int w0 = 0; w0 < m; w0 += window) {

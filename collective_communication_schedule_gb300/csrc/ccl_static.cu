@@ -20,8 +20,8 @@
 #include <mutex>
 #include <string>
 
-#include "ccl_device.cuh"
 #include "ccl_internal.h"
+#include "ccl_core.cuh"
 
 namespace ccl {
 namespace {

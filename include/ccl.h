@@ -299,6 +299,20 @@ typedef enum {
  *                 send from a buffer write straight into the receiver's
  *                 destination buffer (one copy, no FIFO) and keeps FIFOs for
  *                 transfers that are forwarded or reduced.
+ *   codegen     : 0 (default): the library's kernels interpret the plan's
+ *                 step records.  1: ccl_plan_create generates CUDA source
+ *                 for this one plan (ReSCCL report, §II.2: a kernel per
+ *                 schedule instead of a run-time interpreter), compiles it
+ *                 for sm_103a with NVRTC and runs it instead: every
+ *                 threadblock program becomes code with its instructions'
+ *                 buffers, offsets, links and counters written in, and no
+ *                 step, link or dependency table is read on the device.
+ *                 Same steps, waits, status word and results as the
+ *                 interpreted plan.  Identical generated sources are compiled
+ *                 once per process.  Flag protocol only; a plan whose steps
+ *                 the generator cannot express as loops is refused
+ *                 (CCL_ERR_UNSUPPORTED), so is ccl_plan_debug_drop_signal on
+ *                 a generated plan.
  */
 typedef struct {
     int32_t channels;
@@ -319,6 +333,7 @@ typedef struct {
     int32_t protocol;
     int32_t tb_budget;   /* CCL_TB_BALANCED: threadblocks to aim for (0: 256) */
     int32_t engine;      /* CCL_ENGINE_* */
+    int32_t codegen;     /* 1: run a kernel generated and compiled for this plan (see below) */
 } ccl_plan_opts_t;
 
 void ccl_plan_opts_default(ccl_plan_opts_t* o);
@@ -410,9 +425,31 @@ typedef struct {
     int32_t engine;              /* CCL_ENGINE_* */
     int32_t fuse;                /* CCL_FUSE_* mode of the instructions planned (less than the
                                     schedule's when its fused form could not be planned) */
+    int32_t kernel_build;        /* thread limit the launched kernel was built for: 512 (eight
+                                    16-byte vectors in flight per thread) or 1024 (four); 0 from
+                                    ccl_plan_check, which does not choose */
+    int32_t codegen;             /* 1: the plan runs its generated kernel */
+    double codegen_ms;           /* host time to generate and compile it (0 when cached) */
 } ccl_plan_stats_t;
 
 ccl_status_t ccl_plan_stats(ccl_plan_t p, ccl_plan_stats_t* st);
+
+/*
+ * The CUDA source ccl_plan_create would generate for this schedule, size and
+ * options with codegen = 1 (host only, no device needed): copied into buf
+ * (capacity cap bytes, NUL-terminated) unless buf is NULL; *len (may be
+ * NULL) receives its length without the NUL.  With compile = 1 the source
+ * is also compiled for sm_103a with NVRTC and *cubin_bytes (may be NULL)
+ * receives the size of the result.  The kernel is built for 512 threads
+ * when opts->nthreads <= 512, else for 1024.  Errors: those of
+ * ccl_plan_check, CCL_ERR_UNSUPPORTED (the generator cannot express the
+ * plan), CCL_ERR_INVALID_ARG (cap too small, after setting *len),
+ * CCL_ERR_INTERNAL (the compiler rejected the source; the detail holds its
+ * log).
+ */
+ccl_status_t ccl_plan_codegen_source(ccl_schedule_t s, int64_t chunk_elems, int32_t dtype,
+                                     const ccl_plan_opts_t* opts, char* buf, size_t cap, size_t* len,
+                                     int32_t compile, int64_t* cubin_bytes);
 
 /*
  * Run the planner and its deadlock simulation on the host only (no device

@@ -97,3 +97,19 @@ def test_binding_constants_match_the_header():
     for i, name in enumerate(ccl.KIND_NAMES):
         assert vals["I_" + name.upper()] == i, name
     assert vals["I_NKINDS"] == len(ccl.KIND_NAMES)
+
+
+def test_layout_header_codes_match_the_c_abi():
+    """The codes the run-time-compiled kernels take from the layout header
+    (which cannot include the C ABI header) have the C ABI's values."""
+    def codes(path):
+        text = re.sub(r"/\*.*?\*/|//[^\n]*", "", open(path).read(), flags=re.S)
+        vals = {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(CCL_[A-Z0-9_]+)\s*=\s*(-?\d+)", text)}
+        for m in re.finditer(r"#define\s+(CCL_[A-Z0-9_]+)\s+(\d+)\b", text):
+            vals[m.group(1)] = int(m.group(2))
+        return vals
+    abi = codes(os.path.join(ROOT, "include", "ccl.h"))
+    layout = codes(os.path.join(ROOT, "collective_communication_schedule_gb300", "csrc", "ccl_layout.h"))
+    assert len(layout) >= 18
+    for name, v in layout.items():
+        assert abi.get(name) == v, name

@@ -26,7 +26,9 @@ def test_every_row_plans_within_two_ctas_per_sm(row):
     assert 0 < st.nthreadblocks <= 2 * 152
     assert st.schedule_bytes >= st.min_bytes > 0
     assert st.engine == po.get("engine", 0)
-    assert bench.kernel_name(st) == ("ccl_exec_seq_kernel" if st.engine == 1 else "ccl_exec_kernel<0>")
+    maxt = 512 if st.nthreads <= 512 else 1024
+    assert bench.kernel_name(st) == (f"ccl_exec_seq_kernel<{maxt}>" if st.engine == 1
+                                     else f"ccl_exec_kernel<simple, {maxt}>")
 
 
 @pytest.mark.parametrize("name", ["ring_bf16", "ring_f32", "ar_1m"])
