@@ -73,7 +73,7 @@ class PlanOpts(ctypes.Structure):
                 ("instrument", ctypes.c_int32), ("tile_bytes", ctypes.c_int64), ("bulk", ctypes.c_int32),
                 ("link_mode", ctypes.c_int32), ("channel_scaling", ctypes.c_int32), ("mb_window", ctypes.c_int32),
                 ("protocol", ctypes.c_int32), ("tb_budget", ctypes.c_int32), ("engine", ctypes.c_int32),
-                ("codegen", ctypes.c_int32)]
+                ("codegen", ctypes.c_int32), ("cluster", ctypes.c_int32)]
 
 
 class PlanStats(ctypes.Structure):
@@ -86,8 +86,8 @@ class PlanStats(ctypes.Structure):
                 ("slot_bytes", ctypes.c_int64), ("fifo_bytes", ctypes.c_int64), ("device_bytes", ctypes.c_int64),
                 ("compile_ms", ctypes.c_double), ("tile_bytes", ctypes.c_int64), ("stages", ctypes.c_int32),
                 ("mb_window", ctypes.c_int32), ("protocol", ctypes.c_int32), ("engine", ctypes.c_int32),
-                ("fuse", ctypes.c_int32), ("kernel_build", ctypes.c_int32), ("codegen", ctypes.c_int32),
-                ("codegen_ms", ctypes.c_double)]
+                ("fuse", ctypes.c_int32), ("kernel_build", ctypes.c_int32), ("cluster", ctypes.c_int32),
+                ("codegen", ctypes.c_int32), ("codegen_ms", ctypes.c_double)]
 
 
 class StepInfo(ctypes.Structure):

@@ -352,13 +352,14 @@ std::string generate_plan_source(const PlanImage& img, int build, std::string* w
     const std::string maxt = std::to_string(build <= 512 ? 512 : 1024);
     o += "extern \"C\" __global__ void __launch_bounds__(" + maxt +
          ", 1) ccl_gen_kernel(const __grid_constant__ ccl::KParams P)\n{\n";
-    std::string sw = "switch (blockIdx.x) {\n";
+    std::string sw = seq ? "switch (P.cluster > 1 ? blockIdx.x / P.cluster : blockIdx.x) {\n" : "switch (blockIdx.x) {\n";
     for (int b = 0; b < img.ntb; ++b)
         sw += "    case " + std::to_string(b) + ": ccl::gtb" + std::to_string(b) + (seq ? "(P, &abort_flag)" : "(P, &sh)") +
               "; break;\n";
     sw += "    default: break;\n    }\n";
     if (seq) {
-        o += "    __shared__ int abort_flag;\n    " + sw;
+        o += "    __shared__ int abort_flag;\n";
+        o += "    if (P.cluster > 1) ccl::group_sync(P);   // every CTA of the cluster has started\n    " + sw;
     } else {
         o += "    __shared__ __align__(16) ccl::CtlShared sh;\n";
         o += "    extern __shared__ __align__(128) unsigned char stages[];\n";

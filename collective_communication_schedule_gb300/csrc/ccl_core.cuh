@@ -1217,8 +1217,56 @@ struct SeqShared {
     int abort;
 };
 
+// A threadblock program of the sequential engine may run on a cluster of
+// P.cluster CTAs: the cluster's first CTA waits and posts, every CTA moves
+// its share of each slot.  group_sync is the barrier of all of them (a
+// cluster barrier with release / acquire at cluster scope, so the leader's
+// gpu-scope fence before its flag posts covers every CTA's stores).  The
+// leader hands its verdict on a wait to the others by storing it into each
+// CTA's shared flag before the barrier (set_group_flag); every CTA then
+// reads its own copy, so no CTA reads another's shared memory and none can
+// leave while another still accesses its memory.  A kernel with clusters
+// starts with one group_sync, after which every CTA's shared memory exists.
+__device__ __forceinline__ unsigned cluster_rank()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void group_sync(const KParams& P)
+{
+    if (P.cluster > 1) {
+        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    } else {
+        __syncthreads();
+    }
+}
+// the leader's store of v into `flag` of every CTA of its cluster
+__device__ __forceinline__ void set_group_flag(const KParams& P, int* flag, int v)
+{
+    if (P.cluster <= 1) {
+        *flag = v;
+        return;
+    }
+    for (int r = 0; r < P.cluster; ++r) {
+        unsigned remote;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(flag)), "r"(r));
+        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+    }
+}
+// the flag after group_sync (this CTA's copy)
+__device__ __forceinline__ int leader_flag(const KParams& P, const int* flag)
+{
+    (void)P;
+    return *(volatile const int*)flag;
+}
+__device__ __forceinline__ bool seq_leader(const KParams& P)
+{
+    return threadIdx.x == 0 && (P.cluster <= 1 || cluster_rank() == 0);
+}
+
 // One step after its dependency counters are satisfied, run by every thread
-// of the CTA with the same record (the library's kernel reads it from shared
+// of the CTA (of every CTA of the program's cluster) with the same record (the library's kernel reads it from shared
 // memory, a generated kernel builds it from constants).  Lin / Lout: its
 // links, or null.  `abort` is a shared flag; t_start and waited are thread
 // 0's stamps for the timeline.  False when a wait gave up.
@@ -1227,10 +1275,14 @@ __device__ __forceinline__ bool seq_step(const KParams& P, int* abort, const DRe
                                          const DLink* Lout, int si, unsigned exec_mod, unsigned long long t_start,
                                          unsigned long long waited)
 {
+    const int C = P.cluster > 1 ? P.cluster : 1;
     const int tid = threadIdx.x, T = blockDim.x;
+    const int crank = C > 1 ? (int)cluster_rank() : 0;
+    const bool leader = tid == 0 && crank == 0;
     const unsigned S = (unsigned)P.S;
     const int es = (st.dtype == CCL_BF16 || st.dtype == CCL_F16) ? 2 : 4;
     const int esh = es == 2 ? 1 : 2;
+    const long long ve = 16 / es;
     const unsigned long long base_in = Lin ? (unsigned long long)(P.exec * Lin->total) : 0;
     const unsigned long long base_out = Lout ? (unsigned long long)(P.exec * Lout->total) : 0;
     const long long slot_elems = P.slot_bytes >> esh;
@@ -1249,17 +1301,26 @@ __device__ __forceinline__ bool seq_step(const KParams& P, int* abort, const DRe
         const unsigned long long sin = base_in + st.seq_in + k;
         const unsigned long long sout = base_out + st.seq_out + k;
         if (linked) {
-            if (tid == 0) *abort = wait_slots(P, Lin, Lout, sin, sout, in_idx, out_idx, 1, si, waited) == 0;
-            __syncthreads();
-            if (*abort) return false;
+            if (leader) set_group_flag(P, abort, wait_slots(P, Lin, Lout, sin, sout, in_idx, out_idx, 1, si, waited) == 0);
+            group_sync(P);
+            if (leader_flag(P, abort)) return false;
         }
-        if (tid == 0 && P.timeline && k == 0) t_pub = gtimer();
-        const long long e0 = k * slot_elems;
+        if (leader && P.timeline && k == 0) t_pub = gtimer();
+        long long e0 = k * slot_elems;
         long long n = st.nelem - e0;
         if (n > slot_elems) n = slot_elems;
         if (n < 0) n = 0;
-        const char* slot_in = Lin ? P.fifo + Lin->slot_base + (long long)in_idx * P.slot_stride : nullptr;
-        char* slot_out = Lout ? P.fifo + Lout->slot_base + (long long)out_idx * P.slot_stride : nullptr;
+        long long soff = 0;   // this CTA's share of the slot (16-byte units)
+        if (C > 1) {
+            const long long V = n / ve;
+            const long long lo = (V * crank / C) * ve;
+            const long long hi = crank == C - 1 ? n : (V * (crank + 1) / C) * ve;
+            soff = lo;
+            e0 += lo;
+            n = hi - lo;
+        }
+        const char* slot_in = Lin ? P.fifo + Lin->slot_base + (long long)in_idx * P.slot_stride + soff * es : nullptr;
+        char* slot_out = Lout ? P.fifo + Lout->slot_base + (long long)out_idx * P.slot_stride + soff * es : nullptr;
         const char* a;
         bool as = false;
         if (Lin && st.kind != CCL_I_REDUCE) {
@@ -1288,8 +1349,8 @@ __device__ __forceinline__ bool seq_step(const KParams& P, int* abort, const DRe
             default: move_part<CCL_I32, U>(red, a, as, b, bs, o1, o1s, o2, n, tid, T); break;
             }
         }
-        __syncthreads();
-        if (tid == 0) {
+        group_sync(P);
+        if (leader) {
             if (P.timeline && k == nslots - 1) t_done = gtimer();
             // every thread's stores were observed at the barrier; the
             // fence makes them visible at gpu scope before the flags
@@ -1417,14 +1478,14 @@ __device__ __forceinline__ bool gen_seq_step(const KParams& P, int* abort, const
                                              const int2* dep, int m, int si, unsigned exec_mod)
 {
     unsigned long long t_start = 0, waited = 0;
-    if (threadIdx.x == 0) {
+    if (seq_leader(P)) {
         if (P.timeline) t_start = gtimer();
         int ok = *(volatile int*)P.status == 0;
         if (ok && gi.ndep > 0) ok = wait_gen_deps(P, gi, dep, g.st.mb, m, si, waited);
-        *abort = !ok;
+        set_group_flag(P, abort, !ok);
     }
-    __syncthreads();
-    if (*abort) return false;
+    group_sync(P);
+    if (leader_flag(P, abort)) return false;
     return seq_step<U>(P, abort, g.st, g.st.link_in >= 0 ? &g.lin : nullptr, g.st.link_out >= 0 ? &g.lout : nullptr,
                        si, exec_mod, t_start, waited);
 }

@@ -78,6 +78,7 @@ struct KParams {
     int ns;                        // shared-memory stages of the bulk path (0: off)
     int ll;                        // FIFO slots hold LL lines (data + flag per 64 bits)
     int stream_in;                 // inputs share no memory with outputs: streaming loads allowed
+    int cluster;                   // sequential engine: CTAs (one thread-block cluster) per threadblock program
     char* bufs[3][CCL_MAX_RANKS];
 };
 

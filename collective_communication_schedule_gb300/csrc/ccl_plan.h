@@ -98,6 +98,7 @@ struct PlanImage {
     int32_t instrument = 0;
     int32_t fuse = CCL_FUSE_FULL;    // fusion mode of the instructions planned
     int32_t kbuild = 0;              // thread limit of the kernel build launched (512 or 1024; 0: not chosen)
+    int32_t cluster = 1;             // CTAs per threadblock program (sequential engine)
 };
 
 struct Timeline {

@@ -973,6 +973,10 @@ ccl_status_t build_plan_one(const ccl_schedule& s_in, int64_t ce, int32_t dtype,
         return fail(CCL_ERR_INVALID_ARG, "engine must be CCL_ENGINE_PIPELINED or CCL_ENGINE_SEQUENTIAL");
     if (o.engine == CCL_ENGINE_SEQUENTIAL && o.protocol == CCL_PROTO_LL)
         return fail(CCL_ERR_UNSUPPORTED, "the sequential engine has no LL data path");
+    if (o.cluster != 0 && o.cluster != 1 && o.cluster != 2 && o.cluster != 4 && o.cluster != 8)
+        return fail(CCL_ERR_INVALID_ARG, "cluster must be 0, 1, 2, 4 or 8");
+    if (o.cluster > 1 && o.engine != CCL_ENGINE_SEQUENTIAL)
+        return fail(CCL_ERR_UNSUPPORTED, "clusters of CTAs run the sequential engine only");
     if (o.channel_scaling != 0 && o.channel_scaling != 1)
         return fail(CCL_ERR_INVALID_ARG, "channel_scaling must be 0 or 1");
     if (o.tile_bytes < 16 || o.tile_bytes % 16 || o.tile_bytes > 65536)
@@ -1082,6 +1086,7 @@ ccl_status_t build_plan_one(const ccl_schedule& s_in, int64_t ce, int32_t dtype,
                                       " FIFO slots of " + std::to_string(o.slot_bytes) + " bytes (" + first_why + ")");
 done:
     img->ndirect = ndirect;
+    img->cluster = o.cluster > 1 ? o.cluster : 1;
     if (log_level() >= 1) {
         size_t drains = 0, waiting = 0;
         for (const DStep& d : img->steps) {

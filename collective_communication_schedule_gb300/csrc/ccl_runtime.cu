@@ -80,21 +80,24 @@ __global__ void __launch_bounds__(MAXT, 1) ccl_exec_seq_kernel(const __grid_cons
     constexpr int U = InFlight<MAXT>::U;
     __shared__ __align__(16) SeqShared sh;
     const int tid = threadIdx.x;
-    const int b0 = P.tb_begin[blockIdx.x], b1 = P.tb_begin[blockIdx.x + 1];
+    const int prog = P.cluster > 1 ? blockIdx.x / P.cluster : blockIdx.x;
+    const int b0 = P.tb_begin[prog], b1 = P.tb_begin[prog + 1];
     const unsigned exec_mod = (unsigned)(P.exec % P.S);
+    const bool leader = seq_leader(P);
     const DRec& st = sh.rec;
+    if (P.cluster > 1) group_sync(P);   // every CTA of the cluster has started
     for (int si = b0; si < b1; ++si) {
         unsigned long long t_start = 0, waited = 0;
-        if (tid == 0) {
+        if (tid == 0) sh.rec = P.recs[si];   // every CTA of the program reads the record
+        if (leader) {
             if (P.timeline) t_start = gtimer();
-            sh.rec = P.recs[si];
             int ok = *(volatile int*)P.status == 0;
             if (ok && sh.rec.dep_count > 0)
                 ok = wait_deps(P, P.deps + sh.rec.dep_begin, sh.rec.dep_count, si, waited);
-            sh.abort = !ok;
+            set_group_flag(P, &sh.abort, !ok);
         }
-        __syncthreads();
-        if (sh.abort) return;
+        group_sync(P);
+        if (leader_flag(P, &sh.abort)) return;
         const DLink* Lin = st.link_in >= 0 ? P.links + st.link_in : nullptr;
         const DLink* Lout = st.link_out >= 0 ? P.links + st.link_out : nullptr;
         if (!seq_step<U>(P, &sh.abort, st, Lin, Lout, si, exec_mod, t_start, waited)) return;
@@ -228,6 +231,7 @@ ccl_plan_opts_t merged_opts(const ccl_plan_opts_t* opts)
         o.tb_budget = opts->tb_budget;
         o.engine = opts->engine;
         o.codegen = opts->codegen;
+        o.cluster = opts->cluster;
     }
     return o;
 }
@@ -237,6 +241,34 @@ const void* launch_fn(const ccl_plan* p)
 {
     if (p->gen_kernel) return (const void*)p->gen_kernel;
     return ccl::exec_kernel(p->img.protocol, p->img.engine, p->img.kbuild);
+}
+
+// Blocks of `fn` (threads, dynamic shared memory) the device holds at once,
+// in units of threadblock programs: CTAs per SM x SMs, or with clusters of
+// `cluster` CTAs the clusters that fit.
+cudaError_t resident_programs(const void* fn, int threads, size_t dyn, int cluster, int nsm, int ntb, long long* out)
+{
+    if (cluster <= 1) {
+        int per_sm = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, dyn);
+        *out = (long long)per_sm * nsm;
+        return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(ntb * cluster));
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = dyn;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)cluster;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+    *out = n;
+    return e;
 }
 
 void fill_stats(const ccl::PlanImage& img, ccl_plan_stats_t* st)
@@ -266,6 +298,7 @@ void fill_stats(const ccl::PlanImage& img, ccl_plan_stats_t* st)
     st->engine = img.engine;
     st->fuse = img.fuse;
     st->kernel_build = img.kbuild;
+    st->cluster = img.cluster;
 }
 
 void free_plan(ccl_plan* p)
@@ -346,6 +379,8 @@ void ccl_plan_opts_default(ccl_plan_opts_t* o)
     o->protocol = CCL_PROTO_SIMPLE;
     o->tb_budget = 0;
     o->engine = CCL_ENGINE_PIPELINED;
+    o->codegen = 0;
+    o->cluster = 0;
 }
 
 ccl_status_t ccl_schedule_compile(const ccl_op_t* ops, int32_t nops, int32_t nranks, const int32_t nchunks[3],
@@ -510,11 +545,13 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
         bool fit = false;
         for (int build : {512, 1024}) {
             if (build == 512 && img.nthreads > 512) continue;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &per_sm, ccl::exec_kernel(img.protocol, img.engine, build), img.nthreads, dyn);
+            long long progs = 0;
+            e = resident_programs(ccl::exec_kernel(img.protocol, img.engine, build), img.nthreads, dyn, img.cluster,
+                                  nsm, img.ntb, &progs);
             if (e != cudaSuccess) { delete p; return ccl::cuda_fail(e, "occupancy query"); }
             img.kbuild = build;
-            if ((int64_t)per_sm * nsm >= img.ntb) { fit = true; break; }
+            per_sm = (int)std::min<long long>(progs / std::max(1, nsm), 1 << 20);
+            if (progs >= img.ntb) { fit = true; break; }
         }
         if (fit) break;
         if (ns > 2) { --ns; continue; }
@@ -525,11 +562,19 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
         if (ns < 2) ns = 0;
     }
     img.ns = ns;
-    if ((int64_t)per_sm * nsm < img.ntb) {
-        std::string msg = "plan needs " + std::to_string(img.ntb) + " co-resident threadblocks of " +
-                          std::to_string(img.nthreads) + " threads; the device holds " + std::to_string(per_sm * nsm);
-        delete p;
-        return ccl::fail(CCL_ERR_UNSUPPORTED, msg);
+    {
+        long long progs = 0;
+        e = resident_programs(ccl::exec_kernel(img.protocol, img.engine, img.kbuild), img.nthreads,
+                              (size_t)ns * stage_bytes, img.cluster, nsm, img.ntb, &progs);
+        if (e != cudaSuccess) { delete p; return ccl::cuda_fail(e, "occupancy query"); }
+        if (progs < img.ntb) {
+            std::string msg = "plan needs " + std::to_string(img.ntb) + " co-resident threadblock programs of " +
+                              std::to_string(img.nthreads) + " threads" +
+                              (img.cluster > 1 ? " on clusters of " + std::to_string(img.cluster) + " CTAs" : "") +
+                              "; the device holds " + std::to_string(progs);
+            delete p;
+            return ccl::fail(CCL_ERR_UNSUPPORTED, msg);
+        }
     }
     if (o.codegen) {
         // the plan's own kernel, built for the same thread limit
@@ -548,12 +593,12 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute((const void*)p->gen_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      smem_optin - (int)fa.sharedSizeBytes);
-        int gen_per_sm = 0;
+        long long gen_progs = 0;
         if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&gen_per_sm, (const void*)p->gen_kernel, img.nthreads,
-                                                              (size_t)ns * stage_bytes);
+            e = resident_programs((const void*)p->gen_kernel, img.nthreads, (size_t)ns * stage_bytes, img.cluster, nsm,
+                                  img.ntb, &gen_progs);
         if (e != cudaSuccess) { free_plan(p); return ccl::cuda_fail(e, "load the generated kernel"); }
-        if ((int64_t)gen_per_sm * nsm < img.ntb) {
+        if (gen_progs < img.ntb) {
             free_plan(p);
             return ccl::fail(CCL_ERR_UNSUPPORTED, "the generated kernel's threadblocks cannot all be co-resident");
         }
@@ -616,6 +661,7 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
     k.ns = img.ns;
     k.timeout_ns = (unsigned long long)img.timeout_ms * 1000000ull;
     k.S = img.S;
+    k.cluster = img.cluster;
     for (int r = 0; r < CCL_MAX_RANKS; ++r) k.bufs[2][r] = p->d_scratch[r];
     p->compile_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
     *out = p;
@@ -656,9 +702,28 @@ ccl_status_t ccl_execute(ccl_plan_t p, void* const* in_bufs, void* const* out_bu
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p->img.ntb == 0) return CCL_OK;  // empty program: nothing to move
     void* args[] = {&k};
-    cudaError_t e = cudaLaunchCooperativeKernel(launch_fn(p), dim3(p->img.ntb),
-                                                dim3(p->img.nthreads), args,
-                                                (size_t)p->img.ns * p->img.tile_bytes, s);
+    cudaError_t e;
+    if (p->img.cluster > 1) {
+        // every program on its own cluster, all of them co-resident
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(p->img.ntb * p->img.cluster));
+        cfg.blockDim = dim3((unsigned)p->img.nthreads);
+        cfg.dynamicSmemBytes = (size_t)p->img.ns * p->img.tile_bytes;
+        cfg.stream = s;
+        cudaLaunchAttribute at[2];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = (unsigned)p->img.cluster;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        at[1].id = cudaLaunchAttributeCooperative;
+        at[1].val.cooperative = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 2;
+        e = cudaLaunchKernelExC(&cfg, launch_fn(p), args);
+    } else {
+        e = cudaLaunchCooperativeKernel(launch_fn(p), dim3(p->img.ntb), dim3(p->img.nthreads), args,
+                                        (size_t)p->img.ns * p->img.tile_bytes, s);
+    }
     if (e != cudaSuccess) return ccl::cuda_fail(e, "executor launch");
     p->exec += 1;
     return CCL_OK;

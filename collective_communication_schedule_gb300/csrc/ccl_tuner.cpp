@@ -9,7 +9,8 @@
 // chunk size are optimised one coordinate at a time, raising a parameter
 // while bandwidth keeps improving (bandwidth is unimodal in each of them).
 // Grids: channels {1,2,4,8,12,16,24,32,48}, threads {128,256,512,1024},
-// slot size 16 KiB .. 4 MiB in powers of two.  A probe is the median of
+// slot size 16 KiB .. 4 MiB in powers of two, and on the sequential engine
+// CTAs per threadblock program {1,2,4,8}.  A probe is the median of
 // `reps` CUDA-event-timed executions after one warm-up; a point whose plan
 // cannot be built (threadblocks not co-resident, FIFO too small) scores 0.
 #include <cuda_runtime.h>
@@ -34,11 +35,12 @@ struct Prober {
     cudaStream_t stream;
     int reps;
     int probes = 0;
-    std::map<std::tuple<int, int, int64_t, int, int, int, int>, double> cache;  // -> microseconds (0 = infeasible)
+    std::map<std::tuple<int, int, int64_t, int, int, int, int, int>, double> cache;  // -> microseconds (0 = infeasible)
 
     double time_us(const ccl_plan_opts_t& o)
     {
-        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol, o.link_mode, o.engine);
+        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol, o.link_mode, o.engine,
+                                   o.cluster);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
         ++probes;
@@ -132,6 +134,8 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
         base.protocol = z.protocol;
         base.tb_budget = z.tb_budget;
         base.engine = z.engine;
+        base.cluster = z.cluster;
+        base.codegen = z.codegen;
     }
     if (!base.nthreads) base.nthreads = 512;
     std::vector<int> gc;
@@ -141,10 +145,11 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
     if (to.max_channels && base.channels > to.max_channels) base.channels = to.max_channels;
     std::vector<int> gt(std::begin(kThreads), std::end(kThreads));
     std::vector<int64_t> gs = slot_grid();
-    std::map<std::tuple<int, int, int64_t, int, int, int, int>, double> cache;
+    std::map<std::tuple<int, int, int64_t, int, int, int, int, int>, double> cache;
     int nprobe = 0;
     auto measure = [&](const ccl_plan_opts_t& o) {
-        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol, o.link_mode, o.engine);
+        auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol, o.link_mode, o.engine,
+                                   o.cluster);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
         ++nprobe;
@@ -164,22 +169,30 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
         cur.protocol = sub & 2 ? CCL_PROTO_LL : CCL_PROTO_SIMPLE;
         cur.link_mode = sub & 4 ? CCL_LINK_DIRECT : CCL_LINK_FIFO;
         cur.engine = sub & 8 ? CCL_ENGINE_SEQUENTIAL : CCL_ENGINE_PIPELINED;
+        // the sequential engine also chooses the CTAs per program (clusters)
+        const bool seq = cur.engine == CCL_ENGINE_SEQUENTIAL;
+        const std::vector<int> gk = seq ? std::vector<int>{1, 2, 4, 8} : std::vector<int>{1};
+        if (!seq) cur.cluster = 0;
         int ic = nearest(gc, cur.channels), it = nearest(gt, cur.nthreads), is = nearest(gs, cur.slot_bytes);
-        auto eval = [&](int c, int t, int sl) {
+        int ik = seq ? nearest(gk, std::max(1, cur.cluster)) : 0;
+        auto eval = [&](int c, int t, int sl, int k) {
             ccl_plan_opts_t o = cur;
             o.channels = gc[c];
             o.nthreads = gt[t];
             o.slot_bytes = gs[sl];
+            o.cluster = gk[k] > 1 ? gk[k] : 0;
             return measure(o);
         };
-        double bw = eval(ic, it, is);
+        double bw = eval(ic, it, is, ik);
         for (int round = 0; round < to.max_rounds; ++round) {
             bool moved = false;
-            for (int coord = 0; coord < 3; ++coord) {
-                int* idx = coord == 0 ? &ic : coord == 1 ? &it : &is;
-                int n = coord == 0 ? (int)gc.size() : coord == 1 ? (int)gt.size() : (int)gs.size();
+            for (int coord = 0; coord < (seq ? 4 : 3); ++coord) {
+                int* idx = coord == 0 ? &ic : coord == 1 ? &it : coord == 2 ? &is : &ik;
+                int n = coord == 0 ? (int)gc.size() : coord == 1 ? (int)gt.size() : coord == 2 ? (int)gs.size()
+                                                                                              : (int)gk.size();
                 auto at = [&](int v) {
-                    return coord == 0 ? eval(v, it, is) : coord == 1 ? eval(ic, v, is) : eval(ic, it, v);
+                    return coord == 0 ? eval(v, it, is, ik) : coord == 1 ? eval(ic, v, is, ik)
+                           : coord == 2 ? eval(ic, it, v, ik) : eval(ic, it, is, v);
                 };
                 // raise while bandwidth improves; if the first raise does not
                 // help, try lowering the same way
@@ -206,6 +219,7 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
             overall.channels = gc[ic];
             overall.nthreads = gt[it];
             overall.slot_bytes = gs[is];
+            overall.cluster = gk[ik] > 1 ? gk[ik] : 0;
         }
     }
     *best = overall;

@@ -299,6 +299,15 @@ typedef enum {
  *                 send from a buffer write straight into the receiver's
  *                 destination buffer (one copy, no FIFO) and keeps FIFOs for
  *                 transfers that are forwarded or reduced.
+ *   cluster     : sequential engine only: run every threadblock program on a
+ *                 thread-block cluster of this many CTAs (2, 4 or 8).  The
+ *                 cluster's first CTA waits for the flags and counters and
+ *                 posts them; every CTA moves its 16-byte-granular share of
+ *                 each slot between two cluster barriers.  Same steps,
+ *                 channels and FIFOs (one program per channel); the data of a
+ *                 step moves on `cluster` SMs instead of one, for the
+ *                 latency-bound sizes where a single CTA's data time sets the
+ *                 length of every hop.
  *   codegen     : 0 (default): the library's kernels interpret the plan's
  *                 step records.  1: ccl_plan_create generates CUDA source
  *                 for this one plan (ReSCCL report, §II.2: a kernel per
@@ -334,6 +343,7 @@ typedef struct {
     int32_t tb_budget;   /* CCL_TB_BALANCED: threadblocks to aim for (0: 256) */
     int32_t engine;      /* CCL_ENGINE_* */
     int32_t codegen;     /* 1: run a kernel generated and compiled for this plan (see below) */
+    int32_t cluster;     /* sequential engine: CTAs per threadblock program (0 or 1: one; 2, 4, 8) */
 } ccl_plan_opts_t;
 
 void ccl_plan_opts_default(ccl_plan_opts_t* o);
@@ -428,6 +438,8 @@ typedef struct {
     int32_t kernel_build;        /* thread limit the launched kernel was built for: 512 (eight
                                     16-byte vectors in flight per thread) or 1024 (four); 0 from
                                     ccl_plan_check, which does not choose */
+    int32_t cluster;             /* CTAs per threadblock program (1 unless the sequential engine runs
+                                    on clusters) */
     int32_t codegen;             /* 1: the plan runs its generated kernel */
     double codegen_ms;           /* host time to generate and compile it (0 when cached) */
 } ccl_plan_stats_t;
@@ -597,7 +609,7 @@ ccl_status_t ccl_allreduce_ring_noalloc(void* const* in_bufs, void* const* out_b
  * x protocol (simple / LL) x transport (FIFO / direct) x engine (pipelined
  * / sequential; no LL on the sequential engine) make twelve subspaces; in
  * each, coordinate descent over channels, threads and slot
- * size, driven by a caller-supplied probe that returns the bandwidth of a
+ * size (and CTAs per program on the sequential engine), driven by a caller-supplied probe that returns the bandwidth of a
  * configuration (any unit, <= 0 = cannot run).  start (nullable) is the first point; best gets
  * the winner, *best_bw its bandwidth, *probes the number of distinct
  * configurations probed.  Host only; no device is touched unless the probe

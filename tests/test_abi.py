@@ -113,3 +113,15 @@ def test_layout_header_codes_match_the_c_abi():
     assert len(layout) >= 18
     for name, v in layout.items():
         assert abi.get(name) == v, name
+
+
+def test_default_options_set_every_field():
+    """ccl_plan_opts_default writes every field of ccl_plan_opts_t: the
+    result does not depend on what the memory held before."""
+    import collective_communication_schedule_gb300 as ccl
+    a = ccl.PlanOpts.from_buffer_copy(b"\x5a" * ctypes.sizeof(ccl.PlanOpts))
+    b = ccl.PlanOpts.from_buffer_copy(b"\x00" * ctypes.sizeof(ccl.PlanOpts))
+    ccl.lib.ccl_plan_opts_default(ctypes.byref(a))
+    ccl.lib.ccl_plan_opts_default(ctypes.byref(b))
+    for f, _ in ccl.PlanOpts._fields_:
+        assert getattr(a, f) == getattr(b, f), f

@@ -482,14 +482,15 @@ def test_coordinate_descent_treats_infeasible_points_as_zero():
 def test_coordinate_descent_plateau_stops_early():
     # twelve subspaces (policy x protocol x transport x engine, minus LL on
     # the sequential engine): on a flat surface each tries one step up and
-    # one down per coordinate (at most 6 probes), plus the start
+    # one down per coordinate (at most 6 probes; 8 on the sequential engine,
+    # which also has the CTAs per program), plus the start
     seen = set()
 
     def flat(o):
         seen.add((o.tb_alloc, o.protocol, o.link_mode, o.engine))
         return 1.0
     best, bw, n = ccl.tune_search(flat)
-    assert bw == 1.0 and n <= 1 + 12 * 6
+    assert bw == 1.0 and n <= 1 + 8 * 6 + 4 * 8
     assert len(seen) == 12
     assert (ccl.PROTO_LL, ccl.ENGINE_SEQUENTIAL) not in {(p, e) for _, p, _, e in seen}
 
@@ -627,3 +628,28 @@ def test_coordinate_descent_visits_both_transports():
     assert {m for m, _, _ in seen} == {ccl.LINK_FIFO, ccl.LINK_DIRECT}
     assert len(seen) == 8
     assert best.link_mode == ccl.LINK_DIRECT and bw == pytest.approx(1.5)
+
+
+def test_cluster_option_is_validated_and_reported():
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 8)
+    st = s.check(4096, F32, engine=ccl.ENGINE_SEQUENTIAL, cluster=4)
+    assert st.cluster == 4 and st.nthreadblocks == 8
+    assert s.check(4096, F32).cluster == 1
+    for bad in (3, 16, -1):
+        with pytest.raises(ccl.CclError) as e:
+            s.check(4096, F32, engine=ccl.ENGINE_SEQUENTIAL, cluster=bad)
+        assert e.value.code == 1
+    with pytest.raises(ccl.CclError) as e:
+        s.check(4096, F32, cluster=2)          # pipelined engine
+    assert e.value.code == 5
+
+
+def test_coordinate_descent_tries_clusters_on_the_sequential_engine():
+    seen = set()
+
+    def probe(o):
+        seen.add((o.engine, o.cluster))
+        return 1.0 + (o.cluster if o.engine == ccl.ENGINE_SEQUENTIAL else 0) + 0.001 * o.channels
+    best, bw, n = ccl.tune_search(probe)
+    assert best.engine == ccl.ENGINE_SEQUENTIAL and best.cluster == 8
+    assert all(c in (0, 1) for e, c in seen if e == ccl.ENGINE_PIPELINED)

@@ -92,3 +92,11 @@ def test_debug_hook_is_refused_on_a_generated_plan(ccl):
     with pytest.raises(ccl.CclError) as e:
         plan.debug_drop_signal(0, 0)
     assert e.value.code == 5
+
+
+def test_generated_sequential_kernel_on_clusters(ccl):
+    got, want, plan = run_case(ccl, 0, 8, 0, 3001, F32, "normal", 77, codegen=1, engine=1, cluster=4, channels=2,
+                               slot_bytes=4096)
+    st = plan.stats()
+    assert st.codegen == 1 and st.cluster == 4
+    assert_bitexact(got, want)

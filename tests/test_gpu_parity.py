@@ -389,3 +389,17 @@ def test_inplace_ring_allreduce_bitexact(ccl, fuse, opts, dtype):
     plan.status()
     want, _, _ = oracle.run(ops, R, nch, ce, dtype, ins)
     assert_bitexact(to_host(d, dtype), want)
+
+
+@pytest.mark.parametrize("cluster", [2, 4, 8])
+def test_sequential_engine_on_clusters_bitexact(ccl, cluster):
+    """Every threadblock program on a cluster of CTAs (the first waits and
+    posts, each moves its share of a slot): ragged chunks, several slots per
+    piece, FIFO and direct transport, every dtype."""
+    cases = [(0, 8, 0, 4099, F32, True, 0), (0, 5, 0, 1000, BF16, "nochain", 1), (1, 8, 0, 3001, F16, False, 1),
+             (2, 8, 0, 777, BF16, True, 0), (3, 4, 2, 2048, F32, "nochain", 1), (0, 8, 0, 3, I32, True, 0)]
+    for kind, R, G, ce, dtype, fuse, lm in cases:
+        got, want, plan = run_case(ccl, kind, R, G, ce, dtype, DIST[dtype], 31, fuse=fuse, link_mode=lm,
+                                   engine=ccl.ENGINE_SEQUENTIAL, cluster=cluster, channels=2, slot_bytes=4096)
+        assert plan.stats().cluster == cluster
+        assert_bitexact(got, want)

@@ -199,3 +199,23 @@ def test_execute_host_async_pipelines_two_plans_and_reuses_buffers(ccl):
             want, _, _ = oracle.run(ops, R, nch, ce, dt, host)
             got = [t.numpy().view(np.uint16) if dt != F32 else t.numpy() for t in h_out]
             assert_bitexact(got, want)
+
+
+def test_lost_signal_on_a_cluster_times_out_and_device_stays_usable(ccl):
+    """The same host-made fault on the sequential engine with clusters of
+    four CTAs: the leader's wait gives up, every CTA of every cluster
+    leaves, the status reads CCL_ERR_TIMEOUT."""
+    import torch
+    import datagen
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 4)
+    plan = ccl.Plan(s, 1024, F32, timeout_ms=50, engine=ccl.ENGINE_SEQUENTIAL, cluster=4)
+    plan.debug_drop_signal(0, 0)
+    ins = to_device(datagen.rank_inputs(0, "normal", 4, 4 * 1024, F32), F32)
+    outs = empty_outputs(4, 4 * 1024, F32)
+    plan.execute(ins, outs)
+    torch.cuda.synchronize()
+    with pytest.raises(ccl.CclError) as ei:
+        plan.status()
+    assert ei.value.code == 8
+    got, want, _ = run_case(ccl, 0, 4, 0, 1024, F32, "normal", 0, engine=ccl.ENGINE_SEQUENTIAL, cluster=4)
+    assert_bitexact(got, want)
