@@ -597,18 +597,20 @@ __device__ __forceinline__ unsigned slot_index(unsigned exec_mod, const DLink& L
     return (exec_mod * (unsigned)L.total_mod + (unsigned)seq_mod) % S;
 }
 
-__device__ __forceinline__ SlotCond first_slot_cond(const KParams& P, const DRec& st, unsigned exec_mod)
+// Lin / Lout: the step's links (null when absent)
+__device__ __forceinline__ SlotCond first_slot_cond(const KParams& P, const DRec& st, unsigned exec_mod,
+                                                    const DLink* Lin, const DLink* Lout)
 {
     SlotCond c{nullptr, nullptr, 0, 0};
     const unsigned S = (unsigned)P.S;
-    if (st.link_in >= 0 && !P.ll) {   // LL: the data path polls the lines
-        const DLink& L = P.links[st.link_in];
+    if (Lin && !P.ll) {   // LL: the data path polls the lines
+        const DLink& L = *Lin;
         const unsigned long long s = (unsigned long long)(P.exec * L.total) + st.seq_in;
         c.in = P.flags + L.flag_base + slot_index(exec_mod, L, st.seq_in_mod, S);
         c.vin = s + 1;
     }
-    if (st.link_out >= 0) {
-        const DLink& L = P.links[st.link_out];
+    if (Lout) {
+        const DLink& L = *Lout;
         const unsigned long long s = (unsigned long long)(P.exec * L.total) + st.seq_out;
         if (s + 1 > (unsigned long long)P.S) {
             c.out = P.flags + L.flag_base + S + slot_index(exec_mod, L, st.seq_out_mod, S);
@@ -616,6 +618,12 @@ __device__ __forceinline__ SlotCond first_slot_cond(const KParams& P, const DRec
         }
     }
     return c;
+}
+
+__device__ __forceinline__ SlotCond first_slot_cond(const KParams& P, const DRec& st, unsigned exec_mod)
+{
+    return first_slot_cond(P, st, exec_mod, st.link_in >= 0 ? P.links + st.link_in : nullptr,
+                           st.link_out >= 0 ? P.links + st.link_out : nullptr);
 }
 
 // Poll the conditions of steps [s0, s1) (records in the ring) -- the first
@@ -1213,7 +1221,7 @@ static __device__ void data_warps(const KParams& P, CtlShared* sh)
 // data; no overlap of one step's waits with another step's data.
 // ----------------------------------------------------------------------
 struct SeqShared {
-    DRec rec;
+    DRec rec[2];   // the current step's record and the next one, arriving by cp.async
     int abort;
 };
 
@@ -1471,42 +1479,6 @@ __device__ __forceinline__ long long gen_seg_step(long long base, int n, int w, 
     return base + (long long)w0 * n + (long long)pos * wl + (mb - w0);
 }
 
-// sequential engine: thread 0 waits for the step's counters, then the CTA
-// runs the step; false when a wait gave up
-template <int U>
-__device__ __forceinline__ bool gen_seq_step(const KParams& P, int* abort, const GenStep& g, const GenInstr& gi,
-                                             const int2* dep, int m, int si, unsigned exec_mod)
-{
-    unsigned long long t_start = 0, waited = 0;
-    if (seq_leader(P)) {
-        if (P.timeline) t_start = gtimer();
-        int ok = *(volatile int*)P.status == 0;
-        if (ok && gi.ndep > 0) ok = wait_gen_deps(P, gi, dep, g.st.mb, m, si, waited);
-        set_group_flag(P, abort, !ok);
-    }
-    group_sync(P);
-    if (leader_flag(P, abort)) return false;
-    return seq_step<U>(P, abort, g.st, g.st.link_in >= 0 ? &g.lin : nullptr, g.st.link_out >= 0 ? &g.lout : nullptr,
-                       si, exec_mod, t_start, waited);
-}
-
-// pipelined engine, issuing thread: the step's counters and drain, then its
-// slots handed out (each slot's flags polled as it comes); false after a
-// failed wait (the abort command is published)
-__device__ __forceinline__ bool gen_issue_step(const KParams& P, CtlShared* sh, const GenStep& g, const GenInstr& gi,
-                                               const int2* dep, int m, int drain, int si, int& head, unsigned exec_mod)
-{
-    const unsigned long long t_start = gtimer();
-    unsigned long long waited = 0;
-    if (!wait_drain(P, sh, drain, si, head) ||
-        (gi.ndep > 0 && !wait_gen_deps(P, gi, dep, g.st.mb, m, si, waited))) {
-        publish_cmd(sh, head, 2, 4 * P.timeout_ns);
-        return false;
-    }
-    return issue_step(P, sh, g.st, g.st.link_in >= 0 ? &g.lin : nullptr, g.st.link_out >= 0 ? &g.lout : nullptr, si,
-                      head, 0, exec_mod, t_start, waited);
-}
-
 // The steps of one instruction for micro-batches [w0, w1): the piece of each
 // (the planner's split of the instruction's st.nelem elements into m
 // pieces), its FIFO slots, the sequence numbers (q: the threadblock's
@@ -1542,36 +1514,148 @@ __device__ __forceinline__ void gen_piece(const GenInstr& gi, int m, long long v
     g.st.mb = mb;
 }
 
+// sequential engine: thread 0 of every CTA writes the piece's step into
+// the CTA's shared `gs` (and keeps the link counters q), the leader waits for
+// its counters, then the CTA (the cluster) runs it
 template <int U>
-__device__ __noinline__ bool gen_seq_block(const KParams& P, int* abort, const GenInstr& gi, const int2* dep, int w0,
-                                           int w1, int m, long long ve, long long slot_elems, int S, int& si,
-                                           long long* q, unsigned exec_mod)
+__device__ __noinline__ bool gen_seq_block(const KParams& P, int* abort, GenStep* gs, const GenInstr& gi,
+                                           const int2* dep, int w0, int w1, int m, long long ve,
+                                           long long slot_elems, int S, int& si, long long* q, unsigned exec_mod)
 {
 #pragma unroll 1
     for (int mb = w0; mb < w1; ++mb, ++si) {
-        GenStep g;
-        gen_piece(gi, m, ve, slot_elems, S, mb, q, g);
-        g.st.drain = -1;
-        if (!gen_seq_step<U>(P, abort, g, gi, dep, m, si, exec_mod)) return false;
+        unsigned long long t_start = 0, waited = 0;
+        if (threadIdx.x == 0) {
+            gen_piece(gi, m, ve, slot_elems, S, mb, q, *gs);
+            gs->st.drain = -1;
+        }
+        if (seq_leader(P)) {
+            if (P.timeline) t_start = gtimer();
+            int ok = *(volatile int*)P.status == 0;
+            if (ok && gi.ndep > 0) ok = wait_gen_deps(P, gi, dep, mb, m, si, waited);
+            set_group_flag(P, abort, !ok);
+        }
+        group_sync(P);
+        if (leader_flag(P, abort)) return false;
+        if (!seq_step<U>(P, abort, gs->st, gs->st.link_in >= 0 ? &gs->lin : nullptr,
+                         gs->st.link_out >= 0 ? &gs->lout : nullptr, si, exec_mod, t_start, waited))
+            return false;
+        __syncthreads();   // gs takes the next piece
     }
     return true;
 }
 
+// Poll, in one round trip of relaxed loads, the first-slot flags and the
+// first kDepPoll dependency counters of pieces g[0..n) of one instruction;
+// the length (>= 1) of the leading run whose words are all ready, after one
+// acquire fence, or 0 when the wait for g[0] fails.
+__device__ __forceinline__ int gen_poll(const KParams& P, const GenStep* g, int n, const GenInstr& gi,
+                                        const int2* dep, int m, unsigned exec_mod, int si,
+                                        unsigned long long& waited)
+{
+    constexpr int kC = 2 + kDepPoll;
+    const unsigned long long* ptr[kLook * kC];
+    unsigned long long want[kLook * kC];
+    const unsigned long long base = (unsigned long long)(P.exec * P.m);
+#pragma unroll
+    for (int i = 0; i < kLook; ++i) {
+        for (int k = 0; k < kC; ++k) ptr[i * kC + k] = nullptr;
+        if (i >= n) continue;
+        const SlotCond c = first_slot_cond(P, g[i].st, exec_mod, g[i].st.link_in >= 0 ? &g[i].lin : nullptr,
+                                           g[i].st.link_out >= 0 ? &g[i].lout : nullptr);
+        ptr[i * kC] = c.in;
+        want[i * kC] = c.vin;
+        ptr[i * kC + 1] = c.out;
+        want[i * kC + 1] = c.vout;
+        int k = 0;
+        for (int e = 0; e < gi.ndep && k < kDepPoll; ++e) {
+            const int2 d = dep[gi.dep_first + e];
+            const int mb = g[i].st.mb;
+            if ((d.y & 1) || ((d.y & 2) && mb == 0)) {
+                ptr[i * kC + 2 + k] = P.counters + d.x;
+                want[i * kC + 2 + k] = base + ((d.y & 2) && mb == 0 ? (unsigned long long)m : (unsigned long long)mb + 1);
+                ++k;
+            }
+        }
+    }
+    unsigned long long t0 = 0;
+    unsigned spins = 0;
+    while (true) {
+        unsigned long long x[kLook * kC];
+#pragma unroll
+        for (int k = 0; k < kLook * kC; ++k) x[k] = ptr[k] ? ld_relaxed(ptr[k]) : ~0ull;
+        int r = 0;
+        bool ok = true;
+#pragma unroll
+        for (int i = 0; i < kLook; ++i) {
+#pragma unroll
+            for (int k = 0; k < kC; ++k)
+                if (ptr[i * kC + k] && x[i * kC + k] < want[i * kC + k]) ok = false;
+            if (ok && i < n) r = i + 1;
+        }
+        if (r > 0) {
+            fence_acq_rel_gpu();
+            if (t0) waited += gtimer() - t0;
+            return r;
+        }
+        if (!t0) t0 = gtimer();
+        ++spins;
+        if ((spins & 15) == 0) {
+            if (*(volatile int*)P.status != 0) return 0;
+            if (gtimer() - t0 > P.timeout_ns) {
+                record_timeout(P, si, ptr[0] && x[0] < want[0] ? WAIT_FULL : ptr[1] && x[1] < want[1] ? WAIT_FREE
+                                                                                                    : WAIT_DEP);
+                return 0;
+            }
+        }
+        if (spins > 64) __nanosleep(32);
+    }
+}
+
+// pipelined engine, issuing thread: the pieces of one instruction for
+// micro-batches [w0, w1), kLook at a time: one batched poll of their first
+// slots and counters, then each piece's drain and remaining counters, then
+// its slots handed out
 static __device__ __noinline__ bool gen_issue_block(const KParams& P, CtlShared* sh, const GenInstr& gi,
                                                     const int2* dep, int w0, int w1, int m, long long ve,
                                                     long long slot_elems, int S, int& si, int& head, long long* q,
                                                     unsigned exec_mod)
 {
+    const unsigned long long limit = 4 * P.timeout_ns;
 #pragma unroll 1
-    for (int mb = w0; mb < w1; ++mb, ++si) {
-        GenStep g;
-        gen_piece(gi, m, ve, slot_elems, S, mb, q, g);
-        int drain = -1;
-        if (gi.drain_kind == 2) drain = gi.drain_const;
-        else if (gi.drain_kind == 3) drain = si - gi.drain_dk;
-        else if (gi.drain_kind == 4) drain = (int)gen_seg_step(gi.p_base, gi.p_n, gi.p_w, gi.p_pos, mb, m);
-        g.st.drain = drain;
-        if (!gen_issue_step(P, sh, g, gi, dep, m, drain, si, head, exec_mod)) return false;
+    for (int b0 = w0; b0 < w1; b0 += kLook) {
+        const int n = w1 - b0 < kLook ? w1 - b0 : kLook;
+        GenStep g[kLook];
+        for (int i = 0; i < n; ++i) {
+            const int mb = b0 + i;
+            gen_piece(gi, m, ve, slot_elems, S, mb, q, g[i]);
+            int drain = -1;
+            if (gi.drain_kind == 2) drain = gi.drain_const;
+            else if (gi.drain_kind == 3) drain = si + i - gi.drain_dk;
+            else if (gi.drain_kind == 4) drain = (int)gen_seg_step(gi.p_base, gi.p_n, gi.p_w, gi.p_pos, mb, m);
+            g[i].st.drain = drain;
+        }
+        int i = 0;
+        while (i < n) {
+            const unsigned long long t_start = gtimer();
+            unsigned long long waited = 0;
+            const int r = gen_poll(P, g + i, n - i, gi, dep, m, exec_mod, si, waited);
+            if (r == 0) {
+                publish_cmd(sh, head, 2, limit);
+                return false;
+            }
+            for (int j = 0; j < r; ++j, ++i, ++si) {
+                const GenStep& s = g[i];
+                if (!wait_drain(P, sh, s.st.drain, si, head) ||
+                    (gi.ndep > kDepPoll && !wait_gen_deps(P, gi, dep, s.st.mb, m, si, waited))) {
+                    publish_cmd(sh, head, 2, limit);
+                    return false;
+                }
+                if (!issue_step(P, sh, s.st, s.st.link_in >= 0 ? &s.lin : nullptr,
+                                s.st.link_out >= 0 ? &s.lout : nullptr, si, head, 1, exec_mod, t_start, waited))
+                    return false;
+            }
+        }
     }
     return true;
 }

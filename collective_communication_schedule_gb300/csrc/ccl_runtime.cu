@@ -71,9 +71,10 @@ template __global__ void ccl_exec_kernel<false, 1024>(const __grid_constant__ KP
 template __global__ void ccl_exec_kernel<false, 512>(const __grid_constant__ KParams P);
 template __global__ void ccl_exec_kernel<true, kMaxThreadsLL>(const __grid_constant__ KParams P);
 
-// The library's sequential-engine kernel: thread 0 reads each step record
-// into shared memory and waits for its dependency counters, then the CTA
-// runs the step (seq_step).
+// The library's sequential-engine kernel: thread 0 of every CTA copies the
+// step records into shared memory by cp.async, one step ahead, the leader
+// waits for each step's dependency counters, then the CTA (the cluster) runs
+// the step (seq_step).
 template <int MAXT>
 __global__ void __launch_bounds__(MAXT, 1) ccl_exec_seq_kernel(const __grid_constant__ KParams P)
 {
@@ -84,24 +85,40 @@ __global__ void __launch_bounds__(MAXT, 1) ccl_exec_seq_kernel(const __grid_cons
     const int b0 = P.tb_begin[prog], b1 = P.tb_begin[prog + 1];
     const unsigned exec_mod = (unsigned)(P.exec % P.S);
     const bool leader = seq_leader(P);
-    const DRec& st = sh.rec;
     if (P.cluster > 1) group_sync(P);   // every CTA of the cluster has started
+    if (tid == 0 && b0 < b1) {
+        prefetch_rec(&sh.rec[0], P.recs + b0);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
     for (int si = b0; si < b1; ++si) {
         unsigned long long t_start = 0, waited = 0;
-        if (tid == 0) sh.rec = P.recs[si];   // every CTA of the program reads the record
+        const DRec& st = sh.rec[(si - b0) & 1];
+        if (tid == 0) {
+            // this step's record is here; the next one starts on its way
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            if (si + 1 < b1) {
+                prefetch_rec(&sh.rec[(si + 1 - b0) & 1], P.recs + si + 1);
+                asm volatile("cp.async.commit_group;" ::: "memory");
+            }
+        }
         if (leader) {
             if (P.timeline) t_start = gtimer();
             int ok = *(volatile int*)P.status == 0;
-            if (ok && sh.rec.dep_count > 0)
-                ok = wait_deps(P, P.deps + sh.rec.dep_begin, sh.rec.dep_count, si, waited);
+            if (ok && st.dep_count > 0) ok = wait_deps(P, P.deps + st.dep_begin, st.dep_count, si, waited);
             set_group_flag(P, &sh.abort, !ok);
         }
         group_sync(P);
-        if (leader_flag(P, &sh.abort)) return;
+        if (leader_flag(P, &sh.abort)) {
+            if (tid == 0) asm volatile("cp.async.wait_all;" ::: "memory");   // no copy left in flight
+            return;
+        }
         const DLink* Lin = st.link_in >= 0 ? P.links + st.link_in : nullptr;
         const DLink* Lout = st.link_out >= 0 ? P.links + st.link_out : nullptr;
-        if (!seq_step<U>(P, &sh.abort, st, Lin, Lout, si, exec_mod, t_start, waited)) return;
-        __syncthreads();   // the record is read again by thread 0 for the next step
+        if (!seq_step<U>(P, &sh.abort, st, Lin, Lout, si, exec_mod, t_start, waited)) {
+            if (tid == 0) asm volatile("cp.async.wait_all;" ::: "memory");
+            return;
+        }
+        __syncthreads();   // this record's buffer takes the record after next
     }
 }
 
