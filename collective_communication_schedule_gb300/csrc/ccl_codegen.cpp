@@ -323,7 +323,7 @@ std::string generate_plan_source(const PlanImage& img, int build, std::string* w
     for (int b = 0; b < img.ntb; ++b) {
         if (seq)
             o += "static __device__ __noinline__ void gtb" + std::to_string(b) +
-                 "(const KParams& P, int* abort, GenStep* gs)\n{\n";
+                 "(const KParams& P, int* go, GenStep* gs)\n{\n";
         else o += "static __device__ __noinline__ void gtb" + std::to_string(b) + "(const KParams& P, CtlShared* sh)\n{\n";
         o += "    const unsigned exec_mod = (unsigned)(P.exec % P.S);\n";
         if (!seq) o += "    int head = 0;\n";
@@ -340,7 +340,7 @@ std::string generate_plan_source(const PlanImage& img, int build, std::string* w
             o += "#pragma unroll 1\n        for (int j = " + std::to_string(first) + "; j < " + std::to_string(first + n) +
                  "; ++j)\n";
             if (seq)
-                o += "            if (!gen_seq_block<" + std::to_string(U) + ">(P, abort, gs, kGen[j], kGenDep, w0, w1, " +
+                o += "            if (!gen_seq_block<" + std::to_string(U) + ">(P, go, gs, kGen[j], kGenDep, w0, w1, " +
                      geom + ", si, q, exec_mod)) return;\n";
             else
                 o += "            if (!gen_issue_block(P, sh, kGen[j], kGenDep, w0, w1, " + geom +
@@ -356,11 +356,11 @@ std::string generate_plan_source(const PlanImage& img, int build, std::string* w
          ", 1) ccl_gen_kernel(const __grid_constant__ ccl::KParams P)\n{\n";
     std::string sw = seq ? "switch (P.cluster > 1 ? blockIdx.x / P.cluster : blockIdx.x) {\n" : "switch (blockIdx.x) {\n";
     for (int b = 0; b < img.ntb; ++b)
-        sw += "    case " + std::to_string(b) + ": ccl::gtb" + std::to_string(b) + (seq ? "(P, &abort_flag, &gstep)" : "(P, &sh)") +
+        sw += "    case " + std::to_string(b) + ": ccl::gtb" + std::to_string(b) + (seq ? "(P, &go_flag, &gstep)" : "(P, &sh)") +
               "; break;\n";
     sw += "    default: break;\n    }\n";
     if (seq) {
-        o += "    __shared__ int abort_flag;\n    __shared__ __align__(16) ccl::GenStep gstep;\n";
+        o += "    __shared__ int go_flag;\n    __shared__ __align__(16) ccl::GenStep gstep;\n";
         o += "    if (P.cluster > 1) ccl::group_sync(P);   // every CTA of the cluster has started\n    " + sw;
     } else {
         o += "    __shared__ __align__(16) ccl::CtlShared sh;\n";

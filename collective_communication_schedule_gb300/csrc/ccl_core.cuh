@@ -1222,19 +1222,21 @@ static __device__ void data_warps(const KParams& P, CtlShared* sh)
 // ----------------------------------------------------------------------
 struct SeqShared {
     DRec rec[2];   // the current step's record and the next one, arriving by cp.async
-    int abort;
+    int go;        // thread 0's verdict on the current wait (1: the waits were met)
 };
 
 // A threadblock program of the sequential engine may run on a cluster of
-// P.cluster CTAs: the cluster's first CTA waits and posts, every CTA moves
-// its share of each slot.  group_sync is the barrier of all of them (a
-// cluster barrier with release / acquire at cluster scope, so the leader's
-// gpu-scope fence before its flag posts covers every CTA's stores).  The
-// leader hands its verdict on a wait to the others by storing it into each
-// CTA's shared flag before the barrier (set_group_flag); every CTA then
-// reads its own copy, so no CTA reads another's shared memory and none can
-// leave while another still accesses its memory.  A kernel with clusters
-// starts with one group_sync, after which every CTA's shared memory exists.
+// P.cluster CTAs: every CTA moves its share of each slot, and thread 0 of
+// every CTA waits for the step's counters and the slot's flags itself (the
+// same words; a verdict needs no hand-over between CTAs).  group_sync, after
+// the data, is the barrier of all of them (a cluster barrier with release /
+// acquire at cluster scope), after which the cluster's first CTA issues the
+// gpu-scope fence and posts, covering every CTA's stores.  No CTA leaves
+// early: after a failed wait (recorded in the status word) a CTA skips its
+// data and goes on through the same barriers as the others, whose waits
+// then give up at once on the recorded status -- so a cluster never waits
+// at a barrier for a CTA that has left.  No CTA touches another's shared
+// memory.
 __device__ __forceinline__ unsigned cluster_rank()
 {
     unsigned r;
@@ -1249,39 +1251,52 @@ __device__ __forceinline__ void group_sync(const KParams& P)
         __syncthreads();
     }
 }
-// the leader's store of v into `flag` of every CTA of its cluster
-__device__ __forceinline__ void set_group_flag(const KParams& P, int* flag, int v)
-{
-    if (P.cluster <= 1) {
-        *flag = v;
-        return;
-    }
-    for (int r = 0; r < P.cluster; ++r) {
-        unsigned remote;
-        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(flag)), "r"(r));
-        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
-    }
-}
-// the flag after group_sync (this CTA's copy)
-__device__ __forceinline__ int leader_flag(const KParams& P, const int* flag)
-{
-    (void)P;
-    return *(volatile const int*)flag;
-}
 __device__ __forceinline__ bool seq_leader(const KParams& P)
 {
     return threadIdx.x == 0 && (P.cluster <= 1 || cluster_rank() == 0);
 }
 
-// One step after its dependency counters are satisfied, run by every thread
-// of the CTA (of every CTA of the program's cluster) with the same record (the library's kernel reads it from shared
+// the LL data path of a sequential step, out of line (its polling loops
+// stay out of the register budget of the step's own code)
+static __device__ __noinline__ bool seq_move_ll(const SlotOp& op, int tid, int T, const KParams& P)
+{
+    switch (op.dtype) {
+    case CCL_F32: return move_ll_dt<CCL_F32>(op, tid, T, P);
+    case CCL_BF16: return move_ll_dt<CCL_BF16>(op, tid, T, P);
+    case CCL_F16: return move_ll_dt<CCL_F16>(op, tid, T, P);
+    default: return move_ll_dt<CCL_I32>(op, tid, T, P);
+    }
+}
+
+// Hint the lines of [p, p + bytes) into L2, one 128-byte line per thread
+// and round (addresses stay inside the range)
+__device__ __forceinline__ void prefetch_l2(const char* p, long long bytes, int tid, int T)
+{
+    if (!p) return;
+    for (long long off = (long long)tid * 128; off < bytes; off += (long long)T * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p + off));
+}
+
+// One step, run by every thread of the CTA (of every CTA of the program's
+// cluster) with the same record (the library's kernel reads it from shared
 // memory, a generated kernel builds it from constants).  Lin / Lout: its
-// links, or null.  `abort` is a shared flag; t_start and waited are thread
-// 0's stamps for the timeline.  False when a wait gave up.
+// links, or null.  deps / ndeps: dependency counters thread 0 waits for
+// before the first slot, just before that slot's flags (null when the
+// caller has waited already; pre_ok is then thread 0's verdict on that
+// wait).  `go` is the CTA's shared verdict word; t_start and waited are
+// thread 0's stamps for the timeline.  Never leaves early: a failed wait
+// skips the CTA's data and posts (the status word holds the failure).
+//
+// While the leader waits, every thread hints its share of the operands that
+// are not FIFO slots (the source and local buffers) into L2, so the data
+// phase after the wait reads them from L2.  With the LL protocol the
+// incoming slot's flag is not waited for: the threads poll the slot's lines
+// themselves (move_ll), and the outgoing slot gets lines instead of a full
+// flag, so no fence and flag round trip sits between two hops of a chain.
 template <int U>
-__device__ __forceinline__ bool seq_step(const KParams& P, int* abort, const DRec& st, const DLink* Lin,
-                                         const DLink* Lout, int si, unsigned exec_mod, unsigned long long t_start,
-                                         unsigned long long waited)
+__device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& st, const DLink* Lin,
+                                         const DLink* Lout, const DDep* deps, int ndeps, bool pre_ok, int si,
+                                         unsigned exec_mod, unsigned long long t_start, unsigned long long waited)
 {
     const int C = P.cluster > 1 ? P.cluster : 1;
     const int tid = threadIdx.x, T = blockDim.x;
@@ -1291,6 +1306,7 @@ __device__ __forceinline__ bool seq_step(const KParams& P, int* abort, const DRe
     const int es = (st.dtype == CCL_BF16 || st.dtype == CCL_F16) ? 2 : 4;
     const int esh = es == 2 ? 1 : 2;
     const long long ve = 16 / es;
+    const long long lls = P.ll ? 2 : 1;   // slot bytes per data byte
     const unsigned long long base_in = Lin ? (unsigned long long)(P.exec * Lin->total) : 0;
     const unsigned long long base_out = Lout ? (unsigned long long)(P.exec * Lout->total) : 0;
     const long long slot_elems = P.slot_bytes >> esh;
@@ -1303,17 +1319,12 @@ __device__ __forceinline__ bool seq_step(const KParams& P, int* abort, const DRe
     const char* srcb = st.src_buf >= 0 ? P.bufs[st.src_buf][st.src_rank] + st.src_off * es : nullptr;
     const char* locb = st.loc_buf >= 0 ? P.bufs[st.loc_buf][st.loc_rank] + st.loc_off * es : nullptr;
     char* dstb = st.dst_buf >= 0 ? P.bufs[st.dst_buf][st.dst_rank] + st.dst_off * es : nullptr;
+    const bool a_slot = Lin && st.kind != CCL_I_REDUCE;   // the first operand is the incoming slot
     const bool post = !(st.flags & STEP_NOPOST);
     unsigned long long t_pub = 0, t_done = 0;
     for (long long k = 0; k < nslots; ++k) {
         const unsigned long long sin = base_in + st.seq_in + k;
         const unsigned long long sout = base_out + st.seq_out + k;
-        if (linked) {
-            if (leader) set_group_flag(P, abort, wait_slots(P, Lin, Lout, sin, sout, in_idx, out_idx, 1, si, waited) == 0);
-            group_sync(P);
-            if (leader_flag(P, abort)) return false;
-        }
-        if (leader && P.timeline && k == 0) t_pub = gtimer();
         long long e0 = k * slot_elems;
         long long n = st.nelem - e0;
         if (n > slot_elems) n = slot_elems;
@@ -1327,17 +1338,34 @@ __device__ __forceinline__ bool seq_step(const KParams& P, int* abort, const DRe
             e0 += lo;
             n = hi - lo;
         }
-        const char* slot_in = Lin ? P.fifo + Lin->slot_base + (long long)in_idx * P.slot_stride + soff * es : nullptr;
-        char* slot_out = Lout ? P.fifo + Lout->slot_base + (long long)out_idx * P.slot_stride + soff * es : nullptr;
-        const char* a;
+        const char* a = (a_slot || !srcb) ? nullptr : srcb + e0 * es;
+        const char* b = locb ? locb + e0 * es : nullptr;
+        if (n > 0) {
+            prefetch_l2(a, n * es, tid, T);
+            prefetch_l2(b, n * es, tid, T);
+        }
+        if (linked || k == 0) {
+            if (tid == 0) {
+                int ok = k == 0 ? pre_ok : 1;
+                if (k == 0 && ok && ndeps > 0) ok = wait_deps(P, deps, ndeps, si, waited);
+                if (ok && linked) ok = wait_slots(P, Lin, Lout, sin, sout, in_idx, out_idx, 1, si, waited) != 0;
+                *go = ok;
+            }
+            __syncthreads();
+        }
+        // this CTA's verdict (written before the barrier above; the next
+        // write follows the group barrier below, which every thread reaches
+        // after this read)
+        const bool ok = *(volatile int*)go != 0;
+        if (leader && P.timeline && k == 0) t_pub = gtimer();
+        const char* slot_in = Lin ? P.fifo + Lin->slot_base + (long long)in_idx * P.slot_stride + lls * soff * es : nullptr;
+        char* slot_out = Lout ? P.fifo + Lout->slot_base + (long long)out_idx * P.slot_stride + lls * soff * es : nullptr;
         bool as = false;
-        if (Lin && st.kind != CCL_I_REDUCE) {
+        if (a_slot) {
             a = slot_in;
         } else {
-            a = srcb + e0 * es;
             as = (st.flags & STEP_SRC_STREAM) && P.stream_in;
         }
-        const char* b = locb ? locb + e0 * es : nullptr;
         const bool bs = (st.flags & STEP_LOC_STREAM) && P.stream_in;
         char* o1;
         char* o2 = nullptr;
@@ -1349,24 +1377,50 @@ __device__ __forceinline__ bool seq_step(const KParams& P, int* abort, const DRe
         } else {
             o1 = slot_out;
         }
-        if (n > 0) {
-            switch (st.dtype) {
-            case CCL_F32: move_part<CCL_F32, U>(red, a, as, b, bs, o1, o1s, o2, n, tid, T); break;
-            case CCL_BF16: move_part<CCL_BF16, U>(red, a, as, b, bs, o1, o1s, o2, n, tid, T); break;
-            case CCL_F16: move_part<CCL_F16, U>(red, a, as, b, bs, o1, o1s, o2, n, tid, T); break;
-            default: move_part<CCL_I32, U>(red, a, as, b, bs, o1, o1s, o2, n, tid, T); break;
+        if (ok && n > 0) {
+            if (P.ll && (a_slot || slot_out)) {
+                SlotOp op;
+                op.a = a;
+                op.b = b;
+                op.o1 = o1;
+                op.o2 = o2;
+                op.n = n;
+                op.red = red;
+                op.dtype = st.dtype;
+                op.as = as;
+                op.bs = bs;
+                op.o1s = o1s;
+                op.bulk = 0;
+                op.cmd = 0;
+                op.a_ll = a_slot;
+                op.o1_ll = !dstb;
+                op.o2_ll = dstb && slot_out;
+                op.fin = (unsigned)(sin + 1);
+                op.fout = (unsigned)(sout + 1);
+                // after a recorded failure the part is skipped; the leader
+                // sees the status before its next wait
+                if (*(volatile int*)P.status == 0 && !seq_move_ll(op, tid, T, P)) record_timeout(P, si, WAIT_FULL);
+            } else {
+                switch (st.dtype) {
+                case CCL_F32: move_part<CCL_F32, U>(red, a, as, b, bs, o1, o1s, o2, n, tid, T); break;
+                case CCL_BF16: move_part<CCL_BF16, U>(red, a, as, b, bs, o1, o1s, o2, n, tid, T); break;
+                case CCL_F16: move_part<CCL_F16, U>(red, a, as, b, bs, o1, o1s, o2, n, tid, T); break;
+                default: move_part<CCL_I32, U>(red, a, as, b, bs, o1, o1s, o2, n, tid, T); break;
+                }
             }
         }
         group_sync(P);
         if (leader) {
             if (P.timeline && k == nslots - 1) t_done = gtimer();
             // every thread's stores were observed at the barrier; the
-            // fence makes them visible at gpu scope before the flags
+            // fence makes them visible at gpu scope before the flags.  After
+            // a failed wait (or an LL part that gave up) nothing is posted.
+            const bool pst = post && ok && (!P.ll || *(volatile int*)P.status == 0);
             fence_acq_rel_gpu();
-            if (Lin && post) st_relaxed(P.flags + Lin->flag_base + S + in_idx, sin + 1);
-            if (Lout && post) st_relaxed(P.flags + Lout->flag_base + out_idx, sout + 1);
+            if (Lin && pst) st_relaxed(P.flags + Lin->flag_base + S + in_idx, sin + 1);
+            if (Lout && pst && !P.ll) st_relaxed(P.flags + Lout->flag_base + out_idx, sout + 1);
             if (k == nslots - 1) {
-                if (st.signal >= 0 && post)
+                if (st.signal >= 0 && pst)
                     st_relaxed(P.counters + st.signal, (unsigned long long)(P.exec * P.m + st.mb + 1));
                 if (P.timeline) {
                     unsigned long long* tl = P.timeline + 5ll * si;
@@ -1381,7 +1435,6 @@ __device__ __forceinline__ bool seq_step(const KParams& P, int* abort, const DRe
         if (++in_idx == S) in_idx = 0;
         if (++out_idx == S) out_idx = 0;
     }
-    return true;
 }
 
 
@@ -1515,31 +1568,28 @@ __device__ __forceinline__ void gen_piece(const GenInstr& gi, int m, long long v
 }
 
 // sequential engine: thread 0 of every CTA writes the piece's step into
-// the CTA's shared `gs` (and keeps the link counters q), the leader waits for
-// its counters, then the CTA (the cluster) runs it
+// the CTA's shared `gs` (and keeps the link counters q) and waits for its
+// counters, then the CTA (the cluster) runs it.  Always true: a failed wait
+// leaves the failure in the status word and the program runs on without
+// data (see seq_step).
 template <int U>
-__device__ __noinline__ bool gen_seq_block(const KParams& P, int* abort, GenStep* gs, const GenInstr& gi,
+__device__ __noinline__ bool gen_seq_block(const KParams& P, int* go, GenStep* gs, const GenInstr& gi,
                                            const int2* dep, int w0, int w1, int m, long long ve,
                                            long long slot_elems, int S, int& si, long long* q, unsigned exec_mod)
 {
 #pragma unroll 1
     for (int mb = w0; mb < w1; ++mb, ++si) {
         unsigned long long t_start = 0, waited = 0;
+        bool ok = true;
         if (threadIdx.x == 0) {
             gen_piece(gi, m, ve, slot_elems, S, mb, q, *gs);
             gs->st.drain = -1;
-        }
-        if (seq_leader(P)) {
             if (P.timeline) t_start = gtimer();
-            int ok = *(volatile int*)P.status == 0;
-            if (ok && gi.ndep > 0) ok = wait_gen_deps(P, gi, dep, mb, m, si, waited);
-            set_group_flag(P, abort, !ok);
+            if (gi.ndep > 0) ok = wait_gen_deps(P, gi, dep, mb, m, si, waited);
         }
-        group_sync(P);
-        if (leader_flag(P, abort)) return false;
-        if (!seq_step<U>(P, abort, gs->st, gs->st.link_in >= 0 ? &gs->lin : nullptr,
-                         gs->st.link_out >= 0 ? &gs->lout : nullptr, si, exec_mod, t_start, waited))
-            return false;
+        __syncthreads();   // gs holds the piece
+        seq_step<U>(P, go, gs->st, gs->st.link_in >= 0 ? &gs->lin : nullptr,
+                    gs->st.link_out >= 0 ? &gs->lout : nullptr, nullptr, 0, ok, si, exec_mod, t_start, waited);
         __syncthreads();   // gs takes the next piece
     }
     return true;

@@ -971,8 +971,6 @@ ccl_status_t build_plan_one(const ccl_schedule& s_in, int64_t ce, int32_t dtype,
     if (o.bulk != 0 && o.bulk != 1) return fail(CCL_ERR_INVALID_ARG, "bulk must be 0 or 1");
     if (o.engine != CCL_ENGINE_PIPELINED && o.engine != CCL_ENGINE_SEQUENTIAL)
         return fail(CCL_ERR_INVALID_ARG, "engine must be CCL_ENGINE_PIPELINED or CCL_ENGINE_SEQUENTIAL");
-    if (o.engine == CCL_ENGINE_SEQUENTIAL && o.protocol == CCL_PROTO_LL)
-        return fail(CCL_ERR_UNSUPPORTED, "the sequential engine has no LL data path");
     if (o.cluster != 0 && o.cluster != 1 && o.cluster != 2 && o.cluster != 4 && o.cluster != 8)
         return fail(CCL_ERR_INVALID_ARG, "cluster must be 0, 1, 2, 4 or 8");
     if (o.cluster > 1 && o.engine != CCL_ENGINE_SEQUENTIAL)

@@ -72,9 +72,11 @@ template __global__ void ccl_exec_kernel<false, 512>(const __grid_constant__ KPa
 template __global__ void ccl_exec_kernel<true, kMaxThreadsLL>(const __grid_constant__ KParams P);
 
 // The library's sequential-engine kernel: thread 0 of every CTA copies the
-// step records into shared memory by cp.async, one step ahead, the leader
-// waits for each step's dependency counters, then the CTA (the cluster) runs
-// the step (seq_step).
+// step records into shared memory by cp.async, one step ahead (the next
+// record travels while the current step runs and has arrived at the barrier
+// that ends the step), then the CTA (the cluster) runs each step (seq_step),
+// whose leader waits for the step's dependency counters together with its
+// first slot.
 template <int MAXT>
 __global__ void __launch_bounds__(MAXT, 1) ccl_exec_seq_kernel(const __grid_constant__ KParams P)
 {
@@ -85,40 +87,29 @@ __global__ void __launch_bounds__(MAXT, 1) ccl_exec_seq_kernel(const __grid_cons
     const int b0 = P.tb_begin[prog], b1 = P.tb_begin[prog + 1];
     const unsigned exec_mod = (unsigned)(P.exec % P.S);
     const bool leader = seq_leader(P);
-    if (P.cluster > 1) group_sync(P);   // every CTA of the cluster has started
     if (tid == 0 && b0 < b1) {
         prefetch_rec(&sh.rec[0], P.recs + b0);
         asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_all;" ::: "memory");
     }
+    // every CTA of the cluster has started; the first record is in place
+    group_sync(P);
     for (int si = b0; si < b1; ++si) {
         unsigned long long t_start = 0, waited = 0;
         const DRec& st = sh.rec[(si - b0) & 1];
-        if (tid == 0) {
-            // this step's record is here; the next one starts on its way
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            if (si + 1 < b1) {
-                prefetch_rec(&sh.rec[(si + 1 - b0) & 1], P.recs + si + 1);
-                asm volatile("cp.async.commit_group;" ::: "memory");
-            }
+        if (tid == 0 && si + 1 < b1) {
+            prefetch_rec(&sh.rec[(si + 1 - b0) & 1], P.recs + si + 1);
+            asm volatile("cp.async.commit_group;" ::: "memory");
         }
-        if (leader) {
-            if (P.timeline) t_start = gtimer();
-            int ok = *(volatile int*)P.status == 0;
-            if (ok && st.dep_count > 0) ok = wait_deps(P, P.deps + st.dep_begin, st.dep_count, si, waited);
-            set_group_flag(P, &sh.abort, !ok);
-        }
-        group_sync(P);
-        if (leader_flag(P, &sh.abort)) {
-            if (tid == 0) asm volatile("cp.async.wait_all;" ::: "memory");   // no copy left in flight
-            return;
-        }
+        if (leader && P.timeline) t_start = gtimer();
         const DLink* Lin = st.link_in >= 0 ? P.links + st.link_in : nullptr;
         const DLink* Lout = st.link_out >= 0 ? P.links + st.link_out : nullptr;
-        if (!seq_step<U>(P, &sh.abort, st, Lin, Lout, si, exec_mod, t_start, waited)) {
-            if (tid == 0) asm volatile("cp.async.wait_all;" ::: "memory");
-            return;
-        }
-        __syncthreads();   // this record's buffer takes the record after next
+        seq_step<U>(P, &sh.go, st, Lin, Lout, P.deps + st.dep_begin, st.dep_count, true, si, exec_mod, t_start,
+                    waited);
+        if (tid == 0) asm volatile("cp.async.wait_all;" ::: "memory");   // the next record is here
+        // every thread is done with this record's buffer (it takes the
+        // record after next) and sees the next one
+        __syncthreads();
     }
 }
 

@@ -3,8 +3,7 @@
 // AutoCCL report, "research method" 1-2: implementation parameters (here:
 // the threadblock allocation policy -- one per connection, or packed and
 // balanced --, the FIFO protocol, the transport and the execution engine --
-// pipelined or sequential; the sequential engine has no LL path, so twelve
-// subspaces in all) split the search space
+// pipelined or sequential: sixteen subspaces in all) split the search space
 // into small subspaces; inside each, the resource parameters nChannel, nThread and
 // chunk size are optimised one coordinate at a time, raising a parameter
 // while bandwidth keeps improving (bandwidth is unimodal in each of them).
@@ -161,7 +160,6 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
     ccl_plan_opts_t overall = base;
     double overall_bw = measure(base);
     for (int sub = 0; sub < 16; ++sub) {
-        if ((sub & 2) && (sub & 8)) continue;   // LL on the sequential engine: no such path
         ccl_plan_opts_t cur = base;
         // balanced = packed plus merged link-free threadblocks (the same as
         // packed when every threadblock has a FIFO link)

@@ -292,7 +292,9 @@ typedef enum {
  *                 CCL_ENGINE_SEQUENTIAL: a CTA runs its steps one after
  *                 another; thread 0 waits, every thread moves the slot, a CTA
  *                 barrier, thread 0 fences and posts.  Fewer hand-offs per
- *                 step (for the latency-bound sizes); no bulk copies, no LL.
+ *                 step (for the latency-bound sizes); no bulk copies.  With
+ *                 LL every thread polls the lines of its part of an
+ *                 incoming slot itself.
  *   link_mode   : transport of a transfer (AutoCCL report: implementation
  *                 parameter "transport").  CCL_LINK_FIFO stages every
  *                 transfer in the link FIFO; CCL_LINK_DIRECT lets a plain
@@ -607,7 +609,7 @@ ccl_status_t ccl_allreduce_ring_noalloc(void* const* in_bufs, void* const* out_b
  * The search of ccl_tune on its own (AutoCCL report, research method 1-2):
  * the implementation parameters threadblock policy (connection / balanced)
  * x protocol (simple / LL) x transport (FIFO / direct) x engine (pipelined
- * / sequential; no LL on the sequential engine) make twelve subspaces; in
+ * / sequential) make sixteen subspaces; in
  * each, coordinate descent over channels, threads and slot
  * size (and CTAs per program on the sequential engine), driven by a caller-supplied probe that returns the bandwidth of a
  * configuration (any unit, <= 0 = cannot run).  start (nullable) is the first point; best gets

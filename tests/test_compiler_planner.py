@@ -465,9 +465,9 @@ def test_coordinate_descent_reaches_the_peak_of_unimodal_surfaces(peak):
     best, bw, n = ccl.tune_search(_surface(peak))
     assert (best.channels, best.nthreads, best.slot_bytes) == peak
     assert bw == pytest.approx(1.0)
-    # twelve subspaces (policy x protocol x transport x engine, no LL on the
-    # sequential engine), each probing far fewer points than its 324-point grid
-    assert n <= 12 * 24
+    # sixteen subspaces (policy x protocol x transport x engine), each
+    # probing far fewer points than its 324-point grid
+    assert n <= 16 * 24
 
 
 def test_coordinate_descent_treats_infeasible_points_as_zero():
@@ -480,19 +480,18 @@ def test_coordinate_descent_treats_infeasible_points_as_zero():
 
 
 def test_coordinate_descent_plateau_stops_early():
-    # twelve subspaces (policy x protocol x transport x engine, minus LL on
-    # the sequential engine): on a flat surface each tries one step up and
-    # one down per coordinate (at most 6 probes; 8 on the sequential engine,
-    # which also has the CTAs per program), plus the start
+    # sixteen subspaces (policy x protocol x transport x engine): on a flat
+    # surface each tries one step up and one down per coordinate (at most 6
+    # probes; 8 on the sequential engine, which also has the CTAs per
+    # program), plus the start
     seen = set()
 
     def flat(o):
         seen.add((o.tb_alloc, o.protocol, o.link_mode, o.engine))
         return 1.0
     best, bw, n = ccl.tune_search(flat)
-    assert bw == 1.0 and n <= 1 + 8 * 6 + 4 * 8
-    assert len(seen) == 12
-    assert (ccl.PROTO_LL, ccl.ENGINE_SEQUENTIAL) not in {(p, e) for _, p, _, e in seen}
+    assert bw == 1.0 and n <= 1 + 8 * 6 + 8 * 8
+    assert len(seen) == 16
 
 
 def test_microbatch_window_is_used_when_the_fifo_holds_it():
@@ -572,9 +571,9 @@ def test_engine_option_is_validated():
     with pytest.raises(ccl.CclError) as e:
         s.check(4096, F32, engine=2)
     assert e.value.code == 1
-    with pytest.raises(ccl.CclError) as e:
-        s.check(4096, F32, engine=ccl.ENGINE_SEQUENTIAL, protocol=ccl.PROTO_LL)
-    assert e.value.code == 5
+    # LL slots on the sequential engine, also on clusters
+    ll = s.check(4096, F32, engine=ccl.ENGINE_SEQUENTIAL, protocol=ccl.PROTO_LL, cluster=4)
+    assert (ll.engine, ll.protocol, ll.cluster) == (ccl.ENGINE_SEQUENTIAL, ccl.PROTO_LL, 4)
 
 
 def test_coordinate_descent_visits_both_protocols():

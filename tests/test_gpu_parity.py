@@ -246,6 +246,47 @@ def test_ll_protocol_repeated_executions_and_windows(ccl):
         assert_bitexact(to_host(d_out, F32), want)
 
 
+@pytest.mark.parametrize("kind,R,G", BUILTINS)
+@pytest.mark.parametrize("dtype", [F32, BF16, F16, I32])
+def test_ll_protocol_on_the_sequential_engine_bitexact(ccl, kind, R, G, dtype):
+    """LL slots on the sequential engine (every thread polls the lines of its
+    part of a slot): one CTA per program and clusters of 2 and 4, several
+    slots per piece, two channels, FIFO and direct transport."""
+    # the 32-rank AllToAll's 416 FIFO threadblocks fit on the device only
+    # one CTA each: its clustered cases run direct copies, balanced
+    big = R >= 32
+    for lm, cluster in ((0, 0), (1, 2), (1, 4) if big else (0, 4)):
+        extra = dict(tb_alloc=2, tb_budget=64) if big and cluster else {}
+        got, want, plan = run_case(ccl, kind, R, G, 1024, dtype, DIST[dtype], 19, protocol=1, engine=1, channels=2,
+                                   slot_bytes=2048, link_mode=lm, cluster=cluster, nthreads=128, **extra)
+        assert_bitexact(got, want)
+        st = plan.stats()
+        assert (st.protocol, st.engine, st.cluster) == (1, 1, max(1, cluster))
+
+
+@pytest.mark.parametrize("cluster", [0, 8])
+def test_ll_sequential_repeated_executions_and_windows(ccl, cluster):
+    """Line flags of the sequential engine follow the slot sequence numbers
+    across executions, with micro-batch windows and FIFOs shorter than a
+    link's slots per execution."""
+    import torch
+    import datagen
+    import oracle
+    from gpu_helpers import oracle_program, to_device, empty_outputs, to_host
+    s = ccl.Schedule.builtin(0, 8)
+    plan = ccl.Plan(s, 4096, BF16, protocol=1, engine=1, cluster=cluster, nthreads=256, slot_bytes=2048,
+                    fifo_slots=3, microbatches=4, mb_window=2)
+    ops, nch = oracle_program(0, 8)
+    for it in range(5):
+        ins = datagen.rank_inputs(300 + it, "normal", 8, 8 * 4096, BF16)
+        d_out = empty_outputs(8, 8 * 4096, BF16)
+        plan.execute(to_device(ins, BF16), d_out)
+        torch.cuda.synchronize()
+        plan.status()
+        want, _, _ = oracle.run(ops, 8, nch, 4096, BF16, ins)
+        assert_bitexact(to_host(d_out, BF16), want)
+
+
 @pytest.mark.parametrize("R,tokens,seed", [(4, 64, 1), (8, 96, 2), (32, 48, 3)])
 @pytest.mark.parametrize("dtype", [F32, BF16, I32])
 @pytest.mark.parametrize("link_mode", [0, 1])
@@ -366,7 +407,7 @@ def test_program_that_writes_inputs_bitexact(ccl, fuse, opts):
 
 @pytest.mark.parametrize("fuse", [True, "nochain"])
 @pytest.mark.parametrize("opts", [dict(link_mode=0), dict(link_mode=1, tb_alloc=2), dict(link_mode=1, bulk=1),
-                                  dict(engine=1), dict(protocol=1)])
+                                  dict(engine=1), dict(protocol=1), dict(engine=1, protocol=1, cluster=4)])
 @pytest.mark.parametrize("dtype", [F32, BF16])
 def test_inplace_ring_allreduce_bitexact(ccl, fuse, opts, dtype):
     """In-place ring AllReduce (each rank's input is its output): the ring

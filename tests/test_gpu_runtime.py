@@ -203,8 +203,9 @@ def test_execute_host_async_pipelines_two_plans_and_reuses_buffers(ccl):
 
 def test_lost_signal_on_a_cluster_times_out_and_device_stays_usable(ccl):
     """The same host-made fault on the sequential engine with clusters of
-    four CTAs: the leader's wait gives up, every CTA of every cluster
-    leaves, the status reads CCL_ERR_TIMEOUT."""
+    four CTAs: every CTA of the waiting cluster gives up, the others skip
+    their data through the same barriers once the status is recorded, the
+    kernel ends and the status reads CCL_ERR_TIMEOUT."""
     import torch
     import datagen
     s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 4)
@@ -218,4 +219,29 @@ def test_lost_signal_on_a_cluster_times_out_and_device_stays_usable(ccl):
         plan.status()
     assert ei.value.code == 8
     got, want, _ = run_case(ccl, 0, 4, 0, 1024, F32, "normal", 0, engine=ccl.ENGINE_SEQUENTIAL, cluster=4)
+    assert_bitexact(got, want)
+
+
+def test_lost_consumed_flags_on_ll_sequential_time_out(ccl):
+    """LL slots on the sequential engine carry their data flags in the
+    lines, but a consumer still posts that it has read a slot: a threadblock
+    that posts nothing leaves its producer waiting for a slot to come free
+    (two-slot FIFOs, four slots per step), which gives up after 50 ms."""
+    import torch
+    import datagen
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 4)
+    plan = ccl.Plan(s, 4096, F32, timeout_ms=50, engine=ccl.ENGINE_SEQUENTIAL, protocol=ccl.PROTO_LL, cluster=2,
+                    fifo_slots=2, slot_bytes=4096)
+    n0 = sum(1 for st in plan.steps() if int(st["tb"]) == 0)
+    for i in range(n0):
+        plan.debug_drop_signal(0, i)
+    ins = to_device(datagen.rank_inputs(2, "normal", 4, 4 * 4096, F32), F32)
+    outs = empty_outputs(4, 4 * 4096, F32)
+    plan.execute(ins, outs)
+    torch.cuda.synchronize()
+    with pytest.raises(ccl.CclError) as ei:
+        plan.status()
+    assert ei.value.code == 8
+    got, want, _ = run_case(ccl, 0, 4, 0, 4096, F32, "normal", 2, engine=ccl.ENGINE_SEQUENTIAL, protocol=ccl.PROTO_LL,
+                            cluster=2, fifo_slots=2, slot_bytes=4096)
     assert_bitexact(got, want)
