@@ -512,15 +512,16 @@ def host_link(torch, items, stream):
     def both():
         copy_in()
         copy_out()
+    timed(both)   # first touch of the copy paths, not counted
     t_in, t_out, t_both = timed(copy_in), timed(copy_out), timed(both)
     return {"h2d": round(h2d / (t_in * 1e6), 1), "d2h": round(d2h / (t_out * 1e6), 1),
             "both_each_way": round(max(h2d, d2h) / (t_both * 1e6), 1)}
 
 
-# BASELINE workload 1: ring AllGather and ReduceScatter, 8 ranks, bf16, per-rank
-# buffer (AllGather output, ReduceScatter input) 32 KiB .. 2 MiB and 3 MiB,
-# channels 1..4, normal(0,1) seed 1.  Workload 0's int32 copy: ring AllReduce
-# 8 x 1 MiB, integers in [-1000, 1000], seed 0.
+# The message-size sweep: ring AllGather and ReduceScatter, 8 ranks, bf16,
+# per-rank buffer (AllGather output, ReduceScatter input) 32 KiB .. 2 MiB and
+# 3 MiB, channels 1..4, normal(0,1) seed 1.  The small ring AllReduce's int32
+# copy: 8 x 1 MiB, integers in [-1000, 1000], seed 0.
 SWEEP_KIB = [32, 64, 128, 256, 512, 1024, 2048, 3072]
 TABLE_DIR = os.path.join(ROOT, "collective_communication_schedule_gb300", "tables")
 
@@ -528,7 +529,7 @@ TABLE_DIR = os.path.join(ROOT, "collective_communication_schedule_gb300", "table
 def tuned_table(ccl, torch, datagen, kind, args):
     """The per-size tuning table of a sweep collective: the committed file
     when there is one (and --retune is not given), else tuned now (outside
-    any timed region) and written to gpurun_out/ when that folder exists."""
+    any timed region) and, with --table-out DIR, written there."""
     name = {1: "ring_allgather", 2: "ring_reducescatter"}[kind]
     path = os.path.join(TABLE_DIR, f"{name}_r8_bf16.json")
     if os.path.exists(path) and not args.retune:
@@ -541,16 +542,18 @@ def tuned_table(ccl, torch, datagen, kind, args):
     ins = [torch.from_numpy(a.view("int16")).cuda() for a in datagen.rank_inputs(1, "normal", R, nin, 1)]
     outs = [torch.empty(max(sizes) * (R if kind == 1 else 1), dtype=torch.int16, device="cuda") for _ in range(R)]
     rows = ccl.tune_table(s, 1, sizes, ins, outs, max_rounds=2, reps=5, max_channels=4)
-    out_dir = os.path.join(ROOT, "gpurun_out")
-    if os.path.isdir(out_dir):
+    out_dir = args.table_out
+    if out_dir:
+        os.makedirs(out_dir, exist_ok=True)
         ccl.write_tune_table(rows, 1, os.path.join(out_dir, os.path.basename(path)),
                              note=f"{name} R=8 bf16, channels <= 4, tuned on {torch.cuda.get_device_name()}")
     return rows, "tuned in this run"
 
 
 def run_sweep(ccl, torch, datagen, args, peak):
-    """Workload 1's sweep (every size x channels 1-4, AllGather and
-    ReduceScatter) and workload 0's int32 copy, each with its tuned
+    """The message-size sweep (every size x channels 1-4, AllGather and
+    ReduceScatter, 8 ranks bf16) and the 1 MiB ring AllReduce's int32 copy,
+    each with its tuned
     configuration; median of 20 executions with warm L2 and of 10 with L2
     flushed before each (flush outside the events), threadblock idle
     fractions from one instrumented execution.  Measured after the timed
@@ -615,7 +618,7 @@ def run_sweep(ccl, torch, datagen, args, peak):
                 except ccl.CclError as e:
                     rec["error"] = str(e)[:100]
                 out["rows"].append(rec)
-    # workload 0's int32 copy: the ring AllReduce row's options
+    # the small ring AllReduce's int32 copy: the f32 row's options
     row = [r for r in SUITE if r[0] == "ar_1m"][0]
     sched, popts = schedule_and_opts(ccl, 0, R, 0, row[8])
     ce = 1 * MiB // 4 // R
@@ -1055,6 +1058,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip idle fractions and L2-flushed timings")
     ap.add_argument("--no-sweep", action="store_true", help="skip the AllGather / ReduceScatter size sweep")
     ap.add_argument("--retune", action="store_true", help="tune the sweep's tables now instead of reading them")
+    ap.add_argument("--table-out", default="", help="directory to write tables tuned by --retune to")
     ap.add_argument("--only", default="", help="comma-separated subset of the suite (profiling)")
     ap.add_argument("--scale", type=float, default=1.0, help="chunk size factor (profiling)")
     ap.add_argument("--ablation", action="store_true", help="scheduler x threadblock allocation table")
