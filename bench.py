@@ -109,8 +109,8 @@ def recorded_traffic(kernel):
         with open(os.path.join(ROOT, "profiles", "roofline_traffic.txt")) as f:
             for line in f:
                 if line.strip() and not line.startswith("#"):
-                    k, v = line.split()
-                    kv[k] = v
+                    k, v = line.split(None, 1)
+                    kv[k] = v.strip()
         if kv.get("sources_sha256_16") != sources_hash() or kv.get("kernel") != kernel:
             return None
         return int(kv["traffic_bytes_per_launch"])
