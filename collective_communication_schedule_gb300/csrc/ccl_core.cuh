@@ -530,13 +530,20 @@ static __device__ bool wait_deps(const KParams& P, const DDep* deps, int n, int 
 // Batched form for consecutive slots k .. k+bmax-1 of one step: the flags of
 // all of them are polled with relaxed loads in one round trip; returns how
 // many leading slots are ready (>= 1), after one acquire fence, or 0 when the
-// wait for the first one fails.
+// wait for the first one fails.  out_rel0: the outgoing sequence of slot k
+// counted from the start of this execution.
 constexpr int kBatch = 4;
 static __device__ int wait_slots(const KParams& P, const DLink* Lin, const DLink* Lout, unsigned long long sin0,
-                          unsigned long long sout0, unsigned in_idx0, unsigned out_idx0, int bmax, int si,
-                          unsigned long long& waited)
+                          unsigned long long sout0, long long out_rel0, unsigned in_idx0, unsigned out_idx0, int bmax,
+                          int si, unsigned long long& waited)
 {
     const unsigned S = (unsigned)P.S;
+    // nothing to poll (an LL or absent incoming link, outgoing slots first
+    // used in this execution -- last read in an earlier one, a finished
+    // kernel): every slot is ready, with no fence
+    const bool poll_in = Lin && !P.ll;
+    const bool poll_out = Lout && out_rel0 + bmax - 1 >= (long long)P.S;
+    if (!poll_in && !poll_out) return bmax;
     unsigned long long t0 = 0;
     unsigned spins = 0;
     while (true) {
@@ -549,8 +556,8 @@ static __device__ int wait_slots(const KParams& P, const DLink* Lin, const DLink
                 unsigned ii = in_idx0 + i, io = out_idx0 + i;   // slot indices: i < kBatch, S >= 2
                 while (ii >= S) ii -= S;
                 while (io >= S) io -= S;
-                if (Lin && !P.ll) x[i] = ld_relaxed(P.flags + Lin->flag_base + ii);
-                if (Lout && sout0 + i + 1 > (unsigned long long)P.S) y[i] = ld_relaxed(P.flags + Lout->flag_base + S + io);
+                if (poll_in) x[i] = ld_relaxed(P.flags + Lin->flag_base + ii);
+                if (Lout && out_rel0 + i >= (long long)P.S) y[i] = ld_relaxed(P.flags + Lout->flag_base + S + io);
             }
         }
         int b = 0;
@@ -609,13 +616,13 @@ __device__ __forceinline__ SlotCond first_slot_cond(const KParams& P, const DRec
         c.in = P.flags + L.flag_base + slot_index(exec_mod, L, st.seq_in_mod, S);
         c.vin = s + 1;
     }
-    if (Lout) {
+    // the slot's previous use: in an earlier execution (a finished kernel:
+    // nothing to wait for) unless this execution has used S slots already
+    if (Lout && st.seq_out >= (long long)P.S) {
         const DLink& L = *Lout;
         const unsigned long long s = (unsigned long long)(P.exec * L.total) + st.seq_out;
-        if (s + 1 > (unsigned long long)P.S) {
-            c.out = P.flags + L.flag_base + S + slot_index(exec_mod, L, st.seq_out_mod, S);
-            c.vout = s + 1 - P.S;
-        }
+        c.out = P.flags + L.flag_base + S + slot_index(exec_mod, L, st.seq_out_mod, S);
+        c.vout = s + 1 - P.S;
     }
     return c;
 }
@@ -768,7 +775,7 @@ __device__ __forceinline__ bool issue_step(const KParams& P, CtlShared* sh, cons
         const unsigned long long sout = base_out + st.seq_out + k;
         if (linked && ready_slots == 0) {
             const int bmax = (int)((nslots - k) < kBatch ? (nslots - k) : kBatch);
-            ready_slots = wait_slots(P, Lin, Lout, sin, sout, in_idx, out_idx, bmax, si, waited);
+            ready_slots = wait_slots(P, Lin, Lout, sin, sout, st.seq_out + k, in_idx, out_idx, bmax, si, waited);
             if (ready_slots == 0) {
                 publish_cmd(sh, head, 2, limit);
                 return false;
@@ -830,7 +837,11 @@ __device__ __forceinline__ bool issue_step(const KParams& P, CtlShared* sh, cons
             op.cmd = 0;
             Release& r = sh->rel[q];
             const bool last_tile = u == ntiles - 1;
-            r.consumed = (Lin && post && last_tile) ? P.flags + Lin->flag_base + S + in_idx : nullptr;
+            // a consumed flag matters only to a producer that reuses the slot
+            // within this execution (S sequences later)
+            r.consumed = (Lin && post && last_tile && st.seq_in + k + S < Lin->total)
+                             ? P.flags + Lin->flag_base + S + in_idx
+                             : nullptr;
             r.consumed_v = sin + 1;
             // LL slots carry their flags in the lines
             r.full = (Lout && post && last_tile && !P.ll) ? P.flags + Lout->flag_base + out_idx : nullptr;
@@ -1161,6 +1172,86 @@ __device__ __forceinline__ bool move_ll(const SlotOp& op, int tid, int T, unsign
     return true;
 }
 
+// The same with U vectors per thread in flight (the sequential engine, whose
+// threads all move data): every load of a round -- LL lines and plain
+// operands -- is issued before the first poll, and only the lines that do
+// not carry the flag yet are read again, so a round costs one round trip
+// once the producer's lines have landed.
+template <bool RED, int DT, int U>
+__device__ __forceinline__ bool move_ll_wide(const SlotOp& op, int tid, int T, unsigned long long timeout_ns,
+                                             const int* status)
+{
+    constexpr int ES = (DT == CCL_BF16 || DT == CCL_F16) ? 2 : 4;
+    const long long nv = op.n * ES / 16;
+    const char* a = op.a;
+    const uint4* a16 = reinterpret_cast<const uint4*>(a);
+    const uint4* b16 = reinterpret_cast<const uint4*>(op.b);
+    const bool a_ll = op.a_ll, o1_ll = op.o1_ll, o2_ll = op.o2_ll, as = op.as, bs = op.bs, o1s = op.o1s;
+    char* o1 = op.o1;
+    char* o2 = op.o2;
+    const unsigned fin = op.fin, fout = op.fout;
+    for (long long i0 = tid; i0 < nv; i0 += (long long)U * T) {
+        unsigned long long x0[U], x1[U], x2[U], x3[U];
+        uint4 vb[U];
+        unsigned pend = 0;   // bit u: vector u of the round still lacks the slot's flag
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long j = i0 + (long long)u * T < nv ? i0 + (long long)u * T : nv - 1;
+            if (a_ll) {
+                ll_load2(a + 32 * j, x0[u], x1[u]);
+                ll_load2(a + 32 * j + 16, x2[u], x3[u]);
+            } else {
+                const uint4 v = vload(a16 + j, as);
+                x0[u] = v.x;
+                x1[u] = v.y;
+                x2[u] = v.z;
+                x3[u] = v.w;
+            }
+            vb[u] = RED ? vload(b16 + j, bs) : make_uint4(0, 0, 0, 0);
+        }
+        if (a_ll) {
+            unsigned long long t0 = 0;
+            unsigned spins = 0;
+            while (true) {
+                pend = 0;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const bool ready = (unsigned)(x0[u] >> 32) == fin && (unsigned)(x1[u] >> 32) == fin &&
+                                       (unsigned)(x2[u] >> 32) == fin && (unsigned)(x3[u] >> 32) == fin;
+                    if (!ready && i0 + (long long)u * T < nv) pend |= 1u << u;
+                }
+                if (!pend) break;
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (pend & (1u << u)) {
+                        const long long j = i0 + (long long)u * T;
+                        ll_load2(a + 32 * j, x0[u], x1[u]);
+                        ll_load2(a + 32 * j + 16, x2[u], x3[u]);
+                    }
+                const unsigned long long now = gtimer();
+                if (!t0) t0 = now;
+                else if (now - t0 > timeout_ns) return false;
+                if ((++spins & 63) == 0 && *(const volatile int*)status != 0) return false;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long j = i0 + (long long)u * T;
+            if (j < nv) {
+                const uint4 va = make_uint4((unsigned)x0[u], (unsigned)x1[u], (unsigned)x2[u], (unsigned)x3[u]);
+                const uint4 r = RED ? vadd<DT>(va, vb[u]) : va;
+                if (o1_ll) ll_store_vec(o1, j, r, fout);
+                else vstore(reinterpret_cast<uint4*>(o1) + j, r, o1s);
+                if (o2) {
+                    if (o2_ll) ll_store_vec(o2, j, r, fout);
+                    else vstore(reinterpret_cast<uint4*>(o2) + j, r, false);
+                }
+            }
+        }
+    }
+    return true;
+}
+
 template <int DT>
 __device__ __forceinline__ bool move_ll_dt(const SlotOp& op, int tid, int T, const KParams& P)
 {
@@ -1258,13 +1349,20 @@ __device__ __forceinline__ bool seq_leader(const KParams& P)
 
 // the LL data path of a sequential step, out of line (its polling loops
 // stay out of the register budget of the step's own code)
+template <int DT>
+__device__ __forceinline__ bool seq_move_ll_dt(const SlotOp& op, int tid, int T, const KParams& P)
+{
+    constexpr int UL = 4;   // vectors per thread in flight
+    return op.red ? move_ll_wide<true, DT, UL>(op, tid, T, P.timeout_ns, P.status)
+                  : move_ll_wide<false, DT, UL>(op, tid, T, P.timeout_ns, P.status);
+}
 static __device__ __noinline__ bool seq_move_ll(const SlotOp& op, int tid, int T, const KParams& P)
 {
     switch (op.dtype) {
-    case CCL_F32: return move_ll_dt<CCL_F32>(op, tid, T, P);
-    case CCL_BF16: return move_ll_dt<CCL_BF16>(op, tid, T, P);
-    case CCL_F16: return move_ll_dt<CCL_F16>(op, tid, T, P);
-    default: return move_ll_dt<CCL_I32>(op, tid, T, P);
+    case CCL_F32: return seq_move_ll_dt<CCL_F32>(op, tid, T, P);
+    case CCL_BF16: return seq_move_ll_dt<CCL_BF16>(op, tid, T, P);
+    case CCL_F16: return seq_move_ll_dt<CCL_F16>(op, tid, T, P);
+    default: return seq_move_ll_dt<CCL_I32>(op, tid, T, P);
     }
 }
 
@@ -1348,7 +1446,8 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
             if (tid == 0) {
                 int ok = k == 0 ? pre_ok : 1;
                 if (k == 0 && ok && ndeps > 0) ok = wait_deps(P, deps, ndeps, si, waited);
-                if (ok && linked) ok = wait_slots(P, Lin, Lout, sin, sout, in_idx, out_idx, 1, si, waited) != 0;
+                if (ok && linked)
+                    ok = wait_slots(P, Lin, Lout, sin, sout, st.seq_out + k, in_idx, out_idx, 1, si, waited) != 0;
                 *go = ok;
             }
             __syncthreads();
@@ -1415,12 +1514,19 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
             // every thread's stores were observed at the barrier; the
             // fence makes them visible at gpu scope before the flags.  After
             // a failed wait (or an LL part that gave up) nothing is posted.
-            const bool pst = post && ok && (!P.ll || *(volatile int*)P.status == 0);
-            fence_acq_rel_gpu();
-            if (Lin && pst) st_relaxed(P.flags + Lin->flag_base + S + in_idx, sin + 1);
-            if (Lout && pst && !P.ll) st_relaxed(P.flags + Lout->flag_base + out_idx, sout + 1);
+            // a consumed flag matters only to a producer that reuses the slot
+            // within this execution; an LL slot needs no full flag; with
+            // nothing to post there is no fence either (and an LL part's
+            // failure needs no check)
+            bool p_in = Lin && post && ok && st.seq_in + k + S < Lin->total;
+            bool p_out = Lout && post && ok && !P.ll;
+            bool p_sig = k == nslots - 1 && st.signal >= 0 && post && ok;
+            if (P.ll && (p_in || p_sig) && *(volatile int*)P.status != 0) p_in = p_out = p_sig = false;
+            if (p_in || p_out || p_sig) fence_acq_rel_gpu();
+            if (p_in) st_relaxed(P.flags + Lin->flag_base + S + in_idx, sin + 1);
+            if (p_out) st_relaxed(P.flags + Lout->flag_base + out_idx, sout + 1);
             if (k == nslots - 1) {
-                if (st.signal >= 0 && pst)
+                if (p_sig)
                     st_relaxed(P.counters + st.signal, (unsigned long long)(P.exec * P.m + st.mb + 1));
                 if (P.timeline) {
                     unsigned long long* tl = P.timeline + 5ll * si;

@@ -287,6 +287,39 @@ def test_ll_sequential_repeated_executions_and_windows(ccl, cluster):
         assert_bitexact(to_host(d_out, BF16), want)
 
 
+@pytest.mark.parametrize("engine,protocol,cluster", [(0, 0, 0), (0, 1, 0), (1, 0, 0), (1, 1, 0), (1, 1, 4), (1, 0, 8)])
+@pytest.mark.parametrize("fifo_slots", [13, 14, 16])
+def test_fifo_deeper_than_an_execution_repeated(ccl, engine, protocol, cluster, fifo_slots):
+    """A FIFO that holds every slot a link carries in one execution (the
+    8-rank fused ring sends 14 one-slot pieces per link at this size): no
+    slot is reused inside an execution, so no consumer posts that it has
+    read one and no producer waits for that -- the next execution, a later
+    kernel, reuses the slots.  At 14 slots the FIFO is exactly one
+    execution deep; at 13 the last piece reuses the first slot.  Six
+    executions, bit-exact each time, then in place."""
+    import torch
+    import datagen
+    import oracle
+    from gpu_helpers import oracle_program, to_device, empty_outputs, to_host
+    R, ce = 8, 4096
+    plan = ccl.Plan(ccl.Schedule.builtin(0, R), ce, BF16, engine=engine, protocol=protocol, cluster=cluster,
+                    nthreads=256, slot_bytes=ce * 2, fifo_slots=fifo_slots, channels=1)
+    ops, nch = oracle_program(0, R)
+    for it in range(6):
+        ins = datagen.rank_inputs(400 + it, "normal", R, R * ce, BF16)
+        d_out = empty_outputs(R, R * ce, BF16)
+        plan.execute(to_device(ins, BF16), d_out)
+        torch.cuda.synchronize()
+        plan.status()
+        want, _, _ = oracle.run(ops, R, nch, ce, BF16, ins)
+        assert_bitexact(to_host(d_out, BF16), want)
+    d = to_device(ins, BF16)
+    plan.execute(d, d)
+    torch.cuda.synchronize()
+    plan.status()
+    assert_bitexact(to_host(d, BF16), want)
+
+
 @pytest.mark.parametrize("R,tokens,seed", [(4, 64, 1), (8, 96, 2), (32, 48, 3)])
 @pytest.mark.parametrize("dtype", [F32, BF16, I32])
 @pytest.mark.parametrize("link_mode", [0, 1])
