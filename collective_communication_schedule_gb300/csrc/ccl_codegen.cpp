@@ -299,7 +299,7 @@ std::string generate_plan_source(const PlanImage& img, int build, std::string* w
                 }
                 // DRec: kind dtype link_in link_out src_buf src_rank loc_buf loc_rank dst_buf dst_rank
                 // nslots dep_begin dep_count signal mb flags src_off loc_off dst_off nelem seq_in
-                // seq_out drain seq_in_mod seq_out_mod pad0 (nelem: the whole channel range)
+                // seq_out drain seq_in_mod seq_out_mod link_loc (nelem: the whole channel range)
                 table += "    {{" + std::to_string(D.kind) + ", " + std::to_string(D.dtype) + ", " +
                          std::to_string(D.link_in) + ", " + std::to_string(D.link_out) + ", " + std::to_string(D.src_buf) +
                          ", " + std::to_string(D.src_rank) + ", " + std::to_string(D.loc_buf) + ", " +
@@ -365,7 +365,7 @@ std::string generate_plan_source(const PlanImage& img, int build, std::string* w
     } else {
         o += "    __shared__ __align__(16) ccl::CtlShared sh;\n";
         o += "    extern __shared__ __align__(128) unsigned char stages[];\n";
-        o += "    ccl::ctl_init(&sh);\n";
+        o += "    ccl::ctl_init(P, &sh);\n";
         o += "    const int warp = threadIdx.x >> 5;\n";
         o += "    if (warp < 3) {\n        if ((threadIdx.x & 31) == 0) {\n            if (warp == 0) {\n";
         o += "    " + sw;

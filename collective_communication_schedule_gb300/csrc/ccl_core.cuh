@@ -461,7 +461,23 @@ struct CtlShared {
     int last_head[kHist];               // issuer only: last descriptor of step si % kHist
     const unsigned long long* poll_ptr[kLook * (2 + kDepPoll)];   // issuer only: polled words
     unsigned long long poll_want[kLook * (2 + kDepPoll)];         // and their targets
+    DLink links[kSeqLinks];             // the program's first links (KParams.prog_links)
 };
+
+// A step's link: the program's copy in shared memory when the record says
+// where (link_loc), else the link array
+__device__ __forceinline__ const DLink* step_link(const KParams& P, const DLink* tab, int link, int loc)
+{
+    return link < 0 ? nullptr : loc ? tab + (loc - 1) : P.links + link;
+}
+// copy the program's first links into shared memory (threads < kSeqLinks)
+__device__ __forceinline__ void load_prog_links(const KParams& P, int prog, DLink* tab)
+{
+    if (threadIdx.x < kSeqLinks) {
+        const int id = P.prog_links[prog * kSeqLinks + threadIdx.x];
+        if (id >= 0) tab[threadIdx.x] = P.links[id];
+    }
+}
 
 __device__ __forceinline__ void record_timeout(const KParams& P, int si, int reason)
 {
@@ -627,10 +643,11 @@ __device__ __forceinline__ SlotCond first_slot_cond(const KParams& P, const DRec
     return c;
 }
 
-__device__ __forceinline__ SlotCond first_slot_cond(const KParams& P, const DRec& st, unsigned exec_mod)
+__device__ __forceinline__ SlotCond first_slot_cond(const KParams& P, const DRec& st, unsigned exec_mod,
+                                                    const DLink* tab)
 {
-    return first_slot_cond(P, st, exec_mod, st.link_in >= 0 ? P.links + st.link_in : nullptr,
-                           st.link_out >= 0 ? P.links + st.link_out : nullptr);
+    return first_slot_cond(P, st, exec_mod, step_link(P, tab, st.link_in, st.link_loc & 0xff),
+                           step_link(P, tab, st.link_out, (st.link_loc >> 8) & 0xff));
 }
 
 // Poll the conditions of steps [s0, s1) (records in the ring) -- the first
@@ -655,7 +672,7 @@ static __device__ int poll_steps(const KParams& P, CtlShared* sh, int s0, int s1
             continue;
         }
         const DRec& st = sh->rec[(s0 + i) % (2 * kLook)];
-        const SlotCond c = first_slot_cond(P, st, exec_mod);
+        const SlotCond c = first_slot_cond(P, st, exec_mod, sh->links);
         ptr[0] = c.in;
         want[0] = c.vin;
         ptr[1] = c.out;
@@ -911,8 +928,8 @@ static __device__ void issuer(const KParams& P, CtlShared* sh, int b0, int b1)
             publish_cmd(sh, head, 2, limit);
             return;
         }
-        const DLink* Lin = st.link_in >= 0 ? P.links + st.link_in : nullptr;
-        const DLink* Lout = st.link_out >= 0 ? P.links + st.link_out : nullptr;
+        const DLink* Lin = step_link(P, sh->links, st.link_in, st.link_loc & 0xff);
+        const DLink* Lout = step_link(P, sh->links, st.link_out, (st.link_loc >> 8) & 0xff);
         if (!issue_step(P, sh, st, Lin, Lout, si, head, si < cleared ? 1 : 0, exec_mod, t_start, waited)) return;
     }
     publish_cmd(sh, head, 1, limit);
@@ -1312,8 +1329,9 @@ static __device__ void data_warps(const KParams& P, CtlShared* sh)
 // data; no overlap of one step's waits with another step's data.
 // ----------------------------------------------------------------------
 struct SeqShared {
-    DRec rec[2];   // the current step's record and the next one, arriving by cp.async
-    int go;        // thread 0's verdict on the current wait (1: the waits were met)
+    DRec rec[2];              // the current step's record and the next one, arriving by cp.async
+    DLink links[kSeqLinks];   // the program's first links (KParams.prog_links)
+    int go;                   // thread 0's verdict on the current wait (1: the waits were met)
 };
 
 // A threadblock program of the sequential engine may run on a cluster of
@@ -1545,8 +1563,9 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
 
 
 // mbarriers of a pipelined-engine CTA (thread 0), before the roles start
-__device__ __forceinline__ void ctl_init(CtlShared* sh)
+__device__ __forceinline__ void ctl_init(const KParams& P, CtlShared* sh)
 {
+    load_prog_links(P, blockIdx.x, sh->links);
     if (threadIdx.x == 0) {
         const int nwarps = blockDim.x / 32;
         for (int q = 0; q < kQ; ++q) {

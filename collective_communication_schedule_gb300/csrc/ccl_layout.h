@@ -36,7 +36,8 @@ struct DRec {
     long long nelem, seq_in, seq_out;
     int drain;
     int seq_in_mod, seq_out_mod;   // seq_in % S, seq_out % S (slot index arithmetic in 32 bits)
-    int pad0;
+    int link_loc;                  // 1 + the incoming (bits 0-7) and outgoing (bits 8-15) link's entry in
+                                   // its program's link table (KParams.prog_links); 0: read the link array
 };
 static_assert(sizeof(DRec) == 128, "DRec layout");
 
@@ -56,6 +57,10 @@ struct DDep {
 };
 static_assert(sizeof(DDep) == 16, "DDep layout");
 
+// links a threadblock program keeps in shared memory (the sequential
+// engine); a program's further links are read from the link array
+constexpr int kSeqLinks = 8;
+
 // Kernel parameters of the persistent executor: one CTA per threadblock
 // program, every rank's buffers and every link FIFO in this GPU's memory.
 struct KParams {
@@ -63,6 +68,7 @@ struct KParams {
     const int* tb_begin;
     const DLink* links;
     const DDep* deps;
+    const int* prog_links;         // kSeqLinks link indices per threadblock program (-1: none)
     unsigned long long* flags;
     unsigned long long* counters;
     char* fifo;

@@ -61,6 +61,7 @@ struct PlanImage {
     std::vector<DRec> recs;          // built from instrs + steps at the end of planning
     std::vector<int32_t> tb_begin;   // ntb + 1
     std::vector<DLink> links;
+    std::vector<int32_t> prog_links;  // ntb * kSeqLinks: the first links each program uses (-1: none)
     std::vector<DDep> deps;
     std::vector<int32_t> tb_rank;    // rank each threadblock serves (reporting)
     std::vector<std::vector<SegInfo>> tb_segs;   // segments of every threadblock program

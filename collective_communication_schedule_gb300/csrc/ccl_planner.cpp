@@ -459,6 +459,25 @@ void fill_records(PlanImage* img)
         r.seq_in_mod = (int32_t)(st.seq_in % img->S);
         r.seq_out_mod = (int32_t)(st.seq_out % img->S);
     }
+    // every program's first kSeqLinks distinct links, in order of first use,
+    // and each step's entries in that table
+    img->prog_links.assign((size_t)img->ntb * kSeqLinks, -1);
+    for (int b = 0; b < img->ntb; ++b) {
+        int32_t* tab = &img->prog_links[(size_t)b * kSeqLinks];
+        int n = 0;
+        auto entry = [&](int link) {
+            if (link < 0) return 0;
+            for (int i = 0; i < n; ++i)
+                if (tab[i] == link) return i + 1;
+            if (n == kSeqLinks) return 0;
+            tab[n] = link;
+            return ++n;
+        };
+        for (int k = img->tb_begin[b]; k < img->tb_begin[b + 1]; ++k) {
+            DRec& r = img->recs[k];
+            r.link_loc = entry(r.link_in) | (entry(r.link_out) << 8);
+        }
+    }
 }
 
 // Parallelization factor of every instruction: `p` for all, or (scaled)

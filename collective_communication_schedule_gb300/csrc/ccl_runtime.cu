@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(MAXT, 1) ccl_exec_kernel(const __grid_constant
     __shared__ __align__(16) CtlShared sh;
     extern __shared__ __align__(128) unsigned char stages[];
     const int b0 = P.tb_begin[blockIdx.x], b1 = P.tb_begin[blockIdx.x + 1];
-    ctl_init(&sh);
+    ctl_init(P, &sh);
     const int warp = threadIdx.x >> 5;
     if (warp < 3) {
         if ((threadIdx.x & 31) == 0) {
@@ -92,7 +92,11 @@ __global__ void __launch_bounds__(MAXT, 1) ccl_exec_seq_kernel(const __grid_cons
         asm volatile("cp.async.commit_group;" ::: "memory");
         asm volatile("cp.async.wait_all;" ::: "memory");
     }
-    // every CTA of the cluster has started; the first record is in place
+    // the program's links, read once (a step's link reads would otherwise
+    // go to L2 every step: the acquire fences of the waits drop L1 lines)
+    load_prog_links(P, prog, sh.links);
+    // every CTA of the cluster has started; the first record and the links
+    // are in place
     group_sync(P);
     for (int si = b0; si < b1; ++si) {
         unsigned long long t_start = 0, waited = 0;
@@ -102,8 +106,8 @@ __global__ void __launch_bounds__(MAXT, 1) ccl_exec_seq_kernel(const __grid_cons
             asm volatile("cp.async.commit_group;" ::: "memory");
         }
         if (leader && P.timeline) t_start = gtimer();
-        const DLink* Lin = st.link_in >= 0 ? P.links + st.link_in : nullptr;
-        const DLink* Lout = st.link_out >= 0 ? P.links + st.link_out : nullptr;
+        const DLink* Lin = step_link(P, sh.links, st.link_in, st.link_loc & 0xff);
+        const DLink* Lout = step_link(P, sh.links, st.link_out, (st.link_loc >> 8) & 0xff);
         seq_step<U>(P, &sh.go, st, Lin, Lout, P.deps + st.dep_begin, st.dep_count, true, si, exec_mod, t_start,
                     waited);
         if (tid == 0) asm volatile("cp.async.wait_all;" ::: "memory");   // the next record is here
@@ -617,8 +621,11 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
     size_t o_tb = align_up(o_recs + img.recs.size() * sizeof(ccl::DRec), 256);
     size_t o_links = align_up(o_tb + img.tb_begin.size() * sizeof(int32_t), 256);
     size_t o_deps = align_up(o_links + img.links.size() * sizeof(ccl::DLink), 256);
-    size_t blob = align_up(o_deps + std::max<size_t>(1, img.deps.size()) * sizeof(ccl::DDep), 256);
+    size_t o_plinks = align_up(o_deps + std::max<size_t>(1, img.deps.size()) * sizeof(ccl::DDep), 256);
+    size_t blob = align_up(o_plinks + std::max<size_t>(1, img.prog_links.size()) * sizeof(int32_t), 256);
     std::vector<char> h(blob, 0);
+    if (!img.prog_links.empty())
+        std::memcpy(h.data() + o_plinks, img.prog_links.data(), img.prog_links.size() * sizeof(int32_t));
     std::memcpy(h.data() + o_recs, img.recs.data(), img.recs.size() * sizeof(ccl::DRec));
     std::memcpy(h.data() + o_tb, img.tb_begin.data(), img.tb_begin.size() * sizeof(int32_t));
     std::memcpy(h.data() + o_links, img.links.data(), img.links.size() * sizeof(ccl::DLink));
@@ -656,6 +663,7 @@ ccl_status_t ccl_plan_create(ccl_schedule_t s, int64_t chunk_elems, int32_t dtyp
     k.tb_begin = reinterpret_cast<const int32_t*>(p->d_blob + o_tb);
     k.links = reinterpret_cast<const ccl::DLink*>(p->d_blob + o_links);
     k.deps = reinterpret_cast<const ccl::DDep*>(p->d_blob + o_deps);
+    k.prog_links = reinterpret_cast<const int32_t*>(p->d_blob + o_plinks);
     k.flags = p->d_flags;
     k.counters = p->d_flags + img.links.size() * 2 * img.S;
     k.fifo = p->d_fifo;

@@ -438,6 +438,45 @@ def test_program_that_writes_inputs_bitexact(ccl, fuse, opts):
         assert_bitexact(to_host(d_in, F32), want_in)
 
 
+def many_links_program(R):
+    """Rank 0 hands a running sum to every other rank in turn and takes it
+    back: copy to rank k, rank k adds its input, copy back to rank 0 --
+    2 (R - 1) links, never two active at once, so packing puts all of rank
+    0's on one threadblock."""
+    ops = []
+    for k in range(1, R):
+        ops.append((0, 0, 0, 0, 1, 1, 0, 1) if k == 1 else (0, 0, 1, k - 1, k, 1, 0, 1))
+        ops.append((1, k, 0, 0, k, 1, 0, 1))
+        ops.append((0, k, 1, 0, 0, 1, k, 1))
+    return ops
+
+
+@pytest.mark.parametrize("fuse", [True, False])
+@pytest.mark.parametrize("opts", [dict(), dict(protocol=1), dict(engine=1), dict(engine=1, protocol=1, cluster=2)])
+def test_program_with_more_links_than_the_shared_link_table(ccl, fuse, opts):
+    """A threadblock program on 24 links: the first ones come from the copy
+    of the program's links in shared memory, the rest from the link array."""
+    import torch
+    import datagen
+    import oracle
+    from gpu_helpers import to_device, empty_outputs, to_host
+    R, ce = 13, 4096
+    nch = (R, R, R)
+    ops = many_links_program(R)
+    plan = ccl.Plan(ccl.Schedule.compile(ops, R, nch, fuse=fuse), ce, F32, tb_alloc=1, link_mode=0, channels=1,
+                    slot_bytes=4096, **opts)
+    st = plan.stats()
+    assert st.nlinks == 2 * (R - 1) and st.nthreadblocks == R
+    for rep in range(2):
+        ins = datagen.rank_inputs(60 + rep, "normal", R, R * ce, F32)
+        d_out = empty_outputs(R, R * ce, F32)
+        plan.execute(to_device(ins, F32), d_out)
+        torch.cuda.synchronize()
+        plan.status()
+        want, _, _ = oracle.run(np.array(ops, np.int32), R, nch, ce, F32, ins)
+        assert_bitexact(to_host(d_out, F32), want)
+
+
 @pytest.mark.parametrize("fuse", [True, "nochain"])
 @pytest.mark.parametrize("opts", [dict(link_mode=0), dict(link_mode=1, tb_alloc=2), dict(link_mode=1, bulk=1),
                                   dict(engine=1), dict(protocol=1), dict(engine=1, protocol=1, cluster=4)])
