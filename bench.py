@@ -60,10 +60,12 @@ SUITE = [
     ("a2n", 5, 24, 8, 0, 16 * MiB, "normal", 4,
      dict(fuse=False, channels=16, link_mode=1, microbatches=8, tb_alloc=2, tb_budget=304, channel_scaling=0)),
     ("ag_3m", 1, 8, 0, 1, 3 * MiB // 8, "normal", 1,
-     # every hop a direct copy into the next rank's output (no FIFO); the
-     # small collectives run on the sequential engine (fewer hand-offs per
-     # step), each program on a cluster of CTAs that share its slots' data
-     dict(fuse=False, channels=4, link_mode=1, engine=1, cluster=4, nthreads=256)),
+     # every hop a direct copy into the next rank's output (no FIFO), the
+     # first one in the same pass as the rank's own block (a copy-send with
+     # its receive folded in); the small collectives run on the sequential
+     # engine (fewer hand-offs per step), each program on a cluster of CTAs
+     # that share its slots' data
+     dict(fuse="nochain", channels=4, link_mode=1, engine=1, cluster=4, nthreads=256)),
     ("rs_3m", 2, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4, engine=1, cluster=4, nthreads=256)),
     ("ar_1m", 0, 8, 0, 0, 1 * MiB // 8, "uniform", 0, dict(fuse="nochain", link_mode=1, channels=1, tb_alloc=2,
                                                             tb_budget=16, engine=1, cluster=8, nthreads=256)),

@@ -831,12 +831,15 @@ __device__ __forceinline__ bool issue_step(const KParams& P, CtlShared* sh, cons
                 op.a = srcb + off;
                 op.as = (st.flags & STEP_SRC_STREAM) && P.stream_in;
             }
-            op.b = locb ? locb + off : nullptr;
+            // a two-destination copy keeps its second destination in the
+            // local-operand range
+            const bool copy2 = st.kind == CCL_I_COPY2;
+            op.b = locb && !copy2 ? locb + off : nullptr;
             op.bs = (st.flags & STEP_LOC_STREAM) && P.stream_in;
             if (dstb) {
                 op.o1 = dstb + off;
                 op.o1s = st.dst_buf == CCL_BUF_OUT;
-                op.o2 = slot_out ? slot_out + lls * soff : nullptr;
+                op.o2 = copy2 ? const_cast<char*>(locb) + off : slot_out ? slot_out + lls * soff : nullptr;
                 op.o2_ll = slot_out && P.ll;
             } else {
                 op.o1 = slot_out + lls * soff;
@@ -1455,7 +1458,10 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
             n = hi - lo;
         }
         const char* a = (a_slot || !srcb) ? nullptr : srcb + e0 * es;
-        const char* b = locb ? locb + e0 * es : nullptr;
+        // a two-destination copy keeps its second destination in the
+        // local-operand range
+        const bool copy2 = st.kind == CCL_I_COPY2;
+        const char* b = locb && !copy2 ? locb + e0 * es : nullptr;
         if (n > 0) {
             prefetch_l2(a, n * es, tid, T);
             prefetch_l2(b, n * es, tid, T);
@@ -1490,7 +1496,7 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
         if (dstb) {
             o1 = dstb + e0 * es;
             o1s = st.dst_buf == CCL_BUF_OUT;
-            o2 = slot_out;
+            o2 = copy2 ? const_cast<char*>(locb) + e0 * es : slot_out;
         } else {
             o1 = slot_out;
         }

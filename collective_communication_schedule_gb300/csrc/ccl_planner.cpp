@@ -263,6 +263,7 @@ void allocate_connection(const ccl_schedule& s, const Timeline& tl, TBList* tbs,
             // a copy into another rank's buffer (direct transport) is a
             // connection of its own to that rank
             if (I.kind == CCL_I_COPY && I.dst.valid() && I.dst.rank != I.rank) out = CCL_MAX_RANKS + I.dst.rank;
+            if (I.kind == CCL_I_COPY2 && I.loc.valid() && I.loc.rank != I.rank) out = CCL_MAX_RANKS + I.loc.rank;
             auto compat = [&](const C& c) {
                 return (in < 0 || c.in < 0 || c.in == in) && (out < 0 || c.out < 0 || c.out == out);
             };
@@ -626,12 +627,14 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     // and a bulk copy from them is ordered after generic-proxy writes; inputs
     // nobody writes are read once and streamed.
     std::vector<char> in_written(s.nranks, 0);
-    for (const Instr& I : s.instrs)
+    for (const Instr& I : s.instrs) {
         if (I.dst.valid() && I.dst.buf == CCL_BUF_IN) in_written[I.dst.rank] = 1;
+        if (I.kind == CCL_I_COPY2 && I.loc.valid() && I.loc.buf == CCL_BUF_IN) in_written[I.loc.rank] = 1;
+    }
     auto stream_bits = [&](const DInstr& D) {
         int32_t f = 0;
         if (D.src_buf == CCL_BUF_IN && !in_written[D.src_rank]) f |= STEP_SRC_STREAM;
-        if (D.loc_buf == CCL_BUF_IN && !in_written[D.loc_rank]) f |= STEP_LOC_STREAM;
+        if (D.kind != CCL_I_COPY2 && D.loc_buf == CCL_BUF_IN && !in_written[D.loc_rank]) f |= STEP_LOC_STREAM;
         return f;
     };
 
@@ -923,7 +926,7 @@ void dump_programs(const ccl_schedule& s, const Timeline& tl, const TBList& tbs,
 // receive into a buffer becomes one copy run by the sender's threadblock
 // straight into the receiver's destination; the receive disappears and
 // every dependency on it moves to the copy.  Nothing is staged in a FIFO.
-ccl_schedule direct_transport(const ccl_schedule& s, int* ndirect)
+ccl_schedule direct_transport(const ccl_schedule& s, int* ndirect, bool copy2)
 {
     ccl_schedule d = s;
     const int ni = (int)s.instrs.size();
@@ -935,10 +938,17 @@ ccl_schedule direct_transport(const ccl_schedule& s, int* ndirect)
         const Xfer& X = s.xfers[x];
         const Instr& snd = s.instrs[X.send_instr];
         const Instr& rcv = s.instrs[X.recv_instr];
-        if (snd.kind != CCL_I_SEND || rcv.kind != CCL_I_RECV) continue;
+        if ((snd.kind != CCL_I_SEND && !(copy2 && snd.kind == CCL_I_COPY_SEND)) || rcv.kind != CCL_I_RECV) continue;
         Instr& c = d.instrs[X.send_instr];
-        c.kind = CCL_I_COPY;
-        c.dst = rcv.dst;
+        if (snd.kind == CCL_I_SEND) {
+            c.kind = CCL_I_COPY;
+            c.dst = rcv.dst;
+        } else {
+            // the copy-send writes its own destination and, in the same
+            // pass, the receiver's (held in the local-operand range)
+            c.kind = CCL_I_COPY2;
+            c.loc = rcv.dst;
+        }
         c.xfer_out = -1;
         drop_x[x] = 1;
         drop_i[X.recv_instr] = 1;
@@ -980,7 +990,7 @@ ccl_schedule direct_transport(const ccl_schedule& s, int* ndirect)
 namespace {
 
 ccl_status_t build_plan_one(const ccl_schedule& s_in, int64_t ce, int32_t dtype, const ccl_plan_opts_t& o,
-                            PlanImage* img)
+                            PlanImage* img, bool copy2)
 {
     if (ce <= 0) return fail(CCL_ERR_INVALID_ARG, "chunk_elems must be positive");
     if (dtype < CCL_F32 || dtype > CCL_I32) return fail(CCL_ERR_INVALID_ARG, "unknown dtype");
@@ -1015,7 +1025,7 @@ ccl_status_t build_plan_one(const ccl_schedule& s_in, int64_t ce, int32_t dtype,
     if (o.link_mode != CCL_LINK_FIFO && o.link_mode != CCL_LINK_DIRECT)
         return fail(CCL_ERR_INVALID_ARG, "unknown link_mode");
     int ndirect = 0;
-    const ccl_schedule s = o.link_mode == CCL_LINK_DIRECT ? direct_transport(s_in, &ndirect) : s_in;
+    const ccl_schedule s = o.link_mode == CCL_LINK_DIRECT ? direct_transport(s_in, &ndirect, copy2) : s_in;
     const int es = esize_of(dtype);
     Timeline tl;
     ccl_status_t st = build_timeline(s, o.scheduler, &tl);
@@ -1166,7 +1176,20 @@ done:
 ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const ccl_plan_opts_t& o,
                         PlanImage* img)
 {
-    ccl_status_t st = build_plan_one(s, ce, dtype, o, img);
+    // with direct transport, a copy-send's receive is folded into a
+    // two-destination copy first; where that makes the timeline cyclic or
+    // the threadblocks deadlock, the copy-send keeps its FIFO
+    const bool direct = o.link_mode == CCL_LINK_DIRECT;
+    auto plan_one = [&](const ccl_schedule& x) {
+        ccl_status_t r = build_plan_one(x, ce, dtype, o, img, true);
+        if (direct && (r == CCL_ERR_CYCLE || r == CCL_ERR_DEADLOCK)) {
+            const std::string why = ccl_last_error_detail();
+            if (build_plan_one(x, ce, dtype, o, img, false) == CCL_OK) return CCL_OK;
+            fail(r, why);
+        }
+        return r;
+    };
+    ccl_status_t st = plan_one(s);
     if ((st != CCL_ERR_CYCLE && st != CCL_ERR_DEADLOCK) || s.fuse == CCL_FUSE_NONE) return st;
     const std::string first = ccl_last_error_detail();
     for (int mode : {CCL_FUSE_NOCHAIN, CCL_FUSE_NONE}) {
@@ -1175,7 +1198,7 @@ ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const 
         if (compile_program(s.ops.data(), (int)s.ops.size(), s.nranks, s.nchunks, mode, &less) != CCL_OK) break;
         less.builtin = s.builtin;
         less.group_size = s.group_size;
-        if (build_plan_one(less, ce, dtype, o, img) == CCL_OK) {
+        if (plan_one(less) == CCL_OK) {
             if (log_level() >= 1)
                 std::fprintf(stderr, "[ccl] fused schedule did not plan (%s); planned with fusion mode %d\n",
                              first.c_str(), mode);

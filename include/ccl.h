@@ -120,7 +120,11 @@ typedef enum {
     CCL_I_RRS = 7,       /* slot_out <- local (+) slot_in       (recv-reduce-send) */
     CCL_I_RRCS = 8,      /* t <- local (+) slot_in; dst <- t; slot_out <- t */
     CCL_I_COPY_SEND = 9, /* dst <- src; slot_out <- src */
-    CCL_I_NKINDS = 10
+    CCL_I_NKINDS = 10,   /* kinds the compiler emits */
+    /* plans only (ccl_plan_steps): a copy-send whose receive direct
+       transport folded in -- dst <- src and loc <- src, loc being the
+       receiver's destination */
+    CCL_I_COPY2 = 10
 } ccl_instr_kind_t;
 
 typedef struct {

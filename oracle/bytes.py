@@ -190,15 +190,17 @@ def fused_instructions(ops, nranks, fuse="full"):
 
 def schedule_bytes(ops, nranks, nchunks, chunk_elems, dtype, fuse="full", direct=True):
     """Bytes one execution reads and writes (buffers and FIFO slots) when
-    ``ops`` runs as fused instructions; ``direct``: plain send -> plain
-    receive pairs are single copies into the receiver's buffer."""
+    ``ops`` runs as fused instructions; ``direct``: a plain receive whose
+    sender is a plain send or a copy-send takes no FIFO: the sender writes
+    the receiver's buffer itself (send 2 + receive 2 -> one copy of 2;
+    copy-send 3 + receive 2 -> one read written twice, 3)."""
     instrs = fused_instructions(ops, nranks, fuse)
     units = sum(FACTOR[k] * cnt for k, _, cnt, _, _ in instrs)
     if direct:
         sender = {s: k for k, _, _, s, _ in instrs if s is not None}
         for k, _, cnt, _, recv in instrs:
-            if k == "recv" and sender[recv] == "send":
-                units -= 2 * cnt        # send 2 + recv 2 -> one copy of 2
+            if k == "recv" and sender[recv] in ("send", "copy_send"):
+                units -= 2 * cnt
     return units * int(chunk_elems) * ESIZE[dtype]
 
 

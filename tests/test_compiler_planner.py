@@ -652,3 +652,23 @@ def test_coordinate_descent_tries_clusters_on_the_sequential_engine():
     best, bw, n = ccl.tune_search(probe)
     assert best.engine == ccl.ENGINE_SEQUENTIAL and best.cluster == 8
     assert all(c in (0, 1) for e, c in seen if e == ccl.ENGINE_PIPELINED)
+
+
+def test_direct_transport_folds_a_copy_send_and_its_receive():
+    """The ring AllGather with copy receives left unchained starts on every
+    rank with a copy-send (own block into the own output, and on to the
+    next rank). Direct transport folds its receive in: one read written to
+    both outputs (3 bytes per element byte) instead of a FIFO hop (3 + 2),
+    the other hops plain copies (2): 15 units per rank, no FIFO left. The
+    oracle's own count agrees."""
+    from oracle import bytes as OB
+    from oracle import schedules as OS
+    R, ce = 8, 1024
+    s = ccl.Schedule.builtin(ccl.RING_ALLGATHER, R, 0, ccl.FLAG_NOCHAIN_COPIES)
+    fifo = s.check(ce, F32, link_mode=ccl.LINK_FIFO)
+    direct = s.check(ce, F32, link_mode=ccl.LINK_DIRECT)
+    assert direct.nlinks == 0 and fifo.nlinks == R
+    assert direct.schedule_bytes == R * 15 * ce * 4
+    assert fifo.schedule_bytes == R * (3 + 7 * 2 + 6 * 2) * ce * 4   # copy-send, 7 receives, 6 sends
+    ops, nch = OS.ring_allgather(R)
+    assert OB.schedule_bytes(ops, R, nch, ce, F32, fuse="nochain", direct=True) == direct.schedule_bytes

@@ -438,6 +438,33 @@ def test_program_that_writes_inputs_bitexact(ccl, fuse, opts):
         assert_bitexact(to_host(d_in, F32), want_in)
 
 
+@pytest.mark.parametrize("opts", [dict(), dict(channels=3, microbatches=2), dict(engine=1), dict(engine=1, cluster=4),
+                                  dict(tb_alloc=2, channels=2), dict(bulk=1, tile_bytes=4096)])
+@pytest.mark.parametrize("dtype", [F32, BF16])
+def test_allgather_with_folded_copy_send_bitexact(ccl, opts, dtype):
+    """Ring AllGather, copy receives unchained, direct transport: each
+    rank's first step writes its block into its own output and the next
+    rank's in one pass (a copy-send with its receive folded in); ragged
+    chunks."""
+    import torch
+    import datagen
+    import oracle
+    from gpu_helpers import oracle_program, to_device, empty_outputs, to_host
+    R, ce = 8, 3001
+    plan = ccl.Plan(ccl.Schedule.builtin(1, R, 0, ccl.FLAG_NOCHAIN_COPIES), ce, dtype, link_mode=1,
+                    slot_bytes=4096, **opts)
+    assert plan.stats().nlinks == 0
+    assert any(st["kind"] == ccl.KIND_NAMES.index("copy2") for st in plan.steps())
+    ops, nch = oracle_program(1, R)
+    ins = datagen.rank_inputs(71, DIST[dtype], R, ce, dtype)
+    d_out = empty_outputs(R, R * ce, dtype)
+    plan.execute(to_device(ins, dtype), d_out)
+    torch.cuda.synchronize()
+    plan.status()
+    want, _, _ = oracle.run(ops, R, nch, ce, dtype, ins)
+    assert_bitexact(to_host(d_out, dtype), want)
+
+
 def many_links_program(R):
     """Rank 0 hands a running sum to every other rank in turn and takes it
     back: copy to rank k, rank k adds its input, copy back to rank 0 --
