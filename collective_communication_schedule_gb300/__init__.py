@@ -31,7 +31,7 @@ MB_AUTO, MB_ALGO, MB_TASK, MB_SEGMENT = 0, 1, 2, 3
 LINK_FIFO, LINK_DIRECT = 0, 1
 PROTO_SIMPLE, PROTO_LL = 0, 1
 ENGINE_PIPELINED, ENGINE_SEQUENTIAL = 0, 1
-KIND_NAMES = ["copy", "reduce", "send", "recv", "rrc", "rcs", "fwd", "rrs", "rrcs", "copy_send", "copy2"]
+KIND_NAMES = ["copy", "reduce", "send", "recv", "rrc", "rcs", "fwd", "rrs", "rrcs", "copy_send", "copy2", "rrc2"]
 DTYPE_NAMES = {F32: "f32", BF16: "bf16", F16: "f16", I32: "i32"}
 ESIZE = {F32: 4, BF16: 2, F16: 2, I32: 4}
 
@@ -73,7 +73,7 @@ class PlanOpts(ctypes.Structure):
                 ("instrument", ctypes.c_int32), ("tile_bytes", ctypes.c_int64), ("bulk", ctypes.c_int32),
                 ("link_mode", ctypes.c_int32), ("channel_scaling", ctypes.c_int32), ("mb_window", ctypes.c_int32),
                 ("protocol", ctypes.c_int32), ("tb_budget", ctypes.c_int32), ("engine", ctypes.c_int32),
-                ("codegen", ctypes.c_int32), ("cluster", ctypes.c_int32)]
+                ("codegen", ctypes.c_int32), ("cluster", ctypes.c_int32), ("fold", ctypes.c_int32)]
 
 
 class PlanStats(ctypes.Structure):

@@ -46,6 +46,7 @@ int64_t kind_bytes_factor(int kind)
     case CCL_I_RRCS: return 4;
     case CCL_I_COPY_SEND: return 3;
     case CCL_I_COPY2: return 3;
+    case CCL_I_RRC2: return 4;
     default: return 0;
     }
 }

@@ -782,7 +782,8 @@ __device__ __forceinline__ bool issue_step(const KParams& P, CtlShared* sh, cons
     unsigned in_idx = Lin ? slot_index(exec_mod, *Lin, st.seq_in_mod, S) : 0;
     unsigned out_idx = Lout ? slot_index(exec_mod, *Lout, st.seq_out_mod, S) : 0;
     const long long span = linked ? slot_elems : tile_elems;
-    const int red = st.kind == CCL_I_REDUCE || st.kind == CCL_I_RRC || st.kind == CCL_I_RRS || st.kind == CCL_I_RRCS;
+    const int red = st.kind == CCL_I_REDUCE || st.kind == CCL_I_RRC || st.kind == CCL_I_RRS || st.kind == CCL_I_RRCS ||
+                    st.kind == CCL_I_RRC2;
     const char* srcb = st.src_buf >= 0 ? P.bufs[st.src_buf][st.src_rank] + st.src_off * es : nullptr;
     const char* locb = st.loc_buf >= 0 ? P.bufs[st.loc_buf][st.loc_rank] + st.loc_off * es : nullptr;
     char* dstb = st.dst_buf >= 0 ? P.bufs[st.dst_buf][st.dst_rank] + st.dst_off * es : nullptr;
@@ -833,13 +834,17 @@ __device__ __forceinline__ bool issue_step(const KParams& P, CtlShared* sh, cons
             }
             // a two-destination copy keeps its second destination in the
             // local-operand range
-            const bool copy2 = st.kind == CCL_I_COPY2;
+            // (a folded recv-reduce-copy-send: in its source range)
+            const bool copy2 = st.kind == CCL_I_COPY2, rrc2 = st.kind == CCL_I_RRC2;
             op.b = locb && !copy2 ? locb + off : nullptr;
             op.bs = (st.flags & STEP_LOC_STREAM) && P.stream_in;
             if (dstb) {
                 op.o1 = dstb + off;
                 op.o1s = st.dst_buf == CCL_BUF_OUT;
-                op.o2 = copy2 ? const_cast<char*>(locb) + off : slot_out ? slot_out + lls * soff : nullptr;
+                op.o2 = copy2  ? const_cast<char*>(locb) + off
+                        : rrc2 ? const_cast<char*>(srcb) + off
+                        : slot_out ? slot_out + lls * soff
+                                   : nullptr;
                 op.o2_ll = slot_out && P.ll;
             } else {
                 op.o1 = slot_out + lls * soff;
@@ -1434,7 +1439,8 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
     if (!linked && st.nelem > 0) nslots = (st.nelem + slot_elems - 1) / slot_elems;
     unsigned in_idx = Lin ? slot_index(exec_mod, *Lin, st.seq_in_mod, S) : 0;
     unsigned out_idx = Lout ? slot_index(exec_mod, *Lout, st.seq_out_mod, S) : 0;
-    const int red = st.kind == CCL_I_REDUCE || st.kind == CCL_I_RRC || st.kind == CCL_I_RRS || st.kind == CCL_I_RRCS;
+    const int red = st.kind == CCL_I_REDUCE || st.kind == CCL_I_RRC || st.kind == CCL_I_RRS || st.kind == CCL_I_RRCS ||
+                    st.kind == CCL_I_RRC2;
     const char* srcb = st.src_buf >= 0 ? P.bufs[st.src_buf][st.src_rank] + st.src_off * es : nullptr;
     const char* locb = st.loc_buf >= 0 ? P.bufs[st.loc_buf][st.loc_rank] + st.loc_off * es : nullptr;
     char* dstb = st.dst_buf >= 0 ? P.bufs[st.dst_buf][st.dst_rank] + st.dst_off * es : nullptr;
@@ -1460,7 +1466,8 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
         const char* a = (a_slot || !srcb) ? nullptr : srcb + e0 * es;
         // a two-destination copy keeps its second destination in the
         // local-operand range
-        const bool copy2 = st.kind == CCL_I_COPY2;
+        // (a folded recv-reduce-copy-send: in its source range)
+        const bool copy2 = st.kind == CCL_I_COPY2, rrc2 = st.kind == CCL_I_RRC2;
         const char* b = locb && !copy2 ? locb + e0 * es : nullptr;
         if (n > 0) {
             prefetch_l2(a, n * es, tid, T);
@@ -1496,7 +1503,7 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
         if (dstb) {
             o1 = dstb + e0 * es;
             o1s = st.dst_buf == CCL_BUF_OUT;
-            o2 = copy2 ? const_cast<char*>(locb) + e0 * es : slot_out;
+            o2 = copy2 ? const_cast<char*>(locb) + e0 * es : rrc2 ? const_cast<char*>(srcb) + e0 * es : slot_out;
         } else {
             o1 = slot_out;
         }

@@ -12,7 +12,8 @@ enum { CCL_F32 = 0, CCL_BF16 = 1, CCL_F16 = 2, CCL_I32 = 3 };
 enum { CCL_BUF_IN = 0, CCL_BUF_OUT = 1, CCL_BUF_SCRATCH = 2 };
 enum {
     CCL_I_COPY = 0, CCL_I_REDUCE = 1, CCL_I_SEND = 2, CCL_I_RECV = 3, CCL_I_RRC = 4,
-    CCL_I_RCS = 5, CCL_I_FWD = 6, CCL_I_RRS = 7, CCL_I_RRCS = 8, CCL_I_COPY_SEND = 9, CCL_I_COPY2 = 10
+    CCL_I_RCS = 5, CCL_I_FWD = 6, CCL_I_RRS = 7, CCL_I_RRCS = 8, CCL_I_COPY_SEND = 9, CCL_I_COPY2 = 10,
+    CCL_I_RRC2 = 11
 };
 enum { CCL_ERR_TIMEOUT = 8 };
 #define CCL_MAX_RANKS 64

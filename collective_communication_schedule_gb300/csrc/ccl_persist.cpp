@@ -204,7 +204,7 @@ const OptField kOptFields[] = {
     OPT_FIELD(microbatches), OPT_FIELD(scheduler), OPT_FIELD(tb_alloc), OPT_FIELD(mb_order),
     OPT_FIELD(timeout_ms), OPT_FIELD(instrument), OPT_FIELD(tile_bytes), OPT_FIELD(bulk),
     OPT_FIELD(link_mode), OPT_FIELD(channel_scaling), OPT_FIELD(mb_window), OPT_FIELD(protocol),
-    OPT_FIELD(tb_budget), OPT_FIELD(engine), OPT_FIELD(codegen), OPT_FIELD(cluster)};
+    OPT_FIELD(tb_budget), OPT_FIELD(engine), OPT_FIELD(codegen), OPT_FIELD(cluster), OPT_FIELD(fold)};
 #undef OPT_FIELD
 
 std::string fmt_double(double x)

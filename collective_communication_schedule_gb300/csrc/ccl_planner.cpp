@@ -264,6 +264,9 @@ void allocate_connection(const ccl_schedule& s, const Timeline& tl, TBList* tbs,
             // connection of its own to that rank
             if (I.kind == CCL_I_COPY && I.dst.valid() && I.dst.rank != I.rank) out = CCL_MAX_RANKS + I.dst.rank;
             if (I.kind == CCL_I_COPY2 && I.loc.valid() && I.loc.rank != I.rank) out = CCL_MAX_RANKS + I.loc.rank;
+            // a folded recv-reduce-copy-send writes the next rank directly
+            // but keeps its incoming link: it joins the threadblock of that
+            // link (no outgoing connection of its own)
             auto compat = [&](const C& c) {
                 return (in < 0 || c.in < 0 || c.in == in) && (out < 0 || c.out < 0 || c.out == out);
             };
@@ -630,10 +633,11 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
     for (const Instr& I : s.instrs) {
         if (I.dst.valid() && I.dst.buf == CCL_BUF_IN) in_written[I.dst.rank] = 1;
         if (I.kind == CCL_I_COPY2 && I.loc.valid() && I.loc.buf == CCL_BUF_IN) in_written[I.loc.rank] = 1;
+        if (I.kind == CCL_I_RRC2 && I.src.valid() && I.src.buf == CCL_BUF_IN) in_written[I.src.rank] = 1;
     }
     auto stream_bits = [&](const DInstr& D) {
         int32_t f = 0;
-        if (D.src_buf == CCL_BUF_IN && !in_written[D.src_rank]) f |= STEP_SRC_STREAM;
+        if (D.kind != CCL_I_RRC2 && D.src_buf == CCL_BUF_IN && !in_written[D.src_rank]) f |= STEP_SRC_STREAM;
         if (D.kind != CCL_I_COPY2 && D.loc_buf == CCL_BUF_IN && !in_written[D.loc_rank]) f |= STEP_LOC_STREAM;
         return f;
     };
@@ -926,7 +930,7 @@ void dump_programs(const ccl_schedule& s, const Timeline& tl, const TBList& tbs,
 // receive into a buffer becomes one copy run by the sender's threadblock
 // straight into the receiver's destination; the receive disappears and
 // every dependency on it moves to the copy.  Nothing is staged in a FIFO.
-ccl_schedule direct_transport(const ccl_schedule& s, int* ndirect, bool copy2)
+ccl_schedule direct_transport(const ccl_schedule& s, int* ndirect, bool fold)
 {
     ccl_schedule d = s;
     const int ni = (int)s.instrs.size();
@@ -938,16 +942,22 @@ ccl_schedule direct_transport(const ccl_schedule& s, int* ndirect, bool copy2)
         const Xfer& X = s.xfers[x];
         const Instr& snd = s.instrs[X.send_instr];
         const Instr& rcv = s.instrs[X.recv_instr];
-        if ((snd.kind != CCL_I_SEND && !(copy2 && snd.kind == CCL_I_COPY_SEND)) || rcv.kind != CCL_I_RECV) continue;
+        const bool foldable = snd.kind == CCL_I_COPY_SEND || snd.kind == CCL_I_RRCS;
+        if ((snd.kind != CCL_I_SEND && !(fold && foldable)) || rcv.kind != CCL_I_RECV) continue;
         Instr& c = d.instrs[X.send_instr];
         if (snd.kind == CCL_I_SEND) {
             c.kind = CCL_I_COPY;
             c.dst = rcv.dst;
-        } else {
+        } else if (snd.kind == CCL_I_COPY_SEND) {
             // the copy-send writes its own destination and, in the same
             // pass, the receiver's (held in the local-operand range)
             c.kind = CCL_I_COPY2;
             c.loc = rcv.dst;
+        } else {
+            // the recv-reduce-copy-send likewise (its source range, unused:
+            // the first operand is the incoming slot)
+            c.kind = CCL_I_RRC2;
+            c.src = rcv.dst;
         }
         c.xfer_out = -1;
         drop_x[x] = 1;
@@ -990,7 +1000,7 @@ ccl_schedule direct_transport(const ccl_schedule& s, int* ndirect, bool copy2)
 namespace {
 
 ccl_status_t build_plan_one(const ccl_schedule& s_in, int64_t ce, int32_t dtype, const ccl_plan_opts_t& o,
-                            PlanImage* img, bool copy2)
+                            PlanImage* img, bool fold)
 {
     if (ce <= 0) return fail(CCL_ERR_INVALID_ARG, "chunk_elems must be positive");
     if (dtype < CCL_F32 || dtype > CCL_I32) return fail(CCL_ERR_INVALID_ARG, "unknown dtype");
@@ -1021,11 +1031,12 @@ ccl_status_t build_plan_one(const ccl_schedule& s_in, int64_t ce, int32_t dtype,
     if (o.protocol == CCL_PROTO_LL && (ce * esize_of(dtype)) % 16)
         return fail(CCL_ERR_UNSUPPORTED, "the LL protocol needs chunks of a multiple of 16 bytes");
     if (o.timeout_ms <= 0) return fail(CCL_ERR_INVALID_ARG, "timeout_ms must be positive");
+    if (o.fold != 0 && o.fold != 1) return fail(CCL_ERR_INVALID_ARG, "fold must be 0 or 1");
 
     if (o.link_mode != CCL_LINK_FIFO && o.link_mode != CCL_LINK_DIRECT)
         return fail(CCL_ERR_INVALID_ARG, "unknown link_mode");
     int ndirect = 0;
-    const ccl_schedule s = o.link_mode == CCL_LINK_DIRECT ? direct_transport(s_in, &ndirect, copy2) : s_in;
+    const ccl_schedule s = o.link_mode == CCL_LINK_DIRECT ? direct_transport(s_in, &ndirect, fold) : s_in;
     const int es = esize_of(dtype);
     Timeline tl;
     ccl_status_t st = build_timeline(s, o.scheduler, &tl);
@@ -1176,13 +1187,14 @@ done:
 ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const ccl_plan_opts_t& o,
                         PlanImage* img)
 {
-    // with direct transport, a copy-send's receive is folded into a
-    // two-destination copy first; where that makes the timeline cyclic or
-    // the threadblocks deadlock, the copy-send keeps its FIFO
-    const bool direct = o.link_mode == CCL_LINK_DIRECT;
+    // with direct transport, the plain receive of a copy-send or a
+    // recv-reduce-copy-send is folded into its sender first (one pass
+    // writes both destinations); where that makes the timeline cyclic or
+    // the threadblocks deadlock, the sender keeps its FIFO
+    const bool fold = o.link_mode == CCL_LINK_DIRECT && o.fold != 0;
     auto plan_one = [&](const ccl_schedule& x) {
-        ccl_status_t r = build_plan_one(x, ce, dtype, o, img, true);
-        if (direct && (r == CCL_ERR_CYCLE || r == CCL_ERR_DEADLOCK)) {
+        ccl_status_t r = build_plan_one(x, ce, dtype, o, img, fold);
+        if (fold && (r == CCL_ERR_CYCLE || r == CCL_ERR_DEADLOCK)) {
             const std::string why = ccl_last_error_detail();
             if (build_plan_one(x, ce, dtype, o, img, false) == CCL_OK) return CCL_OK;
             fail(r, why);

@@ -244,6 +244,7 @@ ccl_plan_opts_t merged_opts(const ccl_plan_opts_t* opts)
         o.engine = opts->engine;
         o.codegen = opts->codegen;
         o.cluster = opts->cluster;
+        o.fold = opts->fold;
     }
     return o;
 }
@@ -393,6 +394,7 @@ void ccl_plan_opts_default(ccl_plan_opts_t* o)
     o->engine = CCL_ENGINE_PIPELINED;
     o->codegen = 0;
     o->cluster = 0;
+    o->fold = 1;
 }
 
 ccl_status_t ccl_schedule_compile(const ccl_op_t* ops, int32_t nops, int32_t nranks, const int32_t nchunks[3],

@@ -121,10 +121,11 @@ typedef enum {
     CCL_I_RRCS = 8,      /* t <- local (+) slot_in; dst <- t; slot_out <- t */
     CCL_I_COPY_SEND = 9, /* dst <- src; slot_out <- src */
     CCL_I_NKINDS = 10,   /* kinds the compiler emits */
-    /* plans only (ccl_plan_steps): a copy-send whose receive direct
-       transport folded in -- dst <- src and loc <- src, loc being the
-       receiver's destination */
-    CCL_I_COPY2 = 10
+    /* plans only (ccl_plan_steps), made by direct transport from a sender
+       and the plain receive it feeds: */
+    CCL_I_COPY2 = 10,    /* copy-send + receive: dst <- src; loc <- src (loc: the receiver's destination) */
+    CCL_I_RRC2 = 11      /* recv-reduce-copy-send + receive: t <- local (+) slot_in; dst <- t; src <- t
+                            (src: the receiver's destination) */
 } ccl_instr_kind_t;
 
 typedef struct {
@@ -306,14 +307,20 @@ typedef enum {
  *                 destination buffer (one copy, no FIFO) and keeps FIFOs for
  *                 transfers that are forwarded or reduced.
  *   cluster     : sequential engine only: run every threadblock program on a
- *                 thread-block cluster of this many CTAs (2, 4 or 8).  The
- *                 cluster's first CTA waits for the flags and counters and
- *                 posts them; every CTA moves its 16-byte-granular share of
- *                 each slot between two cluster barriers.  Same steps,
+ *                 thread-block cluster of this many CTAs (2, 4 or 8).  Every
+ *                 CTA waits for the step's flags and counters itself and
+ *                 moves its 16-byte-granular share of each slot; after one
+ *                 cluster barrier the cluster's first CTA posts.  Same steps,
  *                 channels and FIFOs (one program per channel); the data of a
  *                 step moves on `cluster` SMs instead of one, for the
  *                 latency-bound sizes where a single CTA's data time sets the
  *                 length of every hop.
+ *   fold        : with direct transport, 1 (default): a plain receive fed by
+ *                 a copy-send or a recv-reduce-copy-send is folded into its
+ *                 sender, whose pass then writes the receiver's buffer too
+ *                 (CCL_I_COPY2 / CCL_I_RRC2 steps; one step and 2 bytes per
+ *                 element byte fewer per such pair), unless the plan would
+ *                 then cycle or deadlock.  0: such senders keep their FIFO.
  *   codegen     : 0 (default): the library's kernels interpret the plan's
  *                 step records.  1: ccl_plan_create generates CUDA source
  *                 for this one plan (ReSCCL report, §II.2: a kernel per
@@ -350,6 +357,7 @@ typedef struct {
     int32_t engine;      /* CCL_ENGINE_* */
     int32_t codegen;     /* 1: run a kernel generated and compiled for this plan (see below) */
     int32_t cluster;     /* sequential engine: CTAs per threadblock program (0 or 1: one; 2, 4, 8) */
+    int32_t fold;        /* direct transport: 1 (default) folds plain receives into their senders */
 } ccl_plan_opts_t;
 
 void ccl_plan_opts_default(ccl_plan_opts_t* o);

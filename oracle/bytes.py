@@ -188,18 +188,20 @@ def fused_instructions(ops, nranks, fuse="full"):
     return [(h.kind(), h.rank, h.count, h.send, h.recv) for h in halves if h.alive]
 
 
-def schedule_bytes(ops, nranks, nchunks, chunk_elems, dtype, fuse="full", direct=True):
+def schedule_bytes(ops, nranks, nchunks, chunk_elems, dtype, fuse="full", direct=True, fold=True):
     """Bytes one execution reads and writes (buffers and FIFO slots) when
     ``ops`` runs as fused instructions; ``direct``: a plain receive whose
-    sender is a plain send or a copy-send takes no FIFO: the sender writes
-    the receiver's buffer itself (send 2 + receive 2 -> one copy of 2;
-    copy-send 3 + receive 2 -> one read written twice, 3)."""
+    sender is a plain send, a copy-send or a recv-reduce-copy-send takes no
+    FIFO: the sender writes the receiver's buffer itself (send 2 + receive
+    2 -> one copy of 2; copy-send 3 + receive 2 -> one read written twice,
+    3; recv-reduce-copy-send 4 + receive 2 -> 4; ``fold`` False keeps the
+    last two with their FIFO)."""
     instrs = fused_instructions(ops, nranks, fuse)
     units = sum(FACTOR[k] * cnt for k, _, cnt, _, _ in instrs)
     if direct:
         sender = {s: k for k, _, _, s, _ in instrs if s is not None}
         for k, _, cnt, _, recv in instrs:
-            if k == "recv" and sender[recv] in ("send", "copy_send"):
+            if k == "recv" and (sender[recv] == "send" or (fold and sender[recv] in ("copy_send", "rrcs"))):
                 units -= 2 * cnt
     return units * int(chunk_elems) * ESIZE[dtype]
 

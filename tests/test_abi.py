@@ -96,8 +96,8 @@ def test_binding_constants_match_the_header():
     # instruction kind names are indexed by the header's CCL_I_* values
     for i, name in enumerate(ccl.KIND_NAMES):
         assert vals["I_" + name.upper()] == i, name
-    # the compiler's kinds, then copy2, which only plans contain
-    assert vals["I_NKINDS"] == len(ccl.KIND_NAMES) - 1 and ccl.KIND_NAMES[-1] == "copy2"
+    # the compiler's kinds, then copy2 and rrc2, which only plans contain
+    assert vals["I_NKINDS"] == len(ccl.KIND_NAMES) - 2 and ccl.KIND_NAMES[-2:] == ["copy2", "rrc2"]
 
 
 def test_layout_header_codes_match_the_c_abi():

@@ -36,13 +36,16 @@ def test_ring_rows_match_the_closed_form(name):
     """Ring AllReduce over R ranks of N bytes each: R N (6 - 4/R) schedule
     bytes fully fused through FIFOs; leaving the R - 2 middle all-gather hops
     of every chunk unchained and direct saves one byte per element byte on
-    each of them: N (R - 2) in all."""
+    each of them, N (R - 2) in all; and the first all-gather hop of every
+    chunk -- the recv-reduce-copy-send that completes it and the plain
+    receive it feeds -- writes the next rank's output directly, saving the
+    receive's 2 bytes per element byte: 2 N in all."""
     row = [r for r in bench.SUITE if r[0] == name][0]
     _, kind, R, G, dt, cb, dist, seed, opts = row
     assert opts.get("fuse") == "nochain" and opts.get("link_mode") == 1
     N = R * cb                       # R chunks of cb bytes per rank
     _, st, _ = _plan(row)
-    assert st.schedule_bytes == R * N * 6 - 4 * N - N * (R - 2)
+    assert st.schedule_bytes == R * N * 6 - 4 * N - N * (R - 2) - 2 * N
     assert st.min_bytes == 2 * R * N
 
 

@@ -173,11 +173,13 @@ def test_nochain_keeps_copy_receives_apart():
         nn = nochain.info().bytes_per_chunk_elem_x_esize
         assert nn == nf + R * (R - 2)
         # direct transport: a middle hop is one copy into the next rank's
-        # output (2 bytes per element byte) instead of a receive-copy-send (3)
+        # output (2 bytes per element byte) instead of a receive-copy-send
+        # (3), and the recv-reduce-copy-send that completes a chunk writes
+        # the next rank's output itself, so that rank's receive (2) goes
         ce, es = 64, 4
         st_full = full.check(ce, F32, link_mode=ccl.LINK_DIRECT)
         st_nochain = nochain.check(ce, F32, link_mode=ccl.LINK_DIRECT)
-        assert st_nochain.schedule_bytes == st_full.schedule_bytes - R * (R - 2) * ce * es
+        assert st_nochain.schedule_bytes == st_full.schedule_bytes - R * (R - 2) * ce * es - 2 * R * ce * es
 
 
 def test_fusion_keeps_the_order_of_dependent_sends_on_a_link():
@@ -672,3 +674,16 @@ def test_direct_transport_folds_a_copy_send_and_its_receive():
     assert fifo.schedule_bytes == R * (3 + 7 * 2 + 6 * 2) * ce * 4   # copy-send, 7 receives, 6 sends
     ops, nch = OS.ring_allgather(R)
     assert OB.schedule_bytes(ops, R, nch, ce, F32, fuse="nochain", direct=True) == direct.schedule_bytes
+
+
+def test_fold_option():
+    """fold = 0 keeps the copy-send's FIFO hop (and its bytes); other values
+    than 0 and 1 are refused; the library default folds."""
+    assert ccl.default_opts().fold == 1
+    R, ce = 8, 1024
+    s = ccl.Schedule.builtin(ccl.RING_ALLGATHER, R, 0, ccl.FLAG_NOCHAIN_COPIES)
+    kept = s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=0)
+    assert kept.nlinks == R and kept.schedule_bytes == R * (3 + 2 + 6 * 2) * ce * 4
+    with pytest.raises(ccl.CclError) as e:
+        s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=2)
+    assert e.value.code == 1

@@ -465,6 +465,37 @@ def test_allgather_with_folded_copy_send_bitexact(ccl, opts, dtype):
     assert_bitexact(to_host(d_out, dtype), want)
 
 
+@pytest.mark.parametrize("R", [2, 5, 8])
+@pytest.mark.parametrize("opts", [dict(), dict(channels=3, microbatches=2), dict(engine=1, cluster=4),
+                                  dict(protocol=1), dict(engine=1, protocol=1), dict(bulk=1, tile_bytes=4096)])
+def test_allreduce_with_folded_reduce_copy_send_bitexact(ccl, R, opts):
+    """Ring AllReduce, copy receives unchained, direct transport: the step
+    that completes a chunk (receive, reduce, copy to the own output) also
+    writes the next rank's output, whose receive is folded away; ragged
+    chunks, bf16, then in place."""
+    import torch
+    import datagen
+    import oracle
+    from gpu_helpers import oracle_program, to_device, empty_outputs, to_host
+    ce = 4096 if opts.get("protocol") else 3001
+    plan = ccl.Plan(ccl.Schedule.builtin(0, R, 0, ccl.FLAG_NOCHAIN_COPIES), ce, BF16, link_mode=1,
+                    slot_bytes=4096, **opts)
+    assert any(st["kind"] == ccl.KIND_NAMES.index("rrc2") for st in plan.steps())
+    ops, nch = oracle_program(0, R)
+    ins = datagen.rank_inputs(73, "normal", R, R * ce, BF16)
+    d_out = empty_outputs(R, R * ce, BF16)
+    plan.execute(to_device(ins, BF16), d_out)
+    torch.cuda.synchronize()
+    plan.status()
+    want, _, _ = oracle.run(ops, R, nch, ce, BF16, ins)
+    assert_bitexact(to_host(d_out, BF16), want)
+    d = to_device(ins, BF16)
+    plan.execute(d, d)
+    torch.cuda.synchronize()
+    plan.status()
+    assert_bitexact(to_host(d, BF16), want)
+
+
 def many_links_program(R):
     """Rank 0 hands a running sum to every other rank in turn and takes it
     back: copy to rank k, rank k adds its input, copy back to rank 0 --

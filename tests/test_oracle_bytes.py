@@ -1,8 +1,9 @@
 """The oracle's byte accounting (``oracle.bytes``), pinned to closed forms
 derived by hand from the collective programs and the fused-instruction costs
 (copy 2, send 2, recv 2, reduce / rrc / rcs / rrs / copy-send 3, rrcs 4,
-recv-send 2 bytes per element byte), then compared with the product's own
-count for every benchmark row."""
+recv-send 2 bytes per element byte; with direct transport a plain receive
+is written by its sender), then compared with the product's own count for
+every benchmark row."""
 import numpy as np
 import pytest
 
@@ -16,20 +17,24 @@ F32, BF16, F16, I32 = 0, 1, 2, 3
 def test_ring_allreduce_closed_forms(R):
     """Per rank, n = chunk bytes.  Full fusion: send 2 + (R-2) rrs 3 +
     rrcs 4 + (R-2) rcs 3 + recv 2 = 6R - 4.  Copy receives unchained: the
-    all-gather is R-1 receives and R-2 sends of 2: 3R + 4R - 6 = 7R - 6;
-    with direct transport the R-2 send/receive pairs between plain ends are
-    copies of 2: 3R + 2 + 2(R-2) = 5R - 2.  Unfused: R local copies 2,
-    R-1 reduce transfers 2 + 3, R-1 copy transfers 2 + 2 = 11R - 9."""
+    all-gather is R-1 receives and R-2 sends of 2: 3R + 4R - 6 = 7R - 6.
+    Direct transport: the R-2 send/receive pairs between plain ends become
+    copies of 2, and a plain receive fed by the rrcs that completes a chunk
+    is written by the rrcs itself (its 2 go): unchained 3R + 2 + 2(R-2) - 2
+    = 5R - 4; fully fused only at R = 2, where the rrcs feeds the last
+    receive directly.  Unfused: R local copies 2, R-1 reduce transfers
+    2 + 3, R-1 copy transfers 2 + 2 = 11R - 9."""
     ops, nch = OS.ring_allreduce(R)
     ce, es = 1000, 4
     n = ce * es
+    full_direct = 6 * R - 4 - (2 if R == 2 else 0)
     assert OB.schedule_bytes(ops, R, nch, ce, F32, "full", direct=False) == R * (6 * R - 4) * n
-    assert OB.schedule_bytes(ops, R, nch, ce, F32, "full", direct=True) == R * (6 * R - 4) * n
+    assert OB.schedule_bytes(ops, R, nch, ce, F32, "full", direct=True) == R * full_direct * n
     assert OB.schedule_bytes(ops, R, nch, ce, F32, "nochain", direct=False) == R * (7 * R - 6) * n
-    assert OB.schedule_bytes(ops, R, nch, ce, F32, "nochain", direct=True) == R * (5 * R - 2) * n
+    assert OB.schedule_bytes(ops, R, nch, ce, F32, "nochain", direct=True) == R * (5 * R - 4) * n
     assert OB.schedule_bytes(ops, R, nch, ce, F32, "none", direct=False) == R * (11 * R - 9) * n
-    # per rank N(6 - 4/R) with N = R n bytes per rank
-    assert OB.schedule_bytes(ops, R, nch, ce, F32) * R == R * R * n * (6 * R - 4)
+    # per rank N(6 - 4/R) with N = R n bytes per rank (FIFO transport)
+    assert OB.schedule_bytes(ops, R, nch, ce, F32, direct=False) * R == R * R * n * (6 * R - 4)
 
 
 @pytest.mark.parametrize("R", [2, 4, 8])
@@ -133,17 +138,19 @@ def test_oracle_count_equals_the_product_count_for_every_benchmark_row():
         fl = {"nochain": ccl.FLAG_NOCHAIN_COPIES, False: ccl.FLAG_NOFUSE}.get(opts.get("fuse", True), 0)
         ops, nch = KIND_PROGRAM[kind](R, G)
         direct = popts.get("link_mode", ccl.default_opts().link_mode) == ccl.LINK_DIRECT
-        assert OB.schedule_bytes(ops, R, nch, ce, dt, _fuse_name(fl), direct) == st.schedule_bytes, name
+        fold = bool(popts.get("fold", 1))
+        assert OB.schedule_bytes(ops, R, nch, ce, dt, _fuse_name(fl), direct, fold) == st.schedule_bytes, name
 
 
 @pytest.mark.parametrize("kind,R,G", [(0, 8, 0), (0, 3, 0), (1, 8, 0), (2, 5, 0), (3, 16, 8), (3, 4, 2),
                                       (4, 32, 8), (4, 8, 4), (5, 24, 8), (5, 6, 3)])
 @pytest.mark.parametrize("flags", [0, 2, 4])
-@pytest.mark.parametrize("link_mode", [0, 1])
-def test_oracle_count_equals_the_product_count_for_builtins(kind, R, G, flags, link_mode):
+@pytest.mark.parametrize("link_mode,fold", [(0, 1), (1, 1), (1, 0)])
+def test_oracle_count_equals_the_product_count_for_builtins(kind, R, G, flags, link_mode, fold):
     ops, nch = KIND_PROGRAM[kind](R, G)
-    st = ccl.Schedule.builtin(kind, R, G, flags).check(333, F32, link_mode=link_mode)
-    assert OB.schedule_bytes(ops, R, nch, 333, F32, _fuse_name(flags), link_mode == 1) == st.schedule_bytes
+    st = ccl.Schedule.builtin(kind, R, G, flags).check(333, F32, link_mode=link_mode, fold=fold)
+    assert OB.schedule_bytes(ops, R, nch, 333, F32, _fuse_name(flags), link_mode == 1, bool(fold)) == \
+        st.schedule_bytes
 
 
 def test_oracle_fused_kinds_equal_the_compiled_kinds():
