@@ -445,6 +445,9 @@ def run_gpu(args):
                      "frac": round(achieved / peak, 3), "kernels": kernels,
                      "traffic": recorded_traffic(dom) if not (args.only or args.scale != 1.0) else None,
                      "traffic_unit": "bytes per launch (ncu dram read+write, profiles/roofline_traffic.txt)",
+                     "traffic_basis": "full-size capture of the kernel's launches in one step, one pass each "
+                                      "(pass count checked on half-size captures first; scaled half-size captures "
+                                      "understate the AllReduce rows, whose FIFOs keep their size)",
                      "algorithmic_bytes_per_launch": bytes_dom // n_dom,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},
