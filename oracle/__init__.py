@@ -21,8 +21,9 @@ Contents
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 (closed forms, library special cases, exhaustive rounding checks, brute
-force on tiny inputs).  NaN/Inf propagation through reductions is parity
-unpinned (the workloads are finite).
+force on tiny inputs).  Special values follow IEEE 754 addition in the
+buffer type (pinned against numpy / torch on every pair of special values);
+the payload of a NaN result is not pinned.
 """
 from __future__ import annotations
 

@@ -96,3 +96,31 @@ def assert_bitexact(got, want):
             raise AssertionError(f"rank {r}: {bad.size} elements differ, first at {bad[:8]}: "
                                  f"got {np.ascontiguousarray(g).reshape(-1)[bad[:4]]} "
                                  f"want {np.ascontiguousarray(w).reshape(-1)[bad[:4]]}")
+
+
+def nan_mask(a, dtype):
+    """Elements of a host array (storage form of ``dtype``) that are NaN."""
+    a = np.ascontiguousarray(a)
+    if dtype == 0:
+        return np.isnan(a.view(np.float32))
+    if dtype == 1:
+        u = a.view(np.uint16)
+        return ((u & 0x7F80) == 0x7F80) & ((u & 0x7F) != 0)
+    if dtype == 2:
+        return np.isnan(a.view(np.float16))
+    return np.zeros(a.shape, bool)
+
+
+def assert_bitexact_but_nan(got, want, dtype):
+    """Bit-exact, except that a NaN matches any NaN (payload and sign of a
+    NaN are not pinned)."""
+    for r, (g, w) in enumerate(zip(got, want)):
+        gn, wn = nan_mask(g, dtype), nan_mask(w, dtype)
+        if not np.array_equal(gn, wn):
+            bad = np.nonzero(gn != wn)[0]
+            raise AssertionError(f"rank {r}: NaN at different places, first at {bad[:8]}")
+        g8 = np.ascontiguousarray(g)[~gn]
+        w8 = np.ascontiguousarray(w)[~wn]
+        if not np.array_equal(g8.view(np.uint8), w8.view(np.uint8)):
+            bad = np.nonzero(g8 != w8)[0]
+            raise AssertionError(f"rank {r}: {bad.size} non-NaN elements differ, first at {bad[:8]}")

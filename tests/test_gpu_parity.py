@@ -496,6 +496,44 @@ def test_allreduce_with_folded_reduce_copy_send_bitexact(ccl, R, opts):
     assert_bitexact(to_host(d, BF16), want)
 
 
+SPECIALS = {0: [np.inf, -np.inf, np.nan, 3.0e38], 1: [0x7F80, 0xFF80, 0x7FC0, 0x7F7F], 2: [0x7C00, 0xFC00, 0x7E00, 0x7BFF]}
+
+
+@pytest.mark.parametrize("dtype", [F32, BF16, F16])
+@pytest.mark.parametrize("kind,R,opts", [(0, 8, dict()), (0, 8, dict(engine=1, cluster=4)), (0, 8, dict(protocol=1)),
+                                         (2, 5, dict()), (3, 16, dict(channels=2, microbatches=2))])
+def test_special_values_propagate_as_the_oracle_says(ccl, dtype, kind, R, opts):
+    """Infinities, NaNs and values that overflow when added, planted in the
+    inputs: every output element that is NaN in the oracle's result is NaN
+    on the GPU and the rest is bit-exact (IEEE addition in the buffer type;
+    a NaN's payload is not pinned)."""
+    import torch
+    import datagen
+    import oracle
+    from gpu_helpers import (oracle_program, to_device, empty_outputs, to_host, assert_bitexact_but_nan,
+                             nan_mask)
+    G = 8 if kind == 3 else 0
+    ce = 4096
+    ops, nch = oracle_program(kind, R, G)
+    ins = datagen.rank_inputs(81, DIST[dtype], R, nch[0] * ce, dtype)
+    rng = np.random.default_rng(82)
+    for r in range(R):
+        pos = rng.choice(nch[0] * ce, 24, replace=False)
+        vals = np.array(SPECIALS[dtype] * 6)
+        if dtype == F32:
+            ins[r][pos] = vals.astype(np.float32)
+        else:
+            ins[r][pos] = vals.astype(np.uint16)
+    plan = ccl.Plan(ccl.Schedule.builtin(kind, R, G), ce, dtype, **opts)
+    d_out = empty_outputs(R, nch[1] * ce, dtype)
+    plan.execute(to_device(ins, dtype), d_out)
+    torch.cuda.synchronize()
+    plan.status()
+    want, _, _ = oracle.run(ops, R, nch, ce, dtype, ins)
+    assert any(nan_mask(w, dtype).any() for w in want)
+    assert_bitexact_but_nan(to_host(d_out, dtype), want, dtype)
+
+
 def many_links_program(R):
     """Rank 0 hands a running sum to every other rank in turn and takes it
     back: copy to rank k, rank k adds its input, copy back to rank 0 --

@@ -196,3 +196,62 @@ def test_i32_add_wraps():
     lib.oracle_add_i32.restype = __import__("ctypes").c_int32
     assert lib.oracle_add_i32(2**31 - 1, 1) == -2**31
     assert lib.oracle_add_i32(-5, 3) == -2
+
+
+def _special_values(dtype):
+    """Zeros, ones, the largest finite value, the smallest subnormal, both
+    infinities and NaNs of either sign and two payloads, as storage bits."""
+    if dtype == "f32":
+        b = [0x00000000, 0x80000000, 0x3F800000, 0xBF800000, 0x7F7FFFFF, 0xFF7FFFFF, 0x00000001, 0x80000001,
+             0x7F800000, 0xFF800000, 0x7FC00000, 0xFFC00000, 0x7F800001, 0x7FBFFFFF]
+        return np.array(b, np.uint32)
+    if dtype == "bf16":
+        b = [0x0000, 0x8000, 0x3F80, 0xBF80, 0x7F7F, 0xFF7F, 0x0001, 0x8001, 0x7F80, 0xFF80, 0x7FC0, 0xFFC0,
+             0x7F81, 0x7FBF]
+    else:
+        b = [0x0000, 0x8000, 0x3C00, 0xBC00, 0x7BFF, 0xFBFF, 0x0001, 0x8001, 0x7C00, 0xFC00, 0x7E00, 0xFE00,
+             0x7C01, 0x7DFF]
+    return np.array(b, np.uint16)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_special_values_follow_ieee_through_a_reduction(dtype):
+    """Reading for special values: IEEE 754 addition in the buffer type (for
+    bf16 / f16: widened to f32, added, rounded to nearest even): a NaN
+    operand gives NaN, an infinity plus a finite value keeps the infinity,
+    opposite infinities give NaN, a sum past the largest finite value rounds
+    to infinity.  A NaN's payload and sign are not pinned.  Every pair of
+    special values goes through the oracle's interpreter (a reduce of rank
+    1's input into rank 0's copy of its own) and is checked against numpy
+    (f32, and f16 through an exact float64 sum) or torch (bf16)."""
+    code = {"f32": 0, "bf16": 1, "f16": 2}[dtype]
+    v = _special_values(dtype)
+    a = np.repeat(v, v.size)
+    b = np.tile(v, v.size)
+    n = a.size
+    # out[0] = in[0] + in[1], element by element
+    ops = np.array([(0, 0, 0, 0, 0, 1, 0, 1), (1, 1, 0, 0, 0, 1, 0, 1)], np.int32)
+    ins = [a.view(np.float32), b.view(np.float32)] if dtype == "f32" else [a, b]
+    outs, _, _ = oracle.run(ops, 2, (1, 1, 0), n, code, ins)
+    got = np.asarray(outs[0])
+    got = got.view(np.uint32) if dtype == "f32" else got.view(np.uint16)
+    if dtype == "f32":
+        with np.errstate(over="ignore", invalid="ignore"):
+            ref = (a.view(np.float32) + b.view(np.float32)).view(np.uint32)
+        nan_ref = np.isnan(ref.view(np.float32))
+        nan_got = np.isnan(got.view(np.float32))
+    elif dtype == "bf16":
+        ta = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+        tb = torch.from_numpy(b.view(np.int16)).view(torch.bfloat16)
+        ref = (ta + tb).view(torch.int16).numpy().view(np.uint16)
+        nan_ref = ((ref & 0x7F80) == 0x7F80) & ((ref & 0x7F) != 0)
+        nan_got = ((got & 0x7F80) == 0x7F80) & ((got & 0x7F) != 0)
+    else:
+        with np.errstate(over="ignore", invalid="ignore"):
+            ref = (a.view(np.float16).astype(np.float64) + b.view(np.float16).astype(np.float64)) \
+                .astype(np.float16).view(np.uint16)
+        nan_ref = np.isnan(ref.view(np.float16))
+        nan_got = np.isnan(got.view(np.float16))
+    assert np.array_equal(nan_got, nan_ref)
+    assert nan_ref.any() and (~nan_ref).any()
+    assert np.array_equal(got[~nan_ref], ref[~nan_ref])
