@@ -41,6 +41,13 @@ __device__ __forceinline__ void st_relaxed(unsigned long long* p, unsigned long 
 // acquire-release fence at gpu scope: after relaxed loads that observed a
 // flag it acts as the acquire; before relaxed flag stores, as the release
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// post a flag or counter: a release store when it is the only word posted
+// (`alone`), else a relaxed store after the caller's fence
+__device__ __forceinline__ void post_word(unsigned long long* p, unsigned long long v, bool alone)
+{
+    if (alone) st_release(p, v);
+    else st_relaxed(p, v);
+}
 __device__ __forceinline__ unsigned long long gtimer()
 {
     unsigned long long t;
@@ -505,10 +512,32 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned par,
 // up to kDepBatch counters polled with relaxed loads issued together per
 // round trip, one acquire fence at the end.
 constexpr int kDepBatch = 8;
-static __device__ bool wait_deps(const KParams& P, const DDep* deps, int n, int si, unsigned long long& waited)
+static __device__ bool wait_deps(const KParams& P, const DDep* deps, int n, int si, unsigned long long& waited,
+                                 bool acq1 = false)
 {
     const unsigned long long base = (unsigned long long)(P.exec * P.m);
     unsigned long long t0 = 0;
+    if (n == 1 && acq1) {
+        // one counter (the sequential engine): acquire loads, no separate
+        // fence
+        const unsigned long long* c = P.counters + deps[0].counter;
+        const unsigned long long v = base + deps[0].value;
+        unsigned spins = 0;
+        while (ld_acquire(c) < v) {
+            if (!t0) t0 = gtimer();
+            ++spins;
+            if ((spins & 15) == 0) {
+                if (*(volatile int*)P.status != 0) return false;
+                if (gtimer() - t0 > P.timeout_ns) {
+                    record_timeout(P, si, WAIT_DEP);
+                    return false;
+                }
+            }
+            if (spins > 64) __nanosleep(32);
+        }
+        if (t0) waited += gtimer() - t0;
+        return true;
+    }
     for (int k0 = 0; k0 < n; k0 += kDepBatch) {
         const int nb = n - k0 < kDepBatch ? n - k0 : kDepBatch;
         const unsigned long long* c[kDepBatch];
@@ -551,7 +580,7 @@ static __device__ bool wait_deps(const KParams& P, const DDep* deps, int n, int 
 constexpr int kBatch = 4;
 static __device__ int wait_slots(const KParams& P, const DLink* Lin, const DLink* Lout, unsigned long long sin0,
                           unsigned long long sout0, long long out_rel0, unsigned in_idx0, unsigned out_idx0, int bmax,
-                          int si, unsigned long long& waited)
+                          int si, unsigned long long& waited, bool acq1 = false)
 {
     const unsigned S = (unsigned)P.S;
     // nothing to poll (an LL or absent incoming link, outgoing slots first
@@ -562,6 +591,26 @@ static __device__ int wait_slots(const KParams& P, const DLink* Lin, const DLink
     if (!poll_in && !poll_out) return bmax;
     unsigned long long t0 = 0;
     unsigned spins = 0;
+    if (acq1 && bmax == 1 && poll_in != poll_out) {
+        // one word (the sequential engine): acquire loads, no separate fence
+        const unsigned long long* w = poll_in ? P.flags + Lin->flag_base + in_idx0
+                                              : P.flags + Lout->flag_base + S + out_idx0;
+        const unsigned long long v = poll_in ? sin0 + 1 : sout0 + 1 - P.S;
+        while (ld_acquire(w) < v) {
+            if (!t0) t0 = gtimer();
+            ++spins;
+            if ((spins & 15) == 0) {
+                if (*(volatile int*)P.status != 0) return 0;
+                if (gtimer() - t0 > P.timeout_ns) {
+                    record_timeout(P, si, poll_in ? WAIT_FULL : WAIT_FREE);
+                    return 0;
+                }
+            }
+            if (spins > 64) __nanosleep(32);
+        }
+        if (t0) waited += gtimer() - t0;
+        return 1;
+    }
     while (true) {
         unsigned long long x[kBatch], y[kBatch];
 #pragma unroll
@@ -1476,9 +1525,9 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
         if (linked || k == 0) {
             if (tid == 0) {
                 int ok = k == 0 ? pre_ok : 1;
-                if (k == 0 && ok && ndeps > 0) ok = wait_deps(P, deps, ndeps, si, waited);
+                if (k == 0 && ok && ndeps > 0) ok = wait_deps(P, deps, ndeps, si, waited, true);
                 if (ok && linked)
-                    ok = wait_slots(P, Lin, Lout, sin, sout, st.seq_out + k, in_idx, out_idx, 1, si, waited) != 0;
+                    ok = wait_slots(P, Lin, Lout, sin, sout, st.seq_out + k, in_idx, out_idx, 1, si, waited, true) != 0;
                 *go = ok;
             }
             __syncthreads();
@@ -1553,12 +1602,13 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
             bool p_out = Lout && post && ok && !P.ll;
             bool p_sig = k == nslots - 1 && st.signal >= 0 && post && ok;
             if (P.ll && (p_in || p_sig) && *(volatile int*)P.status != 0) p_in = p_out = p_sig = false;
-            if (p_in || p_out || p_sig) fence_acq_rel_gpu();
-            if (p_in) st_relaxed(P.flags + Lin->flag_base + S + in_idx, sin + 1);
-            if (p_out) st_relaxed(P.flags + Lout->flag_base + out_idx, sout + 1);
+            // one word: a release store; several: one fence, then relaxed stores
+            const bool one = (int)p_in + (int)p_out + (int)p_sig == 1;
+            if ((p_in || p_out || p_sig) && !one) fence_acq_rel_gpu();
+            if (p_in) post_word(P.flags + Lin->flag_base + S + in_idx, sin + 1, one);
+            if (p_out) post_word(P.flags + Lout->flag_base + out_idx, sout + 1, one);
             if (k == nslots - 1) {
-                if (p_sig)
-                    st_relaxed(P.counters + st.signal, (unsigned long long)(P.exec * P.m + st.mb + 1));
+                if (p_sig) post_word(P.counters + st.signal, (unsigned long long)(P.exec * P.m + st.mb + 1), one);
                 if (P.timeline) {
                     unsigned long long* tl = P.timeline + 5ll * si;
                     tl[0] = t_start;
