@@ -681,19 +681,28 @@ def _oracle_inputs(it):
     return [datagen.draw(rng, it["dist"], nin, it["dt"]) for _ in range(it["R"])]
 
 
-def cpu_baseline(items, budget_s, divisor=None):
-    """The oracle (C, one thread) on a bounded sample: every collective of the
-    suite on the same inputs restricted to 1/divisor of the in-chunk offsets
-    (the oracle maps chunk to chunk offset by offset, so a column sample is
-    an exact part of the full result).  divisor=None calibrates it so that the
-    three timed repetitions take about ``budget_s`` seconds."""
-    import numpy as np
+def oracle_prepare(items):
+    """The oracle's programs and host inputs of every collective (drawn once)."""
     import oracle
     oracle.build()
     prepared = []
     for it in items:
         ops, nch = oracle_program(it["kind"], it["R"], it["G"])
         prepared.append((it, ops, nch, _oracle_inputs(it)))
+    return prepared
+
+
+def cpu_baseline(items, budget_s, divisor=None, prepared=None):
+    """The oracle (C, one thread) on a bounded sample: every collective of the
+    suite on the same inputs restricted to 1/divisor of the in-chunk offsets
+    (the oracle maps chunk to chunk offset by offset, so a column sample is
+    an exact part of the full result).  divisor=None calibrates it so that the
+    three timed repetitions take about ``budget_s`` seconds.  ``prepared``:
+    the result of oracle_prepare(items), when the caller keeps it."""
+    import numpy as np
+    import oracle
+    if prepared is None:
+        prepared = oracle_prepare(items)
 
     def one_pass(div, reps):
         t_total, bytes_total, sampled = 0.0, 0.0, []
@@ -740,9 +749,12 @@ def run_reference(args):
         _, nch = oracle_program(kind, R, G)
         items.append(dict(name=name, kind=kind, R=R, G=G, dt=dt, ce=ce, dist=dist, seed=seed, nin=nch[0] * ce,
                           opts=opts))
+    # inputs drawn once; every warm-up and timed step runs the oracle on the
+    # same bounded sample
+    prepared = oracle_prepare(items)
     cb = None
     for _ in range(args.warmup + args.steps):
-        cb = cpu_baseline(items, args.cpu_seconds, divisor=1024)
+        cb = cpu_baseline(items, args.cpu_seconds, divisor=1024, prepared=prepared)
     return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32/bf16/f16 (per collective)", "data": "synthetic (numpy PCG64 seeds 0-4)",
