@@ -37,14 +37,18 @@ def test_lost_signal_times_out_and_device_stays_usable(ccl):
     assert_bitexact(got, want)
 
 
-def test_lost_counter_times_out_and_device_stays_usable(ccl):
+@pytest.mark.parametrize("engine", [0, 1])
+def test_lost_counter_times_out_and_device_stays_usable(ccl, engine):
     """Direct copies signal dependency counters instead of FIFO flags: a
     threadblock of link-free copies that posts none of its counters makes its
-    dependents give up after 50 ms; the GPU then runs a fresh plan."""
+    dependents give up after 50 ms (on the sequential engine the wait for a
+    single counter is a loop of acquire loads); the GPU then runs a fresh
+    plan."""
     import torch
     import datagen
     s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 4, 0, ccl.FLAG_NOCHAIN_COPIES)
-    plan = ccl.Plan(s, 1024, F32, timeout_ms=50, link_mode=ccl.LINK_DIRECT, tb_alloc=ccl.TB_CONNECTION)
+    plan = ccl.Plan(s, 1024, F32, timeout_ms=50, link_mode=ccl.LINK_DIRECT, tb_alloc=ccl.TB_CONNECTION,
+                    engine=engine)
     steps = plan.steps()
     by_tb = {}
     for k, st in enumerate(steps):
@@ -61,7 +65,8 @@ def test_lost_counter_times_out_and_device_stays_usable(ccl):
         plan.status()
     assert ei.value.code == 8
     assert "gave up waiting" in ei.value.detail
-    got, want, _ = run_case(ccl, 0, 4, 0, 1024, F32, "normal", 1, fuse="nochain", link_mode=ccl.LINK_DIRECT)
+    got, want, _ = run_case(ccl, 0, 4, 0, 1024, F32, "normal", 1, fuse="nochain", link_mode=ccl.LINK_DIRECT,
+                            engine=engine)
     assert_bitexact(got, want)
 
 
