@@ -33,6 +33,9 @@ CASES = [
     (5, 6, 3, 640, F32, False, dict(microbatches=2, link_mode=1)),
     (0, 5, 0, 1500, I32, True, dict(mb_order=2, microbatches=3, link_mode=0)),
     (3, 4, 2, 2048, F32, True, dict(bulk=1, tile_bytes=4096, slot_bytes=8192)),
+    # receives folded into their senders (two-destination steps)
+    (1, 8, 0, 999, BF16, "nochain", dict(engine=1, link_mode=1, cluster=4)),
+    (0, 8, 0, 2053, F32, "nochain", dict(link_mode=1, channels=2)),
 ]
 
 
