@@ -249,7 +249,6 @@ std::string generate_plan_source(const PlanImage& img, int build, std::string* w
     // function on its instructions' entries
     std::string o;
     o += "// Kernel generated for one plan (see ccl_codegen.cpp).\n";
-    o += "#define CCL_MOVE_ATTR __noinline__\n";
     o += "#include \"ccl_core.cuh\"\nnamespace ccl {\n";
     (void)total_blocks;
     const int U = build <= 512 ? 8 : 4;
@@ -260,7 +259,10 @@ std::string generate_plan_source(const PlanImage& img, int build, std::string* w
     int nentries = 0, ndeps = 0;
     std::vector<std::vector<int>> seg_first(img.ntb);
     std::vector<int> nq(img.ntb, 0);
+    std::vector<int> prog_first(img.ntb + 1, 0), dep_first_of(img.ntb + 1, 0);   // each program's entries
     for (int b = 0; b < img.ntb; ++b) {
+        prog_first[b] = nentries;
+        dep_first_of[b] = ndeps;
         std::map<int, const InstrForm*> form_of;
         for (const InstrForm& f : forms[b]) form_of[f.ci] = &f;
         std::map<int, int> qin_slot, qout_slot;   // link -> this threadblock's counter
@@ -316,15 +318,38 @@ std::string generate_plan_source(const PlanImage& img, int build, std::string* w
             }
         }
     }
+    prog_first[img.ntb] = nentries;
+    dep_first_of[img.ntb] = ndeps;
+    // Each program copies its own entries (and their dependency lists, with
+    // dep_first rebased) into shared memory at start when they fit: reads of
+    // the table from global memory would go to L2 at every piece (the waits'
+    // acquire fences drop L1 lines).  kTabMax entries of at most 256 bytes.
+    int max_n = 0, max_d = 0;
+    for (int b = 0; b < img.ntb; ++b) {
+        max_n = std::max(max_n, prog_first[b + 1] - prog_first[b]);
+        max_d = std::max(max_d, dep_first_of[b + 1] - dep_first_of[b]);
+    }
+    const bool shared_tab = max_n > 0 && max_n <= 96 && max_n * 256 + max_d * 8 <= 28 * 1024;
+    auto ints = [](const std::vector<int>& v) {
+        std::string r;
+        for (size_t i = 0; i < v.size(); ++i) r += (i ? ", " : "") + std::to_string(v[i]);
+        return r;
+    };
     o += "static __device__ const GenInstr kGen[" + std::to_string(std::max(1, nentries)) + "] = {\n" +
          (nentries ? table : std::string("    {}\n")) + "};\n";
     o += "static __device__ const int2 kGenDep[" + std::to_string(std::max(1, ndeps)) + "] = {\n" +
          (ndeps ? dep_list : std::string("    {0, 0}")) + "\n};\n";
+    o += "static __device__ const int kProgFirst[" + std::to_string(img.ntb + 1) + "] = {" + ints(prog_first) + "};\n";
+    o += "static __device__ const int kDepFirst[" + std::to_string(img.ntb + 1) + "] = {" + ints(dep_first_of) + "};\n";
     for (int b = 0; b < img.ntb; ++b) {
+        // tab: the program's entries (tab[j - first of the program]); dep:
+        // the dependency list its entries index
         if (seq)
             o += "static __device__ __noinline__ void gtb" + std::to_string(b) +
-                 "(const KParams& P, int* go, GenStep* gs)\n{\n";
-        else o += "static __device__ __noinline__ void gtb" + std::to_string(b) + "(const KParams& P, CtlShared* sh)\n{\n";
+                 "(const KParams& P, int* go, GenStep* gs, const GenInstr* tab, const int2* dep)\n{\n";
+        else
+            o += "static __device__ __noinline__ void gtb" + std::to_string(b) +
+                 "(const KParams& P, CtlShared* sh, const GenInstr* tab, const int2* dep)\n{\n";
         o += "    const unsigned exec_mod = (unsigned)(P.exec % P.S);\n";
         if (!seq) o += "    int head = 0;\n";
         o += "    int si = " + std::to_string(img.tb_begin[b]) + ";\n";
@@ -339,11 +364,12 @@ std::string generate_plan_source(const PlanImage& img, int build, std::string* w
                  std::to_string(seg.window) + " : " + std::to_string(m) + ";\n";
             o += "#pragma unroll 1\n        for (int j = " + std::to_string(first) + "; j < " + std::to_string(first + n) +
                  "; ++j)\n";
+            const std::string entry = "tab[j - " + std::to_string(prog_first[b]) + "]";
             if (seq)
-                o += "            if (!gen_seq_block<" + std::to_string(U) + ">(P, go, gs, kGen[j], kGenDep, w0, w1, " +
+                o += "            if (!gen_seq_block<" + std::to_string(U) + ">(P, go, gs, " + entry + ", dep, w0, w1, " +
                      geom + ", si, q, exec_mod)) return;\n";
             else
-                o += "            if (!gen_issue_block(P, sh, kGen[j], kGenDep, w0, w1, " + geom +
+                o += "            if (!gen_issue_block(P, sh, " + entry + ", dep, w0, w1, " + geom +
                      ", si, head, q, exec_mod)) return;\n";
             o += "    }\n";
         }
@@ -354,18 +380,37 @@ std::string generate_plan_source(const PlanImage& img, int build, std::string* w
     const std::string maxt = std::to_string(build <= 512 ? 512 : 1024);
     o += "extern \"C\" __global__ void __launch_bounds__(" + maxt +
          ", 1) ccl_gen_kernel(const __grid_constant__ ccl::KParams P)\n{\n";
-    std::string sw = seq ? "switch (P.cluster > 1 ? blockIdx.x / P.cluster : blockIdx.x) {\n" : "switch (blockIdx.x) {\n";
+    const std::string prog = seq ? "(P.cluster > 1 ? blockIdx.x / P.cluster : blockIdx.x)" : "blockIdx.x";
+    std::string sw = "switch (" + prog + ") {\n";
     for (int b = 0; b < img.ntb; ++b)
-        sw += "    case " + std::to_string(b) + ": ccl::gtb" + std::to_string(b) + (seq ? "(P, &go_flag, &gstep)" : "(P, &sh)") +
-              "; break;\n";
+        sw += "    case " + std::to_string(b) + ": ccl::gtb" + std::to_string(b) +
+              (seq ? "(P, &go_flag, &gstep, gtab, gdep)" : "(P, &sh, gtab, gdep)") + "; break;\n";
+    // the program's table: a copy in shared memory, or the module's arrays
+    std::string tabinit;
+    if (shared_tab) {
+        tabinit += "    __shared__ __align__(16) ccl::GenInstr gtab_s[" + std::to_string(max_n) + "];\n";
+        tabinit += "    __shared__ int2 gdep_s[" + std::to_string(std::max(1, max_d)) + "];\n";
+        tabinit += "    {\n        const int pg = " + prog + ";\n";
+        tabinit += "        const int e0 = ccl::kProgFirst[pg], n = ccl::kProgFirst[pg + 1] - e0;\n";
+        tabinit += "        const int d0 = ccl::kDepFirst[pg], nd = ccl::kDepFirst[pg + 1] - d0;\n";
+        tabinit += "        if ((int)threadIdx.x < n) {\n            ccl::GenInstr g = ccl::kGen[e0 + threadIdx.x];\n";
+        tabinit += "            g.dep_first -= d0;\n            gtab_s[threadIdx.x] = g;\n        }\n";
+        tabinit += "        for (int i = threadIdx.x; i < nd; i += blockDim.x) gdep_s[i] = ccl::kGenDep[d0 + i];\n    }\n";
+        tabinit += "    const ccl::GenInstr* gtab = gtab_s;\n    const int2* gdep = gdep_s;\n";
+    } else {
+        tabinit += "    const ccl::GenInstr* gtab = ccl::kGen + ccl::kProgFirst[" + prog + "];\n";
+        tabinit += "    const int2* gdep = ccl::kGenDep;\n";
+    }
     sw += "    default: break;\n    }\n";
+    o += tabinit;
     if (seq) {
         o += "    __shared__ int go_flag;\n    __shared__ __align__(16) ccl::GenStep gstep;\n";
-        o += "    if (P.cluster > 1) ccl::group_sync(P);   // every CTA of the cluster has started\n    " + sw;
+        o += "    // every CTA of the cluster has started; the table is in place\n";
+        o += "    ccl::group_sync(P);\n    " + sw;
     } else {
         o += "    __shared__ __align__(16) ccl::CtlShared sh;\n";
         o += "    extern __shared__ __align__(128) unsigned char stages[];\n";
-        o += "    ccl::ctl_init(P, &sh);\n";
+        o += "    ccl::ctl_init(P, &sh);   // its barrier also publishes the table\n";
         o += "    const int warp = threadIdx.x >> 5;\n";
         o += "    if (warp < 3) {\n        if ((threadIdx.x & 31) == 0) {\n            if (warp == 0) {\n";
         o += "    " + sw;

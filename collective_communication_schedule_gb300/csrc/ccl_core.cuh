@@ -209,9 +209,8 @@ static __device__ void move_elem(const char* a, const char* b, char* o1, char* o
     }
 }
 
-// Kernels generated for single plans run many steps through one copy of
-// the data path (CCL_MOVE_ATTR __noinline__) to keep their code small; the
-// library's kernels inline it.
+// The data path is inlined into its callers; a translation unit may define
+// CCL_MOVE_ATTR (e.g. __noinline__) first to keep one out-of-line copy.
 #ifndef CCL_MOVE_ATTR
 #define CCL_MOVE_ATTR __forceinline__
 #endif
