@@ -68,9 +68,13 @@ SUITE = [
      # engine (fewer hand-offs per step), each program on a cluster of CTAs
      # that share its slots' data
      dict(fuse="nochain", channels=4, link_mode=1, engine=1, cluster=4, nthreads=256)),
-    ("rs_3m", 2, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4, engine=1, cluster=4, nthreads=256)),
+    # FIFOs at least one execution deep (8 slots): no slot is reused within
+    # an execution, so nothing is posted or waited for its consumption
+    ("rs_3m", 2, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4, engine=1, cluster=4, nthreads=256,
+                                                          fifo_slots=8)),
     ("ar_1m", 0, 8, 0, 0, 1 * MiB // 8, "uniform", 0, dict(fuse="nochain", link_mode=1, channels=1, tb_alloc=2,
-                                                            tb_budget=16, engine=1, cluster=8, nthreads=256)),
+                                                            tb_budget=16, engine=1, cluster=8, nthreads=128,
+                                                            fifo_slots=8)),
 ]
 ESIZE = {0: 4, 1: 2, 2: 2, 3: 4}
 NAMES = {0: "f32", 1: "bf16", 2: "f16", 3: "i32"}
