@@ -46,10 +46,11 @@ SUITE = [
     # fuse="nochain": reductions fused, copy-only receives left unchained so
     # that direct transport makes each all-gather hop one plain copy
     ("hier_ar", 3, 16, 8, 0, 4 * MiB, "normal", 2,
-     # the inter-group step keeps its FIFO hop (folding its receive into the
-     # sender, as the rings do, measured 5 % slower here)
+     # the in-group all-gather's copy hops run two at a time (copy chains
+     # folded); the inter-group step keeps its FIFO hop (folding its
+     # receive into the sender, as the rings do, measured 5 % slower here)
      dict(fuse="nochain", link_mode=1, channels=9, microbatches=16, tb_alloc=1, slot_bytes=65536, fifo_slots=8,
-          mb_window=4, fold=0)),
+          mb_window=4, fold=2)),
     ("a2a", 4, 32, 8, 2, 1 * MiB, "uniform", 3,
      dict(channels=8, link_mode=1, channel_scaling=0, tb_alloc=2, tb_budget=256)),
     ("ring_bf16", 0, 8, 0, 1, 32 * MiB, "normal", 4,
@@ -649,8 +650,10 @@ ORACLE_PROGRAMS = {0: ("ring_allreduce", lambda R, G: (R,)), 1: ("ring_allgather
                    2: ("ring_reducescatter", lambda R, G: (R,)), 3: ("hier_allreduce", lambda R, G: (G, R // G)),
                    4: ("alltoall_two_phase", lambda R, G: (G, R // G)), 5: ("alltonext", lambda R, G: (G, R // G))}
 # the plan option defaults the suite rows rely on (ccl_plan_opts_default):
-# direct transport unless a row asks for FIFOs
+# direct transport unless a row asks for FIFOs, receives and copy chains
+# folded unless a row says otherwise
 DEFAULT_LINK_MODE = 1
+DEFAULT_FOLD = 3
 
 
 def oracle_program(kind, R, G):
@@ -669,7 +672,7 @@ def oracle_bytes(kind, R, G, dt, ce, opts):
     fuse = opts.get("fuse", True)
     mode = "nochain" if fuse == "nochain" else ("full" if fuse else "none")
     direct = opts.get("link_mode", DEFAULT_LINK_MODE) == 1
-    fold = bool(opts.get("fold", 1))
+    fold = int(opts.get("fold", DEFAULT_FOLD))
     return (OB.schedule_bytes(ops, R, nch, ce, dt, mode, direct, fold), OB.min_bytes(ops, R, nch, ce, dt))
 
 

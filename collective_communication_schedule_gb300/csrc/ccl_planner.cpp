@@ -263,7 +263,11 @@ void allocate_connection(const ccl_schedule& s, const Timeline& tl, TBList* tbs,
             // a copy into another rank's buffer (direct transport) is a
             // connection of its own to that rank
             if (I.kind == CCL_I_COPY && I.dst.valid() && I.dst.rank != I.rank) out = CCL_MAX_RANKS + I.dst.rank;
-            if (I.kind == CCL_I_COPY2 && I.loc.valid() && I.loc.rank != I.rank) out = CCL_MAX_RANKS + I.loc.rank;
+            // (a two-destination copy: its first remote destination)
+            if (I.kind == CCL_I_COPY2) {
+                if (I.dst.valid() && I.dst.rank != I.rank) out = CCL_MAX_RANKS + I.dst.rank;
+                else if (I.loc.valid() && I.loc.rank != I.rank) out = CCL_MAX_RANKS + I.loc.rank;
+            }
             // a folded recv-reduce-copy-send writes the next rank directly
             // but keeps its incoming link: it joins the threadblock of that
             // link (no outgoing connection of its own)
@@ -997,10 +1001,129 @@ ccl_schedule direct_transport(const ccl_schedule& s, int* ndirect, bool fold)
     return d;
 }
 
+// Copy chains (after direct transport): a direct copy c2 that sends on,
+// unchanged, exactly the range another direct copy c1 wrote into c2's rank
+// is run by c1's pass instead -- one read written to both destinations (a
+// CCL_I_COPY2 holding the second destination in its local-operand range)
+// instead of c1's write and c2's read-back and write.  A ring AllGather's
+// k copy hops become ceil(k/2) steps.  c1 takes over c2's dependencies in
+// both directions; c2's writes then happen at c1's time, which is sound
+// when every instruction c2 waited for can come before c1 -- a pair whose
+// merged dependencies would close a cycle is left alone.  Pairs are formed
+// in dependency order (smallest index first among the ready ones), so each
+// chain pairs up from its head.
+int fold_copy_chains(ccl_schedule& d)
+{
+    const int ni = (int)d.instrs.size();
+    std::vector<std::set<int>> succ(ni), pred(ni);
+    std::map<std::pair<int, int>, int> exact;   // bit 0: an exact edge, bit 1: a non-exact one
+    auto add_edge = [&](int a, int b, bool ex) {
+        if (a == b) return;
+        succ[a].insert(b);
+        pred[b].insert(a);
+        exact[{a, b}] |= ex ? 1 : 2;
+    };
+    for (const Dep& e : d.deps) add_edge(e.from, e.to, e.exact);
+    for (const Xfer& X : d.xfers)
+        if (X.send_instr >= 0 && X.recv_instr >= 0) {
+            succ[X.send_instr].insert(X.recv_instr);
+            pred[X.recv_instr].insert(X.send_instr);
+        }
+    // topological order, smallest index first
+    std::vector<int> indeg(ni), order;
+    std::set<int> ready;
+    for (int i = 0; i < ni; ++i)
+        if ((indeg[i] = (int)pred[i].size()) == 0) ready.insert(i);
+    while (!ready.empty()) {
+        const int i = *ready.begin();
+        ready.erase(ready.begin());
+        order.push_back(i);
+        for (int j : succ[i])
+            if (--indeg[j] == 0) ready.insert(j);
+    }
+    if ((int)order.size() != ni) return 0;   // cyclic already: the timeline reports it
+    auto direct_copy = [&](int i) {
+        const Instr& I = d.instrs[i];
+        return I.kind == CCL_I_COPY && I.xfer_in < 0 && I.xfer_out < 0 && I.src.valid() && I.dst.valid() &&
+               I.dst.rank != I.rank;
+    };
+    std::vector<char> gone(ni, 0);
+    std::vector<int> mark(ni, -1);
+    int nfold = 0, epoch = 0;
+    for (int c1 : order) {
+        if (gone[c1] || !direct_copy(c1)) continue;
+        const Instr& A = d.instrs[c1];
+        for (int c2 : std::vector<int>(succ[c1].begin(), succ[c1].end())) {
+            if (gone[c2] || !direct_copy(c2)) continue;
+            const Instr& B = d.instrs[c2];
+            if (!B.src.same(A.dst) || B.count != A.count || B.dst.overlaps(A.src) || B.dst.overlaps(A.dst)) continue;
+            // every other instruction c2 waits for must not follow c1
+            std::vector<int> stack{c1};
+            bool cycle = false;
+            mark[c1] = ++epoch;
+            while (!stack.empty() && !cycle) {
+                const int v = stack.back();
+                stack.pop_back();
+                for (int w : succ[v]) {
+                    if (w == c2 || mark[w] == epoch) continue;
+                    if (pred[c2].count(w)) { cycle = true; break; }
+                    mark[w] = epoch;
+                    stack.push_back(w);
+                }
+            }
+            if (cycle) continue;
+            Instr& F = d.instrs[c1];
+            F.kind = CCL_I_COPY2;
+            F.loc = B.dst;
+            for (int x : std::vector<int>(pred[c2].begin(), pred[c2].end())) {
+                const int ex = exact[{x, c2}];
+                succ[x].erase(c2);
+                if (x == c1) continue;
+                if (ex & 1) add_edge(x, c1, true);
+                if (ex & 2) add_edge(x, c1, false);
+            }
+            for (int y : std::vector<int>(succ[c2].begin(), succ[c2].end())) {
+                const int ex = exact[{c2, y}];
+                pred[y].erase(c2);
+                if (ex & 1) add_edge(c1, y, true);
+                if (ex & 2) add_edge(c1, y, false);
+            }
+            pred[c2].clear();
+            succ[c2].clear();
+            gone[c2] = 1;
+            ++nfold;
+            break;
+        }
+    }
+    if (!nfold) return 0;
+    std::vector<int> inew(ni, -1);
+    std::vector<Instr> instrs;
+    for (int i = 0; i < ni; ++i)
+        if (!gone[i]) { inew[i] = (int)instrs.size(); instrs.push_back(d.instrs[i]); }
+    for (auto& X : d.xfers) {
+        X.send_instr = inew[X.send_instr];
+        X.recv_instr = inew[X.recv_instr];
+    }
+    std::vector<Dep> deps;
+    for (int a = 0; a < ni; ++a) {
+        if (gone[a]) continue;
+        for (int b : succ[a]) {
+            if (gone[b]) continue;
+            auto it = exact.find({a, b});
+            if (it == exact.end()) continue;   // a transfer edge
+            if (it->second & 1) deps.push_back(Dep{inew[a], inew[b], true});
+            if (it->second & 2) deps.push_back(Dep{inew[a], inew[b], false});
+        }
+    }
+    d.instrs = std::move(instrs);
+    d.deps = std::move(deps);
+    return nfold;
+}
+
 namespace {
 
 ccl_status_t build_plan_one(const ccl_schedule& s_in, int64_t ce, int32_t dtype, const ccl_plan_opts_t& o,
-                            PlanImage* img, bool fold)
+                            PlanImage* img, int fold)
 {
     if (ce <= 0) return fail(CCL_ERR_INVALID_ARG, "chunk_elems must be positive");
     if (dtype < CCL_F32 || dtype > CCL_I32) return fail(CCL_ERR_INVALID_ARG, "unknown dtype");
@@ -1031,12 +1154,13 @@ ccl_status_t build_plan_one(const ccl_schedule& s_in, int64_t ce, int32_t dtype,
     if (o.protocol == CCL_PROTO_LL && (ce * esize_of(dtype)) % 16)
         return fail(CCL_ERR_UNSUPPORTED, "the LL protocol needs chunks of a multiple of 16 bytes");
     if (o.timeout_ms <= 0) return fail(CCL_ERR_INVALID_ARG, "timeout_ms must be positive");
-    if (o.fold != 0 && o.fold != 1) return fail(CCL_ERR_INVALID_ARG, "fold must be 0 or 1");
+    if (o.fold < 0 || o.fold > 3) return fail(CCL_ERR_INVALID_ARG, "fold must be in 0..3");
 
     if (o.link_mode != CCL_LINK_FIFO && o.link_mode != CCL_LINK_DIRECT)
         return fail(CCL_ERR_INVALID_ARG, "unknown link_mode");
     int ndirect = 0;
-    const ccl_schedule s = o.link_mode == CCL_LINK_DIRECT ? direct_transport(s_in, &ndirect, fold) : s_in;
+    ccl_schedule s = o.link_mode == CCL_LINK_DIRECT ? direct_transport(s_in, &ndirect, (fold & 1) != 0) : s_in;
+    if (o.link_mode == CCL_LINK_DIRECT && (fold & 2)) fold_copy_chains(s);
     const int es = esize_of(dtype);
     Timeline tl;
     ccl_status_t st = build_timeline(s, o.scheduler, &tl);
@@ -1191,12 +1315,12 @@ ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const 
     // recv-reduce-copy-send is folded into its sender first (one pass
     // writes both destinations); where that makes the timeline cyclic or
     // the threadblocks deadlock, the sender keeps its FIFO
-    const bool fold = o.link_mode == CCL_LINK_DIRECT && o.fold != 0;
+    const int fold = o.link_mode == CCL_LINK_DIRECT ? o.fold : 0;
     auto plan_one = [&](const ccl_schedule& x) {
         ccl_status_t r = build_plan_one(x, ce, dtype, o, img, fold);
         if (fold && (r == CCL_ERR_CYCLE || r == CCL_ERR_DEADLOCK)) {
             const std::string why = ccl_last_error_detail();
-            if (build_plan_one(x, ce, dtype, o, img, false) == CCL_OK) return CCL_OK;
+            if (build_plan_one(x, ce, dtype, o, img, 0) == CCL_OK) return CCL_OK;
             fail(r, why);
         }
         return r;

@@ -394,7 +394,7 @@ void ccl_plan_opts_default(ccl_plan_opts_t* o)
     o->engine = CCL_ENGINE_PIPELINED;
     o->codegen = 0;
     o->cluster = 0;
-    o->fold = 1;
+    o->fold = 3;
 }
 
 ccl_status_t ccl_schedule_compile(const ccl_op_t* ops, int32_t nops, int32_t nranks, const int32_t nchunks[3],

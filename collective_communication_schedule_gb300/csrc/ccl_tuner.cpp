@@ -8,8 +8,10 @@
 // chunk size are optimised one coordinate at a time, raising a parameter
 // while bandwidth keeps improving (bandwidth is unimodal in each of them).
 // Grids: channels {1,2,4,8,12,16,24,32,48}, threads {128,256,512,1024},
-// slot size 16 KiB .. 4 MiB in powers of two, and on the sequential engine
-// CTAs per threadblock program {1,2,4,8}.  A probe is the median of
+// slot size 16 KiB .. 4 MiB in powers of two, on the sequential engine
+// CTAs per threadblock program {1,2,4,8}, and with direct transport the
+// folds {0,1,2,3} (receives into senders, copy chains; not unimodal, but
+// the descent starts at the caller's folds and tries its neighbours).  A probe is the median of
 // `reps` CUDA-event-timed executions after one warm-up; a point whose plan
 // cannot be built (threadblocks not co-resident, FIFO too small) scores 0.
 #include <cuda_runtime.h>
@@ -34,12 +36,12 @@ struct Prober {
     cudaStream_t stream;
     int reps;
     int probes = 0;
-    std::map<std::tuple<int, int, int64_t, int, int, int, int, int>, double> cache;  // -> microseconds (0 = infeasible)
+    std::map<std::tuple<int, int, int64_t, int, int, int, int, int, int>, double> cache;  // -> microseconds (0 = infeasible)
 
     double time_us(const ccl_plan_opts_t& o)
     {
         auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol, o.link_mode, o.engine,
-                                   o.cluster);
+                                   o.cluster, o.fold);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
         ++probes;
@@ -135,6 +137,7 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
         base.engine = z.engine;
         base.cluster = z.cluster;
         base.codegen = z.codegen;
+        base.fold = z.fold;
     }
     if (!base.nthreads) base.nthreads = 512;
     std::vector<int> gc;
@@ -144,11 +147,11 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
     if (to.max_channels && base.channels > to.max_channels) base.channels = to.max_channels;
     std::vector<int> gt(std::begin(kThreads), std::end(kThreads));
     std::vector<int64_t> gs = slot_grid();
-    std::map<std::tuple<int, int, int64_t, int, int, int, int, int>, double> cache;
+    std::map<std::tuple<int, int, int64_t, int, int, int, int, int, int>, double> cache;
     int nprobe = 0;
     auto measure = [&](const ccl_plan_opts_t& o) {
         auto key = std::make_tuple(o.channels, o.nthreads, o.slot_bytes, o.tb_alloc, o.protocol, o.link_mode, o.engine,
-                                   o.cluster);
+                                   o.cluster, o.fold);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
         ++nprobe;
@@ -171,26 +174,35 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
         const bool seq = cur.engine == CCL_ENGINE_SEQUENTIAL;
         const std::vector<int> gk = seq ? std::vector<int>{1, 2, 4, 8} : std::vector<int>{1};
         if (!seq) cur.cluster = 0;
+        // direct transport also chooses its folds (receives, copy chains)
+        const bool direct = cur.link_mode == CCL_LINK_DIRECT;
+        const std::vector<int> gf = direct ? std::vector<int>{0, 1, 2, 3} : std::vector<int>{cur.fold};
         int ic = nearest(gc, cur.channels), it = nearest(gt, cur.nthreads), is = nearest(gs, cur.slot_bytes);
         int ik = seq ? nearest(gk, std::max(1, cur.cluster)) : 0;
-        auto eval = [&](int c, int t, int sl, int k) {
+        int ifo = direct ? nearest(gf, cur.fold) : 0;
+        auto eval = [&](int c, int t, int sl, int k, int f) {
             ccl_plan_opts_t o = cur;
             o.channels = gc[c];
             o.nthreads = gt[t];
             o.slot_bytes = gs[sl];
             o.cluster = gk[k] > 1 ? gk[k] : 0;
+            o.fold = gf[f];
             return measure(o);
         };
-        double bw = eval(ic, it, is, ik);
+        std::vector<int> coords{0, 1, 2};
+        if (seq) coords.push_back(3);
+        if (direct) coords.push_back(4);
+        double bw = eval(ic, it, is, ik, ifo);
         for (int round = 0; round < to.max_rounds; ++round) {
             bool moved = false;
-            for (int coord = 0; coord < (seq ? 4 : 3); ++coord) {
-                int* idx = coord == 0 ? &ic : coord == 1 ? &it : coord == 2 ? &is : &ik;
+            for (int coord : coords) {
+                int* idx = coord == 0 ? &ic : coord == 1 ? &it : coord == 2 ? &is : coord == 3 ? &ik : &ifo;
                 int n = coord == 0 ? (int)gc.size() : coord == 1 ? (int)gt.size() : coord == 2 ? (int)gs.size()
-                                                                                              : (int)gk.size();
+                        : coord == 3 ? (int)gk.size() : (int)gf.size();
                 auto at = [&](int v) {
-                    return coord == 0 ? eval(v, it, is, ik) : coord == 1 ? eval(ic, v, is, ik)
-                           : coord == 2 ? eval(ic, it, v, ik) : eval(ic, it, is, v);
+                    return coord == 0 ? eval(v, it, is, ik, ifo) : coord == 1 ? eval(ic, v, is, ik, ifo)
+                           : coord == 2 ? eval(ic, it, v, ik, ifo) : coord == 3 ? eval(ic, it, is, v, ifo)
+                                                                     : eval(ic, it, is, ik, v);
                 };
                 // raise while bandwidth improves; if the first raise does not
                 // help, try lowering the same way
@@ -218,6 +230,7 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
             overall.nthreads = gt[it];
             overall.slot_bytes = gs[is];
             overall.cluster = gk[ik] > 1 ? gk[ik] : 0;
+            overall.fold = gf[ifo];
         }
     }
     *best = overall;

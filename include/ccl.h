@@ -122,8 +122,9 @@ typedef enum {
     CCL_I_COPY_SEND = 9, /* dst <- src; slot_out <- src */
     CCL_I_NKINDS = 10,   /* kinds the compiler emits */
     /* plans only (ccl_plan_steps), made by direct transport from a sender
-       and the plain receive it feeds: */
-    CCL_I_COPY2 = 10,    /* copy-send + receive: dst <- src; loc <- src (loc: the receiver's destination) */
+       and the plain receive it feeds (or the copy that forwards it): */
+    CCL_I_COPY2 = 10,    /* two-destination copy: dst <- src; loc <- src (a copy-send and its receive, or a
+                            chain of two direct copies; loc: the second destination) */
     CCL_I_RRC2 = 11      /* recv-reduce-copy-send + receive: t <- local (+) slot_in; dst <- t; src <- t
                             (src: the receiver's destination) */
 } ccl_instr_kind_t;
@@ -315,12 +316,22 @@ typedef enum {
  *                 step moves on `cluster` SMs instead of one, for the
  *                 latency-bound sizes where a single CTA's data time sets the
  *                 length of every hop.
- *   fold        : with direct transport, 1 (default): a plain receive fed by
- *                 a copy-send or a recv-reduce-copy-send is folded into its
- *                 sender, whose pass then writes the receiver's buffer too
- *                 (CCL_I_COPY2 / CCL_I_RRC2 steps; one step and 2 bytes per
- *                 element byte fewer per such pair), unless the plan would
- *                 then cycle or deadlock.  0: such senders keep their FIFO.
+ *   fold        : with direct transport, a bit mask (default 3: both).
+ *                 Bit 0 (1): a plain receive fed by a copy-send or a
+ *                 recv-reduce-copy-send is folded into its sender, whose
+ *                 pass then writes the receiver's buffer too (CCL_I_COPY2 /
+ *                 CCL_I_RRC2 steps; one step and 2 bytes per element byte
+ *                 fewer per such pair); cleared, such senders keep their
+ *                 FIFO.  Bit 1 (2): copy chains -- a direct copy that sends
+ *                 on, unchanged, exactly the range another direct copy
+ *                 delivered is run by that copy's pass (a CCL_I_COPY2 with
+ *                 two remote destinations: one read written twice, 3 bytes
+ *                 per element byte instead of 2 + 2, one step fewer); a
+ *                 chain of k copies from its head becomes ceil(k/2) steps,
+ *                 and a pair whose merged dependencies would cycle is kept
+ *                 apart.  A folded plan that would cycle or deadlock is
+ *                 planned again without folds.  Values outside 0..3:
+ *                 CCL_ERR_INVALID_ARG.
  *   codegen     : 0 (default): the library's kernels interpret the plan's
  *                 step records.  1: ccl_plan_create generates CUDA source
  *                 for this one plan (ReSCCL report, §II.2: a kernel per
@@ -357,7 +368,8 @@ typedef struct {
     int32_t engine;      /* CCL_ENGINE_* */
     int32_t codegen;     /* 1: run a kernel generated and compiled for this plan (see below) */
     int32_t cluster;     /* sequential engine: CTAs per threadblock program (0 or 1: one; 2, 4, 8) */
-    int32_t fold;        /* direct transport: 1 (default) folds plain receives into their senders */
+    int32_t fold;        /* direct transport: bit 0 folds plain receives into their senders, bit 1
+                            copy chains (default 3) */
 } ccl_plan_opts_t;
 
 void ccl_plan_opts_default(ccl_plan_opts_t* o);
@@ -621,10 +633,11 @@ ccl_status_t ccl_allreduce_ring_noalloc(void* const* in_bufs, void* const* out_b
  * The search of ccl_tune on its own (AutoCCL report, research method 1-2):
  * the implementation parameters threadblock policy (connection / balanced)
  * x protocol (simple / LL) x transport (FIFO / direct) x engine (pipelined
- * / sequential) make sixteen subspaces; in
- * each, coordinate descent over channels, threads and slot
- * size (and CTAs per program on the sequential engine), driven by a caller-supplied probe that returns the bandwidth of a
- * configuration (any unit, <= 0 = cannot run).  start (nullable) is the first point; best gets
+ * / sequential) make sixteen subspaces; in each, coordinate descent over
+ * channels, threads and slot size (and CTAs per program on the sequential
+ * engine, and the folds 0..3 with direct transport), driven by a
+ * caller-supplied probe that returns the bandwidth of a configuration (any
+ * unit, <= 0 = cannot run).  start (nullable) is the first point; best gets
  * the winner, *best_bw its bandwidth, *probes the number of distinct
  * configurations probed.  Host only; no device is touched unless the probe
  * does.

@@ -33,7 +33,9 @@ does), applied per rank in program order until nothing changes:
 
 Direct transport (the plan option): a plain send whose transfer ends in a
 plain receive is one copy into the receiver's buffer (2 bytes per element
-byte instead of 2 + 2).  Channels and micro-batches split ranges without
+byte instead of 2 + 2), and with copy chains folded a copy that sends on
+exactly what another one delivered is written by that one's pass too (3
+instead of 2 + 2).  Channels and micro-batches split ranges without
 changing these totals.
 """
 from __future__ import annotations
@@ -133,6 +135,10 @@ def _plain_send(h):
 def fused_instructions(ops, nranks, fuse="full"):
     """The fused instruction kinds of ``ops`` as (kind, rank, count, sent,
     received) tuples; ``fuse``: "full", "nochain" or "none"."""
+    return [(h.kind(), h.rank, h.count, h.send, h.recv) for h in _fused_halves(ops, nranks, fuse)]
+
+
+def _fused_halves(ops, nranks, fuse):
     halves = _lower(ops)
     if fuse != "none":
         changed = True
@@ -185,24 +191,65 @@ def fused_instructions(ops, nranks, fuse="full"):
                             break
                 if changed:
                     break
-    return [(h.kind(), h.rank, h.count, h.send, h.recv) for h in halves if h.alive]
+    return [h for h in halves if h.alive]
 
 
-def schedule_bytes(ops, nranks, nchunks, chunk_elems, dtype, fuse="full", direct=True, fold=True):
+def _chain_folds(halves):
+    """Element chunks saved by folding copy chains under direct transport.
+
+    A direct copy is a plain send whose transfer ends in a plain receive.
+    When a later direct copy sends on, unchanged, exactly the range an
+    earlier one received, the earlier copy's pass writes both destinations:
+    one read written twice (3) instead of 2 + 2.  A copy that has taken one
+    over writes two places already and takes no other; the transfers are
+    visited in program order, so a chain pairs up from its head.  The
+    second copy's destination must not overlap the first one's ranges."""
+    sends = {h.send: h for h in halves if h.send is not None}
+    recvs = {h.recv: h for h in halves if h.recv is not None}
+    direct = sorted(t for t, h in sends.items() if h.kind() == "send" and recvs[t].kind() == "recv")
+    by_rank = {}
+    for h in sorted(halves, key=lambda h: h.pos):
+        by_rank.setdefault(h.rank, []).append(h)
+    gone, saved = set(), 0
+    for t1 in direct:
+        if t1 in gone:
+            continue
+        s1, r1 = sends[t1], recvs[t1]
+        for t2 in direct:
+            if t2 <= t1 or t2 in gone:
+                continue
+            s2, r2 = sends[t2], recvs[t2]
+            if s2.rank != r1.rank or s2.src != r1.dst or s2.count != r1.count:
+                continue
+            if _overlap(r2.dst, s1.src) or _overlap(r2.dst, r1.dst):
+                continue
+            if not _unchanged(by_rank[r1.rank], r1.dst, r1.pos, s2.pos):
+                continue
+            gone.add(t2)
+            saved += r1.count
+            break
+    return saved
+
+
+def schedule_bytes(ops, nranks, nchunks, chunk_elems, dtype, fuse="full", direct=True, fold=1):
     """Bytes one execution reads and writes (buffers and FIFO slots) when
     ``ops`` runs as fused instructions; ``direct``: a plain receive whose
     sender is a plain send, a copy-send or a recv-reduce-copy-send takes no
     FIFO: the sender writes the receiver's buffer itself (send 2 + receive
     2 -> one copy of 2; copy-send 3 + receive 2 -> one read written twice,
-    3; recv-reduce-copy-send 4 + receive 2 -> 4; ``fold`` False keeps the
-    last two with their FIFO)."""
-    instrs = fused_instructions(ops, nranks, fuse)
-    units = sum(FACTOR[k] * cnt for k, _, cnt, _, _ in instrs)
+    3; recv-reduce-copy-send 4 + receive 2 -> 4).  ``fold`` bit 0 (True)
+    takes the last two without their FIFO (cleared: they keep it); bit 1
+    also folds copy chains (``_chain_folds``)."""
+    halves = _fused_halves(ops, nranks, fuse)
+    units = sum(FACTOR[h.kind()] * h.count for h in halves)
     if direct:
-        sender = {s: k for k, _, _, s, _ in instrs if s is not None}
-        for k, _, cnt, _, recv in instrs:
-            if k == "recv" and (sender[recv] == "send" or (fold and sender[recv] in ("copy_send", "rrcs"))):
-                units -= 2 * cnt
+        sender = {h.send: h.kind() for h in halves if h.send is not None}
+        for h in halves:
+            if h.kind() == "recv" and (sender[h.recv] == "send" or
+                                       (int(fold) & 1 and sender[h.recv] in ("copy_send", "rrcs"))):
+                units -= 2 * h.count
+        if int(fold) & 2:
+            units -= _chain_folds(halves)
     return units * int(chunk_elems) * ESIZE[dtype]
 
 

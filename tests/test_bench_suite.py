@@ -39,13 +39,17 @@ def test_ring_rows_match_the_closed_form(name):
     each of them, N (R - 2) in all; and the first all-gather hop of every
     chunk -- the recv-reduce-copy-send that completes it and the plain
     receive it feeds -- writes the next rank's output directly, saving the
-    receive's 2 bytes per element byte: 2 N in all."""
+    receive's 2 bytes per element byte: 2 N in all.  With copy chains
+    folded the R - 2 middle hops of a chunk run two at a time (one read
+    written to two ranks), one byte per element byte less per pair:
+    floor((R - 2) / 2) N more."""
     row = [r for r in bench.SUITE if r[0] == name][0]
     _, kind, R, G, dt, cb, dist, seed, opts = row
     assert opts.get("fuse") == "nochain" and opts.get("link_mode") == 1
     N = R * cb                       # R chunks of cb bytes per rank
     _, st, _ = _plan(row)
-    assert st.schedule_bytes == R * N * 6 - 4 * N - N * (R - 2) - 2 * N
+    assert opts.get("fold", bench.DEFAULT_FOLD) == 3
+    assert st.schedule_bytes == R * N * 6 - 4 * N - N * (R - 2) - 2 * N - (R - 2) // 2 * N
     assert st.min_bytes == 2 * R * N
 
 
@@ -59,15 +63,23 @@ def test_hier_allgather_benchmark_plans_fit():
     unfused with direct copies, plan within the co-residency limit at the
     benchmark's size and move the same bytes: every one of the R x R output
     chunks is written once by one copy that reads one chunk (2 R^2 chunks),
-    against the collective minimum of R input and R^2 output chunks."""
+    against the collective minimum of R input and R^2 output chunks (copy
+    chains not folded).  With copy chains folded both move fewer bytes, as
+    many as the oracle counts for their programs."""
+    from oracle import bytes as OB
+    from oracle import schedules as OS
     G, ng = 8, 2
     R, ce = G * ng, 2 * MiB
     ops, nch = bench.hier_allgather_program(G, ng)
     hier = ccl.Schedule.compile(ops, R, nch, fuse=False)
     flat = ccl.Schedule.builtin(ccl.RING_ALLGATHER, R, 0, ccl.FLAG_NOFUSE)
-    for s in (hier, flat):
+    for s, prog in ((hier, ops), (flat, OS.ring_allgather(R)[0])):
         for o in (dict(channels=8, link_mode=1), dict(channels=8, link_mode=1, tb_alloc=2, tb_budget=304)):
-            st = s.check(ce, 1, **o)
+            st = s.check(ce, 1, fold=1, **o)
             assert st.nthreadblocks <= 2 * 152
             assert st.schedule_bytes == 2 * R * R * ce * 2
             assert st.min_bytes == (R + R * R) * ce * 2
+            folded = s.check(ce, 1, fold=3, **o)
+            assert folded.nthreadblocks <= 2 * 152
+            assert folded.schedule_bytes < st.schedule_bytes
+            assert folded.schedule_bytes == OB.schedule_bytes(prog, R, nch, ce, 1, "none", True, 3)

@@ -176,9 +176,10 @@ def test_nochain_keeps_copy_receives_apart():
         # output (2 bytes per element byte) instead of a receive-copy-send
         # (3), and the recv-reduce-copy-send that completes a chunk writes
         # the next rank's output itself, so that rank's receive (2) goes
+        # (copy chains not folded)
         ce, es = 64, 4
-        st_full = full.check(ce, F32, link_mode=ccl.LINK_DIRECT)
-        st_nochain = nochain.check(ce, F32, link_mode=ccl.LINK_DIRECT)
+        st_full = full.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=1)
+        st_nochain = nochain.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=1)
         assert st_nochain.schedule_bytes == st_full.schedule_bytes - R * (R - 2) * ce * es - 2 * R * ce * es
 
 
@@ -668,22 +669,90 @@ def test_direct_transport_folds_a_copy_send_and_its_receive():
     R, ce = 8, 1024
     s = ccl.Schedule.builtin(ccl.RING_ALLGATHER, R, 0, ccl.FLAG_NOCHAIN_COPIES)
     fifo = s.check(ce, F32, link_mode=ccl.LINK_FIFO)
-    direct = s.check(ce, F32, link_mode=ccl.LINK_DIRECT)
+    direct = s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=1)
     assert direct.nlinks == 0 and fifo.nlinks == R
     assert direct.schedule_bytes == R * 15 * ce * 4
     assert fifo.schedule_bytes == R * (3 + 7 * 2 + 6 * 2) * ce * 4   # copy-send, 7 receives, 6 sends
     ops, nch = OS.ring_allgather(R)
-    assert OB.schedule_bytes(ops, R, nch, ce, F32, fuse="nochain", direct=True) == direct.schedule_bytes
+    assert OB.schedule_bytes(ops, R, nch, ce, F32, fuse="nochain", direct=True, fold=1) == direct.schedule_bytes
 
 
 def test_fold_option():
-    """fold = 0 keeps the copy-send's FIFO hop (and its bytes); other values
-    than 0 and 1 are refused; the library default folds."""
-    assert ccl.default_opts().fold == 1
+    """fold = 0 keeps the copy-send's FIFO hop (and its bytes); values
+    outside 0..3 are refused; the library default folds receives."""
+    assert ccl.default_opts().fold & 1
     R, ce = 8, 1024
     s = ccl.Schedule.builtin(ccl.RING_ALLGATHER, R, 0, ccl.FLAG_NOCHAIN_COPIES)
     kept = s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=0)
     assert kept.nlinks == R and kept.schedule_bytes == R * (3 + 2 + 6 * 2) * ce * 4
-    with pytest.raises(ccl.CclError) as e:
-        s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=2)
-    assert e.value.code == 1
+    for bad in (-1, 4):
+        with pytest.raises(ccl.CclError) as e:
+            s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=bad)
+        assert e.value.code == 1
+
+
+def test_tuner_keeps_the_starting_fold():
+    """The search starts from the caller's options, folds included (not
+    reset to the library default): the first probe and every FIFO probe
+    carry the caller's fold setting."""
+    seen = []
+
+    def probe(o):
+        seen.append((o.link_mode, o.fold))
+        return 1.0 + 0.001 * o.channels
+    start = ccl.default_opts()
+    start.fold, start.link_mode = 1, ccl.LINK_FIFO
+    ccl.tune_search(probe, start)
+    assert seen[0] == (ccl.LINK_FIFO, 1)
+    assert {f for m, f in seen if m == ccl.LINK_FIFO} == {1}
+
+
+def test_coordinate_descent_chooses_the_folds_with_direct_transport():
+    """With direct transport the folds are a coordinate (from the caller's
+    3 down to 2 here, where the surface peaks); FIFO subspaces keep the
+    caller's folds."""
+    seen = set()
+
+    def probe(o):
+        seen.add((o.link_mode, o.fold))
+        return 1.0 + (0.5 if o.link_mode == ccl.LINK_DIRECT and o.fold == 2 else 0) + 0.001 * o.channels
+    best, bw, n = ccl.tune_search(probe)
+    assert best.link_mode == ccl.LINK_DIRECT and best.fold == 2
+    assert {f for m, f in seen if m == ccl.LINK_FIFO} == {ccl.default_opts().fold}
+    assert {f for m, f in seen if m == ccl.LINK_DIRECT} >= {2, 3}
+
+
+def test_direct_transport_folds_copy_chains():
+    """fold bit 1: the ring AllGather's chain of 6 direct copies after the
+    folded copy-send becomes 3 two-destination copies (3 bytes per element
+    byte each instead of 2 + 2), and every threadblock program 4 steps
+    instead of 7; the plan's steps and bytes say so, with or without the
+    receive fold (bit 0)."""
+    R, ce = 8, 1024
+    s = ccl.Schedule.builtin(ccl.RING_ALLGATHER, R, 0, ccl.FLAG_NOCHAIN_COPIES)
+    units = {0: 3 + 2 + 6 * 2, 1: 3 + 6 * 2, 2: 3 + 2 + 3 * 3, 3: 3 + 3 * 3}
+    for fold, u in units.items():
+        st = s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=fold, microbatches=1)
+        assert st.schedule_bytes == R * u * ce * 4, fold
+    p1 = s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=1, microbatches=1)
+    p3 = s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=3, microbatches=1)
+    assert p1.nsteps == R * 7 and p3.nsteps == R * 4
+    # FIFO transport: nothing to fold
+    assert s.check(ce, F32, link_mode=ccl.LINK_FIFO, fold=3).schedule_bytes == \
+        s.check(ce, F32, link_mode=ccl.LINK_FIFO, fold=0).schedule_bytes
+
+
+def test_copy_chain_fold_keeps_dependencies():
+    """A folded pair runs at the first copy's time, so everything the second
+    copy waited for must be able to come first: a program where a rank
+    overwrites the range it forwards between receiving and sending it keeps
+    the two copies apart (the oracle agrees on the bytes)."""
+    from oracle import bytes as OB
+    IN_, OUT_ = 0, 1
+    ops = [(0, 0, IN_, 0, 1, OUT_, 0, 1),     # rank 0 -> rank 1
+           (0, 1, IN_, 1, 1, OUT_, 0, 1),     # rank 1 overwrites it locally
+           (0, 1, OUT_, 0, 2, OUT_, 0, 1)]    # and forwards the new value
+    s = ccl.Schedule.compile(ops, 3, (2, 2, 0), fuse=False)
+    st = s.check(64, F32, link_mode=ccl.LINK_DIRECT, fold=3)
+    assert st.schedule_bytes == OB.schedule_bytes(ops, 3, (2, 2, 0), 64, F32, "none", True, 3)
+    assert st.schedule_bytes == (2 + 2 + 2) * 64 * 4

@@ -36,6 +36,11 @@ CASES = [
     # receives folded into their senders (two-destination steps)
     (1, 8, 0, 999, BF16, "nochain", dict(engine=1, link_mode=1, cluster=4)),
     (0, 8, 0, 2053, F32, "nochain", dict(link_mode=1, channels=2)),
+    # copy chains folded too (two remote destinations in one step)
+    (1, 8, 0, 999, BF16, "nochain", dict(engine=1, link_mode=1, cluster=4, fold=3)),
+    (0, 8, 0, 2053, F32, "nochain", dict(link_mode=1, channels=2, fold=3)),
+    (3, 8, 4, 1024, F32, "nochain", dict(link_mode=1, microbatches=4, mb_window=2, tb_alloc=1, fold=3)),
+    (5, 6, 3, 640, F32, False, dict(microbatches=2, link_mode=1, fold=2)),
 ]
 
 

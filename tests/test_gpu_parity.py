@@ -496,6 +496,53 @@ def test_allreduce_with_folded_reduce_copy_send_bitexact(ccl, R, opts):
     assert_bitexact(to_host(d, BF16), want)
 
 
+CHAIN_OPTS = [dict(), dict(channels=3, microbatches=2), dict(engine=1), dict(engine=1, cluster=4),
+              dict(protocol=1), dict(engine=1, protocol=1), dict(tb_alloc=2, channels=2),
+              dict(bulk=1, tile_bytes=4096), dict(microbatches=4, mb_window=2, tb_alloc=1)]
+
+
+@pytest.mark.parametrize("opts", CHAIN_OPTS)
+@pytest.mark.parametrize("kind,R,G,fuse,dtype", [(1, 8, 0, "nochain", BF16), (1, 5, 0, "nochain", F32),
+                                                 (0, 8, 0, "nochain", BF16), (0, 4, 0, "nochain", F32),
+                                                 (3, 8, 4, "nochain", F32), (5, 6, 3, False, F32)])
+@pytest.mark.parametrize("fold", [2, 3])
+def test_copy_chains_folded_bitexact(ccl, opts, kind, R, G, fuse, dtype, fold):
+    """Direct transport with copy chains folded: a copy that sends on what
+    another direct copy delivered is written by that copy's pass (two
+    remote destinations in one step) -- ring AllGather and AllReduce
+    all-gather hops, the hierarchical AllReduce's in-group all-gather, the
+    AllToNext relays; every engine, protocol and allocation; ragged chunks
+    (LL: 16-byte multiples); then in place where the collective allows."""
+    import torch
+    import datagen
+    import oracle
+    from gpu_helpers import oracle_program, to_device, empty_outputs, to_host
+    ll = opts.get("protocol") == 1
+    ce = 4096 if ll else 3001
+    flags = ccl.FLAG_NOCHAIN_COPIES if fuse == "nochain" else ccl.FLAG_NOFUSE
+    sched = ccl.Schedule.builtin(kind, R, G, flags)
+    plan = ccl.Plan(sched, ce, dtype, link_mode=1, slot_bytes=4096, fold=fold, **opts)
+    two_remote = [st for st in plan.steps() if st["kind"] == ccl.KIND_NAMES.index("copy2")]
+    assert two_remote
+    assert plan.stats().schedule_bytes < sched.check(ce, dtype, link_mode=1, slot_bytes=4096, fold=fold & 1,
+                                                     **opts).schedule_bytes
+    ops, nch = oracle_program(kind, R, G)
+    nin, nout = nch[0] * ce, nch[1] * ce
+    ins = datagen.rank_inputs(79 + kind, DIST[dtype], R, nin, dtype)
+    d_out = empty_outputs(R, nout, dtype)
+    plan.execute(to_device(ins, dtype), d_out)
+    torch.cuda.synchronize()
+    plan.status()
+    want, _, _ = oracle.run(ops, R, nch, ce, dtype, ins)
+    assert_bitexact(to_host(d_out, dtype), want)
+    if kind == 0:
+        d = to_device(ins, dtype)
+        plan.execute(d, d)
+        torch.cuda.synchronize()
+        plan.status()
+        assert_bitexact(to_host(d, dtype), want)
+
+
 SPECIALS = {0: [np.inf, -np.inf, np.nan, 3.0e38], 1: [0x7F80, 0xFF80, 0x7FC0, 0x7F7F], 2: [0x7C00, 0xFC00, 0x7E00, 0x7BFF]}
 
 

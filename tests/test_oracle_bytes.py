@@ -86,6 +86,57 @@ def test_alltonext_closed_forms():
     assert OB.schedule_bytes(ops, 24, nch, 1000, F32, "none", direct=True) == (21 * 8 * 2 + 2 * (2 * 4 + 6 * 6)) * n
 
 
+@pytest.mark.parametrize("R", [2, 3, 4, 7, 8])
+def test_copy_chain_folds_closed_forms(R):
+    """Direct transport with copy chains folded (fold bit 1): a copy that
+    sends on exactly what another direct copy delivered is written by that
+    copy's pass, one read written twice (3) instead of 2 + 2; a chain of k
+    hops from its head becomes floor(k/2) such pairs and, for odd k, one
+    plain copy.  Ring AllGather, copy receives unchained: the copy-send 3
+    (its receive folded by bit 0, else a FIFO receive 2 more), then a chain
+    of R - 2 copies.  Ring AllReduce likewise: reduce-scatter 3R (send 2,
+    R - 2 rrs 3, rrcs 4; its receive folded by bit 0, else 2 more) and a
+    chain of R - 2 all-gather copies."""
+    chain = 3 * ((R - 2) // 2) + 2 * ((R - 2) % 2)
+    n = 100 * 2
+    ops, nch = OS.ring_allgather(R)
+    for fold, first in ((2, 3 + 2), (3, 3)):
+        assert OB.schedule_bytes(ops, R, nch, 100, BF16, "nochain", True, fold) == R * (first + chain) * n
+    ops, nch = OS.ring_allreduce(R)
+    for fold, rs in ((2, 3 * R + 2), (3, 3 * R)):
+        assert OB.schedule_bytes(ops, R, nch, 100, BF16, "nochain", True, fold) == R * (rs + chain) * n
+
+
+def test_copy_chain_folds_of_the_hierarchical_allreduce_and_alltonext():
+    """Hierarchical AllReduce (G = 8, 2 groups, copy receives unchained,
+    direct): intra reduce-scatter 46 n as above, the inter-group step send 2
+    + rrcs 4 + its receive 2 (folded by bit 0: 6), the intra all-gather of
+    2-chunk slices 7 copies of 4 n -- with chains folded three pairs of 6 n
+    and one copy of 4 n, 22 n.  AllToNext unfused, direct: a part relayed
+    once costs 3 instead of 4, one relayed twice 3 + 2 instead of 6."""
+    ops, nch = OS.hier_allreduce(8, 2)
+    n = 64 * 4
+    for fold, per_rank in ((0, 46 + 8 + 28), (1, 46 + 6 + 28), (2, 46 + 8 + 22), (3, 46 + 6 + 22)):
+        assert OB.schedule_bytes(ops, 16, nch, 64, F32, "nochain", True, fold) == 16 * per_rank * n
+    ops, nch = OS.alltonext(8, 3)
+    n = 1000 * 4
+    assert OB.schedule_bytes(ops, 24, nch, 1000, F32, "none", True, 2) == (21 * 8 * 2 + 2 * (2 * 3 + 6 * 5)) * n
+
+
+def test_planted_mistake_in_the_chain_fold_is_caught():
+    """Folding a copy chain without the head rule (every hop into its
+    predecessor, so the 7-hop all-gather of the ring AllGather at R = 8
+    would count 3 + 6 * 1 extra writes instead of pairs) breaks the pin."""
+    ops, nch = OS.ring_allgather(8)
+    good = OB.schedule_bytes(ops, 8, nch, 10, F32, "nochain", True, 3)
+    saved = OB._chain_folds
+    try:
+        OB._chain_folds = lambda halves: 2 * saved(halves)
+        assert OB.schedule_bytes(ops, 8, nch, 10, F32, "nochain", True, 3) != good
+    finally:
+        OB._chain_folds = saved
+
+
 def test_min_bytes_closed_forms():
     """Every input chunk a program reads, read once, and every output chunk
     it writes, written once: AllReduce R (R + R) chunks, AllGather R (1 +
@@ -129,6 +180,7 @@ def test_oracle_count_equals_the_product_count_for_every_benchmark_row():
     class A:
         only, scale = "", 1.0
     assert bench.DEFAULT_LINK_MODE == ccl.default_opts().link_mode
+    assert bench.DEFAULT_FOLD == ccl.default_opts().fold
     for name, kind, R, G, dt, cb, dist, seed, opts in bench.selected_suite(A):
         sched, popts = bench.schedule_and_opts(ccl, kind, R, G, opts)
         ce = cb // bench.ESIZE[dt]
@@ -138,18 +190,18 @@ def test_oracle_count_equals_the_product_count_for_every_benchmark_row():
         fl = {"nochain": ccl.FLAG_NOCHAIN_COPIES, False: ccl.FLAG_NOFUSE}.get(opts.get("fuse", True), 0)
         ops, nch = KIND_PROGRAM[kind](R, G)
         direct = popts.get("link_mode", ccl.default_opts().link_mode) == ccl.LINK_DIRECT
-        fold = bool(popts.get("fold", 1))
+        fold = int(popts.get("fold", ccl.default_opts().fold))
         assert OB.schedule_bytes(ops, R, nch, ce, dt, _fuse_name(fl), direct, fold) == st.schedule_bytes, name
 
 
 @pytest.mark.parametrize("kind,R,G", [(0, 8, 0), (0, 3, 0), (1, 8, 0), (2, 5, 0), (3, 16, 8), (3, 4, 2),
                                       (4, 32, 8), (4, 8, 4), (5, 24, 8), (5, 6, 3)])
 @pytest.mark.parametrize("flags", [0, 2, 4])
-@pytest.mark.parametrize("link_mode,fold", [(0, 1), (1, 1), (1, 0)])
+@pytest.mark.parametrize("link_mode,fold", [(0, 1), (1, 1), (1, 0), (1, 2), (1, 3)])
 def test_oracle_count_equals_the_product_count_for_builtins(kind, R, G, flags, link_mode, fold):
     ops, nch = KIND_PROGRAM[kind](R, G)
     st = ccl.Schedule.builtin(kind, R, G, flags).check(333, F32, link_mode=link_mode, fold=fold)
-    assert OB.schedule_bytes(ops, R, nch, 333, F32, _fuse_name(flags), link_mode == 1, bool(fold)) == \
+    assert OB.schedule_bytes(ops, R, nch, 333, F32, _fuse_name(flags), link_mode == 1, fold) == \
         st.schedule_bytes
 
 
