@@ -532,10 +532,19 @@ def host_link(torch, items, stream):
 
 # The message-size sweep: ring AllGather and ReduceScatter, 8 ranks, bf16,
 # per-rank buffer (AllGather output, ReduceScatter input) 32 KiB .. 2 MiB and
-# 3 MiB, channels 1..4, normal(0,1) seed 1.  The small ring AllReduce's int32
+# 3 MiB, channels 1..4, normal(0,1) seed 1, each size planned from the
+# collective's tuned table.  The small ring AllReduce's int32
 # copy: 8 x 1 MiB, integers in [-1000, 1000], seed 0.
 SWEEP_KIB = [32, 64, 128, 256, 512, 1024, 2048, 3072]
 TABLE_DIR = os.path.join(ROOT, "collective_communication_schedule_gb300", "tables")
+# the AllGather runs with its copy receives unchained (each hop a direct
+# copy, chains folded two hops per step, as the suite's 3 MiB row); the
+# ReduceScatter has no copy hops and runs fully fused
+SWEEP_NOCHAIN = {1: True, 2: False}
+
+
+def sweep_schedule(ccl, kind, R):
+    return ccl.Schedule.builtin(kind, R, 0, ccl.FLAG_NOCHAIN_COPIES if SWEEP_NOCHAIN[kind] else 0)
 
 
 def tuned_table(ccl, torch, datagen, kind, args):
@@ -549,7 +558,7 @@ def tuned_table(ccl, torch, datagen, kind, args):
         return rows, os.path.relpath(path, ROOT)
     R = 8
     sizes = [kib * 1024 // 2 // R for kib in SWEEP_KIB]
-    s = ccl.Schedule.builtin(kind, R)
+    s = sweep_schedule(ccl, kind, R)
     nin = max(sizes) * (1 if kind == 1 else R)
     ins = [torch.from_numpy(a.view("int16")).cuda() for a in datagen.rank_inputs(1, "normal", R, nin, 1)]
     outs = [torch.empty(max(sizes) * (R if kind == 1 else 1), dtype=torch.int16, device="cuda") for _ in range(R)]
@@ -557,8 +566,9 @@ def tuned_table(ccl, torch, datagen, kind, args):
     out_dir = args.table_out
     if out_dir:
         os.makedirs(out_dir, exist_ok=True)
+        unchained = ", copy receives unchained" if SWEEP_NOCHAIN[kind] else ""
         ccl.write_tune_table(rows, 1, os.path.join(out_dir, os.path.basename(path)),
-                             note=f"{name} R=8 bf16, channels <= 4, tuned on {torch.cuda.get_device_name()}")
+                             note=f"{name} R=8 bf16{unchained}, channels <= 4, tuned on {torch.cuda.get_device_name()}")
     return rows, "tuned in this run"
 
 
@@ -613,7 +623,7 @@ def run_sweep(ccl, torch, datagen, args, peak):
     for kind, kname in ((1, "allgather"), (2, "reducescatter")):
         rows, src = tuned_table(ccl, torch, datagen, kind, args)
         out[f"{kname}_table"] = src
-        sched = ccl.Schedule.builtin(kind, R)
+        sched = sweep_schedule(ccl, kind, R)
         for kib in SWEEP_KIB:
             ce = kib * 1024 // 2 // R
             nin = ce * (1 if kind == 1 else R)

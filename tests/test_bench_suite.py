@@ -83,3 +83,24 @@ def test_hier_allgather_benchmark_plans_fit():
             assert folded.nthreadblocks <= 2 * 152
             assert folded.schedule_bytes < st.schedule_bytes
             assert folded.schedule_bytes == OB.schedule_bytes(prog, R, nch, ce, 1, "none", True, 3)
+
+
+@pytest.mark.parametrize("kind", [1, 2])
+def test_committed_sweep_tables_plan_on_their_schedules(kind):
+    """Every row of a committed tuning table plans, at its size and at
+    channels 1-4, on the schedule the sweep runs it with (the AllGather's
+    copy receives unchained), and the tables cover every sweep size."""
+    import os
+    name = {1: "ring_allgather", 2: "ring_reducescatter"}[kind]
+    rows, dt = ccl.read_tune_table(os.path.join(bench.TABLE_DIR, f"{name}_r8_bf16.json"))
+    R = 8
+    sizes = [kib * 1024 // 2 // R for kib in bench.SWEEP_KIB]
+    assert sorted(r.chunk_elems for r in rows) == sizes and dt == 1
+    s = bench.sweep_schedule(ccl, kind, R)
+    for ce in sizes:
+        base = ccl.lookup_tune_table(rows, ce)
+        for ch in (1, 2, 3, 4):
+            o = ccl.PlanOpts.from_buffer_copy(base)
+            o.channels = ch
+            st = s.check(ce, 1, opts=o)
+            assert st.nthreadblocks <= 2 * 152

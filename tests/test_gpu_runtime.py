@@ -43,12 +43,13 @@ def test_lost_counter_times_out_and_device_stays_usable(ccl, engine):
     threadblock of link-free copies that posts none of its counters makes its
     dependents give up after 50 ms (on the sequential engine the wait for a
     single counter is a loop of acquire loads); the GPU then runs a fresh
-    plan."""
+    plan.  Copy chains stay unfolded, so that the first all-gather copy has
+    a dependent (the copy that forwards its chunk)."""
     import torch
     import datagen
     s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, 4, 0, ccl.FLAG_NOCHAIN_COPIES)
     plan = ccl.Plan(s, 1024, F32, timeout_ms=50, link_mode=ccl.LINK_DIRECT, tb_alloc=ccl.TB_CONNECTION,
-                    engine=engine)
+                    engine=engine, fold=1)
     steps = plan.steps()
     by_tb = {}
     for k, st in enumerate(steps):
