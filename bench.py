@@ -50,7 +50,7 @@ SUITE = [
      # folded); the inter-group step keeps its FIFO hop (folding its
      # receive into the sender, as the rings do, measured 5 % slower here)
      dict(fuse="nochain", link_mode=1, channels=9, microbatches=16, tb_alloc=1, slot_bytes=65536, fifo_slots=8,
-          mb_window=4, fold=2)),
+          mb_window=4, fold=2, nthreads=384)),
     ("a2a", 4, 32, 8, 2, 1 * MiB, "uniform", 3,
      dict(channels=8, link_mode=1, channel_scaling=0, tb_alloc=2, tb_budget=256)),
     ("ring_bf16", 0, 8, 0, 1, 32 * MiB, "normal", 4,
