@@ -47,6 +47,11 @@ int64_t kind_bytes_factor(int kind)
     case CCL_I_COPY_SEND: return 3;
     case CCL_I_COPY2: return 3;
     case CCL_I_RRC2: return 4;
+    case CCL_I_RRS3: return 4;
+    case CCL_I_RRC3: return 4;
+    case CCL_I_RRCS3: return 5;
+    case CCL_I_RSEND: return 3;
+    case CCL_I_RCSEND: return 4;
     default: return 0;
     }
 }

@@ -240,6 +240,126 @@ __device__ __forceinline__ void move_part(bool red, const char* a, bool as, cons
     else move<false, DT, U>(a, as, b, bs, o1, o1s, o2, n, tid, T);
 }
 
+// Three operands (a step that also takes the next step of a reduction chain:
+// its local operand c is added after a + b, each sum rounded to the element
+// type, as the two steps would).  Three quarters of the two-operand path's
+// vectors in flight per operand (the registers of three operands).
+template <int DT, int U>
+__device__ __forceinline__ void move_vec3(const uint4* a, bool as, const uint4* b, bool bs, const uint4* c, bool cs,
+                                          uint4* o1, bool o1s, uint4* o2, long long nv, int tid, int T)
+{
+    long long i = tid;
+    const long long full = nv - (long long)(U - 1) * T;
+    for (; i < full; i += (long long)U * T) {
+        uint4 va[U], vb[U], vc[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            va[u] = vload(a + i + u * T, as);
+            vb[u] = vload(b + i + u * T, bs);
+            vc[u] = vload(c + i + u * T, cs);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint4 r = vadd<DT>(vadd<DT>(va[u], vb[u]), vc[u]);
+            vstore(o1 + i + u * T, r, o1s);
+            if (o2) vstore(o2 + i + u * T, r, false);
+        }
+    }
+    if (i < nv) {
+        uint4 va[U - 1], vb[U - 1], vc[U - 1];
+#pragma unroll
+        for (int u = 0; u < U - 1; ++u) {
+            const long long j = i + u * T < nv ? i + u * T : nv - 1;
+            va[u] = vload(a + j, as);
+            vb[u] = vload(b + j, bs);
+            vc[u] = vload(c + j, cs);
+        }
+#pragma unroll
+        for (int u = 0; u < U - 1; ++u)
+            if (i + u * T < nv) {
+                const uint4 r = vadd<DT>(vadd<DT>(va[u], vb[u]), vc[u]);
+                vstore(o1 + i + u * T, r, o1s);
+                if (o2) vstore(o2 + i + u * T, r, false);
+            }
+    }
+}
+
+template <int DT>
+static __device__ void move_elem3(const char* a, const char* b, const char* c, char* o1, char* o2, long long lo,
+                                  long long hi, int tid, int T)
+{
+    constexpr int ES = (DT == CCL_BF16 || DT == CCL_F16) ? 2 : 4;
+    for (long long i = lo + tid; i < hi; i += T) {
+        if (ES == 4) {
+            unsigned x = __ldcg(reinterpret_cast<const unsigned int*>(a) + i);
+            x = add2<DT>(x, __ldcg(reinterpret_cast<const unsigned int*>(b) + i));
+            x = add2<DT>(x, __ldcg(reinterpret_cast<const unsigned int*>(c) + i));
+            if (o1) __stcg(reinterpret_cast<unsigned int*>(o1) + i, x);
+            if (o2) __stcg(reinterpret_cast<unsigned int*>(o2) + i, x);
+        } else {
+            unsigned x = __ldcg(reinterpret_cast<const unsigned short*>(a) + i);
+            x = add2<DT>(x, __ldcg(reinterpret_cast<const unsigned short*>(b) + i)) & 0xffffu;
+            x = add2<DT>(x, __ldcg(reinterpret_cast<const unsigned short*>(c) + i)) & 0xffffu;
+            if (o1) __stcg(reinterpret_cast<unsigned short*>(o1) + i, (unsigned short)x);
+            if (o2) __stcg(reinterpret_cast<unsigned short*>(o2) + i, (unsigned short)x);
+        }
+    }
+}
+
+// o1 (and o2) <- (a + b) + c over n elements, shared by threads [0, T)
+template <int DT, int U>
+__device__ CCL_MOVE_ATTR void move3(const char* a, bool as, const char* b, bool bs, const char* c, bool cs, char* o1,
+                                    bool o1s, char* o2, long long n, int tid, int T)
+{
+    constexpr int ES = (DT == CCL_BF16 || DT == CCL_F16) ? 2 : 4;
+    constexpr int VE = 16 / ES;
+    constexpr int U3 = U >= 8 ? 6 : 2;
+    const unsigned long long al = (unsigned long long)a | (unsigned long long)b | (unsigned long long)c |
+                                  (unsigned long long)o1 | (unsigned long long)o2;
+    long long nv = 0;
+    if ((al & 15) == 0) {
+        nv = n / VE;
+        move_vec3<DT, U3>(reinterpret_cast<const uint4*>(a), as, reinterpret_cast<const uint4*>(b), bs,
+                          reinterpret_cast<const uint4*>(c), cs, reinterpret_cast<uint4*>(o1), o1s,
+                          reinterpret_cast<uint4*>(o2), nv, tid, T);
+    }
+    if (nv * VE < n) move_elem3<DT>(a, b, c, o1, o2, nv * VE, n, tid, T);
+}
+
+// the dtype dispatch of move3 (inlined into the sequential engine's step;
+// the pipelined engine's data warps call it out of line, move_part3_call,
+// which keeps their two-operand path's registers as they were)
+template <int U>
+__device__ __forceinline__ void move_part3(int dtype, const char* a, bool as, const char* b, bool bs, const char* c,
+                                           bool cs, char* o1, bool o1s, char* o2, long long n, int tid, int T)
+{
+    switch (dtype) {
+    case CCL_F32: move3<CCL_F32, U>(a, as, b, bs, c, cs, o1, o1s, o2, n, tid, T); break;
+    case CCL_BF16: move3<CCL_BF16, U>(a, as, b, bs, c, cs, o1, o1s, o2, n, tid, T); break;
+    case CCL_F16: move3<CCL_F16, U>(a, as, b, bs, c, cs, o1, o1s, o2, n, tid, T); break;
+    default: move3<CCL_I32, U>(a, as, b, bs, c, cs, o1, o1s, o2, n, tid, T); break;
+    }
+}
+
+template <int U>
+__device__ __noinline__ void move_part3_call(int dtype, const char* a, bool as, const char* b, bool bs, const char* c,
+                                             bool cs, char* o1, bool o1s, char* o2, long long n, int tid, int T)
+{
+    move_part3<U>(dtype, a, as, b, bs, c, cs, o1, o1s, o2, n, tid, T);
+}
+
+// kinds that reduce, and those that take a third operand (held in the
+// source range)
+__device__ __forceinline__ bool kind_reduces(int k)
+{
+    return k == CCL_I_REDUCE || k == CCL_I_RRC || k == CCL_I_RRS || k == CCL_I_RRCS || k == CCL_I_RRC2 ||
+           k == CCL_I_RRS3 || k == CCL_I_RRC3 || k == CCL_I_RRCS3 || k == CCL_I_RSEND || k == CCL_I_RCSEND;
+}
+__device__ __forceinline__ bool kind_three(int k)
+{
+    return k == CCL_I_RRS3 || k == CCL_I_RRC3 || k == CCL_I_RRCS3;
+}
+
 // the whole CTA moves the data
 template <int DT>
 __device__ __forceinline__ void move_dt(bool red, const char* a, bool as, const char* b, bool bs, char* o1,
@@ -429,11 +549,12 @@ static_assert(kHist > kQ, "history must reach past the descriptor ring");
 struct SlotOp {
     const char* a;      // data in: incoming slot or source buffer
     const char* b;      // local operand of a reduce
+    const char* c;      // third operand (a folded reduction chain), or null
     char* o1;           // destination buffer, or the outgoing slot
     char* o2;           // outgoing slot when a destination is also written
     long long n;        // elements
     int red, dtype;
-    int as, bs, o1s;    // streaming cache hints (register path)
+    int as, bs, cs, o1s;   // streaming cache hints (register path)
     int bulk;           // moved by the TMA thread
     int cmd;            // 0 move, 1 end, 2 abort
     int a_ll, o1_ll, o2_ll;   // operand is an LL slot
@@ -830,8 +951,8 @@ __device__ __forceinline__ bool issue_step(const KParams& P, CtlShared* sh, cons
     unsigned in_idx = Lin ? slot_index(exec_mod, *Lin, st.seq_in_mod, S) : 0;
     unsigned out_idx = Lout ? slot_index(exec_mod, *Lout, st.seq_out_mod, S) : 0;
     const long long span = linked ? slot_elems : tile_elems;
-    const int red = st.kind == CCL_I_REDUCE || st.kind == CCL_I_RRC || st.kind == CCL_I_RRS || st.kind == CCL_I_RRCS ||
-                    st.kind == CCL_I_RRC2;
+    const int red = kind_reduces(st.kind);
+    const bool three = kind_three(st.kind);
     const char* srcb = st.src_buf >= 0 ? P.bufs[st.src_buf][st.src_rank] + st.src_off * es : nullptr;
     const char* locb = st.loc_buf >= 0 ? P.bufs[st.loc_buf][st.loc_rank] + st.loc_off * es : nullptr;
     char* dstb = st.dst_buf >= 0 ? P.bufs[st.dst_buf][st.dst_rank] + st.dst_off * es : nullptr;
@@ -886,6 +1007,9 @@ __device__ __forceinline__ bool issue_step(const KParams& P, CtlShared* sh, cons
             const bool copy2 = st.kind == CCL_I_COPY2, rrc2 = st.kind == CCL_I_RRC2;
             op.b = locb && !copy2 ? locb + off : nullptr;
             op.bs = (st.flags & STEP_LOC_STREAM) && P.stream_in;
+            // a folded reduction chain's third operand: its source range
+            op.c = three && srcb ? srcb + off : nullptr;
+            op.cs = (st.flags & STEP_SRC_STREAM) && P.stream_in;
             if (dstb) {
                 op.o1 = dstb + off;
                 op.o1s = st.dst_buf == CCL_BUF_OUT;
@@ -1361,6 +1485,8 @@ static __device__ void data_warps(const KParams& P, CtlShared* sh)
                 }
                 if (!ok) record_timeout(P, -1, WAIT_FULL);
             }
+        } else if (!op.bulk && op.n > 0 && op.c) {
+            move_part3_call<U>(op.dtype, op.a, op.as, op.b, op.bs, op.c, op.cs, op.o1, op.o1s, op.o2, op.n, tid, T);
         } else if (!op.bulk && op.n > 0) {
             switch (op.dtype) {
             case CCL_F32: move_part<CCL_F32, U>(op.red, op.a, op.as, op.b, op.bs, op.o1, op.o1s, op.o2, op.n, tid, T); break;
@@ -1487,8 +1613,8 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
     if (!linked && st.nelem > 0) nslots = (st.nelem + slot_elems - 1) / slot_elems;
     unsigned in_idx = Lin ? slot_index(exec_mod, *Lin, st.seq_in_mod, S) : 0;
     unsigned out_idx = Lout ? slot_index(exec_mod, *Lout, st.seq_out_mod, S) : 0;
-    const int red = st.kind == CCL_I_REDUCE || st.kind == CCL_I_RRC || st.kind == CCL_I_RRS || st.kind == CCL_I_RRCS ||
-                    st.kind == CCL_I_RRC2;
+    const int red = kind_reduces(st.kind);
+    const bool three = kind_three(st.kind);
     const char* srcb = st.src_buf >= 0 ? P.bufs[st.src_buf][st.src_rank] + st.src_off * es : nullptr;
     const char* locb = st.loc_buf >= 0 ? P.bufs[st.loc_buf][st.loc_rank] + st.loc_off * es : nullptr;
     char* dstb = st.dst_buf >= 0 ? P.bufs[st.dst_buf][st.dst_rank] + st.dst_off * es : nullptr;
@@ -1520,6 +1646,8 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
         if (n > 0) {
             prefetch_l2(a, n * es, tid, T);
             prefetch_l2(b, n * es, tid, T);
+            // a folded reduction chain's third operand: its source range
+            if (three) prefetch_l2(srcb + e0 * es, n * es, tid, T);
         }
         if (linked || k == 0) {
             if (tid == 0) {
@@ -1560,6 +1688,8 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
                 SlotOp op;
                 op.a = a;
                 op.b = b;
+                op.c = nullptr;   // no folded reduction chains with LL slots
+                op.cs = 0;
                 op.o1 = o1;
                 op.o2 = o2;
                 op.n = n;
@@ -1578,6 +1708,9 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
                 // after a recorded failure the part is skipped; the leader
                 // sees the status before its next wait
                 if (*(volatile int*)P.status == 0 && !seq_move_ll(op, tid, T, P)) record_timeout(P, si, WAIT_FULL);
+            } else if (three) {
+                move_part3<U>(st.dtype, a, as, b, bs, srcb + e0 * es, (st.flags & STEP_SRC_STREAM) && P.stream_in, o1,
+                              o1s, o2, n, tid, T);
             } else {
                 switch (st.dtype) {
                 case CCL_F32: move_part<CCL_F32, U>(red, a, as, b, bs, o1, o1s, o2, n, tid, T); break;

@@ -262,7 +262,8 @@ void allocate_connection(const ccl_schedule& s, const Timeline& tl, TBList* tbs,
             int out = I.xfer_out >= 0 ? s.xfers[I.xfer_out].dst_rank : -1;
             // a copy into another rank's buffer (direct transport) is a
             // connection of its own to that rank
-            if (I.kind == CCL_I_COPY && I.dst.valid() && I.dst.rank != I.rank) out = CCL_MAX_RANKS + I.dst.rank;
+            if ((I.kind == CCL_I_COPY || I.kind == CCL_I_REDUCE) && I.dst.valid() && I.dst.rank != I.rank)
+                out = CCL_MAX_RANKS + I.dst.rank;
             // (a two-destination copy: its first remote destination)
             if (I.kind == CCL_I_COPY2) {
                 if (I.dst.valid() && I.dst.rank != I.rank) out = CCL_MAX_RANKS + I.dst.rank;
@@ -1120,6 +1121,140 @@ int fold_copy_chains(ccl_schedule& d)
     return nfold;
 }
 
+// Reduction chains (after direct transport): a send or recv-reduce-send X
+// whose slot feeds a receive-reduce Y (recv-reduce-send, -copy, or
+// -copy-send) is run as one step by X's threadblock, which reads Y's local
+// operand itself and adds it after X's sum (the chain's order, each sum
+// rounded to the element type): send + rrs -> CCL_I_RSEND, send + rrc ->
+// CCL_I_REDUCE, send + rrcs -> CCL_I_RCSEND, rrs + rrs / rrc / rrcs ->
+// CCL_I_RRS3 / RRC3 / RRCS3 (Y's local operand held in the source range).
+// The slot between them goes (2 bytes per element byte) and so does a hop;
+// the folded step sends on where Y sent (a link two ranks ahead in a
+// ring).  Pairs form in dependency order from each chain's head; a pair
+// whose merged dependencies would close a cycle is left alone.
+int fold_reduce_chains(ccl_schedule& d)
+{
+    const int ni = (int)d.instrs.size();
+    std::vector<std::set<int>> succ(ni), pred(ni);
+    std::map<std::pair<int, int>, int> exact;   // dependency edges: bit 0 exact, bit 1 not
+    auto add_dep = [&](int a, int b, int bits) {
+        if (a == b || !bits) return;
+        succ[a].insert(b);
+        pred[b].insert(a);
+        exact[{a, b}] |= bits;
+    };
+    for (const Dep& e : d.deps) add_dep(e.from, e.to, e.exact ? 1 : 2);
+    auto add_xfer_edge = [&](int a, int b) {
+        if (a < 0 || b < 0) return;
+        succ[a].insert(b);
+        pred[b].insert(a);
+    };
+    for (const Xfer& X : d.xfers) add_xfer_edge(X.send_instr, X.recv_instr);
+    std::vector<int> indeg(ni), order;
+    std::set<int> ready;
+    for (int i = 0; i < ni; ++i)
+        if ((indeg[i] = (int)pred[i].size()) == 0) ready.insert(i);
+    while (!ready.empty()) {
+        const int i = *ready.begin();
+        ready.erase(ready.begin());
+        order.push_back(i);
+        for (int j : succ[i])
+            if (--indeg[j] == 0) ready.insert(j);
+    }
+    if ((int)order.size() != ni) return 0;
+    std::vector<char> gone(ni, 0), merged(ni, 0), xgone(d.xfers.size(), 0);
+    std::vector<int> mark(ni, -1);
+    int nfold = 0, epoch = 0;
+    for (int c1 : order) {
+        if (gone[c1] || merged[c1]) continue;
+        const Instr& X = d.instrs[c1];
+        if ((X.kind != CCL_I_SEND && X.kind != CCL_I_RRS) || X.xfer_out < 0) continue;
+        const int x = X.xfer_out;
+        const int c2 = d.xfers[x].recv_instr;
+        if (c2 < 0 || gone[c2] || merged[c2]) continue;
+        const Instr& Y = d.instrs[c2];
+        if (Y.kind != CCL_I_RRS && Y.kind != CCL_I_RRC && Y.kind != CCL_I_RRCS) continue;
+        if (Y.count != X.count || !Y.loc.valid() || (X.kind == CCL_I_SEND && !X.src.valid())) continue;
+        // everything else Y waits for must be able to come before X
+        std::vector<int> stack{c1};
+        bool cycle = false;
+        mark[c1] = ++epoch;
+        while (!stack.empty() && !cycle) {
+            const int v = stack.back();
+            stack.pop_back();
+            for (int w : succ[v]) {
+                if (w == c2 || mark[w] == epoch) continue;
+                if (pred[c2].count(w)) { cycle = true; break; }
+                mark[w] = epoch;
+                stack.push_back(w);
+            }
+        }
+        if (cycle) continue;
+        Instr F = X;
+        if (X.kind == CCL_I_SEND) {
+            F.loc = Y.loc;
+            F.kind = Y.kind == CCL_I_RRS ? CCL_I_RSEND : Y.kind == CCL_I_RRC ? CCL_I_REDUCE : CCL_I_RCSEND;
+        } else {
+            F.src = Y.loc;
+            F.kind = Y.kind == CCL_I_RRS ? CCL_I_RRS3 : Y.kind == CCL_I_RRC ? CCL_I_RRC3 : CCL_I_RRCS3;
+        }
+        F.dst = Y.dst;
+        F.xfer_out = Y.xfer_out;
+        if (F.xfer_out >= 0) {
+            d.xfers[F.xfer_out].send_instr = c1;
+            d.xfers[F.xfer_out].src_rank = X.rank;
+        }
+        xgone[x] = 1;
+        d.instrs[c1] = F;
+        // c1 takes over c2's edges
+        for (int w : std::vector<int>(pred[c2].begin(), pred[c2].end())) {
+            auto it = exact.find({w, c2});
+            const int bits = it == exact.end() ? 0 : it->second;
+            succ[w].erase(c2);
+            if (w != c1) add_dep(w, c1, bits);
+        }
+        for (int y : std::vector<int>(succ[c2].begin(), succ[c2].end())) {
+            auto it = exact.find({c2, y});
+            pred[y].erase(c2);
+            if (it == exact.end()) add_xfer_edge(c1, y);   // the transfer c2 sent
+            else add_dep(c1, y, it->second);
+        }
+        pred[c2].clear();
+        succ[c2].clear();
+        gone[c2] = 1;
+        merged[c1] = 1;
+        ++nfold;
+    }
+    if (!nfold) return 0;
+    std::vector<int> inew(ni, -1);
+    std::vector<Instr> instrs;
+    for (int i = 0; i < ni; ++i)
+        if (!gone[i]) { inew[i] = (int)instrs.size(); instrs.push_back(d.instrs[i]); }
+    std::vector<int> xnew(d.xfers.size(), -1);
+    std::vector<Xfer> xfers;
+    for (size_t x = 0; x < d.xfers.size(); ++x)
+        if (!xgone[x]) { xnew[x] = (int)xfers.size(); xfers.push_back(d.xfers[x]); }
+    for (auto& I : instrs) {
+        if (I.xfer_in >= 0) I.xfer_in = xnew[I.xfer_in];
+        if (I.xfer_out >= 0) I.xfer_out = xnew[I.xfer_out];
+    }
+    for (auto& X : xfers) {
+        X.send_instr = inew[X.send_instr];
+        X.recv_instr = inew[X.recv_instr];
+    }
+    std::vector<Dep> deps;
+    for (const auto& kv : exact) {
+        const int a = kv.first.first, b = kv.first.second;
+        if (gone[a] || gone[b] || !succ[a].count(b)) continue;
+        if (kv.second & 1) deps.push_back(Dep{inew[a], inew[b], true});
+        if (kv.second & 2) deps.push_back(Dep{inew[a], inew[b], false});
+    }
+    d.instrs = std::move(instrs);
+    d.xfers = std::move(xfers);
+    d.deps = std::move(deps);
+    return nfold;
+}
+
 namespace {
 
 ccl_status_t build_plan_one(const ccl_schedule& s_in, int64_t ce, int32_t dtype, const ccl_plan_opts_t& o,
@@ -1154,13 +1289,20 @@ ccl_status_t build_plan_one(const ccl_schedule& s_in, int64_t ce, int32_t dtype,
     if (o.protocol == CCL_PROTO_LL && (ce * esize_of(dtype)) % 16)
         return fail(CCL_ERR_UNSUPPORTED, "the LL protocol needs chunks of a multiple of 16 bytes");
     if (o.timeout_ms <= 0) return fail(CCL_ERR_INVALID_ARG, "timeout_ms must be positive");
-    if (o.fold < 0 || o.fold > 3) return fail(CCL_ERR_INVALID_ARG, "fold must be in 0..3");
+    if (o.fold < 0 || o.fold > 7) return fail(CCL_ERR_INVALID_ARG, "fold must be in 0..7");
 
     if (o.link_mode != CCL_LINK_FIFO && o.link_mode != CCL_LINK_DIRECT)
         return fail(CCL_ERR_INVALID_ARG, "unknown link_mode");
     int ndirect = 0;
-    ccl_schedule s = o.link_mode == CCL_LINK_DIRECT ? direct_transport(s_in, &ndirect, (fold & 1) != 0) : s_in;
-    if (o.link_mode == CCL_LINK_DIRECT && (fold & 2)) fold_copy_chains(s);
+    ccl_schedule s = s_in;
+    if (o.link_mode == CCL_LINK_DIRECT) {
+        // reduction chains first (a recv-reduce-copy-send taken into a pair
+        // keeps its receive on a FIFO; the LL slots' path takes no third
+        // operand), then plain transfers and receive folds, then copy chains
+        if ((fold & 4) && o.protocol != CCL_PROTO_LL) fold_reduce_chains(s);
+        s = direct_transport(s, &ndirect, (fold & 1) != 0);
+        if (fold & 2) fold_copy_chains(s);
+    }
     const int es = esize_of(dtype);
     Timeline tl;
     ccl_status_t st = build_timeline(s, o.scheduler, &tl);

@@ -125,8 +125,19 @@ typedef enum {
        and the plain receive it feeds (or the copy that forwards it): */
     CCL_I_COPY2 = 10,    /* two-destination copy: dst <- src; loc <- src (a copy-send and its receive, or a
                             chain of two direct copies; loc: the second destination) */
-    CCL_I_RRC2 = 11      /* recv-reduce-copy-send + receive: t <- local (+) slot_in; dst <- t; src <- t
+    CCL_I_RRC2 = 11,     /* recv-reduce-copy-send + receive: t <- local (+) slot_in; dst <- t; src <- t
                             (src: the receiver's destination) */
+    /* plans only, made by direct transport from two consecutive steps of a
+       reduction chain (a send or recv-reduce-send and the receive-reduce
+       that its slot feeds), run by the first one's threadblock, which reads
+       the second one's local operand itself; the sums keep the chain's
+       order, each rounded to the element type: */
+    CCL_I_RRS3 = 12,     /* slot_out <- (slot_in (+) local) (+) src  (src: the second step's local) */
+    CCL_I_RRC3 = 13,     /* dst <- (slot_in (+) local) (+) src */
+    CCL_I_RRCS3 = 14,    /* t <- (slot_in (+) local) (+) src; dst <- t; slot_out <- t */
+    CCL_I_RSEND = 15,    /* slot_out <- src (+) local  (a send and the recv-reduce-send it feeds) */
+    CCL_I_RCSEND = 16    /* t <- src (+) local; dst <- t; slot_out <- t  (a send and a recv-reduce-copy-send);
+                            a send and the recv-reduce-copy it feeds become a CCL_I_REDUCE */
 } ccl_instr_kind_t;
 
 typedef struct {

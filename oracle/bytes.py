@@ -35,8 +35,10 @@ Direct transport (the plan option): a plain send whose transfer ends in a
 plain receive is one copy into the receiver's buffer (2 bytes per element
 byte instead of 2 + 2), and with copy chains folded a copy that sends on
 exactly what another one delivered is written by that one's pass too (3
-instead of 2 + 2).  Channels and micro-batches split ranges without
-changing these totals.
+instead of 2 + 2); with reduction chains folded, two consecutive steps of a
+reduction chain are one step that reads the second rank's local operand
+itself (the slot between them, 2, goes).  Channels and micro-batches split
+ranges without changing these totals.
 """
 from __future__ import annotations
 
@@ -231,6 +233,35 @@ def _chain_folds(halves):
     return saved
 
 
+def _reduce_chain_folds(halves):
+    """Element chunks saved by folding reduction chains under direct
+    transport, and the receive-reduce halves taken into a pair.
+
+    A send or recv-reduce-send whose transfer ends in a receive-reduce
+    (recv-reduce-send, -copy or -copy-send) becomes one step with it: the
+    first rank's pass reads the second rank's local operand itself and adds
+    it after its own sum, so the slot between them -- written once, read
+    once, 2 per element byte -- goes.  A step that has taken one over takes
+    no other, and one taken over is gone; transfers are visited in program
+    order, so each chain pairs up from its head."""
+    sends = {h.send: h for h in halves if h.send is not None}
+    recvs = {h.recv: h for h in halves if h.recv is not None}
+    taken, merged, saved = set(), set(), 0
+    for t in sorted(sends):
+        x = sends[t]
+        if id(x) in taken or id(x) in merged or x.kind() not in ("send", "rrs"):
+            continue
+        y = recvs.get(t)
+        if y is None or id(y) in taken or id(y) in merged or y.kind() not in ("rrs", "rrc", "rrcs"):
+            continue
+        if y.count != x.count:
+            continue
+        taken.add(id(y))
+        merged.add(id(x))
+        saved += 2 * x.count
+    return saved, taken
+
+
 def schedule_bytes(ops, nranks, nchunks, chunk_elems, dtype, fuse="full", direct=True, fold=1):
     """Bytes one execution reads and writes (buffers and FIFO slots) when
     ``ops`` runs as fused instructions; ``direct``: a plain receive whose
@@ -239,14 +270,22 @@ def schedule_bytes(ops, nranks, nchunks, chunk_elems, dtype, fuse="full", direct
     2 -> one copy of 2; copy-send 3 + receive 2 -> one read written twice,
     3; recv-reduce-copy-send 4 + receive 2 -> 4).  ``fold`` bit 0 (True)
     takes the last two without their FIFO (cleared: they keep it); bit 1
-    also folds copy chains (``_chain_folds``)."""
+    also folds copy chains (``_chain_folds``); bit 2 reduction chains
+    (``_reduce_chain_folds``, first: a recv-reduce-copy-send taken into a
+    pair keeps its receive's FIFO)."""
     halves = _fused_halves(ops, nranks, fuse)
     units = sum(FACTOR[h.kind()] * h.count for h in halves)
     if direct:
-        sender = {h.send: h.kind() for h in halves if h.send is not None}
+        taken = set()
+        if int(fold) & 4:
+            saved, taken = _reduce_chain_folds(halves)
+            units -= saved
+        sender = {h.send: h for h in halves if h.send is not None}
         for h in halves:
-            if h.kind() == "recv" and (sender[h.recv] == "send" or
-                                       (int(fold) & 1 and sender[h.recv] in ("copy_send", "rrcs"))):
+            if h.kind() != "recv":
+                continue
+            s = sender[h.recv]
+            if s.kind() == "send" or (int(fold) & 1 and s.kind() in ("copy_send", "rrcs") and id(s) not in taken):
                 units -= 2 * h.count
         if int(fold) & 2:
             units -= _chain_folds(halves)

@@ -96,8 +96,10 @@ def test_binding_constants_match_the_header():
     # instruction kind names are indexed by the header's CCL_I_* values
     for i, name in enumerate(ccl.KIND_NAMES):
         assert vals["I_" + name.upper()] == i, name
-    # the compiler's kinds, then copy2 and rrc2, which only plans contain
-    assert vals["I_NKINDS"] == len(ccl.KIND_NAMES) - 2 and ccl.KIND_NAMES[-2:] == ["copy2", "rrc2"]
+    # the compiler's kinds, then the kinds only plans contain (direct
+    # transport's folds)
+    plan_only = ["copy2", "rrc2", "rrs3", "rrc3", "rrcs3", "rsend", "rcsend"]
+    assert vals["I_NKINDS"] == len(ccl.KIND_NAMES) - len(plan_only) and ccl.KIND_NAMES[vals["I_NKINDS"]:] == plan_only
 
 
 def test_layout_header_codes_match_the_c_abi():

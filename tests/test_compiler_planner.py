@@ -679,13 +679,13 @@ def test_direct_transport_folds_a_copy_send_and_its_receive():
 
 def test_fold_option():
     """fold = 0 keeps the copy-send's FIFO hop (and its bytes); values
-    outside 0..3 are refused; the library default folds receives."""
+    outside 0..7 are refused; the library default folds receives."""
     assert ccl.default_opts().fold & 1
     R, ce = 8, 1024
     s = ccl.Schedule.builtin(ccl.RING_ALLGATHER, R, 0, ccl.FLAG_NOCHAIN_COPIES)
     kept = s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=0)
     assert kept.nlinks == R and kept.schedule_bytes == R * (3 + 2 + 6 * 2) * ce * 4
-    for bad in (-1, 4):
+    for bad in (-1, 8):
         with pytest.raises(ccl.CclError) as e:
             s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=bad)
         assert e.value.code == 1
@@ -740,6 +740,38 @@ def test_direct_transport_folds_copy_chains():
     # FIFO transport: nothing to fold
     assert s.check(ce, F32, link_mode=ccl.LINK_FIFO, fold=3).schedule_bytes == \
         s.check(ce, F32, link_mode=ccl.LINK_FIFO, fold=0).schedule_bytes
+
+
+def test_direct_transport_folds_reduction_chains():
+    """fold bit 2: the ReduceScatter's 8-hop chains (send, 6 rrs, rrc) become
+    4 steps (send + rrs, rrs + rrs twice, rrs + rrc), run two ranks apart:
+    every threadblock program takes 4 steps instead of 8, links go from a
+    rank to the rank two ahead, and 15 instead of 23 bytes per element byte
+    of a chunk move.  With the LL protocol nothing folds (its slot path
+    takes no third operand); FIFO transport folds nothing either."""
+    R, ce = 8, 1024
+    s = ccl.Schedule.builtin(ccl.RING_REDUCESCATTER, R)
+    plain = s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=3, microbatches=1)
+    folded = s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=7, microbatches=1)
+    assert plain.schedule_bytes == R * 23 * ce * 4 and folded.schedule_bytes == R * 15 * ce * 4
+    assert plain.nsteps == R * 8 and folded.nsteps == R * 4
+    assert folded.nthreadblocks == plain.nthreadblocks == R
+    ll = s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=7, protocol=ccl.PROTO_LL)
+    assert ll.schedule_bytes == plain.schedule_bytes
+    fifo = s.check(ce, F32, link_mode=ccl.LINK_FIFO, fold=7)
+    assert fifo.schedule_bytes == plain.schedule_bytes
+
+
+def test_reduce_chain_fold_keeps_the_ring_allreduce_on_one_threadblock_per_rank():
+    """With every fold on, the ring AllReduce's reduce-scatter pairs run two
+    ranks apart and the step that completes a chunk joins the last pair (its
+    receive keeps the FIFO): still one threadblock per rank and channel."""
+    R = 8
+    s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, R, 0, ccl.FLAG_NOCHAIN_COPIES)
+    for ch in (1, 4):
+        st = s.check(1024, F32, link_mode=ccl.LINK_DIRECT, fold=7, channels=ch, tb_alloc=ccl.TB_BALANCED,
+                     tb_budget=R * ch)
+        assert st.nthreadblocks == R * ch
 
 
 def test_copy_chain_fold_keeps_dependencies():

@@ -41,6 +41,10 @@ CASES = [
     (0, 8, 0, 2053, F32, "nochain", dict(link_mode=1, channels=2, fold=3)),
     (3, 8, 4, 1024, F32, "nochain", dict(link_mode=1, microbatches=4, mb_window=2, tb_alloc=1, fold=3)),
     (5, 6, 3, 640, F32, False, dict(microbatches=2, link_mode=1, fold=2)),
+    # reduction chains folded (third operand, steps two ranks apart)
+    (2, 8, 0, 1001, BF16, True, dict(engine=1, link_mode=1, cluster=4, fold=7)),
+    (0, 8, 0, 2053, F16, "nochain", dict(link_mode=1, channels=2, fold=7)),
+    (3, 8, 4, 1024, F32, "nochain", dict(link_mode=1, microbatches=4, mb_window=2, tb_alloc=1, fold=7)),
 ]
 
 

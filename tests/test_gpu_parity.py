@@ -543,6 +543,57 @@ def test_copy_chains_folded_bitexact(ccl, opts, kind, R, G, fuse, dtype, fold):
         assert_bitexact(to_host(d, dtype), want)
 
 
+REDUCE_OPTS = [dict(), dict(channels=3, microbatches=2), dict(engine=1), dict(engine=1, cluster=4),
+               dict(tb_alloc=2, channels=2), dict(bulk=1, tile_bytes=4096),
+               dict(microbatches=4, mb_window=2, tb_alloc=1), dict(protocol=1)]
+
+
+@pytest.mark.parametrize("opts", REDUCE_OPTS)
+@pytest.mark.parametrize("kind,R,G,fuse", [(2, 8, 0, True), (2, 5, 0, True), (2, 2, 0, True), (0, 8, 0, "nochain"),
+                                           (0, 5, 0, "nochain"), (0, 2, 0, "nochain"), (0, 8, 0, True),
+                                           (3, 16, 8, "nochain"), (3, 8, 4, True)])
+@pytest.mark.parametrize("dtype", [F32, BF16, F16, I32])
+def test_reduction_chains_folded_bitexact(ccl, opts, kind, R, G, fuse, dtype):
+    """Direct transport with every fold on (7): consecutive steps of a
+    reduction chain run as one step that reads the next rank's local
+    operand itself and adds it after its own sum -- ReduceScatter, ring
+    AllReduce (even and odd R, the completing step in a pair or alone), the
+    hierarchical AllReduce -- in every dtype (bf16 / f16 would show any
+    change of the summation order), on both engines, clusters, channels and
+    micro-batches, packing, the bulk path and windows; with the LL protocol
+    nothing folds and the result is the same.  Ragged chunks (LL: 16-byte
+    multiples); the AllReduce rows then in place."""
+    import torch
+    import datagen
+    import oracle
+    from gpu_helpers import oracle_program, to_device, empty_outputs, to_host
+    ll = opts.get("protocol") == 1
+    ce = 4096 if ll else 3001
+    flags = ccl.FLAG_NOCHAIN_COPIES if fuse == "nochain" else 0
+    sched = ccl.Schedule.builtin(kind, R, G, flags)
+    plan = ccl.Plan(sched, ce, dtype, link_mode=1, slot_bytes=4096, fold=7, **opts)
+    three = {ccl.KIND_NAMES.index(k) for k in ("rrs3", "rrc3", "rrcs3", "rsend", "rcsend")}
+    assert any(st["kind"] in three for st in plan.steps()) == (not ll)
+    # (never more bytes; at R = 2 the AllReduce's pair costs what the
+    # receive fold it replaces saved)
+    assert plan.stats().schedule_bytes <= sched.check(ce, dtype, link_mode=1, slot_bytes=4096, fold=3,
+                                                      **opts).schedule_bytes
+    ops, nch = oracle_program(kind, R, G)
+    ins = datagen.rank_inputs(83 + kind, DIST[dtype], R, nch[0] * ce, dtype)
+    d_out = empty_outputs(R, nch[1] * ce, dtype)
+    plan.execute(to_device(ins, dtype), d_out)
+    torch.cuda.synchronize()
+    plan.status()
+    want, _, _ = oracle.run(ops, R, nch, ce, dtype, ins)
+    assert_bitexact(to_host(d_out, dtype), want)
+    if kind in (0, 3):
+        d = to_device(ins, dtype)
+        plan.execute(d, d)
+        torch.cuda.synchronize()
+        plan.status()
+        assert_bitexact(to_host(d, dtype), want)
+
+
 SPECIALS = {0: [np.inf, -np.inf, np.nan, 3.0e38], 1: [0x7F80, 0xFF80, 0x7FC0, 0x7F7F], 2: [0x7C00, 0xFC00, 0x7E00, 0x7BFF]}
 
 

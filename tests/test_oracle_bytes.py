@@ -137,6 +137,56 @@ def test_planted_mistake_in_the_chain_fold_is_caught():
         OB._chain_folds = saved
 
 
+@pytest.mark.parametrize("R", [2, 3, 5, 8])
+def test_reduce_chain_folds_closed_forms(R):
+    """Direct transport with reduction chains folded (fold bit 2): a send or
+    recv-reduce-send and the receive-reduce its slot feeds become one step
+    that reads the second rank's local operand itself; the slot between them
+    (written 1, read 1) goes.  A chain of k hops pairs up from its head,
+    floor(k/2) pairs.  ReduceScatter (R hops per chunk): 3R - 1 - 2
+    floor(R/2).  Ring AllReduce, copy receives unchained, all folds (7):
+    the reduce-scatter 3R - 2 floor(R/2); its last step is in a pair for even
+    R, whose receive then keeps its FIFO (2), and alone for odd R, whose
+    receive is folded into it (bit 0); then the all-gather's R - 2 copies
+    fold in pairs (3 per pair, 2 for an odd one out)."""
+    n = 64 * 4
+    ops, nch = OS.ring_reducescatter(R)
+    assert OB.schedule_bytes(ops, R, nch, 64, F32, "full", True, 4) == R * (3 * R - 1 - 2 * (R // 2)) * n
+    ops, nch = OS.ring_allreduce(R)
+    ag = 3 * ((R - 2) // 2) + 2 * ((R - 2) % 2)
+    want = 3 * R - 2 * (R // 2) + (2 if R % 2 == 0 else 0) + ag
+    assert OB.schedule_bytes(ops, R, nch, 64, F32, "nochain", True, 7) == R * want * n
+
+
+def test_reduce_chain_folds_of_the_hierarchical_allreduce():
+    """G = 8, 2 groups, copy receives unchained, direct.  The in-group
+    reduce-scatter's 8 hops of 2-chunk slices (46 n) fold into 4 pairs (16 n
+    less: 30 n); the inter-group send and the recv-reduce-copy-send it feeds
+    become one step (4 n instead of 6 n), whose receive keeps its FIFO (2
+    n): 6 n; the in-group all-gather 28 n, or 22 n with copy chains
+    folded."""
+    ops, nch = OS.hier_allreduce(8, 2)
+    n = 64 * 4
+    for fold, per_rank in ((4, 30 + 6 + 28), (6, 30 + 6 + 22), (7, 30 + 6 + 22)):
+        assert OB.schedule_bytes(ops, 16, nch, 64, F32, "nochain", True, fold) == 16 * per_rank * n
+
+
+def test_planted_mistake_in_the_reduce_chain_fold_is_caught():
+    """Counting every reduction hop as folded into its predecessor (no head
+    rule) breaks the ReduceScatter pin."""
+    ops, nch = OS.ring_reducescatter(8)
+    good = OB.schedule_bytes(ops, 8, nch, 10, F32, "full", True, 4)
+    saved = OB._reduce_chain_folds
+    try:
+        def every_hop(halves):
+            s, taken = saved(halves)
+            return 2 * s, taken
+        OB._reduce_chain_folds = every_hop
+        assert OB.schedule_bytes(ops, 8, nch, 10, F32, "full", True, 4) != good
+    finally:
+        OB._reduce_chain_folds = saved
+
+
 def test_min_bytes_closed_forms():
     """Every input chunk a program reads, read once, and every output chunk
     it writes, written once: AllReduce R (R + R) chunks, AllGather R (1 +
@@ -197,7 +247,7 @@ def test_oracle_count_equals_the_product_count_for_every_benchmark_row():
 @pytest.mark.parametrize("kind,R,G", [(0, 8, 0), (0, 3, 0), (1, 8, 0), (2, 5, 0), (3, 16, 8), (3, 4, 2),
                                       (4, 32, 8), (4, 8, 4), (5, 24, 8), (5, 6, 3)])
 @pytest.mark.parametrize("flags", [0, 2, 4])
-@pytest.mark.parametrize("link_mode,fold", [(0, 1), (1, 1), (1, 0), (1, 2), (1, 3)])
+@pytest.mark.parametrize("link_mode,fold", [(0, 1), (1, 1), (1, 0), (1, 2), (1, 3), (1, 4), (1, 5), (1, 6), (1, 7)])
 def test_oracle_count_equals_the_product_count_for_builtins(kind, R, G, flags, link_mode, fold):
     ops, nch = KIND_PROGRAM[kind](R, G)
     st = ccl.Schedule.builtin(kind, R, G, flags).check(333, F32, link_mode=link_mode, fold=fold)
