@@ -46,19 +46,21 @@ SUITE = [
     # fuse="nochain": reductions fused, copy-only receives left unchained so
     # that direct transport makes each all-gather hop one plain copy
     ("hier_ar", 3, 16, 8, 0, 4 * MiB, "normal", 2,
-     # the in-group all-gather's copy hops run two at a time (copy chains
-     # folded); the inter-group step keeps its FIFO hop (folding its
-     # receive into the sender, as the rings do, measured 5 % slower here)
+     # (every fold: the in-group reduce-scatter runs two ranks per step, the
+     # inter-group send joins the step it feeds, the in-group all-gather's
+     # copies run two ranks per step)
      dict(fuse="nochain", link_mode=1, channels=9, microbatches=16, tb_alloc=1, slot_bytes=65536, fifo_slots=8,
-          mb_window=4, fold=2, nthreads=384)),
+          mb_window=4, fold=7)),
     ("a2a", 4, 32, 8, 2, 1 * MiB, "uniform", 3,
      dict(channels=8, link_mode=1, channel_scaling=0, tb_alloc=2, tb_budget=256)),
+    # reduce-scatter steps two ranks at a time (reduction chains folded),
+    # all-gather copies two ranks at a time (copy chains folded)
     ("ring_bf16", 0, 8, 0, 1, 32 * MiB, "normal", 4,
      dict(fuse="nochain", link_mode=1, channels=24, slot_bytes=131072, microbatches=12, fifo_slots=4, tb_alloc=2,
-          tb_budget=192)),
+          tb_budget=192, fold=7)),
     ("ring_f32", 0, 8, 0, 0, 32 * MiB, "normal", 4,
      dict(fuse="nochain", link_mode=1, channels=24, slot_bytes=131072, microbatches=12, fifo_slots=4, tb_alloc=2,
-          tb_budget=192)),
+          tb_budget=192, fold=7)),
     # relay hops as plain direct copies (no fusion into FIFO forwards)
     ("a2n", 5, 24, 8, 0, 16 * MiB, "normal", 4,
      dict(fuse=False, channels=16, link_mode=1, microbatches=8, tb_alloc=2, tb_budget=304, channel_scaling=0)),
@@ -72,10 +74,10 @@ SUITE = [
     # FIFOs at least one execution deep (8 slots): no slot is reused within
     # an execution, so nothing is posted or waited for its consumption
     ("rs_3m", 2, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4, engine=1, cluster=4, nthreads=256,
-                                                          fifo_slots=8)),
+                                                          fifo_slots=8, fold=7)),
     ("ar_1m", 0, 8, 0, 0, 1 * MiB // 8, "uniform", 0, dict(fuse="nochain", link_mode=1, channels=1, tb_alloc=2,
                                                             tb_budget=16, engine=1, cluster=8, nthreads=128,
-                                                            fifo_slots=8)),
+                                                            fifo_slots=8, fold=7)),
 ]
 ESIZE = {0: 4, 1: 2, 2: 2, 3: 4}
 NAMES = {0: "f32", 1: "bf16", 2: "f16", 3: "i32"}
@@ -661,7 +663,8 @@ ORACLE_PROGRAMS = {0: ("ring_allreduce", lambda R, G: (R,)), 1: ("ring_allgather
                    4: ("alltoall_two_phase", lambda R, G: (G, R // G)), 5: ("alltonext", lambda R, G: (G, R // G))}
 # the plan option defaults the suite rows rely on (ccl_plan_opts_default):
 # direct transport unless a row asks for FIFOs, receives and copy chains
-# folded unless a row says otherwise
+# folded unless a row says otherwise (the rows with reduction chains fold
+# them too: fold 7)
 DEFAULT_LINK_MODE = 1
 DEFAULT_FOLD = 3
 

@@ -9,9 +9,8 @@
 // while bandwidth keeps improving (bandwidth is unimodal in each of them).
 // Grids: channels {1,2,4,8,12,16,24,32,48}, threads {128,256,512,1024},
 // slot size 16 KiB .. 4 MiB in powers of two, on the sequential engine
-// CTAs per threadblock program {1,2,4,8}, and with direct transport the
-// folds {0,1,2,3} (receives into senders, copy chains; not unimodal, but
-// the descent starts at the caller's folds and tries its neighbours).  A probe is the median of
+// CTAs per threadblock program {1,2,4,8}, and with direct transport each
+// fold bit {0,1} (receives into senders, copy chains, reduction chains).  A probe is the median of
 // `reps` CUDA-event-timed executions after one warm-up; a point whose plan
 // cannot be built (threadblocks not co-resident, FIFO too small) scores 0.
 #include <cuda_runtime.h>
@@ -174,35 +173,40 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
         const bool seq = cur.engine == CCL_ENGINE_SEQUENTIAL;
         const std::vector<int> gk = seq ? std::vector<int>{1, 2, 4, 8} : std::vector<int>{1};
         if (!seq) cur.cluster = 0;
-        // direct transport also chooses its folds (receives, copy chains)
+        // direct transport also chooses its folds: each of the three fold
+        // bits (receives, copy chains, reduction chains) a coordinate of its
+        // own with the values 0 and 1
         const bool direct = cur.link_mode == CCL_LINK_DIRECT;
-        const std::vector<int> gf = direct ? std::vector<int>{0, 1, 2, 3} : std::vector<int>{cur.fold};
         int ic = nearest(gc, cur.channels), it = nearest(gt, cur.nthreads), is = nearest(gs, cur.slot_bytes);
         int ik = seq ? nearest(gk, std::max(1, cur.cluster)) : 0;
-        int ifo = direct ? nearest(gf, cur.fold) : 0;
-        auto eval = [&](int c, int t, int sl, int k, int f) {
+        int fb[3] = {cur.fold & 1, (cur.fold >> 1) & 1, (cur.fold >> 2) & 1};
+        auto eval = [&](int c, int t, int sl, int k, const int* f) {
             ccl_plan_opts_t o = cur;
             o.channels = gc[c];
             o.nthreads = gt[t];
             o.slot_bytes = gs[sl];
             o.cluster = gk[k] > 1 ? gk[k] : 0;
-            o.fold = gf[f];
+            if (direct) o.fold = f[0] | (f[1] << 1) | (f[2] << 2);
             return measure(o);
         };
         std::vector<int> coords{0, 1, 2};
         if (seq) coords.push_back(3);
-        if (direct) coords.push_back(4);
-        double bw = eval(ic, it, is, ik, ifo);
+        if (direct) for (int b = 0; b < 3; ++b) coords.push_back(4 + b);
+        double bw = eval(ic, it, is, ik, fb);
         for (int round = 0; round < to.max_rounds; ++round) {
             bool moved = false;
             for (int coord : coords) {
-                int* idx = coord == 0 ? &ic : coord == 1 ? &it : coord == 2 ? &is : coord == 3 ? &ik : &ifo;
+                int* idx = coord == 0 ? &ic : coord == 1 ? &it : coord == 2 ? &is : coord == 3 ? &ik : &fb[coord - 4];
                 int n = coord == 0 ? (int)gc.size() : coord == 1 ? (int)gt.size() : coord == 2 ? (int)gs.size()
-                        : coord == 3 ? (int)gk.size() : (int)gf.size();
+                        : coord == 3 ? (int)gk.size() : 2;
                 auto at = [&](int v) {
-                    return coord == 0 ? eval(v, it, is, ik, ifo) : coord == 1 ? eval(ic, v, is, ik, ifo)
-                           : coord == 2 ? eval(ic, it, v, ik, ifo) : coord == 3 ? eval(ic, it, is, v, ifo)
-                                                                     : eval(ic, it, is, ik, v);
+                    if (coord >= 4) {
+                        int f[3] = {fb[0], fb[1], fb[2]};
+                        f[coord - 4] = v;
+                        return eval(ic, it, is, ik, f);
+                    }
+                    return coord == 0 ? eval(v, it, is, ik, fb) : coord == 1 ? eval(ic, v, is, ik, fb)
+                           : coord == 2 ? eval(ic, it, v, ik, fb) : eval(ic, it, is, v, fb);
                 };
                 // raise while bandwidth improves; if the first raise does not
                 // help, try lowering the same way
@@ -230,7 +234,7 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
             overall.nthreads = gt[it];
             overall.slot_bytes = gs[is];
             overall.cluster = gk[ik] > 1 ? gk[ik] : 0;
-            overall.fold = gf[ifo];
+            if (direct) overall.fold = fb[0] | (fb[1] << 1) | (fb[2] << 2);
         }
     }
     *best = overall;

@@ -327,7 +327,7 @@ typedef enum {
  *                 step moves on `cluster` SMs instead of one, for the
  *                 latency-bound sizes where a single CTA's data time sets the
  *                 length of every hop.
- *   fold        : with direct transport, a bit mask (default 3: both).
+ *   fold        : with direct transport, a bit mask (default 3).
  *                 Bit 0 (1): a plain receive fed by a copy-send or a
  *                 recv-reduce-copy-send is folded into its sender, whose
  *                 pass then writes the receiver's buffer too (CCL_I_COPY2 /
@@ -340,9 +340,24 @@ typedef enum {
  *                 per element byte instead of 2 + 2, one step fewer); a
  *                 chain of k copies from its head becomes ceil(k/2) steps,
  *                 and a pair whose merged dependencies would cycle is kept
- *                 apart.  A folded plan that would cycle or deadlock is
- *                 planned again without folds.  Values outside 0..3:
- *                 CCL_ERR_INVALID_ARG.
+ *                 apart.  Bit 2 (4): reduction chains -- a send or
+ *                 recv-reduce-send and the receive-reduce its slot feeds
+ *                 run as one step on the first one's threadblock, which
+ *                 reads the second rank's local operand itself and adds it
+ *                 after its own sum (the chain's order and rounding; the
+ *                 CCL_I_RSEND, RCSEND, RRS3, RRC3, RRCS3 steps, or a
+ *                 CCL_I_REDUCE across ranks): the slot between them (2
+ *                 bytes per element byte) and a hop go, and the step sends
+ *                 on where the second one sent; folded before bit 0, so a
+ *                 recv-reduce-copy-send taken into a pair keeps its
+ *                 receive's FIFO; not with the LL protocol.  Not in the
+ *                 default: where a chain's other hops stay one rank apart
+ *                 (a fully fused ring AllReduce's all-gather) a rank then
+ *                 needs links one and two ranks away and more
+ *                 threadblocks; with the all-gather hops direct (copy
+ *                 receives unchained) it does not.  A folded plan
+ *                 that would cycle or deadlock is planned again without
+ *                 folds.  Values outside 0..7: CCL_ERR_INVALID_ARG.
  *   codegen     : 0 (default): the library's kernels interpret the plan's
  *                 step records.  1: ccl_plan_create generates CUDA source
  *                 for this one plan (ReSCCL report, §II.2: a kernel per
@@ -380,7 +395,7 @@ typedef struct {
     int32_t codegen;     /* 1: run a kernel generated and compiled for this plan (see below) */
     int32_t cluster;     /* sequential engine: CTAs per threadblock program (0 or 1: one; 2, 4, 8) */
     int32_t fold;        /* direct transport: bit 0 folds plain receives into their senders, bit 1
-                            copy chains (default 3) */
+                            copy chains, bit 2 reduction chains (default 3) */
 } ccl_plan_opts_t;
 
 void ccl_plan_opts_default(ccl_plan_opts_t* o);
@@ -646,7 +661,7 @@ ccl_status_t ccl_allreduce_ring_noalloc(void* const* in_bufs, void* const* out_b
  * x protocol (simple / LL) x transport (FIFO / direct) x engine (pipelined
  * / sequential) make sixteen subspaces; in each, coordinate descent over
  * channels, threads and slot size (and CTAs per program on the sequential
- * engine, and the folds 0..3 with direct transport), driven by a
+ * engine, and each fold bit with direct transport), driven by a
  * caller-supplied probe that returns the bandwidth of a configuration (any
  * unit, <= 0 = cannot run).  start (nullable) is the first point; best gets
  * the winner, *best_bw its bandwidth, *probes the number of distinct

@@ -486,14 +486,15 @@ def test_coordinate_descent_plateau_stops_early():
     # sixteen subspaces (policy x protocol x transport x engine): on a flat
     # surface each tries one step up and one down per coordinate (at most 6
     # probes; 8 on the sequential engine, which also has the CTAs per
-    # program), plus the start
+    # program; 3 more with direct transport, one flip of each fold bit),
+    # plus the start
     seen = set()
 
     def flat(o):
         seen.add((o.tb_alloc, o.protocol, o.link_mode, o.engine))
         return 1.0
     best, bw, n = ccl.tune_search(flat)
-    assert bw == 1.0 and n <= 1 + 8 * 6 + 8 * 8
+    assert bw == 1.0 and n <= 1 + 8 * 6 + 8 * 8 + 8 * 3
     assert len(seen) == 16
 
 
