@@ -49,17 +49,17 @@ SUITE = [
      # (every fold: the in-group reduce-scatter runs two ranks per step, the
      # inter-group send joins the step it feeds, the in-group all-gather's
      # copies run two ranks per step)
-     dict(fuse="nochain", link_mode=1, channels=9, microbatches=16, tb_alloc=1, slot_bytes=65536, fifo_slots=8,
+     dict(fuse="nochain", link_mode=1, channels=8, microbatches=16, tb_alloc=1, slot_bytes=65536, fifo_slots=8,
           mb_window=4, fold=7)),
     ("a2a", 4, 32, 8, 2, 1 * MiB, "uniform", 3,
      dict(channels=8, link_mode=1, channel_scaling=0, tb_alloc=2, tb_budget=256)),
     # reduce-scatter steps two ranks at a time (reduction chains folded),
     # all-gather copies two ranks at a time (copy chains folded)
     ("ring_bf16", 0, 8, 0, 1, 32 * MiB, "normal", 4,
-     dict(fuse="nochain", link_mode=1, channels=24, slot_bytes=131072, microbatches=12, fifo_slots=4, tb_alloc=2,
+     dict(fuse="nochain", link_mode=1, channels=24, slot_bytes=131072, microbatches=16, fifo_slots=4, tb_alloc=2,
           tb_budget=192, fold=7)),
     ("ring_f32", 0, 8, 0, 0, 32 * MiB, "normal", 4,
-     dict(fuse="nochain", link_mode=1, channels=24, slot_bytes=131072, microbatches=12, fifo_slots=4, tb_alloc=2,
+     dict(fuse="nochain", link_mode=1, channels=24, slot_bytes=131072, microbatches=16, fifo_slots=4, tb_alloc=2,
           tb_budget=192, fold=7)),
     # relay hops as plain direct copies (no fusion into FIFO forwards)
     ("a2n", 5, 24, 8, 0, 16 * MiB, "normal", 4,
