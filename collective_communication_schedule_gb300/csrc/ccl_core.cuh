@@ -313,7 +313,7 @@ __device__ CCL_MOVE_ATTR void move3(const char* a, bool as, const char* b, bool 
 {
     constexpr int ES = (DT == CCL_BF16 || DT == CCL_F16) ? 2 : 4;
     constexpr int VE = 16 / ES;
-    constexpr int U3 = U >= 8 ? 6 : 2;
+    constexpr int U3 = U >= 8 ? 6 : 3;
     const unsigned long long al = (unsigned long long)a | (unsigned long long)b | (unsigned long long)c |
                                   (unsigned long long)o1 | (unsigned long long)o2;
     long long nv = 0;
