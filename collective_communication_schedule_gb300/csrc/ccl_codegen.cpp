@@ -301,14 +301,16 @@ std::string generate_plan_source(const PlanImage& img, int build, std::string* w
                 }
                 // DRec: kind dtype link_in link_out src_buf src_rank loc_buf loc_rank dst_buf dst_rank
                 // nslots dep_begin dep_count signal mb flags src_off loc_off dst_off nelem seq_in
-                // seq_out drain seq_in_mod seq_out_mod link_loc (nelem: the whole channel range)
+                // seq_out drain seq_in_mod seq_out_mod link_loc x_buf x_rank x_off (nelem: the whole
+                // channel range)
                 table += "    {{" + std::to_string(D.kind) + ", " + std::to_string(D.dtype) + ", " +
                          std::to_string(D.link_in) + ", " + std::to_string(D.link_out) + ", " + std::to_string(D.src_buf) +
                          ", " + std::to_string(D.src_rank) + ", " + std::to_string(D.loc_buf) + ", " +
                          std::to_string(D.loc_rank) + ", " + std::to_string(D.dst_buf) + ", " + std::to_string(D.dst_rank) +
                          ", 0, 0, 0, " + std::to_string(f.signal) + ", 0, " + std::to_string(f.flags) + ", " +
                          lit(D.src_off) + ", " + lit(D.loc_off) + ", " + lit(D.dst_off) + ", " + lit(D.nelem) +
-                         ", 0, 0, -1, 0, 0, 0}, " + link(D.link_in) + ", " + link(D.link_out) + ", " +
+                         ", 0, 0, -1, 0, 0, 0, " + std::to_string(D.x_buf) + ", " + std::to_string(D.x_rank) + ", " +
+                         lit(D.x_buf >= 0 ? D.x_off : 0) + "}, " + link(D.link_in) + ", " + link(D.link_out) + ", " +
                          std::to_string(dep_first) + ", " + std::to_string(deps.size()) + ", " +
                          std::to_string(seq ? 0 : f.drain_kind) + ", " + std::to_string(f.drain_dk) + ", " +
                          std::to_string(f.drain_const) + ", " + lit(f.p_base) + ", " + std::to_string(f.p_n) + ", " +

@@ -353,11 +353,12 @@ __device__ __noinline__ void move_part3_call(int dtype, const char* a, bool as, 
 __device__ __forceinline__ bool kind_reduces(int k)
 {
     return k == CCL_I_REDUCE || k == CCL_I_RRC || k == CCL_I_RRS || k == CCL_I_RRCS || k == CCL_I_RRC2 ||
-           k == CCL_I_RRS3 || k == CCL_I_RRC3 || k == CCL_I_RRCS3 || k == CCL_I_RSEND || k == CCL_I_RCSEND;
+           k == CCL_I_RRS3 || k == CCL_I_RRC3 || k == CCL_I_RRCS3 || k == CCL_I_RSEND || k == CCL_I_RCSEND ||
+           k == CCL_I_RRC3D || k == CCL_I_REDUCE2;
 }
 __device__ __forceinline__ bool kind_three(int k)
 {
-    return k == CCL_I_RRS3 || k == CCL_I_RRC3 || k == CCL_I_RRCS3;
+    return k == CCL_I_RRS3 || k == CCL_I_RRC3 || k == CCL_I_RRCS3 || k == CCL_I_RRC3D;
 }
 
 // the whole CTA moves the data
@@ -769,7 +770,7 @@ __device__ __forceinline__ void prefetch_rec(DRec* dst, const DRec* src)
 {
     const unsigned d = smem_addr(dst);
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
+    for (int k = 0; k < (int)(sizeof(DRec) / 16); ++k)
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + 16 * k), "l"((const char*)src + 16 * k)
                      : "memory");
 }
@@ -1013,8 +1014,11 @@ __device__ __forceinline__ bool issue_step(const KParams& P, CtlShared* sh, cons
             if (dstb) {
                 op.o1 = dstb + off;
                 op.o1s = st.dst_buf == CCL_BUF_OUT;
+                // (a second destination -- a folded receive -- is written
+                // instead of a slot)
                 op.o2 = copy2  ? const_cast<char*>(locb) + off
                         : rrc2 ? const_cast<char*>(srcb) + off
+                        : st.x_buf >= 0 ? P.bufs[st.x_buf][st.x_rank] + st.x_off * es + off
                         : slot_out ? slot_out + lls * soff
                                    : nullptr;
                 op.o2_ll = slot_out && P.ll;
@@ -1679,7 +1683,12 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
         if (dstb) {
             o1 = dstb + e0 * es;
             o1s = st.dst_buf == CCL_BUF_OUT;
-            o2 = copy2 ? const_cast<char*>(locb) + e0 * es : rrc2 ? const_cast<char*>(srcb) + e0 * es : slot_out;
+            // (a second destination -- a folded receive -- is written
+            // instead of a slot; its address is made here, not kept live)
+            o2 = copy2  ? const_cast<char*>(locb) + e0 * es
+                 : rrc2 ? const_cast<char*>(srcb) + e0 * es
+                 : st.x_buf >= 0 ? P.bufs[st.x_buf][st.x_rank] + (st.x_off + e0) * es
+                                 : slot_out;
         } else {
             o1 = slot_out;
         }
@@ -1868,6 +1877,7 @@ __device__ __forceinline__ void gen_piece(const GenInstr& gi, int m, long long v
     g.st.src_off += off;
     g.st.loc_off += off;
     g.st.dst_off += off;
+    if (g.st.x_buf >= 0) g.st.x_off += off;
     g.st.nelem = len;
     const bool linked = gi.st.link_in >= 0 || gi.st.link_out >= 0;
     const long long ns = (len + slot_elems - 1) / slot_elems;

@@ -38,6 +38,7 @@ struct Instr {
     int kind = CCL_I_COPY;   // ccl_instr_kind_t
     int rank = -1;
     Range src, loc, dst;
+    Range x;                 // second destination of a folded receive (plans only)
     int64_t count = 0;       // chunks
     int xfer_in = -1, xfer_out = -1;
     int position = 0;        // program position (order on its rank)

@@ -13,7 +13,8 @@ enum { CCL_BUF_IN = 0, CCL_BUF_OUT = 1, CCL_BUF_SCRATCH = 2 };
 enum {
     CCL_I_COPY = 0, CCL_I_REDUCE = 1, CCL_I_SEND = 2, CCL_I_RECV = 3, CCL_I_RRC = 4,
     CCL_I_RCS = 5, CCL_I_FWD = 6, CCL_I_RRS = 7, CCL_I_RRCS = 8, CCL_I_COPY_SEND = 9, CCL_I_COPY2 = 10,
-    CCL_I_RRC2 = 11, CCL_I_RRS3 = 12, CCL_I_RRC3 = 13, CCL_I_RRCS3 = 14, CCL_I_RSEND = 15, CCL_I_RCSEND = 16
+    CCL_I_RRC2 = 11, CCL_I_RRS3 = 12, CCL_I_RRC3 = 13, CCL_I_RRCS3 = 14, CCL_I_RSEND = 15, CCL_I_RCSEND = 16,
+    CCL_I_RRC3D = 17, CCL_I_REDUCE2 = 18
 };
 enum { CCL_ERR_TIMEOUT = 8 };
 #define CCL_MAX_RANKS 64
@@ -39,8 +40,10 @@ struct DRec {
     int seq_in_mod, seq_out_mod;   // seq_in % S, seq_out % S (slot index arithmetic in 32 bits)
     int link_loc;                  // 1 + the incoming (bits 0-7) and outgoing (bits 8-15) link's entry in
                                    // its program's link table (KParams.prog_links); 0: read the link array
+    int x_buf, x_rank;             // a second destination (a folded receive of a three-operand or
+    long long x_off;               // cross-rank reduce step), buf -1 when none
 };
-static_assert(sizeof(DRec) == 128, "DRec layout");
+static_assert(sizeof(DRec) == 144, "DRec layout");
 
 struct DLink {
     long long slot_base;  // byte offset of slot 0 in the FIFO pool (slots of slot_stride bytes)

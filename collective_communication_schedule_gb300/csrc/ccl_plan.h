@@ -22,11 +22,12 @@ struct DInstr {
     int32_t src_rank, src_buf;
     int32_t loc_rank, loc_buf;
     int32_t dst_rank, dst_buf;
-    int32_t pad0, pad1;
+    int32_t x_rank, x_buf;          // second destination (buf -1: none)
     int64_t src_off, loc_off, dst_off;
     int64_t nelem;
+    int64_t x_off;
 };
-static_assert(sizeof(DInstr) == 80, "DInstr layout");
+static_assert(sizeof(DInstr) == 88, "DInstr layout");
 
 // One (channel instruction, micro-batch) step of a threadblock program.
 struct DStep {

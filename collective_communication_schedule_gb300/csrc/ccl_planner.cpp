@@ -262,7 +262,8 @@ void allocate_connection(const ccl_schedule& s, const Timeline& tl, TBList* tbs,
             int out = I.xfer_out >= 0 ? s.xfers[I.xfer_out].dst_rank : -1;
             // a copy into another rank's buffer (direct transport) is a
             // connection of its own to that rank
-            if ((I.kind == CCL_I_COPY || I.kind == CCL_I_REDUCE) && I.dst.valid() && I.dst.rank != I.rank)
+            if ((I.kind == CCL_I_COPY || I.kind == CCL_I_REDUCE || I.kind == CCL_I_REDUCE2) && I.dst.valid() &&
+                I.dst.rank != I.rank)
                 out = CCL_MAX_RANKS + I.dst.rank;
             // (a two-destination copy: its first remote destination)
             if (I.kind == CCL_I_COPY2) {
@@ -464,6 +465,8 @@ void fill_records(PlanImage* img)
         r.src_off = in.src_off + st.elem_off;
         r.loc_off = in.loc_off + st.elem_off;
         r.dst_off = in.dst_off + st.elem_off;
+        r.x_buf = in.x_buf; r.x_rank = in.x_rank;
+        r.x_off = in.x_buf >= 0 ? in.x_off + st.elem_off : 0;
         r.nelem = st.nelem; r.seq_in = st.seq_in; r.seq_out = st.seq_out;
         r.seq_in_mod = (int32_t)(st.seq_in % img->S);
         r.seq_out_mod = (int32_t)(st.seq_out % img->S);
@@ -621,9 +624,11 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
             D.src_off = I.src.valid() ? I.src.off * ce + pce.off : 0;
             D.loc_off = I.loc.valid() ? I.loc.off * ce + pce.off : 0;
             D.dst_off = I.dst.valid() ? I.dst.off * ce + pce.off : 0;
+            D.x_rank = I.x.rank; D.x_buf = I.x.valid() ? I.x.buf : -1;
+            D.x_off = I.x.valid() ? I.x.off * ce + pce.off : 0;
             D.nelem = pce.len;
             sched_bytes += kind_bytes_factor(I.kind) * pce.len * es;
-            for (const Range* rg : {&I.src, &I.loc, &I.dst})
+            for (const Range* rg : {&I.src, &I.loc, &I.dst, &I.x})
                 if (rg->valid() && rg->buf == CCL_BUF_SCRATCH) img->scratch_used[rg->rank] = true;
         }
     }
@@ -639,6 +644,7 @@ ccl_status_t build_image(const ccl_schedule& s, const Timeline& tl, const TBList
         if (I.dst.valid() && I.dst.buf == CCL_BUF_IN) in_written[I.dst.rank] = 1;
         if (I.kind == CCL_I_COPY2 && I.loc.valid() && I.loc.buf == CCL_BUF_IN) in_written[I.loc.rank] = 1;
         if (I.kind == CCL_I_RRC2 && I.src.valid() && I.src.buf == CCL_BUF_IN) in_written[I.src.rank] = 1;
+        if (I.x.valid() && I.x.buf == CCL_BUF_IN) in_written[I.x.rank] = 1;
     }
     auto stream_bits = [&](const DInstr& D) {
         int32_t f = 0;
@@ -947,7 +953,8 @@ ccl_schedule direct_transport(const ccl_schedule& s, int* ndirect, bool fold)
         const Xfer& X = s.xfers[x];
         const Instr& snd = s.instrs[X.send_instr];
         const Instr& rcv = s.instrs[X.recv_instr];
-        const bool foldable = snd.kind == CCL_I_COPY_SEND || snd.kind == CCL_I_RRCS;
+        const bool foldable = snd.kind == CCL_I_COPY_SEND || snd.kind == CCL_I_RRCS || snd.kind == CCL_I_RRCS3 ||
+                              snd.kind == CCL_I_RCSEND;
         if ((snd.kind != CCL_I_SEND && !(fold && foldable)) || rcv.kind != CCL_I_RECV) continue;
         Instr& c = d.instrs[X.send_instr];
         if (snd.kind == CCL_I_SEND) {
@@ -958,11 +965,16 @@ ccl_schedule direct_transport(const ccl_schedule& s, int* ndirect, bool fold)
             // pass, the receiver's (held in the local-operand range)
             c.kind = CCL_I_COPY2;
             c.loc = rcv.dst;
-        } else {
+        } else if (snd.kind == CCL_I_RRCS) {
             // the recv-reduce-copy-send likewise (its source range, unused:
             // the first operand is the incoming slot)
             c.kind = CCL_I_RRC2;
             c.src = rcv.dst;
+        } else {
+            // a folded reduction step that sends its result on writes the
+            // receiver's destination as its second destination instead
+            c.kind = snd.kind == CCL_I_RRCS3 ? CCL_I_RRC3D : CCL_I_REDUCE2;
+            c.x = rcv.dst;
         }
         c.xfer_out = -1;
         drop_x[x] = 1;

@@ -136,8 +136,12 @@ typedef enum {
     CCL_I_RRC3 = 13,     /* dst <- (slot_in (+) local) (+) src */
     CCL_I_RRCS3 = 14,    /* t <- (slot_in (+) local) (+) src; dst <- t; slot_out <- t */
     CCL_I_RSEND = 15,    /* slot_out <- src (+) local  (a send and the recv-reduce-send it feeds) */
-    CCL_I_RCSEND = 16    /* t <- src (+) local; dst <- t; slot_out <- t  (a send and a recv-reduce-copy-send);
+    CCL_I_RCSEND = 16,   /* t <- src (+) local; dst <- t; slot_out <- t  (a send and a recv-reduce-copy-send);
                             a send and the recv-reduce-copy it feeds become a CCL_I_REDUCE */
+    /* and with the plain receive that the last two feed folded in (a
+       second destination x, the receiver's, instead of the slot): */
+    CCL_I_RRC3D = 17,    /* t <- (slot_in (+) local) (+) src; dst <- t; x <- t */
+    CCL_I_REDUCE2 = 18   /* t <- src (+) local; dst <- t; x <- t */
 } ccl_instr_kind_t;
 
 typedef struct {
@@ -348,9 +352,10 @@ typedef enum {
  *                 CCL_I_RSEND, RCSEND, RRS3, RRC3, RRCS3 steps, or a
  *                 CCL_I_REDUCE across ranks): the slot between them (2
  *                 bytes per element byte) and a hop go, and the step sends
- *                 on where the second one sent; folded before bit 0, so a
- *                 recv-reduce-copy-send taken into a pair keeps its
- *                 receive's FIFO; not with the LL protocol.  Not in the
+ *                 on where the second one sent; with bit 0 the plain
+ *                 receive such a step feeds is folded into it as a second
+ *                 destination (CCL_I_RRC3D, CCL_I_REDUCE2); not with the LL
+ *                 protocol.  Not in the
  *                 default: where a chain's other hops stay one rank apart
  *                 (a fully fused ring AllReduce's all-gather) a rank then
  *                 needs links one and two ranks away and more

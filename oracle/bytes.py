@@ -271,21 +271,21 @@ def schedule_bytes(ops, nranks, nchunks, chunk_elems, dtype, fuse="full", direct
     3; recv-reduce-copy-send 4 + receive 2 -> 4).  ``fold`` bit 0 (True)
     takes the last two without their FIFO (cleared: they keep it); bit 1
     also folds copy chains (``_chain_folds``); bit 2 reduction chains
-    (``_reduce_chain_folds``, first: a recv-reduce-copy-send taken into a
-    pair keeps its receive's FIFO)."""
+    (``_reduce_chain_folds``; the receive fed by a recv-reduce-copy-send
+    taken into a pair is folded into the pair's step the same way)."""
     halves = _fused_halves(ops, nranks, fuse)
     units = sum(FACTOR[h.kind()] * h.count for h in halves)
     if direct:
-        taken = set()
         if int(fold) & 4:
-            saved, taken = _reduce_chain_folds(halves)
-            units -= saved
+            units -= _reduce_chain_folds(halves)[0]
         sender = {h.send: h for h in halves if h.send is not None}
         for h in halves:
             if h.kind() != "recv":
                 continue
             s = sender[h.recv]
-            if s.kind() == "send" or (int(fold) & 1 and s.kind() in ("copy_send", "rrcs") and id(s) not in taken):
+            # (a recv-reduce-copy-send taken into a reduction pair still
+            # writes the receiver's buffer itself)
+            if s.kind() == "send" or (int(fold) & 1 and s.kind() in ("copy_send", "rrcs")):
                 units -= 2 * h.count
         if int(fold) & 2:
             units -= _chain_folds(halves)

@@ -42,17 +42,16 @@ def test_ring_rows_match_the_closed_form(name):
     receive's 2 bytes per element byte: 2 N in all.  With every fold
     (7), per rank and chunk of cb bytes: the reduce-scatter's R steps (3R
     units) pair up into floor(R/2) steps that read the next rank's input
-    themselves (2 units less each); for even R the completing step is in a
-    pair and its receive keeps its FIFO (2), for odd R it is folded; the
-    R - 2 middle all-gather hops run two at a time (3 per pair, 2 for an
-    odd one out)."""
+    themselves (2 units less each); the receive the completing step feeds
+    is folded into it; the R - 2 middle all-gather hops run two at a time (3
+    per pair, 2 for an odd one out)."""
     row = [r for r in bench.SUITE if r[0] == name][0]
     _, kind, R, G, dt, cb, dist, seed, opts = row
     assert opts.get("fuse") == "nochain" and opts.get("link_mode") == 1
     N = R * cb                       # R chunks of cb bytes per rank
     _, st, _ = _plan(row)
     assert opts.get("fold", bench.DEFAULT_FOLD) == 7
-    units = 3 * R - 2 * (R // 2) + (2 if R % 2 == 0 else 0) + 3 * ((R - 2) // 2) + 2 * ((R - 2) % 2)
+    units = 3 * R - 2 * (R // 2) + 3 * ((R - 2) // 2) + 2 * ((R - 2) % 2)
     assert st.schedule_bytes == R * units * cb
     assert st.min_bytes == 2 * R * N
 

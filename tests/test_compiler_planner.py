@@ -765,8 +765,9 @@ def test_direct_transport_folds_reduction_chains():
 
 def test_reduce_chain_fold_keeps_the_ring_allreduce_on_one_threadblock_per_rank():
     """With every fold on, the ring AllReduce's reduce-scatter pairs run two
-    ranks apart and the step that completes a chunk joins the last pair (its
-    receive keeps the FIFO): still one threadblock per rank and channel."""
+    ranks apart and the step that completes a chunk joins the last pair and
+    writes the next rank's output itself: still one threadblock per rank and
+    channel."""
     R = 8
     s = ccl.Schedule.builtin(ccl.RING_ALLREDUCE, R, 0, ccl.FLAG_NOCHAIN_COPIES)
     for ch in (1, 4):

@@ -573,7 +573,8 @@ def test_reduction_chains_folded_bitexact(ccl, opts, kind, R, G, fuse, dtype):
     sched = ccl.Schedule.builtin(kind, R, G, flags)
     plan = ccl.Plan(sched, ce, dtype, link_mode=1, slot_bytes=4096, fold=7, **opts)
     # (a send folded into the recv-reduce-copy it feeds is a reduce)
-    three = {ccl.KIND_NAMES.index(k) for k in ("rrs3", "rrc3", "rrcs3", "rsend", "rcsend", "reduce")}
+    three = {ccl.KIND_NAMES.index(k) for k in ("rrs3", "rrc3", "rrcs3", "rsend", "rcsend", "reduce", "rrc3d",
+                                                 "reduce2")}
     assert any(st["kind"] in three for st in plan.steps()) == (not ll)
     # (never more bytes; at R = 2 the AllReduce's pair costs what the
     # receive fold it replaces saved)

@@ -145,16 +145,15 @@ def test_reduce_chain_folds_closed_forms(R):
     (written 1, read 1) goes.  A chain of k hops pairs up from its head,
     floor(k/2) pairs.  ReduceScatter (R hops per chunk): 3R - 1 - 2
     floor(R/2).  Ring AllReduce, copy receives unchained, all folds (7):
-    the reduce-scatter 3R - 2 floor(R/2); its last step is in a pair for even
-    R, whose receive then keeps its FIFO (2), and alone for odd R, whose
-    receive is folded into it (bit 0); then the all-gather's R - 2 copies
-    fold in pairs (3 per pair, 2 for an odd one out)."""
+    the reduce-scatter 3R - 2 floor(R/2); the receive its last step feeds
+    is folded into that step (bit 0), paired or not; then the all-gather's
+    R - 2 copies fold in pairs (3 per pair, 2 for an odd one out)."""
     n = 64 * 4
     ops, nch = OS.ring_reducescatter(R)
     assert OB.schedule_bytes(ops, R, nch, 64, F32, "full", True, 4) == R * (3 * R - 1 - 2 * (R // 2)) * n
     ops, nch = OS.ring_allreduce(R)
     ag = 3 * ((R - 2) // 2) + 2 * ((R - 2) % 2)
-    want = 3 * R - 2 * (R // 2) + (2 if R % 2 == 0 else 0) + ag
+    want = 3 * R - 2 * (R // 2) + ag
     assert OB.schedule_bytes(ops, R, nch, 64, F32, "nochain", True, 7) == R * want * n
 
 
@@ -163,11 +162,11 @@ def test_reduce_chain_folds_of_the_hierarchical_allreduce():
     reduce-scatter's 8 hops of 2-chunk slices (46 n) fold into 4 pairs (16 n
     less: 30 n); the inter-group send and the recv-reduce-copy-send it feeds
     become one step (4 n instead of 6 n), whose receive keeps its FIFO (2
-    n): 6 n; the in-group all-gather 28 n, or 22 n with copy chains
-    folded."""
+    n) unless receives fold as well (bit 0): 6 n or 4 n; the in-group
+    all-gather 28 n, or 22 n with copy chains folded."""
     ops, nch = OS.hier_allreduce(8, 2)
     n = 64 * 4
-    for fold, per_rank in ((4, 30 + 6 + 28), (6, 30 + 6 + 22), (7, 30 + 6 + 22)):
+    for fold, per_rank in ((4, 30 + 6 + 28), (5, 30 + 4 + 28), (6, 30 + 6 + 22), (7, 30 + 4 + 22)):
         assert OB.schedule_bytes(ops, 16, nch, 64, F32, "nochain", True, fold) == 16 * per_rank * n
 
 
