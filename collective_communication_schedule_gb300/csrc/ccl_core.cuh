@@ -508,7 +508,7 @@ __device__ __forceinline__ bool mbar_test(unsigned long long* bar, unsigned pari
 // Warp-specialised executor.  Four roles per CTA:
 //
 //  * issuer (warp 0, lane 0) walks the threadblock program.  Step records
-//    (128 bytes each) arrive by cp.async in batches of kLook, one batch
+//    (144 bytes each) arrive by cp.async in batches of kLook, one batch
 //    ahead.  It waits (bounded) for the first slot of up to kLook coming
 //    steps -- incoming slot full, outgoing slot free -- and for their first
 //    kDepPoll dependency counters, polling all those words with relaxed

@@ -28,8 +28,8 @@ enum : int { STEP_NOPOST = 1, STEP_SRC_STREAM = 2, STEP_LOC_STREAM = 4 };
 // what a failed wait was waiting for (status word [3])
 enum WaitReason : int { WAIT_DEP = 1, WAIT_FULL = 2, WAIT_FREE = 3, WAIT_DONE = 4 };
 
-// Everything the executor needs for one step, denormalised (one 128-byte
-// record per step, so the control warp prefetches a step with one load).
+// Everything the executor needs for one step, denormalised (one 144-byte
+// record per step, prefetched as one group of 16-byte asynchronous copies).
 struct DRec {
     int kind, dtype, link_in, link_out;
     int src_buf, src_rank, loc_buf, loc_rank, dst_buf, dst_rank;
