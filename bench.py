@@ -411,6 +411,9 @@ def run_gpu(args):
 
     e2e_pass()   # warm
     torch.cuda.synchronize()
+    # the host link just before and just after the end-to-end steps (the
+    # host side of a shared machine changes from minute to minute)
+    link_before = host_link(torch, items, stream)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for s in e2e_streams[1:]:
@@ -461,10 +464,14 @@ def run_gpu(args):
         "e2e": {"value": round(sched_bytes / (e2e_ms * 1e6), 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3), "steps": Ke,
                 "mode": args.e2e_mode, "streams": len(e2e_streams),
-                # the same host buffers copied alone (no kernels): the floor of
-                # ms_per_step is max(h2d, d2h) bytes / these rates
+                # the same host buffers copied alone (no kernels), just after
+                # and just before the end-to-end steps: ms_per_step cannot be
+                # below either probe's floor_ms (the slowest of one way in, one
+                # way out and both at once); the floor reported is the higher
+                # of the two
                 "host_link_gbs": link,
-                "floor_ms_from_link": round(max(h2d, d2h) / (link["both_each_way"] * 1e6), 3)
+                "host_link_before_gbs": link_before,
+                "floor_ms_from_link": max(link.get("floor_ms", 0), link_before.get("floor_ms", 0))
                 if link.get("both_each_way") else None},
         # bytes every collective must move at least (each input read once,
         # each output written once) per second of the step: unlike `value`,
@@ -528,8 +535,11 @@ def host_link(torch, items, stream):
         copy_out()
     timed(both)   # first touch of the copy paths, not counted
     t_in, t_out, t_both = timed(copy_in), timed(copy_out), timed(both)
+    # the end-to-end step cannot be shorter than either direction alone or
+    # than both at once
     return {"h2d": round(h2d / (t_in * 1e6), 1), "d2h": round(d2h / (t_out * 1e6), 1),
-            "both_each_way": round(max(h2d, d2h) / (t_both * 1e6), 1)}
+            "both_each_way": round(max(h2d, d2h) / (t_both * 1e6), 1),
+            "floor_ms": round(max(t_in, t_out, t_both), 3)}
 
 
 # The message-size sweep: ring AllGather and ReduceScatter, 8 ranks, bf16,
