@@ -343,14 +343,18 @@ void pack_state_based(const ccl_schedule& s, const Timeline& tl, TBList* tbs, st
     }
 }
 
-// Balanced allocation: threadblocks that run only link-free instructions
-// (local copies, direct copies: no FIFO, so any number of them may share a
-// threadblock) are merged into at most `cap` threadblocks, largest first into
-// the least loaded (bytes in chunk units).  A link-free instruction needs no
-// particular rank's threadblock, so the bins take threadblocks of every rank;
-// inside a bin instructions run by sub-pipeline (a dependent task always has
-// a later one), then program position.  The rank of a merged threadblock is
-// that of its largest part (reporting only).
+// Balanced allocation: the instructions of threadblocks that run only
+// link-free instructions (local copies, direct copies: no FIFO, so any number
+// of them may share a threadblock, and one threadblock's may be split) are
+// spread over at most `cap` threadblocks, largest first into the least
+// loaded (bytes in chunk units).  A link-free instruction needs no particular
+// rank's threadblock, so the bins take instructions of every rank; inside a
+// bin instructions run longest dependent chain first, then by sub-pipeline
+// and program position.  Binning instructions rather than whole
+// threadblocks matters when there are a few more threadblocks than bins
+// (21 connections of 8 parts over 19 bins: two bins would carry 16 parts,
+// the rest about 9).  The rank of a merged threadblock is that of its
+// largest part (reporting only).
 void balance_linkfree(const ccl_schedule& s, const Timeline& tl, TBList* tbs, std::vector<int>* tb_rank, int cap)
 {
     struct B { int rank; std::vector<int> instrs; int64_t load; int64_t top; };
@@ -362,30 +366,58 @@ void balance_linkfree(const ccl_schedule& s, const Timeline& tl, TBList* tbs, st
         if (link_free) free_tbs.push_back((int)t);
         else out.push_back(B{(*tb_rank)[t], (*tbs)[t], 0, 0});
     }
-    auto weight = [&](int t) {
-        int64_t w = 0;
-        for (int i : (*tbs)[t]) w += s.instrs[i].count;
-        return w;
-    };
     if ((int)free_tbs.size() <= cap) {
         for (int t : free_tbs) out.push_back(B{(*tb_rank)[t], (*tbs)[t], 0, 0});
     } else {
-        std::stable_sort(free_tbs.begin(), free_tbs.end(), [&](int a, int b) { return weight(a) > weight(b); });
+        std::vector<std::pair<int, int>> items;   // (instruction, rank)
+        for (int t : free_tbs)
+            for (int i : (*tbs)[t]) items.push_back({i, (*tb_rank)[t]});
+        std::stable_sort(items.begin(), items.end(), [&](const std::pair<int, int>& a, const std::pair<int, int>& b) {
+            return s.instrs[a.first].count > s.instrs[b.first].count;
+        });
         std::vector<B> bins(cap, B{-1, {}, 0, 0});
-        for (int t : free_tbs) {
+        for (const auto& it : items) {
             int k = 0;
             for (int b = 1; b < cap; ++b)
                 if (bins[b].load < bins[k].load) k = b;
-            const int64_t w = weight(t);
-            bins[k].instrs.insert(bins[k].instrs.end(), (*tbs)[t].begin(), (*tbs)[t].end());
+            const int64_t w = s.instrs[it.first].count;
+            bins[k].instrs.push_back(it.first);
             bins[k].load += w;
             if (w > bins[k].top) {
                 bins[k].top = w;
-                bins[k].rank = (*tb_rank)[t];
+                bins[k].rank = it.second;
+            }
+        }
+        // inside a bin, the instructions with the longest chain of
+        // dependent instructions after them first (a relay's first hop
+        // before a large independent copy: the copy would hold the chain
+        // back); a producer's chain is longer than its consumer's, so the
+        // order respects dependencies in and across bins
+        const int ni = (int)s.instrs.size();
+        std::vector<std::vector<int>> pred(ni);
+        std::vector<int> nsucc(ni, 0);
+        auto edge = [&](int a, int b) {
+            pred[b].push_back(a);
+            ++nsucc[a];
+        };
+        for (const Dep& e : s.deps) edge(e.from, e.to);
+        for (const Xfer& X : s.xfers)
+            if (X.send_instr >= 0 && X.recv_instr >= 0) edge(X.send_instr, X.recv_instr);
+        // from the sinks back (the graph is acyclic: the timeline was built)
+        std::vector<int> height(ni, 0), todo;
+        for (int i = 0; i < ni; ++i)
+            if (nsucc[i] == 0) todo.push_back(i);
+        while (!todo.empty()) {
+            const int j = todo.back();
+            todo.pop_back();
+            for (int i : pred[j]) {
+                height[i] = std::max(height[i], height[j] + 1);
+                if (--nsucc[i] == 0) todo.push_back(i);
             }
         }
         for (auto& b : bins) {
             std::sort(b.instrs.begin(), b.instrs.end(), [&](int a, int c) {
+                if (height[a] != height[c]) return height[a] > height[c];
                 if (tl.sp_key[a] != tl.sp_key[c]) return tl.sp_key[a] < tl.sp_key[c];
                 if (s.instrs[a].position != s.instrs[c].position)
                     return s.instrs[a].position < s.instrs[c].position;
