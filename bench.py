@@ -61,9 +61,11 @@ SUITE = [
     ("ring_f32", 0, 8, 0, 0, 32 * MiB, "normal", 4,
      dict(fuse="nochain", link_mode=1, channels=24, slot_bytes=131072, microbatches=16, fifo_slots=4, tb_alloc=2,
           tb_budget=192, fold=7)),
-    # relay hops as plain direct copies (no fusion into FIFO forwards)
+    # relay hops as plain direct copies (no fusion into FIFO forwards); the
+    # link-free copies binned into 144 threadblocks, one per SM (the
+    # 512-thread build)
     ("a2n", 5, 24, 8, 0, 16 * MiB, "normal", 4,
-     dict(fuse=False, channels=16, link_mode=1, microbatches=8, tb_alloc=2, tb_budget=304, channel_scaling=0)),
+     dict(fuse=False, channels=16, link_mode=1, microbatches=16, tb_alloc=2, tb_budget=152, channel_scaling=0)),
     ("ag_3m", 1, 8, 0, 1, 3 * MiB // 8, "normal", 1,
      # every hop a direct copy into the next rank's output (no FIFO), the
      # first one in the same pass as the rank's own block (a copy-send with
