@@ -32,7 +32,7 @@ LINK_FIFO, LINK_DIRECT = 0, 1
 PROTO_SIMPLE, PROTO_LL = 0, 1
 ENGINE_PIPELINED, ENGINE_SEQUENTIAL = 0, 1
 KIND_NAMES = ["copy", "reduce", "send", "recv", "rrc", "rcs", "fwd", "rrs", "rrcs", "copy_send", "copy2", "rrc2",
-              "rrs3", "rrc3", "rrcs3", "rsend", "rcsend", "rrc3d", "reduce2"]
+              "rrs3", "rrc3", "rrcs3", "rsend", "rcsend", "rrc3d", "reduce2", "copy3"]
 DTYPE_NAMES = {F32: "f32", BF16: "bf16", F16: "f16", I32: "i32"}
 ESIZE = {F32: 4, BF16: 2, F16: 2, I32: 4}
 

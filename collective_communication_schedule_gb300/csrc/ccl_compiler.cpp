@@ -54,6 +54,7 @@ int64_t kind_bytes_factor(int kind)
     case CCL_I_RCSEND: return 4;
     case CCL_I_RRC3D: return 5;
     case CCL_I_REDUCE2: return 4;
+    case CCL_I_COPY3: return 4;
     default: return 0;
     }
 }

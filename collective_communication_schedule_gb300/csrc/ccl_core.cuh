@@ -348,6 +348,63 @@ __device__ __noinline__ void move_part3_call(int dtype, const char* a, bool as, 
     move_part3<U>(dtype, a, as, b, bs, c, cs, o1, o1s, o2, n, tid, T);
 }
 
+// A copy to three destinations (a folded chain of three direct copies):
+// 16-byte vectors when every address allows, else elements of es bytes.
+// Inlined into the sequential engine's step; the pipelined engine's data
+// warps call it out of line (copy3_call), which keeps their registers.
+__device__ __forceinline__ void copy3_part(const char* a, char* o1, char* o2, char* o3, long long n, int es, int tid,
+                                           int T)
+{
+    const unsigned long long al = (unsigned long long)a | (unsigned long long)o1 | (unsigned long long)o2 |
+                                  (unsigned long long)o3;
+    const long long ve = 16 / es;
+    long long nv = 0;
+    if ((al & 15) == 0) {
+        nv = n / ve;
+        const uint4* va = reinterpret_cast<const uint4*>(a);
+        uint4* v1 = reinterpret_cast<uint4*>(o1);
+        uint4* v2 = reinterpret_cast<uint4*>(o2);
+        uint4* v3 = reinterpret_cast<uint4*>(o3);
+        long long i = tid;
+        for (; i + 3 * (long long)T < nv; i += 4 * (long long)T) {
+            uint4 r[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) r[u] = __ldcg(va + i + u * T);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                __stcg(v1 + i + u * T, r[u]);
+                __stcg(v2 + i + u * T, r[u]);
+                __stcg(v3 + i + u * T, r[u]);
+            }
+        }
+        for (; i < nv; i += T) {
+            const uint4 r = __ldcg(va + i);
+            __stcg(v1 + i, r);
+            __stcg(v2 + i, r);
+            __stcg(v3 + i, r);
+        }
+    }
+    for (long long i = nv * ve + tid; i < n; i += T) {
+        if (es == 4) {
+            const unsigned x = __ldcg(reinterpret_cast<const unsigned*>(a) + i);
+            __stcg(reinterpret_cast<unsigned*>(o1) + i, x);
+            __stcg(reinterpret_cast<unsigned*>(o2) + i, x);
+            __stcg(reinterpret_cast<unsigned*>(o3) + i, x);
+        } else {
+            const unsigned short x = __ldcg(reinterpret_cast<const unsigned short*>(a) + i);
+            __stcg(reinterpret_cast<unsigned short*>(o1) + i, x);
+            __stcg(reinterpret_cast<unsigned short*>(o2) + i, x);
+            __stcg(reinterpret_cast<unsigned short*>(o3) + i, x);
+        }
+    }
+}
+
+static __device__ __noinline__ void copy3_call(const char* a, char* o1, char* o2, char* o3, long long n, int es, int tid,
+                                        int T)
+{
+    copy3_part(a, o1, o2, o3, n, es, tid, T);
+}
+
 // kinds that reduce, and those that take a third operand (held in the
 // source range)
 __device__ __forceinline__ bool kind_reduces(int k)
@@ -553,6 +610,7 @@ struct SlotOp {
     const char* c;      // third operand (a folded reduction chain), or null
     char* o1;           // destination buffer, or the outgoing slot
     char* o2;           // outgoing slot when a destination is also written
+    char* o3;           // third destination (a folded chain of three copies), or null
     long long n;        // elements
     int red, dtype;
     int as, bs, cs, o1s;   // streaming cache hints (register path)
@@ -1005,8 +1063,9 @@ __device__ __forceinline__ bool issue_step(const KParams& P, CtlShared* sh, cons
             // a two-destination copy keeps its second destination in the
             // local-operand range
             // (a folded recv-reduce-copy-send: in its source range)
-            const bool copy2 = st.kind == CCL_I_COPY2, rrc2 = st.kind == CCL_I_RRC2;
+            const bool copy2 = st.kind == CCL_I_COPY2 || st.kind == CCL_I_COPY3, rrc2 = st.kind == CCL_I_RRC2;
             op.b = locb && !copy2 ? locb + off : nullptr;
+            op.o3 = st.kind == CCL_I_COPY3 ? P.bufs[st.x_buf][st.x_rank] + st.x_off * es + off : nullptr;
             op.bs = (st.flags & STEP_LOC_STREAM) && P.stream_in;
             // a folded reduction chain's third operand: its source range
             op.c = three && srcb ? srcb + off : nullptr;
@@ -1033,7 +1092,7 @@ __device__ __forceinline__ bool issue_step(const KParams& P, CtlShared* sh, cons
             op.n = tn;
             op.red = red;
             op.dtype = st.dtype;
-            op.bulk = P.ns > 0 && !red && tn > 0 && ((tn * es) & 15) == 0 && aligned16(op.a) &&
+            op.bulk = P.ns > 0 && !red && !op.o3 && tn > 0 && ((tn * es) & 15) == 0 && aligned16(op.a) &&
                       aligned16(op.o1) && (!op.o2 || aligned16(op.o2)) && !op.a_ll && !op.o1_ll && !op.o2_ll;
             op.cmd = 0;
             Release& r = sh->rel[q];
@@ -1489,6 +1548,8 @@ static __device__ void data_warps(const KParams& P, CtlShared* sh)
                 }
                 if (!ok) record_timeout(P, -1, WAIT_FULL);
             }
+        } else if (!op.bulk && op.n > 0 && op.o3) {
+            copy3_call(op.a, op.o1, op.o2, op.o3, op.n, (op.dtype == CCL_BF16 || op.dtype == CCL_F16) ? 2 : 4, tid, T);
         } else if (!op.bulk && op.n > 0 && op.c) {
             move_part3_call<U>(op.dtype, op.a, op.as, op.b, op.bs, op.c, op.cs, op.o1, op.o1s, op.o2, op.n, tid, T);
         } else if (!op.bulk && op.n > 0) {
@@ -1645,7 +1706,7 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
         // a two-destination copy keeps its second destination in the
         // local-operand range
         // (a folded recv-reduce-copy-send: in its source range)
-        const bool copy2 = st.kind == CCL_I_COPY2, rrc2 = st.kind == CCL_I_RRC2;
+        const bool copy2 = st.kind == CCL_I_COPY2 || st.kind == CCL_I_COPY3, rrc2 = st.kind == CCL_I_RRC2;
         const char* b = locb && !copy2 ? locb + e0 * es : nullptr;
         if (n > 0) {
             prefetch_l2(a, n * es, tid, T);
@@ -1699,6 +1760,7 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
                 op.b = b;
                 op.c = nullptr;   // no folded reduction chains with LL slots
                 op.cs = 0;
+                op.o3 = nullptr;
                 op.o1 = o1;
                 op.o2 = o2;
                 op.n = n;
@@ -1717,6 +1779,8 @@ __device__ __forceinline__ void seq_step(const KParams& P, int* go, const DRec& 
                 // after a recorded failure the part is skipped; the leader
                 // sees the status before its next wait
                 if (*(volatile int*)P.status == 0 && !seq_move_ll(op, tid, T, P)) record_timeout(P, si, WAIT_FULL);
+            } else if (st.kind == CCL_I_COPY3) {
+                copy3_part(a, o1, o2, P.bufs[st.x_buf][st.x_rank] + (st.x_off + e0) * es, n, es, tid, T);
             } else if (three) {
                 move_part3<U>(st.dtype, a, as, b, bs, srcb + e0 * es, (st.flags & STEP_SRC_STREAM) && P.stream_in, o1,
                               o1s, o2, n, tid, T);

@@ -14,7 +14,7 @@ enum {
     CCL_I_COPY = 0, CCL_I_REDUCE = 1, CCL_I_SEND = 2, CCL_I_RECV = 3, CCL_I_RRC = 4,
     CCL_I_RCS = 5, CCL_I_FWD = 6, CCL_I_RRS = 7, CCL_I_RRCS = 8, CCL_I_COPY_SEND = 9, CCL_I_COPY2 = 10,
     CCL_I_RRC2 = 11, CCL_I_RRS3 = 12, CCL_I_RRC3 = 13, CCL_I_RRCS3 = 14, CCL_I_RSEND = 15, CCL_I_RCSEND = 16,
-    CCL_I_RRC3D = 17, CCL_I_REDUCE2 = 18
+    CCL_I_RRC3D = 17, CCL_I_REDUCE2 = 18, CCL_I_COPY3 = 19
 };
 enum { CCL_ERR_TIMEOUT = 8 };
 #define CCL_MAX_RANKS 64

@@ -1050,14 +1050,16 @@ ccl_schedule direct_transport(const ccl_schedule& s, int* ndirect, bool fold)
 // unchanged, exactly the range another direct copy c1 wrote into c2's rank
 // is run by c1's pass instead -- one read written to both destinations (a
 // CCL_I_COPY2 holding the second destination in its local-operand range)
-// instead of c1's write and c2's read-back and write.  A ring AllGather's
-// k copy hops become ceil(k/2) steps.  c1 takes over c2's dependencies in
+// instead of c1's write and c2's read-back and write; with depth 3 the copy
+// that forwards the second destination joins as well (a CCL_I_COPY3, its
+// third destination in the x range).  A ring AllGather's k copy hops become
+// ceil(k/2) (ceil(k/3)) steps.  c1 takes over c2's dependencies in
 // both directions; c2's writes then happen at c1's time, which is sound
 // when every instruction c2 waited for can come before c1 -- a pair whose
 // merged dependencies would close a cycle is left alone.  Pairs are formed
 // in dependency order (smallest index first among the ready ones), so each
 // chain pairs up from its head.
-int fold_copy_chains(ccl_schedule& d)
+int fold_copy_chains(ccl_schedule& d, int depth)
 {
     const int ni = (int)d.instrs.size();
     std::vector<std::set<int>> succ(ni), pred(ni);
@@ -1097,47 +1099,62 @@ int fold_copy_chains(ccl_schedule& d)
     int nfold = 0, epoch = 0;
     for (int c1 : order) {
         if (gone[c1] || !direct_copy(c1)) continue;
-        const Instr& A = d.instrs[c1];
-        for (int c2 : std::vector<int>(succ[c1].begin(), succ[c1].end())) {
-            if (gone[c2] || !direct_copy(c2)) continue;
-            const Instr& B = d.instrs[c2];
-            if (!B.src.same(A.dst) || B.count != A.count || B.dst.overlaps(A.src) || B.dst.overlaps(A.dst)) continue;
-            // every other instruction c2 waits for must not follow c1
-            std::vector<int> stack{c1};
-            bool cycle = false;
-            mark[c1] = ++epoch;
-            while (!stack.empty() && !cycle) {
-                const int v = stack.back();
-                stack.pop_back();
-                for (int w : succ[v]) {
-                    if (w == c2 || mark[w] == epoch) continue;
-                    if (pred[c2].count(w)) { cycle = true; break; }
-                    mark[w] = epoch;
-                    stack.push_back(w);
+        // up to `depth` destinations: each fold takes the copy that forwards
+        // the step's last destination
+        for (int held = 1; held < depth; ++held) {
+            const Instr& A = d.instrs[c1];
+            const Range last = held == 1 ? A.dst : A.loc;
+            bool folded = false;
+            for (int c2 : std::vector<int>(succ[c1].begin(), succ[c1].end())) {
+                if (gone[c2] || !direct_copy(c2)) continue;
+                const Instr& B = d.instrs[c2];
+                if (!B.src.same(last) || B.count != A.count || B.dst.overlaps(A.src) || B.dst.overlaps(A.dst) ||
+                    (held == 2 && B.dst.overlaps(A.loc)))
+                    continue;
+                // every other instruction c2 waits for must not follow c1
+                std::vector<int> stack{c1};
+                bool cycle = false;
+                mark[c1] = ++epoch;
+                while (!stack.empty() && !cycle) {
+                    const int v = stack.back();
+                    stack.pop_back();
+                    for (int w : succ[v]) {
+                        if (w == c2 || mark[w] == epoch) continue;
+                        if (pred[c2].count(w)) { cycle = true; break; }
+                        mark[w] = epoch;
+                        stack.push_back(w);
+                    }
                 }
+                if (cycle) continue;
+                Instr& F = d.instrs[c1];
+                if (held == 1) {
+                    F.kind = CCL_I_COPY2;
+                    F.loc = B.dst;
+                } else {
+                    F.kind = CCL_I_COPY3;
+                    F.x = B.dst;
+                }
+                for (int x : std::vector<int>(pred[c2].begin(), pred[c2].end())) {
+                    const int ex = exact[{x, c2}];
+                    succ[x].erase(c2);
+                    if (x == c1) continue;
+                    if (ex & 1) add_edge(x, c1, true);
+                    if (ex & 2) add_edge(x, c1, false);
+                }
+                for (int y : std::vector<int>(succ[c2].begin(), succ[c2].end())) {
+                    const int ex = exact[{c2, y}];
+                    pred[y].erase(c2);
+                    if (ex & 1) add_edge(c1, y, true);
+                    if (ex & 2) add_edge(c1, y, false);
+                }
+                pred[c2].clear();
+                succ[c2].clear();
+                gone[c2] = 1;
+                ++nfold;
+                folded = true;
+                break;
             }
-            if (cycle) continue;
-            Instr& F = d.instrs[c1];
-            F.kind = CCL_I_COPY2;
-            F.loc = B.dst;
-            for (int x : std::vector<int>(pred[c2].begin(), pred[c2].end())) {
-                const int ex = exact[{x, c2}];
-                succ[x].erase(c2);
-                if (x == c1) continue;
-                if (ex & 1) add_edge(x, c1, true);
-                if (ex & 2) add_edge(x, c1, false);
-            }
-            for (int y : std::vector<int>(succ[c2].begin(), succ[c2].end())) {
-                const int ex = exact[{c2, y}];
-                pred[y].erase(c2);
-                if (ex & 1) add_edge(c1, y, true);
-                if (ex & 2) add_edge(c1, y, false);
-            }
-            pred[c2].clear();
-            succ[c2].clear();
-            gone[c2] = 1;
-            ++nfold;
-            break;
+            if (!folded) break;
         }
     }
     if (!nfold) return 0;
@@ -1333,7 +1350,7 @@ ccl_status_t build_plan_one(const ccl_schedule& s_in, int64_t ce, int32_t dtype,
     if (o.protocol == CCL_PROTO_LL && (ce * esize_of(dtype)) % 16)
         return fail(CCL_ERR_UNSUPPORTED, "the LL protocol needs chunks of a multiple of 16 bytes");
     if (o.timeout_ms <= 0) return fail(CCL_ERR_INVALID_ARG, "timeout_ms must be positive");
-    if (o.fold < 0 || o.fold > 7) return fail(CCL_ERR_INVALID_ARG, "fold must be in 0..7");
+    if (o.fold < 0 || o.fold > 15) return fail(CCL_ERR_INVALID_ARG, "fold must be in 0..15");
 
     if (o.link_mode != CCL_LINK_FIFO && o.link_mode != CCL_LINK_DIRECT)
         return fail(CCL_ERR_INVALID_ARG, "unknown link_mode");
@@ -1345,7 +1362,8 @@ ccl_status_t build_plan_one(const ccl_schedule& s_in, int64_t ce, int32_t dtype,
         // operand), then plain transfers and receive folds, then copy chains
         if ((fold & 4) && o.protocol != CCL_PROTO_LL) fold_reduce_chains(s);
         s = direct_transport(s, &ndirect, (fold & 1) != 0);
-        if (fold & 2) fold_copy_chains(s);
+        // copy chains: two hops per step (bit 1), three (bit 3)
+        if (fold & 10) fold_copy_chains(s, (fold & 8) ? 3 : 2);
     }
     const int es = esize_of(dtype);
     Timeline tl;

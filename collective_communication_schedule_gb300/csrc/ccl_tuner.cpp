@@ -10,7 +10,8 @@
 // Grids: channels {1,2,4,8,12,16,24,32,48}, threads {128,256,512,1024},
 // slot size 16 KiB .. 4 MiB in powers of two, on the sequential engine
 // CTAs per threadblock program {1,2,4,8}, and with direct transport each
-// fold bit {0,1} (receives into senders, copy chains, reduction chains).  A probe is the median of
+// fold bit {0,1} (receives into senders, copy chains, reduction chains,
+// three-hop copy chains).  A probe is the median of
 // `reps` CUDA-event-timed executions after one warm-up; a point whose plan
 // cannot be built (threadblocks not co-resident, FIFO too small) scores 0.
 #include <cuda_runtime.h>
@@ -173,25 +174,25 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
         const bool seq = cur.engine == CCL_ENGINE_SEQUENTIAL;
         const std::vector<int> gk = seq ? std::vector<int>{1, 2, 4, 8} : std::vector<int>{1};
         if (!seq) cur.cluster = 0;
-        // direct transport also chooses its folds: each of the three fold
-        // bits (receives, copy chains, reduction chains) a coordinate of its
-        // own with the values 0 and 1
+        // direct transport also chooses its folds: each of the four fold
+        // bits (receives, copy chains, reduction chains, three-hop copy
+        // chains) a coordinate of its own with the values 0 and 1
         const bool direct = cur.link_mode == CCL_LINK_DIRECT;
         int ic = nearest(gc, cur.channels), it = nearest(gt, cur.nthreads), is = nearest(gs, cur.slot_bytes);
         int ik = seq ? nearest(gk, std::max(1, cur.cluster)) : 0;
-        int fb[3] = {cur.fold & 1, (cur.fold >> 1) & 1, (cur.fold >> 2) & 1};
+        int fb[4] = {cur.fold & 1, (cur.fold >> 1) & 1, (cur.fold >> 2) & 1, (cur.fold >> 3) & 1};
         auto eval = [&](int c, int t, int sl, int k, const int* f) {
             ccl_plan_opts_t o = cur;
             o.channels = gc[c];
             o.nthreads = gt[t];
             o.slot_bytes = gs[sl];
             o.cluster = gk[k] > 1 ? gk[k] : 0;
-            if (direct) o.fold = f[0] | (f[1] << 1) | (f[2] << 2);
+            if (direct) o.fold = f[0] | (f[1] << 1) | (f[2] << 2) | (f[3] << 3);
             return measure(o);
         };
         std::vector<int> coords{0, 1, 2};
         if (seq) coords.push_back(3);
-        if (direct) for (int b = 0; b < 3; ++b) coords.push_back(4 + b);
+        if (direct) for (int b = 0; b < 4; ++b) coords.push_back(4 + b);
         double bw = eval(ic, it, is, ik, fb);
         for (int round = 0; round < to.max_rounds; ++round) {
             bool moved = false;
@@ -201,7 +202,7 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
                         : coord == 3 ? (int)gk.size() : 2;
                 auto at = [&](int v) {
                     if (coord >= 4) {
-                        int f[3] = {fb[0], fb[1], fb[2]};
+                        int f[4] = {fb[0], fb[1], fb[2], fb[3]};
                         f[coord - 4] = v;
                         return eval(ic, it, is, ik, f);
                     }
@@ -234,7 +235,7 @@ extern "C" ccl_status_t ccl_tune_search(const ccl_plan_opts_t* start, const ccl_
             overall.nthreads = gt[it];
             overall.slot_bytes = gs[is];
             overall.cluster = gk[ik] > 1 ? gk[ik] : 0;
-            if (direct) overall.fold = fb[0] | (fb[1] << 1) | (fb[2] << 2);
+            if (direct) overall.fold = fb[0] | (fb[1] << 1) | (fb[2] << 2) | (fb[3] << 3);
         }
     }
     *best = overall;

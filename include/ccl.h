@@ -141,7 +141,8 @@ typedef enum {
     /* and with the plain receive that the last two feed folded in (a
        second destination x, the receiver's, instead of the slot): */
     CCL_I_RRC3D = 17,    /* t <- (slot_in (+) local) (+) src; dst <- t; x <- t */
-    CCL_I_REDUCE2 = 18   /* t <- src (+) local; dst <- t; x <- t */
+    CCL_I_REDUCE2 = 18,  /* t <- src (+) local; dst <- t; x <- t */
+    CCL_I_COPY3 = 19     /* dst <- src; loc <- src; x <- src  (a chain of three direct copies) */
 } ccl_instr_kind_t;
 
 typedef struct {
@@ -355,14 +356,17 @@ typedef enum {
  *                 on where the second one sent; with bit 0 the plain
  *                 receive such a step feeds is folded into it as a second
  *                 destination (CCL_I_RRC3D, CCL_I_REDUCE2); not with the LL
- *                 protocol.  Not in the
+ *                 protocol.  Bit 3 (8): copy chains three hops per step
+ *                 (CCL_I_COPY3, its third destination in the fourth range:
+ *                 one read written three times, 4 bytes per element byte
+ *                 instead of 2 + 2 + 2).  Bit 2 is not in the
  *                 default: where a chain's other hops stay one rank apart
  *                 (a fully fused ring AllReduce's all-gather) a rank then
  *                 needs links one and two ranks away and more
  *                 threadblocks; with the all-gather hops direct (copy
  *                 receives unchained) it does not.  A folded plan
  *                 that would cycle or deadlock is planned again without
- *                 folds.  Values outside 0..7: CCL_ERR_INVALID_ARG.
+ *                 folds.  Values outside 0..15: CCL_ERR_INVALID_ARG.
  *   codegen     : 0 (default): the library's kernels interpret the plan's
  *                 step records.  1: ccl_plan_create generates CUDA source
  *                 for this one plan (ReSCCL report, §II.2: a kernel per
@@ -400,7 +404,7 @@ typedef struct {
     int32_t codegen;     /* 1: run a kernel generated and compiled for this plan (see below) */
     int32_t cluster;     /* sequential engine: CTAs per threadblock program (0 or 1: one; 2, 4, 8) */
     int32_t fold;        /* direct transport: bit 0 folds plain receives into their senders, bit 1
-                            copy chains, bit 2 reduction chains (default 3) */
+                            copy chains, bit 2 reduction chains, bit 3 three-hop copy chains (default 3) */
 } ccl_plan_opts_t;
 
 void ccl_plan_opts_default(ccl_plan_opts_t* o);

@@ -196,16 +196,18 @@ def _fused_halves(ops, nranks, fuse):
     return [h for h in halves if h.alive]
 
 
-def _chain_folds(halves):
+def _chain_folds(halves, depth=2):
     """Element chunks saved by folding copy chains under direct transport.
 
     A direct copy is a plain send whose transfer ends in a plain receive.
     When a later direct copy sends on, unchanged, exactly the range an
     earlier one received, the earlier copy's pass writes both destinations:
-    one read written twice (3) instead of 2 + 2.  A copy that has taken one
-    over writes two places already and takes no other; the transfers are
-    visited in program order, so a chain pairs up from its head.  The
-    second copy's destination must not overlap the first one's ranges."""
+    one read written twice (3) instead of 2 + 2; with ``depth`` 3 the copy
+    that forwards that second destination joins too (one read written three
+    times, 4 instead of 2 + 2 + 2).  A step holds at most ``depth``
+    destinations and each copy it takes over saves 1; the transfers are
+    visited in program order, so a chain groups up from its head.  A copy
+    taken over must not write over the step's other ranges."""
     sends = {h.send: h for h in halves if h.send is not None}
     recvs = {h.recv: h for h in halves if h.recv is not None}
     direct = sorted(t for t, h in sends.items() if h.kind() == "send" and recvs[t].kind() == "recv")
@@ -216,20 +218,28 @@ def _chain_folds(halves):
     for t1 in direct:
         if t1 in gone:
             continue
-        s1, r1 = sends[t1], recvs[t1]
-        for t2 in direct:
-            if t2 <= t1 or t2 in gone:
-                continue
-            s2, r2 = sends[t2], recvs[t2]
-            if s2.rank != r1.rank or s2.src != r1.dst or s2.count != r1.count:
-                continue
-            if _overlap(r2.dst, s1.src) or _overlap(r2.dst, r1.dst):
-                continue
-            if not _unchanged(by_rank[r1.rank], r1.dst, r1.pos, s2.pos):
-                continue
-            gone.add(t2)
-            saved += r1.count
-            break
+        s1, last = sends[t1], recvs[t1]
+        ranges = [s1.src, last.dst]
+        for _ in range(depth - 1):
+            found = None
+            for t2 in direct:
+                if t2 <= t1 or t2 in gone:
+                    continue
+                s2, r2 = sends[t2], recvs[t2]
+                if s2.rank != last.rank or s2.src != last.dst or s2.count != last.count:
+                    continue
+                if any(_overlap(r2.dst, r) for r in ranges):
+                    continue
+                if not _unchanged(by_rank[last.rank], last.dst, last.pos, s2.pos):
+                    continue
+                found = t2
+                break
+            if found is None:
+                break
+            gone.add(found)
+            saved += last.count
+            last = recvs[found]
+            ranges.append(last.dst)
     return saved
 
 
@@ -270,7 +280,8 @@ def schedule_bytes(ops, nranks, nchunks, chunk_elems, dtype, fuse="full", direct
     2 -> one copy of 2; copy-send 3 + receive 2 -> one read written twice,
     3; recv-reduce-copy-send 4 + receive 2 -> 4).  ``fold`` bit 0 (True)
     takes the last two without their FIFO (cleared: they keep it); bit 1
-    also folds copy chains (``_chain_folds``); bit 2 reduction chains
+    also folds copy chains two hops per step (``_chain_folds``), bit 3
+    three; bit 2 reduction chains
     (``_reduce_chain_folds``; the receive fed by a recv-reduce-copy-send
     taken into a pair is folded into the pair's step the same way)."""
     halves = _fused_halves(ops, nranks, fuse)
@@ -287,8 +298,8 @@ def schedule_bytes(ops, nranks, nchunks, chunk_elems, dtype, fuse="full", direct
             # writes the receiver's buffer itself)
             if s.kind() == "send" or (int(fold) & 1 and s.kind() in ("copy_send", "rrcs")):
                 units -= 2 * h.count
-        if int(fold) & 2:
-            units -= _chain_folds(halves)
+        if int(fold) & 10:
+            units -= _chain_folds(halves, 3 if int(fold) & 8 else 2)
     return units * int(chunk_elems) * ESIZE[dtype]
 
 

@@ -98,7 +98,7 @@ def test_binding_constants_match_the_header():
         assert vals["I_" + name.upper()] == i, name
     # the compiler's kinds, then the kinds only plans contain (direct
     # transport's folds)
-    plan_only = ["copy2", "rrc2", "rrs3", "rrc3", "rrcs3", "rsend", "rcsend", "rrc3d", "reduce2"]
+    plan_only = ["copy2", "rrc2", "rrs3", "rrc3", "rrcs3", "rsend", "rcsend", "rrc3d", "reduce2", "copy3"]
     assert vals["I_NKINDS"] == len(ccl.KIND_NAMES) - len(plan_only) and ccl.KIND_NAMES[vals["I_NKINDS"]:] == plan_only
 
 

@@ -486,7 +486,7 @@ def test_coordinate_descent_plateau_stops_early():
     # sixteen subspaces (policy x protocol x transport x engine): on a flat
     # surface each tries one step up and one down per coordinate (at most 6
     # probes; 8 on the sequential engine, which also has the CTAs per
-    # program; 3 more with direct transport, one flip of each fold bit),
+    # program; 4 more with direct transport, one flip of each fold bit),
     # plus the start
     seen = set()
 
@@ -494,7 +494,7 @@ def test_coordinate_descent_plateau_stops_early():
         seen.add((o.tb_alloc, o.protocol, o.link_mode, o.engine))
         return 1.0
     best, bw, n = ccl.tune_search(flat)
-    assert bw == 1.0 and n <= 1 + 8 * 6 + 8 * 8 + 8 * 3
+    assert bw == 1.0 and n <= 1 + 8 * 6 + 8 * 8 + 8 * 4
     assert len(seen) == 16
 
 
@@ -680,13 +680,13 @@ def test_direct_transport_folds_a_copy_send_and_its_receive():
 
 def test_fold_option():
     """fold = 0 keeps the copy-send's FIFO hop (and its bytes); values
-    outside 0..7 are refused; the library default folds receives."""
+    outside 0..15 are refused; the library default folds receives."""
     assert ccl.default_opts().fold & 1
     R, ce = 8, 1024
     s = ccl.Schedule.builtin(ccl.RING_ALLGATHER, R, 0, ccl.FLAG_NOCHAIN_COPIES)
     kept = s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=0)
     assert kept.nlinks == R and kept.schedule_bytes == R * (3 + 2 + 6 * 2) * ce * 4
-    for bad in (-1, 8):
+    for bad in (-1, 16):
         with pytest.raises(ccl.CclError) as e:
             s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=bad)
         assert e.value.code == 1
@@ -741,6 +741,19 @@ def test_direct_transport_folds_copy_chains():
     # FIFO transport: nothing to fold
     assert s.check(ce, F32, link_mode=ccl.LINK_FIFO, fold=3).schedule_bytes == \
         s.check(ce, F32, link_mode=ccl.LINK_FIFO, fold=0).schedule_bytes
+
+
+def test_copy_chains_fold_three_hops_per_step():
+    """fold bit 3: the ring AllGather's chain of 6 direct copies after the
+    folded copy-send becomes 2 three-destination copies: 3 steps per
+    program instead of 4 (7 unfolded), 3 + 2 * 4 bytes per element byte of
+    a chunk instead of 3 + 3 * 3."""
+    R, ce = 8, 1024
+    s = ccl.Schedule.builtin(ccl.RING_ALLGATHER, R, 0, ccl.FLAG_NOCHAIN_COPIES)
+    p3 = s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=3, microbatches=1)
+    p11 = s.check(ce, F32, link_mode=ccl.LINK_DIRECT, fold=11, microbatches=1)
+    assert p3.nsteps == R * 4 and p11.nsteps == R * 3
+    assert p3.schedule_bytes == R * 12 * ce * 4 and p11.schedule_bytes == R * 11 * ce * 4
 
 
 def test_direct_transport_folds_reduction_chains():

@@ -107,6 +107,21 @@ def test_copy_chain_folds_closed_forms(R):
         assert OB.schedule_bytes(ops, R, nch, 100, BF16, "nochain", True, fold) == R * (rs + chain) * n
 
 
+@pytest.mark.parametrize("R", [2, 3, 4, 5, 8, 9])
+def test_copy_chain_folds_three_hops_per_step(R):
+    """fold bit 3: a chain of k direct copies groups into floor(k/3) steps of
+    one read written three times (4 instead of 2 + 2 + 2) and, for k mod 3
+    = 2, a pair (3) or, for k mod 3 = 1, a single copy (2).  Ring AllGather,
+    copy receives unchained, with the copy-send's receive folded (3): a
+    chain of R - 2 copies."""
+    k = R - 2
+    chain = 4 * (k // 3) + {0: 0, 1: 2, 2: 3}[k % 3]
+    ops, nch = OS.ring_allgather(R)
+    n = 100 * 2
+    assert OB.schedule_bytes(ops, R, nch, 100, BF16, "nochain", True, 11) == R * (3 + chain) * n
+    assert OB.schedule_bytes(ops, R, nch, 100, BF16, "nochain", True, 15) == R * (3 + chain) * n
+
+
 def test_copy_chain_folds_of_the_hierarchical_allreduce_and_alltonext():
     """Hierarchical AllReduce (G = 8, 2 groups, copy receives unchained,
     direct): intra reduce-scatter 46 n as above, the inter-group step send 2
@@ -131,7 +146,7 @@ def test_planted_mistake_in_the_chain_fold_is_caught():
     good = OB.schedule_bytes(ops, 8, nch, 10, F32, "nochain", True, 3)
     saved = OB._chain_folds
     try:
-        OB._chain_folds = lambda halves: 2 * saved(halves)
+        OB._chain_folds = lambda halves, depth=2: 2 * saved(halves, depth)
         assert OB.schedule_bytes(ops, 8, nch, 10, F32, "nochain", True, 3) != good
     finally:
         OB._chain_folds = saved
@@ -246,7 +261,8 @@ def test_oracle_count_equals_the_product_count_for_every_benchmark_row():
 @pytest.mark.parametrize("kind,R,G", [(0, 8, 0), (0, 3, 0), (1, 8, 0), (2, 5, 0), (3, 16, 8), (3, 4, 2),
                                       (4, 32, 8), (4, 8, 4), (5, 24, 8), (5, 6, 3)])
 @pytest.mark.parametrize("flags", [0, 2, 4])
-@pytest.mark.parametrize("link_mode,fold", [(0, 1), (1, 1), (1, 0), (1, 2), (1, 3), (1, 4), (1, 5), (1, 6), (1, 7)])
+@pytest.mark.parametrize("link_mode,fold", [(0, 1), (1, 1), (1, 0), (1, 2), (1, 3), (1, 4), (1, 5), (1, 6), (1, 7),
+                                            (1, 10), (1, 15)])
 def test_oracle_count_equals_the_product_count_for_builtins(kind, R, G, flags, link_mode, fold):
     ops, nch = KIND_PROGRAM[kind](R, G)
     st = ccl.Schedule.builtin(kind, R, G, flags).check(333, F32, link_mode=link_mode, fold=fold)
