@@ -65,21 +65,23 @@ SUITE = [
     # link-free copies binned into 144 threadblocks, one per SM (the
     # 512-thread build)
     ("a2n", 5, 24, 8, 0, 16 * MiB, "normal", 4,
-     dict(fuse=False, channels=16, link_mode=1, microbatches=16, tb_alloc=2, tb_budget=152, channel_scaling=0)),
+     dict(fuse=False, channels=16, link_mode=1, microbatches=16, tb_alloc=2, tb_budget=152, channel_scaling=0,
+          fold=15)),
     ("ag_3m", 1, 8, 0, 1, 3 * MiB // 8, "normal", 1,
      # every hop a direct copy into the next rank's output (no FIFO), the
      # first one in the same pass as the rank's own block (a copy-send with
      # its receive folded in); the small collectives run on the sequential
      # engine (fewer hand-offs per step), each program on a cluster of CTAs
      # that share its slots' data
-     dict(fuse="nochain", channels=4, link_mode=1, engine=1, cluster=4, nthreads=256)),
+     # (copy chains three hops per step: 3 steps per program)
+     dict(fuse="nochain", channels=4, link_mode=1, engine=1, cluster=4, nthreads=256, fold=15)),
     # FIFOs at least one execution deep (8 slots): no slot is reused within
     # an execution, so nothing is posted or waited for its consumption
     ("rs_3m", 2, 8, 0, 1, 3 * MiB // 8, "normal", 1, dict(channels=4, engine=1, cluster=4, nthreads=256,
                                                           fifo_slots=8, fold=7)),
     ("ar_1m", 0, 8, 0, 0, 1 * MiB // 8, "uniform", 0, dict(fuse="nochain", link_mode=1, channels=1, tb_alloc=2,
                                                             tb_budget=16, engine=1, cluster=8, nthreads=128,
-                                                            fifo_slots=8, fold=7)),
+                                                            fifo_slots=8, fold=15)),
 ]
 ESIZE = {0: 4, 1: 2, 2: 2, 3: 4}
 NAMES = {0: "f32", 1: "bf16", 2: "f16", 3: "i32"}

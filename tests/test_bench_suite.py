@@ -44,14 +44,18 @@ def test_ring_rows_match_the_closed_form(name):
     units) pair up into floor(R/2) steps that read the next rank's input
     themselves (2 units less each); the receive the completing step feeds
     is folded into it; the R - 2 middle all-gather hops run two at a time (3
-    per pair, 2 for an odd one out)."""
+    per pair, 2 for an odd one out), or three (4 per triple) with fold bit
+    3."""
     row = [r for r in bench.SUITE if r[0] == name][0]
     _, kind, R, G, dt, cb, dist, seed, opts = row
     assert opts.get("fuse") == "nochain" and opts.get("link_mode") == 1
     N = R * cb                       # R chunks of cb bytes per rank
     _, st, _ = _plan(row)
-    assert opts.get("fold", bench.DEFAULT_FOLD) == 7
-    units = 3 * R - 2 * (R // 2) + 3 * ((R - 2) // 2) + 2 * ((R - 2) % 2)
+    fold = opts.get("fold", bench.DEFAULT_FOLD)
+    assert fold & 7 == 7
+    k = R - 2    # all-gather copies: pairs (3 each), or triples (4 each) with bit 3
+    chain = 4 * (k // 3) + (0, 2, 3)[k % 3] if fold & 8 else 3 * (k // 2) + 2 * (k % 2)
+    units = 3 * R - 2 * (R // 2) + chain
     assert st.schedule_bytes == R * units * cb
     assert st.min_bytes == 2 * R * N
 
