@@ -1517,14 +1517,22 @@ ccl_status_t build_plan(const ccl_schedule& s, int64_t ce, int32_t dtype, const 
 {
     // with direct transport, the plain receive of a copy-send or a
     // recv-reduce-copy-send is folded into its sender first (one pass
-    // writes both destinations); where that makes the timeline cyclic or
-    // the threadblocks deadlock, the sender keeps its FIFO
+    // writes both destinations); where the folds make the timeline cyclic
+    // or the threadblocks deadlock, they are given up a kind at a time:
+    // three-hop copy chains first (keeping two hops), then reduction
+    // chains, then both, then all copy chains, then the receive folds
     const int fold = o.link_mode == CCL_LINK_DIRECT ? o.fold : 0;
     auto plan_one = [&](const ccl_schedule& x) {
         ccl_status_t r = build_plan_one(x, ce, dtype, o, img, fold);
         if (fold && (r == CCL_ERR_CYCLE || r == CCL_ERR_DEADLOCK)) {
             const std::string why = ccl_last_error_detail();
-            if (build_plan_one(x, ce, dtype, o, img, 0) == CCL_OK) return CCL_OK;
+            const int two = (fold & ~8) | (fold & 8 ? 2 : 0);   // three hops -> two
+            int tried[7] = {fold}, ntried = 1;
+            for (int f : {two, fold & ~4, two & ~4, fold & 5, fold & 1, 0}) {
+                if (std::find(tried, tried + ntried, f) != tried + ntried) continue;
+                tried[ntried++] = f;
+                if (build_plan_one(x, ce, dtype, o, img, f) == CCL_OK) return CCL_OK;
+            }
             fail(r, why);
         }
         return r;

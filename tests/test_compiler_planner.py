@@ -322,6 +322,56 @@ def test_random_programs_fused_equal_oracle(seed, fuse):
         assert np.array_equal(got[r], want[r])
 
 
+def chain_program(seed, R=4, C=4, nops=30):
+    """A seeded random program rich in chains: most ops read a range that
+    one of the last few ops wrote (a copy or reduction passed on) and write
+    another rank, the rest read an input.  Reads of scratch (and the
+    destination of a reduction into scratch) only touch chunks an earlier op
+    wrote, so the result does not depend on scratch's initial bytes;
+    outputs start as the same sentinel on both sides."""
+    rng = np.random.default_rng(seed)
+    ops, written, recent = [], set(), []
+    while len(ops) < nops:
+        op = int(rng.random() < 0.4)
+        if recent and rng.random() < 0.7:
+            sr, sb, so, cnt = recent[-1 - int(rng.integers(0, min(4, len(recent))))]
+        else:
+            cnt = int(rng.integers(1, 3))
+            sr, sb, so = int(rng.integers(0, R)), 0, int(rng.integers(0, C - cnt + 1))
+        dr = (sr + int(rng.integers(1, R))) % R if rng.random() < 0.9 else sr
+        db = int(rng.choice([1, 2]))
+        do = int(rng.integers(0, C - cnt + 1))
+        if sb == 2 and any((sr, 2, c) not in written for c in range(so, so + cnt)):
+            continue
+        if op == 1 and db == 2 and any((dr, 2, c) not in written for c in range(do, do + cnt)):
+            continue
+        if sr == dr and sb == db and so < do + cnt and do < so + cnt:
+            continue
+        ops.append((op, sr, sb, so, dr, db, do, cnt))
+        written |= {(dr, db, c) for c in range(do, do + cnt)}
+        recent.append((dr, db, do, cnt))
+    return ops, (C, C, C)
+
+
+@pytest.mark.parametrize("seed", range(40))
+@pytest.mark.parametrize("fuse", [ccl.FUSE_FULL, ccl.FUSE_NOCHAIN, ccl.FUSE_NONE])
+def test_chain_programs_plan_with_every_fold(seed, fuse):
+    """Random chain-rich programs plan on direct transport under every fold
+    mask, and each fold bit only ever saves schedule bytes: where a fold
+    would make the timeline cyclic or the threadblocks deadlock, the planner
+    gives up that kind of fold alone (three hops -> two, then reduction
+    chains, ...) and keeps the rest.  Compared within one fusion form (a
+    fold can let a fused form plan that otherwise falls back to a less
+    fused one)."""
+    ops, nch = chain_program(seed)
+    s = ccl.Schedule.compile(ops, 4, nch, fuse=fuse)
+    st = [s.check(3001, F32, link_mode=ccl.LINK_DIRECT, slot_bytes=4096, fold=f) for f in range(16)]
+    for f in range(16):
+        for g in (0, f & ~2, f & ~4, f & ~8):
+            if st[f].fuse == st[g].fuse:
+                assert st[f].schedule_bytes <= st[g].schedule_bytes, (f, g)
+
+
 @pytest.mark.parametrize("bad", [
     [(0, 0, 0, 0, 0, 0, 0, 1)],            # overlapping source and destination
     [(0, 0, 0, 3, 1, 1, 0, 2)],            # source range outside the buffer
