@@ -596,6 +596,54 @@ def test_reduction_chains_folded_bitexact(ccl, opts, kind, R, G, fuse, dtype):
         assert_bitexact(to_host(d, dtype), want)
 
 
+@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("fuse", [True, "nochain", False])
+@pytest.mark.parametrize("fold", [7, 15])
+@pytest.mark.parametrize("opts", [dict(), dict(engine=1), dict(channels=2, microbatches=2), dict(protocol=1)])
+def test_random_chain_programs_folded_bitexact(ccl, seed, fuse, fold, opts):
+    """Random chain-rich chunk programs over 4 ranks (copies and reductions
+    handed on from rank to rank, into outputs and scratch), planned on
+    direct transport with the copy-chain and reduction-chain folds on, run
+    on the GPU: bit-exact against the oracle's program-order run in f32 and
+    bf16 (bf16 shows any change of a chain's summation order)."""
+    import torch
+    import datagen
+    import oracle
+    from gpu_helpers import to_device, empty_outputs, to_host
+    from test_compiler_planner import chain_program
+    ops, nch = chain_program(seed)
+    R = 4
+    ce = 4096 if opts.get("protocol") == 1 else 3001
+    mode = {True: ccl.FUSE_FULL, "nochain": ccl.FUSE_NOCHAIN, False: ccl.FUSE_NONE}[fuse]
+    sched = ccl.Schedule.compile(ops, R, nch, fuse=mode)
+    for dtype in (F32, BF16):
+        plan = ccl.Plan(sched, ce, dtype, link_mode=1, slot_bytes=4096, fold=fold, **opts)
+        ins = datagen.rank_inputs(90 + seed, DIST[dtype], R, nch[0] * ce, dtype)
+        d_out = empty_outputs(R, nch[1] * ce, dtype)
+        plan.execute(to_device(ins, dtype), d_out)
+        torch.cuda.synchronize()
+        plan.status()
+        want, _, _ = oracle.run(np.array(ops, np.int32), R, nch, ce, dtype, ins)
+        assert_bitexact(to_host(d_out, dtype), want)
+
+
+def test_random_chain_programs_take_every_fold(ccl):
+    """The random programs above do exercise the folds: across the seeds
+    the plans hold two- and three-destination copies and three-operand
+    reductions."""
+    from test_compiler_planner import chain_program
+    seen = set()
+    for seed in range(8):
+        ops, nch = chain_program(seed)
+        for mode in (ccl.FUSE_FULL, ccl.FUSE_NOCHAIN, ccl.FUSE_NONE):
+            for fold in (7, 15):
+                plan = ccl.Plan(ccl.Schedule.compile(ops, 4, nch, fuse=mode), 3001, F32, link_mode=1,
+                                slot_bytes=4096, fold=fold)
+                seen |= {ccl.KIND_NAMES[st["kind"]] for st in plan.steps()}
+    assert {"copy2", "copy3"} <= seen
+    assert seen & {"rrs3", "rrc3", "rrcs3", "rsend", "rcsend", "rrc3d", "reduce2"}
+
+
 SPECIALS = {0: [np.inf, -np.inf, np.nan, 3.0e38], 1: [0x7F80, 0xFF80, 0x7FC0, 0x7F7F], 2: [0x7C00, 0xFC00, 0x7E00, 0x7BFF]}
 
 
