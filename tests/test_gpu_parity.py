@@ -596,23 +596,31 @@ def test_reduction_chains_folded_bitexact(ccl, opts, kind, R, G, fuse, dtype):
         assert_bitexact(to_host(d, dtype), want)
 
 
+CHAIN_PROGRAM_OPTS = [dict(), dict(engine=1), dict(engine=1, cluster=4), dict(channels=2, microbatches=2),
+                      dict(protocol=1), dict(bulk=1, tile_bytes=4096), dict(tb_alloc=2, channels=2),
+                      dict(microbatches=4, mb_window=2, tb_alloc=1)]
+
+
 @pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("shape", [(4, 4, 30), (6, 6, 40)])
 @pytest.mark.parametrize("fuse", [True, "nochain", False])
 @pytest.mark.parametrize("fold", [7, 15])
-@pytest.mark.parametrize("opts", [dict(), dict(engine=1), dict(channels=2, microbatches=2), dict(protocol=1)])
-def test_random_chain_programs_folded_bitexact(ccl, seed, fuse, fold, opts):
-    """Random chain-rich chunk programs over 4 ranks (copies and reductions
-    handed on from rank to rank, into outputs and scratch), planned on
-    direct transport with the copy-chain and reduction-chain folds on, run
-    on the GPU: bit-exact against the oracle's program-order run in f32 and
-    bf16 (bf16 shows any change of a chain's summation order)."""
+@pytest.mark.parametrize("opts", CHAIN_PROGRAM_OPTS)
+def test_random_chain_programs_folded_bitexact(ccl, seed, shape, fuse, fold, opts):
+    """Random chain-rich chunk programs over 4 and 6 ranks (copies and
+    reductions handed on from rank to rank, into outputs and scratch),
+    planned on direct transport with the copy-chain and reduction-chain
+    folds on, run on the GPU on both engines, clusters, channels and
+    micro-batches, LL, the bulk path, packing and windows: bit-exact against
+    the oracle's program-order run in f32 and bf16 (bf16 shows any change of
+    a chain's summation order)."""
     import torch
     import datagen
     import oracle
     from gpu_helpers import to_device, empty_outputs, to_host
     from test_compiler_planner import chain_program
-    ops, nch = chain_program(seed)
-    R = 4
+    R, C, nops = shape
+    ops, nch = chain_program(seed, R=R, C=C, nops=nops)
     ce = 4096 if opts.get("protocol") == 1 else 3001
     mode = {True: ccl.FUSE_FULL, "nochain": ccl.FUSE_NOCHAIN, False: ccl.FUSE_NONE}[fuse]
     sched = ccl.Schedule.compile(ops, R, nch, fuse=mode)
