@@ -635,6 +635,35 @@ def test_random_chain_programs_folded_bitexact(ccl, seed, shape, fuse, fold, opt
         assert_bitexact(to_host(d_out, dtype), want)
 
 
+@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("shape", [(4, 4, 30), (6, 6, 40)])
+@pytest.mark.parametrize("fuse", [True, "nochain", False])
+@pytest.mark.parametrize("opts", [dict(), dict(fifo_slots=2), dict(engine=1), dict(protocol=1),
+                                  dict(channels=2, microbatches=2), dict(tb_alloc=1)])
+def test_random_chain_programs_through_fifos_bitexact(ccl, seed, shape, fuse, opts):
+    """The same random programs over FIFO links (a fused send holds its
+    slot while the receiver works; two slots a link at the least): where
+    the fused form's timeline or slot count cannot be met the plan is made
+    from a less fused compilation, and the result stays bit-exact."""
+    import torch
+    import datagen
+    import oracle
+    from gpu_helpers import to_device, empty_outputs, to_host
+    from test_compiler_planner import chain_program
+    R, C, nops = shape
+    ops, nch = chain_program(seed, R=R, C=C, nops=nops)
+    ce = 4096 if opts.get("protocol") == 1 else 3001
+    mode = {True: ccl.FUSE_FULL, "nochain": ccl.FUSE_NOCHAIN, False: ccl.FUSE_NONE}[fuse]
+    plan = ccl.Plan(ccl.Schedule.compile(ops, R, nch, fuse=mode), ce, BF16, link_mode=0, slot_bytes=4096, **opts)
+    ins = datagen.rank_inputs(95 + seed, "normal", R, nch[0] * ce, BF16)
+    d_out = empty_outputs(R, nch[1] * ce, BF16)
+    plan.execute(to_device(ins, BF16), d_out)
+    torch.cuda.synchronize()
+    plan.status()
+    want, _, _ = oracle.run(np.array(ops, np.int32), R, nch, ce, BF16, ins)
+    assert_bitexact(to_host(d_out, BF16), want)
+
+
 def test_random_chain_programs_take_every_fold(ccl):
     """The random programs above do exercise the folds: across the seeds
     the plans hold two- and three-destination copies and three-operand
